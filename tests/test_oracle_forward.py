@@ -1,0 +1,125 @@
+"""Pins of the oracle's forward (CPU only).
+
+With operands whose quantisation is lossless, the quantised forward reduces to
+a plain float64 MLP computed with numpy, exactly.  One-hot fc1 weights make
+every index mistake visible: a wrong expert, a transposed weight, swapped
+SwiGLU halves or a misplaced routing prob all change the result.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mxfp8_nvfp4_block_gb300.inputs import bits, make_inputs
+
+
+def bf16_of(v64):
+    """Reference bf16 rounding of exactly-float-representable values (torch)."""
+    return torch.from_numpy(np.asarray(v64, np.float64).astype(np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def as_bits(a):
+    return bf16_of(np.asarray(a, np.float64))
+
+
+def onehot_w1(rng, G, n1, K):
+    W = np.zeros((G, n1, K))
+    perms = []
+    for g in range(G):
+        p = rng.integers(0, K, n1)
+        W[g, np.arange(n1), p] = 1.0
+        perms.append(p)
+    return W, perms
+
+
+@pytest.mark.parametrize("fmt_name", ["mxfp8", "nvfp4"])
+def test_srelu_forward_lossless_equals_plain_mlp(orc, fmt_name):
+    fmt = orc.MXFP8 if fmt_name == "mxfp8" else orc.NVFP4
+    rng = np.random.default_rng(11)
+    G, K, N = 4, 64, 64
+    splits = np.array([9, 0, 33, 5])
+    M = splits.sum()
+    offs = np.concatenate([[0], np.cumsum(splits)])
+    if fmt == orc.MXFP8:
+        x = rng.choice([0.0, 1, 2, 4, -1, -2, -4], size=(M, K))
+        probs = rng.choice([0.5, 1.0], size=M).astype(np.float32)
+    else:
+        x = rng.choice([0.0, 2, 4, -2, -4], size=(M, K))
+        probs = np.ones(M, np.float32)
+        for g in range(G):
+            if splits[g]:
+                x[offs[g]] = 4.0     # group amax of x = 4, and an fc1 output row of 4s
+    W1, perms = onehot_w1(rng, G, N, K)
+    W2 = rng.choice([0.0, 1, 2, -1, -2, 4, -4], size=(G, K, N))
+    W2[:, 0, 0] = 4.0
+    out = orc.forward(as_bits(x), splits, as_bits(W1), as_bits(W2), probs, orc.SRELU, fmt)
+    for g in range(G):
+        sl = slice(offs[g], offs[g + 1])
+        h = x[sl][:, perms[g]]
+        f = np.maximum(h, 0) ** 2 * probs[sl, None].astype(np.float64)
+        assert np.array_equal(out["fc2x"][sl], bf16_of(f))
+        y = f @ W2[g].T
+        assert np.array_equal(out["y"][sl], bf16_of(y)), g
+
+
+def test_swiglu_forward_gate_up_order_and_prob(orc):
+    rng = np.random.default_rng(12)
+    G, K, N = 3, 64, 64
+    splits = np.array([20, 7, 0])
+    M = splits.sum()
+    offs = np.concatenate([[0], np.cumsum(splits)])
+    x = rng.choice([0.0, 1, 2, 4, -1, -2, -4], size=(M, K))
+    probs = rng.uniform(0, 1, M).astype(np.float32)
+    W1, perms = onehot_w1(rng, G, 2 * N, K)
+    W2 = rng.standard_normal((G, K, N)) / 8
+    W2b = orc.bf16_to_f64(as_bits(W2))
+    out = orc.forward(as_bits(x), splits, as_bits(W1), as_bits(W2), probs, orc.SWIGLU, orc.MXFP8)
+    for g in range(2):
+        sl = slice(offs[g], offs[g + 1])
+        h = x[sl][:, perms[g]]                      # exact fc1 output
+        gate, up = h[:, :N], h[:, N:]
+        a = gate / (1 + np.exp(-gate)) * up * probs[sl, None].astype(np.float64)
+        f = orc.bf16_to_f64(bf16_of(a))
+        assert np.array_equal(out["fc2x"][sl], bf16_of(a))
+        y_dense = f @ W2b[g].T                       # fc2 without the fc2_x quantisation
+        y = orc.bf16_to_f64(out["y"][sl])
+        rel = np.linalg.norm(y - y_dense) / np.linalg.norm(y_dense)
+        assert rel < 0.05, rel
+        a_sw = up / (1 + np.exp(-up)) * gate * probs[sl, None]   # halves swapped
+        assert np.linalg.norm(orc.bf16_to_f64(bf16_of(a_sw)) - f) / np.linalg.norm(f) > 0.3
+
+
+def test_nvfp4_forward_close_to_dense_mlp(orc):
+    """Random operands: the NVFP4 forward stays within quantisation noise of the
+    unquantised float64 MLP; the per-group scales (alpha) are applied."""
+    rng = np.random.default_rng(13)
+    G, K, N = 3, 128, 128
+    splits = np.array([70, 0, 58])
+    M = splits.sum()
+    offs = np.concatenate([[0], np.cumsum(splits)])
+    x = rng.standard_normal((M, K)) * 3
+    W1 = rng.standard_normal((G, N, K)) / np.sqrt(K) * np.array([1, 10, 0.1])[:, None, None]
+    W2 = rng.standard_normal((G, K, N)) / np.sqrt(K)
+    probs = rng.uniform(0, 1, M).astype(np.float32)
+    xb, W1b, W2b = as_bits(x), as_bits(W1), as_bits(W2)
+    out = orc.forward(xb, splits, W1b, W2b, probs, orc.SRELU, orc.NVFP4)
+    xf, W1f, W2f = (orc.bf16_to_f64(t) for t in (xb, W1b, W2b))
+    for g in (0, 2):
+        sl = slice(offs[g], offs[g + 1])
+        h = xf[sl] @ W1f[g].T
+        y = (np.maximum(h, 0) ** 2 * probs[sl, None]) @ W2f[g].T
+        got = orc.bf16_to_f64(out["y"][sl])
+        rel = np.linalg.norm(got - y) / np.linalg.norm(y)
+        assert rel < 0.3, (g, rel)
+    assert out["fc2x_S"][1] == 1.0 and out["x_amax"][1] == 0.0
+
+
+def test_forward_row_subset_matches_full(orc):
+    d = make_inputs("tiny")
+    args = (bits(d["x"]), d["splits"].numpy(), bits(d["W1"]), bits(d["W2"]), d["probs"].numpy(),
+            orc.SWIGLU, orc.MXFP8)
+    full = orc.forward(*args)
+    rows = np.array([0, 5, 199, 200, 349, 350, 511])
+    part = orc.forward(*args, rows=rows)
+    assert np.array_equal(part["y"][rows], full["y"][rows])
+    assert np.array_equal(part["fc2x_codes"][rows], full["fc2x_codes"][rows])
