@@ -1,0 +1,251 @@
+/*
+ * gmlp.h -- C ABI of the fused grouped-MLP forward for mixture-of-experts
+ * layers with MXFP8 / NVFP4 block quantisation, for GB300 (sm_103a).
+ *
+ * Library: libgmlp.so (hand-written CUDA; TMA, tcgen05 block-scaled MMA, TMEM).
+ *
+ * What it computes (TransformerEngine pull-request pages):
+ *   - PR #2769 "GEMM + Swiglu fused Grouped MLP for MXFP8", Greptile summary and
+ *     sequence diagram: MXFP8 x (a_tensor) -> FC1 GLU kernel with the stacked
+ *     expert weights (b_tensor) and per-token probs (prob_tensor) -> MXFP8
+ *     activation (d_tensor, sfd_row_tensor) -> FC2 kernel -> output.
+ *   - PR #3837 "Reduce NVFP4 quantization work for the fused GroupedMLP fc2
+ *     input with activation recompute", Description, Changes and flowchart:
+ *     FC1 + activation -> fc2 input and its (pre-RHT, post-RHT) amax ->
+ *     row-wise NVFP4 quantization -> FC2; the group Hadamard-amax pass and the
+ *     quantize-with-amax cast as separate calls.
+ *   - PR #3631 "Add NVTE_CUTEDSL_FUSED_GROUPED_MLP_WARN_FALLBACK", Changes:
+ *     the fusion preconditions; here each unmet one is a status code, and there
+ *     is no fallback path.
+ *
+ * Conventions (all calls):
+ *   - Every pointer argument named as device memory is a device pointer owned
+ *     by the caller; the library never allocates, frees or keeps it.  Device
+ *     pointers must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` and never synchronise the host,
+ *     except gmlp_check_device_status.  Host structs are read during the call
+ *     only.
+ *   - bf16 tensors are passed as uint16_t bit patterns, row-major.
+ *   - x is token-sorted: the rows of group g are rows off_g .. off_g + m_g - 1
+ *     with off_g = m_0 + ... + m_{g-1}; split_sizes (int64, device, [G]) stay on
+ *     the device, so M (their sum) is passed from the host.  The sum must equal
+ *     M; a negative size or a sum above M is detected on the device and
+ *     reported by gmlp_check_device_status as GMLP_ERR_DEVICE_BOUNDS (no
+ *     output written past M).
+ *   - Host-side argument checks return a status before anything is launched.
+ *     No C++ exception crosses the ABI.  gmlp_last_error() describes the last
+ *     non-OK status of the calling thread.
+ *
+ * Formats (fixed by the method statement; the pages give no arithmetic):
+ *   MXFP8: E4M3 codes (max 448, no infinity), one E8M0 scale per 1x32 block
+ *     along a row: e = floor(log2 amax) - 8 (clamped to [-127,127], amax 0 ->
+ *     -127), byte e + 127, codes E4M3(x * 2^-e), round-to-nearest-even,
+ *     saturating.
+ *   NVFP4: E2M1 codes packed two per byte (even element in the low nibble),
+ *     one E4M3 scale per 1x16 block, and an FP32 global scale per group
+ *     S = 448*6 / amax (amax 0 -> 1).  Block: t = (b/6)*S in FP32, sf = E4M3(t),
+ *     enc = S/sf (0 when sf is 0), codes E2M1(x * enc).  Dequantised value:
+ *     code * sf / S.
+ *   RHT: y = 1/4 * H16 * diag(s) * v over 16 consecutive ROWS of one column
+ *     of one group (chunks start at the group's first row; a short last chunk
+ *     is zero-padded), s_i = -1 when bit i of rht_sign_mask is set; FP32.
+ *
+ * Scale layouts of rowwise outputs ([rows, cols/block] logical):
+ *   GMLP_SCALES_COMPACT:    row-major [M][cols/block].
+ *   GMLP_SCALES_GEMM_TILED: what the tensor-core MMA reads.  Each group's rows
+ *     are cut into 128-row tiles counted from the group's first row (the last
+ *     tile padded); group g's tiles are numbered from T_g = sum_{h<g}
+ *     ceil(m_h/128).  A tile's scale columns are cut into runs of 4; every
+ *     (tile, run) pair is a 512-byte block at byte ((T_g + t) * (cols/block/4)
+ *     + run) * 512, and the scale of tile row r, run column j sits at
+ *     (r % 32) * 16 + (r / 32) * 4 + j inside it.  Padding rows' bytes are
+ *     unspecified.  Buffer size: gmlp_tiled_scales_bytes().  cols/block must be
+ *     a multiple of 4.
+ * Columnwise NVFP4 output (per group, groups concatenated in order): codes
+ *   [cols][Mpad_g/2] and scales [cols][Mpad_g/16], Mpad_g = 16*ceil(m_g/16).
+ */
+#ifndef GMLP_H_
+#define GMLP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GMLP_API __attribute__((visibility("default")))
+#else
+#define GMLP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+struct CUevent_st;
+typedef struct CUstream_st* gmlp_stream; /* a cudaStream_t; NULL = legacy default stream */
+typedef struct CUevent_st* gmlp_event;   /* a cudaEvent_t */
+
+typedef enum gmlp_status {
+  GMLP_OK = 0,
+  GMLP_ERR_INVALID_ARG = 1,        /* NULL or misaligned pointer, bad enum value */
+  GMLP_ERR_INVALID_DIMS = 2,       /* a size outside the supported range (see each call) */
+  GMLP_ERR_UNSUPPORTED_RECIPE = 3, /* format / option combination this path does not have */
+  GMLP_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
+  GMLP_ERR_WORKSPACE = 5,          /* workspace NULL or smaller than the size query returns */
+  GMLP_ERR_CUDA = 6,               /* a CUDA runtime / driver call failed (see gmlp_last_error) */
+  GMLP_ERR_DEVICE_TIMEOUT = 7,     /* a kernel gave up a bounded wait (device status word) */
+  GMLP_ERR_DEVICE_BOUNDS = 8       /* split_sizes negative or summing past M (device status word) */
+} gmlp_status;
+
+typedef enum gmlp_format { GMLP_MXFP8 = 0, GMLP_NVFP4 = 1 } gmlp_format;
+typedef enum gmlp_act { GMLP_ACT_SWIGLU = 0, GMLP_ACT_SRELU = 1 } gmlp_act;
+typedef enum gmlp_scale_layout { GMLP_SCALES_COMPACT = 0, GMLP_SCALES_GEMM_TILED = 1 } gmlp_scale_layout;
+
+/* Quantisation recipe (PR #3631 Changes, the recipe preconditions; PR #3837,
+ * rht_sign_mask).  MXFP8 always uses E4M3 (E5M2 gradients are not a forward
+ * concern); NVFP4 may run with or without the RHT on its columnwise output. */
+typedef struct gmlp_recipe {
+  int32_t format;         /* gmlp_format */
+  int32_t use_rht;        /* NVFP4 columnwise output: apply the 16-point RHT (0/1) */
+  uint32_t rht_sign_mask; /* low 16 bits: bit i set negates element i of each chunk */
+  int32_t scale_layout;   /* gmlp_scale_layout of rowwise scales */
+} gmlp_recipe;
+
+/* A quantised tensor: two caller-owned device buffers. */
+typedef struct gmlp_qtensor {
+  uint8_t* codes;
+  uint8_t* scales;
+} gmlp_qtensor;
+
+/* Bytes of a GEMM_TILED scale buffer for M rows in G groups with `nscale`
+ * scale columns per row (cols/32 for MXFP8, cols/16 for NVFP4). */
+GMLP_API size_t gmlp_tiled_scales_bytes(int64_t M, int32_t G, int64_t nscale);
+
+/* gmlp_group_hadamard_amax -- nvfp4_group_hadamard_amax (PR #3837, Changes:
+ * the binding exposes the group Hadamard-amax pass on its own; the sign-mask
+ * fix makes the mask part of the post-RHT amax).  One read-only pass over a
+ * token-sorted bf16 x [M, K]:
+ *   amax_pre[g]  = max |x| over group g's rows,
+ *   amax_post[g] = max |RHT(chunk)| over all columns and 16-row chunks of group g.
+ * amax_pre, amax_post: device float [G], overwritten (0 for an empty group).
+ * Limits: 1 <= G <= 512, K % 128 == 0, M >= 0 (M == 0 writes zeros). */
+GMLP_API gmlp_status gmlp_group_hadamard_amax(const uint16_t* x, int64_t M, int64_t K,
+                                     const int64_t* split_sizes, int32_t G,
+                                     uint32_t rht_sign_mask, float* amax_pre, float* amax_post,
+                                     gmlp_stream stream);
+
+/* gmlp_group_quantize_with_amax -- nvfp4_group_quantize_with_amax (PR #3837,
+ * Changes: the backward re-quantisation reuses the forward amaxes, so this call
+ * is the cast alone, with the amaxes the caller supplies).
+ *   row_out (nullable): rowwise codes [M][K] (MXFP8) / [M][K/2] (NVFP4) and
+ *     scales in recipe->scale_layout.  NVFP4 rowwise uses S_g from amax_pre[g].
+ *   col_out (nullable, NVFP4 only): columnwise codes/scales (layout above) of
+ *     the RHT-transformed chunks with S_g from amax_post[g] when
+ *     recipe->use_rht, else of the plain chunks with S_g from amax_pre[g].
+ *   amax_pre / amax_post: device float [G] (NVFP4; ignored for MXFP8).
+ * Limits: 1 <= G <= 512, K % 128 == 0.  MXFP8 with col_out is
+ * GMLP_ERR_UNSUPPORTED_RECIPE.  At least one of row_out / col_out. */
+GMLP_API gmlp_status gmlp_group_quantize_with_amax(const uint16_t* x, int64_t M, int64_t K,
+                                          const int64_t* split_sizes, int32_t G,
+                                          const gmlp_recipe* recipe, const float* amax_pre,
+                                          const float* amax_post, const gmlp_qtensor* row_out,
+                                          const gmlp_qtensor* col_out, gmlp_stream stream);
+
+/* gmlp_group_quantize -- the generic group quantize (PR #3837, Description:
+ * the fc2-input group quantize, row- and/or column-wise, with the split sizes
+ * kept on the device; PR #3631 recipe checks).
+ * MXFP8: one pass, amax_pre/amax_post unused (may be NULL).
+ * NVFP4: first the per-group amax (the Hadamard-amax pass when col_out and
+ * use_rht, else max |x| only), written to amax_pre [G] (and amax_post [G]
+ * when that pass runs; amax_post may be NULL otherwise), then the cast as in
+ * gmlp_group_quantize_with_amax. */
+GMLP_API gmlp_status gmlp_group_quantize(const uint16_t* x, int64_t M, int64_t K,
+                                const int64_t* split_sizes, int32_t G, const gmlp_recipe* recipe,
+                                const gmlp_qtensor* row_out, const gmlp_qtensor* col_out,
+                                float* amax_pre, float* amax_post, gmlp_stream stream);
+
+/* Quantised stacked expert weights (PR #2769: single grouped weight, the
+ * b_tensor of the FC1 / FC2 kernels).  Produced by gmlp_prepare_weights. */
+typedef struct gmlp_qweight {
+  const uint8_t* codes;       /* [G][rows][cols] (MXFP8) / [G][rows][cols/2] (NVFP4) */
+  const uint8_t* scales;      /* GEMM_TILED, the G experts as G groups of `rows` rows */
+  const float* global_scale;  /* NVFP4: [G] per-expert S; NULL for MXFP8 */
+  int64_t rows;               /* output features of the GEMM (fc1: 2N or N; fc2: K) */
+  int64_t cols;               /* contraction features (fc1: K; fc2: N) */
+  int32_t G;
+  int32_t format;             /* gmlp_format */
+  int32_t swiglu_interleaved; /* 1: rows hold the SwiGLU gate/up interleave below */
+  int32_t reserved;
+} gmlp_qweight;
+
+/* gmlp_prepare_weights -- per-expert quantisation of stacked bf16 weights W
+ * [G][rows][cols] along cols (done once per weight version, off the forward's
+ * timed path).  NVFP4 uses one global scale per expert from that expert's
+ * amax, written to amax [G] and global_scale [G] (device; NULL for MXFP8).
+ * swiglu_interleave = 1 (fc1 of SwiGLU, rows = 2N with gate rows [0,N) and up
+ * rows [N,2N)) stores the rows in the order the fused epilogue wants: output
+ * row p of an expert holds logical row 32c + i (gate) for p = 64c + i and
+ * N + 32c + i (up) for p = 64c + 32 + i, i < 32.
+ * codes: [G][rows][cols or cols/2]; scales: gmlp_tiled_scales_bytes(G*rows, G,
+ * cols/block) bytes.  Limits: rows % 128 == 0, cols % 128 == 0 (NVFP4: % 256),
+ * swiglu_interleave needs rows % 64 == 0. */
+GMLP_API gmlp_status gmlp_prepare_weights(const uint16_t* W, int32_t G, int64_t rows, int64_t cols,
+                                 int32_t swiglu_interleave, int32_t format, uint8_t* codes,
+                                 uint8_t* scales, float* global_scale, float* amax,
+                                 gmlp_stream stream);
+
+/* Optional extras of gmlp_forward (every field nullable / zero). */
+typedef struct gmlp_fwd_aux {
+  uint8_t* fc2x_codes;     /* out: fc2 input codes [M][N] (MXFP8) / [M][N/2] (NVFP4) */
+  uint8_t* fc2x_scales;    /* out: fc2 input scales, GEMM_TILED */
+  uint16_t* fc2x_bf16;     /* out, NVFP4: bf16 fc2_x [M][N] */
+  float* fc2x_amax_pre;    /* out, NVFP4: [G] per-group max |fc2_x| */
+  float* fc2x_amax_post;   /* out, NVFP4: [G] per-group post-RHT amax of fc2_x */
+  gmlp_event* stage_events; /* recorded on `stream` after each kernel of the call */
+  int32_t n_stage_events;   /* MXFP8: 3 (x quant, fc1, fc2); NVFP4: 5 (x amax, x quant, fc1, fc2_x quant, fc2) */
+  int32_t reserved;
+} gmlp_fwd_aux;
+
+/* Workspace bytes gmlp_forward needs for these sizes (x and fc2_x codes and
+ * scales, per-group amaxes and scales). */
+GMLP_API size_t gmlp_forward_workspace_size(int64_t M, int64_t K, int64_t N, int32_t G, int32_t act,
+                                   const gmlp_recipe* recipe);
+
+/* gmlp_forward -- the fused grouped-MLP forward (PR #2769 sequence diagram,
+ * forward pass; PR #3837 flowchart):
+ *   1. x [M,K] bf16 -> rowwise MXFP8 / NVFP4 (per-group amax) codes + scales;
+ *   2. fc1 per group g: H = dq(xq_g) dq(W1q_g)^T (FP32 accumulate; NVFP4 times
+ *      1/(S_x,g S_w1,g));
+ *   3. h = bf16(H); act = SwiGLU (silu(gate)*up) or SReLU (max(h,0)^2);
+ *      fc2_x = bf16(act * probs[t]) (probs NULL = 1);
+ *   4. MXFP8: fc2_x is quantised inside the fc1 epilogue and never stored in
+ *      bf16.  NVFP4: the epilogue stores bf16 fc2_x and the per-group
+ *      (pre-RHT, post-RHT) amax, then fc2_x is cast with that amax;
+ *   5. fc2 per group: y_g = bf16(dq(fc2xq_g) dq(W2q_g)^T) [M,K] row-major.
+ * W1: rows 2N (SwiGLU, interleaved) or N (SReLU), cols K; W2: rows K, cols N;
+ * both with recipe->format.  y: device bf16 [M][K], rows of empty groups and
+ * rows past sum(split_sizes) untouched.
+ * Limits: 1 <= G <= 512, K % 256 == 0, N % 128 == 0 (SReLU or NVFP4: N % 256
+ * == 0), recipe->scale_layout is ignored (the GEMMs read GEMM_TILED).
+ * workspace: >= gmlp_forward_workspace_size() bytes of device memory. */
+GMLP_API gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N,
+                         const int64_t* split_sizes, int32_t G, const gmlp_qweight* W1,
+                         const gmlp_qweight* W2, const float* probs, int32_t act,
+                         const gmlp_recipe* recipe, uint16_t* y, const gmlp_fwd_aux* aux,
+                         void* workspace, size_t workspace_bytes, gmlp_stream stream);
+
+/* Synchronises `stream`, then reads and clears the device status word the
+ * kernels set on a bounded-wait timeout or inconsistent split sizes. */
+GMLP_API gmlp_status gmlp_check_device_status(gmlp_stream stream);
+
+/* Text of the calling thread's last non-OK status ("" if none). */
+GMLP_API const char* gmlp_last_error(void);
+
+/* Library version string. */
+GMLP_API const char* gmlp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GMLP_H_ */

@@ -1,0 +1,516 @@
+// api.cu -- the extern "C" entry points of libgmlp.so declared in
+// include/gmlp.h: host-side argument checks (a status before any launch,
+// replacing the silent unfused fallback and its warning described in PR #3631
+// "Add NVTE_CUTEDSL_FUSED_GROUPED_MLP_WARN_FALLBACK", Changes), workspace
+// carving and the launch sequence of each call.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "internal.h"
+
+namespace gmlp {
+
+int quant_read_clear_status();
+int gemm_read_clear_status();
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+gmlp_status fail(gmlp_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+gmlp_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(GMLP_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+gmlp_status check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  static int cached[64] = {};  // 0 unknown, 1 ok, 2 bad
+  if (dev < 64 && cached[dev] == 1) return GMLP_OK;
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(GMLP_ERR_UNSUPPORTED_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                major, minor);
+  if (dev < 64) cached[dev] = 1;
+  return GMLP_OK;
+}
+
+gmlp_status check_groups(int32_t G, int64_t M, const int64_t* split_sizes) {
+  if (G < 1 || G > kMaxGroups) return fail(GMLP_ERR_INVALID_DIMS, "G = %d outside [1, %d]", G, kMaxGroups);
+  if (M < 0 || M > (int64_t)0x7FFFFFFF) return fail(GMLP_ERR_INVALID_DIMS, "M = %lld outside [0, 2^31)", (long long)M);
+  if (!split_sizes) return fail(GMLP_ERR_INVALID_ARG, "split_sizes is NULL");
+  if ((reinterpret_cast<uintptr_t>(split_sizes) & 7) != 0)
+    return fail(GMLP_ERR_INVALID_ARG, "split_sizes is not 8-byte aligned");
+  return GMLP_OK;
+}
+
+#define GMLP_TRY(expr)                 \
+  do {                                 \
+    gmlp_status st_ = (expr);          \
+    if (st_ != GMLP_OK) return st_;    \
+  } while (0)
+
+#define GMLP_CUDA(expr, where)                         \
+  do {                                                 \
+    cudaError_t e_ = (expr);                           \
+    if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+  } while (0)
+
+size_t tiled_bytes(int64_t M, int32_t G, int64_t nscale) {
+  return (size_t)((M + 127) / 128 + G) * 128 * (size_t)nscale;
+}
+
+struct FwdLayout {
+  size_t x_codes, x_scales, f_codes, f_scales, f_bf16, amax, total;
+};
+
+FwdLayout fwd_layout(int64_t M, int64_t K, int64_t N, int32_t G, int fmt) {
+  FwdLayout L{};
+  size_t cur = 0;
+  auto take = [&](size_t b) {
+    size_t o = cur;
+    cur += align256(b);
+    return o;
+  };
+  const int blk = fmt == GMLP_MXFP8 ? 32 : 16;
+  const int cdiv = fmt == GMLP_MXFP8 ? 1 : 2;
+  L.x_codes = take((size_t)M * K / cdiv);
+  L.x_scales = take(tiled_bytes(M, G, K / blk));
+  L.f_codes = take((size_t)M * N / cdiv);
+  L.f_scales = take(tiled_bytes(M, G, N / blk));
+  if (fmt == GMLP_NVFP4) {
+    L.f_bf16 = take((size_t)M * N * 2);
+    L.amax = take((size_t)3 * G * sizeof(float));
+  }
+  L.total = cur;
+  return L;
+}
+
+gmlp_status check_recipe(const gmlp_recipe* r) {
+  if (!r) return fail(GMLP_ERR_INVALID_ARG, "recipe is NULL");
+  if (r->format != GMLP_MXFP8 && r->format != GMLP_NVFP4)
+    return fail(GMLP_ERR_UNSUPPORTED_RECIPE, "recipe format %d is neither MXFP8 nor NVFP4", r->format);
+  if (r->scale_layout != GMLP_SCALES_COMPACT && r->scale_layout != GMLP_SCALES_GEMM_TILED)
+    return fail(GMLP_ERR_INVALID_ARG, "scale_layout %d unknown", r->scale_layout);
+  return GMLP_OK;
+}
+
+gmlp_status check_qtensor(const gmlp_qtensor* t, const char* what) {
+  if (!t) return GMLP_OK;
+  if (!t->codes || !t->scales) return fail(GMLP_ERR_INVALID_ARG, "%s codes/scales NULL", what);
+  if (!aligned16(t->codes) || !aligned16(t->scales))
+    return fail(GMLP_ERR_INVALID_ARG, "%s codes/scales not 16-byte aligned", what);
+  return GMLP_OK;
+}
+
+}  // namespace
+
+int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 1;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+}  // namespace gmlp
+
+using namespace gmlp;
+
+extern "C" {
+
+const char* gmlp_last_error(void) { return g_last_error; }
+
+const char* gmlp_version(void) { return "gmlp 0.1 (sm_103a)"; }
+
+size_t gmlp_tiled_scales_bytes(int64_t M, int32_t G, int64_t nscale) {
+  if (M < 0 || G < 0 || nscale < 0) return 0;
+  return tiled_bytes(M, G, nscale);
+}
+
+gmlp_status gmlp_group_hadamard_amax(const uint16_t* x, int64_t M, int64_t K, const int64_t* split_sizes,
+                                     int32_t G, uint32_t rht_sign_mask, float* amax_pre, float* amax_post,
+                                     gmlp_stream stream) {
+  g_last_error[0] = 0;
+  GMLP_TRY(check_groups(G, M, split_sizes));
+  if (K <= 0 || K % 128) return fail(GMLP_ERR_INVALID_DIMS, "K = %lld must be a positive multiple of 128", (long long)K);
+  if ((M > 0 && !x) || !amax_pre || !amax_post) return fail(GMLP_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned16(x) || !aligned16(amax_pre) || !aligned16(amax_post))
+    return fail(GMLP_ERR_INVALID_ARG, "pointer not 16-byte aligned");
+  GMLP_TRY(check_device());
+  GroupSrc gs{split_sizes, 0, G, M};
+  GMLP_CUDA(launch_hadamard_amax(x, M, K, gs, rht_sign_mask, amax_pre, amax_post, (cudaStream_t)stream),
+            "hadamard_amax launch");
+  return GMLP_OK;
+}
+
+static gmlp_status quantize_with_amax_impl(const uint16_t* x, int64_t M, int64_t K, const int64_t* split_sizes,
+                                           int32_t G, const gmlp_recipe* r, const float* amax_pre,
+                                           const float* amax_post, const gmlp_qtensor* row_out,
+                                           const gmlp_qtensor* col_out, cudaStream_t s) {
+  GroupSrc gs{split_sizes, 0, G, M};
+  if (r->format == GMLP_MXFP8) {
+    RowQuantArgs a{};
+    a.x = x;
+    a.M = M;
+    a.K = K;
+    a.grp = gs;
+    a.format = GMLP_MXFP8;
+    a.tiled = r->scale_layout == GMLP_SCALES_GEMM_TILED;
+    a.codes = row_out->codes;
+    a.scales = row_out->scales;
+    GMLP_CUDA(launch_row_quant(a, s), "row_quant launch");
+    return GMLP_OK;
+  }
+  if (col_out) {
+    ColQuantArgs c{};
+    c.x = x;
+    c.M = M;
+    c.K = K;
+    c.grp = gs;
+    c.use_rht = r->use_rht != 0;
+    c.mask = r->rht_sign_mask & 0xFFFFu;
+    c.amax_row = amax_pre;
+    c.amax_col = r->use_rht ? amax_post : amax_pre;
+    c.row_codes = row_out ? row_out->codes : nullptr;
+    c.row_scales = row_out ? row_out->scales : nullptr;
+    c.row_tiled = r->scale_layout == GMLP_SCALES_GEMM_TILED;
+    c.col_codes = col_out->codes;
+    c.col_scales = col_out->scales;
+    GMLP_CUDA(launch_col_quant(c, s), "col_quant launch");
+    return GMLP_OK;
+  }
+  RowQuantArgs a{};
+  a.x = x;
+  a.M = M;
+  a.K = K;
+  a.grp = gs;
+  a.format = GMLP_NVFP4;
+  a.tiled = r->scale_layout == GMLP_SCALES_GEMM_TILED;
+  a.codes = row_out->codes;
+  a.scales = row_out->scales;
+  a.amax = amax_pre;
+  GMLP_CUDA(launch_row_quant(a, s), "row_quant launch");
+  return GMLP_OK;
+}
+
+static gmlp_status check_quant_args(const uint16_t* x, int64_t M, int64_t K, const int64_t* split_sizes, int32_t G,
+                                    const gmlp_recipe* recipe, const gmlp_qtensor* row_out,
+                                    const gmlp_qtensor* col_out) {
+  GMLP_TRY(check_groups(G, M, split_sizes));
+  GMLP_TRY(check_recipe(recipe));
+  if (K <= 0 || K % 128) return fail(GMLP_ERR_INVALID_DIMS, "K = %lld must be a positive multiple of 128", (long long)K);
+  if (M > 0 && !x) return fail(GMLP_ERR_INVALID_ARG, "x is NULL");
+  if (!aligned16(x)) return fail(GMLP_ERR_INVALID_ARG, "x not 16-byte aligned");
+  if (!row_out && !col_out) return fail(GMLP_ERR_INVALID_ARG, "neither row_out nor col_out given");
+  if (recipe->format == GMLP_MXFP8 && col_out)
+    return fail(GMLP_ERR_UNSUPPORTED_RECIPE, "columnwise MXFP8 output is not part of this path");
+  GMLP_TRY(check_qtensor(row_out, "row_out"));
+  GMLP_TRY(check_qtensor(col_out, "col_out"));
+  return GMLP_OK;
+}
+
+gmlp_status gmlp_group_quantize_with_amax(const uint16_t* x, int64_t M, int64_t K, const int64_t* split_sizes,
+                                          int32_t G, const gmlp_recipe* recipe, const float* amax_pre,
+                                          const float* amax_post, const gmlp_qtensor* row_out,
+                                          const gmlp_qtensor* col_out, gmlp_stream stream) {
+  g_last_error[0] = 0;
+  GMLP_TRY(check_quant_args(x, M, K, split_sizes, G, recipe, row_out, col_out));
+  if (recipe->format == GMLP_NVFP4) {
+    if (!amax_pre) return fail(GMLP_ERR_INVALID_ARG, "NVFP4 needs amax_pre");
+    if (col_out && recipe->use_rht && !amax_post) return fail(GMLP_ERR_INVALID_ARG, "RHT columnwise needs amax_post");
+  }
+  GMLP_TRY(check_device());
+  return quantize_with_amax_impl(x, M, K, split_sizes, G, recipe, amax_pre, amax_post, row_out, col_out,
+                                 (cudaStream_t)stream);
+}
+
+gmlp_status gmlp_group_quantize(const uint16_t* x, int64_t M, int64_t K, const int64_t* split_sizes, int32_t G,
+                                const gmlp_recipe* recipe, const gmlp_qtensor* row_out,
+                                const gmlp_qtensor* col_out, float* amax_pre, float* amax_post,
+                                gmlp_stream stream) {
+  g_last_error[0] = 0;
+  GMLP_TRY(check_quant_args(x, M, K, split_sizes, G, recipe, row_out, col_out));
+  const bool hadamard = recipe->format == GMLP_NVFP4 && col_out && recipe->use_rht;
+  if (recipe->format == GMLP_NVFP4) {
+    if (!amax_pre || (hadamard && !amax_post))
+      return fail(GMLP_ERR_INVALID_ARG, "NVFP4 needs amax_pre (and amax_post for the RHT columnwise output)");
+    if (!aligned16(amax_pre) || !aligned16(amax_post)) return fail(GMLP_ERR_INVALID_ARG, "amax not 16-byte aligned");
+  }
+  GMLP_TRY(check_device());
+  cudaStream_t s = (cudaStream_t)stream;
+  GroupSrc gs{split_sizes, 0, G, M};
+  if (hadamard) {
+    GMLP_CUDA(launch_hadamard_amax(x, M, K, gs, recipe->rht_sign_mask, amax_pre, amax_post, s), "hadamard_amax launch");
+  } else if (recipe->format == GMLP_NVFP4) {
+    GMLP_CUDA(launch_group_amax(x, M, K, gs, amax_pre, s), "group_amax launch");
+  }
+  return quantize_with_amax_impl(x, M, K, split_sizes, G, recipe, amax_pre, amax_post, row_out, col_out, s);
+}
+
+gmlp_status gmlp_prepare_weights(const uint16_t* W, int32_t G, int64_t rows, int64_t cols, int32_t swiglu_interleave,
+                                 int32_t format, uint8_t* codes, uint8_t* scales, float* global_scale, float* amax,
+                                 gmlp_stream stream) {
+  g_last_error[0] = 0;
+  if (G < 1 || G > kMaxGroups) return fail(GMLP_ERR_INVALID_DIMS, "G = %d outside [1, %d]", G, kMaxGroups);
+  if (format != GMLP_MXFP8 && format != GMLP_NVFP4) return fail(GMLP_ERR_UNSUPPORTED_RECIPE, "format %d", format);
+  if (rows <= 0 || rows % 128 || (int64_t)G * rows > 0x7FFFFFFF)
+    return fail(GMLP_ERR_INVALID_DIMS, "rows = %lld must be a positive multiple of 128", (long long)rows);
+  const int64_t cmod = format == GMLP_MXFP8 ? 128 : 256;
+  if (cols <= 0 || cols % cmod)
+    return fail(GMLP_ERR_INVALID_DIMS, "cols = %lld must be a positive multiple of %lld", (long long)cols, (long long)cmod);
+  if (swiglu_interleave && rows % 64) return fail(GMLP_ERR_INVALID_DIMS, "SwiGLU interleave needs rows %% 64 == 0");
+  if (!W || !codes || !scales || !aligned16(W) || !aligned16(codes) || !aligned16(scales))
+    return fail(GMLP_ERR_INVALID_ARG, "W/codes/scales NULL or not 16-byte aligned");
+  if (format == GMLP_NVFP4 && (!global_scale || !amax))
+    return fail(GMLP_ERR_INVALID_ARG, "NVFP4 weights need global_scale and amax buffers");
+  GMLP_TRY(check_device());
+  cudaStream_t s = (cudaStream_t)stream;
+  GroupSrc gs{nullptr, (int32_t)rows, G, (int64_t)G * rows};
+  RowQuantArgs a{};
+  a.x = W;
+  a.M = (int64_t)G * rows;
+  a.K = cols;
+  a.grp = gs;
+  a.format = format;
+  a.tiled = 1;
+  a.codes = codes;
+  a.scales = scales;
+  a.swiglu_interleave = swiglu_interleave != 0;
+  if (format == GMLP_NVFP4) {
+    GMLP_CUDA(launch_group_amax(W, a.M, cols, gs, amax, s), "group_amax launch");
+    a.amax = amax;
+    a.S_out = global_scale;
+  }
+  GMLP_CUDA(launch_row_quant(a, s), "row_quant launch");
+  return GMLP_OK;
+}
+
+size_t gmlp_forward_workspace_size(int64_t M, int64_t K, int64_t N, int32_t G, int32_t act,
+                                   const gmlp_recipe* recipe) {
+  (void)act;
+  if (!recipe || M < 0 || K <= 0 || N <= 0 || G < 1) return 0;
+  return fwd_layout(M, K, N, G, recipe->format).total;
+}
+
+gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, const int64_t* split_sizes, int32_t G,
+                         const gmlp_qweight* W1, const gmlp_qweight* W2, const float* probs, int32_t act,
+                         const gmlp_recipe* recipe, uint16_t* y, const gmlp_fwd_aux* aux, void* workspace,
+                         size_t workspace_bytes, gmlp_stream stream) {
+  g_last_error[0] = 0;
+  GMLP_TRY(check_groups(G, M, split_sizes));
+  GMLP_TRY(check_recipe(recipe));
+  if (act != GMLP_ACT_SWIGLU && act != GMLP_ACT_SRELU) return fail(GMLP_ERR_INVALID_ARG, "act = %d unknown", act);
+  const int fmt = recipe->format;
+  const int64_t n1 = act == GMLP_ACT_SWIGLU ? 2 * N : N;
+  if (K <= 0 || K % 256) return fail(GMLP_ERR_INVALID_DIMS, "K = %lld must be a positive multiple of 256", (long long)K);
+  if (N <= 0 || n1 % 256 || N % (fmt == GMLP_NVFP4 ? 256 : 128))
+    return fail(GMLP_ERR_INVALID_DIMS, "N = %lld: need fc1 width %% 256 == 0 and N %% %d == 0", (long long)N,
+                fmt == GMLP_NVFP4 ? 256 : 128);
+  if (!W1 || !W2) return fail(GMLP_ERR_INVALID_ARG, "W1 / W2 NULL");
+  if (W1->G != G || W2->G != G) return fail(GMLP_ERR_INVALID_DIMS, "weights have %d / %d experts, G = %d", W1->G, W2->G, G);
+  if (W1->format != fmt || W2->format != fmt)
+    return fail(GMLP_ERR_UNSUPPORTED_RECIPE, "weight formats differ from the recipe's");
+  if (W1->rows != n1 || W1->cols != K)
+    return fail(GMLP_ERR_INVALID_DIMS, "W1 is [%lld x %lld], expected [%lld x %lld]", (long long)W1->rows,
+                (long long)W1->cols, (long long)n1, (long long)K);
+  if (W2->rows != K || W2->cols != N)
+    return fail(GMLP_ERR_INVALID_DIMS, "W2 is [%lld x %lld], expected [%lld x %lld]", (long long)W2->rows,
+                (long long)W2->cols, (long long)K, (long long)N);
+  if ((W1->swiglu_interleaved != 0) != (act == GMLP_ACT_SWIGLU) || W2->swiglu_interleaved)
+    return fail(GMLP_ERR_INVALID_ARG, "W1 must be SwiGLU-interleaved exactly for SwiGLU; W2 never");
+  if (!W1->codes || !W1->scales || !W2->codes || !W2->scales || !aligned16(W1->codes) || !aligned16(W1->scales) ||
+      !aligned16(W2->codes) || !aligned16(W2->scales))
+    return fail(GMLP_ERR_INVALID_ARG, "weight codes/scales NULL or not 16-byte aligned");
+  if (fmt == GMLP_NVFP4 && (!W1->global_scale || !W2->global_scale))
+    return fail(GMLP_ERR_INVALID_ARG, "NVFP4 weights need global_scale");
+  if ((M > 0 && (!x || !y)) || !aligned16(x) || !aligned16(y))
+    return fail(GMLP_ERR_INVALID_ARG, "x / y NULL or not 16-byte aligned");
+  if (probs && (reinterpret_cast<uintptr_t>(probs) & 3)) return fail(GMLP_ERR_INVALID_ARG, "probs misaligned");
+  const FwdLayout L = fwd_layout(M, K, N, G, fmt);
+  if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
+    return fail(GMLP_ERR_WORKSPACE, "workspace %zu bytes, need %zu (16-byte aligned)", workspace_bytes, L.total);
+  if (aux && aux->n_stage_events > 0 && !aux->stage_events) return fail(GMLP_ERR_INVALID_ARG, "stage_events NULL");
+  GMLP_TRY(check_device());
+
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* x_codes = ws + L.x_codes;
+  uint8_t* x_scales = ws + L.x_scales;
+  uint8_t* f_codes = (aux && aux->fc2x_codes) ? aux->fc2x_codes : ws + L.f_codes;
+  uint8_t* f_scales = (aux && aux->fc2x_scales) ? aux->fc2x_scales : ws + L.f_scales;
+  if (!aligned16(f_codes) || !aligned16(f_scales)) return fail(GMLP_ERR_INVALID_ARG, "aux fc2x buffers misaligned");
+  GroupSrc gs{split_sizes, 0, G, M};
+  int ev = 0;
+  auto mark = [&]() -> gmlp_status {
+    if (aux && ev < aux->n_stage_events) {
+      cudaError_t e = cudaEventRecord((cudaEvent_t)aux->stage_events[ev], s);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    }
+    ++ev;
+    return GMLP_OK;
+  };
+
+  const int epi1 = act == GMLP_ACT_SWIGLU ? EPI_FC1_SWIGLU : EPI_FC1_SRELU;
+  if (fmt == GMLP_MXFP8) {
+    RowQuantArgs q{};
+    q.x = x;
+    q.M = M;
+    q.K = K;
+    q.grp = gs;
+    q.format = GMLP_MXFP8;
+    q.tiled = 1;
+    q.codes = x_codes;
+    q.scales = x_scales;
+    GMLP_CUDA(launch_row_quant(q, s), "x quantise launch");
+    GMLP_TRY(mark());
+    GemmArgs g1{};
+    g1.format = GMLP_MXFP8;
+    g1.epi = epi1;
+    g1.a_codes = x_codes;
+    g1.a_scales = x_scales;
+    g1.b_codes = W1->codes;
+    g1.b_scales = W1->scales;
+    g1.M = M;
+    g1.kbytes = K;
+    g1.n_out = n1;
+    g1.grp = gs;
+    g1.probs = probs;
+    g1.out_codes = f_codes;
+    g1.out_scales = f_scales;
+    g1.n_cols_out = N;
+    GMLP_CUDA(launch_gemm(g1, s), "fc1 launch");
+    GMLP_TRY(mark());
+    GemmArgs g2{};
+    g2.format = GMLP_MXFP8;
+    g2.epi = EPI_FC2;
+    g2.a_codes = f_codes;
+    g2.a_scales = f_scales;
+    g2.b_codes = W2->codes;
+    g2.b_scales = W2->scales;
+    g2.M = M;
+    g2.kbytes = N;
+    g2.n_out = K;
+    g2.grp = gs;
+    g2.out_bf16 = y;
+    g2.n_cols_out = K;
+    GMLP_CUDA(launch_gemm(g2, s), "fc2 launch");
+    GMLP_TRY(mark());
+    return GMLP_OK;
+  }
+
+  // NVFP4
+  float* amax_ws = reinterpret_cast<float*>(ws + L.amax);
+  float* x_amax = amax_ws;
+  float* f_pre = (aux && aux->fc2x_amax_pre) ? aux->fc2x_amax_pre : amax_ws + G;
+  float* f_post = (aux && aux->fc2x_amax_post) ? aux->fc2x_amax_post : amax_ws + 2 * G;
+  uint16_t* f_bf16 = (aux && aux->fc2x_bf16) ? aux->fc2x_bf16 : reinterpret_cast<uint16_t*>(ws + L.f_bf16);
+  if (!aligned16(f_bf16)) return fail(GMLP_ERR_INVALID_ARG, "aux fc2x_bf16 misaligned");
+  GMLP_CUDA(launch_group_amax(x, M, K, gs, x_amax, s), "x amax launch");
+  GMLP_TRY(mark());
+  {
+    RowQuantArgs q{};
+    q.x = x;
+    q.M = M;
+    q.K = K;
+    q.grp = gs;
+    q.format = GMLP_NVFP4;
+    q.tiled = 1;
+    q.codes = x_codes;
+    q.scales = x_scales;
+    q.amax = x_amax;
+    GMLP_CUDA(launch_row_quant(q, s), "x quantise launch");
+    GMLP_CUDA(cudaMemsetAsync(f_pre, 0, sizeof(float) * G, s), "memset");
+    GMLP_CUDA(cudaMemsetAsync(f_post, 0, sizeof(float) * G, s), "memset");
+  }
+  GMLP_TRY(mark());
+  GemmArgs g1{};
+  g1.format = GMLP_NVFP4;
+  g1.epi = epi1;
+  g1.a_codes = x_codes;
+  g1.a_scales = x_scales;
+  g1.b_codes = W1->codes;
+  g1.b_scales = W1->scales;
+  g1.M = M;
+  g1.kbytes = K / 2;
+  g1.n_out = n1;
+  g1.grp = gs;
+  g1.a_amax = x_amax;
+  g1.b_S = W1->global_scale;
+  g1.probs = probs;
+  g1.out_bf16 = f_bf16;
+  g1.amax_pre = f_pre;
+  g1.amax_post = f_post;
+  g1.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
+  g1.n_cols_out = N;
+  GMLP_CUDA(launch_gemm(g1, s), "fc1 launch");
+  GMLP_TRY(mark());
+  {
+    RowQuantArgs q{};
+    q.x = f_bf16;
+    q.M = M;
+    q.K = N;
+    q.grp = gs;
+    q.format = GMLP_NVFP4;
+    q.tiled = 1;
+    q.codes = f_codes;
+    q.scales = f_scales;
+    q.amax = f_pre;
+    GMLP_CUDA(launch_row_quant(q, s), "fc2_x quantise launch");
+  }
+  GMLP_TRY(mark());
+  GemmArgs g2{};
+  g2.format = GMLP_NVFP4;
+  g2.epi = EPI_FC2;
+  g2.a_codes = f_codes;
+  g2.a_scales = f_scales;
+  g2.b_codes = W2->codes;
+  g2.b_scales = W2->scales;
+  g2.M = M;
+  g2.kbytes = N / 2;
+  g2.n_out = K;
+  g2.grp = gs;
+  g2.a_amax = f_pre;
+  g2.b_S = W2->global_scale;
+  g2.out_bf16 = y;
+  g2.n_cols_out = K;
+  GMLP_CUDA(launch_gemm(g2, s), "fc2 launch");
+  GMLP_TRY(mark());
+  return GMLP_OK;
+}
+
+gmlp_status gmlp_check_device_status(gmlp_stream stream) {
+  g_last_error[0] = 0;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  const int a = quant_read_clear_status();
+  const int b = gemm_read_clear_status();
+  const int code = a ? a : b;
+  if (code < 0) return fail(GMLP_ERR_CUDA, "reading the device status word failed");
+  if (code == GMLP_ERR_DEVICE_TIMEOUT) return fail(GMLP_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait");
+  if (code == GMLP_ERR_DEVICE_BOUNDS)
+    return fail(GMLP_ERR_DEVICE_BOUNDS, "split_sizes negative or summing past M");
+  if (code) return fail((gmlp_status)code, "device status %d", code);
+  return GMLP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,513 @@
+// gemm.cu -- persistent grouped GEMM on block-scaled tcgen05 tensor cores with
+// the fused fc1 epilogue (activation x prob, then MXFP8 requantisation or
+// bf16 + NVFP4 amaxes) and the fc2 bf16 epilogue.
+//
+// Method: PR #2769 "GEMM + Swiglu fused Grouped MLP for MXFP8" (sequence
+// diagram: the FC1 GLU kernel takes the MXFP8 a_tensor, the b_tensor weights
+// and prob_tensor and writes the MXFP8 activation with its row scales; the
+// FC2 kernel writes the output) and PR #3837 "Reduce NVFP4 quantization work
+// for the fused GroupedMLP fc2 input with activation recompute" (the
+// Hadamard-fused fc1 kernel returns fc2_x and its pre-RHT and post-RHT amax;
+// the sign mask enters the post-RHT amax; the accumulator is rounded through
+// the bf16 C type before the activation).
+//
+// Design (GB300, one CTA per SM, 320 threads):
+//   warp 0    TMA producer: A tile 128 x 128 B, B tile 256 x 128 B (128-byte
+//             swizzle) and the tile's scale blocks (bulk copies) per stage,
+//             4 stages, one mbarrier pair per stage;
+//   warp 1    TMEM owner and MMA issuer: per stage the scale blocks go to TMEM
+//             (tcgen05.cp 32x128b.warpx4), then 4 MMAs (M=128, N=256, K=32
+//             FP8 / K=64 FP4) accumulate into 256 TMEM columns;
+//   warps 2-9 epilogue: each drains its 32 lanes x 128 columns into
+//             registers, frees the accumulator at once (so the next tile's
+//             mainloop overlaps the epilogue math), then computes and stores.
+// Tiles: (expert g, 128-row tile of g's tokens, 256-column output tile),
+// ordered expert-major and handed out round-robin to the persistent CTAs.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "device.cuh"
+
+namespace gmlp {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreadsGemm = 320;
+constexpr int kBM = 128, kBN = 256, kBKBytes = 128;
+constexpr int kATileBytes = kBM * kBKBytes;  // 16 KB
+constexpr int kBTileBytes = kBN * kBKBytes;  // 32 KB
+constexpr uint32_t kAccCols = 256;
+constexpr uint32_t kTmemCols = 512;
+
+template <int FMT>
+struct Fmt {
+  // bytes of scale factors per 128 rows per stage: MXFP8 4 scales/row (one
+  // 512-byte block), NVFP4 16 scales/row (four blocks)
+  static constexpr int kSfBytes = FMT == GMLP_MXFP8 ? 512 : 2048;
+  static constexpr uint32_t kSfCols = FMT == GMLP_MXFP8 ? 16 : 64;  // TMEM columns per stage
+  static constexpr size_t kSmem = (size_t)kStages * (kATileBytes + kBTileBytes + 3 * kSfBytes);
+};
+
+// Instruction descriptor (tcgen05 block-scaled kinds): A/B formats in bits
+// 7..9 / 10..12 (MXFP8: E4M3 = 0; NVFP4 kind: E2M1 = 1), K-major A and B,
+// N >> 3 in bits 17..22, scale type in bit 23 (UE8M0 = 1, UE4M3 = 0),
+// M >> 4 in bits 24..28, scale-factor byte selectors in bits 4..5 (B) and
+// 29..30 (A).
+template <int FMT>
+__device__ __forceinline__ uint32_t idesc_for(int k) {
+  if (FMT == GMLP_MXFP8)
+    return (uint32_t(kBN >> 3) << 17) | (1u << 23) | (uint32_t(kBM >> 4) << 24) | (uint32_t(k) << 4) |
+           (uint32_t(k) << 29);
+  return (1u << 7) | (1u << 10) | (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+}
+
+struct Tile {
+  int g, mt, nt;
+};
+
+__device__ __forceinline__ Tile decode_tile(const int* off, const int* ip, int G, int w) {
+  int lo = 0, hi = G - 1;  // largest g with ip[g] <= w
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ip[mid] <= w) lo = mid; else hi = mid - 1;
+  }
+  Tile t;
+  t.g = lo;
+  const int mtiles = (off[lo + 1] - off[lo] + kBM - 1) / kBM;
+  const int local = w - ip[lo];
+  t.nt = local / mtiles;
+  t.mt = local % mtiles;
+  return t;
+}
+
+// Bounded wait used only while shutting down after an abort (no new report).
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > 500000000ull) return;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return bf16_bits(lo) | (bf16_bits(hi) << 16);
+}
+
+// MXFP8 quantisation of 32 consecutive values f (bf16-exact FP32) into 8
+// code words; returns the scale exponent.
+__device__ __forceinline__ int mx_block(const float* f, uint32_t* words) {
+  float am = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(f[i]));
+  const int e = mxfp8_exponent(am);
+  const float mul = exp2_neg(e);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    words[i] = e4m3x2(__fmul_rn(f[4 * i], mul), __fmul_rn(f[4 * i + 1], mul)) |
+               (e4m3x2(__fmul_rn(f[4 * i + 2], mul), __fmul_rn(f[4 * i + 3], mul)) << 16);
+  return e;
+}
+
+__device__ __forceinline__ float silu_times(float gate, float up) {
+  return gate / (1.0f + expf(-gate)) * up;
+}
+
+// ------------------------------------------------------------------ epilogues
+
+template <int FMT, int EPI>
+__device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Tile& t, const int* off,
+                                         const int* tb, int q, int lane, int half) {
+  const int row = 32 * q + lane;
+  const int m_g = off[t.g + 1] - off[t.g];
+  const int lr = t.mt * kBM + row;
+  const bool valid = lr < m_g;
+  const int64_t grow = (int64_t)off[t.g] + lr;
+  float alpha = 1.0f;
+  if (FMT == GMLP_NVFP4) alpha = __fdiv_rn(1.0f, __fmul_rn(nvfp4_global_scale(a.a_amax[t.g]), a.b_S[t.g]));
+
+  if (EPI == EPI_FC2) {
+    if (!valid) return;
+    uint16_t* yrow = a.out_bf16 + grow * a.n_cols_out + (int64_t)t.nt * kBN + half * 128;
+#pragma unroll
+    for (int j = 0; j < 128; j += 8) {
+      uint4 o;
+      o.x = pack_bf16x2(acc[j] * alpha, acc[j + 1] * alpha);
+      o.y = pack_bf16x2(acc[j + 2] * alpha, acc[j + 3] * alpha);
+      o.z = pack_bf16x2(acc[j + 4] * alpha, acc[j + 5] * alpha);
+      o.w = pack_bf16x2(acc[j + 6] * alpha, acc[j + 7] * alpha);
+      *reinterpret_cast<uint4*>(yrow + j) = o;
+    }
+    return;
+  }
+
+  const float prob = (valid && a.probs) ? a.probs[grow] : 1.0f;
+  constexpr int kOut = EPI == EPI_FC1_SWIGLU ? 64 : 128;  // fc2_x values this thread produces
+  // fc2_x = bf16(act(bf16(acc * alpha)) * prob), in place in acc[0..kOut)
+  if (EPI == EPI_FC1_SWIGLU) {
+    // 64-column chunks hold 32 gate then 32 up columns of the same 32 outputs
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float hg = round_bf16(acc[64 * b + i] * alpha);
+        const float hu = round_bf16(acc[64 * b + 32 + i] * alpha);
+        acc[32 * b + i] = round_bf16(silu_times(hg, hu) * prob);
+      }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 128; ++i) {
+      const float h = fmaxf(round_bf16(acc[i] * alpha), 0.0f);
+      acc[i] = round_bf16(h * h * prob);
+    }
+  }
+  const int64_t oc0 = (int64_t)t.nt * (kBN / (EPI == EPI_FC1_SWIGLU ? 2 : 1)) + half * kOut;
+
+  if (FMT == GMLP_MXFP8) {
+    constexpr int kBlocks = kOut / 32;
+    uint32_t sbytes = 0;
+#pragma unroll
+    for (int b = 0; b < kBlocks; ++b) {
+      uint32_t words[8];
+      const int e = mx_block(acc + 32 * b, words);
+      sbytes |= uint32_t(e + 127) << (8 * b);
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(a.out_codes + grow * a.n_cols_out + oc0 + 32 * b);
+        dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
+        dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
+      }
+    }
+    if (valid) {
+      const int nscale = (int)(a.n_cols_out / 32);
+      const int kidx = (int)(oc0 / 32);
+      const int64_t blk = (int64_t)(tb[t.g] + t.mt) * (nscale >> 2) + (kidx >> 2);
+      uint8_t* dst = a.out_scales + blk * 512 + lane * 16 + q * 4 + (kidx & 3);
+      if (kBlocks == 2)
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)sbytes;
+      else
+        *reinterpret_cast<uint32_t*>(dst) = sbytes;
+    }
+  } else {
+    // NVFP4: store bf16 fc2_x; per-group max |fc2_x| and post-RHT amax over
+    // 16-row column chunks (lanes 0-15 and 16-31 each hold one chunk; rows
+    // past the group end count as zero).
+    float pre = 0.0f, post = 0.0f;
+    const bool neg = (a.rht_mask >> (lane & 15)) & 1u;
+#pragma unroll
+    for (int c = 0; c < kOut; ++c) {
+      float v = valid ? acc[c] : 0.0f;
+      pre = fmaxf(pre, fabsf(v));
+      if (neg) v = -v;
+#pragma unroll
+      for (int h = 1; h < 16; h <<= 1) {
+        const float p = __shfl_xor_sync(0xffffffffu, v, h);
+        v = (lane & h) ? (p - v) : (v + p);
+      }
+      post = fmaxf(post, fabsf(v));
+    }
+    if (valid) {
+      uint16_t* dst = a.out_bf16 + grow * a.n_cols_out + oc0;
+#pragma unroll
+      for (int j = 0; j < kOut; j += 8) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[j], acc[j + 1]);
+        o.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+        o.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
+        o.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+        *reinterpret_cast<uint4*>(dst + j) = o;
+      }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      pre = fmaxf(pre, __shfl_xor_sync(0xffffffffu, pre, d));
+      post = fmaxf(post, __shfl_xor_sync(0xffffffffu, post, d));
+    }
+    if (lane == 0) {
+      atomicMax(reinterpret_cast<int*>(a.amax_pre + t.g), __float_as_int(pre));
+      atomicMax(reinterpret_cast<int*>(a.amax_post + t.g), __float_as_int(post * 0.25f));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int FMT, int EPI>
+__global__ void __launch_bounds__(kThreadsGemm, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmArgs a) {
+  using F = Fmt<FMT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + kStages * kATileBytes;
+  uint8_t* sSFA = sB + kStages * kBTileBytes;
+  uint8_t* sSFB = sSFA + kStages * F::kSfBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + kStages * 2 * F::kSfBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  int* bad = reinterpret_cast<int*>(tslot + 2);
+  int* off = reinterpret_cast<int*>(tslot + 4);
+  int* tb = off + kMaxGroups + 1;
+  int* ip = tb + kMaxGroups + 1;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int G = a.grp.G;
+  const int n_tiles = (int)(a.n_out / kBN);
+  const int KB = (int)(a.kbytes / kBKBytes);
+
+  if (warp == 0) {
+    // group tables: row offsets, 128-row tile bases, tile-work prefix
+    long long c0 = 0, c1 = 0, c2 = 0;
+    int b = 0;
+    for (int base = 0; base < G; base += 32) {
+      const int g = base + lane;
+      long long m = 0;
+      if (g < G) {
+        m = a.grp.splits ? (long long)a.grp.splits[g] : (long long)a.grp.uniform_m;
+        if (m < 0 || m > a.grp.M) {
+          b = 1;
+          m = 0;
+        }
+      }
+      const long long v0 = m, v1 = (m + kBM - 1) / kBM, v2 = v1 * n_tiles;
+      long long i0 = v0, i1 = v1, i2 = v2;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const long long t0 = __shfl_up_sync(0xffffffffu, i0, d), t1 = __shfl_up_sync(0xffffffffu, i1, d),
+                        t2 = __shfl_up_sync(0xffffffffu, i2, d);
+        if (lane >= d) {
+          i0 += t0;
+          i1 += t1;
+          i2 += t2;
+        }
+      }
+      if (g < G) {
+        off[g] = (int)(c0 + i0 - v0);
+        tb[g] = (int)(c1 + i1 - v1);
+        ip[g] = (int)(c2 + i2 - v2);
+      }
+      c0 += __shfl_sync(0xffffffffu, i0, 31);
+      c1 += __shfl_sync(0xffffffffu, i1, 31);
+      c2 += __shfl_sync(0xffffffffu, i2, 31);
+      if (c0 > a.grp.M) b = 1;
+    }
+    b = __any_sync(0xffffffffu, b);
+    if (lane == 0) {
+      off[G] = (int)c0;
+      tb[G] = (int)c1;
+      ip[G] = (int)c2;
+      *bad = b;
+      if (b && blockIdx.x == 0) report_device_error(GMLP_ERR_DEVICE_BOUNDS);
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+    }
+  } else if (warp == 1) {
+    tmem_alloc(tslot, kTmemCols);
+  } else if (threadIdx.x == 64) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 8);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const int total = *bad ? 0 : ip[G];
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    const uint64_t pol_a = policy_evict_normal();
+    const uint64_t pol_b = policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0, armed = 0, armed_parity = 0;
+    constexpr uint32_t kTx = kATileBytes + kBTileBytes + 3 * F::kSfBytes;
+    for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+      const Tile t = decode_tile(off, ip, G, w);
+      const int rowA = off[t.g] + t.mt * kBM;
+      const int64_t tileA = tb[t.g] + t.mt;
+      const int64_t rowB = (int64_t)t.g * a.n_out + (int64_t)t.nt * kBN;
+      const int64_t tileB = rowB / 128;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&full[stage], kTx);
+        armed |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        tma_load_2d(sA + stage * kATileBytes, &tmA, kb * kBKBytes, rowA, &full[stage], pol_a);
+        tma_load_2d(sB + stage * kBTileBytes, &tmB, kb * kBKBytes, (int32_t)rowB, &full[stage], pol_b);
+        bulk_load(sSFA + stage * F::kSfBytes, a.a_scales + (tileA * KB + kb) * F::kSfBytes, F::kSfBytes,
+                  &full[stage]);
+        uint8_t* sfb = sSFB + stage * 2 * F::kSfBytes;
+        bulk_load(sfb, a.b_scales + (tileB * KB + kb) * F::kSfBytes, F::kSfBytes, &full[stage]);
+        bulk_load(sfb + F::kSfBytes, a.b_scales + ((tileB + 1) * KB + kb) * F::kSfBytes, F::kSfBytes,
+                  &full[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    // every copy this thread started must land before the CTA exits
+    for (int s = 0; s < kStages; ++s)
+      if (armed & (1u << s)) mbar_wait_drain(&full[s], (armed_parity >> s) & 1u);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    int stage = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    const uint32_t sf_base = tbase + kAccCols;
+    for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+      if (!mbar_wait(tempty, acc_phase ^ 1, abort_flag)) break;
+      tc_fence_after();
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sfa_t = sf_base + stage * F::kSfCols;
+        const uint32_t sfb_t = sfa_t + (FMT == GMLP_MXFP8 ? 4 : 16);
+        const uint32_t sA_addr = smem_u32(sA + stage * kATileBytes);
+        const uint32_t sB_addr = smem_u32(sB + stage * kBTileBytes);
+        const uint32_t sfa_addr = smem_u32(sSFA + stage * F::kSfBytes);
+        const uint32_t sfb_addr = smem_u32(sSFB + stage * 2 * F::kSfBytes);
+        if (FMT == GMLP_MXFP8) {
+          tc_cp_32x128b_x4(sfa_t, smem_desc(sfa_addr, 0, 128, 0));
+          tc_cp_32x128b_x4(sfb_t, smem_desc(sfb_addr, 0, 128, 0));
+          tc_cp_32x128b_x4(sfb_t + 4, smem_desc(sfb_addr + 512, 0, 128, 0));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            tc_cp_32x128b_x4(sfa_t + 4 * k, smem_desc(sfa_addr + 512 * k, 0, 128, 0));
+            tc_cp_32x128b_x4(sfb_t + 8 * k, smem_desc(sfb_addr + 512 * k, 0, 128, 0));
+            tc_cp_32x128b_x4(sfb_t + 8 * k + 4, smem_desc(sfb_addr + 2048 + 512 * k, 0, 128, 0));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t ad = smem_desc(sA_addr + 32 * k, 16, 1024, 2);
+          const uint64_t bd = smem_desc(sB_addr + 32 * k, 16, 1024, 2);
+          const uint32_t accumulate = (kb > 0 || k > 0) ? 1u : 0u;
+          if (FMT == GMLP_MXFP8)
+            tc_mma_mxf8(tbase, ad, bd, idesc_for<FMT>(k), sfa_t, sfb_t, accumulate);
+          else
+            tc_mma_nvf4(tbase, ad, bd, idesc_for<FMT>(k), sfa_t + 4 * k, sfb_t + 8 * k, accumulate);
+        }
+        tc_commit(&empty[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      tc_commit(tfull);
+      acc_phase ^= 1;
+    }
+    // all MMAs and copies this thread issued complete before TMEM is freed
+    tc_commit(drain);
+    mbar_wait_drain(drain, 0);
+  } else if (warp >= 2) {
+    // ---------------- epilogue
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    uint32_t acc_phase = 0;
+    for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+      const Tile t = decode_tile(off, ip, G, w);
+      if (!mbar_wait(tfull, acc_phase, abort_flag)) break;
+      tc_fence_after();
+      float acc[128];
+      const uint32_t taddr = tbase + (uint32_t(32 * q) << 16) + uint32_t(half * 128);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tmem_ld32(taddr + 32 * j, acc + 32 * j);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+      acc_phase ^= 1;
+      epilogue<FMT, EPI>(a, acc, t, off, tb, q, lane, half);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2D uint8 tensor map over [rows][row_bytes] with a box of box_rows x 128
+// bytes and the 128-byte swizzle the MMA descriptors assume.
+bool make_tmap(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)kBKBytes, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int FMT, int EPI>
+cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
+  const size_t smem = Fmt<FMT>::kSmem + 1024 + 256 + 3 * (kMaxGroups + 1) * sizeof(int);
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_set[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev & 63] = true;
+  }
+  CUtensorMap ta, tbm;
+  if (!make_tmap(&ta, a.a_codes, a.kbytes, a.M, kBM)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tbm, a.b_codes, a.kbytes, (int64_t)a.grp.G * a.n_out, kBN)) return cudaErrorInvalidValue;
+  const int64_t max_tiles = ((a.M + kBM - 1) / kBM + a.grp.G) * (a.n_out / kBN);
+  int grid = num_sms();
+  if (max_tiles < grid) grid = (int)max_tiles;
+  if (grid < 1) grid = 1;
+  gemm_kernel<FMT, EPI><<<grid, kThreadsGemm, smem, s>>>(ta, tbm, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_read_clear_status() { return read_clear_status(); }
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
+  if (a.M == 0) return cudaSuccess;
+  if (a.format == GMLP_MXFP8) {
+    if (a.epi == EPI_FC1_SWIGLU) return launch_t<GMLP_MXFP8, EPI_FC1_SWIGLU>(a, s);
+    if (a.epi == EPI_FC1_SRELU) return launch_t<GMLP_MXFP8, EPI_FC1_SRELU>(a, s);
+    return launch_t<GMLP_MXFP8, EPI_FC2>(a, s);
+  }
+  if (a.epi == EPI_FC1_SWIGLU) return launch_t<GMLP_NVFP4, EPI_FC1_SWIGLU>(a, s);
+  if (a.epi == EPI_FC1_SRELU) return launch_t<GMLP_NVFP4, EPI_FC1_SRELU>(a, s);
+  return launch_t<GMLP_NVFP4, EPI_FC2>(a, s);
+}
+
+}  // namespace gmlp

@@ -1,0 +1,102 @@
+// internal.h -- declarations shared by the CUDA path's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gmlp.h"
+
+namespace gmlp {
+
+constexpr int kMaxGroups = 512;
+
+// Per-group tables every kernel derives from split_sizes at its start
+// (split sizes stay on the device).  When `splits` is null the G groups all
+// have `uniform_m` rows (the experts of a stacked weight).
+struct GroupSrc {
+  const int64_t* splits;
+  int32_t uniform_m;
+  int32_t G;
+  int64_t M;
+};
+
+// ---- quantisers (quant.cu) ----
+
+struct RowQuantArgs {
+  const uint16_t* x;        // bf16 [M][K] (or weights [G][rows][K])
+  int64_t M, K;
+  GroupSrc grp;
+  int format;               // GMLP_MXFP8 / GMLP_NVFP4
+  int tiled;                // scales in GEMM_TILED layout
+  uint8_t* codes;
+  uint8_t* scales;
+  const float* amax;        // NVFP4: per-group amax giving S_g
+  float* S_out;             // optional: write S_g for every group
+  int swiglu_interleave;    // weights: gate/up 32-row interleave within each group
+  float* zero_ptr;          // optional: floats zeroed by the first CTA (for later atomics)
+  int zero_count;
+};
+cudaError_t launch_row_quant(const RowQuantArgs& a, cudaStream_t s);
+
+// per-group max |x| into amax[G] (zeroed by the launcher)
+cudaError_t launch_group_amax(const uint16_t* x, int64_t M, int64_t K, GroupSrc grp, float* amax,
+                              cudaStream_t s);
+
+cudaError_t launch_hadamard_amax(const uint16_t* x, int64_t M, int64_t K, GroupSrc grp, uint32_t mask,
+                                 float* amax_pre, float* amax_post, cudaStream_t s);
+
+struct ColQuantArgs {
+  const uint16_t* x;
+  int64_t M, K;
+  GroupSrc grp;
+  int use_rht;
+  uint32_t mask;
+  const float* amax_row;    // S for the rowwise output
+  const float* amax_col;    // S for the columnwise output
+  uint8_t* row_codes;       // nullable: also write rowwise NVFP4 in the same pass
+  uint8_t* row_scales;
+  int row_tiled;
+  uint8_t* col_codes;
+  uint8_t* col_scales;
+};
+cudaError_t launch_col_quant(const ColQuantArgs& a, cudaStream_t s);
+
+// ---- grouped GEMM (gemm.cu) ----
+
+enum Epilogue : int {
+  EPI_FC1_SWIGLU = 0,  // fc1 + SwiGLU (gate/up 32-column interleave) x prob
+  EPI_FC1_SRELU = 1,   // fc1 + squared ReLU x prob
+  EPI_FC2 = 2,         // fc2: bf16 output
+};
+
+struct GemmArgs {
+  int format;              // GMLP_MXFP8 / GMLP_NVFP4 (both operands)
+  int epi;                 // Epilogue
+  const uint8_t* a_codes;  // [M][kbytes]
+  const uint8_t* a_scales; // GEMM_TILED, groups of the token split
+  const uint8_t* b_codes;  // [G][n_out][kbytes]
+  const uint8_t* b_scales; // GEMM_TILED, experts as groups of n_out rows
+  int64_t M;
+  int64_t kbytes;          // contraction bytes per row (K or K/2)
+  int64_t n_out;           // accumulator columns per expert (fc1: 2N or N; fc2: K)
+  GroupSrc grp;
+  const float* a_amax;     // NVFP4: per-group amax of A (S_a = 2688 / amax)
+  const float* b_S;        // NVFP4: per-expert S of B
+  const float* probs;      // fc1: [M] or null
+  // MXFP8 fc1 outputs (fc2_x quantised in the epilogue)
+  uint8_t* out_codes;      // [M][n_cols_out]
+  uint8_t* out_scales;     // GEMM_TILED over the token split
+  // NVFP4 fc1 output and fc2 output
+  uint16_t* out_bf16;      // [M][n_cols_out]
+  float* amax_pre;         // NVFP4 fc1: [G] (atomicMax, zeroed before)
+  float* amax_post;
+  uint32_t rht_mask;
+  int64_t n_cols_out;      // row length of the output (fc1: N; fc2: K)
+};
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace gmlp

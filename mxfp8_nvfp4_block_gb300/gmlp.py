@@ -1,0 +1,255 @@
+"""Thin ctypes binding of libgmlp.so (include/gmlp.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch provides device memory and streams.  If the library is
+missing or fails to load, :func:`load` raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgmlp.so")
+
+OK, ERR_INVALID_ARG, ERR_INVALID_DIMS, ERR_UNSUPPORTED_RECIPE, ERR_UNSUPPORTED_DEVICE, ERR_WORKSPACE, \
+    ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_DEVICE_BOUNDS = range(9)
+MXFP8, NVFP4 = 0, 1
+SWIGLU, SRELU = 0, 1
+COMPACT, GEMM_TILED = 0, 1
+
+EXPORTS = ["gmlp_tiled_scales_bytes", "gmlp_group_hadamard_amax", "gmlp_group_quantize_with_amax",
+           "gmlp_group_quantize", "gmlp_prepare_weights", "gmlp_forward_workspace_size", "gmlp_forward",
+           "gmlp_check_device_status", "gmlp_last_error", "gmlp_version"]
+
+
+class Recipe(ctypes.Structure):
+    _fields_ = [("format", ctypes.c_int32), ("use_rht", ctypes.c_int32), ("rht_sign_mask", ctypes.c_uint32),
+                ("scale_layout", ctypes.c_int32)]
+
+
+class QTensor(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+class QWeightC(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("global_scale", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("G", ctypes.c_int32),
+                ("format", ctypes.c_int32), ("swiglu_interleaved", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class FwdAux(ctypes.Structure):
+    _fields_ = [("fc2x_codes", ctypes.c_void_p), ("fc2x_scales", ctypes.c_void_p), ("fc2x_bf16", ctypes.c_void_p),
+                ("fc2x_amax_pre", ctypes.c_void_p), ("fc2x_amax_post", ctypes.c_void_p),
+                ("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("n_stage_events", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+_vp, _i64, _i32, _u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libgmlp.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libgmlp.so not found at {path}: build it with __graft_entry__.build()")
+    L = ctypes.CDLL(path)
+    sigs = {
+        "gmlp_tiled_scales_bytes": (ctypes.c_size_t, [_i64, _i32, _i64]),
+        "gmlp_group_hadamard_amax": (_i32, [_vp, _i64, _i64, _vp, _i32, _u32, _vp, _vp, _vp]),
+        "gmlp_group_quantize_with_amax": (_i32, [_vp, _i64, _i64, _vp, _i32, ctypes.POINTER(Recipe), _vp, _vp,
+                                                 ctypes.POINTER(QTensor), ctypes.POINTER(QTensor), _vp]),
+        "gmlp_group_quantize": (_i32, [_vp, _i64, _i64, _vp, _i32, ctypes.POINTER(Recipe),
+                                       ctypes.POINTER(QTensor), ctypes.POINTER(QTensor), _vp, _vp, _vp]),
+        "gmlp_prepare_weights": (_i32, [_vp, _i32, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+        "gmlp_forward_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i32, _i32, ctypes.POINTER(Recipe)]),
+        "gmlp_forward": (_i32, [_vp, _i64, _i64, _i64, _vp, _i32, ctypes.POINTER(QWeightC),
+                                ctypes.POINTER(QWeightC), _vp, _i32, ctypes.POINTER(Recipe), _vp,
+                                ctypes.POINTER(FwdAux), _vp, ctypes.c_size_t, _vp]),
+        "gmlp_check_device_status": (_i32, [_vp]),
+        "gmlp_last_error": (ctypes.c_char_p, []),
+        "gmlp_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sigs.items():
+        f = getattr(L, name)
+        f.restype, f.argtypes = res, args
+    _lib = L
+    return L
+
+
+class GmlpError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"gmlp status {status}: {msg}")
+        self.status = status
+
+
+def _check(st: int) -> None:
+    if st != OK:
+        raise GmlpError(st, load().gmlp_last_error().decode())
+
+
+def _p(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def recipe(fmt: int, use_rht: bool = False, mask: int = 0, layout: int = GEMM_TILED) -> Recipe:
+    return Recipe(fmt, int(bool(use_rht)), int(mask) & 0xFFFF, layout)
+
+
+def tiled_scales_bytes(M: int, G: int, nscale: int) -> int:
+    return load().gmlp_tiled_scales_bytes(M, G, nscale)
+
+
+def _u8(n, device):
+    return torch.empty(max(int(n), 16), dtype=torch.uint8, device=device)
+
+
+def _bits(x: torch.Tensor) -> torch.Tensor:
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous()
+    return x
+
+
+# ------------------------------------------------------------------ quantisers
+
+def group_hadamard_amax(x: torch.Tensor, splits: torch.Tensor, mask: int, stream=None):
+    """Per-group (pre-RHT, post-RHT) amax of bf16 x [M, K]."""
+    x = _bits(x)
+    M, K = x.shape
+    G = splits.numel()
+    pre = torch.empty(G, dtype=torch.float32, device=x.device)
+    post = torch.empty(G, dtype=torch.float32, device=x.device)
+    _check(load().gmlp_group_hadamard_amax(_p(x), M, K, _p(splits), G, mask, _p(pre), _p(post), _stream(stream)))
+    return pre, post
+
+
+def alloc_quant_outputs(M: int, K: int, G: int, fmt: int, layout: int, rowwise: bool, columnwise: bool,
+                        splits_host=None, device="cuda"):
+    """Caller-side device buffers for a group quantisation."""
+    out = {}
+    blk, cdiv = (32, 1) if fmt == MXFP8 else (16, 2)
+    if rowwise:
+        ns = K // blk
+        sbytes = tiled_scales_bytes(M, G, ns) if layout == GEMM_TILED else M * ns
+        out["row"] = (_u8(M * K // cdiv, device), _u8(sbytes, device))
+    if columnwise:
+        mp = sum((int(m) + 15) // 16 * 16 for m in splits_host)
+        out["col"] = (_u8(K * mp // 2, device), _u8(K * mp // 16, device))
+    return out
+
+
+def group_quantize_with_amax(x, splits, rec: Recipe, amax_pre=None, amax_post=None, *, rowwise=True,
+                             columnwise=False, splits_host=None, stream=None) -> dict:
+    x = _bits(x)
+    M, K = x.shape
+    G = splits.numel()
+    bufs = alloc_quant_outputs(M, K, G, rec.format, rec.scale_layout, rowwise, columnwise, splits_host, x.device)
+    row = QTensor(bufs["row"][0].data_ptr(), bufs["row"][1].data_ptr()) if rowwise else None
+    col = QTensor(bufs["col"][0].data_ptr(), bufs["col"][1].data_ptr()) if columnwise else None
+    _check(load().gmlp_group_quantize_with_amax(
+        _p(x), M, K, _p(splits), G, ctypes.byref(rec), _p(amax_pre), _p(amax_post),
+        ctypes.byref(row) if row else None, ctypes.byref(col) if col else None, _stream(stream)))
+    return bufs
+
+
+def group_quantize(x, splits, rec: Recipe, *, rowwise=True, columnwise=False, splits_host=None,
+                   stream=None) -> dict:
+    x = _bits(x)
+    M, K = x.shape
+    G = splits.numel()
+    bufs = alloc_quant_outputs(M, K, G, rec.format, rec.scale_layout, rowwise, columnwise, splits_host, x.device)
+    pre = post = None
+    if rec.format == NVFP4:
+        pre = torch.empty(G, dtype=torch.float32, device=x.device)
+        post = torch.empty(G, dtype=torch.float32, device=x.device)
+        bufs["amax_pre"], bufs["amax_post"] = pre, post
+    row = QTensor(bufs["row"][0].data_ptr(), bufs["row"][1].data_ptr()) if rowwise else None
+    col = QTensor(bufs["col"][0].data_ptr(), bufs["col"][1].data_ptr()) if columnwise else None
+    _check(load().gmlp_group_quantize(
+        _p(x), M, K, _p(splits), G, ctypes.byref(rec), ctypes.byref(row) if row else None,
+        ctypes.byref(col) if col else None, _p(pre), _p(post), _stream(stream)))
+    return bufs
+
+
+# ------------------------------------------------------------------ weights
+
+@dataclass
+class QWeight:
+    codes: torch.Tensor
+    scales: torch.Tensor
+    global_scale: torch.Tensor | None
+    amax: torch.Tensor | None
+    rows: int
+    cols: int
+    G: int
+    format: int
+    swiglu: bool
+
+    def c(self) -> QWeightC:
+        return QWeightC(self.codes.data_ptr(), self.scales.data_ptr(), _p(self.global_scale), self.rows,
+                        self.cols, self.G, self.format, int(self.swiglu), 0)
+
+
+def prepare_weights(W: torch.Tensor, fmt: int, swiglu_interleave: bool = False, stream=None) -> QWeight:
+    """Quantise stacked expert weights W [G, rows, cols] (bf16, cuda)."""
+    W = _bits(W)
+    G, rows, cols = W.shape
+    blk, cdiv = (32, 1) if fmt == MXFP8 else (16, 2)
+    codes = _u8(G * rows * cols // cdiv, W.device)
+    scales = _u8(tiled_scales_bytes(G * rows, G, cols // blk), W.device)
+    gs = am = None
+    if fmt == NVFP4:
+        gs = torch.empty(G, dtype=torch.float32, device=W.device)
+        am = torch.empty(G, dtype=torch.float32, device=W.device)
+    _check(load().gmlp_prepare_weights(_p(W), G, rows, cols, int(bool(swiglu_interleave)), fmt, _p(codes),
+                                       _p(scales), _p(gs), _p(am), _stream(stream)))
+    return QWeight(codes, scales, gs, am, rows, cols, G, fmt, bool(swiglu_interleave))
+
+
+# ------------------------------------------------------------------ forward
+
+def forward_workspace_size(M: int, K: int, N: int, G: int, act: int, rec: Recipe) -> int:
+    return load().gmlp_forward_workspace_size(M, K, N, G, act, ctypes.byref(rec))
+
+
+def forward(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *, y=None, workspace=None,
+            aux: dict | None = None, events=None, stream=None) -> torch.Tensor:
+    """y = fused grouped-MLP forward of bf16 x [M, K]."""
+    x = _bits(x)
+    M, K = x.shape
+    N = W2.cols
+    G = splits.numel()
+    if y is None:
+        y = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    need = forward_workspace_size(M, K, N, G, act, rec)
+    if workspace is None:
+        workspace = _u8(need, x.device)
+    aux_c = None
+    ev_arr = None
+    if aux is not None or events is not None:
+        aux = aux or {}
+        aux_c = FwdAux(_p(aux.get("fc2x_codes")), _p(aux.get("fc2x_scales")), _p(aux.get("fc2x_bf16")),
+                       _p(aux.get("fc2x_amax_pre")), _p(aux.get("fc2x_amax_post")), None, 0, 0)
+        if events:
+            ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+            aux_c.stage_events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))
+            aux_c.n_stage_events = len(events)
+    w1c, w2c = W1.c(), W2.c()
+    _check(load().gmlp_forward(_p(x), M, K, N, _p(splits), G, ctypes.byref(w1c), ctypes.byref(w2c), _p(probs),
+                               act, ctypes.byref(rec), _p(y), ctypes.byref(aux_c) if aux_c else None,
+                               _p(workspace), workspace.numel(), _stream(stream)))
+    return y
+
+
+def check_device_status(stream=None) -> None:
+    _check(load().gmlp_check_device_status(_stream(stream)))

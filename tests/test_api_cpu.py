@@ -1,0 +1,128 @@
+"""The C ABI library loads, exports every symbol include/gmlp.h declares, and its
+host-side checks return the documented statuses before any launch (CPU only:
+no call here reaches the device)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mxfp8_nvfp4_block_gb300 import build, gmlp
+    build.build()
+    return gmlp.load(), gmlp
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "gmlp.h")).read()
+    return sorted(set(re.findall(r"^GMLP_API [^;(]*?\b(gmlp_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert len(names) >= 10
+    out = subprocess.run(["nm", "-D", "--defined-only", lib[1].LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r" T (gmlp_\w+)", out))
+    assert set(names) <= exported, set(names) - exported
+    assert set(lib[1].EXPORTS) == set(names)
+    for n in names:
+        getattr(lib[0], n)
+
+
+def test_version_and_sizes(lib):
+    L, g = lib
+    assert b"sm_103a" in L.gmlp_version()
+    assert g.tiled_scales_bytes(512, 4, 8) == (4 + 4) * 128 * 8
+    assert g.tiled_scales_bytes(0, 3, 4) == 3 * 128 * 4
+    r = g.recipe(g.MXFP8)
+    n = g.forward_workspace_size(512, 256, 256, 4, g.SWIGLU, r)
+    assert n >= 512 * 256 * 2
+    assert g.forward_workspace_size(512, 256, 256, 4, g.SWIGLU, g.recipe(g.NVFP4)) > 512 * 256 * 2
+
+
+FAKE = 1 << 20   # an aligned non-null address; validation fails before anything dereferences it
+
+
+def test_quantize_argument_checks(lib):
+    L, g = lib
+    r = g.recipe(g.MXFP8)
+    qt = g.QTensor(FAKE, FAKE)
+    # G out of range
+    assert L.gmlp_group_quantize(FAKE, 64, 128, FAKE, 0, ctypes.byref(r), ctypes.byref(qt), None, None, None,
+                                 None) == g.ERR_INVALID_DIMS
+    assert L.gmlp_group_quantize(FAKE, 64, 128, FAKE, 513, ctypes.byref(r), ctypes.byref(qt), None, None, None,
+                                 None) == g.ERR_INVALID_DIMS
+    # K not a multiple of 128
+    assert L.gmlp_group_quantize(FAKE, 64, 96, FAKE, 2, ctypes.byref(r), ctypes.byref(qt), None, None, None,
+                                 None) == g.ERR_INVALID_DIMS
+    assert b"K" in L.gmlp_last_error()
+    # NULL recipe / split sizes / outputs
+    assert L.gmlp_group_quantize(FAKE, 64, 128, FAKE, 2, None, ctypes.byref(qt), None, None, None,
+                                 None) == g.ERR_INVALID_ARG
+    assert L.gmlp_group_quantize(FAKE, 64, 128, None, 2, ctypes.byref(r), ctypes.byref(qt), None, None, None,
+                                 None) == g.ERR_INVALID_ARG
+    assert L.gmlp_group_quantize(FAKE, 64, 128, FAKE, 2, ctypes.byref(r), None, None, None, None,
+                                 None) == g.ERR_INVALID_ARG
+    # misaligned x
+    assert L.gmlp_group_quantize(FAKE + 2, 64, 128, FAKE, 2, ctypes.byref(r), ctypes.byref(qt), None, None, None,
+                                 None) == g.ERR_INVALID_ARG
+    # MXFP8 has no columnwise output here
+    assert L.gmlp_group_quantize(FAKE, 64, 128, FAKE, 2, ctypes.byref(r), ctypes.byref(qt), ctypes.byref(qt),
+                                 None, None, None) == g.ERR_UNSUPPORTED_RECIPE
+    # unknown format
+    bad = g.Recipe(7, 0, 0, 1)
+    assert L.gmlp_group_quantize(FAKE, 64, 128, FAKE, 2, ctypes.byref(bad), ctypes.byref(qt), None, None, None,
+                                 None) == g.ERR_UNSUPPORTED_RECIPE
+    # NVFP4 needs amax buffers
+    rn = g.recipe(g.NVFP4, use_rht=True)
+    assert L.gmlp_group_quantize(FAKE, 64, 128, FAKE, 2, ctypes.byref(rn), ctypes.byref(qt), ctypes.byref(qt),
+                                 FAKE, None, None) == g.ERR_INVALID_ARG
+    assert L.gmlp_group_hadamard_amax(FAKE, 64, 100, FAKE, 2, 0, FAKE, FAKE, None) == g.ERR_INVALID_DIMS
+    assert L.gmlp_group_hadamard_amax(FAKE, 64, 128, FAKE, 2, 0, None, FAKE, None) == g.ERR_INVALID_ARG
+
+
+def test_forward_argument_checks(lib):
+    L, g = lib
+    r = g.recipe(g.MXFP8)
+    w1 = g.QWeightC(FAKE, FAKE, None, 512, 256, 4, g.MXFP8, 1, 0)
+    w2 = g.QWeightC(FAKE, FAKE, None, 256, 256, 4, g.MXFP8, 0, 0)
+    need = g.forward_workspace_size(512, 256, 256, 4, g.SWIGLU, r)
+
+    def call(M=512, K=256, N=256, G=4, W1=w1, W2=w2, act=g.SWIGLU, rec=r, ws=FAKE, wsb=need):
+        return L.gmlp_forward(FAKE, M, K, N, FAKE, G, ctypes.byref(W1), ctypes.byref(W2), None, act,
+                              ctypes.byref(rec), FAKE, None, ws, wsb, None)
+
+    assert call(K=128) == g.ERR_INVALID_DIMS                        # K % 256
+    assert call(N=192) == g.ERR_INVALID_DIMS                        # N % 128
+    assert call(G=3) == g.ERR_INVALID_DIMS                          # weights have 4 experts
+    assert call(act=9) == g.ERR_INVALID_ARG
+    assert call(wsb=need - 1) == g.ERR_WORKSPACE
+    assert call(ws=None) == g.ERR_WORKSPACE
+    assert call(rec=g.recipe(g.NVFP4)) == g.ERR_UNSUPPORTED_RECIPE  # weight format differs
+    w1_plain = g.QWeightC(FAKE, FAKE, None, 512, 256, 4, g.MXFP8, 0, 0)
+    assert call(W1=w1_plain) == g.ERR_INVALID_ARG                   # SwiGLU needs the interleave
+    assert call(act=g.SRELU) == g.ERR_INVALID_DIMS                  # SReLU W1 has N rows
+    w1_nv = g.QWeightC(FAKE, FAKE, None, 512, 256, 4, g.NVFP4, 1, 0)
+    w2_nv = g.QWeightC(FAKE, FAKE, None, 256, 256, 4, g.NVFP4, 0, 0)
+    rn = g.recipe(g.NVFP4)
+    assert call(W1=w1_nv, W2=w2_nv, rec=rn, wsb=1 << 30) == g.ERR_INVALID_ARG   # no global scales
+    assert L.gmlp_prepare_weights(FAKE, 4, 100, 256, 0, g.MXFP8, FAKE, FAKE, None, None, None) == g.ERR_INVALID_DIMS
+    assert L.gmlp_prepare_weights(FAKE, 4, 128, 128, 0, g.NVFP4, FAKE, FAKE, FAKE, FAKE, None) == g.ERR_INVALID_DIMS
+    assert L.gmlp_prepare_weights(FAKE, 4, 128, 256, 0, g.NVFP4, FAKE, FAKE, None, None, None) == g.ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from mxfp8_nvfp4_block_gb300 import gmlp
+    saved = gmlp._lib
+    gmlp._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="not found"):
+            gmlp.load(str(tmp_path / "missing.so"))
+    finally:
+        gmlp._lib = saved

@@ -1,0 +1,212 @@
+"""Parity of the fused grouped-MLP forward (CUDA path, through the C ABI) with
+the oracle.
+
+* Lossless operands (one-hot fc1 weights, small powers of two): the block-
+  scaled MMA, the scale layouts, the tile map over ragged groups and the fused
+  epilogues must reproduce the oracle's y bit for bit.
+* The workloads: >= 99.9% of fc2_x codes identical with the rest one code step
+  apart, and normalised Frobenius error of y <= 1e-2.
+* The NVFP4 epilogue's fused (pre, post)-RHT amax equals the standalone group
+  Hadamard-amax of the bf16 fc2_x it stored, bitwise.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mxfp8_nvfp4_block_gb300.inputs import WORKLOADS, bits, make_inputs
+from parity import code_match_report, frob, np_bits, np_u8
+
+pytestmark = pytest.mark.gpu
+
+CODE_MATCH = 0.999   # fraction of identical fc2_x codes
+Y_TOL = 1e-2         # normalised Frobenius error of y
+
+
+def bf16_cpu(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
+
+
+def run_gpu(gm, d, fmt, act, mask=0, probs=True):
+    w1 = gm.prepare_weights(d["W1"].cuda(), fmt, swiglu_interleave=(act == gm.SWIGLU))
+    w2 = gm.prepare_weights(d["W2"].cuda(), fmt)
+    M, N = d["x"].shape[0], d["W2"].shape[2]
+    G = d["splits"].numel()
+    cdiv = 1 if fmt == gm.MXFP8 else 2
+    aux = {"fc2x_codes": torch.zeros(M * N // cdiv + 16, dtype=torch.uint8, device="cuda"),
+           "fc2x_scales": torch.zeros(gm.tiled_scales_bytes(M, G, N // (32 if fmt == 0 else 16)) + 16,
+                                      dtype=torch.uint8, device="cuda")}
+    if fmt == gm.NVFP4:
+        aux["fc2x_bf16"] = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+        aux["fc2x_amax_pre"] = torch.zeros(G, dtype=torch.float32, device="cuda")
+        aux["fc2x_amax_post"] = torch.zeros(G, dtype=torch.float32, device="cuda")
+    rec = gm.recipe(fmt, use_rht=True, mask=mask)
+    p = d["probs"].cuda() if probs else None
+    y = torch.full((M, d["x"].shape[1]), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gm.forward(d["x"].cuda(), d["splits"].cuda(), w1, w2, p, act, rec, y=y, aux=aux)
+    gm.check_device_status()
+    torch.cuda.synchronize()
+    return y, aux
+
+
+def onehot_case(fmt, act, splits, K, N, seed):
+    rng = np.random.default_rng(seed)
+    G = len(splits)
+    M = int(sum(splits))
+    offs = np.concatenate([[0], np.cumsum(splits)])
+    n1 = 2 * N if act == 0 else N
+    if fmt == 0:
+        x = rng.choice([0.0, 1, 2, 4, -1, -2, -4], size=(M, K))
+        probs = rng.choice([0.5, 1.0], size=M).astype(np.float32)
+    else:
+        x = rng.choice([0.0, 2, 4, -2, -4], size=(M, K))
+        probs = np.ones(M, np.float32)
+        for g in range(G):
+            if splits[g]:
+                x[offs[g]] = 4.0
+    W1 = np.zeros((G, n1, K))
+    for g in range(G):
+        W1[g, np.arange(n1), rng.integers(0, K, n1)] = 1.0
+    if fmt == 0:
+        W2 = rng.choice([0.0, 1, 2, -1, -2, 4, -4], size=(G, K, N))
+    else:      # one-hot rows keep |y| <= 64 so the fc2 alpha product stays exact after bf16 rounding
+        W2 = np.zeros((G, K, N))
+        for g in range(G):
+            W2[g, np.arange(K), rng.integers(0, N, K)] = rng.choice([1.0, -2, 4], K)
+            W2[g, 0, :] = 0
+            W2[g, 0, 0] = 4.0
+    return dict(x=bf16_cpu(x), splits=torch.tensor(splits, dtype=torch.int64), W1=bf16_cpu(W1),
+                W2=bf16_cpu(W2), probs=torch.from_numpy(probs))
+
+
+@pytest.mark.parametrize("fmt,act", [(0, 1), (1, 1), (0, 0), (1, 0)],
+                         ids=["mxfp8-srelu", "nvfp4-srelu", "mxfp8-swiglu", "nvfp4-swiglu"])
+def test_forward_lossless_bitexact(orc, gm, fmt, act):
+    if act == 0:
+        splits, K, N = [130, 0, 257, 5, 128], 512, 256      # SwiGLU: fc1 width 512
+    else:
+        splits, K, N = [130, 0, 257, 5, 128], 512, 512
+    d = onehot_case(fmt, act, splits, K, N, seed=fmt * 10 + act)
+    y, aux = run_gpu(gm, d, fmt, act)
+    ref = orc.forward(bits(d["x"]), np.array(splits), bits(d["W1"]), bits(d["W2"]), d["probs"].numpy(), act, fmt)
+    M = sum(splits)
+    if act == 1:
+        # SReLU on these operands is lossless end to end: bit-exact fc2_x codes and y
+        cdiv = 1 if fmt == 0 else 2
+        assert np.array_equal(np_u8(aux["fc2x_codes"], M * N // cdiv).reshape(M, -1), ref["fc2x_codes"])
+        assert np.array_equal(np_bits(y), ref["y"])
+    else:
+        # SwiGLU: exact fc1 (one-hot), then silu in FP32 vs FP64
+        frac, steps = code_match_report(fmt, np_u8(aux["fc2x_codes"], M * N // (1 if fmt == 0 else 2)).reshape(M, -1),
+                                        ref["fc2x_codes"],
+                                        orc.tiled_to_compact(np_u8(aux["fc2x_scales"]), splits, N // (32 if fmt == 0 else 16)),
+                                        ref["fc2x_scales"],
+                                        g_S=None if fmt == 0 else np.repeat(
+                                            [orc.nvfp4_global_scale(a) for a in aux["fc2x_amax_pre"].cpu().numpy()], splits),
+                                        o_S=None if fmt == 0 else np.repeat(ref["fc2x_S"], splits))
+        assert frac >= CODE_MATCH and steps <= 1.0 + 1e-9, (frac, steps)
+        assert frob(y.float().cpu().numpy(), orc.bf16_to_f64(ref["y"])) <= Y_TOL
+
+
+def forward_parity(orc, gm, name, rows=None):
+    d = make_inputs(name)
+    w = d["workload"]
+    splits = d["splits"].numpy()
+    y, aux = run_gpu(gm, d, w.fmt, w.act, mask=d["mask"])
+    ref = orc.forward(bits(d["x"]), splits, bits(d["W1"]), bits(d["W2"]), d["probs"].numpy(), w.act, w.fmt,
+                      rows=rows, rht_mask=d["mask"])
+    sel = ref["rows"]
+    cdiv, blk = (1, 32) if w.fmt == 0 else (2, 16)
+    g_codes = np_u8(aux["fc2x_codes"], w.M * w.N // cdiv).reshape(w.M, -1)
+    g_scales = orc.tiled_to_compact(np_u8(aux["fc2x_scales"]), splits, w.N // blk)
+    gS = oS = None
+    if w.fmt == 1:
+        gpre = aux["fc2x_amax_pre"].cpu().numpy()
+        gS = np.repeat([orc.nvfp4_global_scale(a) for a in gpre], splits)
+        oS = np.repeat(ref["fc2x_S"], splits)
+    frac, steps = code_match_report(w.fmt, g_codes, ref["fc2x_codes"], g_scales, ref["fc2x_scales"], gS, oS, rows=sel)
+    err = frob(y.float().cpu().numpy()[sel], orc.bf16_to_f64(ref["y"])[sel])
+    print(f"{name}: code match {frac:.6f} (max {steps:.2f} steps), y error {err:.3e}")
+    assert frac >= CODE_MATCH, frac
+    assert steps <= 1.0 + 1e-9, steps
+    assert err <= Y_TOL, err
+    return d, y, aux, ref
+
+
+def test_forward_tiny(orc, gm):
+    forward_parity(orc, gm, "tiny")
+
+
+def test_forward_mx_swiglu_full(orc, gm):
+    forward_parity(orc, gm, "mx_swiglu")
+
+
+def test_forward_nv_srelu_full(orc, gm):
+    d, y, aux, ref = forward_parity(orc, gm, "nv_srelu")
+    # amax of fc2_x: the oracle's from its own fc2_x; relative agreement
+    np.testing.assert_allclose(aux["fc2x_amax_pre"].cpu().numpy(), ref["fc2x_amax_pre"], rtol=2e-2)
+    np.testing.assert_allclose(aux["fc2x_amax_post"].cpu().numpy(), ref["fc2x_amax_post"], rtol=2e-2)
+
+
+def test_forward_mx_skew_sampled(orc, gm):
+    """Zipf-skewed 64 experts at full size; the oracle evaluates a row sample that
+    covers every non-empty expert (MXFP8 rows are independent)."""
+    w = WORKLOADS["mx_skew"]
+    from mxfp8_nvfp4_block_gb300.inputs import make_splits
+    s = make_splits(w)
+    offs = np.concatenate([[0], np.cumsum(s)])
+    rng = np.random.default_rng(0)
+    rows = []
+    for g in range(w.G):
+        if s[g]:
+            rows += [offs[g], offs[g + 1] - 1]
+            rows += list(rng.integers(offs[g], offs[g + 1], min(8, s[g])))
+    rows = np.unique(np.array(rows, dtype=np.int64))
+    forward_parity(orc, gm, "mx_skew", rows=rows)
+
+
+def test_fused_amax_equals_standalone_hadamard_amax(orc, gm):
+    """The NVFP4 fc1 epilogue's (pre, post)-RHT amax of fc2_x is bit-identical to
+    the standalone group Hadamard-amax pass over the bf16 fc2_x it stored."""
+    d = make_inputs("tiny")
+    d["W1"] = d["W1"][:, :256].contiguous()      # SReLU: W1 [G, N, K]
+    _, aux = run_gpu(gm, d, 1, 1, mask=0x9C31)
+    pre, post = gm.group_hadamard_amax(aux["fc2x_bf16"], d["splits"].cuda(), 0x9C31)
+    assert torch.equal(pre, aux["fc2x_amax_pre"])
+    assert torch.equal(post, aux["fc2x_amax_post"])
+
+
+def test_sign_mask_changes_post_rht_amax(orc, gm):
+    """SReLU-shaped fc2_x (non-negative): the plain transform's amax exceeds the
+    sign-masked one (the pages saw up to ~17% for SReLU activations)."""
+    d = make_inputs("tiny")
+    d["W1"] = d["W1"][:, :256].contiguous()
+    _, aux = run_gpu(gm, d, 1, 1, mask=0x9C31)
+    pre0, post0 = gm.group_hadamard_amax(aux["fc2x_bf16"], d["splits"].cuda(), 0)
+    ratio = (post0 / aux["fc2x_amax_post"]).cpu().numpy()
+    print("plain / masked post-RHT amax:", ratio)
+    assert (ratio > 1.0).all()
+
+
+def test_forward_no_probs_and_empty_groups(orc, gm):
+    splits = [0, 300, 0, 0, 212]
+    rng = np.random.default_rng(5)
+    M, K, N, G = sum(splits), 256, 256, len(splits)
+    d = dict(x=bf16_cpu(rng.standard_normal((M, K))), splits=torch.tensor(splits),
+             W1=bf16_cpu(rng.standard_normal((G, 2 * N, K)) / 16), W2=bf16_cpu(rng.standard_normal((G, K, N)) / 16),
+             probs=torch.ones(M))
+    y, aux = run_gpu(gm, d, 0, 0, probs=False)
+    ref = orc.forward(bits(d["x"]), np.array(splits), bits(d["W1"]), bits(d["W2"]), None, 0, 0)
+    assert frob(y.float().cpu().numpy(), orc.bf16_to_f64(ref["y"])) <= Y_TOL
+
+
+def test_forward_rows_past_splits_untouched(gm):
+    """Rows past sum(split_sizes) (here M is larger) keep their contents."""
+    rng = np.random.default_rng(6)
+    splits = [100, 60]
+    M, K, N, G = 256, 256, 256, 2
+    d = dict(x=bf16_cpu(rng.standard_normal((M, K))), splits=torch.tensor(splits),
+             W1=bf16_cpu(rng.standard_normal((G, 2 * N, K)) / 16), W2=bf16_cpu(rng.standard_normal((G, K, N)) / 16),
+             probs=torch.rand(M))
+    y, _ = run_gpu(gm, d, 0, 0)
+    assert torch.isnan(y[160:].float()).all()
+    assert not torch.isnan(y[:160].float()).any()
