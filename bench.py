@@ -1,0 +1,401 @@
+"""Benchmark of the fused grouped-MLP forward (MXFP8 / NVFP4 block quantisation) on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gmlp|reference] [--workload NAME]
+
+One step = one gmlp_forward over the workload's synthetic batch: x quantise,
+fc1 grouped GEMM with the fused activation x prob and fc2_x requantisation,
+fc2 grouped GEMM (NVFP4 adds the x amax pass and the fc2_x cast).  Weights are
+quantised once before timing.  The default workload is the MXFP8 SwiGLU MoE
+layer with 8 experts, K=2048, N=1024 and 16384 tokens.
+
+Prints one JSON line (rank 0).  value = TFLOP/s of the GEMMs (2*M*K*N1 +
+2*M*N*K) over the device-timed steps, inputs resident in HBM, L2 flushed
+between steps.  e2e = the same metric through the C ABI with the step's x,
+probs and split sizes copied from pinned host memory and y copied back inside
+the timed region.  --impl reference times the oracle (the CPU restatement)
+on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mxfp8_nvfp4_block_gb300.inputs import WORKLOADS, bits, make_inputs  # noqa: E402
+
+METRIC = "fused grouped-MLP fwd TFLOPS (% FP8/FP4 peak); group-quantize GB/s (% HBM)"
+WORKLOAD_TEXT = {
+    "mx_swiglu": "MXFP8 SwiGLU grouped MLP: 8 experts, K=2048, N=1024 (W1_g [2N,K], W2_g [K,N]), 16384 tokens, "
+                 "Dirichlet(1) splits with one empty expert, seed 1",
+    "nv_srelu": "NVFP4+RHT SReLU grouped MLP: 8 experts, K=4096, N=2048, 32768 tokens uniform, 0.1% x outliers x50, "
+                "seed 2",
+    "mx_skew": "MXFP8 SwiGLU grouped MLP, Zipf(1.1) routing: 64 experts, K=7168, N=2048, 65536 tokens, seed 3",
+    "tiny": "MXFP8 SwiGLU grouped MLP: 4 experts, K=256, N=256, 512 tokens, seed 0",
+}
+NOMINAL_RATIO = {0: 2.0, 1: 6.0}   # dense FP8 / bf16 and FP4 / bf16 (4.5 and 13.5 vs 2.25 PFLOP/s)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples taken while the timed region runs."""
+
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines: list[tuple[float, str]] = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        t1 = getattr(self, "t1", time.time())
+        rows = [ln for ts, ln in self.lines if self.t0 - 0.05 <= ts <= t1 + 0.05]
+        if not rows:
+            rows = [ln for _, ln in self.lines[-3:]]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [c.strip() for c in r.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args, rank: int, world: int) -> dict:
+    from mxfp8_nvfp4_block_gb300 import gmlp
+    gmlp.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    name = args.workload
+    d = make_inputs(name)
+    w = d["workload"]
+    fmt, act = w.fmt, w.act
+    rec = gmlp.recipe(fmt, use_rht=True, mask=d["mask"])
+    stream = torch.cuda.current_stream()
+    x = d["x"].to(dev)
+    splits = d["splits"].to(dev)
+    probs = d["probs"].to(dev)
+    W1 = gmlp.prepare_weights(d["W1"].to(dev), fmt, swiglu_interleave=(act == gmlp.SWIGLU))
+    W2 = gmlp.prepare_weights(d["W2"].to(dev), fmt)
+    del d["W1"], d["W2"]
+    y = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(gmlp.forward_workspace_size(w.M, w.K, w.N, w.G, act, rec), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > 129 MB of L2
+    n_stage = 3 if fmt == gmlp.MXFP8 else 5
+    K_steps, W_steps = args.steps, args.warmup
+
+    def ev():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        return e
+
+    starts = [ev() for _ in range(K_steps)]
+    stages = [[ev() for _ in range(n_stage)] for _ in range(K_steps)]
+    torch.cuda.synchronize()
+
+    for _ in range(W_steps):
+        flush.zero_()
+        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws)
+    gmlp.check_device_status()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for i in range(K_steps):
+            flush.zero_()
+            starts[i].record(stream)
+            gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, events=stages[i])
+        torch.cuda.synchronize()
+        clk.mark_end()
+    if world > 1:
+        torch.distributed.barrier()
+    gmlp.check_device_status()
+    step_ms = [starts[i].elapsed_time(stages[i][-1]) for i in range(K_steps)]
+    bounds = [[starts[i]] + stages[i] for i in range(K_steps)]
+    stage_ms = [statistics.mean(b[j].elapsed_time(b[j + 1]) for b in bounds) for j in range(n_stage)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K_steps
+    value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers
+    x_h = d["x"].pin_memory()
+    p_h = d["probs"].pin_memory()
+    s_h = d["splits"].pin_memory()
+    y_h = torch.empty((w.M, w.K), dtype=torch.bfloat16).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for it in range(W_steps + K_steps):
+        if it == W_steps:
+            torch.cuda.synchronize()
+            e0.record()
+        x.copy_(x_h, non_blocking=True)
+        probs.copy_(p_h, non_blocking=True)
+        splits.copy_(s_h, non_blocking=True)
+        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws)
+        y_h.copy_(y, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    gmlp.check_device_status()
+    e2e_ms = e0.elapsed_time(e1) / K_steps
+    h2d = x_h.numel() * 2 + p_h.numel() * 4 + s_h.numel() * 8
+    d2h = y_h.numel() * 2
+
+    hbm, bf16_burst, _, src = peaks()
+    fc1_idx = 1 if fmt == gmlp.MXFP8 else 2
+    fc1_flops = 2.0 * w.M * w.K * w.n1
+    fc1_ms = stage_ms[fc1_idx]
+    peak = bf16_burst * NOMINAL_RATIO[fmt]
+    quant_idx = 0 if fmt == gmlp.MXFP8 else 1
+    cdiv, blk = (1, 32) if fmt == gmlp.MXFP8 else (2, 16)
+    q_bytes = w.M * w.K * 2 + w.M * w.K // cdiv + w.M * w.K // blk
+    achieved = fc1_flops / (fc1_ms * 1e-3) / 1e12
+    out = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K_steps,
+        "warmup": W_steps,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp8" if fmt == gmlp.MXFP8 else "nvfp4",
+        "data": "synthetic",
+        "config": {"workload": f"{name}: {WORKLOAD_TEXT.get(name, name)}",
+                   "l2": "flushed between timed steps (256 MiB write, outside the step events)",
+                   "weights": "quantised once before timing", "flops_per_step": w.flops},
+        "e2e": {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": K_steps * n_stage,
+        "stages_ms": [round(s, 5) for s in stage_ms],
+        "roofline": {"kernel": "fc1 grouped GEMM (gemm_kernel, fused activation + requant epilogue)",
+                     "bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4),
+                     "peak_source": f"{src} bf16 burst {bf16_burst} x nominal {'FP8' if fmt == 0 else 'FP4'}/bf16 "
+                                    f"ratio {NOMINAL_RATIO[fmt]}",
+                     "traffic": None},
+        "x_quantize": {"ms": round(stage_ms[quant_idx], 5), "bytes": q_bytes,
+                       "GB_s": round(q_bytes / (stage_ms[quant_idx] * 1e-3) / 1e9, 1),
+                       "frac_hbm": round(q_bytes / (stage_ms[quant_idx] * 1e-3) / 1e9 / hbm, 4)},
+        "clocks": clk.summary(),
+    }
+    if args.quant and rank == 0:
+        out["group_quantize"] = bench_quantizer(gmlp, dev, hbm)
+    return out
+
+
+def bench_quantizer(gmlp, dev, hbm) -> dict:
+    """Standalone NVFP4 group Hadamard-amax + quantize-with-amax (row + column,
+    RHT) on bf16 [131072, 4096], 8 groups (inputs 1 GiB, larger than L2)."""
+    d = make_inputs("nv_quant")
+    w = d["workload"]
+    x = d["x"].to(dev)
+    splits = d["splits"].to(dev)
+    sh = d["splits"].tolist()
+    rec = gmlp.recipe(gmlp.NVFP4, use_rht=True, mask=d["mask"])
+    reps = 10
+    for _ in range(2):
+        pre, post = gmlp.group_hadamard_amax(x, splits, d["mask"])
+    torch.cuda.synchronize()
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    e[0].record()
+    for _ in range(reps):
+        gmlp.group_hadamard_amax(x, splits, d["mask"])
+    e[1].record()
+    torch.cuda.synchronize()
+    t_amax = e[0].elapsed_time(e[1]) / reps
+    for _ in range(2):
+        out = gmlp.group_quantize_with_amax(x, splits, rec, pre, post, rowwise=True, columnwise=True, splits_host=sh)
+    torch.cuda.synchronize()
+    e[0].record()
+    for _ in range(reps):
+        out = gmlp.group_quantize_with_amax(x, splits, rec, pre, post, rowwise=True, columnwise=True, splits_host=sh)
+    e[1].record()
+    torch.cuda.synchronize()
+    gmlp.check_device_status()
+    t_cast = e[0].elapsed_time(e[1]) / reps
+    M, K = w.M, w.K
+    mpad = sum((m + 15) // 16 * 16 for m in sh)
+    rd = M * K * 2
+    wr = M * K // 2 + M * K // 16 + K * mpad // 2 + K * mpad // 16
+    del out, x
+    return {"workload": "nv_quant: NVFP4 group quantise, bf16 [131072, 4096], 8 groups Dirichlet(0.5), "
+                        "row + column (RHT)",
+            "hadamard_amax": {"ms": round(t_amax, 4), "bytes": rd, "GB_s": round(rd / t_amax / 1e6, 1),
+                              "frac_hbm": round(rd / t_amax / 1e6 / hbm, 4)},
+            "quantize_with_amax": {"ms": round(t_cast, 4), "bytes": rd + wr,
+                                   "GB_s": round((rd + wr) / t_cast / 1e6, 1),
+                                   "frac_hbm": round((rd + wr) / t_cast / 1e6 / hbm, 4)}}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(name: str, target_s: float = 10.0, max_reps: int = 3) -> dict:
+    """The oracle as it stands on the host cores, on the full workload (repeated
+    until about target_s of CPU work)."""
+    import oracle
+    d = make_inputs(name)
+    w = d["workload"]
+    xb, W1, W2 = bits(d["x"]), bits(d["W1"]), bits(d["W2"])
+    qw1, qw2 = oracle.quantize_weights(W1, w.fmt), oracle.quantize_weights(W2, w.fmt)
+    t0 = time.time()
+    reps = 0
+    while True:
+        oracle.forward(xb, d["splits"].numpy(), W1, W2, d["probs"].numpy(), w.act, w.fmt, qw1=qw1, qw2=qw2,
+                       rht_mask=d["mask"])
+        reps += 1
+        el = time.time() - t0
+        if el >= target_s or reps >= max_reps:
+            break
+    cores = len(os.sched_getaffinity(0))
+    return {"value": round(reps * w.flops / el / 1e12, 5), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} full forward(s) of {name} (all {w.M} tokens; weights pre-quantised), "
+                      f"{el:.1f} s, numpy float64 GEMMs + C format arithmetic"}
+
+
+def run_reference(args) -> dict:
+    """The reference arm: the oracle on the host, each step a bounded row
+    sample (MXFP8 rows are independent) of the same workload."""
+    import oracle
+    d = make_inputs(args.workload)
+    w = d["workload"]
+    xb, W1, W2 = bits(d["x"]), bits(d["W1"]), bits(d["W2"])
+    qw1, qw2 = oracle.quantize_weights(W1, w.fmt), oracle.quantize_weights(W2, w.fmt)
+    splits = d["splits"].numpy()
+    rng = np.random.default_rng(0)
+    frac = 1.0
+    rows = None
+    if w.fmt == 0:
+        # size the per-step row sample so the whole run stays near two minutes
+        probe = np.sort(rng.choice(w.M, max(64, w.M // 64), replace=False))
+        t0 = time.time()
+        oracle.forward(xb, splits, W1, W2, d["probs"].numpy(), w.act, w.fmt, rows=probe, qw1=qw1, qw2=qw2)
+        per_row = (time.time() - t0) / len(probe)
+        n = int(min(w.M // 8, max(64, 120.0 / (args.steps + args.warmup) / per_row)))
+        rows = np.sort(rng.choice(w.M, n, replace=False))
+        frac = n / w.M
+    flops = w.flops * frac
+
+    def step():
+        oracle.forward(xb, splits, W1, W2, d["probs"].numpy(), w.act, w.fmt, rows=rows, qw1=qw1, qw2=qw2,
+                       rht_mask=d["mask"])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.time()
+    for _ in range(args.steps):
+        step()
+    el = time.time() - t0
+    v = flops * args.steps / el / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"{len(rows)} random rows of the {w.M} tokens per step" if rows is not None
+              else f"all {w.M} tokens per step")
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload)}"},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gmlp", choices=["gmlp", "reference"])
+    ap.add_argument("--workload", default="mx_swiglu", choices=[k for k in WORKLOADS if k != "nv_quant"])
+    ap.add_argument("--no-quant", dest="quant", action="store_false", help="skip the standalone quantiser leg")
+    ap.add_argument("--no-cpu", dest="cpu", action="store_false", help="skip the oracle CPU-baseline leg")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a GPU for the gmlp arm")
+    out = run_gpu(args, rank, world)
+    if rank == 0:
+        if args.cpu:
+            out["cpu_baseline"] = oracle_sample(args.workload)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

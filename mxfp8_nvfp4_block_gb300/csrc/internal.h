@@ -6,7 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/gmlp.h"
+#include "gmlp.h"
 
 namespace gmlp {
 
