@@ -234,6 +234,30 @@ GMLP_API gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64
                          const gmlp_recipe* recipe, uint16_t* y, const gmlp_fwd_aux* aux,
                          void* workspace, size_t workspace_bytes, gmlp_stream stream);
 
+/* gmlp_forward_noalloc -- gmlp_forward without a caller workspace.  The
+ * pages have no counterpart: this is an addition for callers that cannot
+ * allocate device memory themselves -- for example code running inside a
+ * host framework that owns every device allocation through its own fixed
+ * pool, real-time loops that must not pay the implicit device synchronisation
+ * of cudaMalloc/cudaFree, or bindings that have no device allocator at all.
+ * The scratch is a static device array inside the library, 64 MiB, which
+ * every GPU that loads the library keeps reserved until the process exits;
+ * sizes whose gmlp_forward_workspace_size() exceeds it are rejected with
+ * GMLP_ERR_WORKSPACE before anything is launched.  The call allocates
+ * nothing: the caller still provides x, y, the weights and the aux outputs.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the one array and it keeps the previous call's contents
+ * (the forward zeroes what it accumulates into), so calls whose work overlaps
+ * on the GPU -- on different streams, or from different threads -- race; keep
+ * them ordered on one stream.  Arguments, limits and results are those of
+ * gmlp_forward. */
+GMLP_API gmlp_status gmlp_forward_noalloc(const uint16_t* x, int64_t M, int64_t K, int64_t N,
+                                          const int64_t* split_sizes, int32_t G, const gmlp_qweight* W1,
+                                          const gmlp_qweight* W2, const float* probs, int32_t act,
+                                          const gmlp_recipe* recipe, uint16_t* y, const gmlp_fwd_aux* aux,
+                                          gmlp_stream stream);
+
 /* Synchronises `stream`, then reads and clears the device status word the
  * kernels set on a bounded-wait timeout or inconsistent split sizes. */
 GMLP_API gmlp_status gmlp_check_device_status(gmlp_stream stream);

@@ -120,6 +120,9 @@ gmlp_status check_qtensor(const gmlp_qtensor* t, const char* what) {
 
 }  // namespace
 
+// Error text for entry points defined in other files of the library.
+gmlp_status set_last_error(gmlp_status st, const char* msg) { return fail(st, "%s", msg); }
+
 int num_sms() {
   static int cached[64] = {};
   int dev = 0;

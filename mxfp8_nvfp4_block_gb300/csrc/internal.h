@@ -99,4 +99,6 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 
 int num_sms();
 
+gmlp_status set_last_error(gmlp_status st, const char* msg);
+
 }  // namespace gmlp

@@ -23,7 +23,7 @@ COMPACT, GEMM_TILED = 0, 1
 
 EXPORTS = ["gmlp_tiled_scales_bytes", "gmlp_group_hadamard_amax", "gmlp_group_quantize_with_amax",
            "gmlp_group_quantize", "gmlp_prepare_weights", "gmlp_forward_workspace_size", "gmlp_forward",
-           "gmlp_check_device_status", "gmlp_last_error", "gmlp_version"]
+           "gmlp_check_device_status", "gmlp_last_error", "gmlp_version", "gmlp_forward_noalloc"]
 
 
 class Recipe(ctypes.Structure):
@@ -72,6 +72,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gmlp_forward": (_i32, [_vp, _i64, _i64, _i64, _vp, _i32, ctypes.POINTER(QWeightC),
                                 ctypes.POINTER(QWeightC), _vp, _i32, ctypes.POINTER(Recipe), _vp,
                                 ctypes.POINTER(FwdAux), _vp, ctypes.c_size_t, _vp]),
+        "gmlp_forward_noalloc": (_i32, [_vp, _i64, _i64, _i64, _vp, _i32, ctypes.POINTER(QWeightC),
+                                        ctypes.POINTER(QWeightC), _vp, _i32, ctypes.POINTER(Recipe), _vp,
+                                        ctypes.POINTER(FwdAux), _vp]),
         "gmlp_check_device_status": (_i32, [_vp]),
         "gmlp_last_error": (ctypes.c_char_p, []),
         "gmlp_version": (ctypes.c_char_p, []),
@@ -248,6 +251,21 @@ def forward(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *
     _check(load().gmlp_forward(_p(x), M, K, N, _p(splits), G, ctypes.byref(w1c), ctypes.byref(w2c), _p(probs),
                                act, ctypes.byref(rec), _p(y), ctypes.byref(aux_c) if aux_c else None,
                                _p(workspace), workspace.numel(), _stream(stream)))
+    return y
+
+
+def forward_noalloc(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *, y=None,
+                    stream=None) -> torch.Tensor:
+    """Same as :func:`forward`, but the library uses its own fixed static scratch
+    instead of a workspace (for callers that cannot allocate device memory)."""
+    x = _bits(x)
+    M, K = x.shape
+    G = splits.numel()
+    if y is None:
+        y = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    w1c, w2c = W1.c(), W2.c()
+    _check(load().gmlp_forward_noalloc(_p(x), M, K, W2.cols, _p(splits), G, ctypes.byref(w1c), ctypes.byref(w2c),
+                                       _p(probs), act, ctypes.byref(rec), _p(y), None, _stream(stream)))
     return y
 
 
