@@ -11,14 +11,14 @@
 // the sign mask enters the post-RHT amax; the accumulator is rounded through
 // the bf16 C type before the activation).
 //
-// Design (GB300, one CTA per SM, 320 threads):
+// Design (GB300, one CTA per SM, 576 threads):
 //   warp 0    TMA producer: A tile 128 x 128 B, B tile 256 x 128 B (128-byte
 //             swizzle) and the tile's scale blocks (bulk copies) per stage,
 //             4 stages, one mbarrier pair per stage;
 //   warp 1    TMEM owner and MMA issuer: per stage the scale blocks go to TMEM
 //             (tcgen05.cp 32x128b.warpx4), then 4 MMAs (M=128, N=256, K=32
 //             FP8 / K=64 FP4) accumulate into 256 TMEM columns;
-//   warps 2-9 epilogue: each drains its 32 lanes x 128 columns into
+//   warps 2-17 epilogue: each drains its 32 lanes x 64 columns into
 //             registers, frees the accumulator at once (so the next tile's
 //             mainloop overlaps the epilogue math), then computes and stores.
 // Tiles: (expert g, 128-row tile of g's tokens, 256-column output tile),
@@ -34,7 +34,8 @@ namespace gmlp {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreadsGemm = 320;
+constexpr int kThreadsGemm = 576;  // 2 control warps + 16 epilogue warps
+constexpr int kEpiWarps = 16;
 constexpr int kBM = 128, kBN = 256, kBKBytes = 128;
 constexpr int kATileBytes = kBM * kBKBytes;  // 16 KB
 constexpr int kBTileBytes = kBN * kBKBytes;  // 32 KB
@@ -89,17 +90,34 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
     if (globaltimer() - t0 > 500000000ull) return;
 }
 
+// 32-byte store (one full sector per lane); dst must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return bf16_bits(lo) | (bf16_bits(hi) << 16);
+}
+
+// Max |f| over n values as a balanced tree (short dependency chains).
+template <int n>
+__device__ __forceinline__ float tree_amax(const float* f) {
+  float m[n / 2];
+#pragma unroll
+  for (int i = 0; i < n / 2; ++i) m[i] = fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1]));
+#pragma unroll
+  for (int w = n / 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  return m[0];
 }
 
 // MXFP8 quantisation of 32 consecutive values f (bf16-exact FP32) into 8
 // code words; returns the scale exponent.
 __device__ __forceinline__ int mx_block(const float* f, uint32_t* words) {
-  float am = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(f[i]));
-  const int e = mxfp8_exponent(am);
+  const int e = mxfp8_exponent(tree_amax<32>(f));
   const float mul = exp2_neg(e);
 #pragma unroll
   for (int i = 0; i < 8; ++i)
@@ -108,15 +126,21 @@ __device__ __forceinline__ int mx_block(const float* f, uint32_t* words) {
   return e;
 }
 
+// silu(gate) * up in FP32 with the fast exponential and division (their
+// error is far below the bf16 rounding that follows).
 __device__ __forceinline__ float silu_times(float gate, float up) {
-  return gate / (1.0f + expf(-gate)) * up;
+  return __fdividef(gate, 1.0f + __expf(fminf(-gate, 80.0f))) * up;
 }
 
 // ------------------------------------------------------------------ epilogues
 
+// One epilogue thread owns one accumulator row (TMEM lane 32q + lane) and a
+// 64-column slice of the 256-column tile.
+constexpr int kSliceCols = 64;
+
 template <int FMT, int EPI>
 __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Tile& t, const int* off,
-                                         const int* tb, int q, int lane, int half) {
+                                         const int* tb, int q, int lane, int slice, float prob) {
   const int row = 32 * q + lane;
   const int m_g = off[t.g + 1] - off[t.g];
   const int lr = t.mt * kBM + row;
@@ -127,40 +151,35 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
 
   if (EPI == EPI_FC2) {
     if (!valid) return;
-    uint16_t* yrow = a.out_bf16 + grow * a.n_cols_out + (int64_t)t.nt * kBN + half * 128;
+    uint16_t* yrow = a.out_bf16 + grow * a.n_cols_out + (int64_t)t.nt * kBN + slice * kSliceCols;
 #pragma unroll
-    for (int j = 0; j < 128; j += 8) {
-      uint4 o;
-      o.x = pack_bf16x2(acc[j] * alpha, acc[j + 1] * alpha);
-      o.y = pack_bf16x2(acc[j + 2] * alpha, acc[j + 3] * alpha);
-      o.z = pack_bf16x2(acc[j + 4] * alpha, acc[j + 5] * alpha);
-      o.w = pack_bf16x2(acc[j + 6] * alpha, acc[j + 7] * alpha);
-      *reinterpret_cast<uint4*>(yrow + j) = o;
+    for (int j = 0; j < kSliceCols; j += 16) {
+      uint32_t o[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) o[k] = pack_bf16x2(acc[j + 2 * k] * alpha, acc[j + 2 * k + 1] * alpha);
+      st_global_v8(yrow + j, o);
     }
     return;
   }
 
-  const float prob = (valid && a.probs) ? a.probs[grow] : 1.0f;
-  constexpr int kOut = EPI == EPI_FC1_SWIGLU ? 64 : 128;  // fc2_x values this thread produces
+  constexpr int kOut = EPI == EPI_FC1_SWIGLU ? 32 : 64;  // fc2_x values this thread produces
   // fc2_x = bf16(act(bf16(acc * alpha)) * prob), in place in acc[0..kOut)
   if (EPI == EPI_FC1_SWIGLU) {
-    // 64-column chunks hold 32 gate then 32 up columns of the same 32 outputs
+    // a 64-column slice holds 32 gate then 32 up columns of the same 32 outputs
 #pragma unroll
-    for (int b = 0; b < 2; ++b)
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float hg = round_bf16(acc[64 * b + i] * alpha);
-        const float hu = round_bf16(acc[64 * b + 32 + i] * alpha);
-        acc[32 * b + i] = round_bf16(silu_times(hg, hu) * prob);
-      }
+    for (int i = 0; i < 32; ++i) {
+      const float hg = round_bf16(acc[i] * alpha);
+      const float hu = round_bf16(acc[32 + i] * alpha);
+      acc[i] = round_bf16(silu_times(hg, hu) * prob);
+    }
   } else {
 #pragma unroll
-    for (int i = 0; i < 128; ++i) {
+    for (int i = 0; i < 64; ++i) {
       const float h = fmaxf(round_bf16(acc[i] * alpha), 0.0f);
       acc[i] = round_bf16(h * h * prob);
     }
   }
-  const int64_t oc0 = (int64_t)t.nt * (kBN / (EPI == EPI_FC1_SWIGLU ? 2 : 1)) + half * kOut;
+  const int64_t oc0 = (int64_t)t.nt * (kBN / (EPI == EPI_FC1_SWIGLU ? 2 : 1)) + slice * kOut;
 
   if (FMT == GMLP_MXFP8) {
     constexpr int kBlocks = kOut / 32;
@@ -170,21 +189,17 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
       uint32_t words[8];
       const int e = mx_block(acc + 32 * b, words);
       sbytes |= uint32_t(e + 127) << (8 * b);
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out_codes + grow * a.n_cols_out + oc0 + 32 * b);
-        dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
-        dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
-      }
+      if (valid) st_global_v8(a.out_codes + grow * a.n_cols_out + oc0 + 32 * b, words);
     }
     if (valid) {
       const int nscale = (int)(a.n_cols_out / 32);
       const int kidx = (int)(oc0 / 32);
       const int64_t blk = (int64_t)(tb[t.g] + t.mt) * (nscale >> 2) + (kidx >> 2);
       uint8_t* dst = a.out_scales + blk * 512 + lane * 16 + q * 4 + (kidx & 3);
-      if (kBlocks == 2)
-        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)sbytes;
+      if (kBlocks == 1)
+        *dst = (uint8_t)sbytes;
       else
-        *reinterpret_cast<uint32_t*>(dst) = sbytes;
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)sbytes;
     }
   } else {
     // NVFP4: store bf16 fc2_x; per-group max |fc2_x| and post-RHT amax over
@@ -207,13 +222,11 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
     if (valid) {
       uint16_t* dst = a.out_bf16 + grow * a.n_cols_out + oc0;
 #pragma unroll
-      for (int j = 0; j < kOut; j += 8) {
-        uint4 o;
-        o.x = pack_bf16x2(acc[j], acc[j + 1]);
-        o.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
-        o.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
-        o.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
-        *reinterpret_cast<uint4*>(dst + j) = o;
+      for (int j = 0; j < kOut; j += 16) {
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] = pack_bf16x2(acc[j + 2 * k], acc[j + 2 * k + 1]);
+        st_global_v8(dst + j, o);
       }
     }
 #pragma unroll
@@ -312,7 +325,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 8);
+    mbar_init(tempty, kEpiWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -415,24 +428,30 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     tc_commit(drain);
     mbar_wait_drain(drain, 0);
   } else if (warp >= 2) {
-    // ---------------- epilogue
+    // ---------------- epilogue: 16 warps; warp w reads TMEM lanes 32 * (w % 4)
+    // and the 64-column slice (w - 2) / 4 of the accumulator
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int slice = (warp - 2) >> 2;
     uint32_t acc_phase = 0;
     for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
       const Tile t = decode_tile(off, ip, G, w);
+      float prob = 1.0f;
+      if (EPI != EPI_FC2 && a.probs) {
+        const int lr = t.mt * kBM + 32 * q + lane;
+        if (lr < off[t.g + 1] - off[t.g]) prob = __ldg(a.probs + off[t.g] + lr);
+      }
       if (!mbar_wait(tfull, acc_phase, abort_flag)) break;
       tc_fence_after();
-      float acc[128];
-      const uint32_t taddr = tbase + (uint32_t(32 * q) << 16) + uint32_t(half * 128);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tmem_ld32(taddr + 32 * j, acc + 32 * j);
+      float acc[kSliceCols];
+      const uint32_t taddr = tbase + (uint32_t(32 * q) << 16) + uint32_t(slice * kSliceCols);
+      tmem_ld32(taddr, acc);
+      tmem_ld32(taddr + 32, acc + 32);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty);
       acc_phase ^= 1;
-      epilogue<FMT, EPI>(a, acc, t, off, tb, q, lane, half);
+      epilogue<FMT, EPI>(a, acc, t, off, tb, q, lane, slice, prob);
     }
   }
   __syncthreads();
