@@ -203,7 +203,8 @@ typedef struct gmlp_fwd_aux {
   float* fc2x_amax_post;   /* out, NVFP4: [G] per-group post-RHT amax of fc2_x */
   gmlp_event* stage_events; /* recorded on `stream` after each kernel of the call */
   int32_t n_stage_events;   /* MXFP8: 3 (x quant, fc1, fc2); NVFP4: 5 (x amax, x quant, fc1, fc2_x quant, fc2) */
-  int32_t reserved;
+  int32_t gemm_mode;        /* 0: one CTA per 128 x 256 tile (default); 2: CTA pairs on 256 x 256 tiles
+                               (cta_group::2 MMA, each CTA loading half of the B tile) */
 } gmlp_fwd_aux;
 
 /* Workspace bytes gmlp_forward needs for these sizes (x and fc2_x codes and

@@ -353,6 +353,8 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
     return fail(GMLP_ERR_WORKSPACE, "workspace %zu bytes, need %zu (16-byte aligned)", workspace_bytes, L.total);
   if (aux && aux->n_stage_events > 0 && !aux->stage_events) return fail(GMLP_ERR_INVALID_ARG, "stage_events NULL");
+  if (aux && aux->gemm_mode != 0 && aux->gemm_mode != 2)
+    return fail(GMLP_ERR_INVALID_ARG, "gemm_mode %d is neither 0 nor 2", aux->gemm_mode);
   GMLP_TRY(check_device());
 
   cudaStream_t s = (cudaStream_t)stream;
@@ -401,6 +403,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     g1.out_codes = f_codes;
     g1.out_scales = f_scales;
     g1.n_cols_out = N;
+    g1.pair = (aux && aux->gemm_mode == 2) ? 2 : 1;
     GMLP_CUDA(launch_gemm(g1, s), "fc1 launch");
     GMLP_TRY(mark());
     GemmArgs g2{};
@@ -416,6 +419,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     g2.grp = gs;
     g2.out_bf16 = y;
     g2.n_cols_out = K;
+    g2.pair = (aux && aux->gemm_mode == 2) ? 2 : 1;
     GMLP_CUDA(launch_gemm(g2, s), "fc2 launch");
     GMLP_TRY(mark());
     return GMLP_OK;
@@ -465,6 +469,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   g1.amax_post = f_post;
   g1.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
   g1.n_cols_out = N;
+    g1.pair = (aux && aux->gemm_mode == 2) ? 2 : 1;
   GMLP_CUDA(launch_gemm(g1, s), "fc1 launch");
   GMLP_TRY(mark());
   {
@@ -496,6 +501,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   g2.b_S = W2->global_scale;
   g2.out_bf16 = y;
   g2.n_cols_out = K;
+    g2.pair = (aux && aux->gemm_mode == 2) ? 2 : 1;
   GMLP_CUDA(launch_gemm(g2, s), "fc2 launch");
   GMLP_TRY(mark());
   return GMLP_OK;

@@ -33,22 +33,30 @@ namespace gmlp {
 
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kThreadsGemm = 576;  // 2 control warps + 16 epilogue warps
 constexpr int kEpiWarps = 16;
 constexpr int kBM = 128, kBN = 256, kBKBytes = 128;
 constexpr int kATileBytes = kBM * kBKBytes;  // 16 KB
-constexpr int kBTileBytes = kBN * kBKBytes;  // 32 KB
 constexpr uint32_t kAccCols = 256;
 constexpr uint32_t kTmemCols = 512;
 
-template <int FMT>
-struct Fmt {
+// Per-format, per-shape constants.  PAIR = 1: one CTA computes a 128 x 256
+// tile with cta_group::1 MMAs.  PAIR = 2: a CTA pair (cluster of 2) computes a
+// 256 x 256 tile with cta_group::2 MMAs; each CTA loads its own 128 A rows and
+// one 128-row half of the B tile, so each SM takes in a third fewer bytes.
+template <int FMT, int PAIR>
+struct Cfg {
   // bytes of scale factors per 128 rows per stage: MXFP8 4 scales/row (one
   // 512-byte block), NVFP4 16 scales/row (four blocks)
   static constexpr int kSfBytes = FMT == GMLP_MXFP8 ? 512 : 2048;
-  static constexpr uint32_t kSfCols = FMT == GMLP_MXFP8 ? 16 : 64;  // TMEM columns per stage
-  static constexpr size_t kSmem = (size_t)kStages * (kATileBytes + kBTileBytes + 3 * kSfBytes);
+  static constexpr int kBRows = kBN / PAIR;                   // B rows held per CTA
+  static constexpr int kBTileBytes = kBRows * kBKBytes;
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes + 3 * kSfBytes;  // SFA + both SFB halves
+  static constexpr int kStages = PAIR == 1 ? 4 : (FMT == GMLP_MXFP8 ? 6 : 5);
+  static constexpr uint32_t kSfCols = FMT == GMLP_MXFP8 ? 16 : 48;  // TMEM columns per stage
+  static constexpr uint32_t kSfbOff = FMT == GMLP_MXFP8 ? 4 : 16;   // SFB after SFA within a stage
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes;
+  static constexpr int kTileRows = kBM * PAIR;
 };
 
 // Instruction descriptor (tcgen05 block-scaled kinds): A/B formats in bits
@@ -56,18 +64,19 @@ struct Fmt {
 // N >> 3 in bits 17..22, scale type in bit 23 (UE8M0 = 1, UE4M3 = 0),
 // M >> 4 in bits 24..28, scale-factor byte selectors in bits 4..5 (B) and
 // 29..30 (A).
-template <int FMT>
+template <int FMT, int MROWS>
 __device__ __forceinline__ uint32_t idesc_for(int k) {
   if (FMT == GMLP_MXFP8)
-    return (uint32_t(kBN >> 3) << 17) | (1u << 23) | (uint32_t(kBM >> 4) << 24) | (uint32_t(k) << 4) |
+    return (uint32_t(kBN >> 3) << 17) | (1u << 23) | (uint32_t(MROWS >> 4) << 24) | (uint32_t(k) << 4) |
            (uint32_t(k) << 29);
-  return (1u << 7) | (1u << 10) | (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+  return (1u << 7) | (1u << 10) | (uint32_t(kBN >> 3) << 17) | (uint32_t(MROWS >> 4) << 24);
 }
 
 struct Tile {
   int g, mt, nt;
 };
 
+template <int TILE_ROWS>
 __device__ __forceinline__ Tile decode_tile(const int* off, const int* ip, int G, int w) {
   int lo = 0, hi = G - 1;  // largest g with ip[g] <= w
   while (lo < hi) {
@@ -76,7 +85,7 @@ __device__ __forceinline__ Tile decode_tile(const int* off, const int* ip, int G
   }
   Tile t;
   t.g = lo;
-  const int mtiles = (off[lo + 1] - off[lo] + kBM - 1) / kBM;
+  const int mtiles = (off[lo + 1] - off[lo] + TILE_ROWS - 1) / TILE_ROWS;
   const int local = w - ip[lo];
   t.nt = local / mtiles;
   t.mt = local % mtiles;
@@ -140,10 +149,10 @@ constexpr int kSliceCols = 64;
 
 template <int FMT, int EPI>
 __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Tile& t, const int* off,
-                                         const int* tb, int q, int lane, int slice, float prob) {
+                                         const int* tb, int row_base, int q, int lane, int slice, float prob) {
   const int row = 32 * q + lane;
   const int m_g = off[t.g + 1] - off[t.g];
-  const int lr = t.mt * kBM + row;
+  const int lr = row_base + row;  // row within the group
   const bool valid = lr < m_g;
   const int64_t grow = (int64_t)off[t.g] + lr;
   float alpha = 1.0f;
@@ -194,7 +203,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
     if (valid) {
       const int nscale = (int)(a.n_cols_out / 32);
       const int kidx = (int)(oc0 / 32);
-      const int64_t blk = (int64_t)(tb[t.g] + t.mt) * (nscale >> 2) + (kidx >> 2);
+      const int64_t blk = (int64_t)(tb[t.g] + (lr >> 7)) * (nscale >> 2) + (kidx >> 2);
       uint8_t* dst = a.out_scales + blk * 512 + lane * 16 + q * 4 + (kidx & 3);
       if (kBlocks == 1)
         *dst = (uint8_t)sbytes;
@@ -241,22 +250,126 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
   }
 }
 
+
+// ------------------------------------------------------------------ CTA-pair helpers
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of the same shared-memory offset in CTA `rank`
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Tensor load into this CTA's shared memory that completes its bytes on the
+// pair leader's mbarrier (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tmap, int32_t x, int32_t y,
+                                                 uint32_t bar_cluster, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
+      : "memory");
+}
+
+template <int PAIR>
+__device__ __forceinline__ void tmem_alloc_g(uint32_t* slot) {
+  if (PAIR == 1) {
+    tmem_alloc(slot, kTmemCols);
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+}
+
+template <int PAIR>
+__device__ __forceinline__ void tmem_dealloc_g(uint32_t taddr) {
+  if (PAIR == 1)
+    tmem_dealloc(taddr, kTmemCols);
+  else
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kTmemCols) : "memory");
+}
+
+// Arrive on `bar` (same offset in both CTAs of a pair) when this thread's
+// tcgen05 operations complete.
+template <int PAIR>
+__device__ __forceinline__ void tc_commit_g(uint64_t* bar) {
+  if (PAIR == 1)
+    tc_commit(bar);
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
+template <int PAIR>
+__device__ __forceinline__ void tc_cp_g(uint32_t taddr, uint64_t sdesc) {
+  if (PAIR == 1)
+    tc_cp_32x128b_x4(taddr, sdesc);
+  else
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+template <int FMT, int PAIR>
+__device__ __forceinline__ void tc_mma_g(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                         uint32_t sfb, uint32_t accumulate) {
+  if (PAIR == 1) {
+    if (FMT == GMLP_MXFP8)
+      tc_mma_mxf8(d, adesc, bdesc, idesc, sfa, sfb, accumulate);
+    else
+      tc_mma_nvf4(d, adesc, bdesc, idesc, sfa, sfb, accumulate);
+  } else if (FMT == GMLP_MXFP8) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(
+            d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(
+            d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 
-template <int FMT, int EPI>
+template <int FMT, int EPI, int PAIR>
 __global__ void __launch_bounds__(kThreadsGemm, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const GemmArgs a) {
-  using F = Fmt<FMT>;
+  using C = Cfg<FMT, PAIR>;
+  constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = sA + kStages * kATileBytes;
-  uint8_t* sSFA = sB + kStages * kBTileBytes;
-  uint8_t* sSFB = sSFA + kStages * F::kSfBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + kStages * 2 * F::kSfBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
+  uint8_t* sB = sA + S * kATileBytes;
+  uint8_t* sSFA = sB + S * C::kBTileBytes;
+  uint8_t* sSFB = sSFA + S * C::kSfBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + S * 2 * C::kSfBytes);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -270,6 +383,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   const int G = a.grp.G;
   const int n_tiles = (int)(a.n_out / kBN);
   const int KB = (int)(a.kbytes / kBKBytes);
+  const uint32_t crank = PAIR == 2 ? cluster_ctarank() : 0;
+  const int rank = (int)(crank & 1);          // position in the pair
+  const uint32_t leader = crank & ~1u;        // cluster rank of the pair leader
+  const int unit = blockIdx.x / PAIR, n_units = gridDim.x / PAIR;
 
   if (warp == 0) {
     // group tables: row offsets, 128-row tile bases, tile-work prefix
@@ -285,7 +402,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           m = 0;
         }
       }
-      const long long v0 = m, v1 = (m + kBM - 1) / kBM, v2 = v1 * n_tiles;
+      const long long v0 = m, v1 = (m + kBM - 1) / kBM, v2 = (m + C::kTileRows - 1) / C::kTileRows * n_tiles;
       long long i0 = v0, i1 = v1, i2 = v2;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -316,67 +433,91 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       if (b && blockIdx.x == 0) report_device_error(GMLP_ERR_DEVICE_BOUNDS);
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
+      if (PAIR == 2) {
+        prefetch_tmap(&tmSFA);
+        prefetch_tmap(&tmSFB);
+      }
     }
   } else if (warp == 1) {
-    tmem_alloc(tslot, kTmemCols);
+    tmem_alloc_g<PAIR>(tslot);
   } else if (threadIdx.x == 64) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, kEpiWarps);
+    mbar_init(tempty, kEpiWarps * PAIR);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR == 2) cluster_sync();  // the peer's barriers exist before anyone signals them
   tc_fence_after();
   const uint32_t tbase = *tslot;
   const int total = *bad ? 0 : ip[G];
 
   if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer (both CTAs of a pair load their own halves)
     const uint64_t pol_a = policy_evict_normal();
     const uint64_t pol_b = policy_evict_last();
     int stage = 0;
     uint32_t phase = 0, armed = 0, armed_parity = 0;
-    constexpr uint32_t kTx = kATileBytes + kBTileBytes + 3 * F::kSfBytes;
-    for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
-      const Tile t = decode_tile(off, ip, G, w);
-      const int rowA = off[t.g] + t.mt * kBM;
-      const int64_t tileA = tb[t.g] + t.mt;
-      const int64_t rowB = (int64_t)t.g * a.n_out + (int64_t)t.nt * kBN;
-      const int64_t tileB = rowB / 128;
+    constexpr uint32_t kTx = (uint32_t)C::kStageBytes * PAIR;
+    constexpr int kSfRows = C::kSfBytes / 256;  // SF tensor-map rows per 128-row block
+    for (int w = unit; w < total && !*abort_flag; w += n_units) {
+      const Tile t = decode_tile<C::kTileRows>(off, ip, G, w);
+      const int row0 = t.mt * C::kTileRows + kBM * rank;  // first row of this CTA within the group
+      const int rowA = off[t.g] + row0;
+      const int64_t tileA = tb[t.g] + (row0 >> 7);
+      const int64_t rowB0 = (int64_t)t.g * a.n_out + (int64_t)t.nt * kBN;
+      const int64_t tileB = rowB0 / 128;
+      const int32_t rowB = (int32_t)(rowB0 + rank * C::kBRows);
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&full[stage], kTx);
-        armed |= 1u << stage;
-        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-        tma_load_2d(sA + stage * kATileBytes, &tmA, kb * kBKBytes, rowA, &full[stage], pol_a);
-        tma_load_2d(sB + stage * kBTileBytes, &tmB, kb * kBKBytes, (int32_t)rowB, &full[stage], pol_b);
-        bulk_load(sSFA + stage * F::kSfBytes, a.a_scales + (tileA * KB + kb) * F::kSfBytes, F::kSfBytes,
-                  &full[stage]);
-        uint8_t* sfb = sSFB + stage * 2 * F::kSfBytes;
-        bulk_load(sfb, a.b_scales + (tileB * KB + kb) * F::kSfBytes, F::kSfBytes, &full[stage]);
-        bulk_load(sfb + F::kSfBytes, a.b_scales + ((tileB + 1) * KB + kb) * F::kSfBytes, F::kSfBytes,
-                  &full[stage]);
-        if (++stage == kStages) {
+        uint8_t* sfb = sSFB + stage * 2 * C::kSfBytes;
+        if (PAIR == 1) {
+          mbar_arrive_expect_tx(&full[stage], kTx);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          tma_load_2d(sA + stage * kATileBytes, &tmA, kb * kBKBytes, rowA, &full[stage], pol_a);
+          tma_load_2d(sB + stage * C::kBTileBytes, &tmB, kb * kBKBytes, rowB, &full[stage], pol_b);
+          bulk_load(sSFA + stage * C::kSfBytes, a.a_scales + (tileA * KB + kb) * C::kSfBytes, C::kSfBytes,
+                    &full[stage]);
+          bulk_load(sfb, a.b_scales + (tileB * KB + kb) * C::kSfBytes, C::kSfBytes, &full[stage]);
+          bulk_load(sfb + C::kSfBytes, a.b_scales + ((tileB + 1) * KB + kb) * C::kSfBytes, C::kSfBytes,
+                    &full[stage]);
+        } else {
+          const uint32_t bar = mapa_shared(smem_u32(&full[stage]), leader);
+          if (rank == 0) {
+            mbar_arrive_expect_tx(&full[stage], kTx);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          }
+          tma_load_2d_pair(sA + stage * kATileBytes, &tmA, kb * kBKBytes, rowA, bar, pol_a);
+          tma_load_2d_pair(sB + stage * C::kBTileBytes, &tmB, kb * kBKBytes, rowB, bar, pol_b);
+          tma_load_2d_pair(sSFA + stage * C::kSfBytes, &tmSFA, 0, (int32_t)((tileA * KB + kb) * kSfRows), bar,
+                           pol_a);
+          tma_load_2d_pair(sfb, &tmSFB, 0, (int32_t)((tileB * KB + kb) * kSfRows), bar, pol_b);
+          tma_load_2d_pair(sfb + C::kSfBytes, &tmSFB, 0, (int32_t)(((tileB + 1) * KB + kb) * kSfRows), bar,
+                           pol_b);
+        }
+        if (++stage == S) {
           stage = 0;
           phase ^= 1;
         }
       }
     }
-    // every copy this thread started must land before the CTA exits
-    for (int s = 0; s < kStages; ++s)
+    // every copy signalled on this CTA's barriers must land before it exits
+    for (int s = 0; s < S; ++s)
       if (armed & (1u << s)) mbar_wait_drain(&full[s], (armed_parity >> s) & 1u);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------- MMA issuer (the pair leader issues for both CTAs)
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
     const uint32_t sf_base = tbase + kAccCols;
-    for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+    for (int w = unit; w < total && !*abort_flag; w += n_units) {
       if (!mbar_wait(tempty, acc_phase ^ 1, abort_flag)) break;
       tc_fence_after();
       bool ok = true;
@@ -386,22 +527,22 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t sfa_t = sf_base + stage * F::kSfCols;
-        const uint32_t sfb_t = sfa_t + (FMT == GMLP_MXFP8 ? 4 : 16);
+        const uint32_t sfa_t = sf_base + stage * C::kSfCols;
+        const uint32_t sfb_t = sfa_t + C::kSfbOff;
         const uint32_t sA_addr = smem_u32(sA + stage * kATileBytes);
-        const uint32_t sB_addr = smem_u32(sB + stage * kBTileBytes);
-        const uint32_t sfa_addr = smem_u32(sSFA + stage * F::kSfBytes);
-        const uint32_t sfb_addr = smem_u32(sSFB + stage * 2 * F::kSfBytes);
+        const uint32_t sB_addr = smem_u32(sB + stage * C::kBTileBytes);
+        const uint32_t sfa_addr = smem_u32(sSFA + stage * C::kSfBytes);
+        const uint32_t sfb_addr = smem_u32(sSFB + stage * 2 * C::kSfBytes);
         if (FMT == GMLP_MXFP8) {
-          tc_cp_32x128b_x4(sfa_t, smem_desc(sfa_addr, 0, 128, 0));
-          tc_cp_32x128b_x4(sfb_t, smem_desc(sfb_addr, 0, 128, 0));
-          tc_cp_32x128b_x4(sfb_t + 4, smem_desc(sfb_addr + 512, 0, 128, 0));
+          tc_cp_g<PAIR>(sfa_t, smem_desc(sfa_addr, 0, 128, 0));
+          tc_cp_g<PAIR>(sfb_t, smem_desc(sfb_addr, 0, 128, 0));
+          tc_cp_g<PAIR>(sfb_t + 4, smem_desc(sfb_addr + 512, 0, 128, 0));
         } else {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            tc_cp_32x128b_x4(sfa_t + 4 * k, smem_desc(sfa_addr + 512 * k, 0, 128, 0));
-            tc_cp_32x128b_x4(sfb_t + 8 * k, smem_desc(sfb_addr + 512 * k, 0, 128, 0));
-            tc_cp_32x128b_x4(sfb_t + 8 * k + 4, smem_desc(sfb_addr + 2048 + 512 * k, 0, 128, 0));
+            tc_cp_g<PAIR>(sfa_t + 4 * k, smem_desc(sfa_addr + 512 * k, 0, 128, 0));
+            tc_cp_g<PAIR>(sfb_t + 8 * k, smem_desc(sfb_addr + 512 * k, 0, 128, 0));
+            tc_cp_g<PAIR>(sfb_t + 8 * k + 4, smem_desc(sfb_addr + 2048 + 512 * k, 0, 128, 0));
           }
         }
 #pragma unroll
@@ -410,34 +551,37 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           const uint64_t bd = smem_desc(sB_addr + 32 * k, 16, 1024, 2);
           const uint32_t accumulate = (kb > 0 || k > 0) ? 1u : 0u;
           if (FMT == GMLP_MXFP8)
-            tc_mma_mxf8(tbase, ad, bd, idesc_for<FMT>(k), sfa_t, sfb_t, accumulate);
+            tc_mma_g<FMT, PAIR>(tbase, ad, bd, idesc_for<FMT, kBM * PAIR>(k), sfa_t, sfb_t, accumulate);
           else
-            tc_mma_nvf4(tbase, ad, bd, idesc_for<FMT>(k), sfa_t + 4 * k, sfb_t + 8 * k, accumulate);
+            tc_mma_g<FMT, PAIR>(tbase, ad, bd, idesc_for<FMT, kBM * PAIR>(k), sfa_t + 4 * k, sfb_t + 8 * k,
+                                accumulate);
         }
-        tc_commit(&empty[stage]);
-        if (++stage == kStages) {
+        tc_commit_g<PAIR>(&empty[stage]);
+        if (++stage == S) {
           stage = 0;
           phase ^= 1;
         }
       }
       if (!ok) break;
-      tc_commit(tfull);
+      tc_commit_g<PAIR>(tfull);
       acc_phase ^= 1;
     }
     // all MMAs and copies this thread issued complete before TMEM is freed
-    tc_commit(drain);
+    tc_commit_g<PAIR>(drain);
     mbar_wait_drain(drain, 0);
   } else if (warp >= 2) {
     // ---------------- epilogue: 16 warps; warp w reads TMEM lanes 32 * (w % 4)
-    // and the 64-column slice (w - 2) / 4 of the accumulator
+    // and the 64-column slice (w - 2) / 4 of this CTA's 128 accumulator rows
     const int q = warp & 3;
     const int slice = (warp - 2) >> 2;
+    const uint32_t tempty_addr = PAIR == 2 ? mapa_shared(smem_u32(tempty), leader) : 0;
     uint32_t acc_phase = 0;
-    for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
-      const Tile t = decode_tile(off, ip, G, w);
+    for (int w = unit; w < total && !*abort_flag; w += n_units) {
+      const Tile t = decode_tile<C::kTileRows>(off, ip, G, w);
+      const int row_base = t.mt * C::kTileRows + kBM * rank;
       float prob = 1.0f;
       if (EPI != EPI_FC2 && a.probs) {
-        const int lr = t.mt * kBM + 32 * q + lane;
+        const int lr = row_base + 32 * q + lane;
         if (lr < off[t.g + 1] - off[t.g]) prob = __ldg(a.probs + off[t.g] + lr);
       }
       if (!mbar_wait(tfull, acc_phase, abort_flag)) break;
@@ -449,15 +593,21 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
+      if (lane == 0) {
+        if (PAIR == 1)
+          mbar_arrive(tempty);
+        else
+          mbar_arrive_cluster(tempty_addr);
+      }
       acc_phase ^= 1;
-      epilogue<FMT, EPI>(a, acc, t, off, tb, q, lane, slice, prob);
+      epilogue<FMT, EPI>(a, acc, t, off, tb, row_base, q, lane, slice, prob);
     }
   }
   __syncthreads();
+  if (PAIR == 2) cluster_sync();  // neither CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tbase, kTmemCols);
+    tmem_dealloc_g<PAIR>(tbase);
   }
 }
 
@@ -476,57 +626,93 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D uint8 tensor map over [rows][row_bytes] with a box of box_rows x 128
-// bytes and the 128-byte swizzle the MMA descriptors assume.
-bool make_tmap(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows, int box_rows) {
+// 2D uint8 tensor map over [rows][row_bytes] with a box of box_rows x box_bytes.
+bool make_tmap(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows, int box_bytes, int box_rows,
+               CUtensorMapSwizzle swz) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  cuuint32_t box[2] = {(cuuint32_t)kBKBytes, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int FMT, int EPI>
+template <int FMT, int EPI, int PAIR>
 cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
-  const size_t smem = Fmt<FMT>::kSmem + 1024 + 256 + 3 * (kMaxGroups + 1) * sizeof(int);
+  using C = Cfg<FMT, PAIR>;
+  const size_t smem = C::kSmem + 1024 + 256 + 3 * (kMaxGroups + 1) * sizeof(int);
+  auto kern = gemm_kernel<FMT, EPI, PAIR>;
   static bool attr_set[64] = {};
+  static int max_units[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreadsGemm);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR == 2 ? 1 : 0;
   if (!attr_set[dev & 63]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    int units = num_sms() / PAIR;
+    if (PAIR == 2) {
+      cfg.gridDim = dim3(2 * units);
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (clusters < 1) return cudaErrorInvalidConfiguration;
+      if (clusters < units) units = clusters;
+    }
+    max_units[dev & 63] = units;
     attr_set[dev & 63] = true;
   }
-  CUtensorMap ta, tbm;
-  if (!make_tmap(&ta, a.a_codes, a.kbytes, a.M, kBM)) return cudaErrorInvalidValue;
-  if (!make_tmap(&tbm, a.b_codes, a.kbytes, (int64_t)a.grp.G * a.n_out, kBN)) return cudaErrorInvalidValue;
-  const int64_t max_tiles = ((a.M + kBM - 1) / kBM + a.grp.G) * (a.n_out / kBN);
-  int grid = num_sms();
-  if (max_tiles < grid) grid = (int)max_tiles;
-  if (grid < 1) grid = 1;
-  gemm_kernel<FMT, EPI><<<grid, kThreadsGemm, smem, s>>>(ta, tbm, a);
-  return cudaGetLastError();
+  const int nscale = (int)(FMT == GMLP_MXFP8 ? a.kbytes / 32 : a.kbytes / 8);
+  const int64_t sfa_bytes = ((a.M + 127) / 128 + a.grp.G) * 128LL * nscale;
+  const int64_t sfb_bytes = (int64_t)a.grp.G * a.n_out * nscale;
+  CUtensorMap ta, tbm, tsa, tsb;
+  if (!make_tmap(&ta, a.a_codes, a.kbytes, a.M, kBKBytes, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tbm, a.b_codes, a.kbytes, (int64_t)a.grp.G * a.n_out, kBKBytes, C::kBRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tsa, a.a_scales, 256, sfa_bytes / 256, 256, C::kSfBytes / 256, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_tmap(&tsb, a.b_scales, 256, sfb_bytes / 256, 256, C::kSfBytes / 256, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  const int64_t max_tiles = ((a.M + C::kTileRows - 1) / C::kTileRows + a.grp.G) * (a.n_out / kBN);
+  int64_t units = max_units[dev & 63];
+  if (max_tiles < units) units = max_tiles;
+  if (units < 1) units = 1;
+  cfg.gridDim = dim3((unsigned)(units * PAIR));
+  return cudaLaunchKernelEx(&cfg, kern, ta, tbm, tsa, tsb, a);
 }
 
 }  // namespace
 
 int gemm_read_clear_status() { return read_clear_status(); }
 
+// Single-CTA tiles unless the caller asks for CTA pairs.
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.M == 0) return cudaSuccess;
+  const bool pair = a.pair == 2;
+#define GMLP_LAUNCH(F, E) \
+  return pair ? launch_t<F, E, 2>(a, s) : launch_t<F, E, 1>(a, s)
   if (a.format == GMLP_MXFP8) {
-    if (a.epi == EPI_FC1_SWIGLU) return launch_t<GMLP_MXFP8, EPI_FC1_SWIGLU>(a, s);
-    if (a.epi == EPI_FC1_SRELU) return launch_t<GMLP_MXFP8, EPI_FC1_SRELU>(a, s);
-    return launch_t<GMLP_MXFP8, EPI_FC2>(a, s);
+    if (a.epi == EPI_FC1_SWIGLU) GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_SWIGLU);
+    if (a.epi == EPI_FC1_SRELU) GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_SRELU);
+    GMLP_LAUNCH(GMLP_MXFP8, EPI_FC2);
   }
-  if (a.epi == EPI_FC1_SWIGLU) return launch_t<GMLP_NVFP4, EPI_FC1_SWIGLU>(a, s);
-  if (a.epi == EPI_FC1_SRELU) return launch_t<GMLP_NVFP4, EPI_FC1_SRELU>(a, s);
-  return launch_t<GMLP_NVFP4, EPI_FC2>(a, s);
+  if (a.epi == EPI_FC1_SWIGLU) GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SWIGLU);
+  if (a.epi == EPI_FC1_SRELU) GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SRELU);
+  GMLP_LAUNCH(GMLP_NVFP4, EPI_FC2);
+#undef GMLP_LAUNCH
 }
 
 }  // namespace gmlp

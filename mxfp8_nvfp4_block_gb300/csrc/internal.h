@@ -94,6 +94,7 @@ struct GemmArgs {
   float* amax_post;
   uint32_t rht_mask;
   int64_t n_cols_out;      // row length of the output (fc1: N; fc2: K)
+  int pair;                // 2: CTA pairs (cta_group::2); otherwise single-CTA tiles
 };
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 

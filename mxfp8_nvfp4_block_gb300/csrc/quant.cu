@@ -21,7 +21,7 @@ constexpr int kWarps = kThreads / 32;
 struct SmemGroups {
   int off[kMaxGroups + 1];  // first row of each group
   int tb[kMaxGroups + 1];   // first 128-row tile of each group (GEMM_TILED scales)
-  int up[kMaxGroups + 1];   // first work unit (16-row chunk x 256-column slab)
+  int up[kMaxGroups + 1];   // first work unit (unit_rows-row block x 256-column slab)
   int mp[kMaxGroups + 1];   // prefix of the 16-row padded group sizes
   int bad;
 };
@@ -29,7 +29,7 @@ struct SmemGroups {
 // Warp 0 scans the G split sizes (32 at a time); everything is validated
 // against M.  Negative sizes or a total above M set GMLP_ERR_DEVICE_BOUNDS and
 // t.bad, and the kernel does nothing.
-__device__ void build_group_tables(const GroupSrc& gs, int slabs, SmemGroups& t) {
+__device__ void build_group_tables(const GroupSrc& gs, int slabs, SmemGroups& t, int unit_rows = 16) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     long long c0 = 0, c1 = 0, c2 = 0, c3 = 0;
@@ -45,7 +45,7 @@ __device__ void build_group_tables(const GroupSrc& gs, int slabs, SmemGroups& t)
         }
       }
       const long long ch = (m + 15) >> 4;
-      long long v0 = m, v1 = (m + 127) >> 7, v2 = ch * slabs, v3 = ch * 16;
+      long long v0 = m, v1 = (m + 127) >> 7, v2 = (m + unit_rows - 1) / unit_rows * slabs, v3 = ch * 16;
       long long i0 = v0, i1 = v1, i2 = v2, i3 = v3;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -204,10 +204,16 @@ __global__ void __launch_bounds__(kThreads) row_quant_kernel(RowQuantArgs a) {
                         (e4m3x2(__fmul_rn(f[2], mul), __fmul_rn(f[3], mul)) << 16);
           uint32_t w1 = e4m3x2(__fmul_rn(f[4], mul), __fmul_rn(f[5], mul)) |
                         (e4m3x2(__fmul_rn(f[6], mul), __fmul_rn(f[7], mul)) << 16);
+          // scale bytes of 4 consecutive blocks (lanes 0,4,8,12 and 16,..,28) go out as one word
+          const uint32_t sb = (uint32_t)(e + 127);
+          const int lb = lane & 16;
+          const uint32_t word = __shfl_sync(0xffffffffu, sb, lb) | (__shfl_sync(0xffffffffu, sb, lb + 4) << 8) |
+                                (__shfl_sync(0xffffffffu, sb, lb + 8) << 16) |
+                                (__shfl_sync(0xffffffffu, sb, lb + 12) << 24);
           if (c < nch) {
             *reinterpret_cast<uint2*>(a.codes + r * K + (int64_t)c * 8) = make_uint2(w0, w1);
-            if ((lane & 3) == 0)
-              a.scales[scale_offset(a.tiled, t, g, r, c >> 2, nscale)] = (uint8_t)(e + 127);
+            if ((lane & 15) == 0)
+              *reinterpret_cast<uint32_t*>(a.scales + scale_offset(a.tiled, t, g, r, c >> 2, nscale)) = word;
           }
         } else {
           am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
@@ -217,9 +223,15 @@ __global__ void __launch_bounds__(kThreads) row_quant_kernel(RowQuantArgs a) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             word |= e2m1x2(__fmul_rn(f[2 * i], enc), __fmul_rn(f[2 * i + 1], enc)) << (8 * i);
+          // scale bytes of 4 consecutive blocks (lanes 8k, 8k+2, 8k+4, 8k+6) go out as one word
+          const int lb = lane & 24;
+          const uint32_t sw = __shfl_sync(0xffffffffu, sf, lb) | (__shfl_sync(0xffffffffu, sf, lb + 2) << 8) |
+                              (__shfl_sync(0xffffffffu, sf, lb + 4) << 16) |
+                              (__shfl_sync(0xffffffffu, sf, lb + 6) << 24);
           if (c < nch) {
             *reinterpret_cast<uint32_t*>(a.codes + r * (K / 2) + (int64_t)c * 4) = word;
-            if ((lane & 1) == 0) a.scales[scale_offset(a.tiled, t, g, r, c >> 1, nscale)] = (uint8_t)sf;
+            if ((lane & 7) == 0)
+              *reinterpret_cast<uint32_t*>(a.scales + scale_offset(a.tiled, t, g, r, c >> 1, nscale)) = sw;
           }
         }
       }
@@ -387,34 +399,57 @@ __global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const uint16_t*
 
 // ------------------------------------------------------------------ row + column NVFP4 cast
 
+// Tiles of 128 rows x 256 columns of one group, staged in shared memory.
+constexpr int kTileR = 128, kTileC = 256;
+constexpr size_t kColSmem = (size_t)kTileR * kTileC * 2 + kTileC * 64 + kTileC * 8;
+
 __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
   __shared__ SmemGroups t;
+  extern __shared__ uint4 dyn_smem[];
+  uint16_t* tile = reinterpret_cast<uint16_t*>(dyn_smem);             // [128][256] bf16
+  uint8_t* ccode = reinterpret_cast<uint8_t*>(tile + kTileR * kTileC);  // [256 columns][8 chunks x 8 B]
+  uint8_t* cscale = ccode + kTileC * 64;                                // [256 columns][8 chunks]
   const int64_t K = a.K;
-  const int slabs = (int)((K + 255) / 256);
-  build_group_tables(a.grp, slabs, t);
+  const int slabs = (int)((K + kTileC - 1) / kTileC);
+  build_group_tables(a.grp, slabs, t, kTileR);
   if (t.bad) return;
   const int G = a.grp.G;
-  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nscale_row = (int)(K / 16);
-  const int64_t units = t.up[G];
-  const int64_t warps = (int64_t)gridDim.x * kWarps;
-  const int64_t w = (int64_t)blockIdx.x * kWarps + threadIdx.x / 32;
-  const int64_t upw = (units + warps - 1) / warps;
-  const int64_t u0 = w * upw, u1 = min(units, u0 + upw);
-  if (u0 >= u1) return;
-  int g = find_unit_group(t, G, u0);
-  for (int64_t u = u0; u < u1; ++u) {
-    while (t.up[g + 1] <= u) ++g;
-    const Unit un = decode_unit(t, g, u, K, lane);
-    uint4 v[16];
-    load_unit(a.x, K, un, v);
+  for (int64_t u = blockIdx.x; u < t.up[G]; u += gridDim.x) {
+    const int g = find_unit_group(t, G, u);
+    const int m = t.off[g + 1] - t.off[g];
+    const int ntile = (m + kTileR - 1) / kTileR;
+    const int local = (int)(u - t.up[g]);
+    const int slab = local / ntile, b = local % ntile;
+    const int64_t row0 = (int64_t)t.off[g] + (int64_t)b * kTileR;
+    const int nvalid = min(kTileR, m - b * kTileR);
+    const int64_t col0 = (int64_t)slab * kTileC;
+    const int ncols = (int)min((int64_t)kTileC, K - col0);
+
+    // phase 1: the tile into shared memory (rows past the group end as zeros)
+    __syncthreads();
+    {
+      uint4 v[16];
+#pragma unroll
+      for (int it = 0; it < 16; ++it) {
+        const int r = it * 8 + (tid >> 5), c8 = (tid & 31) * 8;
+        v[it] = (r < nvalid && c8 < ncols) ? ld_stream(a.x + (row0 + r) * K + col0 + c8) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int it = 0; it < 16; ++it) {
+        const int r = it * 8 + (tid >> 5), c8 = (tid & 31) * 8;
+        *reinterpret_cast<uint4*>(tile + r * kTileC + c8) = v[it];
+      }
+    }
+    __syncthreads();
+
+    // phase 2: rowwise NVFP4 (16 consecutive columns per block), one warp per row
     if (a.row_codes) {
       const float S = nvfp4_global_scale(a.amax_row[g]);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (i >= un.nvalid) break;
+      for (int r = warp; r < nvalid; r += kWarps) {
         float f[8];
-        unpack8(v[i], f);
+        unpack8(*reinterpret_cast<const uint4*>(tile + r * kTileC + lane * 8), f);
         float am = 0.0f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) am = fmaxf(am, fabsf(f[k]));
@@ -425,22 +460,30 @@ __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           word |= e2m1x2(__fmul_rn(f[2 * k], enc), __fmul_rn(f[2 * k + 1], enc)) << (8 * k);
-        if (un.active) {
-          const int64_t r = un.row0 + i;
-          *reinterpret_cast<uint32_t*>(a.row_codes + r * (K / 2) + un.col0 / 2) = word;
-          if ((lane & 1) == 0)
-            a.row_scales[scale_offset(a.row_tiled, t, g, r, (int)(un.col0 >> 4), nscale_row)] = (uint8_t)sf;
+        const int lb = lane & 24;
+        const uint32_t sw = __shfl_sync(0xffffffffu, sf, lb) | (__shfl_sync(0xffffffffu, sf, lb + 2) << 8) |
+                            (__shfl_sync(0xffffffffu, sf, lb + 4) << 16) | (__shfl_sync(0xffffffffu, sf, lb + 6) << 24);
+        if (lane * 8 < ncols) {
+          const int64_t rg = row0 + r;
+          *reinterpret_cast<uint32_t*>(a.row_codes + rg * (K / 2) + (col0 + lane * 8) / 2) = word;
+          if ((lane & 7) == 0)
+            *reinterpret_cast<uint32_t*>(a.row_scales + scale_offset(a.row_tiled, t, g, rg,
+                                                                     (int)((col0 + lane * 8) >> 4), nscale_row)) = sw;
         }
       }
     }
-    if (a.col_codes && un.active) {
+
+    // phase 3: columnwise NVFP4 (16 consecutive rows per block, RHT first), one
+    // thread per column, results staged in shared memory
+    const int nch = min(8, (nvalid + 15) >> 4);
+    if (a.col_codes && tid < ncols) {
       const float S = nvfp4_global_scale(a.amax_col[g]);
-      const int64_t mpad = (int64_t)(t.mp[g + 1] - t.mp[g]);
-      const int64_t cbase = K * (int64_t)t.mp[g] / 2, sbase = K * (int64_t)t.mp[g] / 16;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
+      for (int j = 0; j < 8; ++j) {
+        if (j >= nch) break;
         float y[16];
-        column16(v, cc, y);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = bf16_bits_to_float(tile[(16 * j + i) * kTileC + tid]);
         if (a.use_rht) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -449,27 +492,63 @@ __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) y[i] = y[i] * 0.25f;
         }
-        float b = 0.0f;
+        float bmax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(y[i]));
+        for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(y[i]));
         uint32_t sf;
-        const float enc = nvfp4_block_encode(b, S, &sf);
+        const float enc = nvfp4_block_encode(bmax, S, &sf);
         uint32_t lo = 0, hi = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           lo |= e2m1x2(__fmul_rn(y[2 * k], enc), __fmul_rn(y[2 * k + 1], enc)) << (8 * k);
           hi |= e2m1x2(__fmul_rn(y[8 + 2 * k], enc), __fmul_rn(y[9 + 2 * k], enc)) << (8 * k);
         }
-        const int64_t col = un.col0 + cc;
-        *reinterpret_cast<uint2*>(a.col_codes + cbase + col * (mpad / 2) + 8LL * un.j) = make_uint2(lo, hi);
-        a.col_scales[sbase + col * (mpad / 16) + un.j] = (uint8_t)sf;
+        *reinterpret_cast<uint2*>(ccode + tid * 64 + 8 * j) = make_uint2(lo, hi);
+        cscale[tid * 8 + j] = (uint8_t)sf;
+      }
+    }
+    __syncthreads();
+
+    // phase 4: each column's run of nch chunks is contiguous in the columnwise
+    // layout; 8 lanes write one column (4 columns per warp instruction)
+    if (a.col_codes) {
+      const int64_t mpad = (int64_t)(t.mp[g + 1] - t.mp[g]);
+      const int64_t cbase = K * (int64_t)t.mp[g] / 2, sbase = K * (int64_t)t.mp[g] / 16;
+      const int j = lane & 7;
+      for (int cc = warp * 4 + (lane >> 3); cc < ncols; cc += kWarps * 4) {
+        if (j < nch) {
+          const int64_t col = col0 + cc;
+          *reinterpret_cast<uint2*>(a.col_codes + cbase + col * (mpad / 2) + 8LL * (8 * b + j)) =
+              *reinterpret_cast<const uint2*>(ccode + cc * 64 + 8 * j);
+          a.col_scales[sbase + col * (mpad / 16) + 8 * b + j] = cscale[cc * 8 + j];
+        }
       }
     }
   }
 }
 
-int grid_for(int64_t work_warps) {
-  const int64_t max_blocks = (int64_t)num_sms() * 8;
+// Persistent grid: as many blocks as fit on the device at once (one wave),
+// fewer when there is less work.
+template <typename Kern>
+int grid_for(Kern kern, int64_t work_warps, size_t smem = 0) {
+  static int per_sm_cache[64][8] = {};
+  static const void* keys[64][8] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int per_sm = 0;
+  for (int i = 0; i < 8; ++i)
+    if (keys[dev & 63][i] == (const void*)kern) per_sm = per_sm_cache[dev & 63][i];
+  if (!per_sm) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    for (int i = 0; i < 8; ++i)
+      if (!keys[dev & 63][i]) {
+        keys[dev & 63][i] = (const void*)kern;
+        per_sm_cache[dev & 63][i] = per_sm;
+        break;
+      }
+  }
+  const int64_t max_blocks = (int64_t)num_sms() * per_sm;
   int64_t blocks = (work_warps + kWarps - 1) / kWarps;
   if (blocks > max_blocks) blocks = max_blocks;
   return (int)(blocks < 1 ? 1 : blocks);
@@ -480,11 +559,10 @@ int grid_for(int64_t work_warps) {
 int quant_read_clear_status() { return read_clear_status(); }
 
 cudaError_t launch_row_quant(const RowQuantArgs& a, cudaStream_t s) {
-  const int grid = grid_for(a.M);
   if (a.format == GMLP_MXFP8)
-    row_quant_kernel<GMLP_MXFP8><<<grid, kThreads, 0, s>>>(a);
+    row_quant_kernel<GMLP_MXFP8><<<grid_for(row_quant_kernel<GMLP_MXFP8>, a.M), kThreads, 0, s>>>(a);
   else
-    row_quant_kernel<GMLP_NVFP4><<<grid, kThreads, 0, s>>>(a);
+    row_quant_kernel<GMLP_NVFP4><<<grid_for(row_quant_kernel<GMLP_NVFP4>, a.M), kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -492,7 +570,7 @@ cudaError_t launch_group_amax(const uint16_t* x, int64_t M, int64_t K, GroupSrc 
                               cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float) * grp.G, s);
   if (e != cudaSuccess) return e;
-  group_amax_kernel<<<grid_for(M), kThreads, 0, s>>>(x, K, grp, amax);
+  group_amax_kernel<<<grid_for(group_amax_kernel, M), kThreads, 0, s>>>(x, K, grp, amax);
   return cudaGetLastError();
 }
 
@@ -502,13 +580,24 @@ cudaError_t launch_hadamard_amax(const uint16_t* x, int64_t M, int64_t K, GroupS
   if (e == cudaSuccess) e = cudaMemsetAsync(amax_post, 0, sizeof(float) * grp.G, s);
   if (e != cudaSuccess) return e;
   const int64_t units = ((M + 15) / 16 + grp.G) * ((K + 255) / 256);
-  hadamard_amax_kernel<<<grid_for(units), kThreads, 0, s>>>(x, K, grp, mask & 0xFFFFu, amax_pre, amax_post);
+  hadamard_amax_kernel<<<grid_for(hadamard_amax_kernel, units), kThreads, 0, s>>>(x, K, grp, mask & 0xFFFFu, amax_pre,
+                                                                                  amax_post);
   return cudaGetLastError();
 }
 
 cudaError_t launch_col_quant(const ColQuantArgs& a, cudaStream_t s) {
-  const int64_t units = ((a.M + 15) / 16 + a.grp.G) * ((a.K + 255) / 256);
-  col_quant_kernel<<<grid_for(units), kThreads, 0, s>>>(a);
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(col_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kColSmem);
+    if (e != cudaSuccess) return e;
+    attr[dev & 63] = true;
+  }
+  const int64_t units = ((a.M + kTileR - 1) / kTileR + a.grp.G) * ((a.K + kTileC - 1) / kTileC);
+  int64_t grid = (int64_t)num_sms() * 2;
+  if (units < grid) grid = units;
+  col_quant_kernel<<<(int)(grid < 1 ? 1 : grid), kThreads, kColSmem, s>>>(a);
   return cudaGetLastError();
 }
 

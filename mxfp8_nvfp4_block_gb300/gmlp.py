@@ -45,7 +45,7 @@ class FwdAux(ctypes.Structure):
     _fields_ = [("fc2x_codes", ctypes.c_void_p), ("fc2x_scales", ctypes.c_void_p), ("fc2x_bf16", ctypes.c_void_p),
                 ("fc2x_amax_pre", ctypes.c_void_p), ("fc2x_amax_post", ctypes.c_void_p),
                 ("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("n_stage_events", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("gemm_mode", ctypes.c_int32)]
 
 
 _lib = None
@@ -226,7 +226,7 @@ def forward_workspace_size(M: int, K: int, N: int, G: int, act: int, rec: Recipe
 
 
 def forward(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *, y=None, workspace=None,
-            aux: dict | None = None, events=None, stream=None) -> torch.Tensor:
+            aux: dict | None = None, events=None, gemm_mode: int = 0, stream=None) -> torch.Tensor:
     """y = fused grouped-MLP forward of bf16 x [M, K]."""
     x = _bits(x)
     M, K = x.shape
@@ -239,10 +239,10 @@ def forward(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *
         workspace = _u8(need, x.device)
     aux_c = None
     ev_arr = None
-    if aux is not None or events is not None:
+    if aux is not None or events is not None or gemm_mode:
         aux = aux or {}
         aux_c = FwdAux(_p(aux.get("fc2x_codes")), _p(aux.get("fc2x_scales")), _p(aux.get("fc2x_bf16")),
-                       _p(aux.get("fc2x_amax_pre")), _p(aux.get("fc2x_amax_post")), None, 0, 0)
+                       _p(aux.get("fc2x_amax_pre")), _p(aux.get("fc2x_amax_post")), None, 0, int(gemm_mode))
         if events:
             ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
             aux_c.stage_events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))

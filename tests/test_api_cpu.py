@@ -98,6 +98,9 @@ def test_forward_argument_checks(lib):
         return L.gmlp_forward(FAKE, M, K, N, FAKE, G, ctypes.byref(W1), ctypes.byref(W2), None, act,
                               ctypes.byref(rec), FAKE, None, ws, wsb, None)
 
+    bad_aux = g.FwdAux(None, None, None, None, None, None, 0, 1)
+    assert L.gmlp_forward(FAKE, 512, 256, 256, FAKE, 4, ctypes.byref(w1), ctypes.byref(w2), None, g.SWIGLU,
+                          ctypes.byref(r), FAKE, ctypes.byref(bad_aux), FAKE, need, None) == g.ERR_INVALID_ARG
     assert call(K=128) == g.ERR_INVALID_DIMS                        # K % 256
     assert call(N=192) == g.ERR_INVALID_DIMS                        # N % 128
     assert call(G=3) == g.ERR_INVALID_DIMS                          # weights have 4 experts

@@ -26,7 +26,7 @@ def bf16_cpu(a):
     return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
 
 
-def run_gpu(gm, d, fmt, act, mask=0, probs=True):
+def run_gpu(gm, d, fmt, act, mask=0, probs=True, gemm_mode=0):
     w1 = gm.prepare_weights(d["W1"].cuda(), fmt, swiglu_interleave=(act == gm.SWIGLU))
     w2 = gm.prepare_weights(d["W2"].cuda(), fmt)
     M, N = d["x"].shape[0], d["W2"].shape[2]
@@ -42,7 +42,7 @@ def run_gpu(gm, d, fmt, act, mask=0, probs=True):
     rec = gm.recipe(fmt, use_rht=True, mask=mask)
     p = d["probs"].cuda() if probs else None
     y = torch.full((M, d["x"].shape[1]), float("nan"), dtype=torch.bfloat16, device="cuda")
-    gm.forward(d["x"].cuda(), d["splits"].cuda(), w1, w2, p, act, rec, y=y, aux=aux)
+    gm.forward(d["x"].cuda(), d["splits"].cuda(), w1, w2, p, act, rec, y=y, aux=aux, gemm_mode=gemm_mode)
     gm.check_device_status()
     torch.cuda.synchronize()
     return y, aux
@@ -78,15 +78,16 @@ def onehot_case(fmt, act, splits, K, N, seed):
                 W2=bf16_cpu(W2), probs=torch.from_numpy(probs))
 
 
+@pytest.mark.parametrize("gemm_mode", [0, 2], ids=["cta", "cta_pair"])
 @pytest.mark.parametrize("fmt,act", [(0, 1), (1, 1), (0, 0), (1, 0)],
                          ids=["mxfp8-srelu", "nvfp4-srelu", "mxfp8-swiglu", "nvfp4-swiglu"])
-def test_forward_lossless_bitexact(orc, gm, fmt, act):
+def test_forward_lossless_bitexact(orc, gm, fmt, act, gemm_mode):
     if act == 0:
         splits, K, N = [130, 0, 257, 5, 128], 512, 256      # SwiGLU: fc1 width 512
     else:
         splits, K, N = [130, 0, 257, 5, 128], 512, 512
     d = onehot_case(fmt, act, splits, K, N, seed=fmt * 10 + act)
-    y, aux = run_gpu(gm, d, fmt, act)
+    y, aux = run_gpu(gm, d, fmt, act, gemm_mode=gemm_mode)
     ref = orc.forward(bits(d["x"]), np.array(splits), bits(d["W1"]), bits(d["W2"]), d["probs"].numpy(), act, fmt)
     M = sum(splits)
     if act == 1:
@@ -107,11 +108,11 @@ def test_forward_lossless_bitexact(orc, gm, fmt, act):
         assert frob(y.float().cpu().numpy(), orc.bf16_to_f64(ref["y"])) <= Y_TOL
 
 
-def forward_parity(orc, gm, name, rows=None):
+def forward_parity(orc, gm, name, rows=None, gemm_mode=0):
     d = make_inputs(name)
     w = d["workload"]
     splits = d["splits"].numpy()
-    y, aux = run_gpu(gm, d, w.fmt, w.act, mask=d["mask"])
+    y, aux = run_gpu(gm, d, w.fmt, w.act, mask=d["mask"], gemm_mode=gemm_mode)
     ref = orc.forward(bits(d["x"]), splits, bits(d["W1"]), bits(d["W2"]), d["probs"].numpy(), w.act, w.fmt,
                       rows=rows, rht_mask=d["mask"])
     sel = ref["rows"]
@@ -138,6 +139,12 @@ def test_forward_tiny(orc, gm):
 
 def test_forward_mx_swiglu_full(orc, gm):
     forward_parity(orc, gm, "mx_swiglu")
+
+
+@pytest.mark.parametrize("name", ["mx_swiglu", "nv_srelu"])
+def test_forward_cta_pair_mode(orc, gm, name):
+    """The CTA-pair GEMM mode (cta_group::2, 256 x 256 tiles) on full workloads."""
+    forward_parity(orc, gm, name, gemm_mode=2)
 
 
 def test_forward_nv_srelu_full(orc, gm):
