@@ -399,16 +399,17 @@ __global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const uint16_t*
 
 // ------------------------------------------------------------------ row + column NVFP4 cast
 
-// Tiles of 128 rows x 256 columns of one group, staged in shared memory.
-constexpr int kTileR = 128, kTileC = 256;
-constexpr size_t kColSmem = (size_t)kTileR * kTileC * 2 + kTileC * 64 + kTileC * 8;
+// Tiles of 64 rows x 256 columns of one group, staged in shared memory
+// (4 column chunks of 16 rows each).
+constexpr int kTileR = 64, kTileC = 256, kChunks = kTileR / 16;
+constexpr size_t kColSmem = (size_t)kTileR * kTileC * 2 + kTileC * 8 * kChunks + kTileC * kChunks;
 
 __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
   __shared__ SmemGroups t;
   extern __shared__ uint4 dyn_smem[];
-  uint16_t* tile = reinterpret_cast<uint16_t*>(dyn_smem);             // [128][256] bf16
-  uint8_t* ccode = reinterpret_cast<uint8_t*>(tile + kTileR * kTileC);  // [256 columns][8 chunks x 8 B]
-  uint8_t* cscale = ccode + kTileC * 64;                                // [256 columns][8 chunks]
+  uint16_t* tile = reinterpret_cast<uint16_t*>(dyn_smem);             // [kTileR][256] bf16
+  uint8_t* ccode = reinterpret_cast<uint8_t*>(tile + kTileR * kTileC);  // [256 columns][kChunks x 8 B]
+  uint8_t* cscale = ccode + kTileC * 8 * kChunks;                       // [256 columns][kChunks]
   const int64_t K = a.K;
   const int slabs = (int)((K + kTileC - 1) / kTileC);
   build_group_tables(a.grp, slabs, t, kTileR);
@@ -430,14 +431,15 @@ __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
     // phase 1: the tile into shared memory (rows past the group end as zeros)
     __syncthreads();
     {
-      uint4 v[16];
+      constexpr int kIt = kTileR / kWarps;
+      uint4 v[kIt];
 #pragma unroll
-      for (int it = 0; it < 16; ++it) {
+      for (int it = 0; it < kIt; ++it) {
         const int r = it * 8 + (tid >> 5), c8 = (tid & 31) * 8;
         v[it] = (r < nvalid && c8 < ncols) ? ld_stream(a.x + (row0 + r) * K + col0 + c8) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int it = 0; it < 16; ++it) {
+      for (int it = 0; it < kIt; ++it) {
         const int r = it * 8 + (tid >> 5), c8 = (tid & 31) * 8;
         *reinterpret_cast<uint4*>(tile + r * kTileC + c8) = v[it];
       }
@@ -475,11 +477,11 @@ __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
 
     // phase 3: columnwise NVFP4 (16 consecutive rows per block, RHT first), one
     // thread per column, results staged in shared memory
-    const int nch = min(8, (nvalid + 15) >> 4);
+    const int nch = min(kChunks, (nvalid + 15) >> 4);
     if (a.col_codes && tid < ncols) {
       const float S = nvfp4_global_scale(a.amax_col[g]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < kChunks; ++j) {
         if (j >= nch) break;
         float y[16];
 #pragma unroll
@@ -503,24 +505,25 @@ __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
           lo |= e2m1x2(__fmul_rn(y[2 * k], enc), __fmul_rn(y[2 * k + 1], enc)) << (8 * k);
           hi |= e2m1x2(__fmul_rn(y[8 + 2 * k], enc), __fmul_rn(y[9 + 2 * k], enc)) << (8 * k);
         }
-        *reinterpret_cast<uint2*>(ccode + tid * 64 + 8 * j) = make_uint2(lo, hi);
-        cscale[tid * 8 + j] = (uint8_t)sf;
+        *reinterpret_cast<uint2*>(ccode + tid * 8 * kChunks + 8 * j) = make_uint2(lo, hi);
+        cscale[tid * kChunks + j] = (uint8_t)sf;
       }
     }
     __syncthreads();
 
     // phase 4: each column's run of nch chunks is contiguous in the columnwise
-    // layout; 8 lanes write one column (4 columns per warp instruction)
+    // layout; kChunks lanes write one column (32 / kChunks columns per warp instruction)
     if (a.col_codes) {
       const int64_t mpad = (int64_t)(t.mp[g + 1] - t.mp[g]);
       const int64_t cbase = K * (int64_t)t.mp[g] / 2, sbase = K * (int64_t)t.mp[g] / 16;
-      const int j = lane & 7;
-      for (int cc = warp * 4 + (lane >> 3); cc < ncols; cc += kWarps * 4) {
+      constexpr int kColsPerWarp = 32 / kChunks;
+      const int j = lane % kChunks;
+      for (int cc = warp * kColsPerWarp + lane / kChunks; cc < ncols; cc += kWarps * kColsPerWarp) {
         if (j < nch) {
           const int64_t col = col0 + cc;
-          *reinterpret_cast<uint2*>(a.col_codes + cbase + col * (mpad / 2) + 8LL * (8 * b + j)) =
-              *reinterpret_cast<const uint2*>(ccode + cc * 64 + 8 * j);
-          a.col_scales[sbase + col * (mpad / 16) + 8 * b + j] = cscale[cc * 8 + j];
+          *reinterpret_cast<uint2*>(a.col_codes + cbase + col * (mpad / 2) + 8LL * (kChunks * b + j)) =
+              *reinterpret_cast<const uint2*>(ccode + cc * 8 * kChunks + 8 * j);
+          a.col_scales[sbase + col * (mpad / 16) + kChunks * b + j] = cscale[cc * kChunks + j];
         }
       }
     }
@@ -595,7 +598,7 @@ cudaError_t launch_col_quant(const ColQuantArgs& a, cudaStream_t s) {
     attr[dev & 63] = true;
   }
   const int64_t units = ((a.M + kTileR - 1) / kTileR + a.grp.G) * ((a.K + kTileC - 1) / kTileC);
-  int64_t grid = (int64_t)num_sms() * 2;
+  int64_t grid = (int64_t)num_sms() * 4;
   if (units < grid) grid = units;
   col_quant_kernel<<<(int)(grid < 1 ? 1 : grid), kThreads, kColSmem, s>>>(a);
   return cudaGetLastError();
