@@ -404,6 +404,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     g1.out_scales = f_scales;
     g1.n_cols_out = N;
     g1.pair = (aux && aux->gemm_mode == 2) ? 2 : 1;
+    g1.pdl = 1;
     GMLP_CUDA(launch_gemm(g1, s), "fc1 launch");
     GMLP_TRY(mark());
     GemmArgs g2{};
@@ -420,6 +421,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     g2.out_bf16 = y;
     g2.n_cols_out = K;
     g2.pair = (aux && aux->gemm_mode == 2) ? 2 : 1;
+    g2.pdl = 1;
     GMLP_CUDA(launch_gemm(g2, s), "fc2 launch");
     GMLP_TRY(mark());
     return GMLP_OK;
@@ -445,9 +447,12 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     q.codes = x_codes;
     q.scales = x_scales;
     q.amax = x_amax;
+    q.zero_ptr = f_pre;   // fc1's epilogue max-accumulates into these
+    q.zero_count = G;
+    q.zero_ptr2 = f_post;
+    q.zero_count2 = G;
+    q.pdl = 1;
     GMLP_CUDA(launch_row_quant(q, s), "x quantise launch");
-    GMLP_CUDA(cudaMemsetAsync(f_pre, 0, sizeof(float) * G, s), "memset");
-    GMLP_CUDA(cudaMemsetAsync(f_post, 0, sizeof(float) * G, s), "memset");
   }
   GMLP_TRY(mark());
   GemmArgs g1{};
@@ -470,6 +475,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   g1.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
   g1.n_cols_out = N;
     g1.pair = (aux && aux->gemm_mode == 2) ? 2 : 1;
+    g1.pdl = 1;
   GMLP_CUDA(launch_gemm(g1, s), "fc1 launch");
   GMLP_TRY(mark());
   {
@@ -483,6 +489,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     q.codes = f_codes;
     q.scales = f_scales;
     q.amax = f_pre;
+    q.pdl = 1;
     GMLP_CUDA(launch_row_quant(q, s), "fc2_x quantise launch");
   }
   GMLP_TRY(mark());
@@ -502,6 +509,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   g2.out_bf16 = y;
   g2.n_cols_out = K;
     g2.pair = (aux && aux->gemm_mode == 2) ? 2 : 1;
+    g2.pdl = 1;
   GMLP_CUDA(launch_gemm(g2, s), "fc2 launch");
   GMLP_TRY(mark());
   return GMLP_OK;

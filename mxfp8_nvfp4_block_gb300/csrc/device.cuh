@@ -95,6 +95,18 @@ __device__ __forceinline__ float nvfp4_block_encode(float b, float S, uint32_t* 
   return sfv == 0.0f ? 0.0f : __fdiv_rn(S, sfv);
 }
 
+// ----------------------------------------------------------------- dependent launch
+
+// Wait until the preceding kernel in the stream (launched before this one with
+// programmatic stream serialization) has completed and its writes are visible.
+// A kernel launched normally returns at once.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel in the stream begin its prologue.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- bounded waits
 
 // A wait gives up after this many nanoseconds of %globaltimer; the longest

@@ -455,6 +455,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   __syncthreads();
   if (PAIR == 2) cluster_sync();  // the peer's barriers exist before anyone signals them
   tc_fence_after();
+  griddep_wait();                 // the previous kernel's outputs (A operand, amaxes) are complete
+  griddep_launch_dependents();
   const uint32_t tbase = *tslot;
   const int total = *bad ? 0 : ip[G];
 
@@ -651,11 +653,13 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kThreadsGemm);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -691,6 +695,12 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
   if (max_tiles < units) units = max_tiles;
   if (units < 1) units = 1;
   cfg.gridDim = dim3((unsigned)(units * PAIR));
+  if (PAIR == 2) {
+    cfg.numAttrs = a.pdl ? 2 : 1;
+  } else if (a.pdl) {
+    cfg.attrs = attr + 1;
+    cfg.numAttrs = 1;
+  }
   return cudaLaunchKernelEx(&cfg, kern, ta, tbm, tsa, tsb, a);
 }
 

@@ -37,6 +37,9 @@ struct RowQuantArgs {
   int swiglu_interleave;    // weights: gate/up 32-row interleave within each group
   float* zero_ptr;          // optional: floats zeroed by the first CTA (for later atomics)
   int zero_count;
+  float* zero_ptr2;         // optional second range
+  int zero_count2;
+  int pdl;                  // launch as a programmatic dependent of the previous kernel
 };
 cudaError_t launch_row_quant(const RowQuantArgs& a, cudaStream_t s);
 
@@ -95,6 +98,7 @@ struct GemmArgs {
   uint32_t rht_mask;
   int64_t n_cols_out;      // row length of the output (fc1: N; fc2: K)
   int pair;                // 2: CTA pairs (cta_group::2); otherwise single-CTA tiles
+  int pdl;                 // launch as a programmatic dependent of the previous kernel
 };
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 

@@ -148,11 +148,15 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads) row_quant_kernel(RowQuantArgs a) {
   __shared__ SmemGroups t;
   build_group_tables(a.grp, 1, t);
+  griddep_wait();
+  griddep_launch_dependents();
   if (t.bad) return;
   const int G = a.grp.G;
   if (blockIdx.x == 0) {
     if (a.zero_ptr)
       for (int i = threadIdx.x; i < a.zero_count; i += kThreads) a.zero_ptr[i] = 0.0f;
+    if (a.zero_ptr2)
+      for (int i = threadIdx.x; i < a.zero_count2; i += kThreads) a.zero_ptr2[i] = 0.0f;
     if (a.S_out)
       for (int g = threadIdx.x; g < G; g += kThreads) a.S_out[g] = nvfp4_global_scale(a.amax[g]);
   }
@@ -245,6 +249,8 @@ __global__ void __launch_bounds__(kThreads) group_amax_kernel(const uint16_t* x,
                                                               float* amax) {
   __shared__ SmemGroups t;
   build_group_tables(grp, 1, t);
+  griddep_wait();
+  griddep_launch_dependents();
   if (t.bad) return;
   const int G = grp.G;
   const int nch = (int)(K / 8);
@@ -350,6 +356,8 @@ __global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const uint16_t*
   __shared__ SmemGroups t;
   const int slabs = (int)((K + 255) / 256);
   build_group_tables(grp, slabs, t);
+  griddep_wait();
+  griddep_launch_dependents();
   if (t.bad) return;
   const int G = grp.G;
   const int lane = threadIdx.x & 31;
@@ -413,6 +421,8 @@ __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
   const int64_t K = a.K;
   const int slabs = (int)((K + kTileC - 1) / kTileC);
   build_group_tables(a.grp, slabs, t, kTileR);
+  griddep_wait();
+  griddep_launch_dependents();
   if (t.bad) return;
   const int G = a.grp.G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -561,12 +571,26 @@ int grid_for(Kern kern, int64_t work_warps, size_t smem = 0) {
 
 int quant_read_clear_status() { return read_clear_status(); }
 
+// Launch with programmatic stream serialization when `pdl` is set.
+template <typename... Args>
+cudaError_t launch_ex(void (*kern)(Args...), int grid, size_t smem, cudaStream_t s, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_row_quant(const RowQuantArgs& a, cudaStream_t s) {
   if (a.format == GMLP_MXFP8)
-    row_quant_kernel<GMLP_MXFP8><<<grid_for(row_quant_kernel<GMLP_MXFP8>, a.M), kThreads, 0, s>>>(a);
-  else
-    row_quant_kernel<GMLP_NVFP4><<<grid_for(row_quant_kernel<GMLP_NVFP4>, a.M), kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+    return launch_ex(row_quant_kernel<GMLP_MXFP8>, grid_for(row_quant_kernel<GMLP_MXFP8>, a.M), 0, s, a.pdl != 0, a);
+  return launch_ex(row_quant_kernel<GMLP_NVFP4>, grid_for(row_quant_kernel<GMLP_NVFP4>, a.M), 0, s, a.pdl != 0, a);
 }
 
 cudaError_t launch_group_amax(const uint16_t* x, int64_t M, int64_t K, GroupSrc grp, float* amax,
