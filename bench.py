@@ -157,7 +157,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
 
     for _ in range(W_steps):
         flush.zero_()
-        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws)
+        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode)
     gmlp.check_device_status()
     torch.cuda.synchronize()
     if world > 1:
@@ -169,7 +169,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
         for i in range(K_steps):
             flush.zero_()
             starts[i].record(stream)
-            gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws)
+            gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode)
             ends[i].record(stream)
         torch.cuda.synchronize()
         # pass 2: events after every kernel of the step, for per-kernel times
@@ -177,7 +177,8 @@ def run_gpu(args, rank: int, world: int) -> dict:
         for i in range(K_steps):
             flush.zero_()
             starts2[i].record(stream)
-            gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, events=stages[i])
+            gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, events=stages[i],
+                         gemm_mode=args.gemm_mode)
         torch.cuda.synchronize()
         clk.mark_end()
     if world > 1:
@@ -207,7 +208,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
         x.copy_(x_h, non_blocking=True)
         probs.copy_(p_h, non_blocking=True)
         splits.copy_(s_h, non_blocking=True)
-        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws)
+        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode)
         y_h.copy_(y, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
@@ -242,7 +243,8 @@ def run_gpu(args, rank: int, world: int) -> dict:
                    "l2": "flushed between timed steps (256 MiB write, outside the step events)",
                    "timing": "value: per-step start/end events; stages_ms and roofline: a second timed pass with "
                              "an event after every kernel",
-                   "weights": "quantised once before timing", "flops_per_step": w.flops},
+                   "weights": "quantised once before timing", "flops_per_step": w.flops,
+                   "gemm_mode": args.gemm_mode},
         "e2e": {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": K_steps * n_stage,
@@ -385,6 +387,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gmlp", choices=["gmlp", "reference"])
     ap.add_argument("--workload", default="mx_swiglu", choices=[k for k in WORKLOADS if k != "nv_quant"])
+    ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 2],
+                    help="0: one CTA per 128x256 tile; 2: CTA pairs on 256x256 tiles")
     ap.add_argument("--no-quant", dest="quant", action="store_false", help="skip the standalone quantiser leg")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false", help="skip the oracle CPU-baseline leg")
     args = ap.parse_args()
