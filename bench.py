@@ -44,6 +44,16 @@ WORKLOAD_TEXT = {
     "tiny": "MXFP8 SwiGLU grouped MLP: 4 experts, K=256, N=256, 512 tokens, seed 0",
 }
 NOMINAL_RATIO = {0: 2.0, 1: 6.0}   # dense FP8 / bf16 and FP4 / bf16 (4.5 and 13.5 vs 2.25 PFLOP/s)
+# DRAM bytes (read + write) per fc1 launch from one ncu capture
+# (profiles/gemm_mx_swiglu.md), valid only for the gemm.cu it was taken on.
+FC1_TRAFFIC = {("mx_swiglu", "0c36d48e6179db50b91df757bfe12724cc0a257c"): 65026816 + 4565504}
+
+
+def fc1_traffic(workload: str):
+    import hashlib
+    src = os.path.join(ROOT, "mxfp8_nvfp4_block_gb300", "csrc", "gemm.cu")
+    digest = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    return FC1_TRAFFIC.get((workload, digest))
 
 
 def peaks():
@@ -120,6 +130,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ multi-rank timing
+
+def max_over_ranks(total_ms: float, world: int, device) -> float:
+    """Slowest rank's timed total (every rank processes its own batch)."""
+    if world <= 1:
+        return total_ms
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: the FLOPs all ranks processed over the slowest rank's time."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def run_gpu(args, rank: int, world: int) -> dict:
@@ -187,13 +213,9 @@ def run_gpu(args, rank: int, world: int) -> dict:
     step_ms = [starts[i].elapsed_time(ends[i]) for i in range(K_steps)]
     bounds = [[starts2[i]] + stages[i] for i in range(K_steps)]
     stage_ms = [statistics.mean(b[j].elapsed_time(b[j + 1]) for b in bounds) for j in range(n_stage)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / K_steps
-    value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(w.flops, world, ms_per_step)
 
     # ---- end to end through the C ABI with host buffers
     x_h = d["x"].pin_memory()
@@ -254,7 +276,8 @@ def run_gpu(args, rank: int, world: int) -> dict:
                      "frac": round(achieved / peak, 4),
                      "peak_source": f"{src} bf16 burst {bf16_burst} x nominal {'FP8' if fmt == 0 else 'FP4'}/bf16 "
                                     f"ratio {NOMINAL_RATIO[fmt]}",
-                     "traffic": None},
+                     "traffic": fc1_traffic(name), "traffic_unit": "bytes per launch (ncu, null if the kernel "
+                                                                   "changed since the capture)"},
         "x_quantize": {"ms": round(stage_ms[quant_idx], 5), "bytes": q_bytes,
                        "GB_s": round(q_bytes / (stage_ms[quant_idx] * 1e-3) / 1e9, 1),
                        "frac_hbm": round(q_bytes / (stage_ms[quant_idx] * 1e-3) / 1e9 / hbm, 4)},

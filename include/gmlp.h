@@ -263,6 +263,13 @@ GMLP_API gmlp_status gmlp_forward_noalloc(const uint16_t* x, int64_t M, int64_t 
  * kernels set on a bounded-wait timeout or inconsistent split sizes. */
 GMLP_API gmlp_status gmlp_check_device_status(gmlp_stream stream);
 
+/* Self-test of the device failure path (no counterpart on the pages): one
+ * warp waits, through the same bounded mbarrier wait the kernels use, on a
+ * barrier nothing arrives at.  After limit_ns (1 us .. 2 s) the wait gives up
+ * and sets the device status word, which the next gmlp_check_device_status
+ * returns as GMLP_ERR_DEVICE_TIMEOUT; the context stays usable. */
+GMLP_API gmlp_status gmlp_selftest_bounded_wait(uint64_t limit_ns, gmlp_stream stream);
+
 /* Text of the calling thread's last non-OK status ("" if none). */
 GMLP_API const char* gmlp_last_error(void);
 

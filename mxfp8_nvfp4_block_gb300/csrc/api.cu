@@ -515,6 +515,15 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   return GMLP_OK;
 }
 
+gmlp_status gmlp_selftest_bounded_wait(uint64_t limit_ns, gmlp_stream stream) {
+  g_last_error[0] = 0;
+  if (limit_ns < 1000 || limit_ns > 2000000000ull)
+    return fail(GMLP_ERR_INVALID_ARG, "limit_ns %llu outside [1 us, 2 s]", (unsigned long long)limit_ns);
+  GMLP_TRY(check_device());
+  GMLP_CUDA(launch_selftest_wait(limit_ns, (cudaStream_t)stream), "selftest launch");
+  return GMLP_OK;
+}
+
 gmlp_status gmlp_check_device_status(gmlp_stream stream) {
   g_last_error[0] = 0;
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);

@@ -567,7 +567,29 @@ int grid_for(Kern kern, int64_t work_warps, size_t smem = 0) {
   return (int)(blocks < 1 ? 1 : blocks);
 }
 
+// One warp waits, through the kernels' bounded wait, on an mbarrier that
+// nothing arrives at; the wait gives up after limit_ns and reports
+// GMLP_ERR_DEVICE_TIMEOUT in the status word.
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, limit_ns);
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_arrive(&bar);  // complete the phase before the barrier goes away
+}
+
 }  // namespace
+
+cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(limit_ns);
+  return cudaGetLastError();
+}
 
 int quant_read_clear_status() { return read_clear_status(); }
 

@@ -23,7 +23,8 @@ COMPACT, GEMM_TILED = 0, 1
 
 EXPORTS = ["gmlp_tiled_scales_bytes", "gmlp_group_hadamard_amax", "gmlp_group_quantize_with_amax",
            "gmlp_group_quantize", "gmlp_prepare_weights", "gmlp_forward_workspace_size", "gmlp_forward",
-           "gmlp_check_device_status", "gmlp_last_error", "gmlp_version", "gmlp_forward_noalloc"]
+           "gmlp_check_device_status", "gmlp_last_error", "gmlp_version", "gmlp_forward_noalloc",
+           "gmlp_selftest_bounded_wait"]
 
 
 class Recipe(ctypes.Structure):
@@ -76,6 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                         ctypes.POINTER(QWeightC), _vp, _i32, ctypes.POINTER(Recipe), _vp,
                                         ctypes.POINTER(FwdAux), _vp]),
         "gmlp_check_device_status": (_i32, [_vp]),
+        "gmlp_selftest_bounded_wait": (_i32, [ctypes.c_uint64, _vp]),
         "gmlp_last_error": (ctypes.c_char_p, []),
         "gmlp_version": (ctypes.c_char_p, []),
     }
@@ -267,6 +269,11 @@ def forward_noalloc(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: R
     _check(load().gmlp_forward_noalloc(_p(x), M, K, W2.cols, _p(splits), G, ctypes.byref(w1c), ctypes.byref(w2c),
                                        _p(probs), act, ctypes.byref(rec), _p(y), None, _stream(stream)))
     return y
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Make a bounded device wait run out (see gmlp_selftest_bounded_wait)."""
+    _check(load().gmlp_selftest_bounded_wait(int(limit_ns), _stream(stream)))
 
 
 def check_device_status(stream=None) -> None:

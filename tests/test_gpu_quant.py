@@ -167,3 +167,20 @@ def test_split_sizes_past_M_reported(gm):
     with pytest.raises(gm.GmlpError):
         gm.check_device_status()
     del out
+
+
+def test_bounded_wait_times_out_and_reports(gm):
+    """A wait that nothing completes gives up after its limit; the host reads
+    GMLP_ERR_DEVICE_TIMEOUT and the context keeps working."""
+    import time
+    t0 = time.time()
+    gm.selftest_bounded_wait(50_000_000)           # 50 ms
+    with pytest.raises(gm.GmlpError) as e:
+        gm.check_device_status()
+    assert e.value.status == gm.ERR_DEVICE_TIMEOUT
+    assert time.time() - t0 < 10
+    gm.check_device_status()                        # cleared
+    x = torch.ones((32, 128), dtype=torch.bfloat16).cuda()
+    pre, post = gm.group_hadamard_amax(x, torch.tensor([32]).cuda(), 0)
+    gm.check_device_status()
+    assert pre.item() == 1.0 and post.item() == 4.0
