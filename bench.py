@@ -413,6 +413,8 @@ def main():
     ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 2],
                     help="0: one CTA per 128x256 tile; 2: CTA pairs on 256x256 tiles")
     ap.add_argument("--no-quant", dest="quant", action="store_false", help="skip the standalone quantiser leg")
+    ap.add_argument("--quant-only", action="store_true",
+                    help="run only the standalone NVFP4 quantiser leg and print its JSON")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false", help="skip the oracle CPU-baseline leg")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -428,6 +430,12 @@ def main():
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a GPU for the gmlp arm")
+    if args.quant_only:
+        from mxfp8_nvfp4_block_gb300 import gmlp
+        gmlp.load()
+        if rank == 0:
+            print(json.dumps(bench_quantizer(gmlp, torch.device("cuda", torch.cuda.current_device()), peaks()[0])))
+        return
     out = run_gpu(args, rank, world)
     if rank == 0:
         if args.cpu:

@@ -412,10 +412,38 @@ __global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const uint16_t*
 constexpr int kTileR = 64, kTileC = 256, kChunks = kTileR / 16;
 constexpr size_t kColSmem = (size_t)kTileR * kTileC * 2 + kTileC * 8 * kChunks + kTileC * kChunks;
 
+// E4M3 scale byte of an NVFP4 block with max b under global scale S:
+// E4M3(fp32(fp32(b / 6) * S)).
+__device__ __forceinline__ uint32_t nvfp4_block_sf(float b, float S) {
+  return e4m3x2(__fmul_rn(__fdiv_rn(b, 6.0f), S), 0.0f) & 0xFF;
+}
+
+// enc[c] = fp32(S / E4M3(c)) for every scale byte c a block can take (0 -> 0):
+// the same IEEE division the block encode performs, once per code.
+__device__ __forceinline__ void fill_enc_table(float* enc, float S, int tid) {
+  if (tid < 128) {
+    const float sv = e4m3_to_float((uint32_t)tid);
+    enc[tid] = (tid == 0 || tid == 127) ? 0.0f : __fdiv_rn(S, sv);
+  }
+}
+
+// 16 values -> 8 bytes of E2M1 codes (even element in the low nibble)
+__device__ __forceinline__ uint2 e2m1_pack16(const float* v, float enc) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    lo |= e2m1x2(__fmul_rn(v[2 * k], enc), __fmul_rn(v[2 * k + 1], enc)) << (8 * k);
+    hi |= e2m1x2(__fmul_rn(v[8 + 2 * k], enc), __fmul_rn(v[9 + 2 * k], enc)) << (8 * k);
+  }
+  return make_uint2(lo, hi);
+}
+
 __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
   __shared__ SmemGroups t;
+  __shared__ float enc_row[128], enc_col[128];
   extern __shared__ uint4 dyn_smem[];
   uint16_t* tile = reinterpret_cast<uint16_t*>(dyn_smem);             // [kTileR][256] bf16
+  const uint32_t* tile32 = reinterpret_cast<const uint32_t*>(tile);   // [kTileR][128] bf16 pairs
   uint8_t* ccode = reinterpret_cast<uint8_t*>(tile + kTileR * kTileC);  // [256 columns][kChunks x 8 B]
   uint8_t* cscale = ccode + kTileC * 8 * kChunks;                       // [256 columns][kChunks]
   const int64_t K = a.K;
@@ -427,6 +455,8 @@ __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
   const int G = a.grp.G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nscale_row = (int)(K / 16);
+  int cur_g = -1;
+  float S_row = 0.0f, S_col = 0.0f;
   for (int64_t u = blockIdx.x; u < t.up[G]; u += gridDim.x) {
     const int g = find_unit_group(t, G, u);
     const int m = t.off[g + 1] - t.off[g];
@@ -438,8 +468,15 @@ __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
     const int64_t col0 = (int64_t)slab * kTileC;
     const int ncols = (int)min((int64_t)kTileC, K - col0);
 
+    __syncthreads();  // the previous tile is done with shared memory
+    if (g != cur_g) {
+      cur_g = g;
+      S_row = a.row_codes ? nvfp4_global_scale(a.amax_row[g]) : 0.0f;
+      S_col = a.col_codes ? nvfp4_global_scale(a.amax_col[g]) : 0.0f;
+      fill_enc_table(enc_row, S_row, tid);
+      fill_enc_table(enc_col, S_col, tid);
+    }
     // phase 1: the tile into shared memory (rows past the group end as zeros)
-    __syncthreads();
     {
       constexpr int kIt = kTileR / kWarps;
       uint4 v[kIt];
@@ -456,67 +493,76 @@ __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
     }
     __syncthreads();
 
-    // phase 2: rowwise NVFP4 (16 consecutive columns per block), one warp per row
+    // phase 2: rowwise NVFP4, one thread per 16-column block (16 threads per row)
     if (a.row_codes) {
-      const float S = nvfp4_global_scale(a.amax_row[g]);
-      for (int r = warp; r < nvalid; r += kWarps) {
-        float f[8];
-        unpack8(*reinterpret_cast<const uint4*>(tile + r * kTileC + lane * 8), f);
+      const int nblk = ncols / 16;
+      for (int base = warp * 32; base < nvalid * 16; base += kThreads) {
+        const int i = base + lane, r = i >> 4, bb = i & 15;
+        const bool ok = r < nvalid && bb < nblk;
+        float f[16];
+        unpack8(*reinterpret_cast<const uint4*>(tile + r * kTileC + 16 * bb), f);
+        unpack8(*reinterpret_cast<const uint4*>(tile + r * kTileC + 16 * bb + 8), f + 8);
         float am = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) am = fmaxf(am, fabsf(f[k]));
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-        uint32_t sf;
-        const float enc = nvfp4_block_encode(am, S, &sf);
-        uint32_t word = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          word |= e2m1x2(__fmul_rn(f[2 * k], enc), __fmul_rn(f[2 * k + 1], enc)) << (8 * k);
-        const int lb = lane & 24;
-        const uint32_t sw = __shfl_sync(0xffffffffu, sf, lb) | (__shfl_sync(0xffffffffu, sf, lb + 2) << 8) |
-                            (__shfl_sync(0xffffffffu, sf, lb + 4) << 16) | (__shfl_sync(0xffffffffu, sf, lb + 6) << 24);
-        if (lane * 8 < ncols) {
+        for (int k = 0; k < 16; ++k) am = fmaxf(am, fabsf(f[k]));
+        const uint32_t sf = nvfp4_block_sf(am, S_row);
+        const uint2 codes = e2m1_pack16(f, enc_row[sf]);
+        const int lb = lane & ~3;
+        const uint32_t sw = __shfl_sync(0xffffffffu, sf, lb) | (__shfl_sync(0xffffffffu, sf, lb + 1) << 8) |
+                            (__shfl_sync(0xffffffffu, sf, lb + 2) << 16) | (__shfl_sync(0xffffffffu, sf, lb + 3) << 24);
+        if (ok) {
           const int64_t rg = row0 + r;
-          *reinterpret_cast<uint32_t*>(a.row_codes + rg * (K / 2) + (col0 + lane * 8) / 2) = word;
-          if ((lane & 7) == 0)
+          *reinterpret_cast<uint2*>(a.row_codes + rg * (K / 2) + (col0 >> 1) + 8 * bb) = codes;
+          if ((bb & 3) == 0)
             *reinterpret_cast<uint32_t*>(a.row_scales + scale_offset(a.row_tiled, t, g, rg,
-                                                                     (int)((col0 + lane * 8) >> 4), nscale_row)) = sw;
+                                                                     (int)(col0 >> 4) + bb, nscale_row)) = sw;
         }
       }
     }
 
-    // phase 3: columnwise NVFP4 (16 consecutive rows per block, RHT first), one
-    // thread per column, results staged in shared memory
+    // phase 3: columnwise NVFP4 (16 consecutive rows per block, RHT first):
+    // thread = two adjacent columns x two chunks; results staged in shared memory
     const int nch = min(kChunks, (nvalid + 15) >> 4);
-    if (a.col_codes && tid < ncols) {
-      const float S = nvfp4_global_scale(a.amax_col[g]);
+    if (a.col_codes) {
+      const int cp = tid & 127;
 #pragma unroll
-      for (int j = 0; j < kChunks; ++j) {
-        if (j >= nch) break;
-        float y[16];
+      for (int jq = 0; jq < 2; ++jq) {
+        const int j = (tid >> 7) * 2 + jq;
+        if (j < nch && 2 * cp < ncols) {
+          float y0[16], y1[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] = bf16_bits_to_float(tile[(16 * j + i) * kTileC + tid]);
-        if (a.use_rht) {
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t w = tile32[(16 * j + i) * (kTileC / 2) + cp];
+            y0[i] = bf16_bits_to_float(w & 0xFFFF);
+            y1[i] = bf16_bits_to_float(w >> 16);
+          }
+          if (a.use_rht) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if ((a.mask >> i) & 1u) y[i] = -y[i];
-          fwht16(y);
+            for (int i = 0; i < 16; ++i)
+              if ((a.mask >> i) & 1u) {
+                y0[i] = -y0[i];
+                y1[i] = -y1[i];
+              }
+            fwht16(y0);
+            fwht16(y1);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) y[i] = y[i] * 0.25f;
+            for (int i = 0; i < 16; ++i) {
+              y0[i] = y0[i] * 0.25f;
+              y1[i] = y1[i] * 0.25f;
+            }
+          }
+          float b0 = 0.0f, b1 = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            b0 = fmaxf(b0, fabsf(y0[i]));
+            b1 = fmaxf(b1, fabsf(y1[i]));
+          }
+          const uint32_t sf0 = nvfp4_block_sf(b0, S_col), sf1 = nvfp4_block_sf(b1, S_col);
+          *reinterpret_cast<uint2*>(ccode + (2 * cp) * 8 * kChunks + 8 * j) = e2m1_pack16(y0, enc_col[sf0]);
+          *reinterpret_cast<uint2*>(ccode + (2 * cp + 1) * 8 * kChunks + 8 * j) = e2m1_pack16(y1, enc_col[sf1]);
+          cscale[(2 * cp) * kChunks + j] = (uint8_t)sf0;
+          cscale[(2 * cp + 1) * kChunks + j] = (uint8_t)sf1;
         }
-        float bmax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(y[i]));
-        uint32_t sf;
-        const float enc = nvfp4_block_encode(bmax, S, &sf);
-        uint32_t lo = 0, hi = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          lo |= e2m1x2(__fmul_rn(y[2 * k], enc), __fmul_rn(y[2 * k + 1], enc)) << (8 * k);
-          hi |= e2m1x2(__fmul_rn(y[8 + 2 * k], enc), __fmul_rn(y[9 + 2 * k], enc)) << (8 * k);
-        }
-        *reinterpret_cast<uint2*>(ccode + tid * 8 * kChunks + 8 * j) = make_uint2(lo, hi);
-        cscale[tid * kChunks + j] = (uint8_t)sf;
       }
     }
     __syncthreads();
@@ -644,9 +690,7 @@ cudaError_t launch_col_quant(const ColQuantArgs& a, cudaStream_t s) {
     attr[dev & 63] = true;
   }
   const int64_t units = ((a.M + kTileR - 1) / kTileR + a.grp.G) * ((a.K + kTileC - 1) / kTileC);
-  int64_t grid = (int64_t)num_sms() * 4;
-  if (units < grid) grid = units;
-  col_quant_kernel<<<(int)(grid < 1 ? 1 : grid), kThreads, kColSmem, s>>>(a);
+  col_quant_kernel<<<grid_for(col_quant_kernel, units * kWarps, kColSmem), kThreads, kColSmem, s>>>(a);
   return cudaGetLastError();
 }
 
