@@ -427,15 +427,78 @@ __device__ __forceinline__ void fill_enc_table(float* enc, float S, int tid) {
   }
 }
 
+// Eight FP32 values (already multiplied by the encode factor) -> four E2M1
+// code bytes packed into one word, element 0 in the low nibble.
+__device__ __forceinline__ uint32_t e2m1_pack8(const float* p) {
+  uint32_t w;
+  asm("{\n .reg .b8 q0, q1, q2, q3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n"
+      " mov.b32 %0, {q0, q1, q2, q3};\n}"
+      : "=r"(w)
+      : "f"(p[0]), "f"(p[1]), "f"(p[2]), "f"(p[3]), "f"(p[4]), "f"(p[5]), "f"(p[6]), "f"(p[7]));
+  return w;
+}
+
+
+// Packed pairs of FP32 (two columns side by side); each lane of the pair is an
+// IEEE round-to-nearest-even operation, identical to the scalar one.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float a, float b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float lo2(f32x2 v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return a;
+}
+__device__ __forceinline__ float hi2(f32x2 v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return b;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // 16 values -> 8 bytes of E2M1 codes (even element in the low nibble)
 __device__ __forceinline__ uint2 e2m1_pack16(const float* v, float enc) {
-  uint32_t lo = 0, hi = 0;
+  float p[16];
+  const f32x2 e2 = pk2(enc, enc);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    lo |= e2m1x2(__fmul_rn(v[2 * k], enc), __fmul_rn(v[2 * k + 1], enc)) << (8 * k);
-    hi |= e2m1x2(__fmul_rn(v[8 + 2 * k], enc), __fmul_rn(v[9 + 2 * k], enc)) << (8 * k);
+  for (int k = 0; k < 16; k += 2) {
+    const f32x2 q = mul2(pk2(v[k], v[k + 1]), e2);
+    p[k] = lo2(q);
+    p[k + 1] = hi2(q);
   }
-  return make_uint2(lo, hi);
+  return make_uint2(e2m1_pack8(p), e2m1_pack8(p + 8));
+}
+
+// The 16-point FWHT stages of fwht16 on two columns at once.
+__device__ __forceinline__ void fwht16x2(f32x2* w) {
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (!(i & h)) {
+        const f32x2 p = w[i], q = w[i + h];
+        w[i] = add2(p, q);
+        w[i + h] = sub2(p, q);
+      }
 }
 
 __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
@@ -521,45 +584,49 @@ __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
     }
 
     // phase 3: columnwise NVFP4 (16 consecutive rows per block, RHT first):
-    // thread = two adjacent columns x two chunks; results staged in shared memory
+    // thread = two adjacent columns (packed FP32 pairs) x two chunks; results
+    // staged in shared memory
     const int nch = min(kChunks, (nvalid + 15) >> 4);
     if (a.col_codes) {
       const int cp = tid & 127;
+      const uint32_t sm = a.use_rht ? a.mask : 0u;
 #pragma unroll
       for (int jq = 0; jq < 2; ++jq) {
         const int j = (tid >> 7) * 2 + jq;
         if (j < nch && 2 * cp < ncols) {
-          float y0[16], y1[16];
+          f32x2 y[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
+            // bf16 pair -> FP32 pair, the sign of row i flipped through its sign bit
             const uint32_t w = tile32[(16 * j + i) * (kTileC / 2) + cp];
-            y0[i] = bf16_bits_to_float(w & 0xFFFF);
-            y1[i] = bf16_bits_to_float(w >> 16);
+            const uint32_t sb = (sm << (31 - i)) & 0x80000000u;
+            y[i] = pk2(__uint_as_float((w << 16) ^ sb), __uint_as_float((w & 0xFFFF0000u) ^ sb));
           }
           if (a.use_rht) {
+            fwht16x2(y);
+            const f32x2 quarter = pk2(0.25f, 0.25f);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if ((a.mask >> i) & 1u) {
-                y0[i] = -y0[i];
-                y1[i] = -y1[i];
-              }
-            fwht16(y0);
-            fwht16(y1);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              y0[i] = y0[i] * 0.25f;
-              y1[i] = y1[i] * 0.25f;
-            }
+            for (int i = 0; i < 16; ++i) y[i] = mul2(y[i], quarter);
           }
           float b0 = 0.0f, b1 = 0.0f;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            b0 = fmaxf(b0, fabsf(y0[i]));
-            b1 = fmaxf(b1, fabsf(y1[i]));
+            b0 = fmaxf(b0, fabsf(lo2(y[i])));
+            b1 = fmaxf(b1, fabsf(hi2(y[i])));
           }
           const uint32_t sf0 = nvfp4_block_sf(b0, S_col), sf1 = nvfp4_block_sf(b1, S_col);
-          *reinterpret_cast<uint2*>(ccode + (2 * cp) * 8 * kChunks + 8 * j) = e2m1_pack16(y0, enc_col[sf0]);
-          *reinterpret_cast<uint2*>(ccode + (2 * cp + 1) * 8 * kChunks + 8 * j) = e2m1_pack16(y1, enc_col[sf1]);
+          const f32x2 enc = pk2(enc_col[sf0], enc_col[sf1]);
+          float p0[16], p1[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const f32x2 q = mul2(y[i], enc);
+            p0[i] = lo2(q);
+            p1[i] = hi2(q);
+          }
+          *reinterpret_cast<uint2*>(ccode + (2 * cp) * 8 * kChunks + 8 * j) =
+              make_uint2(e2m1_pack8(p0), e2m1_pack8(p0 + 8));
+          *reinterpret_cast<uint2*>(ccode + (2 * cp + 1) * 8 * kChunks + 8 * j) =
+              make_uint2(e2m1_pack8(p1), e2m1_pack8(p1 + 8));
           cscale[(2 * cp) * kChunks + j] = (uint8_t)sf0;
           cscale[(2 * cp + 1) * kChunks + j] = (uint8_t)sf1;
         }
