@@ -148,6 +148,11 @@ def job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
 
 # ------------------------------------------------------------------ GPU arm
 
+L2_TEXT = {"write": "flushed between timed steps (256 MiB write, outside the step events)",
+           "clean": "flushed between timed steps (256 MiB write, then a 256 MiB read of a second buffer so the "
+                    "step starts on a cold L2 without the write's dirty lines; outside the step events)"}
+
+
 def run_gpu(args, rank: int, world: int) -> dict:
     from mxfp8_nvfp4_block_gb300 import gmlp
     gmlp.load()
@@ -167,6 +172,14 @@ def run_gpu(args, rank: int, world: int) -> dict:
     y = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(gmlp.forward_workspace_size(w.M, w.K, w.N, w.G, act, rec), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > 129 MB of L2
+    sweep = torch.zeros(64 * 1024 * 1024, dtype=torch.int32, device=dev) if args.l2_flush == "clean" else None
+
+    def flush_l2():
+        # write 256 MiB; "clean" then reads another 256 MiB so that the write's
+        # dirty lines are written back here and the step starts on a cold, clean L2
+        flush.zero_()
+        if sweep is not None:
+            torch.amax(sweep)
     n_stage = 3 if fmt == gmlp.MXFP8 else 5
     K_steps, W_steps = args.steps, args.warmup
 
@@ -182,7 +195,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
     torch.cuda.synchronize()
 
     for _ in range(W_steps):
-        flush.zero_()
+        flush_l2()
         gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode)
     gmlp.check_device_status()
     torch.cuda.synchronize()
@@ -193,7 +206,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
         # pass 1 (the reported steps): one event before and after each step, so the
         # kernels of a step overlap their neighbours' prologues as in normal use
         for i in range(K_steps):
-            flush.zero_()
+            flush_l2()
             starts[i].record(stream)
             gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode)
             ends[i].record(stream)
@@ -201,7 +214,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
         # pass 2: events after every kernel of the step, for per-kernel times
         # (an event between kernels stops that overlap, so these steps run slightly longer)
         for i in range(K_steps):
-            flush.zero_()
+            flush_l2()
             starts2[i].record(stream)
             gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, events=stages[i],
                          gemm_mode=args.gemm_mode)
@@ -262,7 +275,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
         "dtype": "mxfp8" if fmt == gmlp.MXFP8 else "nvfp4",
         "data": "synthetic",
         "config": {"workload": f"{name}: {WORKLOAD_TEXT.get(name, name)}",
-                   "l2": "flushed between timed steps (256 MiB write, outside the step events)",
+                   "l2": L2_TEXT[args.l2_flush],
                    "timing": "value: per-step start/end events; stages_ms and roofline: a second timed pass with "
                              "an event after every kernel",
                    "weights": "quantised once before timing", "flops_per_step": w.flops,
@@ -283,8 +296,33 @@ def run_gpu(args, rank: int, world: int) -> dict:
                        "frac_hbm": round(q_bytes / (stage_ms[quant_idx] * 1e-3) / 1e9 / hbm, 4)},
         "clocks": clk.summary(),
     }
+    ceiling = mma_ceiling(gmlp, fmt)
+    out["roofline"]["mma_loop_tflops"] = ceiling
+    out["roofline"]["frac_of_mma_loop"] = round(achieved / ceiling["with_scale_copies"], 4)
     if args.quant and rank == 0:
         out["group_quantize"] = bench_quantizer(gmlp, dev, hbm)
+    return out
+
+
+def mma_ceiling(gmlp, fmt: int, iters: int = 32768, reps: int = 5) -> dict:
+    """Tensor-core ceiling of the GEMM mainloop's MMA shape: gmlp_mma_peak on
+    every SM (no global memory), with and without the per-stage scale copies."""
+    out = {}
+    for copy in (True, False):
+        for _ in range(3):
+            gmlp.mma_peak(fmt, copy, iters)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            gmlp.mma_peak(fmt, copy, iters)
+        e1.record()
+        torch.cuda.synchronize()
+        gmlp.check_device_status()
+        ms = e0.elapsed_time(e1) / reps
+        n_sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        tf = gmlp.mma_peak_flops(fmt, iters, n_sm) / (ms * 1e-3) / 1e12
+        out["with_scale_copies" if copy else "scales_resident"] = round(tf, 1)
     return out
 
 
@@ -412,6 +450,8 @@ def main():
     ap.add_argument("--workload", default="mx_swiglu", choices=[k for k in WORKLOADS if k != "nv_quant"])
     ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 2],
                     help="0: one CTA per 128x256 tile; 2: CTA pairs on 256x256 tiles")
+    ap.add_argument("--l2-flush", default="write", choices=["write", "clean"],
+                    help="between timed steps: write 256 MiB, or write 256 MiB then read another 256 MiB")
     ap.add_argument("--no-quant", dest="quant", action="store_false", help="skip the standalone quantiser leg")
     ap.add_argument("--quant-only", action="store_true",
                     help="run only the standalone NVFP4 quantiser leg and print its JSON")

@@ -270,6 +270,19 @@ GMLP_API gmlp_status gmlp_check_device_status(gmlp_stream stream);
  * returns as GMLP_ERR_DEVICE_TIMEOUT; the context stays usable. */
 GMLP_API gmlp_status gmlp_selftest_bounded_wait(uint64_t limit_ns, gmlp_stream stream);
 
+/* Tensor-core ceiling of the grouped GEMM's mainloop (a measurement tool; the
+ * pages have no counterpart).  Launches `ctas` CTAs (<= 0: one per SM), each
+ * issuing `iters` stages (1 .. 2^24) of the GEMM's block-scaled MMA mix from
+ * shared memory filled once with random codes: per stage four M=128, N=256
+ * MMAs (K = 32 for GMLP_MXFP8, 64 for GMLP_NVFP4) and one commit, preceded,
+ * when scale_copy != 0, by the stage's scale-factor copies to TMEM (3 for
+ * MXFP8, 12 for NVFP4), as in the GEMM.  Reads and writes no global memory.
+ * One launch performs ctas * iters * 4 * 2 * 128 * 256 * K floating-point
+ * operations; time it with events on `stream`.  A stage waits for the MMAs of
+ * the stage four back (bounded; a timeout sets the device status word). */
+GMLP_API gmlp_status gmlp_mma_peak(int32_t format, int32_t scale_copy, int64_t iters, int32_t ctas,
+                                   gmlp_stream stream);
+
 /* Text of the calling thread's last non-OK status ("" if none). */
 GMLP_API const char* gmlp_last_error(void);
 

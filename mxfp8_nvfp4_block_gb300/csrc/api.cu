@@ -13,6 +13,7 @@ namespace gmlp {
 
 int quant_read_clear_status();
 int gemm_read_clear_status();
+int peak_read_clear_status();
 
 namespace {
 
@@ -524,13 +525,26 @@ gmlp_status gmlp_selftest_bounded_wait(uint64_t limit_ns, gmlp_stream stream) {
   return GMLP_OK;
 }
 
+gmlp_status gmlp_mma_peak(int32_t format, int32_t scale_copy, int64_t iters, int32_t ctas, gmlp_stream stream) {
+  g_last_error[0] = 0;
+  if (format != GMLP_MXFP8 && format != GMLP_NVFP4) return fail(GMLP_ERR_INVALID_ARG, "format %d", format);
+  if (iters < 1 || iters > (int64_t(1) << 24))
+    return fail(GMLP_ERR_INVALID_ARG, "iters %lld outside [1, 2^24]", (long long)iters);
+  GMLP_TRY(check_device());
+  const int n = ctas > 0 ? ctas : num_sms();
+  if (n > 65535) return fail(GMLP_ERR_INVALID_ARG, "ctas %d", n);
+  GMLP_CUDA(launch_mma_peak(format, scale_copy != 0, iters, n, (cudaStream_t)stream), "mma peak launch");
+  return GMLP_OK;
+}
+
 gmlp_status gmlp_check_device_status(gmlp_stream stream) {
   g_last_error[0] = 0;
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   const int a = quant_read_clear_status();
   const int b = gemm_read_clear_status();
-  const int code = a ? a : b;
+  const int c = peak_read_clear_status();
+  const int code = a ? a : (b ? b : c);
   if (code < 0) return fail(GMLP_ERR_CUDA, "reading the device status word failed");
   if (code == GMLP_ERR_DEVICE_TIMEOUT) return fail(GMLP_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait");
   if (code == GMLP_ERR_DEVICE_BOUNDS)

@@ -105,6 +105,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 int num_sms();
 
 cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t s);
+cudaError_t launch_mma_peak(int format, bool scale_copy, int64_t iters, int ctas, cudaStream_t s);
 
 gmlp_status set_last_error(gmlp_status st, const char* msg);
 

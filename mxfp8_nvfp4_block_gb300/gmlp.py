@@ -24,7 +24,7 @@ COMPACT, GEMM_TILED = 0, 1
 EXPORTS = ["gmlp_tiled_scales_bytes", "gmlp_group_hadamard_amax", "gmlp_group_quantize_with_amax",
            "gmlp_group_quantize", "gmlp_prepare_weights", "gmlp_forward_workspace_size", "gmlp_forward",
            "gmlp_check_device_status", "gmlp_last_error", "gmlp_version", "gmlp_forward_noalloc",
-           "gmlp_selftest_bounded_wait"]
+           "gmlp_selftest_bounded_wait", "gmlp_mma_peak"]
 
 
 class Recipe(ctypes.Structure):
@@ -78,6 +78,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                         ctypes.POINTER(FwdAux), _vp]),
         "gmlp_check_device_status": (_i32, [_vp]),
         "gmlp_selftest_bounded_wait": (_i32, [ctypes.c_uint64, _vp]),
+        "gmlp_mma_peak": (_i32, [_i32, _i32, ctypes.c_int64, _i32, _vp]),
         "gmlp_last_error": (ctypes.c_char_p, []),
         "gmlp_version": (ctypes.c_char_p, []),
     }
@@ -274,6 +275,17 @@ def forward_noalloc(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: R
 def selftest_bounded_wait(limit_ns: int, stream=None) -> None:
     """Make a bounded device wait run out (see gmlp_selftest_bounded_wait)."""
     _check(load().gmlp_selftest_bounded_wait(int(limit_ns), _stream(stream)))
+
+
+def mma_peak(fmt: int, scale_copy: bool, iters: int, ctas: int = 0, stream=None) -> None:
+    """Launch the tensor-core ceiling loop (see gmlp_mma_peak); asynchronous."""
+    _check(load().gmlp_mma_peak(int(fmt), int(bool(scale_copy)), int(iters), int(ctas), _stream(stream)))
+
+
+def mma_peak_flops(fmt: int, iters: int, ctas: int) -> float:
+    """Floating-point operations of one gmlp_mma_peak launch."""
+    k = 32 if fmt == MXFP8 else 64
+    return float(ctas) * iters * 4 * 2 * 128 * 256 * k
 
 
 def check_device_status(stream=None) -> None:

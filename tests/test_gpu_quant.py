@@ -184,3 +184,24 @@ def test_bounded_wait_times_out_and_reports(gm):
     pre, post = gm.group_hadamard_amax(x, torch.tensor([32]).cuda(), 0)
     gm.check_device_status()
     assert pre.item() == 1.0 and post.item() == 4.0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_mma_peak_loop_runs_at_a_plausible_rate(gm, fmt):
+    """The tensor-core ceiling loop completes, reports no device error and runs
+    at a rate between a fifth of and just above the nominal dense peak (FP8
+    4.5 PFLOP/s, FP4 13.5 PFLOP/s): far above would mean it skips work."""
+    nominal = 4500.0 if fmt == gm.MXFP8 else 13500.0
+    ctas = torch.cuda.get_device_properties(0).multi_processor_count
+    for copy in (True, False):
+        gm.mma_peak(fmt, copy, 256)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        gm.mma_peak(fmt, copy, 8192)
+        e1.record()
+        torch.cuda.synchronize()
+        gm.check_device_status()
+        tflops = gm.mma_peak_flops(fmt, 8192, ctas) / (e0.elapsed_time(e1) * 1e-3) / 1e12
+        assert nominal / 5 < tflops < nominal * 1.1, (copy, tflops)
