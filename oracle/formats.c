@@ -184,9 +184,12 @@ float orc_nvfp4_global_scale(float amax) {
 /* One 1x16 NVFP4 block of FP32 values v under global scale S:
  *   b   = max |v_i|
  *   t   = fp32(fp32(b / 6) * S),  sf = E4M3(t)            (block scale byte)
- *   enc = sf == 0 ? 0 : fp32(S / sf)
+ *   enc = sf == 0 ? 0 : min(fp32(S / sf), FLT_MAX)
  *   q_i = E2M1(fp32(v_i * enc))                           (codes)
- * Codes are packed two per byte, the even element in the low nibble. */
+ * Codes are packed two per byte, the even element in the low nibble.  The
+ * encode factor saturates at FLT_MAX as S does (reading: the format has no
+ * infinities, so a zero element stays zero when S / sf overflows; this only
+ * happens when the group amax is below ~1e-35). */
 void orc_nvfp4_quantize_block(const float* v, float S, uint8_t* codes8, uint8_t* sf_out) {
   float b = 0.0f;
   for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(v[i]));
@@ -195,6 +198,7 @@ void orc_nvfp4_quantize_block(const float* v, float S, uint8_t* codes8, uint8_t*
   uint8_t sf = orc_e4m3_encode((double)t);
   float sfv = (float)orc_e4m3_decode(sf);
   float enc = (sfv == 0.0f) ? 0.0f : S / sfv;
+  if (isinf(enc)) enc = FLT_MAX;
   for (int i = 0; i < 16; i += 2) {
     float p0 = v[i] * enc;
     float p1 = v[i + 1] * enc;

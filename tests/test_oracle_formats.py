@@ -215,6 +215,22 @@ def test_nvfp4_block_exact_values(orc):
     assert nib[0] == 0 and nib[-1] == 0
 
 
+def test_nvfp4_encode_factor_saturates(orc):
+    """S = FLT_MAX (group amax below 2688 / FLT_MAX) and a block max b = 2^-126
+    give t = fp32(b / 6) * FLT_MAX ~ 0.667 -> sf = E4M3 0.6875 (0x33), and
+    S / sf overflows; the encode factor stays at FLT_MAX, so zeros encode to
+    zero with their sign and the other values by their finite products
+    (b -> 4.0, b / 2 -> 2.0, 2^-140 -> 2.4e-4 -> 0)."""
+    fmax = np.float32(np.finfo(np.float32).max)
+    b = np.float32(2.0 ** -126)
+    tiny = np.float32(2.0 ** -140)
+    vals = np.array([b, 0.0, -0.0, -b, tiny, -tiny, b / 2, 0.0] + [0.0] * 8, np.float32)
+    codes, sf = orc.nvfp4_quantize_block(vals, fmax)
+    assert sf == 0x33
+    nib = (np.stack([codes & 15, codes >> 4], axis=1).reshape(-1)).tolist()
+    assert nib[:8] == [6, 0, 8, 14, 0, 8, 4, 0]
+
+
 @pytest.mark.parametrize("amax_level", [1.0, 2.0, 4.0])
 def test_nvfp4_lossless_set(orc, amax_level):
     """Entries in {0, +-1, +-2, +-4} with group amax 4 round-trip exactly for any block maximum."""
