@@ -85,16 +85,6 @@ __device__ __forceinline__ float nvfp4_global_scale(float amax) {
   return isinf(S) ? 3.402823466e38f : S;
 }
 
-// NVFP4 block encode factor from the block max b under global scale S:
-// t = (b / 6) * S, sf = E4M3(t) (returned in *sf_byte), enc = S / sf (0 if sf == 0).
-__device__ __forceinline__ float nvfp4_block_encode(float b, float S, uint32_t* sf_byte) {
-  float t = __fmul_rn(__fdiv_rn(b, 6.0f), S);
-  uint32_t sf = e4m3x2(t, 0.0f) & 0xFF;
-  *sf_byte = sf;
-  float sfv = e4m3_to_float(sf);
-  return sfv == 0.0f ? 0.0f : __fdiv_rn(S, sfv);
-}
-
 // ----------------------------------------------------------------- dependent launch
 
 // Wait until the preceding kernel in the stream (launched before this one with

@@ -141,105 +141,263 @@ __device__ __forceinline__ int find_unit_group(const SmemGroups& t, int G, int64
 
 // ------------------------------------------------------------------ rowwise cast
 
-// One warp per row (contiguous row ranges per warp); lane l takes 16-byte
-// chunks l, l+32, ... of the row.  MXFP8: 4 lanes per 32-element block;
-// NVFP4: 2 lanes per 16-element block.
+// E4M3 scale byte of an NVFP4 block with max b under global scale S:
+// E4M3(fp32(fp32(b / 6) * S)).
+__device__ __forceinline__ uint32_t nvfp4_block_sf(float b, float S) {
+  return e4m3x2(__fmul_rn(__fdiv_rn(b, 6.0f), S), 0.0f) & 0xFF;
+}
+
+// NVFP4 encode factor for block scale byte c under global scale S:
+// fp32(S / E4M3(c)), saturated at FLT_MAX as S is (0 for c = 0).
+__device__ __forceinline__ float nvfp4_enc(float S, uint32_t c) {
+  return (c == 0 || c == 127) ? 0.0f : fminf(__fdiv_rn(S, e4m3_to_float(c)), 3.402823466e38f);
+}
+
+// enc[c] for every scale byte c a block can take: the block encode's IEEE
+// division, once per code.
+__device__ __forceinline__ void fill_enc_table(float* enc, float S, int tid) {
+  if (tid < 128) enc[tid] = nvfp4_enc(S, (uint32_t)tid);
+}
+
+// Eight FP32 values (already multiplied by the encode factor) -> four E2M1
+// code bytes packed into one word, element 0 in the low nibble.
+__device__ __forceinline__ uint32_t e2m1_pack8(const float* p) {
+  uint32_t w;
+  asm("{\n .reg .b8 q0, q1, q2, q3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n"
+      " mov.b32 %0, {q0, q1, q2, q3};\n}"
+      : "=r"(w)
+      : "f"(p[0]), "f"(p[1]), "f"(p[2]), "f"(p[3]), "f"(p[4]), "f"(p[5]), "f"(p[6]), "f"(p[7]));
+  return w;
+}
+
+
+// Packed pairs of FP32 (two columns side by side); each lane of the pair is an
+// IEEE round-to-nearest-even operation, identical to the scalar one.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float a, float b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float lo2(f32x2 v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return a;
+}
+__device__ __forceinline__ float hi2(f32x2 v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return b;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// max(|a|, |b|) on packed bf16 pairs (sign bits set to the xor of the inputs'
+// signs; a NaN operand yields the other one).
+__device__ __forceinline__ uint32_t bmax_abs2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Max |x| over the 8 bf16 values of v as a bf16 bit pattern (0..0x7f80):
+// NaN values are ignored and a chunk of eight NaNs gives 0, as a chain of
+// fmaxf starting from 0 would.
+__device__ __forceinline__ uint32_t amax8_bits(const uint4& v) {
+  uint32_t m = bmax_abs2(bmax_abs2(v.x, v.y), bmax_abs2(v.z, v.w));
+  m = bmax_abs2(m, __byte_perm(m, 0, 0x1032)) & 0x7fffu;
+  return m > 0x7f80u ? 0u : m;
+}
+
+// Four FP32 values -> four E4M3 bytes (element 0 in the low byte).
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n .reg .b16 lo, hi;\n cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n mov.b32 %0, {lo, hi};\n}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+
+// The 8 bf16 values of v (element 2i in the low half of word i) as four
+// packed FP32 pairs multiplied by m: exact bf16 -> FP32 widening, then one
+// IEEE round-to-nearest-even product per element.
+__device__ __forceinline__ void scale8(const uint4& v, float m, float* q) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const f32x2 m2 = pk2(m, m);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const f32x2 p = mul2(pk2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u)), m2);
+    q[2 * i] = lo2(p);
+    q[2 * i + 1] = hi2(p);
+  }
+}
+
+// Bytes of lanes l, l+s, l+2s, l+3s packed into one word (valid in lanes
+// whose l+3s stays inside the warp).
+__device__ __forceinline__ uint32_t gather4_bytes(uint32_t byte, int s) {
+  const uint32_t pair = byte | (__shfl_down_sync(0xffffffffu, byte, s) << 8);
+  return pair | (__shfl_down_sync(0xffffffffu, pair, 2 * s) << 16);
+}
+
+// Work every launch of the row quantiser does first: the zeroing requests and
+// the per-group global scales (block 0 only).
+__device__ __forceinline__ void row_quant_setup(const RowQuantArgs& a, int nthreads) {
+  if (blockIdx.x != 0) return;
+  if (a.zero_ptr)
+    for (int i = threadIdx.x; i < a.zero_count; i += nthreads) a.zero_ptr[i] = 0.0f;
+  if (a.zero_ptr2)
+    for (int i = threadIdx.x; i < a.zero_count2; i += nthreads) a.zero_ptr2[i] = 0.0f;
+  if (a.S_out)
+    for (int g = threadIdx.x; g < a.grp.G; g += nthreads) a.S_out[g] = nvfp4_global_scale(a.amax[g]);
+}
+
+// E4M3 scale byte of an NVFP4 block whose max |x| is the bf16 value with bits
+// m (0..0x7f80), under global scale S: E4M3(fp32(fp32(b / 6) * S)).  The
+// quotient fp32(b / 6) comes from q1 = fp32(b * fp32(1/6)) and one residual
+// correction fp32(fma(fma(-6, q1, b), fp32(1/6), q1)); for every finite bf16
+// b this equals the IEEE quotient (checked exhaustively over all 2^15
+// magnitudes), and b = inf keeps inf.
+__device__ __forceinline__ uint32_t nvfp4_block_sf_bf16(uint32_t m, float S) {
+  const float b = __uint_as_float(m << 16);
+  const float r6 = __uint_as_float(0x3e2aaaabu);  // fp32(1/6)
+  const float q1 = __fmul_rn(b, r6);
+  const float q = m >= 0x7f80u ? b : __fmaf_rn(__fmaf_rn(-6.0f, q1, b), r6, q1);
+  return e4m3x2(__fmul_rn(q, S), 0.0f) & 0xFF;
+}
+
+// One pass of the row quantiser: lane l takes chunks c0+l, c0+l+32, ...,
+// c0+l+96 of the row (FULL: all inside the row, no per-lane checks).  MXFP8
+// blocks (32 elements) span 4 lanes, NVFP4 blocks (16) span 2; four
+// consecutive blocks' scale bytes go out as one word from lanes 0/16 (MXFP8)
+// or 0/8/16/24 (NVFP4).
+template <int FMT, bool FULL>
+__device__ __forceinline__ void row_pass(const RowQuantArgs& a, const uint4* xr, uint8_t* crow, uint8_t* srow,
+                                         int c0, int cpr, int lane, float S, const float* enc) {
+  constexpr int U = 4;
+  uint4 v[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int c = c0 + 32 * u + lane;
+    v[u] = (FULL || c < cpr) ? ld_stream(xr + c) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int c = c0 + 32 * u + lane;
+    const bool active = FULL || c < cpr;
+    uint32_t m = amax8_bits(v[u]);
+    if (FMT == GMLP_MXFP8) {
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      const int e = max((int)(m >> 7) - 135, -127);  // floor(log2 amax) - 8 from the bf16 exponent
+      float q[8];
+      scale8(v[u], exp2_neg(e), q);
+      const uint32_t word = gather4_bytes((uint32_t)(e + 127), 4);
+      if (active) {
+        *reinterpret_cast<uint2*>(crow + c * 8) =
+            make_uint2(e4m3x4(q[0], q[1], q[2], q[3]), e4m3x4(q[4], q[5], q[6], q[7]));
+        if ((lane & 15) == 0) *reinterpret_cast<uint32_t*>(srow + (a.tiled ? (c >> 4) * 512 : (c >> 2))) = word;
+      }
+    } else {
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      const uint32_t sf = nvfp4_block_sf_bf16(m, S);
+      float q[8];
+      scale8(v[u], enc[sf], q);
+      const uint32_t word = gather4_bytes(sf, 2);
+      if (active) {
+        *reinterpret_cast<uint32_t*>(crow + c * 4) = e2m1_pack8(q);
+        if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(srow + (a.tiled ? (c >> 3) * 512 : (c >> 1))) = word;
+      }
+    }
+  }
+}
+
+// Row quantiser.  The rows are cut into passes of 128 16-byte chunks (the last
+// pass of a row may be shorter); warp w takes an equal contiguous share of
+// the passes.  NVFP4 encode factors S / E4M3(sf) come from a per-warp table
+// of the current group.
 template <int FMT>
 __global__ void __launch_bounds__(kThreads) row_quant_kernel(RowQuantArgs a) {
   __shared__ SmemGroups t;
+  __shared__ float enc_tab[FMT == GMLP_NVFP4 ? kWarps : 1][128];
   build_group_tables(a.grp, 1, t);
   griddep_wait();
   griddep_launch_dependents();
   if (t.bad) return;
+  row_quant_setup(a, kThreads);
   const int G = a.grp.G;
-  if (blockIdx.x == 0) {
-    if (a.zero_ptr)
-      for (int i = threadIdx.x; i < a.zero_count; i += kThreads) a.zero_ptr[i] = 0.0f;
-    if (a.zero_ptr2)
-      for (int i = threadIdx.x; i < a.zero_count2; i += kThreads) a.zero_ptr2[i] = 0.0f;
-    if (a.S_out)
-      for (int g = threadIdx.x; g < G; g += kThreads) a.S_out[g] = nvfp4_global_scale(a.amax[g]);
-  }
   const int64_t K = a.K;
-  const int nch = (int)(K / 8);
+  const int cpr = (int)(K / 8);            // 16-byte chunks per row
+  const int ppr = (cpr + 127) / 128;       // passes per row
   const int nscale = (int)(FMT == GMLP_MXFP8 ? K / 32 : K / 16);
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, wib = threadIdx.x / 32;
   const int64_t rows = t.off[G];
   const int64_t warps = (int64_t)gridDim.x * kWarps;
-  const int64_t w = (int64_t)blockIdx.x * kWarps + threadIdx.x / 32;
-  const int64_t rpw = (rows + warps - 1) / warps;
-  const int64_t r0 = w * rpw, r1 = min(rows, r0 + rpw);
-  if (r0 >= r1) return;
-  int g = find_group(t, G, r0);
-  constexpr int U = 4;
-  for (int64_t r = r0; r < r1; ++r) {
+  const int64_t w = (int64_t)blockIdx.x * kWarps + wib;
+  const int64_t P = rows * ppr;
+  const int64_t p0 = P * w / warps, p1 = P * (w + 1) / warps;
+  if (p0 >= p1) return;
+  float* enc = enc_tab[FMT == GMLP_NVFP4 ? wib : 0];
+  int r = (int)(p0 / ppr), j = (int)(p0 - (int64_t)r * ppr);  // row and pass within the row
+  int g = find_group(t, G, r);
+  int g_tab = -1;
+  float S = 0.0f;
+  for (int64_t p = p0; p < p1; ++p, ++j) {
+    if (j == ppr) {
+      j = 0;
+      ++r;
+    }
+    const int c0 = j * 128;
     while (t.off[g + 1] <= r) ++g;
     int64_t src = r;
     if (a.swiglu_interleave) {
-      const int p = (int)(r - t.off[g]);
+      const int pr = r - t.off[g];
       const int half = (t.off[g + 1] - t.off[g]) >> 1;
-      const int c = p >> 6, i = p & 63;
+      const int c = pr >> 6, i = pr & 63;
       src = t.off[g] + (i < 32 ? 32 * c + i : half + 32 * c + (i - 32));
     }
-    const uint4* xr = reinterpret_cast<const uint4*>(a.x + src * K);
-    float S = 0.0f;
-    if (FMT == GMLP_NVFP4) S = nvfp4_global_scale(a.amax[g]);
-    for (int c0 = 0; c0 < nch; c0 += 32 * U) {
-      uint4 v[U];
+    if (FMT == GMLP_NVFP4 && g != g_tab) {
+      S = nvfp4_global_scale(a.amax[g]);
+      __syncwarp();
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int c = c0 + 32 * u + lane;
-        v[u] = c < nch ? ld_stream(xr + c) : make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < 4; ++i) {
+        const int c = lane + 32 * i;
+        enc[c] = nvfp4_enc(S, (uint32_t)c);
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int c = c0 + 32 * u + lane;
-        float f[8];
-        unpack8(v[u], f);
-        float am = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
-        if (FMT == GMLP_MXFP8) {
-          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-          const int e = mxfp8_exponent(am);
-          const float mul = exp2_neg(e);
-          uint32_t w0 = e4m3x2(__fmul_rn(f[0], mul), __fmul_rn(f[1], mul)) |
-                        (e4m3x2(__fmul_rn(f[2], mul), __fmul_rn(f[3], mul)) << 16);
-          uint32_t w1 = e4m3x2(__fmul_rn(f[4], mul), __fmul_rn(f[5], mul)) |
-                        (e4m3x2(__fmul_rn(f[6], mul), __fmul_rn(f[7], mul)) << 16);
-          // scale bytes of 4 consecutive blocks (lanes 0,4,8,12 and 16,..,28) go out as one word
-          const uint32_t sb = (uint32_t)(e + 127);
-          const int lb = lane & 16;
-          const uint32_t word = __shfl_sync(0xffffffffu, sb, lb) | (__shfl_sync(0xffffffffu, sb, lb + 4) << 8) |
-                                (__shfl_sync(0xffffffffu, sb, lb + 8) << 16) |
-                                (__shfl_sync(0xffffffffu, sb, lb + 12) << 24);
-          if (c < nch) {
-            *reinterpret_cast<uint2*>(a.codes + r * K + (int64_t)c * 8) = make_uint2(w0, w1);
-            if ((lane & 15) == 0)
-              *reinterpret_cast<uint32_t*>(a.scales + scale_offset(a.tiled, t, g, r, c >> 2, nscale)) = word;
-          }
-        } else {
-          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-          uint32_t sf;
-          const float enc = nvfp4_block_encode(am, S, &sf);
-          uint32_t word = 0;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            word |= e2m1x2(__fmul_rn(f[2 * i], enc), __fmul_rn(f[2 * i + 1], enc)) << (8 * i);
-          // scale bytes of 4 consecutive blocks (lanes 8k, 8k+2, 8k+4, 8k+6) go out as one word
-          const int lb = lane & 24;
-          const uint32_t sw = __shfl_sync(0xffffffffu, sf, lb) | (__shfl_sync(0xffffffffu, sf, lb + 2) << 8) |
-                              (__shfl_sync(0xffffffffu, sf, lb + 4) << 16) |
-                              (__shfl_sync(0xffffffffu, sf, lb + 6) << 24);
-          if (c < nch) {
-            *reinterpret_cast<uint32_t*>(a.codes + r * (K / 2) + (int64_t)c * 4) = word;
-            if ((lane & 7) == 0)
-              *reinterpret_cast<uint32_t*>(a.scales + scale_offset(a.tiled, t, g, r, c >> 1, nscale)) = sw;
-          }
-        }
-      }
+      __syncwarp();
+      g_tab = g;
     }
+    // scale-word address of the row: tiled (128-row tile, 512-byte blocks of
+    // 4 scales x 128 rows) or compact [rows][nscale]
+    uint8_t* srow;
+    if (a.tiled) {
+      const int lr = r - t.off[g];
+      const int rr = lr & 127;
+      srow = a.scales + (int64_t)(t.tb[g] + (lr >> 7)) * (nscale >> 2) * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
+    } else {
+      srow = a.scales + (int64_t)r * nscale;
+    }
+    const uint4* xr = reinterpret_cast<const uint4*>(a.x + src * K);
+    uint8_t* crow = a.codes + (int64_t)r * (FMT == GMLP_MXFP8 ? K : K / 2);
+    if (c0 + 128 <= cpr)
+      row_pass<FMT, true>(a, xr, crow, srow, c0, cpr, lane, S, enc);
+    else
+      row_pass<FMT, false>(a, xr, crow, srow, c0, cpr, lane, S, enc);
   }
 }
 
@@ -262,13 +420,13 @@ __global__ void __launch_bounds__(kThreads) group_amax_kernel(const uint16_t* x,
   const int64_t r0 = w * rpw, r1 = min(rows, r0 + rpw);
   if (r0 >= r1) return;
   int g = find_group(t, G, r0);
-  float m = 0.0f;
-  constexpr int U = 4;
+  uint32_t m = 0;  // running max |x| as bf16 bits (non-negative, so integer order is value order)
+  constexpr int U = 8;
   for (int64_t r = r0; r < r1; ++r) {
     if (t.off[g + 1] <= r) {
-      m = warp_max(m);
-      if (lane == 0) atomic_max_nonneg(amax + g, m);
-      m = 0.0f;
+      const float mf = warp_max(__uint_as_float(m << 16));
+      if (lane == 0) atomic_max_nonneg(amax + g, mf);
+      m = 0;
       while (t.off[g + 1] <= r) ++g;
     }
     const uint4* xr = reinterpret_cast<const uint4*>(x + r * K);
@@ -280,16 +438,11 @@ __global__ void __launch_bounds__(kThreads) group_amax_kernel(const uint16_t* x,
         v[u] = c < nch ? ld_stream(xr + c) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float f[8];
-        unpack8(v[u], f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
-      }
+      for (int u = 0; u < U; ++u) m = max(m, amax8_bits(v[u]));
     }
   }
-  m = warp_max(m);
-  if (lane == 0) atomic_max_nonneg(amax + g, m);
+  const float mf = warp_max(__uint_as_float(m << 16));
+  if (lane == 0) atomic_max_nonneg(amax + g, mf);
 }
 
 // ------------------------------------------------------------------ Hadamard helpers
@@ -412,68 +565,6 @@ __global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const uint16_t*
 constexpr int kTileR = 64, kTileC = 256, kChunks = kTileR / 16;
 constexpr size_t kColSmem = (size_t)kTileR * kTileC * 2 + kTileC * 8 * kChunks + kTileC * kChunks;
 
-// E4M3 scale byte of an NVFP4 block with max b under global scale S:
-// E4M3(fp32(fp32(b / 6) * S)).
-__device__ __forceinline__ uint32_t nvfp4_block_sf(float b, float S) {
-  return e4m3x2(__fmul_rn(__fdiv_rn(b, 6.0f), S), 0.0f) & 0xFF;
-}
-
-// enc[c] = fp32(S / E4M3(c)) for every scale byte c a block can take (0 -> 0):
-// the same IEEE division the block encode performs, once per code.
-__device__ __forceinline__ void fill_enc_table(float* enc, float S, int tid) {
-  if (tid < 128) {
-    const float sv = e4m3_to_float((uint32_t)tid);
-    enc[tid] = (tid == 0 || tid == 127) ? 0.0f : __fdiv_rn(S, sv);
-  }
-}
-
-// Eight FP32 values (already multiplied by the encode factor) -> four E2M1
-// code bytes packed into one word, element 0 in the low nibble.
-__device__ __forceinline__ uint32_t e2m1_pack8(const float* p) {
-  uint32_t w;
-  asm("{\n .reg .b8 q0, q1, q2, q3;\n"
-      " cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n"
-      " cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n"
-      " mov.b32 %0, {q0, q1, q2, q3};\n}"
-      : "=r"(w)
-      : "f"(p[0]), "f"(p[1]), "f"(p[2]), "f"(p[3]), "f"(p[4]), "f"(p[5]), "f"(p[6]), "f"(p[7]));
-  return w;
-}
-
-
-// Packed pairs of FP32 (two columns side by side); each lane of the pair is an
-// IEEE round-to-nearest-even operation, identical to the scalar one.
-typedef unsigned long long f32x2;
-__device__ __forceinline__ f32x2 pk2(float a, float b) {
-  f32x2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ float lo2(f32x2 v) {
-  float a, b;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-  return a;
-}
-__device__ __forceinline__ float hi2(f32x2 v) {
-  float a, b;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-  return b;
-}
-__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
-  f32x2 r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
-  f32x2 r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
-  f32x2 r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
 
 // 16 values -> 8 bytes of E2M1 codes (even element in the low nibble)
 __device__ __forceinline__ uint2 e2m1_pack16(const float* v, float enc) {

@@ -53,8 +53,10 @@ def gpu_call(gm, fn, *a, **k):
     return out
 
 
+# K = 128, 384: rows shorter than one 128-chunk pass; 1152: one full pass and a
+# ragged one; 2048: full passes only
 @pytest.mark.parametrize("layout", [0, 1], ids=["compact", "tiled"])
-@pytest.mark.parametrize("K", [128, 384])
+@pytest.mark.parametrize("K", [128, 384, 1152, 2048])
 @pytest.mark.parametrize("case", list(SPLITS))
 def test_mxfp8_rowwise_bitexact(orc, gm, case, K, layout):
     splits = np.array(SPLITS[case], dtype=np.int64)
@@ -69,10 +71,11 @@ def test_mxfp8_rowwise_bitexact(orc, gm, case, K, layout):
 
 
 @pytest.mark.parametrize("layout", [0, 1], ids=["compact", "tiled"])
+@pytest.mark.parametrize("K", [256, 1152, 2048])
 @pytest.mark.parametrize("case", list(SPLITS))
-def test_nvfp4_rowwise_bitexact(orc, gm, case, layout):
+def test_nvfp4_rowwise_bitexact(orc, gm, case, K, layout):
     splits = np.array(SPLITS[case], dtype=np.int64)
-    M, K = int(splits.sum()), 256
+    M = int(splits.sum())
     x = rich_x(M, K, seed=7 + len(splits))
     out = gpu_call(gm, gm.group_quantize, x.cuda(), torch.from_numpy(splits).cuda(),
                    gm.recipe(gm.NVFP4, layout=layout))
@@ -82,6 +85,32 @@ def test_nvfp4_rowwise_bitexact(orc, gm, case, layout):
     sc = np_u8(out["row"][1])
     got = orc.tiled_to_compact(sc, splits, K // 16) if layout else sc[:M * K // 16].reshape(M, K // 16)
     assert np.array_equal(got, ref["row_scales"])
+
+
+def test_nvfp4_rowwise_every_bf16_block_max(orc, gm):
+    """Every positive finite bf16 magnitude is the max of one 16-element block
+    (one row of 128 consecutive magnitudes per group, so the block scales span
+    the E4M3 range); codes, scales and amaxes bit-exact."""
+    K = 2048
+    pats = np.arange(1, 0x7F80, dtype=np.uint32)
+    M = -(-len(pats) // (K // 16))
+    pats = np.concatenate([pats, np.full(M * (K // 16) - len(pats), 0x3F80, np.uint32)])
+    rng = np.random.default_rng(11)
+    top = (pats << 16).view(np.float32).astype(np.float64)
+    x = top[:, None] * rng.uniform(0.0, 1.0, (len(pats), 16))
+    x[:, 0] = top
+    x *= rng.choice([-1.0, 1.0], x.shape)
+    xt = bf16_cpu(x.reshape(M, K))
+    splits = np.ones(M, dtype=np.int64)
+    for lo in range(0, M, 512):  # at most 512 groups per call
+        part = xt[lo:lo + 512]
+        sp = splits[lo:lo + 512]
+        m = part.shape[0]
+        out = gpu_call(gm, gm.group_quantize, part.cuda(), torch.from_numpy(sp).cuda(), gm.recipe(gm.NVFP4, layout=0))
+        ref = orc.group_quantize(bits(part), sp, orc.NVFP4)
+        assert np.array_equal(out["amax_pre"].cpu().numpy(), ref["amax_pre"])
+        assert np.array_equal(np_u8(out["row"][0], m * K // 2).reshape(m, K // 2), ref["row_codes"])
+        assert np.array_equal(np_u8(out["row"][1])[:m * K // 16].reshape(m, K // 16), ref["row_scales"])
 
 
 @pytest.mark.parametrize("mask", [0, 0xFFFF, 0x5A3C, 0x8001])
