@@ -99,7 +99,11 @@ typedef enum gmlp_status {
 
 typedef enum gmlp_format { GMLP_MXFP8 = 0, GMLP_NVFP4 = 1 } gmlp_format;
 typedef enum gmlp_act { GMLP_ACT_SWIGLU = 0, GMLP_ACT_SRELU = 1 } gmlp_act;
-typedef enum gmlp_scale_layout { GMLP_SCALES_COMPACT = 0, GMLP_SCALES_GEMM_TILED = 1 } gmlp_scale_layout;
+typedef enum gmlp_scale_layout {
+  GMLP_SCALES_COMPACT = 0,
+  GMLP_SCALES_GEMM_TILED = 1,
+  GMLP_SCALES_GEMM_TILED_X4 = 2 /* NVFP4 weights only: see gmlp_replicate_weight_scales */
+} gmlp_scale_layout;
 
 /* Quantisation recipe (PR #3631 Changes, the recipe preconditions; PR #3837,
  * rht_sign_mask).  MXFP8 always uses E4M3 (E5M2 gradients are not a forward
@@ -164,6 +168,21 @@ GMLP_API gmlp_status gmlp_group_quantize(const uint16_t* x, int64_t M, int64_t K
                                 const gmlp_qtensor* row_out, const gmlp_qtensor* col_out,
                                 float* amax_pre, float* amax_post, gmlp_stream stream);
 
+/* gmlp_replicate_weight_scales -- GEMM_TILED_X4 copy of NVFP4 weight scales
+ * (no counterpart on the pages: a layout for this GEMM).  `tiled` holds the
+ * GEMM_TILED scales of G experts of `rows` rows (from gmlp_prepare_weights,
+ * cols/16 scale columns, so runs of 4 columns R = cols/64 and stages of 4 runs
+ * KB = cols/256).  For tile pair P (tiles 2P, 2P+1 of the stacked experts),
+ * stage kb < KB and run k < 4, `out` holds at byte ((P * KB + kb) * 4 + k) *
+ * 4096 the 512-byte block (tile 2P, run 4kb+k) four times, then the block
+ * (tile 2P+1, run 4kb+k) four times: the image the GEMM copies into tensor
+ * memory with one 128-row copy per MMA instead of two.  out: 4 * G * rows *
+ * (cols / 16) bytes, device, 16-byte aligned; neither buffer is kept.  Limits: rows % 256 == 0, cols % 256 == 0.
+ * gmlp_forward reads it when a weight's scale_layout is GEMM_TILED_X4 (not in
+ * CTA-pair mode). */
+GMLP_API gmlp_status gmlp_replicate_weight_scales(const uint8_t* tiled, int32_t G, int64_t rows, int64_t cols,
+                                                  uint8_t* out, gmlp_stream stream);
+
 /* Quantised stacked expert weights (PR #2769: single grouped weight, the
  * b_tensor of the FC1 / FC2 kernels).  Produced by gmlp_prepare_weights. */
 typedef struct gmlp_qweight {
@@ -175,7 +194,8 @@ typedef struct gmlp_qweight {
   int32_t G;
   int32_t format;             /* gmlp_format */
   int32_t swiglu_interleaved; /* 1: rows hold the SwiGLU gate/up interleave below */
-  int32_t reserved;
+  int32_t scale_layout;       /* layout of `scales`: 0 or GMLP_SCALES_GEMM_TILED, or (NVFP4)
+                                 GMLP_SCALES_GEMM_TILED_X4 from gmlp_replicate_weight_scales */
 } gmlp_qweight;
 
 /* gmlp_prepare_weights -- per-expert quantisation of stacked bf16 weights W

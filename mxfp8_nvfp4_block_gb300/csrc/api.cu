@@ -342,6 +342,14 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
                 (long long)W2->cols, (long long)K, (long long)N);
   if ((W1->swiglu_interleaved != 0) != (act == GMLP_ACT_SWIGLU) || W2->swiglu_interleaved)
     return fail(GMLP_ERR_INVALID_ARG, "W1 must be SwiGLU-interleaved exactly for SwiGLU; W2 never");
+  for (const gmlp_qweight* W : {W1, W2})
+    if (!(W->scale_layout == 0 || W->scale_layout == GMLP_SCALES_GEMM_TILED ||
+          (W->scale_layout == GMLP_SCALES_GEMM_TILED_X4 && fmt == GMLP_NVFP4)))
+      return fail(GMLP_ERR_INVALID_ARG, "weight scale_layout %d: GEMM_TILED, or GEMM_TILED_X4 for NVFP4",
+                  W->scale_layout);
+  const bool x4_1 = W1->scale_layout == GMLP_SCALES_GEMM_TILED_X4, x4_2 = W2->scale_layout == GMLP_SCALES_GEMM_TILED_X4;
+  if (aux && aux->gemm_mode == 2 && (x4_1 || x4_2))
+    return fail(GMLP_ERR_INVALID_ARG, "gemm_mode 2 (CTA pairs) reads GEMM_TILED weight scales, not GEMM_TILED_X4");
   if (!W1->codes || !W1->scales || !W2->codes || !W2->scales || !aligned16(W1->codes) || !aligned16(W1->scales) ||
       !aligned16(W2->codes) || !aligned16(W2->scales))
     return fail(GMLP_ERR_INVALID_ARG, "weight codes/scales NULL or not 16-byte aligned");
@@ -469,6 +477,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   g1.grp = gs;
   g1.a_amax = x_amax;
   g1.b_S = W1->global_scale;
+  g1.b_x4 = x4_1;
   g1.probs = probs;
   g1.out_bf16 = f_bf16;
   g1.amax_pre = f_pre;
@@ -507,6 +516,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   g2.grp = gs;
   g2.a_amax = f_pre;
   g2.b_S = W2->global_scale;
+  g2.b_x4 = x4_2;
   g2.out_bf16 = y;
   g2.n_cols_out = K;
     g2.pair = (aux && aux->gemm_mode == 2) ? 2 : 1;
@@ -522,6 +532,20 @@ gmlp_status gmlp_selftest_bounded_wait(uint64_t limit_ns, gmlp_stream stream) {
     return fail(GMLP_ERR_INVALID_ARG, "limit_ns %llu outside [1 us, 2 s]", (unsigned long long)limit_ns);
   GMLP_TRY(check_device());
   GMLP_CUDA(launch_selftest_wait(limit_ns, (cudaStream_t)stream), "selftest launch");
+  return GMLP_OK;
+}
+
+gmlp_status gmlp_replicate_weight_scales(const uint8_t* tiled, int32_t G, int64_t rows, int64_t cols, uint8_t* out,
+                                         gmlp_stream stream) {
+  g_last_error[0] = 0;
+  if (!tiled || !out || !aligned16(tiled) || !aligned16(out))
+    return fail(GMLP_ERR_INVALID_ARG, "tiled / out NULL or not 16-byte aligned");
+  if (G < 1 || G > kMaxGroups || rows <= 0 || cols <= 0 || rows % 256 || cols % 256)
+    return fail(GMLP_ERR_INVALID_DIMS, "G = %d, rows = %lld, cols = %lld: need 1 <= G <= %d, rows and cols %% 256 == 0",
+                G, (long long)rows, (long long)cols, kMaxGroups);
+  GMLP_TRY(check_device());
+  GMLP_CUDA(launch_replicate_scales(tiled, (int64_t)G * rows / 256, cols / 64, out, (cudaStream_t)stream),
+            "replicate launch");
   return GMLP_OK;
 }
 

@@ -230,6 +230,12 @@ __device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// Copy 128 rows x 32 bytes of shared memory into TMEM: row i -> lane i,
+// columns taddr .. taddr + 7.
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Block-scaled MMAs, D(tmem) (+)= A(smem) * B(smem)^T with per-block scales in TMEM.
 __device__ __forceinline__ void tc_mma_mxf8(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t sfa, uint32_t sfb, uint32_t accumulate) {

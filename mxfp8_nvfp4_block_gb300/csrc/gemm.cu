@@ -44,15 +44,23 @@ constexpr uint32_t kTmemCols = 512;
 // tile with cta_group::1 MMAs.  PAIR = 2: a CTA pair (cluster of 2) computes a
 // 256 x 256 tile with cta_group::2 MMAs; each CTA loads its own 128 A rows and
 // one 128-row half of the B tile, so each SM takes in a third fewer bytes.
-template <int FMT, int PAIR>
+//
+// X4 (NVFP4, single CTA): the B scales come replicated four times (weight
+// layout GEMM_TILED_X4), so one 128x256b copy places the scales of both
+// 128-row halves of the B tile for one MMA, replacing two 32x128b.warpx4
+// copies; each copy instruction costs the same tensor-pipe time whatever its
+// size, and NVFP4 needs 12 of the small ones per stage.  A stage is then
+// 66 KB, so 3 stages fit.
+template <int FMT, int PAIR, bool X4 = false>
 struct Cfg {
   // bytes of scale factors per 128 rows per stage: MXFP8 4 scales/row (one
   // 512-byte block), NVFP4 16 scales/row (four blocks)
   static constexpr int kSfBytes = FMT == GMLP_MXFP8 ? 512 : 2048;
+  static constexpr int kSfBBytes = X4 ? 8 * kSfBytes : 2 * kSfBytes;  // B scales per stage (both halves)
   static constexpr int kBRows = kBN / PAIR;                   // B rows held per CTA
   static constexpr int kBTileBytes = kBRows * kBKBytes;
-  static constexpr int kStageBytes = kATileBytes + kBTileBytes + 3 * kSfBytes;  // SFA + both SFB halves
-  static constexpr int kStages = PAIR == 1 ? 4 : (FMT == GMLP_MXFP8 ? 6 : 5);
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes + kSfBytes + kSfBBytes;
+  static constexpr int kStages = X4 ? 3 : PAIR == 1 ? 4 : (FMT == GMLP_MXFP8 ? 6 : 5);
   static constexpr uint32_t kSfCols = FMT == GMLP_MXFP8 ? 16 : 48;  // TMEM columns per stage
   static constexpr uint32_t kSfbOff = FMT == GMLP_MXFP8 ? 4 : 16;   // SFB after SFA within a stage
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes;
@@ -354,12 +362,12 @@ __device__ __forceinline__ void tc_mma_g(uint32_t d, uint64_t adesc, uint64_t bd
 
 // ------------------------------------------------------------------ kernel
 
-template <int FMT, int EPI, int PAIR>
+template <int FMT, int EPI, int PAIR, bool X4>
 __global__ void __launch_bounds__(kThreadsGemm, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const GemmArgs a) {
-  using C = Cfg<FMT, PAIR>;
+  using C = Cfg<FMT, PAIR, X4>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -367,7 +375,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   uint8_t* sB = sA + S * kATileBytes;
   uint8_t* sSFA = sB + S * C::kBTileBytes;
   uint8_t* sSFB = sSFA + S * C::kSfBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + S * 2 * C::kSfBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + S * C::kSfBBytes);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 1;
@@ -478,7 +486,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       const int32_t rowB = (int32_t)(rowB0 + rank * C::kBRows);
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
-        uint8_t* sfb = sSFB + stage * 2 * C::kSfBytes;
+        uint8_t* sfb = sSFB + stage * C::kSfBBytes;
         if (PAIR == 1) {
           mbar_arrive_expect_tx(&full[stage], kTx);
           armed |= 1u << stage;
@@ -487,9 +495,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           tma_load_2d(sB + stage * C::kBTileBytes, &tmB, kb * kBKBytes, rowB, &full[stage], pol_b);
           bulk_load(sSFA + stage * C::kSfBytes, a.a_scales + (tileA * KB + kb) * C::kSfBytes, C::kSfBytes,
                     &full[stage]);
-          bulk_load(sfb, a.b_scales + (tileB * KB + kb) * C::kSfBytes, C::kSfBytes, &full[stage]);
-          bulk_load(sfb + C::kSfBytes, a.b_scales + ((tileB + 1) * KB + kb) * C::kSfBytes, C::kSfBytes,
-                    &full[stage]);
+          if (X4) {
+            bulk_load(sfb, a.b_scales + ((tileB >> 1) * KB + kb) * C::kSfBBytes, C::kSfBBytes, &full[stage]);
+          } else {
+            bulk_load(sfb, a.b_scales + (tileB * KB + kb) * C::kSfBytes, C::kSfBytes, &full[stage]);
+            bulk_load(sfb + C::kSfBytes, a.b_scales + ((tileB + 1) * KB + kb) * C::kSfBytes, C::kSfBytes,
+                      &full[stage]);
+          }
         } else {
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), leader);
           if (rank == 0) {
@@ -534,11 +546,19 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         const uint32_t sA_addr = smem_u32(sA + stage * kATileBytes);
         const uint32_t sB_addr = smem_u32(sB + stage * C::kBTileBytes);
         const uint32_t sfa_addr = smem_u32(sSFA + stage * C::kSfBytes);
-        const uint32_t sfb_addr = smem_u32(sSFB + stage * 2 * C::kSfBytes);
+        const uint32_t sfb_addr = smem_u32(sSFB + stage * C::kSfBBytes);
         if (FMT == GMLP_MXFP8) {
           tc_cp_g<PAIR>(sfa_t, smem_desc(sfa_addr, 0, 128, 0));
           tc_cp_g<PAIR>(sfb_t, smem_desc(sfb_addr, 0, 128, 0));
           tc_cp_g<PAIR>(sfb_t + 4, smem_desc(sfb_addr + 512, 0, 128, 0));
+        } else if (X4) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            tc_cp_32x128b_x4(sfa_t + 4 * k, smem_desc(sfa_addr + 512 * k, 0, 128, 0));
+            // [4 x half-0 block | 4 x half-1 block]: 128 rows x 32 bytes, the two
+            // 16-byte column halves 2048 bytes apart, 8-row groups 128 apart
+            tc_cp_128x256b(sfb_t + 8 * k, smem_desc(sfb_addr + 4096 * k, 2048, 128, 0));
+          }
         } else {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -643,11 +663,11 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows
   return r == CUDA_SUCCESS;
 }
 
-template <int FMT, int EPI, int PAIR>
+template <int FMT, int EPI, int PAIR, bool X4 = false>
 cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
-  using C = Cfg<FMT, PAIR>;
+  using C = Cfg<FMT, PAIR, X4>;
   const size_t smem = C::kSmem + 1024 + 256 + 3 * (kMaxGroups + 1) * sizeof(int);
-  auto kern = gemm_kernel<FMT, EPI, PAIR>;
+  auto kern = gemm_kernel<FMT, EPI, PAIR, X4>;
   static bool attr_set[64] = {};
   static int max_units[64] = {};
   int dev = 0;
@@ -718,6 +738,11 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
     if (a.epi == EPI_FC1_SWIGLU) GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_SWIGLU);
     if (a.epi == EPI_FC1_SRELU) GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_SRELU);
     GMLP_LAUNCH(GMLP_MXFP8, EPI_FC2);
+  }
+  if (a.b_x4) {  // replicated B scales: single-CTA tiles only
+    if (a.epi == EPI_FC1_SWIGLU) return launch_t<GMLP_NVFP4, EPI_FC1_SWIGLU, 1, true>(a, s);
+    if (a.epi == EPI_FC1_SRELU) return launch_t<GMLP_NVFP4, EPI_FC1_SRELU, 1, true>(a, s);
+    return launch_t<GMLP_NVFP4, EPI_FC2, 1, true>(a, s);
   }
   if (a.epi == EPI_FC1_SWIGLU) GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SWIGLU);
   if (a.epi == EPI_FC1_SRELU) GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SRELU);

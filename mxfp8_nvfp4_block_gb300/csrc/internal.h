@@ -97,6 +97,7 @@ struct GemmArgs {
   float* amax_post;
   uint32_t rht_mask;
   int64_t n_cols_out;      // row length of the output (fc1: N; fc2: K)
+  int b_x4;                // NVFP4: b_scales in the replicated GEMM_TILED_X4 layout
   int pair;                // 2: CTA pairs (cta_group::2); otherwise single-CTA tiles
   int pdl;                 // launch as a programmatic dependent of the previous kernel
 };
@@ -106,6 +107,9 @@ int num_sms();
 
 cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_mma_peak(int format, bool scale_copy, int64_t iters, int ctas, cudaStream_t s);
+
+// NVFP4 weight scales: GEMM_TILED -> GEMM_TILED_X4 (see gmlp_replicate_weight_scales)
+cudaError_t launch_replicate_scales(const uint8_t* tiled, int64_t pairs, int64_t runs, uint8_t* out, cudaStream_t s);
 
 gmlp_status set_last_error(gmlp_status st, const char* msg);
 

@@ -286,9 +286,9 @@ __device__ __forceinline__ uint32_t nvfp4_block_sf_bf16(uint32_t m, float S) {
 // blocks (32 elements) span 4 lanes, NVFP4 blocks (16) span 2; four
 // consecutive blocks' scale bytes go out as one word from lanes 0/16 (MXFP8)
 // or 0/8/16/24 (NVFP4).
-template <int FMT, bool FULL>
-__device__ __forceinline__ void row_pass(const RowQuantArgs& a, const uint4* xr, uint8_t* crow, uint8_t* srow,
-                                         int c0, int cpr, int lane, float S, const float* enc) {
+template <int FMT, bool TILED, bool FULL>
+__device__ __forceinline__ void row_pass(const uint4* xr, uint8_t* crow, uint8_t* srow, int c0, int cpr, int lane,
+                                         float S, const float* enc) {
   constexpr int U = 4;
   uint4 v[U];
 #pragma unroll
@@ -311,7 +311,7 @@ __device__ __forceinline__ void row_pass(const RowQuantArgs& a, const uint4* xr,
       if (active) {
         *reinterpret_cast<uint2*>(crow + c * 8) =
             make_uint2(e4m3x4(q[0], q[1], q[2], q[3]), e4m3x4(q[4], q[5], q[6], q[7]));
-        if ((lane & 15) == 0) *reinterpret_cast<uint32_t*>(srow + (a.tiled ? (c >> 4) * 512 : (c >> 2))) = word;
+        if ((lane & 15) == 0) *reinterpret_cast<uint32_t*>(srow + (TILED ? (c >> 4) * 512 : (c >> 2))) = word;
       }
     } else {
       m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
@@ -321,7 +321,7 @@ __device__ __forceinline__ void row_pass(const RowQuantArgs& a, const uint4* xr,
       const uint32_t word = gather4_bytes(sf, 2);
       if (active) {
         *reinterpret_cast<uint32_t*>(crow + c * 4) = e2m1_pack8(q);
-        if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(srow + (a.tiled ? (c >> 3) * 512 : (c >> 1))) = word;
+        if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(srow + (TILED ? (c >> 3) * 512 : (c >> 1))) = word;
       }
     }
   }
@@ -329,10 +329,10 @@ __device__ __forceinline__ void row_pass(const RowQuantArgs& a, const uint4* xr,
 
 // Row quantiser.  The rows are cut into passes of 128 16-byte chunks (the last
 // pass of a row may be shorter); warp w takes an equal contiguous share of
-// the passes.  NVFP4 encode factors S / E4M3(sf) come from a per-warp table
-// of the current group.
-template <int FMT>
-__global__ void __launch_bounds__(kThreads) row_quant_kernel(RowQuantArgs a) {
+// the passes and sets up each row it touches once.  NVFP4 encode factors
+// S / E4M3(sf) come from a per-warp table of the current group.
+template <int FMT, bool TILED>
+__global__ void __launch_bounds__(kThreads, 5) row_quant_kernel(RowQuantArgs a) {
   __shared__ SmemGroups t;
   __shared__ float enc_tab[FMT == GMLP_NVFP4 ? kWarps : 1][128];
   build_group_tables(a.grp, 1, t);
@@ -353,16 +353,14 @@ __global__ void __launch_bounds__(kThreads) row_quant_kernel(RowQuantArgs a) {
   const int64_t p0 = P * w / warps, p1 = P * (w + 1) / warps;
   if (p0 >= p1) return;
   float* enc = enc_tab[FMT == GMLP_NVFP4 ? wib : 0];
-  int r = (int)(p0 / ppr), j = (int)(p0 - (int64_t)r * ppr);  // row and pass within the row
+  int r = (int)(p0 / ppr), j = (int)(p0 - (int64_t)r * ppr);  // first row and pass within it
+  int64_t left = p1 - p0;                                       // passes still to do
   int g = find_group(t, G, r);
   int g_tab = -1;
   float S = 0.0f;
-  for (int64_t p = p0; p < p1; ++p, ++j) {
-    if (j == ppr) {
-      j = 0;
-      ++r;
-    }
-    const int c0 = j * 128;
+  for (; left > 0; ++r, j = 0) {
+    const int jend = (int)min((int64_t)ppr, j + left);
+    left -= jend - j;
     while (t.off[g + 1] <= r) ++g;
     int64_t src = r;
     if (a.swiglu_interleave) {
@@ -375,17 +373,14 @@ __global__ void __launch_bounds__(kThreads) row_quant_kernel(RowQuantArgs a) {
       S = nvfp4_global_scale(a.amax[g]);
       __syncwarp();
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = lane + 32 * i;
-        enc[c] = nvfp4_enc(S, (uint32_t)c);
-      }
+      for (int i = 0; i < 4; ++i) enc[lane + 32 * i] = nvfp4_enc(S, (uint32_t)(lane + 32 * i));
       __syncwarp();
       g_tab = g;
     }
     // scale-word address of the row: tiled (128-row tile, 512-byte blocks of
     // 4 scales x 128 rows) or compact [rows][nscale]
     uint8_t* srow;
-    if (a.tiled) {
+    if (TILED) {
       const int lr = r - t.off[g];
       const int rr = lr & 127;
       srow = a.scales + (int64_t)(t.tb[g] + (lr >> 7)) * (nscale >> 2) * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
@@ -394,10 +389,13 @@ __global__ void __launch_bounds__(kThreads) row_quant_kernel(RowQuantArgs a) {
     }
     const uint4* xr = reinterpret_cast<const uint4*>(a.x + src * K);
     uint8_t* crow = a.codes + (int64_t)r * (FMT == GMLP_MXFP8 ? K : K / 2);
-    if (c0 + 128 <= cpr)
-      row_pass<FMT, true>(a, xr, crow, srow, c0, cpr, lane, S, enc);
-    else
-      row_pass<FMT, false>(a, xr, crow, srow, c0, cpr, lane, S, enc);
+    for (; j < jend; ++j) {
+      const int c0 = j * 128;
+      if (c0 + 128 <= cpr)
+        row_pass<FMT, TILED, true>(xr, crow, srow, c0, cpr, lane, S, enc);
+      else
+        row_pass<FMT, TILED, false>(xr, crow, srow, c0, cpr, lane, S, enc);
+    }
   }
 }
 
@@ -790,12 +788,40 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns) {
 
 }  // namespace
 
+// GEMM_TILED -> GEMM_TILED_X4 for NVFP4 weight scales: for 128-row tile pair
+// P, stage kb (4 runs) and run k of the stage, the 4096 bytes at
+// ((P * KB + kb) * 4 + k) * 4096 hold tile 2P's block (kb, k) four times, then
+// tile 2P+1's block four times.  One 16-byte word per thread step.
+__global__ void replicate_scales_kernel(const uint8_t* in, int64_t pairs, int64_t runs, uint8_t* out) {
+  const int64_t KB = runs / 4;
+  const int64_t n16 = pairs * KB * 4 * 4096 / 16;
+  for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < n16; o += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t ob = o * 16;
+    const int64_t blk = ob >> 12;
+    const int within = (int)(ob & 4095);
+    const int h = within >> 11, i = within & 511;
+    const int64_t pk = blk >> 2, k = blk & 3;
+    const int64_t kb = pk % KB, P = pk / KB;
+    const int64_t src = ((2 * P + h) * runs + 4 * kb + k) * 512 + i;
+    reinterpret_cast<uint4*>(out)[o] = *reinterpret_cast<const uint4*>(in + src);
+  }
+}
+
 cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t s) {
   selftest_wait_kernel<<<1, 32, 0, s>>>(limit_ns);
   return cudaGetLastError();
 }
 
 int quant_read_clear_status() { return read_clear_status(); }
+
+cudaError_t launch_replicate_scales(const uint8_t* tiled, int64_t pairs, int64_t runs, uint8_t* out, cudaStream_t s) {
+  const int64_t n16 = pairs * (runs / 4) * 4 * 4096 / 16;
+  if (n16 == 0) return cudaSuccess;
+  int64_t grid = (n16 + 255) / 256;
+  if (grid > (int64_t)num_sms() * 8) grid = (int64_t)num_sms() * 8;
+  replicate_scales_kernel<<<(unsigned)grid, 256, 0, s>>>(tiled, pairs, runs, out);
+  return cudaGetLastError();
+}
 
 // Launch with programmatic stream serialization when `pdl` is set.
 template <typename... Args>
@@ -813,10 +839,16 @@ cudaError_t launch_ex(void (*kern)(Args...), int grid, size_t smem, cudaStream_t
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+template <int FMT, bool TILED>
+cudaError_t launch_row_quant_t(const RowQuantArgs& a, cudaStream_t s) {
+  auto kern = row_quant_kernel<FMT, TILED>;
+  return launch_ex(kern, grid_for(kern, a.M), 0, s, a.pdl != 0, a);
+}
+
 cudaError_t launch_row_quant(const RowQuantArgs& a, cudaStream_t s) {
   if (a.format == GMLP_MXFP8)
-    return launch_ex(row_quant_kernel<GMLP_MXFP8>, grid_for(row_quant_kernel<GMLP_MXFP8>, a.M), 0, s, a.pdl != 0, a);
-  return launch_ex(row_quant_kernel<GMLP_NVFP4>, grid_for(row_quant_kernel<GMLP_NVFP4>, a.M), 0, s, a.pdl != 0, a);
+    return a.tiled ? launch_row_quant_t<GMLP_MXFP8, true>(a, s) : launch_row_quant_t<GMLP_MXFP8, false>(a, s);
+  return a.tiled ? launch_row_quant_t<GMLP_NVFP4, true>(a, s) : launch_row_quant_t<GMLP_NVFP4, false>(a, s);
 }
 
 cudaError_t launch_group_amax(const uint16_t* x, int64_t M, int64_t K, GroupSrc grp, float* amax,

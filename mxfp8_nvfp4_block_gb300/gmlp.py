@@ -19,12 +19,13 @@ OK, ERR_INVALID_ARG, ERR_INVALID_DIMS, ERR_UNSUPPORTED_RECIPE, ERR_UNSUPPORTED_D
     ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_DEVICE_BOUNDS = range(9)
 MXFP8, NVFP4 = 0, 1
 SWIGLU, SRELU = 0, 1
-COMPACT, GEMM_TILED = 0, 1
+COMPACT, GEMM_TILED, GEMM_TILED_X4 = 0, 1, 2
+SCALES_GEMM_TILED, SCALES_GEMM_TILED_X4 = GEMM_TILED, GEMM_TILED_X4
 
 EXPORTS = ["gmlp_tiled_scales_bytes", "gmlp_group_hadamard_amax", "gmlp_group_quantize_with_amax",
            "gmlp_group_quantize", "gmlp_prepare_weights", "gmlp_forward_workspace_size", "gmlp_forward",
            "gmlp_check_device_status", "gmlp_last_error", "gmlp_version", "gmlp_forward_noalloc",
-           "gmlp_selftest_bounded_wait", "gmlp_mma_peak"]
+           "gmlp_selftest_bounded_wait", "gmlp_mma_peak", "gmlp_replicate_weight_scales"]
 
 
 class Recipe(ctypes.Structure):
@@ -39,7 +40,7 @@ class QTensor(ctypes.Structure):
 class QWeightC(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("global_scale", ctypes.c_void_p),
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("G", ctypes.c_int32),
-                ("format", ctypes.c_int32), ("swiglu_interleaved", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("format", ctypes.c_int32), ("swiglu_interleaved", ctypes.c_int32), ("scale_layout", ctypes.c_int32)]
 
 
 class FwdAux(ctypes.Structure):
@@ -79,6 +80,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gmlp_check_device_status": (_i32, [_vp]),
         "gmlp_selftest_bounded_wait": (_i32, [ctypes.c_uint64, _vp]),
         "gmlp_mma_peak": (_i32, [_i32, _i32, ctypes.c_int64, _i32, _vp]),
+        "gmlp_replicate_weight_scales": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
         "gmlp_last_error": (ctypes.c_char_p, []),
         "gmlp_version": (ctypes.c_char_p, []),
     }
@@ -192,7 +194,7 @@ def group_quantize(x, splits, rec: Recipe, *, rowwise=True, columnwise=False, sp
 @dataclass
 class QWeight:
     codes: torch.Tensor
-    scales: torch.Tensor
+    scales: torch.Tensor                 # GEMM_TILED
     global_scale: torch.Tensor | None
     amax: torch.Tensor | None
     rows: int
@@ -200,14 +202,28 @@ class QWeight:
     G: int
     format: int
     swiglu: bool
+    scales_x4: torch.Tensor | None = None  # NVFP4: GEMM_TILED_X4 copy the forward reads when present
 
     def c(self) -> QWeightC:
+        if self.scales_x4 is not None:
+            return QWeightC(self.codes.data_ptr(), self.scales_x4.data_ptr(), _p(self.global_scale), self.rows,
+                            self.cols, self.G, self.format, int(self.swiglu), SCALES_GEMM_TILED_X4)
         return QWeightC(self.codes.data_ptr(), self.scales.data_ptr(), _p(self.global_scale), self.rows,
-                        self.cols, self.G, self.format, int(self.swiglu), 0)
+                        self.cols, self.G, self.format, int(self.swiglu), SCALES_GEMM_TILED)
 
 
-def prepare_weights(W: torch.Tensor, fmt: int, swiglu_interleave: bool = False, stream=None) -> QWeight:
-    """Quantise stacked expert weights W [G, rows, cols] (bf16, cuda)."""
+def replicate_weight_scales(q: "QWeight", stream=None) -> torch.Tensor:
+    """GEMM_TILED_X4 copy of NVFP4 weight scales (see gmlp_replicate_weight_scales)."""
+    out = _u8(4 * q.G * q.rows * (q.cols // 16), q.scales.device)
+    _check(load().gmlp_replicate_weight_scales(_p(q.scales), q.G, q.rows, q.cols, _p(out), _stream(stream)))
+    return out
+
+
+def prepare_weights(W: torch.Tensor, fmt: int, swiglu_interleave: bool = False, x4: bool | None = None,
+                    stream=None) -> QWeight:
+    """Quantise stacked expert weights W [G, rows, cols] (bf16, cuda).  NVFP4
+    weights with rows and cols multiples of 256 also get the GEMM_TILED_X4
+    scale copy the forward reads (x4=False keeps GEMM_TILED only)."""
     W = _bits(W)
     G, rows, cols = W.shape
     blk, cdiv = (32, 1) if fmt == MXFP8 else (16, 2)
@@ -219,7 +235,12 @@ def prepare_weights(W: torch.Tensor, fmt: int, swiglu_interleave: bool = False, 
         am = torch.empty(G, dtype=torch.float32, device=W.device)
     _check(load().gmlp_prepare_weights(_p(W), G, rows, cols, int(bool(swiglu_interleave)), fmt, _p(codes),
                                        _p(scales), _p(gs), _p(am), _stream(stream)))
-    return QWeight(codes, scales, gs, am, rows, cols, G, fmt, bool(swiglu_interleave))
+    q = QWeight(codes, scales, gs, am, rows, cols, G, fmt, bool(swiglu_interleave))
+    if x4 is None:
+        x4 = fmt == NVFP4 and rows % 256 == 0 and cols % 256 == 0
+    if x4:
+        q.scales_x4 = replicate_weight_scales(q, stream)
+    return q
 
 
 # ------------------------------------------------------------------ forward

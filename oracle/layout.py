@@ -63,3 +63,13 @@ def compact_to_tiled(scales: np.ndarray, splits, ks: int, fill: int = 0) -> np.n
     out = np.full(tiled_size(M, ks, len(splits)), fill, dtype=np.uint8)
     out[tiled_index(splits, ks)] = scales
     return out
+
+
+def tiled_to_x4(buf: np.ndarray, pairs: int, runs: int) -> np.ndarray:
+    """GEMM_TILED_X4 image of GEMM_TILED scales of `2 * pairs` 128-row tiles with
+    `runs` runs of 4 scale columns each (runs % 4 == 0): for tile pair P, stage
+    kb and run k of the stage, 4096 bytes = the block (2P, 4kb+k) four times,
+    then the block (2P+1, 4kb+k) four times."""
+    blocks = np.asarray(buf, np.uint8)[:2 * pairs * runs * 512].reshape(pairs, 2, runs // 4, 4, 512)
+    img = np.broadcast_to(blocks.transpose(0, 2, 3, 1, 4)[:, :, :, :, None, :], (pairs, runs // 4, 4, 2, 4, 512))
+    return np.ascontiguousarray(img).reshape(-1)

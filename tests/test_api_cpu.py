@@ -139,3 +139,28 @@ def test_mma_peak_argument_checks(lib):
     assert b"iters" in L.gmlp_last_error()
     assert g.mma_peak_flops(g.MXFP8, 10, 2) == 2 * 10 * 4 * 2 * 128 * 256 * 32
     assert g.mma_peak_flops(g.NVFP4, 10, 2) == 2 * 10 * 4 * 2 * 128 * 256 * 64
+
+
+def test_replicate_weight_scales_argument_checks(lib):
+    L, g = lib
+    assert L.gmlp_replicate_weight_scales(None, 2, 256, 256, FAKE, None) == g.ERR_INVALID_ARG
+    assert L.gmlp_replicate_weight_scales(FAKE, 2, 128, 256, FAKE, None) == g.ERR_INVALID_DIMS   # rows % 256
+    assert L.gmlp_replicate_weight_scales(FAKE, 2, 256, 384, FAKE, None) == g.ERR_INVALID_DIMS   # cols % 256
+    assert L.gmlp_replicate_weight_scales(FAKE, 0, 256, 256, FAKE, None) == g.ERR_INVALID_DIMS
+
+
+def test_forward_weight_scale_layout_checks(lib):
+    L, g = lib
+    rn = g.recipe(g.NVFP4)
+    need = g.forward_workspace_size(512, 256, 256, 4, g.SRELU, rn)
+
+    def call(l1=0, l2=0, fmt=g.NVFP4, aux=None):
+        w1 = g.QWeightC(FAKE, FAKE, FAKE, 256, 256, 4, fmt, 0, l1)
+        w2 = g.QWeightC(FAKE, FAKE, FAKE, 256, 256, 4, fmt, 0, l2)
+        return L.gmlp_forward(FAKE, 512, 256, 256, FAKE, 4, ctypes.byref(w1), ctypes.byref(w2), None, g.SRELU,
+                              ctypes.byref(g.recipe(fmt)), FAKE, aux, FAKE, need, None)
+
+    assert call(l1=3) == g.ERR_INVALID_ARG
+    assert call(l2=g.GEMM_TILED_X4, fmt=g.MXFP8) == g.ERR_INVALID_ARG    # X4 is an NVFP4 layout
+    pair = g.FwdAux(None, None, None, None, None, None, 0, 2)
+    assert call(l1=g.GEMM_TILED_X4, aux=ctypes.byref(pair)) == g.ERR_INVALID_ARG   # CTA pairs read GEMM_TILED

@@ -26,9 +26,13 @@ def bf16_cpu(a):
     return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
 
 
-def run_gpu(gm, d, fmt, act, mask=0, probs=True, gemm_mode=0):
-    w1 = gm.prepare_weights(d["W1"].cuda(), fmt, swiglu_interleave=(act == gm.SWIGLU))
-    w2 = gm.prepare_weights(d["W2"].cuda(), fmt)
+def run_gpu(gm, d, fmt, act, mask=0, probs=True, gemm_mode=0, x4=None):
+    # NVFP4 weights carry the replicated (GEMM_TILED_X4) scales by default; the
+    # CTA-pair mode reads GEMM_TILED ones
+    if gemm_mode == 2:
+        x4 = False
+    w1 = gm.prepare_weights(d["W1"].cuda(), fmt, swiglu_interleave=(act == gm.SWIGLU), x4=x4)
+    w2 = gm.prepare_weights(d["W2"].cuda(), fmt, x4=x4)
     M, N = d["x"].shape[0], d["W2"].shape[2]
     G = d["splits"].numel()
     cdiv = 1 if fmt == gm.MXFP8 else 2
@@ -106,6 +110,37 @@ def test_forward_lossless_bitexact(orc, gm, fmt, act, gemm_mode):
                                         o_S=None if fmt == 0 else np.repeat(ref["fc2x_S"], splits))
         assert frac >= CODE_MATCH and steps <= 1.0 + 1e-9, (frac, steps)
         assert frob(y.float().cpu().numpy(), orc.bf16_to_f64(ref["y"])) <= Y_TOL
+
+
+@pytest.mark.parametrize("act", [0, 1], ids=["swiglu", "srelu"])
+def test_forward_nvfp4_x4_scales_match_tiled(gm, act):
+    """The GEMM reading replicated weight scales (one 128x256b tensor-memory copy
+    per MMA) gives bit-identical outputs to the one reading GEMM_TILED scales."""
+    rng = np.random.default_rng(21 + act)
+    splits, K, N = [130, 0, 257, 5, 128, 700], 512, 512
+    G, M = len(splits), sum(splits)
+    n1 = 2 * N if act == 0 else N
+    d = dict(x=bf16_cpu(rng.standard_normal((M, K))), splits=torch.tensor(splits, dtype=torch.int64),
+             W1=bf16_cpu(rng.standard_normal((G, n1, K)) / np.sqrt(K)),
+             W2=bf16_cpu(rng.standard_normal((G, K, N)) / np.sqrt(N)),
+             probs=torch.from_numpy(rng.uniform(0, 1, M).astype(np.float32)))
+    y4, a4 = run_gpu(gm, d, 1, act, mask=0x3C5A, x4=True)
+    yt, at = run_gpu(gm, d, 1, act, mask=0x3C5A, x4=False)
+    assert np.array_equal(np_bits(y4), np_bits(yt))
+    for key in ("fc2x_codes", "fc2x_scales", "fc2x_amax_pre", "fc2x_amax_post"):
+        assert torch.equal(a4[key], at[key]), key
+    assert torch.equal(a4["fc2x_bf16"].view(torch.int16), at["fc2x_bf16"].view(torch.int16))
+
+
+def test_replicate_weight_scales_bitexact(orc, gm):
+    rng = np.random.default_rng(4)
+    G, rows, cols = 3, 512, 768
+    W = bf16_cpu(rng.standard_normal((G, rows, cols)))
+    q = gm.prepare_weights(W.cuda(), gm.NVFP4)
+    gm.check_device_status()
+    tiled = np_u8(q.scales)
+    want = orc.tiled_to_x4(tiled, G * rows // 256, cols // 64)
+    assert np.array_equal(np_u8(q.scales_x4), want)
 
 
 def forward_parity(orc, gm, name, rows=None, gemm_mode=0):

@@ -34,3 +34,34 @@ def test_tiled_is_injective_and_bounded(orc):
             assert idx.max() < orc.tiled_size(int(np.sum(splits)), ks, G)
         sc = rng.integers(0, 256, (int(np.sum(splits)), ks)).astype(np.uint8)
         assert np.array_equal(orc.tiled_to_compact(orc.compact_to_tiled(sc, splits, ks), splits, ks), sc)
+
+
+def test_x4_image_feeds_each_b_row_its_scales(orc):
+    """GEMM_TILED_X4 checked through what the GEMM does with it: a 128-row x
+    32-byte tensor-memory copy (lane L <- row L; row L = 16 bytes at 16 L and 16
+    bytes at 2048 + 16 L) of each 4096-byte unit, then the MMA reading B row n
+    (half h = n // 128, r = n % 128) at lane r % 32, column 4 h + r // 32, byte
+    j.  Every B row must see its own compact scales, and the four lane quarters
+    must hold the same bytes."""
+    rng = np.random.default_rng(3)
+    G, rows, cols = 2, 512, 512                       # NVFP4: 32 scale columns per row
+    ks = cols // 16
+    compact = rng.integers(0, 256, (G * rows, ks), dtype=np.uint8)
+    splits = np.full(G, rows)
+    tiled = orc.compact_to_tiled(compact, splits, ks)
+    runs, KB = ks // 4, ks // 16
+    x4 = orc.tiled_to_x4(tiled, G * rows // 256, runs)
+    assert x4.size == 4 * G * rows * ks
+    for P in range(G * rows // 256):
+        for kb in range(KB):
+            for k in range(4):
+                unit = x4[((P * KB + kb) * 4 + k) * 4096:][:4096]
+                lanes = np.stack([np.concatenate([unit[16 * L:16 * L + 16], unit[2048 + 16 * L:2048 + 16 * L + 16]])
+                                  for L in range(128)])          # [128 lanes, 32 bytes = 8 columns]
+                assert np.array_equal(lanes[:32], lanes[32:64]) and np.array_equal(lanes[:32], lanes[96:])
+                for n in range(256):
+                    h, r = divmod(n, 128)
+                    col = 4 * h + r // 32
+                    got = lanes[r % 32, 4 * col:4 * col + 4]
+                    want = compact[256 * P + n, (4 * kb + k) * 4:(4 * kb + k) * 4 + 4]
+                    assert np.array_equal(got, want), (P, kb, k, n)
