@@ -294,9 +294,11 @@ GMLP_API gmlp_status gmlp_selftest_bounded_wait(uint64_t limit_ns, gmlp_stream s
  * pages have no counterpart).  Launches `ctas` CTAs (<= 0: one per SM), each
  * issuing `iters` stages (1 .. 2^24) of the GEMM's block-scaled MMA mix from
  * shared memory filled once with random codes: per stage four M=128, N=256
- * MMAs (K = 32 for GMLP_MXFP8, 64 for GMLP_NVFP4) and one commit, preceded,
- * when scale_copy != 0, by the stage's scale-factor copies to TMEM (3 for
- * MXFP8, 12 for NVFP4), as in the GEMM.  Reads and writes no global memory.
+ * MMAs (K = 32 for GMLP_MXFP8, 64 for GMLP_NVFP4) and one commit, preceded by
+ * the stage's scale-factor copies to TMEM as in the GEMM: scale_copy 0 none
+ * (copied once up front), 1 those for GEMM_TILED weight scales (3 for MXFP8,
+ * 12 for NVFP4), 2 (NVFP4 only) those for GEMM_TILED_X4 weight scales (4 + 4).
+ * Reads and writes no global memory.
  * One launch performs ctas * iters * 4 * 2 * 128 * 256 * K floating-point
  * operations; time it with events on `stream`.  A stage waits for the MMAs of
  * the stage four back (bounded; a timeout sets the device status word). */

@@ -106,7 +106,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 int num_sms();
 
 cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t s);
-cudaError_t launch_mma_peak(int format, bool scale_copy, int64_t iters, int ctas, cudaStream_t s);
+cudaError_t launch_mma_peak(int format, int scale_copy, int64_t iters, int ctas, cudaStream_t s);
 
 // NVFP4 weight scales: GEMM_TILED -> GEMM_TILED_X4 (see gmlp_replicate_weight_scales)
 cudaError_t launch_replicate_scales(const uint8_t* tiled, int64_t pairs, int64_t runs, uint8_t* out, cudaStream_t s);

@@ -8,8 +8,11 @@
 // A stage s reuses the shared-memory buffers and scale columns of stage s - 4,
 // so the issuer waits for that stage's commit before overwriting its scales,
 // exactly as the GEMM's producer waits on its `empty` barrier (here with an
-// infinitely fast producer).  With SFCOPY = false the scales of all four
-// stages are copied once before the loop, which isolates the copy cost.
+// infinitely fast producer).  SFCOPY = 0: the scales of all four stages are
+// copied once before the loop, which isolates the copy cost; 1: the copies of
+// GEMM_TILED weight scales (3 per stage for MXFP8, 12 for NVFP4); 2 (NVFP4):
+// those of GEMM_TILED_X4 weight scales (4 SFA copies and 4 128x256b SFB copies
+// per stage, all from the stage's first 6 KB of scale bytes).
 #include "device.cuh"
 
 namespace gmlp {
@@ -59,7 +62,7 @@ __device__ __forceinline__ uint32_t scale_word(uint32_t i) {
   return FMT == GMLP_MXFP8 ? (0x78787878u + (h & 0x0f0f0f0fu)) : (0x30303030u + (h & 0x1f1f1f1fu));
 }
 
-template <int FMT, bool SFCOPY>
+template <int FMT, int SFCOPY>
 __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters) {
   using C = PeakCfg<FMT>;
   extern __shared__ uint8_t smem_raw[];
@@ -102,7 +105,13 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters
       const uint32_t sfb_t = sfa_t + C::kSfbOff;
       const uint32_t sfa = smem_u32(sSF + stage * 3 * C::kSfBytes);
       const uint32_t sfb = sfa + C::kSfBytes;
-      if (FMT == GMLP_MXFP8) {
+      if (FMT == GMLP_NVFP4 && SFCOPY == 2) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          tc_cp_32x128b_x4(sfa_t + 4 * k, smem_desc(sfa + 512 * k, 0, 128, 0));
+          tc_cp_128x256b(sfb_t + 8 * k, smem_desc(sfb, 2048, 128, 0));
+        }
+      } else if (FMT == GMLP_MXFP8) {
         tc_cp_32x128b_x4(sfa_t, smem_desc(sfa, 0, 128, 0));
         tc_cp_32x128b_x4(sfb_t, smem_desc(sfb, 0, 128, 0));
         tc_cp_32x128b_x4(sfb_t + 4, smem_desc(sfb + 512, 0, 128, 0));
@@ -115,7 +124,7 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters
         }
       }
     };
-    if (!SFCOPY)
+    if (SFCOPY == 0)
       for (int s = 0; s < kStagesP; ++s) copy_scales(s);
     bool ok = true;
     for (int64_t it = 0; it < iters && ok; ++it) {
@@ -125,7 +134,7 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters
         if (!ok) break;
         tc_fence_after();
       }
-      if (SFCOPY) copy_scales(stage);
+      if (SFCOPY != 0) copy_scales(stage);
       const uint32_t sfa_t = sf_base + stage * C::kSfCols;
       const uint32_t sfb_t = sfa_t + C::kSfbOff;
       const uint32_t a_addr = smem_u32(sA + stage * kATile);
@@ -161,7 +170,7 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-template <int FMT, bool SFCOPY>
+template <int FMT, int SFCOPY>
 cudaError_t launch_peak_t(int64_t iters, int ctas, cudaStream_t s) {
   auto kern = mma_peak_kernel<FMT, SFCOPY>;
   constexpr size_t smem = PeakCfg<FMT>::kSmem;
@@ -173,11 +182,11 @@ cudaError_t launch_peak_t(int64_t iters, int ctas, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_mma_peak(int format, bool scale_copy, int64_t iters, int ctas, cudaStream_t s) {
+cudaError_t launch_mma_peak(int format, int scale_copy, int64_t iters, int ctas, cudaStream_t s) {
   if (format == GMLP_MXFP8)
-    return scale_copy ? launch_peak_t<GMLP_MXFP8, true>(iters, ctas, s)
-                      : launch_peak_t<GMLP_MXFP8, false>(iters, ctas, s);
-  return scale_copy ? launch_peak_t<GMLP_NVFP4, true>(iters, ctas, s) : launch_peak_t<GMLP_NVFP4, false>(iters, ctas, s);
+    return scale_copy ? launch_peak_t<GMLP_MXFP8, 1>(iters, ctas, s) : launch_peak_t<GMLP_MXFP8, 0>(iters, ctas, s);
+  if (scale_copy == 2) return launch_peak_t<GMLP_NVFP4, 2>(iters, ctas, s);
+  return scale_copy ? launch_peak_t<GMLP_NVFP4, 1>(iters, ctas, s) : launch_peak_t<GMLP_NVFP4, 0>(iters, ctas, s);
 }
 
 int peak_read_clear_status() { return read_clear_status(); }

@@ -298,9 +298,10 @@ def selftest_bounded_wait(limit_ns: int, stream=None) -> None:
     _check(load().gmlp_selftest_bounded_wait(int(limit_ns), _stream(stream)))
 
 
-def mma_peak(fmt: int, scale_copy: bool, iters: int, ctas: int = 0, stream=None) -> None:
-    """Launch the tensor-core ceiling loop (see gmlp_mma_peak); asynchronous."""
-    _check(load().gmlp_mma_peak(int(fmt), int(bool(scale_copy)), int(iters), int(ctas), _stream(stream)))
+def mma_peak(fmt: int, scale_copy: int, iters: int, ctas: int = 0, stream=None) -> None:
+    """Launch the tensor-core ceiling loop (see gmlp_mma_peak); asynchronous.
+    scale_copy: 0 none, 1 GEMM_TILED weight-scale copies, 2 GEMM_TILED_X4 ones."""
+    _check(load().gmlp_mma_peak(int(fmt), int(scale_copy), int(iters), int(ctas), _stream(stream)))
 
 
 def mma_peak_flops(fmt: int, iters: int, ctas: int) -> float:

@@ -223,7 +223,7 @@ def test_mma_peak_loop_runs_at_a_plausible_rate(gm, fmt):
     4.5 PFLOP/s, FP4 13.5 PFLOP/s): far above would mean it skips work."""
     nominal = 4500.0 if fmt == gm.MXFP8 else 13500.0
     ctas = torch.cuda.get_device_properties(0).multi_processor_count
-    for copy in (True, False):
+    for copy in ((1, 2, 0) if fmt == gm.NVFP4 else (1, 0)):
         gm.mma_peak(fmt, copy, 256)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
