@@ -46,7 +46,8 @@ WORKLOAD_TEXT = {
 NOMINAL_RATIO = {0: 2.0, 1: 6.0}   # dense FP8 / bf16 and FP4 / bf16 (4.5 and 13.5 vs 2.25 PFLOP/s)
 # DRAM bytes (read + write) per fc1 launch from one ncu capture
 # (profiles/gemm_mx_swiglu.md), valid only for the gemm.cu it was taken on.
-FC1_TRAFFIC = {("mx_swiglu", "0c36d48e6179db50b91df757bfe12724cc0a257c"): 65026816 + 4565504}
+FC1_TRAFFIC = {("mx_swiglu", "c1e1067c12d12aa78d485ffa9be7e7c889c6d6d8"): 65025280 + 4927232,
+               ("nv_srelu", "c1e1067c12d12aa78d485ffa9be7e7c889c6d6d8"): 126107136 + 98628864}
 
 
 def fc1_traffic(workload: str):
