@@ -172,6 +172,12 @@ def run_gpu(args, rank: int, world: int) -> dict:
     del d["W1"], d["W2"]
     y = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(gmlp.forward_workspace_size(w.M, w.K, w.N, w.G, act, rec), dtype=torch.uint8, device=dev)
+    colwise = None
+    if args.fc2x_colwise and fmt == gmlp.NVFP4:
+        # the no-recompute training variant: fc2_x also cast columnwise (RHT) in the same pass
+        ncol = w.N * (w.M + 16 * w.G)
+        colwise = {"fc2x_col_codes": torch.empty(ncol // 2, dtype=torch.uint8, device=dev),
+                   "fc2x_col_scales": torch.empty(ncol // 16, dtype=torch.uint8, device=dev)}
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > 129 MB of L2
     sweep = torch.zeros(64 * 1024 * 1024, dtype=torch.int32, device=dev) if args.l2_flush == "clean" else None
 
@@ -197,7 +203,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
 
     for _ in range(W_steps):
         flush_l2()
-        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode)
+        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise)
     gmlp.check_device_status()
     torch.cuda.synchronize()
     if world > 1:
@@ -209,7 +215,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
         for i in range(K_steps):
             flush_l2()
             starts[i].record(stream)
-            gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode)
+            gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise)
             ends[i].record(stream)
         torch.cuda.synchronize()
         # pass 2: events after every kernel of the step, for per-kernel times
@@ -218,7 +224,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
             flush_l2()
             starts2[i].record(stream)
             gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, events=stages[i],
-                         gemm_mode=args.gemm_mode)
+                         gemm_mode=args.gemm_mode, aux=colwise)
         torch.cuda.synchronize()
         clk.mark_end()
     if world > 1:
@@ -244,7 +250,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
         x.copy_(x_h, non_blocking=True)
         probs.copy_(p_h, non_blocking=True)
         splits.copy_(s_h, non_blocking=True)
-        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode)
+        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise)
         y_h.copy_(y, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
@@ -280,7 +286,8 @@ def run_gpu(args, rank: int, world: int) -> dict:
                    "timing": "value: per-step start/end events; stages_ms and roofline: a second timed pass with "
                              "an event after every kernel",
                    "weights": "quantised once before timing", "flops_per_step": w.flops,
-                   "gemm_mode": args.gemm_mode},
+                   "gemm_mode": args.gemm_mode,
+                   "fc2x_columnwise": bool(colwise)},
         "e2e": {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": K_steps * n_stage,
@@ -297,6 +304,12 @@ def run_gpu(args, rank: int, world: int) -> dict:
                        "frac_hbm": round(q_bytes / (stage_ms[quant_idx] * 1e-3) / 1e9 / hbm, 4)},
         "clocks": clk.summary(),
     }
+    if fmt == gmlp.NVFP4:
+        # fc2_x cast: bf16 in, rowwise NVFP4 out (+ the columnwise copy with --fc2x-colwise)
+        f_bytes = w.M * w.N * 2 + (w.M * w.N // 2 + w.M * w.N // 16) * (2 if colwise else 1)
+        out["fc2x_cast"] = {"ms": round(stage_ms[3], 5), "bytes": f_bytes, "columnwise": bool(colwise),
+                            "GB_s": round(f_bytes / (stage_ms[3] * 1e-3) / 1e9, 1),
+                            "frac_hbm": round(f_bytes / (stage_ms[3] * 1e-3) / 1e9 / hbm, 4)}
     ceiling = mma_ceiling(gmlp, fmt)
     out["roofline"]["mma_loop_tflops"] = ceiling
     # the loop with the copy mix the forward's GEMM issues (NVFP4 weights carry X4 scales)
@@ -455,6 +468,8 @@ def main():
     ap.add_argument("--workload", default="mx_swiglu", choices=[k for k in WORKLOADS if k != "nv_quant"])
     ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 2],
                     help="0: one CTA per 128x256 tile; 2: CTA pairs on 256x256 tiles")
+    ap.add_argument("--fc2x-colwise", action="store_true",
+                    help="NVFP4: also write the columnwise (RHT) NVFP4 fc2_x each step (no-recompute training path)")
     ap.add_argument("--l2-flush", default="write", choices=["write", "clean"],
                     help="between timed steps: write 256 MiB, or write 256 MiB then read another 256 MiB")
     ap.add_argument("--no-quant", dest="quant", action="store_false", help="skip the standalone quantiser leg")

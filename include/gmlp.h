@@ -225,6 +225,18 @@ typedef struct gmlp_fwd_aux {
   int32_t n_stage_events;   /* MXFP8: 3 (x quant, fc1, fc2); NVFP4: 5 (x amax, x quant, fc1, fc2_x quant, fc2) */
   int32_t gemm_mode;        /* 0: one CTA per 128 x 256 tile (default); 2: CTA pairs on 256 x 256 tiles
                                (cta_group::2 MMA, each CTA loading half of the B tile) */
+  /* out, NVFP4, optional (both or neither): columnwise NVFP4 of fc2_x, the
+   * wgrad operand of a training step that does not recompute fc2_x (PR #3837
+   * Changes: columnwise data is requested only when the backward will not
+   * rebuild the tensor).  16-row column chunks per group, RHT with the
+   * recipe's sign mask when recipe->use_rht, global scale from the fused
+   * post-RHT (or, without RHT, pre-RHT) amax; layout as the columnwise output
+   * of gmlp_group_quantize_with_amax: per group codes [N][Mpad_g/2] and
+   * scales [N][Mpad_g/16], Mpad_g = 16 * ceil(m_g / 16), groups in order.
+   * N * (M + 16 * G) / 2 and N * (M + 16 * G) / 16 bytes hold any split.  The
+   * same pass writes fc2's rowwise operand. */
+  uint8_t* fc2x_col_codes;
+  uint8_t* fc2x_col_scales;
 } gmlp_fwd_aux;
 
 /* Workspace bytes gmlp_forward needs for these sizes (x and fc2_x codes and

@@ -362,6 +362,12 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
     return fail(GMLP_ERR_WORKSPACE, "workspace %zu bytes, need %zu (16-byte aligned)", workspace_bytes, L.total);
   if (aux && aux->n_stage_events > 0 && !aux->stage_events) return fail(GMLP_ERR_INVALID_ARG, "stage_events NULL");
+  if (aux && (aux->fc2x_col_codes || aux->fc2x_col_scales)) {
+    if (fmt != GMLP_NVFP4) return fail(GMLP_ERR_INVALID_ARG, "columnwise fc2_x output is an NVFP4 output");
+    if (!aux->fc2x_col_codes || !aux->fc2x_col_scales || !aligned16(aux->fc2x_col_codes) ||
+        !aligned16(aux->fc2x_col_scales))
+      return fail(GMLP_ERR_INVALID_ARG, "fc2x_col_codes / fc2x_col_scales: both, 16-byte aligned");
+  }
   if (aux && aux->gemm_mode != 0 && aux->gemm_mode != 2)
     return fail(GMLP_ERR_INVALID_ARG, "gemm_mode %d is neither 0 nor 2", aux->gemm_mode);
   GMLP_TRY(check_device());
@@ -488,7 +494,25 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     g1.pdl = 1;
   GMLP_CUDA(launch_gemm(g1, s), "fc1 launch");
   GMLP_TRY(mark());
-  {
+  if (aux && aux->fc2x_col_codes) {
+    // rowwise (fc2's operand) and columnwise (RHT) NVFP4 of fc2_x in one pass,
+    // both from the amaxes the fc1 epilogue produced
+    ColQuantArgs c{};
+    c.x = f_bf16;
+    c.M = M;
+    c.K = N;
+    c.grp = gs;
+    c.use_rht = recipe->use_rht != 0;
+    c.mask = recipe->rht_sign_mask & 0xFFFFu;
+    c.amax_row = f_pre;
+    c.amax_col = recipe->use_rht ? f_post : f_pre;
+    c.row_codes = f_codes;
+    c.row_scales = f_scales;
+    c.row_tiled = 1;
+    c.col_codes = aux->fc2x_col_codes;
+    c.col_scales = aux->fc2x_col_scales;
+    GMLP_CUDA(launch_col_quant(c, s), "fc2_x row + column quantise launch");
+  } else {
     RowQuantArgs q{};
     q.x = f_bf16;
     q.M = M;

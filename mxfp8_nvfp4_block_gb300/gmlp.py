@@ -47,7 +47,8 @@ class FwdAux(ctypes.Structure):
     _fields_ = [("fc2x_codes", ctypes.c_void_p), ("fc2x_scales", ctypes.c_void_p), ("fc2x_bf16", ctypes.c_void_p),
                 ("fc2x_amax_pre", ctypes.c_void_p), ("fc2x_amax_post", ctypes.c_void_p),
                 ("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("n_stage_events", ctypes.c_int32),
-                ("gemm_mode", ctypes.c_int32)]
+                ("gemm_mode", ctypes.c_int32), ("fc2x_col_codes", ctypes.c_void_p),
+                ("fc2x_col_scales", ctypes.c_void_p)]
 
 
 _lib = None
@@ -266,7 +267,8 @@ def forward(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *
     if aux is not None or events is not None or gemm_mode:
         aux = aux or {}
         aux_c = FwdAux(_p(aux.get("fc2x_codes")), _p(aux.get("fc2x_scales")), _p(aux.get("fc2x_bf16")),
-                       _p(aux.get("fc2x_amax_pre")), _p(aux.get("fc2x_amax_post")), None, 0, int(gemm_mode))
+                       _p(aux.get("fc2x_amax_pre")), _p(aux.get("fc2x_amax_post")), None, 0, int(gemm_mode),
+                       _p(aux.get("fc2x_col_codes")), _p(aux.get("fc2x_col_scales")))
         if events:
             ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
             aux_c.stage_events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))

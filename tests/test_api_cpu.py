@@ -167,3 +167,15 @@ def test_forward_weight_scale_layout_checks(lib):
     assert call(l2=g.GEMM_TILED_X4, fmt=g.MXFP8) == g.ERR_INVALID_ARG    # X4 is an NVFP4 layout
     pair = g.FwdAux(None, None, None, None, None, None, 0, 2)
     assert call(l1=g.GEMM_TILED_X4, aux=ctypes.byref(pair)) == g.ERR_INVALID_ARG   # CTA pairs read GEMM_TILED
+
+
+def test_forward_columnwise_fc2x_checks(lib):
+    L, g = lib
+    r = g.recipe(g.MXFP8)
+    w1 = g.QWeightC(FAKE, FAKE, None, 512, 256, 4, g.MXFP8, 1, 0)
+    w2 = g.QWeightC(FAKE, FAKE, None, 256, 256, 4, g.MXFP8, 0, 0)
+    need = g.forward_workspace_size(512, 256, 256, 4, g.SWIGLU, r)
+    aux = g.FwdAux(None, None, None, None, None, None, 0, 0, FAKE, FAKE)
+    assert L.gmlp_forward(FAKE, 512, 256, 256, FAKE, 4, ctypes.byref(w1), ctypes.byref(w2), None, g.SWIGLU,
+                          ctypes.byref(r), FAKE, ctypes.byref(aux), FAKE, need, None) == g.ERR_INVALID_ARG
+    assert b"NVFP4" in L.gmlp_last_error()

@@ -132,6 +132,42 @@ def test_forward_nvfp4_x4_scales_match_tiled(gm, act):
     assert torch.equal(a4["fc2x_bf16"].view(torch.int16), at["fc2x_bf16"].view(torch.int16))
 
 
+@pytest.mark.parametrize("use_rht", [True, False])
+def test_forward_nvfp4_columnwise_fc2x(orc, gm, use_rht):
+    """The forward's optional columnwise NVFP4 fc2_x (no-recompute training
+    path): bit-exact against the oracle's quantize-with-amax of the GPU's own
+    bf16 fc2_x and fused amaxes; fc2's rowwise operand and y are unchanged."""
+    rng = np.random.default_rng(31)
+    splits, K, N = [130, 0, 257, 5, 1, 128, 700], 512, 512
+    G, M = len(splits), sum(splits)
+    d = dict(x=bf16_cpu(rng.standard_normal((M, K))), splits=torch.tensor(splits, dtype=torch.int64),
+             W1=bf16_cpu(rng.standard_normal((G, N, K)) / np.sqrt(K)),
+             W2=bf16_cpu(rng.standard_normal((G, K, N)) / np.sqrt(N)),
+             probs=torch.from_numpy(rng.uniform(0, 1, M).astype(np.float32)))
+    mask = 0x5AC3
+    y0, a0 = run_gpu(gm, d, 1, 1, mask=mask)
+    w1 = gm.prepare_weights(d["W1"].cuda(), gm.NVFP4)
+    w2 = gm.prepare_weights(d["W2"].cuda(), gm.NVFP4)
+    ncol = N * (M + 16 * G)
+    aux = {k: torch.zeros_like(v) for k, v in a0.items()}
+    aux["fc2x_col_codes"] = torch.zeros(ncol // 2, dtype=torch.uint8, device="cuda")
+    aux["fc2x_col_scales"] = torch.zeros(ncol // 16, dtype=torch.uint8, device="cuda")
+    rec = gm.recipe(gm.NVFP4, use_rht=use_rht, mask=mask)
+    y = torch.empty_like(y0)
+    gm.forward(d["x"].cuda(), d["splits"].cuda(), w1, w2, d["probs"].cuda(), gm.SRELU, rec, y=y, aux=aux)
+    gm.check_device_status()
+    assert np.array_equal(np_bits(y), np_bits(y0))
+    assert torch.equal(aux["fc2x_codes"], a0["fc2x_codes"]) and torch.equal(aux["fc2x_scales"], a0["fc2x_scales"])
+    fx = aux["fc2x_bf16"].cpu().view(torch.int16).numpy().view(np.uint16)
+    pre = aux["fc2x_amax_pre"].cpu().numpy()
+    post = aux["fc2x_amax_post"].cpu().numpy()
+    ref = orc.group_quantize_with_amax(fx, np.array(splits), orc.NVFP4, pre, post, rowwise=False, columnwise=True,
+                                       use_rht=use_rht, mask=mask)
+    nb = len(ref["col_codes"])
+    assert np.array_equal(np_u8(aux["fc2x_col_codes"], nb), ref["col_codes"])
+    assert np.array_equal(np_u8(aux["fc2x_col_scales"], len(ref["col_scales"])), ref["col_scales"])
+
+
 def test_replicate_weight_scales_bitexact(orc, gm):
     rng = np.random.default_rng(4)
     G, rows, cols = 3, 512, 768
