@@ -645,26 +645,25 @@ __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
     }
     __syncthreads();
 
-    // phase 2: rowwise NVFP4, one thread per 16-column block (16 threads per row)
+    // phase 2: rowwise NVFP4, one thread per 16-column block (16 threads per
+    // row): packed bf16 max, the exact division-free b / 6, encode table
     if (a.row_codes) {
       const int nblk = ncols / 16;
       for (int base = warp * 32; base < nvalid * 16; base += kThreads) {
         const int i = base + lane, r = i >> 4, bb = i & 15;
         const bool ok = r < nvalid && bb < nblk;
-        float f[16];
-        unpack8(*reinterpret_cast<const uint4*>(tile + r * kTileC + 16 * bb), f);
-        unpack8(*reinterpret_cast<const uint4*>(tile + r * kTileC + 16 * bb + 8), f + 8);
-        float am = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) am = fmaxf(am, fabsf(f[k]));
-        const uint32_t sf = nvfp4_block_sf(am, S_row);
-        const uint2 codes = e2m1_pack16(f, enc_row[sf]);
-        const int lb = lane & ~3;
-        const uint32_t sw = __shfl_sync(0xffffffffu, sf, lb) | (__shfl_sync(0xffffffffu, sf, lb + 1) << 8) |
-                            (__shfl_sync(0xffffffffu, sf, lb + 2) << 16) | (__shfl_sync(0xffffffffu, sf, lb + 3) << 24);
+        const uint4 v0 = *reinterpret_cast<const uint4*>(tile + r * kTileC + 16 * bb);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(tile + r * kTileC + 16 * bb + 8);
+        const uint32_t sf = nvfp4_block_sf_bf16(max(amax8_bits(v0), amax8_bits(v1)), S_row);
+        const float enc = enc_row[sf];
+        float q0[8], q1[8];
+        scale8(v0, enc, q0);
+        scale8(v1, enc, q1);
+        const uint32_t sw = gather4_bytes(sf, 1);
         if (ok) {
           const int64_t rg = row0 + r;
-          *reinterpret_cast<uint2*>(a.row_codes + rg * (K / 2) + (col0 >> 1) + 8 * bb) = codes;
+          *reinterpret_cast<uint2*>(a.row_codes + rg * (K / 2) + (col0 >> 1) + 8 * bb) =
+              make_uint2(e2m1_pack8(q0), e2m1_pack8(q1));
           if ((bb & 3) == 0)
             *reinterpret_cast<uint32_t*>(a.row_scales + scale_offset(a.row_tiled, t, g, rg,
                                                                      (int)(col0 >> 4) + bb, nscale_row)) = sw;
