@@ -41,6 +41,8 @@ WORKLOAD_TEXT = {
     "nv_srelu": "NVFP4+RHT SReLU grouped MLP: 8 experts, K=4096, N=2048, 32768 tokens uniform, 0.1% x outliers x50, "
                 "seed 2",
     "mx_skew": "MXFP8 SwiGLU grouped MLP, Zipf(1.1) routing: 64 experts, K=7168, N=2048, 65536 tokens, seed 3",
+    "nv_tanh_srelu": "NVFP4+RHT tanh-SReLU (soft-clamp scale 8) grouped MLP on the nv_srelu inputs: 8 experts, "
+                     "K=4096, N=2048, 32768 tokens, seed 2",
     "tiny": "MXFP8 SwiGLU grouped MLP: 4 experts, K=256, N=256, 512 tokens, seed 0",
 }
 NOMINAL_RATIO = {0: 2.0, 1: 6.0}   # dense FP8 / bf16 and FP4 / bf16 (4.5 and 13.5 vs 2.25 PFLOP/s)
@@ -203,7 +205,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
 
     for _ in range(W_steps):
         flush_l2()
-        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise)
+        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise, tanh_clamp_scale=w.tanh_clamp_scale)
     gmlp.check_device_status()
     torch.cuda.synchronize()
     if world > 1:
@@ -215,7 +217,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
         for i in range(K_steps):
             flush_l2()
             starts[i].record(stream)
-            gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise)
+            gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise, tanh_clamp_scale=w.tanh_clamp_scale)
             ends[i].record(stream)
         torch.cuda.synchronize()
         # pass 2: events after every kernel of the step, for per-kernel times
@@ -224,7 +226,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
             flush_l2()
             starts2[i].record(stream)
             gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, events=stages[i],
-                         gemm_mode=args.gemm_mode, aux=colwise)
+                         gemm_mode=args.gemm_mode, aux=colwise, tanh_clamp_scale=w.tanh_clamp_scale)
         torch.cuda.synchronize()
         clk.mark_end()
     if world > 1:
@@ -250,7 +252,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
         x.copy_(x_h, non_blocking=True)
         probs.copy_(p_h, non_blocking=True)
         splits.copy_(s_h, non_blocking=True)
-        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise)
+        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise, tanh_clamp_scale=w.tanh_clamp_scale)
         y_h.copy_(y, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
@@ -402,7 +404,7 @@ def oracle_sample(name: str, target_s: float = 10.0, max_reps: int = 3) -> dict:
     reps = 0
     while True:
         oracle.forward(xb, d["splits"].numpy(), W1, W2, d["probs"].numpy(), w.act, w.fmt, qw1=qw1, qw2=qw2,
-                       rht_mask=d["mask"])
+                       rht_mask=d["mask"], tanh_clamp_scale=w.tanh_clamp_scale)
         reps += 1
         el = time.time() - t0
         if el >= target_s or reps >= max_reps:
@@ -429,7 +431,8 @@ def run_reference(args) -> dict:
         # size the per-step row sample so the whole run stays near two minutes
         probe = np.sort(rng.choice(w.M, max(64, w.M // 64), replace=False))
         t0 = time.time()
-        oracle.forward(xb, splits, W1, W2, d["probs"].numpy(), w.act, w.fmt, rows=probe, qw1=qw1, qw2=qw2)
+        oracle.forward(xb, splits, W1, W2, d["probs"].numpy(), w.act, w.fmt, rows=probe, qw1=qw1, qw2=qw2,
+                       tanh_clamp_scale=w.tanh_clamp_scale)
         per_row = (time.time() - t0) / len(probe)
         n = int(min(w.M // 8, max(64, 120.0 / (args.steps + args.warmup) / per_row)))
         rows = np.sort(rng.choice(w.M, n, replace=False))
@@ -438,7 +441,7 @@ def run_reference(args) -> dict:
 
     def step():
         oracle.forward(xb, splits, W1, W2, d["probs"].numpy(), w.act, w.fmt, rows=rows, qw1=qw1, qw2=qw2,
-                       rht_mask=d["mask"])
+                       rht_mask=d["mask"], tanh_clamp_scale=w.tanh_clamp_scale)
 
     for _ in range(args.warmup):
         step()

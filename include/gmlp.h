@@ -98,7 +98,11 @@ typedef enum gmlp_status {
 } gmlp_status;
 
 typedef enum gmlp_format { GMLP_MXFP8 = 0, GMLP_NVFP4 = 1 } gmlp_format;
-typedef enum gmlp_act { GMLP_ACT_SWIGLU = 0, GMLP_ACT_SRELU = 1 } gmlp_act;
+/* GMLP_ACT_TANH_SRELU: the SReLU soft clamp of PR #3837 (Changes, ScaledTanhSReLU
+ * with tanh_clamp_scale c); the pages give no formula, the reading here is the
+ * soft clamp of the SReLU output at c: c * tanh(max(h,0)^2 / c).  c comes in
+ * gmlp_fwd_aux.tanh_clamp_scale. */
+typedef enum gmlp_act { GMLP_ACT_SWIGLU = 0, GMLP_ACT_SRELU = 1, GMLP_ACT_TANH_SRELU = 2 } gmlp_act;
 typedef enum gmlp_scale_layout {
   GMLP_SCALES_COMPACT = 0,
   GMLP_SCALES_GEMM_TILED = 1,
@@ -237,6 +241,7 @@ typedef struct gmlp_fwd_aux {
    * same pass writes fc2's rowwise operand. */
   uint8_t* fc2x_col_codes;
   uint8_t* fc2x_col_scales;
+  float tanh_clamp_scale;  /* GMLP_ACT_TANH_SRELU: the soft-clamp scale c (> 0, finite); aux is then required */
 } gmlp_fwd_aux;
 
 /* Workspace bytes gmlp_forward needs for these sizes (x and fc2_x codes and
@@ -249,7 +254,8 @@ GMLP_API size_t gmlp_forward_workspace_size(int64_t M, int64_t K, int64_t N, int
  *   1. x [M,K] bf16 -> rowwise MXFP8 / NVFP4 (per-group amax) codes + scales;
  *   2. fc1 per group g: H = dq(xq_g) dq(W1q_g)^T (FP32 accumulate; NVFP4 times
  *      1/(S_x,g S_w1,g));
- *   3. h = bf16(H); act = SwiGLU (silu(gate)*up) or SReLU (max(h,0)^2);
+ *   3. h = bf16(H); act = SwiGLU (silu(gate)*up), SReLU (max(h,0)^2) or
+ *      tanh-SReLU (c * tanh(max(h,0)^2 / c));
  *      fc2_x = bf16(act * probs[t]) (probs NULL = 1);
  *   4. MXFP8: fc2_x is quantised inside the fc1 epilogue and never stored in
  *      bf16.  NVFP4: the epilogue stores bf16 fc2_x and the per-group

@@ -3,6 +3,7 @@
 // replacing the silent unfused fallback and its warning described in PR #3631
 // "Add NVTE_CUTEDSL_FUSED_GROUPED_MLP_WARN_FALLBACK", Changes), workspace
 // carving and the launch sequence of each call.
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -323,7 +324,10 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   g_last_error[0] = 0;
   GMLP_TRY(check_groups(G, M, split_sizes));
   GMLP_TRY(check_recipe(recipe));
-  if (act != GMLP_ACT_SWIGLU && act != GMLP_ACT_SRELU) return fail(GMLP_ERR_INVALID_ARG, "act = %d unknown", act);
+  if (act != GMLP_ACT_SWIGLU && act != GMLP_ACT_SRELU && act != GMLP_ACT_TANH_SRELU)
+    return fail(GMLP_ERR_INVALID_ARG, "act = %d unknown", act);
+  if (act == GMLP_ACT_TANH_SRELU && !(aux && aux->tanh_clamp_scale > 0.0f && std::isfinite(aux->tanh_clamp_scale)))
+    return fail(GMLP_ERR_INVALID_ARG, "tanh-SReLU needs aux->tanh_clamp_scale > 0 and finite");
   const int fmt = recipe->format;
   const int64_t n1 = act == GMLP_ACT_SWIGLU ? 2 * N : N;
   if (K <= 0 || K % 256) return fail(GMLP_ERR_INVALID_DIMS, "K = %lld must be a positive multiple of 256", (long long)K);
@@ -390,7 +394,8 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     return GMLP_OK;
   };
 
-  const int epi1 = act == GMLP_ACT_SWIGLU ? EPI_FC1_SWIGLU : EPI_FC1_SRELU;
+  const int epi1 = act == GMLP_ACT_SWIGLU ? EPI_FC1_SWIGLU : act == GMLP_ACT_SRELU ? EPI_FC1_SRELU : EPI_FC1_TANH_SRELU;
+  const float tanh_c = act == GMLP_ACT_TANH_SRELU ? aux->tanh_clamp_scale : 0.0f;
   if (fmt == GMLP_MXFP8) {
     RowQuantArgs q{};
     q.x = x;
@@ -415,6 +420,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     g1.n_out = n1;
     g1.grp = gs;
     g1.probs = probs;
+    g1.tanh_c = tanh_c;
     g1.out_codes = f_codes;
     g1.out_scales = f_scales;
     g1.n_cols_out = N;
@@ -485,6 +491,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   g1.b_S = W1->global_scale;
   g1.b_x4 = x4_1;
   g1.probs = probs;
+  g1.tanh_c = tanh_c;
   g1.out_bf16 = f_bf16;
   g1.amax_pre = f_pre;
   g1.amax_post = f_post;

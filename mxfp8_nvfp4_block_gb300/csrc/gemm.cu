@@ -189,6 +189,14 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
       const float hu = round_bf16(acc[32 + i] * alpha);
       acc[i] = round_bf16(silu_times(hg, hu) * prob);
     }
+  } else if (EPI == EPI_FC1_TANH_SRELU) {
+    // soft clamp of the squared ReLU at c: c * tanh(h^2 / c)
+    const float c = a.tanh_c, inv_c = __frcp_rn(a.tanh_c);
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float h = fmaxf(round_bf16(acc[i] * alpha), 0.0f);
+      acc[i] = round_bf16(c * tanhf(h * h * inv_c) * prob);
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
@@ -737,15 +745,18 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.format == GMLP_MXFP8) {
     if (a.epi == EPI_FC1_SWIGLU) GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_SWIGLU);
     if (a.epi == EPI_FC1_SRELU) GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_SRELU);
+    if (a.epi == EPI_FC1_TANH_SRELU) GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_TANH_SRELU);
     GMLP_LAUNCH(GMLP_MXFP8, EPI_FC2);
   }
   if (a.b_x4) {  // replicated B scales: single-CTA tiles only
     if (a.epi == EPI_FC1_SWIGLU) return launch_t<GMLP_NVFP4, EPI_FC1_SWIGLU, 1, true>(a, s);
     if (a.epi == EPI_FC1_SRELU) return launch_t<GMLP_NVFP4, EPI_FC1_SRELU, 1, true>(a, s);
+    if (a.epi == EPI_FC1_TANH_SRELU) return launch_t<GMLP_NVFP4, EPI_FC1_TANH_SRELU, 1, true>(a, s);
     return launch_t<GMLP_NVFP4, EPI_FC2, 1, true>(a, s);
   }
   if (a.epi == EPI_FC1_SWIGLU) GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SWIGLU);
   if (a.epi == EPI_FC1_SRELU) GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SRELU);
+  if (a.epi == EPI_FC1_TANH_SRELU) GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_TANH_SRELU);
   GMLP_LAUNCH(GMLP_NVFP4, EPI_FC2);
 #undef GMLP_LAUNCH
 }

@@ -72,6 +72,7 @@ enum Epilogue : int {
   EPI_FC1_SWIGLU = 0,  // fc1 + SwiGLU (gate/up 32-column interleave) x prob
   EPI_FC1_SRELU = 1,   // fc1 + squared ReLU x prob
   EPI_FC2 = 2,         // fc2: bf16 output
+  EPI_FC1_TANH_SRELU = 3,  // fc1 + tanh soft clamp of the squared ReLU x prob
 };
 
 struct GemmArgs {
@@ -96,6 +97,7 @@ struct GemmArgs {
   float* amax_pre;         // NVFP4 fc1: [G] (atomicMax, zeroed before)
   float* amax_post;
   uint32_t rht_mask;
+  float tanh_c;            // EPI_FC1_TANH_SRELU: soft-clamp scale
   int64_t n_cols_out;      // row length of the output (fc1: N; fc2: K)
   int b_x4;                // NVFP4: b_scales in the replicated GEMM_TILED_X4 layout
   int pair;                // 2: CTA pairs (cta_group::2); otherwise single-CTA tiles

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(HERE, "libgmlp.so")
 OK, ERR_INVALID_ARG, ERR_INVALID_DIMS, ERR_UNSUPPORTED_RECIPE, ERR_UNSUPPORTED_DEVICE, ERR_WORKSPACE, \
     ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_DEVICE_BOUNDS = range(9)
 MXFP8, NVFP4 = 0, 1
-SWIGLU, SRELU = 0, 1
+SWIGLU, SRELU, TANH_SRELU = 0, 1, 2
 COMPACT, GEMM_TILED, GEMM_TILED_X4 = 0, 1, 2
 SCALES_GEMM_TILED, SCALES_GEMM_TILED_X4 = GEMM_TILED, GEMM_TILED_X4
 
@@ -48,7 +48,7 @@ class FwdAux(ctypes.Structure):
                 ("fc2x_amax_pre", ctypes.c_void_p), ("fc2x_amax_post", ctypes.c_void_p),
                 ("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("n_stage_events", ctypes.c_int32),
                 ("gemm_mode", ctypes.c_int32), ("fc2x_col_codes", ctypes.c_void_p),
-                ("fc2x_col_scales", ctypes.c_void_p)]
+                ("fc2x_col_scales", ctypes.c_void_p), ("tanh_clamp_scale", ctypes.c_float)]
 
 
 _lib = None
@@ -251,7 +251,8 @@ def forward_workspace_size(M: int, K: int, N: int, G: int, act: int, rec: Recipe
 
 
 def forward(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *, y=None, workspace=None,
-            aux: dict | None = None, events=None, gemm_mode: int = 0, stream=None) -> torch.Tensor:
+            aux: dict | None = None, events=None, gemm_mode: int = 0, tanh_clamp_scale: float = 0.0,
+            stream=None) -> torch.Tensor:
     """y = fused grouped-MLP forward of bf16 x [M, K]."""
     x = _bits(x)
     M, K = x.shape
@@ -264,11 +265,11 @@ def forward(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *
         workspace = _u8(need, x.device)
     aux_c = None
     ev_arr = None
-    if aux is not None or events is not None or gemm_mode:
+    if aux is not None or events is not None or gemm_mode or act == TANH_SRELU:
         aux = aux or {}
         aux_c = FwdAux(_p(aux.get("fc2x_codes")), _p(aux.get("fc2x_scales")), _p(aux.get("fc2x_bf16")),
                        _p(aux.get("fc2x_amax_pre")), _p(aux.get("fc2x_amax_post")), None, 0, int(gemm_mode),
-                       _p(aux.get("fc2x_col_codes")), _p(aux.get("fc2x_col_scales")))
+                       _p(aux.get("fc2x_col_codes")), _p(aux.get("fc2x_col_scales")), float(tanh_clamp_scale))
         if events:
             ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
             aux_c.stage_events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))
@@ -281,7 +282,7 @@ def forward(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *
 
 
 def forward_noalloc(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *, y=None,
-                    stream=None) -> torch.Tensor:
+                    tanh_clamp_scale: float = 0.0, stream=None) -> torch.Tensor:
     """Same as :func:`forward`, but the library uses its own fixed static scratch
     instead of a workspace (for callers that cannot allocate device memory)."""
     x = _bits(x)
@@ -290,8 +291,10 @@ def forward_noalloc(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: R
     if y is None:
         y = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
     w1c, w2c = W1.c(), W2.c()
+    aux_c = FwdAux(tanh_clamp_scale=float(tanh_clamp_scale)) if act == TANH_SRELU else None
     _check(load().gmlp_forward_noalloc(_p(x), M, K, W2.cols, _p(splits), G, ctypes.byref(w1c), ctypes.byref(w2c),
-                                       _p(probs), act, ctypes.byref(rec), _p(y), None, _stream(stream)))
+                                       _p(probs), act, ctypes.byref(rec), _p(y),
+                                       ctypes.byref(aux_c) if aux_c else None, _stream(stream)))
     return y
 
 

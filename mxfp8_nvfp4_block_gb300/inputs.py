@@ -14,6 +14,8 @@ U(0,1) fp32):
 * ``nv_srelu``  NVFP4 + RHT squared-ReLU, G=8, K=4096, N=2048, M=32768 split
   uniformly; exactly round(0.001*M*K) entries of x (a random permutation's
   prefix) multiplied by 50; a random 16-bit RHT sign mask; seed 2.
+* ``nv_tanh_srelu`` the ``nv_srelu`` inputs (same seed, same bytes) with the
+  tanh-SReLU activation, soft-clamp scale 8.
 * ``mx_skew``   MXFP8 SwiGLU, G=64, K=7168, N=2048, M=65536; counts multinomial
   over p_k ~ k^-1.1, then experts 56..63 overwritten with uniform integers in
   [0, 8] (expert 63 forced to 0) and expert 0 absorbing the difference; seed 3.
@@ -32,7 +34,7 @@ import numpy as np
 import torch
 
 MXFP8, NVFP4 = 0, 1
-SWIGLU, SRELU = 0, 1
+SWIGLU, SRELU, TANH_SRELU = 0, 1, 2
 
 
 @dataclass(frozen=True)
@@ -46,6 +48,7 @@ class Workload:
     M: int
     seed: int
     quant_only: bool = False
+    tanh_clamp_scale: float = 0.0   # tanh-SReLU soft-clamp scale
 
     @property
     def n1(self) -> int:
@@ -62,6 +65,7 @@ WORKLOADS = {
     "mx_swiglu": Workload("mx_swiglu", MXFP8, SWIGLU, 8, 2048, 1024, 16384, 1),
     "nv_srelu": Workload("nv_srelu", NVFP4, SRELU, 8, 4096, 2048, 32768, 2),
     "mx_skew": Workload("mx_skew", MXFP8, SWIGLU, 64, 7168, 2048, 65536, 3),
+    "nv_tanh_srelu": Workload("nv_tanh_srelu", NVFP4, TANH_SRELU, 8, 4096, 2048, 32768, 2, tanh_clamp_scale=8.0),
     "nv_quant": Workload("nv_quant", NVFP4, SRELU, 8, 4096, 0, 131072, 4, quant_only=True),
 }
 
@@ -74,7 +78,7 @@ def make_splits(w: Workload) -> np.ndarray:
         p = rng.dirichlet(np.ones(w.G))
         p[w.G - 1] = 0.0
         s = rng.multinomial(w.M, p / p.sum())
-    elif w.name == "nv_srelu":
+    elif w.name in ("nv_srelu", "nv_tanh_srelu"):
         s = np.full(w.G, w.M // w.G)
     elif w.name == "mx_skew":
         p = np.arange(1, w.G + 1, dtype=np.float64) ** -1.1
@@ -102,7 +106,7 @@ def _normal(gen, shape, std=1.0):
 
 def make_x(w: Workload, gen: torch.Generator) -> torch.Tensor:
     x = torch.randn((w.M, w.K), generator=gen, dtype=torch.float32)
-    if w.name == "nv_srelu":
+    if w.name in ("nv_srelu", "nv_tanh_srelu"):
         n_out = int(round(0.001 * w.M * w.K))
         idx = torch.randperm(w.M * w.K, generator=gen)[:n_out]
         x.view(-1)[idx] *= 50.0

@@ -19,7 +19,7 @@ Layout:
 Parity pins live in tests/test_oracle_*.py.  Functions without a pin: none.
 """
 from ._lib import build, lib  # noqa: F401
-from .forward import SRELU, SWIGLU, activation, dequant_weight, forward, quantize_weights  # noqa: F401
+from .forward import SRELU, SWIGLU, TANH_SRELU, activation, dequant_weight, forward, quantize_weights  # noqa: F401
 from .layout import (compact_to_tiled, group_offsets, tile_bases, tiled_index, tiled_size,  # noqa: F401
                      tiled_to_compact, tiled_to_x4)
 from .quant import (MXFP8, NVFP4, amax_bf16, bf16_to_f64, f64_to_bf16, group_amax,  # noqa: F401

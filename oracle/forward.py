@@ -18,7 +18,7 @@ from .quant import (MXFP8, NVFP4, amax_bf16, bf16_to_f64, f64_to_bf16, group_had
                     mxfp8_dequant_rows, mxfp8_quantize_rows, nvfp4_dequant_rows, nvfp4_global_scale,
                     nvfp4_quantize_rows)
 
-SWIGLU, SRELU = 0, 1
+SWIGLU, SRELU, TANH_SRELU = 0, 1, 2
 
 
 def quantize_weights(W, fmt: int) -> dict:
@@ -47,22 +47,29 @@ def dequant_weight(qw: dict, g: int, fmt: int) -> np.ndarray:
     return nvfp4_dequant_rows(qw["codes"][g], qw["scales"][g], qw["S"][g])
 
 
-def activation(h: np.ndarray, act: int) -> np.ndarray:
+def activation(h: np.ndarray, act: int, tanh_clamp_scale: float | None = None) -> np.ndarray:
     """SwiGLU: silu(gate) * up with gate = first half of the fc1 columns, up =
-    second half, silu(u) = u / (1 + exp(-u)); SReLU: max(h, 0)^2.  float64."""
+    second half, silu(u) = u / (1 + exp(-u)); SReLU: max(h, 0)^2; tanh-SReLU
+    (PR #3837 Changes, "ScaledTanhSReLU", the SReLU soft clamp with
+    tanh_clamp_scale c; reading: the soft clamp of the SReLU output at c):
+    c * tanh(max(h, 0)^2 / c).  float64."""
     if act == SWIGLU:
         n = h.shape[1] // 2
         gate, up = h[:, :n], h[:, n:]
         return gate / (1.0 + np.exp(-gate)) * up
-    return np.square(np.maximum(h, 0.0))
+    t = np.square(np.maximum(h, 0.0))
+    if act == TANH_SRELU:
+        c = float(tanh_clamp_scale)
+        return c * np.tanh(t / c)
+    return t
 
 
 def forward(x, splits, W1, W2, probs, act: int, fmt: int, *, rows=None, qw1=None, qw2=None,
-            rht_mask: int = 0) -> dict:
+            rht_mask: int = 0, tanh_clamp_scale: float | None = None) -> dict:
     """Oracle forward.
 
     x [M, K] bf16 bits (uint16), token-sorted; splits [G]; W1 [G, N1, K] with
-    N1 = 2N (SwiGLU, gate rows then up rows) or N (SReLU); W2 [G, K, N];
+    N1 = 2N (SwiGLU, gate rows then up rows) or N (SReLU, tanh-SReLU); W2 [G, K, N];
     probs [M] float32 or None (= 1).
 
     Steps per group g (rows off_g .. off_g + m_g):
@@ -127,7 +134,7 @@ def forward(x, splits, W1, W2, probs, act: int, fmt: int, *, rows=None, qw1=None
         # step 2-4
         acc = xd @ dequant_weight(qw1, g, fmt).T
         h = bf16_to_f64(f64_to_bf16(acc))
-        a = activation(h, act)
+        a = activation(h, act, tanh_clamp_scale)
         f = f64_to_bf16(a * probs[sel].astype(np.float64)[:, None])
         out["fc2x"][sel] = f
         # step 5

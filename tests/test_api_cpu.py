@@ -179,3 +179,20 @@ def test_forward_columnwise_fc2x_checks(lib):
     assert L.gmlp_forward(FAKE, 512, 256, 256, FAKE, 4, ctypes.byref(w1), ctypes.byref(w2), None, g.SWIGLU,
                           ctypes.byref(r), FAKE, ctypes.byref(aux), FAKE, need, None) == g.ERR_INVALID_ARG
     assert b"NVFP4" in L.gmlp_last_error()
+
+
+def test_forward_tanh_srelu_needs_a_clamp_scale(lib):
+    L, g = lib
+    r = g.recipe(g.NVFP4)
+    w1 = g.QWeightC(FAKE, FAKE, FAKE, 256, 256, 4, g.NVFP4, 0, 0)
+    w2 = g.QWeightC(FAKE, FAKE, FAKE, 256, 256, 4, g.NVFP4, 0, 0)
+    need = g.forward_workspace_size(512, 256, 256, 4, g.TANH_SRELU, r)
+
+    def call(aux):
+        return L.gmlp_forward(FAKE, 512, 256, 256, FAKE, 4, ctypes.byref(w1), ctypes.byref(w2), None, g.TANH_SRELU,
+                              ctypes.byref(r), FAKE, aux, FAKE, need, None)
+
+    assert call(None) == g.ERR_INVALID_ARG
+    assert call(ctypes.byref(g.FwdAux(tanh_clamp_scale=0.0))) == g.ERR_INVALID_ARG
+    assert call(ctypes.byref(g.FwdAux(tanh_clamp_scale=float("inf")))) == g.ERR_INVALID_ARG
+    assert b"tanh" in L.gmlp_last_error()

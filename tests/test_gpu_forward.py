@@ -26,7 +26,7 @@ def bf16_cpu(a):
     return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
 
 
-def run_gpu(gm, d, fmt, act, mask=0, probs=True, gemm_mode=0, x4=None):
+def run_gpu(gm, d, fmt, act, mask=0, probs=True, gemm_mode=0, x4=None, tanh_c=0.0):
     # NVFP4 weights carry the replicated (GEMM_TILED_X4) scales by default; the
     # CTA-pair mode reads GEMM_TILED ones
     if gemm_mode == 2:
@@ -46,7 +46,8 @@ def run_gpu(gm, d, fmt, act, mask=0, probs=True, gemm_mode=0, x4=None):
     rec = gm.recipe(fmt, use_rht=True, mask=mask)
     p = d["probs"].cuda() if probs else None
     y = torch.full((M, d["x"].shape[1]), float("nan"), dtype=torch.bfloat16, device="cuda")
-    gm.forward(d["x"].cuda(), d["splits"].cuda(), w1, w2, p, act, rec, y=y, aux=aux, gemm_mode=gemm_mode)
+    gm.forward(d["x"].cuda(), d["splits"].cuda(), w1, w2, p, act, rec, y=y, aux=aux, gemm_mode=gemm_mode,
+               tanh_clamp_scale=tanh_c)
     gm.check_device_status()
     torch.cuda.synchronize()
     return y, aux
@@ -183,9 +184,9 @@ def forward_parity(orc, gm, name, rows=None, gemm_mode=0):
     d = make_inputs(name)
     w = d["workload"]
     splits = d["splits"].numpy()
-    y, aux = run_gpu(gm, d, w.fmt, w.act, mask=d["mask"], gemm_mode=gemm_mode)
+    y, aux = run_gpu(gm, d, w.fmt, w.act, mask=d["mask"], gemm_mode=gemm_mode, tanh_c=w.tanh_clamp_scale)
     ref = orc.forward(bits(d["x"]), splits, bits(d["W1"]), bits(d["W2"]), d["probs"].numpy(), w.act, w.fmt,
-                      rows=rows, rht_mask=d["mask"])
+                      rows=rows, rht_mask=d["mask"], tanh_clamp_scale=w.tanh_clamp_scale)
     sel = ref["rows"]
     cdiv, blk = (1, 32) if w.fmt == 0 else (2, 16)
     g_codes = np_u8(aux["fc2x_codes"], w.M * w.N // cdiv).reshape(w.M, -1)
@@ -225,6 +226,38 @@ def test_forward_nv_srelu_full(orc, gm):
     np.testing.assert_allclose(aux["fc2x_amax_post"].cpu().numpy(), ref["fc2x_amax_post"], rtol=2e-2)
 
 
+def test_forward_nv_tanh_srelu_full(orc, gm):
+    """NVFP4 + RHT tanh-SReLU on the nv_srelu inputs (soft-clamp scale 8)."""
+    d, y, aux, ref = forward_parity(orc, gm, "nv_tanh_srelu")
+    np.testing.assert_allclose(aux["fc2x_amax_pre"].cpu().numpy(), ref["fc2x_amax_pre"], rtol=2e-2)
+    assert aux["fc2x_amax_pre"].max().item() <= 8.0   # the clamp bounds fc2_x by c (probs <= 1)
+
+
+@pytest.mark.parametrize("fmt", [0, 1], ids=["mxfp8", "nvfp4"])
+def test_forward_tanh_srelu_small(orc, gm, fmt):
+    """tanh-SReLU on ragged groups, clamp scale 0.5 so most outputs are clamped."""
+    rng = np.random.default_rng(41 + fmt)
+    splits, K, N = [130, 0, 257, 5, 1, 128], 512, 512
+    G, M = len(splits), sum(splits)
+    d = dict(x=bf16_cpu(rng.standard_normal((M, K))), splits=torch.tensor(splits, dtype=torch.int64),
+             W1=bf16_cpu(rng.standard_normal((G, N, K)) / np.sqrt(K)),
+             W2=bf16_cpu(rng.standard_normal((G, K, N)) / np.sqrt(N)),
+             probs=torch.from_numpy(rng.uniform(0, 1, M).astype(np.float32)))
+    y, aux = run_gpu(gm, d, fmt, 2, mask=0x1357, tanh_c=0.5)
+    ref = orc.forward(bits(d["x"]), np.array(splits), bits(d["W1"]), bits(d["W2"]), d["probs"].numpy(), 2, fmt,
+                      rht_mask=0x1357, tanh_clamp_scale=0.5)
+    cdiv, blk = (1, 32) if fmt == 0 else (2, 16)
+    gS = oS = None
+    if fmt == 1:
+        gS = np.repeat([orc.nvfp4_global_scale(a) for a in aux["fc2x_amax_pre"].cpu().numpy()], splits)
+        oS = np.repeat(ref["fc2x_S"], splits)
+    frac, steps = code_match_report(fmt, np_u8(aux["fc2x_codes"], M * N // cdiv).reshape(M, -1), ref["fc2x_codes"],
+                                    orc.tiled_to_compact(np_u8(aux["fc2x_scales"]), splits, N // blk),
+                                    ref["fc2x_scales"], gS, oS)
+    assert frac >= CODE_MATCH and steps <= 1.0 + 1e-9, (frac, steps)
+    assert frob(y.float().cpu().numpy(), orc.bf16_to_f64(ref["y"])) <= Y_TOL
+
+
 def test_forward_mx_skew_sampled(orc, gm):
     """Zipf-skewed 64 experts at full size; the oracle evaluates a row sample that
     covers every non-empty expert (MXFP8 rows are independent)."""
@@ -242,12 +275,14 @@ def test_forward_mx_skew_sampled(orc, gm):
     forward_parity(orc, gm, "mx_skew", rows=rows)
 
 
-def test_fused_amax_equals_standalone_hadamard_amax(orc, gm):
+@pytest.mark.parametrize("act", [1, 2], ids=["srelu", "tanh_srelu"])
+def test_fused_amax_equals_standalone_hadamard_amax(orc, gm, act):
     """The NVFP4 fc1 epilogue's (pre, post)-RHT amax of fc2_x is bit-identical to
-    the standalone group Hadamard-amax pass over the bf16 fc2_x it stored."""
+    the standalone group Hadamard-amax pass over the bf16 fc2_x it stored (the
+    pages check this for SReLU, tanh-SReLU and SwiGLU)."""
     d = make_inputs("tiny")
     d["W1"] = d["W1"][:, :256].contiguous()      # SReLU: W1 [G, N, K]
-    _, aux = run_gpu(gm, d, 1, 1, mask=0x9C31)
+    _, aux = run_gpu(gm, d, 1, act, mask=0x9C31, tanh_c=0.5)
     pre, post = gm.group_hadamard_amax(aux["fc2x_bf16"], d["splits"].cuda(), 0x9C31)
     assert torch.equal(pre, aux["fc2x_amax_pre"])
     assert torch.equal(post, aux["fc2x_amax_post"])

@@ -123,3 +123,37 @@ def test_forward_row_subset_matches_full(orc):
     part = orc.forward(*args, rows=rows)
     assert np.array_equal(part["y"][rows], full["y"][rows])
     assert np.array_equal(part["fc2x_codes"][rows], full["fc2x_codes"][rows])
+
+
+def test_tanh_srelu_activation_closed_forms(orc):
+    """c * tanh(max(h,0)^2 / c): zero for h <= 0; the SReLU value while h^2 << c
+    (tanh z = z - z^3/3 + ...); exactly c once tanh saturates in float64; c/2 at
+    h^2 = c * atanh(1/2); increasing in h and below c."""
+    c = 8.0
+    h = np.array([[-3.0, -0.0, 0.0, 1e-3, 100.0, np.sqrt(c * np.arctanh(0.5))]])
+    y = orc.activation(h, orc.TANH_SRELU, c)[0]
+    assert y[0] == 0.0 and y[1] == 0.0 and y[2] == 0.0
+    assert abs(y[3] / 1e-6 - 1.0) < 1e-12
+    assert y[4] == c
+    assert abs(y[5] - c / 2) < 1e-12
+    hs = np.linspace(0, 6, 1001)[None, :]
+    ys = orc.activation(hs, orc.TANH_SRELU, c)[0]
+    assert np.all(np.diff(ys) > 0) and ys.max() < c
+    # the clamp only acts on large outputs: equal to SReLU within the cubic term
+    sr = orc.activation(hs, orc.SRELU)[0]
+    assert np.all(np.abs(ys - sr) <= sr ** 3 / (3 * c * c) + 1e-15)
+
+
+def test_tanh_srelu_forward_reduces_to_srelu_for_a_huge_clamp(orc):
+    """With c = 1e30 the clamp is the identity to far below bf16 resolution, so
+    the whole forward (activation, x prob, bf16, fc2_x quantisation, fc2) gives
+    SReLU's bytes: the tanh branch is wired in the same place."""
+    d = make_inputs("tiny")
+    x, W1, W2 = bits(d["x"]), bits(d["W1"]), bits(d["W2"])
+    splits = d["splits"].numpy()
+    G, N = len(splits), W2.shape[2]
+    W1s = W1[:, :N, :]                    # SReLU / tanh-SReLU take N fc1 rows
+    for fmt in (orc.MXFP8, orc.NVFP4):
+        a = orc.forward(x, splits, W1s, W2, d["probs"].numpy(), orc.SRELU, fmt)
+        b = orc.forward(x, splits, W1s, W2, d["probs"].numpy(), orc.TANH_SRELU, fmt, tanh_clamp_scale=1e30)
+        assert np.array_equal(a["fc2x"], b["fc2x"]) and np.array_equal(a["y"], b["y"])
