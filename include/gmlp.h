@@ -172,6 +172,18 @@ GMLP_API gmlp_status gmlp_group_quantize(const uint16_t* x, int64_t M, int64_t K
                                 const gmlp_qtensor* row_out, const gmlp_qtensor* col_out,
                                 float* amax_pre, float* amax_post, gmlp_stream stream);
 
+/* gmlp_prepare_weights_discrete -- as gmlp_prepare_weights, but expert g's
+ * bf16 weight [rows][cols] is at W_experts[g] (a host array of G device
+ * pointers, each 16-byte aligned; PR #2769 discusses discrete per-expert
+ * weights next to the single grouped weight).  The outputs are the same
+ * stacked codes, GEMM_TILED scales, amax and global_scale, so the forward
+ * reads either alike.  One quantisation launch per expert (plus one amax
+ * launch for NVFP4). */
+GMLP_API gmlp_status gmlp_prepare_weights_discrete(const uint16_t* const* W_experts, int32_t G, int64_t rows,
+                                                   int64_t cols, int32_t swiglu_interleave, int32_t format,
+                                                   uint8_t* codes, uint8_t* scales, float* global_scale,
+                                                   float* amax, gmlp_stream stream);
+
 /* gmlp_replicate_weight_scales -- GEMM_TILED_X4 copy of NVFP4 weight scales
  * (no counterpart on the pages: a layout for this GEMM).  `tiled` holds the
  * GEMM_TILED scales of G experts of `rows` rows (from gmlp_prepare_weights,
@@ -200,6 +212,11 @@ typedef struct gmlp_qweight {
   int32_t swiglu_interleaved; /* 1: rows hold the SwiGLU gate/up interleave below */
   int32_t scale_layout;       /* layout of `scales`: 0 or GMLP_SCALES_GEMM_TILED, or (NVFP4)
                                  GMLP_SCALES_GEMM_TILED_X4 from gmlp_replicate_weight_scales */
+  const uint16_t* bias;       /* optional bf16 [G][rows] in logical row order (fc1 SwiGLU: gate rows
+                                 [0,N) then up rows [N,2N), whatever the interleave of `codes`); the
+                                 GEMM adds it to the FP32 accumulator (after the NVFP4 1/(S_a S_b)
+                                 factor) before the bf16 rounding (PR #2769: the FC1 kernel takes a
+                                 bias); 16-byte aligned; NULL = none */
 } gmlp_qweight;
 
 /* gmlp_prepare_weights -- per-expert quantisation of stacked bf16 weights W

@@ -141,6 +141,55 @@ int num_sms() {
 
 using namespace gmlp;
 
+// Weight quantisation of G experts, either stacked (Wp[0] -> [G][rows][cols])
+// or one pointer per expert (discrete: Wp[g] -> [rows][cols]); the outputs
+// are the same stacked codes, GEMM_TILED scales (expert g's tiles from g *
+// rows / 128) and per-expert amax / global scale.
+static gmlp_status prepare_weights_impl(const uint16_t* const* Wp, bool discrete, int32_t G, int64_t rows,
+                                        int64_t cols, int32_t swiglu_interleave, int32_t format, uint8_t* codes,
+                                        uint8_t* scales, float* global_scale, float* amax, cudaStream_t s) {
+  if (G < 1 || G > kMaxGroups) return fail(GMLP_ERR_INVALID_DIMS, "G = %d outside [1, %d]", G, kMaxGroups);
+  if (format != GMLP_MXFP8 && format != GMLP_NVFP4) return fail(GMLP_ERR_UNSUPPORTED_RECIPE, "format %d", format);
+  if (rows <= 0 || rows % 128 || (int64_t)G * rows > 0x7FFFFFFF)
+    return fail(GMLP_ERR_INVALID_DIMS, "rows = %lld must be a positive multiple of 128", (long long)rows);
+  const int64_t cmod = format == GMLP_MXFP8 ? 128 : 256;
+  if (cols <= 0 || cols % cmod)
+    return fail(GMLP_ERR_INVALID_DIMS, "cols = %lld must be a positive multiple of %lld", (long long)cols, (long long)cmod);
+  if (swiglu_interleave && rows % 64) return fail(GMLP_ERR_INVALID_DIMS, "SwiGLU interleave needs rows %% 64 == 0");
+  const int n_src = discrete ? G : 1;
+  for (int i = 0; i < n_src; ++i)
+    if (!Wp[i] || !aligned16(Wp[i])) return fail(GMLP_ERR_INVALID_ARG, "weight %d NULL or not 16-byte aligned", i);
+  if (!codes || !scales || !aligned16(codes) || !aligned16(scales))
+    return fail(GMLP_ERR_INVALID_ARG, "codes/scales NULL or not 16-byte aligned");
+  if (format == GMLP_NVFP4 && (!global_scale || !amax))
+    return fail(GMLP_ERR_INVALID_ARG, "NVFP4 weights need global_scale and amax buffers");
+  GMLP_TRY(check_device());
+  const int64_t code_bytes = rows * cols / (format == GMLP_MXFP8 ? 1 : 2);           // per expert
+  const int64_t scale_bytes = rows / 128 * (cols / (format == GMLP_MXFP8 ? 32 : 16) / 4) * 512;
+  const int calls = discrete ? G : 1;
+  const int32_t Gc = discrete ? 1 : G;
+  for (int i = 0; i < calls; ++i) {
+    GroupSrc gs{nullptr, (int32_t)rows, Gc, (int64_t)Gc * rows};
+    RowQuantArgs a{};
+    a.x = Wp[i];
+    a.M = (int64_t)Gc * rows;
+    a.K = cols;
+    a.grp = gs;
+    a.format = format;
+    a.tiled = 1;
+    a.codes = codes + i * code_bytes;
+    a.scales = scales + i * scale_bytes;
+    a.swiglu_interleave = swiglu_interleave != 0;
+    if (format == GMLP_NVFP4) {
+      GMLP_CUDA(launch_group_amax(Wp[i], a.M, cols, gs, amax + i, s), "group_amax launch");
+      a.amax = amax + i;
+      a.S_out = global_scale + i;
+    }
+    GMLP_CUDA(launch_row_quant(a, s), "row_quant launch");
+  }
+  return GMLP_OK;
+}
+
 extern "C" {
 
 const char* gmlp_last_error(void) { return g_last_error; }
@@ -276,38 +325,17 @@ gmlp_status gmlp_prepare_weights(const uint16_t* W, int32_t G, int64_t rows, int
                                  int32_t format, uint8_t* codes, uint8_t* scales, float* global_scale, float* amax,
                                  gmlp_stream stream) {
   g_last_error[0] = 0;
-  if (G < 1 || G > kMaxGroups) return fail(GMLP_ERR_INVALID_DIMS, "G = %d outside [1, %d]", G, kMaxGroups);
-  if (format != GMLP_MXFP8 && format != GMLP_NVFP4) return fail(GMLP_ERR_UNSUPPORTED_RECIPE, "format %d", format);
-  if (rows <= 0 || rows % 128 || (int64_t)G * rows > 0x7FFFFFFF)
-    return fail(GMLP_ERR_INVALID_DIMS, "rows = %lld must be a positive multiple of 128", (long long)rows);
-  const int64_t cmod = format == GMLP_MXFP8 ? 128 : 256;
-  if (cols <= 0 || cols % cmod)
-    return fail(GMLP_ERR_INVALID_DIMS, "cols = %lld must be a positive multiple of %lld", (long long)cols, (long long)cmod);
-  if (swiglu_interleave && rows % 64) return fail(GMLP_ERR_INVALID_DIMS, "SwiGLU interleave needs rows %% 64 == 0");
-  if (!W || !codes || !scales || !aligned16(W) || !aligned16(codes) || !aligned16(scales))
-    return fail(GMLP_ERR_INVALID_ARG, "W/codes/scales NULL or not 16-byte aligned");
-  if (format == GMLP_NVFP4 && (!global_scale || !amax))
-    return fail(GMLP_ERR_INVALID_ARG, "NVFP4 weights need global_scale and amax buffers");
-  GMLP_TRY(check_device());
-  cudaStream_t s = (cudaStream_t)stream;
-  GroupSrc gs{nullptr, (int32_t)rows, G, (int64_t)G * rows};
-  RowQuantArgs a{};
-  a.x = W;
-  a.M = (int64_t)G * rows;
-  a.K = cols;
-  a.grp = gs;
-  a.format = format;
-  a.tiled = 1;
-  a.codes = codes;
-  a.scales = scales;
-  a.swiglu_interleave = swiglu_interleave != 0;
-  if (format == GMLP_NVFP4) {
-    GMLP_CUDA(launch_group_amax(W, a.M, cols, gs, amax, s), "group_amax launch");
-    a.amax = amax;
-    a.S_out = global_scale;
-  }
-  GMLP_CUDA(launch_row_quant(a, s), "row_quant launch");
-  return GMLP_OK;
+  return prepare_weights_impl(&W, false, G, rows, cols, swiglu_interleave, format, codes, scales, global_scale, amax,
+                              (cudaStream_t)stream);
+}
+
+gmlp_status gmlp_prepare_weights_discrete(const uint16_t* const* W_experts, int32_t G, int64_t rows, int64_t cols,
+                                          int32_t swiglu_interleave, int32_t format, uint8_t* codes, uint8_t* scales,
+                                          float* global_scale, float* amax, gmlp_stream stream) {
+  g_last_error[0] = 0;
+  if (!W_experts) return fail(GMLP_ERR_INVALID_ARG, "W_experts NULL");
+  return prepare_weights_impl(W_experts, true, G, rows, cols, swiglu_interleave, format, codes, scales, global_scale,
+                              amax, (cudaStream_t)stream);
 }
 
 size_t gmlp_forward_workspace_size(int64_t M, int64_t K, int64_t N, int32_t G, int32_t act,
@@ -357,6 +385,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   if (!W1->codes || !W1->scales || !W2->codes || !W2->scales || !aligned16(W1->codes) || !aligned16(W1->scales) ||
       !aligned16(W2->codes) || !aligned16(W2->scales))
     return fail(GMLP_ERR_INVALID_ARG, "weight codes/scales NULL or not 16-byte aligned");
+  if (!aligned16(W1->bias) || !aligned16(W2->bias)) return fail(GMLP_ERR_INVALID_ARG, "weight bias not 16-byte aligned");
   if (fmt == GMLP_NVFP4 && (!W1->global_scale || !W2->global_scale))
     return fail(GMLP_ERR_INVALID_ARG, "NVFP4 weights need global_scale");
   if ((M > 0 && (!x || !y)) || !aligned16(x) || !aligned16(y))
@@ -415,6 +444,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     g1.a_scales = x_scales;
     g1.b_codes = W1->codes;
     g1.b_scales = W1->scales;
+    g1.bias = W1->bias;
     g1.M = M;
     g1.kbytes = K;
     g1.n_out = n1;
@@ -435,6 +465,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     g2.a_scales = f_scales;
     g2.b_codes = W2->codes;
     g2.b_scales = W2->scales;
+    g2.bias = W2->bias;
     g2.M = M;
     g2.kbytes = N;
     g2.n_out = K;
@@ -483,6 +514,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   g1.a_scales = x_scales;
   g1.b_codes = W1->codes;
   g1.b_scales = W1->scales;
+  g1.bias = W1->bias;
   g1.M = M;
   g1.kbytes = K / 2;
   g1.n_out = n1;
@@ -541,6 +573,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   g2.a_scales = f_scales;
   g2.b_codes = W2->codes;
   g2.b_scales = W2->scales;
+  g2.bias = W2->bias;
   g2.M = M;
   g2.kbytes = N / 2;
   g2.n_out = K;

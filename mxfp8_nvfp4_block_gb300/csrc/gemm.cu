@@ -165,6 +165,31 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
   const int64_t grow = (int64_t)off[t.g] + lr;
   float alpha = 1.0f;
   if (FMT == GMLP_NVFP4) alpha = __fdiv_rn(1.0f, __fmul_rn(nvfp4_global_scale(a.a_amax[t.g]), a.b_S[t.g]));
+  if (a.bias) {
+    // per-expert bias, added to the FP32 accumulator before any rounding; the
+    // slice's two 32-column runs map to logical rows b0 and b1 of the bias
+    // (SwiGLU: its gate and up rows under the 32-row interleave)
+    const uint16_t* bg = a.bias + (int64_t)t.g * a.n_out;
+    int b0, b1;
+    if (EPI == EPI_FC1_SWIGLU) {
+      const int c = t.nt * (kBN / 64) + slice;
+      b0 = 32 * c;
+      b1 = (int)(a.n_out / 2) + 32 * c;
+    } else {
+      b0 = t.nt * kBN + slice * kSliceCols;
+      b1 = b0 + 32;
+    }
+#pragma unroll
+    for (int j = 0; j < kSliceCols; j += 8) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(bg + (j < 32 ? b0 + j : b1 + (j - 32))));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        acc[j + k] = __fadd_rn(__fmul_rn(acc[j + k], alpha),
+                               bf16_bits_to_float((k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu)));
+    }
+    alpha = 1.0f;
+  }
 
   if (EPI == EPI_FC2) {
     if (!valid) return;

@@ -88,6 +88,7 @@ struct GemmArgs {
   GroupSrc grp;
   const float* a_amax;     // NVFP4: per-group amax of A (S_a = 2688 / amax)
   const float* b_S;        // NVFP4: per-expert S of B
+  const uint16_t* bias;    // optional bf16 [G][n_out], logical row order of B (before any interleave)
   const float* probs;      // fc1: [M] or null
   // MXFP8 fc1 outputs (fc2_x quantised in the epilogue)
   uint8_t* out_codes;      // [M][n_cols_out]

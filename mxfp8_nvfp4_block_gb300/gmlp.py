@@ -25,7 +25,8 @@ SCALES_GEMM_TILED, SCALES_GEMM_TILED_X4 = GEMM_TILED, GEMM_TILED_X4
 EXPORTS = ["gmlp_tiled_scales_bytes", "gmlp_group_hadamard_amax", "gmlp_group_quantize_with_amax",
            "gmlp_group_quantize", "gmlp_prepare_weights", "gmlp_forward_workspace_size", "gmlp_forward",
            "gmlp_check_device_status", "gmlp_last_error", "gmlp_version", "gmlp_forward_noalloc",
-           "gmlp_selftest_bounded_wait", "gmlp_mma_peak", "gmlp_replicate_weight_scales"]
+           "gmlp_selftest_bounded_wait", "gmlp_mma_peak", "gmlp_replicate_weight_scales",
+           "gmlp_prepare_weights_discrete"]
 
 
 class Recipe(ctypes.Structure):
@@ -40,7 +41,8 @@ class QTensor(ctypes.Structure):
 class QWeightC(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("global_scale", ctypes.c_void_p),
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("G", ctypes.c_int32),
-                ("format", ctypes.c_int32), ("swiglu_interleaved", ctypes.c_int32), ("scale_layout", ctypes.c_int32)]
+                ("format", ctypes.c_int32), ("swiglu_interleaved", ctypes.c_int32), ("scale_layout", ctypes.c_int32),
+                ("bias", ctypes.c_void_p)]
 
 
 class FwdAux(ctypes.Structure):
@@ -71,6 +73,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gmlp_group_quantize": (_i32, [_vp, _i64, _i64, _vp, _i32, ctypes.POINTER(Recipe),
                                        ctypes.POINTER(QTensor), ctypes.POINTER(QTensor), _vp, _vp, _vp]),
         "gmlp_prepare_weights": (_i32, [_vp, _i32, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+        "gmlp_prepare_weights_discrete": (_i32, [ctypes.POINTER(ctypes.c_void_p), _i32, _i64, _i64, _i32, _i32, _vp,
+                                                 _vp, _vp, _vp, _vp]),
         "gmlp_forward_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i32, _i32, ctypes.POINTER(Recipe)]),
         "gmlp_forward": (_i32, [_vp, _i64, _i64, _i64, _vp, _i32, ctypes.POINTER(QWeightC),
                                 ctypes.POINTER(QWeightC), _vp, _i32, ctypes.POINTER(Recipe), _vp,
@@ -204,13 +208,14 @@ class QWeight:
     format: int
     swiglu: bool
     scales_x4: torch.Tensor | None = None  # NVFP4: GEMM_TILED_X4 copy the forward reads when present
+    bias: torch.Tensor | None = None       # optional bf16 [G, rows], logical row order
 
     def c(self) -> QWeightC:
         if self.scales_x4 is not None:
             return QWeightC(self.codes.data_ptr(), self.scales_x4.data_ptr(), _p(self.global_scale), self.rows,
-                            self.cols, self.G, self.format, int(self.swiglu), SCALES_GEMM_TILED_X4)
+                            self.cols, self.G, self.format, int(self.swiglu), SCALES_GEMM_TILED_X4, _p(self.bias))
         return QWeightC(self.codes.data_ptr(), self.scales.data_ptr(), _p(self.global_scale), self.rows,
-                        self.cols, self.G, self.format, int(self.swiglu), SCALES_GEMM_TILED)
+                        self.cols, self.G, self.format, int(self.swiglu), SCALES_GEMM_TILED, _p(self.bias))
 
 
 def replicate_weight_scales(q: "QWeight", stream=None) -> torch.Tensor:
@@ -220,23 +225,39 @@ def replicate_weight_scales(q: "QWeight", stream=None) -> torch.Tensor:
     return out
 
 
-def prepare_weights(W: torch.Tensor, fmt: int, swiglu_interleave: bool = False, x4: bool | None = None,
+def prepare_weights(W, fmt: int, swiglu_interleave: bool = False, x4: bool | None = None, bias=None,
                     stream=None) -> QWeight:
-    """Quantise stacked expert weights W [G, rows, cols] (bf16, cuda).  NVFP4
-    weights with rows and cols multiples of 256 also get the GEMM_TILED_X4
-    scale copy the forward reads (x4=False keeps GEMM_TILED only)."""
-    W = _bits(W)
-    G, rows, cols = W.shape
+    """Quantise expert weights: W is a stacked bf16 [G, rows, cols] cuda tensor,
+    or a list of G bf16 [rows, cols] tensors (discrete per-expert weights).
+    NVFP4 weights with rows and cols multiples of 256 also get the
+    GEMM_TILED_X4 scale copy the forward reads (x4=False keeps GEMM_TILED
+    only).  bias: optional bf16 [G, rows] added in fc1 / fc2."""
+    discrete = isinstance(W, (list, tuple))
+    if discrete:
+        Ws = [_bits(w) for w in W]
+        G, (rows, cols) = len(Ws), Ws[0].shape
+        dev = Ws[0].device
+    else:
+        W = _bits(W)
+        G, rows, cols = W.shape
+        dev = W.device
     blk, cdiv = (32, 1) if fmt == MXFP8 else (16, 2)
-    codes = _u8(G * rows * cols // cdiv, W.device)
-    scales = _u8(tiled_scales_bytes(G * rows, G, cols // blk), W.device)
+    codes = _u8(G * rows * cols // cdiv, dev)
+    scales = _u8(tiled_scales_bytes(G * rows, G, cols // blk), dev)
     gs = am = None
     if fmt == NVFP4:
-        gs = torch.empty(G, dtype=torch.float32, device=W.device)
-        am = torch.empty(G, dtype=torch.float32, device=W.device)
-    _check(load().gmlp_prepare_weights(_p(W), G, rows, cols, int(bool(swiglu_interleave)), fmt, _p(codes),
-                                       _p(scales), _p(gs), _p(am), _stream(stream)))
+        gs = torch.empty(G, dtype=torch.float32, device=dev)
+        am = torch.empty(G, dtype=torch.float32, device=dev)
+    if discrete:
+        ptrs = (ctypes.c_void_p * G)(*[w.data_ptr() for w in Ws])
+        _check(load().gmlp_prepare_weights_discrete(ptrs, G, rows, cols, int(bool(swiglu_interleave)), fmt,
+                                                    _p(codes), _p(scales), _p(gs), _p(am), _stream(stream)))
+    else:
+        _check(load().gmlp_prepare_weights(_p(W), G, rows, cols, int(bool(swiglu_interleave)), fmt, _p(codes),
+                                           _p(scales), _p(gs), _p(am), _stream(stream)))
     q = QWeight(codes, scales, gs, am, rows, cols, G, fmt, bool(swiglu_interleave))
+    if bias is not None:
+        q.bias = _bits(bias).reshape(G, rows).contiguous()
     if x4 is None:
         x4 = fmt == NVFP4 and rows % 256 == 0 and cols % 256 == 0
     if x4:

@@ -65,7 +65,7 @@ def activation(h: np.ndarray, act: int, tanh_clamp_scale: float | None = None) -
 
 
 def forward(x, splits, W1, W2, probs, act: int, fmt: int, *, rows=None, qw1=None, qw2=None,
-            rht_mask: int = 0, tanh_clamp_scale: float | None = None) -> dict:
+            rht_mask: int = 0, tanh_clamp_scale: float | None = None, b1=None, b2=None) -> dict:
     """Oracle forward.
 
     x [M, K] bf16 bits (uint16), token-sorted; splits [G]; W1 [G, N1, K] with
@@ -82,6 +82,9 @@ def forward(x, splits, W1, W2, probs, act: int, fmt: int, *, rows=None, qw1=None
          group's amax of f; the post-RHT amax of f (16-row column chunks, sign
          mask ``rht_mask``) is reported alongside.
       6. y = bf16(dq(fc2xq_g) @ dq(W2q_g)^T) in float64.
+    ``b1`` [G, N1] / ``b2`` [G, K]: optional per-expert biases (bf16 values, logical
+    row order) added to the float64 accumulators of steps 2 and 6 before their
+    bf16 rounding (PR #2769: the FC1 kernel takes a bias).
 
     ``rows``: optional sorted global row indices.  MXFP8 rows are independent, so
     only those rows are evaluated (the rest of y, fc2_x and the codes are zero).
@@ -133,6 +136,8 @@ def forward(x, splits, W1, W2, probs, act: int, fmt: int, *, rows=None, qw1=None
             xd = nvfp4_dequant_rows(*nvfp4_quantize_rows(xs, Sx), Sx)
         # step 2-4
         acc = xd @ dequant_weight(qw1, g, fmt).T
+        if b1 is not None:
+            acc = acc + np.asarray(b1, np.float64)[g][None, :]
         h = bf16_to_f64(f64_to_bf16(acc))
         a = activation(h, act, tanh_clamp_scale)
         f = f64_to_bf16(a * probs[sel].astype(np.float64)[:, None])
@@ -149,5 +154,8 @@ def forward(x, splits, W1, W2, probs, act: int, fmt: int, *, rows=None, qw1=None
             fd = nvfp4_dequant_rows(fq, fs, Sf)
         out["fc2x_codes"][sel], out["fc2x_scales"][sel] = fq, fs
         # step 6
-        out["y"][sel] = f64_to_bf16(fd @ dequant_weight(qw2, g, fmt).T)
+        acc2 = fd @ dequant_weight(qw2, g, fmt).T
+        if b2 is not None:
+            acc2 = acc2 + np.asarray(b2, np.float64)[g][None, :]
+        out["y"][sel] = f64_to_bf16(acc2)
     return out

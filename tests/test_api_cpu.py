@@ -196,3 +196,22 @@ def test_forward_tanh_srelu_needs_a_clamp_scale(lib):
     assert call(ctypes.byref(g.FwdAux(tanh_clamp_scale=0.0))) == g.ERR_INVALID_ARG
     assert call(ctypes.byref(g.FwdAux(tanh_clamp_scale=float("inf")))) == g.ERR_INVALID_ARG
     assert b"tanh" in L.gmlp_last_error()
+
+
+def test_prepare_weights_discrete_and_bias_checks(lib):
+    L, g = lib
+    ptrs = (ctypes.c_void_p * 2)(FAKE, None)
+    assert L.gmlp_prepare_weights_discrete(None, 2, 256, 256, 0, g.MXFP8, FAKE, FAKE, None, None, None) \
+        == g.ERR_INVALID_ARG
+    assert L.gmlp_prepare_weights_discrete(ptrs, 2, 256, 256, 0, g.MXFP8, FAKE, FAKE, None, None, None) \
+        == g.ERR_INVALID_ARG                                               # expert 1 NULL
+    assert b"weight 1" in L.gmlp_last_error()
+    assert L.gmlp_prepare_weights_discrete(ptrs, 2, 200, 256, 0, g.MXFP8, FAKE, FAKE, None, None, None) \
+        == g.ERR_INVALID_DIMS
+    r = g.recipe(g.MXFP8)
+    need = g.forward_workspace_size(512, 256, 256, 4, g.SRELU, r)
+    w1 = g.QWeightC(FAKE, FAKE, None, 256, 256, 4, g.MXFP8, 0, 0, FAKE + 2)   # misaligned bias
+    w2 = g.QWeightC(FAKE, FAKE, None, 256, 256, 4, g.MXFP8, 0, 0)
+    assert L.gmlp_forward(FAKE, 512, 256, 256, FAKE, 4, ctypes.byref(w1), ctypes.byref(w2), None, g.SRELU,
+                          ctypes.byref(r), FAKE, None, FAKE, need, None) == g.ERR_INVALID_ARG
+    assert b"bias" in L.gmlp_last_error()

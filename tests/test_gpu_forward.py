@@ -169,6 +169,85 @@ def test_forward_nvfp4_columnwise_fc2x(orc, gm, use_rht):
     assert np.array_equal(np_u8(aux["fc2x_col_scales"], len(ref["col_scales"])), ref["col_scales"])
 
 
+@pytest.mark.parametrize("fmt", [0, 1], ids=["mxfp8", "nvfp4"])
+def test_forward_biases_lossless_bitexact(orc, gm, fmt):
+    """Per-expert fc1 and fc2 biases on lossless operands (SReLU): fc2_x codes
+    and y bit-exact against the oracle, ragged and empty groups."""
+    rng = np.random.default_rng(23 + fmt)
+    splits, K, N = [130, 0, 257, 5, 128], 512, 256
+    G, M = len(splits), sum(splits)
+    offs = np.concatenate([[0], np.cumsum(splits)])
+    xs, bs = ([0.0, 1, 2, -1, -2], [0.0, 0.0, 1.0, -1.0, 2.0]) if fmt == 0 else ([0.0, 2, -2], [0.0, 2.0])
+    x = rng.choice(xs, size=(M, K))
+    for g in range(G):
+        if splits[g]:
+            x[offs[g]] = 2.0
+    W1 = np.zeros((G, N, K))
+    for g in range(G):
+        W1[g, np.arange(N), rng.integers(0, K, N)] = 1.0
+    W2 = np.zeros((G, K, N))
+    for g in range(G):
+        W2[g, np.arange(K), rng.integers(0, N, K)] = rng.choice([1.0, -1.0, 2.0], K)
+    b1 = rng.choice(bs, size=(G, N))
+    b2 = rng.choice([0.0, 1.0, -2.0, 4.0], size=(G, K))
+    xt, W1t, W2t = bf16_cpu(x), bf16_cpu(W1), bf16_cpu(W2)
+    b1t, b2t = bf16_cpu(b1), bf16_cpu(b2)
+    w1 = gm.prepare_weights(W1t.cuda(), fmt, bias=b1t.cuda())
+    w2 = gm.prepare_weights(W2t.cuda(), fmt, bias=b2t.cuda())
+    cdiv = 1 if fmt == 0 else 2
+    aux = {"fc2x_codes": torch.zeros(M * N // cdiv + 16, dtype=torch.uint8, device="cuda")}
+    y = gm.forward(xt.cuda(), torch.tensor(splits).cuda(), w1, w2, None, gm.SRELU, gm.recipe(fmt), aux=aux)
+    gm.check_device_status()
+    ref = orc.forward(bits(xt), np.array(splits), bits(W1t), bits(W2t), None, 1, fmt, b1=b1, b2=b2)
+    assert np.array_equal(np_u8(aux["fc2x_codes"], M * N // cdiv).reshape(M, -1), ref["fc2x_codes"])
+    assert np.array_equal(np_bits(y), ref["y"])
+
+
+def test_forward_swiglu_bias_follows_the_interleave(orc, gm):
+    """fc1 bias given in logical gate/up order reaches the right accumulator
+    columns of the interleaved W1 (MXFP8 SwiGLU, random data, tolerance)."""
+    rng = np.random.default_rng(29)
+    splits, K, N = [130, 0, 257, 5, 128], 512, 256
+    G, M = len(splits), sum(splits)
+    d = dict(x=bf16_cpu(rng.standard_normal((M, K))), splits=torch.tensor(splits, dtype=torch.int64),
+             W1=bf16_cpu(rng.standard_normal((G, 2 * N, K)) / np.sqrt(K)),
+             W2=bf16_cpu(rng.standard_normal((G, K, N)) / np.sqrt(N)),
+             probs=torch.from_numpy(rng.uniform(0, 1, M).astype(np.float32)))
+    b1 = bf16_cpu(rng.standard_normal((G, 2 * N)))
+    b2 = bf16_cpu(rng.standard_normal((G, K)) * 0.1)
+    w1 = gm.prepare_weights(d["W1"].cuda(), gm.MXFP8, swiglu_interleave=True, bias=b1.cuda())
+    w2 = gm.prepare_weights(d["W2"].cuda(), gm.MXFP8, bias=b2.cuda())
+    aux = {"fc2x_codes": torch.zeros(M * N + 16, dtype=torch.uint8, device="cuda"),
+           "fc2x_scales": torch.zeros(gm.tiled_scales_bytes(M, G, N // 32) + 16, dtype=torch.uint8, device="cuda")}
+    y = gm.forward(d["x"].cuda(), d["splits"].cuda(), w1, w2, d["probs"].cuda(), gm.SWIGLU, gm.recipe(gm.MXFP8),
+                   aux=aux)
+    gm.check_device_status()
+    ref = orc.forward(bits(d["x"]), np.array(splits), bits(d["W1"]), bits(d["W2"]), d["probs"].numpy(), 0, 0,
+                      b1=orc.bf16_to_f64(bits(b1)), b2=orc.bf16_to_f64(bits(b2)))
+    frac, steps = code_match_report(0, np_u8(aux["fc2x_codes"], M * N).reshape(M, -1), ref["fc2x_codes"],
+                                    orc.tiled_to_compact(np_u8(aux["fc2x_scales"]), splits, N // 32),
+                                    ref["fc2x_scales"])
+    assert frac >= CODE_MATCH and steps <= 1.0 + 1e-9, (frac, steps)
+    assert frob(y.float().cpu().numpy(), orc.bf16_to_f64(ref["y"])) <= Y_TOL
+
+
+@pytest.mark.parametrize("fmt,swiglu", [(0, True), (1, False)], ids=["mxfp8-swiglu", "nvfp4"])
+def test_prepare_weights_discrete_matches_stacked(gm, fmt, swiglu):
+    """One device pointer per expert gives the stacked preparation's bytes."""
+    rng = np.random.default_rng(37)
+    G, rows, cols = 3, 512, 512
+    W = bf16_cpu(rng.standard_normal((G, rows, cols)) * np.array([1.0, 1e-3, 30.0])[:, None, None]).cuda()
+    a = gm.prepare_weights(W, fmt, swiglu_interleave=swiglu)
+    b = gm.prepare_weights([W[g].clone() for g in range(G)], fmt, swiglu_interleave=swiglu)
+    gm.check_device_status()
+    assert torch.equal(a.codes, b.codes)
+    used = G * rows // 128 * (cols // (32 if fmt == 0 else 16) // 4) * 512
+    assert torch.equal(a.scales[:used], b.scales[:used])
+    if fmt == 1:
+        assert torch.equal(a.global_scale, b.global_scale) and torch.equal(a.amax, b.amax)
+        assert torch.equal(a.scales_x4, b.scales_x4)
+
+
 def test_replicate_weight_scales_bitexact(orc, gm):
     rng = np.random.default_rng(4)
     G, rows, cols = 3, 512, 768

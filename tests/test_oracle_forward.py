@@ -157,3 +157,36 @@ def test_tanh_srelu_forward_reduces_to_srelu_for_a_huge_clamp(orc):
         a = orc.forward(x, splits, W1s, W2, d["probs"].numpy(), orc.SRELU, fmt)
         b = orc.forward(x, splits, W1s, W2, d["probs"].numpy(), orc.TANH_SRELU, fmt, tanh_clamp_scale=1e30)
         assert np.array_equal(a["fc2x"], b["fc2x"]) and np.array_equal(a["y"], b["y"])
+
+
+@pytest.mark.parametrize("fmt_name", ["mxfp8", "nvfp4"])
+def test_biases_enter_before_rounding_exactly(orc, fmt_name):
+    """Integer biases on lossless operands: fc2_x = bf16((h + b1)^2 * prob) and
+    y = bf16(f @ W2^T + b2) exactly, for every group (fc1 bias before the
+    activation, fc2 bias before the output rounding)."""
+    fmt = orc.MXFP8 if fmt_name == "mxfp8" else orc.NVFP4
+    rng = np.random.default_rng(17)
+    G, K, N = 3, 64, 64
+    splits = np.array([7, 0, 12])
+    M = splits.sum()
+    offs = np.concatenate([[0], np.cumsum(splits)])
+    # operand sets kept exactly representable through both formats (NVFP4: h + b1
+    # in {0, +-2, 4} so fc2_x in {0, 4, 16})
+    xs, bs = ([0.0, 1, 2, -1, -2], [0.0, 0.0, 1.0, -1.0, 2.0]) if fmt == orc.MXFP8 else ([0.0, 2, -2], [0.0, 2.0])
+    x = rng.choice(xs, size=(M, K))
+    for g in range(G):
+        if splits[g]:
+            x[offs[g]] = 2.0
+    W1, perms = onehot_w1(rng, G, N, K)
+    b1 = rng.choice(bs, size=(G, N))
+    W2 = np.zeros((G, K, N))
+    for g in range(G):
+        W2[g, np.arange(K), rng.integers(0, N, K)] = rng.choice([1.0, -1.0, 2.0], K)
+    b2 = rng.choice([0.0, 1.0, -2.0, 4.0], size=(G, K))
+    probs = np.ones(M, np.float32)
+    out = orc.forward(as_bits(x), splits, as_bits(W1), as_bits(W2), probs, orc.SRELU, fmt, b1=b1, b2=b2)
+    for g in range(G):
+        sl = slice(offs[g], offs[g + 1])
+        f = np.maximum(x[sl][:, perms[g]] + b1[g], 0) ** 2
+        assert np.array_equal(out["fc2x"][sl], bf16_of(f)), g
+        assert np.array_equal(out["y"][sl], bf16_of(f @ W2[g].T + b2[g])), g
