@@ -259,6 +259,11 @@ typedef struct gmlp_fwd_aux {
   uint8_t* fc2x_col_codes;
   uint8_t* fc2x_col_scales;
   float tanh_clamp_scale;  /* GMLP_ACT_TANH_SRELU: the soft-clamp scale c (> 0, finite); aux is then required */
+  /* out, optional: the activation input h = bf16(fc1 accumulator) [M][N1] in
+   * logical column order (SwiGLU: gate columns [0,N), up [N,2N)), the tensor
+   * the backward's dGLU step reads (PR #2769 sequence diagram: c_tensor,
+   * swiglu_in).  16-byte aligned. */
+  uint16_t* fc1_pre_act;
 } gmlp_fwd_aux;
 
 /* Workspace bytes gmlp_forward needs for these sizes (x and fc2_x codes and
@@ -317,6 +322,33 @@ GMLP_API gmlp_status gmlp_forward_noalloc(const uint16_t* x, int64_t M, int64_t 
 /* Synchronises `stream`, then reads and clears the device status word the
  * kernels set on a bounded-wait timeout or inconsistent split sizes. */
 GMLP_API gmlp_status gmlp_check_device_status(gmlp_stream stream);
+
+/* Workspace bytes gmlp_backward_dgrad needs (dy and fc1_dy codes and scales). */
+GMLP_API size_t gmlp_backward_workspace_size(int64_t M, int64_t K, int64_t N, int32_t G, int32_t act);
+
+/* gmlp_backward_dgrad -- the data-gradient half of the fused grouped-MLP
+ * backward, MXFP8 (PR #2769 sequence diagram, backward pass: "FC2 dGLU
+ * kernel" then "FC1 dGrad kernel"; the weight gradients are not computed):
+ *   1. dy [M,K] bf16 -> rowwise MXFP8 (1x32 blocks along K);
+ *   2. per expert g: dfc2x = bf16(dq(dy_g) dq(W2t_g)^T) [m_g, N] (W2t = W2^T,
+ *      [N][K] per expert, quantised along K);
+ *   3. with the forward's activation input h (pre_act, gmlp_fwd_aux.fc1_pre_act)
+ *      and prob p: SwiGLU (g = h[:, :N], u = h[:, N:]): dg = dfc2x p u silu'(g),
+ *      du = dfc2x p silu(g); SReLU: dh = dfc2x p 2 max(h,0); fc1_dy =
+ *      bf16(dg | du) or bf16(dh) [M, N1], quantised to MXFP8 rowwise (codes and
+ *      GEMM_TILED scales to fc1_dy_codes / fc1_dy_scales when given);
+ *      dprob[t] = sum_n dfc2x[t,n] act(h)[t,n] (zeroed, then accumulated);
+ *   4. dx = bf16(dq(fc1_dy_g) dq(W1t_g)^T) [m_g, K] (W1t = W1^T in logical
+ *      gate/up order, [K][N1] per expert, quantised along N1).
+ * W2t / W1t come from gmlp_prepare_weights on the transposed bf16 weights
+ * (no interleave).  probs NULL = 1; dprob NULL skips it.  act: SWIGLU or SRELU.
+ * Limits: K % 256 == 0, N % 256 == 0. */
+GMLP_API gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_t N,
+                                         const int64_t* split_sizes, int32_t G, const gmlp_qweight* W2t,
+                                         const gmlp_qweight* W1t, const uint16_t* pre_act, const float* probs,
+                                         int32_t act, const gmlp_recipe* recipe, uint16_t* dx, float* dprob,
+                                         uint8_t* fc1_dy_codes, uint8_t* fc1_dy_scales, void* workspace,
+                                         size_t workspace_bytes, gmlp_stream stream);
 
 /* Self-test of the device failure path (no counterpart on the pages): one
  * warp waits, through the same bounded mbarrier wait the kernels use, on a

@@ -103,6 +103,27 @@ FwdLayout fwd_layout(int64_t M, int64_t K, int64_t N, int32_t G, int fmt) {
   return L;
 }
 
+struct BwdLayout {
+  size_t dy_codes, dy_scales, g_codes, g_scales, total;
+};
+
+// backward workspace: dy (MXFP8 rowwise, GEMM_TILED scales) and fc1_dy (same)
+BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N1, int32_t G) {
+  BwdLayout L{};
+  size_t cur = 0;
+  auto take = [&](size_t b) {
+    size_t o = cur;
+    cur += align256(b);
+    return o;
+  };
+  L.dy_codes = take((size_t)M * K);
+  L.dy_scales = take(tiled_bytes(M, G, K / 32));
+  L.g_codes = take((size_t)M * N1);
+  L.g_scales = take(tiled_bytes(M, G, N1 / 32));
+  L.total = cur;
+  return L;
+}
+
 gmlp_status check_recipe(const gmlp_recipe* r) {
   if (!r) return fail(GMLP_ERR_INVALID_ARG, "recipe is NULL");
   if (r->format != GMLP_MXFP8 && r->format != GMLP_NVFP4)
@@ -401,6 +422,9 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
         !aligned16(aux->fc2x_col_scales))
       return fail(GMLP_ERR_INVALID_ARG, "fc2x_col_codes / fc2x_col_scales: both, 16-byte aligned");
   }
+  if (aux && !aligned16(aux->fc1_pre_act)) return fail(GMLP_ERR_INVALID_ARG, "fc1_pre_act not 16-byte aligned");
+  if (aux && aux->gemm_mode == 2 && (aux->fc1_pre_act || W1->bias || W2->bias))
+    return fail(GMLP_ERR_INVALID_ARG, "gemm_mode 2 (CTA pairs) takes no biases and saves no activation input");
   if (aux && aux->gemm_mode != 0 && aux->gemm_mode != 2)
     return fail(GMLP_ERR_INVALID_ARG, "gemm_mode %d is neither 0 nor 2", aux->gemm_mode);
   GMLP_TRY(check_device());
@@ -451,6 +475,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     g1.grp = gs;
     g1.probs = probs;
     g1.tanh_c = tanh_c;
+    g1.pre_act_out = aux ? aux->fc1_pre_act : nullptr;
     g1.out_codes = f_codes;
     g1.out_scales = f_scales;
     g1.n_cols_out = N;
@@ -524,6 +549,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   g1.b_x4 = x4_1;
   g1.probs = probs;
   g1.tanh_c = tanh_c;
+  g1.pre_act_out = aux ? aux->fc1_pre_act : nullptr;
   g1.out_bf16 = f_bf16;
   g1.amax_pre = f_pre;
   g1.amax_post = f_post;
@@ -596,6 +622,106 @@ gmlp_status gmlp_selftest_bounded_wait(uint64_t limit_ns, gmlp_stream stream) {
     return fail(GMLP_ERR_INVALID_ARG, "limit_ns %llu outside [1 us, 2 s]", (unsigned long long)limit_ns);
   GMLP_TRY(check_device());
   GMLP_CUDA(launch_selftest_wait(limit_ns, (cudaStream_t)stream), "selftest launch");
+  return GMLP_OK;
+}
+
+size_t gmlp_backward_workspace_size(int64_t M, int64_t K, int64_t N, int32_t G, int32_t act) {
+  if (M < 0 || K <= 0 || N <= 0 || G < 1) return 0;
+  return bwd_layout(M, K, act == GMLP_ACT_SWIGLU ? 2 * N : N, G).total;
+}
+
+gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_t N, const int64_t* split_sizes,
+                                int32_t G, const gmlp_qweight* W2t, const gmlp_qweight* W1t,
+                                const uint16_t* pre_act, const float* probs, int32_t act, const gmlp_recipe* recipe,
+                                uint16_t* dx, float* dprob, uint8_t* fc1_dy_codes, uint8_t* fc1_dy_scales,
+                                void* workspace, size_t workspace_bytes, gmlp_stream stream) {
+  g_last_error[0] = 0;
+  GMLP_TRY(check_groups(G, M, split_sizes));
+  GMLP_TRY(check_recipe(recipe));
+  if (recipe->format != GMLP_MXFP8)
+    return fail(GMLP_ERR_UNSUPPORTED_RECIPE, "the backward dgrad path is MXFP8 (as the pages' backward)");
+  if (act != GMLP_ACT_SWIGLU && act != GMLP_ACT_SRELU)
+    return fail(GMLP_ERR_INVALID_ARG, "backward act = %d: SwiGLU or SReLU", act);
+  const int64_t N1 = act == GMLP_ACT_SWIGLU ? 2 * N : N;
+  if (K <= 0 || K % 256 || N <= 0 || N % 256)
+    return fail(GMLP_ERR_INVALID_DIMS, "K = %lld, N = %lld: both positive multiples of 256", (long long)K,
+                (long long)N);
+  if (!W2t || !W1t || W2t->G != G || W1t->G != G || W2t->format != GMLP_MXFP8 || W1t->format != GMLP_MXFP8)
+    return fail(GMLP_ERR_INVALID_ARG, "W2t / W1t: MXFP8 weights of G experts");
+  if (W2t->rows != N || W2t->cols != K || W1t->rows != K || W1t->cols != N1)
+    return fail(GMLP_ERR_INVALID_DIMS, "W2t must be [N x K] and W1t [K x N1] per expert (the transposed weights)");
+  if (W2t->swiglu_interleaved || W1t->swiglu_interleaved || W2t->bias || W1t->bias)
+    return fail(GMLP_ERR_INVALID_ARG, "transposed weights carry no interleave and no bias");
+  if (!W2t->codes || !W2t->scales || !W1t->codes || !W1t->scales || !aligned16(W2t->codes) ||
+      !aligned16(W2t->scales) || !aligned16(W1t->codes) || !aligned16(W1t->scales))
+    return fail(GMLP_ERR_INVALID_ARG, "weight codes/scales NULL or not 16-byte aligned");
+  if ((M > 0 && (!dy || !dx || !pre_act)) || !aligned16(dy) || !aligned16(dx) || !aligned16(pre_act))
+    return fail(GMLP_ERR_INVALID_ARG, "dy / dx / pre_act NULL or not 16-byte aligned");
+  if ((fc1_dy_codes == nullptr) != (fc1_dy_scales == nullptr) || !aligned16(fc1_dy_codes) ||
+      !aligned16(fc1_dy_scales))
+    return fail(GMLP_ERR_INVALID_ARG, "fc1_dy_codes / fc1_dy_scales: both or neither, 16-byte aligned");
+  if (probs && (reinterpret_cast<uintptr_t>(probs) & 3)) return fail(GMLP_ERR_INVALID_ARG, "probs misaligned");
+  const BwdLayout L = bwd_layout(M, K, N1, G);
+  if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
+    return fail(GMLP_ERR_WORKSPACE, "workspace %zu bytes, need %zu (16-byte aligned)", workspace_bytes, L.total);
+  GMLP_TRY(check_device());
+  if (M == 0) return GMLP_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* dy_codes = ws + L.dy_codes;
+  uint8_t* dy_scales = ws + L.dy_scales;
+  uint8_t* g_codes = fc1_dy_codes ? fc1_dy_codes : ws + L.g_codes;
+  uint8_t* g_scales = fc1_dy_scales ? fc1_dy_scales : ws + L.g_scales;
+  GroupSrc gs{split_sizes, 0, G, M};
+  if (dprob) GMLP_CUDA(cudaMemsetAsync(dprob, 0, sizeof(float) * M, s), "dprob memset");
+  {
+    RowQuantArgs q{};
+    q.x = dy;
+    q.M = M;
+    q.K = K;
+    q.grp = gs;
+    q.format = GMLP_MXFP8;
+    q.tiled = 1;
+    q.codes = dy_codes;
+    q.scales = dy_scales;
+    GMLP_CUDA(launch_row_quant(q, s), "dy quantise launch");
+  }
+  GemmArgs g1{};  // FC2 dGLU: dfc2x = dy W2 per expert, then dGLU x prob -> fc1_dy (MXFP8), dprob
+  g1.format = GMLP_MXFP8;
+  g1.epi = act == GMLP_ACT_SWIGLU ? EPI_DGLU_SWIGLU : EPI_DSRELU;
+  g1.a_codes = dy_codes;
+  g1.a_scales = dy_scales;
+  g1.b_codes = W2t->codes;
+  g1.b_scales = W2t->scales;
+  g1.M = M;
+  g1.kbytes = K;
+  g1.n_out = N;
+  g1.grp = gs;
+  g1.probs = probs;
+  g1.act_in = pre_act;
+  g1.dprob = dprob;
+  g1.out_codes = g_codes;
+  g1.out_scales = g_scales;
+  g1.n_cols_out = N1;
+  g1.pair = 1;
+  g1.pdl = 1;
+  GMLP_CUDA(launch_gemm(g1, s), "dGLU launch");
+  GemmArgs g2{};  // FC1 dgrad: dx = fc1_dy W1 per expert
+  g2.format = GMLP_MXFP8;
+  g2.epi = EPI_FC2;
+  g2.a_codes = g_codes;
+  g2.a_scales = g_scales;
+  g2.b_codes = W1t->codes;
+  g2.b_scales = W1t->scales;
+  g2.M = M;
+  g2.kbytes = N1;
+  g2.n_out = K;
+  g2.grp = gs;
+  g2.out_bf16 = dx;
+  g2.n_cols_out = K;
+  g2.pair = 1;
+  g2.pdl = 1;
+  GMLP_CUDA(launch_gemm(g2, s), "fc1 dgrad launch");
   return GMLP_OK;
 }
 

@@ -151,11 +151,129 @@ __device__ __forceinline__ float silu_times(float gate, float up) {
 
 // ------------------------------------------------------------------ epilogues
 
+
 // One epilogue thread owns one accumulator row (TMEM lane 32q + lane) and a
 // 64-column slice of the 256-column tile.
 constexpr int kSliceCols = 64;
 
-template <int FMT, int EPI>
+// silu'(g) = s (1 + g (1 - s)), s = sigmoid(g)
+__device__ __forceinline__ float dsilu(float g, float sg) { return sg * (1.0f + g * (1.0f - sg)); }
+
+// Backward "dGLU" epilogue (MXFP8): acc holds dfc2x for this thread's row and
+// 64 fc2_x columns n0..n0+63; d = bf16(dfc2x) (the C dtype).  With the
+// forward's activation input h (SwiGLU: gate g at column n, up u at N + n):
+//   SwiGLU: a = silu(g) u; dg = d prob u silu'(g); du = d prob silu(g)
+//   SReLU:  a = max(h,0)^2; dh = d prob 2 max(h,0)
+// fc1_dy = bf16(dg | du | dh) quantised to MXFP8 in 1x32 blocks (codes
+// [M][N1], scales GEMM_TILED for the fc1 dgrad), and dprob[row] += sum d a.
+// Each 32-column block is evaluated twice (block max, then codes) so that only
+// the packed d values stay in registers.
+// The dGLU values of one element: v0 = fc1_dy of the gate (or of h), v1 =
+// fc1_dy of the up column (SwiGLU), act_d = d * a for dprob.
+template <int EPI>
+__device__ __forceinline__ void dglu_values(float d, float g, float u, float prob, float& v0, float& v1,
+                                            float& act_d) {
+  const float da = d * prob;
+  if (EPI == EPI_DGLU_SWIGLU) {
+    const float sg = __fdividef(1.0f, 1.0f + __expf(fminf(-g, 80.0f)));
+    const float silu = g * sg;
+    act_d = d * (silu * u);
+    v0 = round_bf16(da * u * dsilu(g, sg));
+    v1 = round_bf16(da * silu);
+  } else {
+    const float r = fmaxf(g, 0.0f);
+    act_d = d * (r * r);
+    v0 = round_bf16(da * 2.0f * r);
+    v1 = 0.0f;
+  }
+}
+
+__device__ __forceinline__ float bf16_half(uint32_t w, int hi) {
+  return bf16_bits_to_float(hi ? (w >> 16) : (w & 0xFFFFu));
+}
+
+// max(|a|, |b|) of packed bf16 pairs (sign bits are the xor of the inputs').
+__device__ __forceinline__ uint32_t bmax_abs2_g(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// MXFP8 block of 32 bf16 values held as 16 packed pairs: scale exponent from
+// the bf16 block max, 32 E4M3 codes (element 0 in the low byte) to dst.
+__device__ __forceinline__ int mx_block_packed(const uint32_t* w, uint8_t* dst) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = bmax_abs2_g(m, w[i]);
+  m = bmax_abs2_g(m, __byte_perm(m, 0, 0x1032)) & 0x7fffu;
+  const int e = mxfp8_exponent(__uint_as_float(m << 16));
+  const float mul = exp2_neg(e);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t w0 = w[8 * h + 2 * j], w1 = w[8 * h + 2 * j + 1];
+      o[j] = e4m3x2(__fmul_rn(bf16_half(w0, 0), mul), __fmul_rn(bf16_half(w0, 1), mul)) |
+             (e4m3x2(__fmul_rn(bf16_half(w1, 0), mul), __fmul_rn(bf16_half(w1, 1), mul)) << 16);
+    }
+    *reinterpret_cast<uint4*>(dst + 16 * h) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  return e;
+}
+
+template <int EPI>
+__device__ __forceinline__ void dglu_epilogue(const GemmArgs& a, const float* acc, const Tile& t, const int* tb,
+                                              int lr, int64_t grow, bool valid, int q, int lane, int slice,
+                                              float prob) {
+  if (!valid) return;
+  constexpr bool kGlu = EPI == EPI_DGLU_SWIGLU;
+  const int n0 = t.nt * kBN + slice * kSliceCols;
+  const int64_t N1 = a.n_cols_out;
+  const int64_t N = kGlu ? N1 / 2 : N1;
+  const uint16_t* hrow = a.act_in + grow * N1;
+  uint8_t* crow = a.out_codes + grow * N1;
+  const int nscale = (int)(N1 / 32);
+  const int64_t sbase = (int64_t)(tb[t.g] + (lr >> 7)) * (nscale >> 2) * 512 + lane * 16 + q * 4;
+  uint32_t dw[32];  // d = bf16(dfc2x), packed pairs (the accumulator registers die here)
+#pragma unroll
+  for (int i = 0; i < 32; ++i) dw[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+  float dsum = 0.0f;
+  constexpr int kOuts = kGlu ? 2 : 1;  // fc1_dy outputs per fc2_x column (gate and up, or h)
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {  // the slice's two 32-column blocks
+#pragma unroll
+    for (int o = 0; o < kOuts; ++o) {
+      uint32_t ow[16];  // fc1_dy values of output o (bf16), packed pairs
+#pragma unroll
+      for (int c = 0; c < 32; c += 8) {
+        const uint4 g8 = __ldg(reinterpret_cast<const uint4*>(hrow + n0 + 32 * b + c));
+        const uint4 u8 = kGlu ? __ldg(reinterpret_cast<const uint4*>(hrow + N + n0 + 32 * b + c)) : g8;
+        const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w}, uw[4] = {u8.x, u8.y, u8.z, u8.w};
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+          float v[2];
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            float v0, v1, ad;
+            dglu_values<EPI>(bf16_half(dw[(32 * b + c + k) >> 1], kk), bf16_half(gw[k >> 1], kk),
+                             bf16_half(uw[k >> 1], kk), prob, v0, v1, ad);
+            v[kk] = o == 0 ? v0 : v1;
+            if (o == 0) dsum += ad;
+          }
+          ow[(c + k) >> 1] = pack_bf16x2(v[0], v[1]);
+        }
+      }
+      const int64_t col = (o == 0 ? 0 : N) + n0 + 32 * b;
+      const int e = mx_block_packed(ow, crow + col);
+      const int kidx = (int)(col / 32);
+      a.out_scales[sbase + (int64_t)(kidx >> 2) * 512 + (kidx & 3)] = (uint8_t)(e + 127);
+    }
+  }
+  if (a.dprob) atomicAdd(a.dprob + grow, dsum);
+}
+
+template <int FMT, int EPI, bool XT>
 __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Tile& t, const int* off,
                                          const int* tb, int row_base, int q, int lane, int slice, float prob) {
   const int row = 32 * q + lane;
@@ -165,7 +283,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
   const int64_t grow = (int64_t)off[t.g] + lr;
   float alpha = 1.0f;
   if (FMT == GMLP_NVFP4) alpha = __fdiv_rn(1.0f, __fmul_rn(nvfp4_global_scale(a.a_amax[t.g]), a.b_S[t.g]));
-  if (a.bias) {
+  if (XT && a.bias) {
     // per-expert bias, added to the FP32 accumulator before any rounding; the
     // slice's two 32-column runs map to logical rows b0 and b1 of the bias
     // (SwiGLU: its gate and up rows under the 32-row interleave)
@@ -191,6 +309,11 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
     alpha = 1.0f;
   }
 
+  if (EPI == EPI_DGLU_SWIGLU || EPI == EPI_DSRELU) {
+    dglu_epilogue<EPI>(a, acc, t, tb, lr, grow, valid, q, lane, slice, prob);
+    return;
+  }
+
   if (EPI == EPI_FC2) {
     if (!valid) return;
     uint16_t* yrow = a.out_bf16 + grow * a.n_cols_out + (int64_t)t.nt * kBN + slice * kSliceCols;
@@ -205,6 +328,20 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
   }
 
   constexpr int kOut = EPI == EPI_FC1_SWIGLU ? 32 : 64;  // fc2_x values this thread produces
+  const int64_t oc0 = (int64_t)t.nt * (kBN / (EPI == EPI_FC1_SWIGLU ? 2 : 1)) + slice * kOut;
+  if (XT && a.pre_act_out && valid) {
+    // the activation input h = bf16(acc * alpha) in logical column order (the
+    // backward's saved tensor): SwiGLU gate columns oc0.., up columns N + oc0..
+    uint16_t* hrow = a.pre_act_out + grow * a.n_out;
+#pragma unroll
+    for (int j = 0; j < 64; j += 16) {
+      uint32_t o[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) o[k] = pack_bf16x2(acc[j + 2 * k] * alpha, acc[j + 2 * k + 1] * alpha);
+      const int64_t col = EPI == EPI_FC1_SWIGLU ? (j < 32 ? oc0 + j : a.n_cols_out + oc0 + (j - 32)) : oc0 + j;
+      st_global_v8(hrow + col, o);
+    }
+  }
   // fc2_x = bf16(act(bf16(acc * alpha)) * prob), in place in acc[0..kOut)
   if (EPI == EPI_FC1_SWIGLU) {
     // a 64-column slice holds 32 gate then 32 up columns of the same 32 outputs
@@ -229,7 +366,6 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
       acc[i] = round_bf16(h * h * prob);
     }
   }
-  const int64_t oc0 = (int64_t)t.nt * (kBN / (EPI == EPI_FC1_SWIGLU ? 2 : 1)) + slice * kOut;
 
   if (FMT == GMLP_MXFP8) {
     constexpr int kBlocks = kOut / 32;
@@ -395,7 +531,7 @@ __device__ __forceinline__ void tc_mma_g(uint32_t d, uint64_t adesc, uint64_t bd
 
 // ------------------------------------------------------------------ kernel
 
-template <int FMT, int EPI, int PAIR, bool X4>
+template <int FMT, int EPI, int PAIR, bool X4, bool XT>
 __global__ void __launch_bounds__(kThreadsGemm, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -655,7 +791,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           mbar_arrive_cluster(tempty_addr);
       }
       acc_phase ^= 1;
-      epilogue<FMT, EPI>(a, acc, t, off, tb, row_base, q, lane, slice, prob);
+      epilogue<FMT, EPI, XT>(a, acc, t, off, tb, row_base, q, lane, slice, prob);
     }
   }
   __syncthreads();
@@ -696,11 +832,11 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows
   return r == CUDA_SUCCESS;
 }
 
-template <int FMT, int EPI, int PAIR, bool X4 = false>
+template <int FMT, int EPI, int PAIR, bool X4 = false, bool XT = false>
 cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
   using C = Cfg<FMT, PAIR, X4>;
   const size_t smem = C::kSmem + 1024 + 256 + 3 * (kMaxGroups + 1) * sizeof(int);
-  auto kern = gemm_kernel<FMT, EPI, PAIR, X4>;
+  auto kern = gemm_kernel<FMT, EPI, PAIR, X4, XT>;
   static bool attr_set[64] = {};
   static int max_units[64] = {};
   int dev = 0;
@@ -761,29 +897,39 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
 
 int gemm_read_clear_status() { return read_clear_status(); }
 
-// Single-CTA tiles unless the caller asks for CTA pairs.
+// Single-CTA tiles unless the caller asks for CTA pairs.  Biases and the
+// saved activation input (XT) have their own single-CTA instantiations, so the
+// plain kernels keep their registers.
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.M == 0) return cudaSuccess;
   const bool pair = a.pair == 2;
-#define GMLP_LAUNCH(F, E) \
-  return pair ? launch_t<F, E, 2>(a, s) : launch_t<F, E, 1>(a, s)
+  const bool xt = a.bias || a.pre_act_out;
+  if (xt && pair) return cudaErrorInvalidConfiguration;  // rejected by the API before
+#define GMLP_ONE(F, E, X4) \
+  return xt ? launch_t<F, E, 1, X4, true>(a, s) : launch_t<F, E, 1, X4, false>(a, s)
+#define GMLP_LAUNCH(F, E)                                        \
+  if (pair) return launch_t<F, E, 2, false, false>(a, s);        \
+  GMLP_ONE(F, E, false)
   if (a.format == GMLP_MXFP8) {
-    if (a.epi == EPI_FC1_SWIGLU) GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_SWIGLU);
-    if (a.epi == EPI_FC1_SRELU) GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_SRELU);
-    if (a.epi == EPI_FC1_TANH_SRELU) GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_TANH_SRELU);
+    if (a.epi == EPI_FC1_SWIGLU) { GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_SWIGLU); }
+    if (a.epi == EPI_FC1_SRELU) { GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_SRELU); }
+    if (a.epi == EPI_FC1_TANH_SRELU) { GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_TANH_SRELU); }
+    if (a.epi == EPI_DGLU_SWIGLU) return launch_t<GMLP_MXFP8, EPI_DGLU_SWIGLU, 1>(a, s);
+    if (a.epi == EPI_DSRELU) return launch_t<GMLP_MXFP8, EPI_DSRELU, 1>(a, s);
     GMLP_LAUNCH(GMLP_MXFP8, EPI_FC2);
   }
   if (a.b_x4) {  // replicated B scales: single-CTA tiles only
-    if (a.epi == EPI_FC1_SWIGLU) return launch_t<GMLP_NVFP4, EPI_FC1_SWIGLU, 1, true>(a, s);
-    if (a.epi == EPI_FC1_SRELU) return launch_t<GMLP_NVFP4, EPI_FC1_SRELU, 1, true>(a, s);
-    if (a.epi == EPI_FC1_TANH_SRELU) return launch_t<GMLP_NVFP4, EPI_FC1_TANH_SRELU, 1, true>(a, s);
-    return launch_t<GMLP_NVFP4, EPI_FC2, 1, true>(a, s);
+    if (a.epi == EPI_FC1_SWIGLU) { GMLP_ONE(GMLP_NVFP4, EPI_FC1_SWIGLU, true); }
+    if (a.epi == EPI_FC1_SRELU) { GMLP_ONE(GMLP_NVFP4, EPI_FC1_SRELU, true); }
+    if (a.epi == EPI_FC1_TANH_SRELU) { GMLP_ONE(GMLP_NVFP4, EPI_FC1_TANH_SRELU, true); }
+    GMLP_ONE(GMLP_NVFP4, EPI_FC2, true);
   }
-  if (a.epi == EPI_FC1_SWIGLU) GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SWIGLU);
-  if (a.epi == EPI_FC1_SRELU) GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SRELU);
-  if (a.epi == EPI_FC1_TANH_SRELU) GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_TANH_SRELU);
+  if (a.epi == EPI_FC1_SWIGLU) { GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SWIGLU); }
+  if (a.epi == EPI_FC1_SRELU) { GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SRELU); }
+  if (a.epi == EPI_FC1_TANH_SRELU) { GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_TANH_SRELU); }
   GMLP_LAUNCH(GMLP_NVFP4, EPI_FC2);
 #undef GMLP_LAUNCH
+#undef GMLP_ONE
 }
 
 }  // namespace gmlp

@@ -73,6 +73,8 @@ enum Epilogue : int {
   EPI_FC1_SRELU = 1,   // fc1 + squared ReLU x prob
   EPI_FC2 = 2,         // fc2: bf16 output
   EPI_FC1_TANH_SRELU = 3,  // fc1 + tanh soft clamp of the squared ReLU x prob
+  EPI_DGLU_SWIGLU = 4,     // backward: dfc2x -> dSwiGLU x prob (fc1_dy, MXFP8) and dprob
+  EPI_DSRELU = 5,          // backward: dfc2x -> dSReLU x prob (fc1_dy, MXFP8) and dprob
 };
 
 struct GemmArgs {
@@ -95,6 +97,9 @@ struct GemmArgs {
   uint8_t* out_scales;     // GEMM_TILED over the token split
   // NVFP4 fc1 output and fc2 output
   uint16_t* out_bf16;      // [M][n_cols_out]
+  uint16_t* pre_act_out;   // optional fc1: bf16 activation input [M][n_out], logical column order
+  const uint16_t* act_in;  // backward dGLU: the forward's bf16 activation input [M][n_cols_out]
+  float* dprob;            // backward dGLU: [M] d(loss)/d(prob), accumulated with atomicAdd (zeroed before)
   float* amax_pre;         // NVFP4 fc1: [G] (atomicMax, zeroed before)
   float* amax_post;
   uint32_t rht_mask;

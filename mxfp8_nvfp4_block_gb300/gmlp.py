@@ -26,7 +26,7 @@ EXPORTS = ["gmlp_tiled_scales_bytes", "gmlp_group_hadamard_amax", "gmlp_group_qu
            "gmlp_group_quantize", "gmlp_prepare_weights", "gmlp_forward_workspace_size", "gmlp_forward",
            "gmlp_check_device_status", "gmlp_last_error", "gmlp_version", "gmlp_forward_noalloc",
            "gmlp_selftest_bounded_wait", "gmlp_mma_peak", "gmlp_replicate_weight_scales",
-           "gmlp_prepare_weights_discrete"]
+           "gmlp_prepare_weights_discrete", "gmlp_backward_workspace_size", "gmlp_backward_dgrad"]
 
 
 class Recipe(ctypes.Structure):
@@ -50,7 +50,8 @@ class FwdAux(ctypes.Structure):
                 ("fc2x_amax_pre", ctypes.c_void_p), ("fc2x_amax_post", ctypes.c_void_p),
                 ("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("n_stage_events", ctypes.c_int32),
                 ("gemm_mode", ctypes.c_int32), ("fc2x_col_codes", ctypes.c_void_p),
-                ("fc2x_col_scales", ctypes.c_void_p), ("tanh_clamp_scale", ctypes.c_float)]
+                ("fc2x_col_scales", ctypes.c_void_p), ("tanh_clamp_scale", ctypes.c_float),
+                ("fc1_pre_act", ctypes.c_void_p)]
 
 
 _lib = None
@@ -86,6 +87,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gmlp_selftest_bounded_wait": (_i32, [ctypes.c_uint64, _vp]),
         "gmlp_mma_peak": (_i32, [_i32, _i32, ctypes.c_int64, _i32, _vp]),
         "gmlp_replicate_weight_scales": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp]),
+        "gmlp_backward_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
+        "gmlp_backward_dgrad": (_i32, [_vp, _i64, _i64, _i64, _vp, _i32, ctypes.POINTER(QWeightC),
+                                       ctypes.POINTER(QWeightC), _vp, _vp, _i32, ctypes.POINTER(Recipe), _vp, _vp,
+                                       _vp, _vp, _vp, ctypes.c_size_t, _vp]),
         "gmlp_last_error": (ctypes.c_char_p, []),
         "gmlp_version": (ctypes.c_char_p, []),
     }
@@ -290,7 +295,8 @@ def forward(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *
         aux = aux or {}
         aux_c = FwdAux(_p(aux.get("fc2x_codes")), _p(aux.get("fc2x_scales")), _p(aux.get("fc2x_bf16")),
                        _p(aux.get("fc2x_amax_pre")), _p(aux.get("fc2x_amax_post")), None, 0, int(gemm_mode),
-                       _p(aux.get("fc2x_col_codes")), _p(aux.get("fc2x_col_scales")), float(tanh_clamp_scale))
+                       _p(aux.get("fc2x_col_codes")), _p(aux.get("fc2x_col_scales")), float(tanh_clamp_scale),
+                       _p(aux.get("fc1_pre_act")))
         if events:
             ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
             aux_c.stage_events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))
@@ -317,6 +323,36 @@ def forward_noalloc(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: R
                                        _p(probs), act, ctypes.byref(rec), _p(y),
                                        ctypes.byref(aux_c) if aux_c else None, _stream(stream)))
     return y
+
+
+# ------------------------------------------------------------------ backward (data gradients)
+
+def prepare_transposed_weights(W: torch.Tensor, fmt: int = MXFP8, stream=None) -> "QWeight":
+    """Quantise W [G, R, C] transposed ([G, C, R], quantised along R): the
+    operand the backward dgrad GEMMs read (W2t from W2, W1t from W1 in logical
+    gate/up order)."""
+    return prepare_weights(_bits(W).transpose(1, 2).contiguous(), fmt, x4=False, stream=stream)
+
+
+def backward_dgrad(dy, splits, W2t: "QWeight", W1t: "QWeight", pre_act, probs, act: int, rec: Recipe, *,
+                   dx=None, want_dprob: bool = True, fc1_dy: dict | None = None, workspace=None, stream=None):
+    """dx (and dprob) of the fused grouped MLP (see gmlp_backward_dgrad)."""
+    dy = _bits(dy)
+    M, K = dy.shape
+    N = W2t.rows
+    G = splits.numel()
+    if dx is None:
+        dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
+    dprob = torch.empty(M, dtype=torch.float32, device=dy.device) if want_dprob else None
+    need = load().gmlp_backward_workspace_size(M, K, N, G, act)
+    if workspace is None:
+        workspace = _u8(need, dy.device)
+    fc1_dy = fc1_dy or {}
+    _check(load().gmlp_backward_dgrad(_p(dy), M, K, N, _p(splits), G, ctypes.byref(W2t.c()), ctypes.byref(W1t.c()),
+                                      _p(pre_act), _p(probs), act, ctypes.byref(rec), _p(dx), _p(dprob),
+                                      _p(fc1_dy.get("codes")), _p(fc1_dy.get("scales")), _p(workspace),
+                                      workspace.numel(), _stream(stream)))
+    return dx, dprob
 
 
 def selftest_bounded_wait(limit_ns: int, stream=None) -> None:

@@ -19,6 +19,7 @@ Layout:
 Parity pins live in tests/test_oracle_*.py.  Functions without a pin: none.
 """
 from ._lib import build, lib  # noqa: F401
+from .backward import backward_dgrad, dact  # noqa: F401
 from .forward import SRELU, SWIGLU, TANH_SRELU, activation, dequant_weight, forward, quantize_weights  # noqa: F401
 from .layout import (compact_to_tiled, group_offsets, tile_bases, tiled_index, tiled_size,  # noqa: F401
                      tiled_to_compact, tiled_to_x4)

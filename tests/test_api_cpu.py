@@ -215,3 +215,21 @@ def test_prepare_weights_discrete_and_bias_checks(lib):
     assert L.gmlp_forward(FAKE, 512, 256, 256, FAKE, 4, ctypes.byref(w1), ctypes.byref(w2), None, g.SRELU,
                           ctypes.byref(r), FAKE, None, FAKE, need, None) == g.ERR_INVALID_ARG
     assert b"bias" in L.gmlp_last_error()
+
+
+def test_backward_dgrad_checks(lib):
+    L, g = lib
+    r = g.recipe(g.MXFP8)
+    w2t = g.QWeightC(FAKE, FAKE, None, 256, 512, 4, g.MXFP8, 0, 0)   # [N x K]
+    w1t = g.QWeightC(FAKE, FAKE, None, 512, 256, 4, g.MXFP8, 0, 0)   # [K x N1] (SReLU)
+    need = L.gmlp_backward_workspace_size(512, 512, 256, 4, g.SRELU)
+
+    def call(K=512, N=256, act=g.SRELU, rec=r, W2t=w2t, W1t=w1t, pre=FAKE):
+        return L.gmlp_backward_dgrad(FAKE, 512, K, N, FAKE, 4, ctypes.byref(W2t), ctypes.byref(W1t), pre, None, act,
+                                     ctypes.byref(rec), FAKE, None, None, None, FAKE, need, None)
+
+    assert call(rec=g.recipe(g.NVFP4)) == g.ERR_UNSUPPORTED_RECIPE
+    assert call(act=g.TANH_SRELU) == g.ERR_INVALID_ARG
+    assert call(N=128) == g.ERR_INVALID_DIMS
+    assert call(W2t=w1t) == g.ERR_INVALID_DIMS          # shapes swapped
+    assert call(pre=None) == g.ERR_INVALID_ARG

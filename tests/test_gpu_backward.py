@@ -1,0 +1,88 @@
+"""Parity of the data-gradient backward (CUDA path, through the C ABI) with the
+oracle: fc2 dGLU (dSwiGLU / dSReLU x prob, dprob, fc1_dy in MXFP8) and the fc1
+dgrad, on the forward's own saved activation input."""
+import numpy as np
+import pytest
+import torch
+
+from mxfp8_nvfp4_block_gb300.inputs import bits
+from parity import code_match_report, frob, np_bits, np_u8
+
+pytestmark = pytest.mark.gpu
+
+
+def bf16_cpu(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
+
+
+def forward_with_h(gm, x, splits, W1, W2, probs, act):
+    """Forward that also returns the saved activation input h [M, N1]."""
+    M, N = x.shape[0], W2.shape[2]
+    n1 = W1.shape[1]
+    w1 = gm.prepare_weights(W1.cuda(), gm.MXFP8, swiglu_interleave=(act == gm.SWIGLU))
+    w2 = gm.prepare_weights(W2.cuda(), gm.MXFP8)
+    h = torch.full((M, n1), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y = gm.forward(x.cuda(), splits.cuda(), w1, w2, probs, act, gm.recipe(gm.MXFP8), aux={"fc1_pre_act": h})
+    gm.check_device_status()
+    return y, h
+
+
+def run_backward(gm, dy, splits, W1, W2, h, probs, act):
+    M, N1 = h.shape
+    G = splits.numel()
+    w2t = gm.prepare_transposed_weights(W2.cuda())
+    w1t = gm.prepare_transposed_weights(W1.cuda())
+    fc1 = {"codes": torch.zeros(M * N1 + 16, dtype=torch.uint8, device="cuda"),
+           "scales": torch.zeros(gm.tiled_scales_bytes(M, G, N1 // 32) + 16, dtype=torch.uint8, device="cuda")}
+    dx, dprob = gm.backward_dgrad(dy.cuda(), splits.cuda(), w2t, w1t, h, probs, act, gm.recipe(gm.MXFP8), fc1_dy=fc1)
+    gm.check_device_status()
+    return dx, dprob, fc1
+
+
+@pytest.mark.parametrize("act", [0, 1], ids=["swiglu", "srelu"])
+def test_backward_dgrad_parity(orc, gm, act):
+    rng = np.random.default_rng(61 + act)
+    splits_l, K, N = [130, 0, 257, 5, 1, 128], 512, 256
+    G, M = len(splits_l), sum(splits_l)
+    n1 = 2 * N if act == 0 else N
+    splits = torch.tensor(splits_l, dtype=torch.int64)
+    x = bf16_cpu(rng.standard_normal((M, K)))
+    W1 = bf16_cpu(rng.standard_normal((G, n1, K)) / np.sqrt(K))
+    W2 = bf16_cpu(rng.standard_normal((G, K, N)) / np.sqrt(N))
+    probs = torch.from_numpy(rng.uniform(0.1, 1, M).astype(np.float32)).cuda()
+    _, h = forward_with_h(gm, x, splits, W1, W2, probs, act)
+    assert not torch.isnan(h.float()).any()
+    dy = bf16_cpu(rng.standard_normal((M, K)))
+    dx, dprob, fc1 = run_backward(gm, dy, splits, W1, W2, h, probs, act)
+    hb = h.cpu().view(torch.int16).numpy().view(np.uint16)
+    ref = orc.backward_dgrad(bits(dy), np.array(splits_l), bits(W1), bits(W2), hb, probs.cpu().numpy(), act)
+    frac, steps = code_match_report(0, np_u8(fc1["codes"], M * n1).reshape(M, n1), ref["fc1_dy_codes"],
+                                    orc.tiled_to_compact(np_u8(fc1["scales"]), np.array(splits_l), n1 // 32),
+                                    ref["fc1_dy_scales"])
+    print(f"fc1_dy code match {frac:.6f} (max {steps:.2f} steps)")
+    assert frac >= 0.999 and steps <= 1.0 + 1e-9, (frac, steps)
+    err = frob(dx.float().cpu().numpy(), orc.bf16_to_f64(ref["dx"]))
+    perr = frob(dprob.cpu().numpy(), ref["dprob"])
+    print(f"dx error {err:.3e}, dprob error {perr:.3e}")
+    assert err <= 1e-2 and perr <= 1e-2
+
+
+def test_backward_dgrad_lossless_bitexact(orc, gm):
+    """SReLU, small-integer operands, one-hot weights: dx and fc1_dy exact."""
+    rng = np.random.default_rng(71)
+    splits_l, K, N = [130, 0, 257, 5, 128], 512, 256
+    G, M = len(splits_l), sum(splits_l)
+    splits = torch.tensor(splits_l, dtype=torch.int64)
+    W2 = np.zeros((G, K, N))
+    W1 = np.zeros((G, N, K))
+    for g in range(G):
+        W2[g, rng.integers(0, K, N), np.arange(N)] = 1.0
+        W1[g, np.arange(N), rng.integers(0, K, N)] = 1.0
+    h = bf16_cpu(rng.choice([0.0, 1.0, -1.0, 2.0], size=(M, N))).cuda()
+    dy = bf16_cpu(rng.choice([0.0, 1.0, -1.0], size=(M, K)))
+    dx, dprob, fc1 = run_backward(gm, dy, splits, bf16_cpu(W1), bf16_cpu(W2), h, None, 1)
+    hb = h.cpu().view(torch.int16).numpy().view(np.uint16)
+    ref = orc.backward_dgrad(bits(dy), np.array(splits_l), bits(bf16_cpu(W1)), bits(bf16_cpu(W2)), hb, None, 1)
+    assert np.array_equal(np_u8(fc1["codes"], M * N).reshape(M, N), ref["fc1_dy_codes"])
+    assert np.array_equal(np_bits(dx), ref["dx"])
+    assert np.array_equal(dprob.cpu().numpy().astype(np.float64), ref["dprob"])

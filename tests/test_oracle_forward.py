@@ -190,3 +190,53 @@ def test_biases_enter_before_rounding_exactly(orc, fmt_name):
         f = np.maximum(x[sl][:, perms[g]] + b1[g], 0) ** 2
         assert np.array_equal(out["fc2x"][sl], bf16_of(f)), g
         assert np.array_equal(out["y"][sl], bf16_of(f @ W2[g].T + b2[g])), g
+
+
+@pytest.mark.parametrize("act", [0, 1], ids=["swiglu", "srelu"])
+def test_dact_matches_finite_differences(orc, act):
+    """The backward's activation derivatives against central differences of the
+    forward activation (an independent evaluation of the same function)."""
+    rng = np.random.default_rng(5)
+    n = 64
+    h = rng.standard_normal((4, 2 * n if act == 0 else n)) * 3
+    if act == 1:
+        h[np.abs(h) < 1e-3] = 0.5          # keep away from the kink at 0
+    d0, d1 = orc.dact(h, act)
+    eps = 1e-6
+    if act == 0:
+        for part, d in ((slice(0, n), d0), (slice(n, 2 * n), d1)):
+            hp, hm = h.copy(), h.copy()
+            hp[:, part] += eps
+            hm[:, part] -= eps
+            fd = (orc.activation(hp, act) - orc.activation(hm, act)) / (2 * eps)
+            np.testing.assert_allclose(d, fd, rtol=1e-6, atol=1e-8)
+    else:
+        fd = (orc.activation(h + eps, act) - orc.activation(h - eps, act)) / (2 * eps)
+        np.testing.assert_allclose(d0, fd, rtol=1e-6, atol=1e-8)
+
+
+def test_backward_dgrad_lossless_equals_plain_backprop(orc):
+    """SReLU with small-integer operands and one-hot weights: every step of the
+    data-gradient backward is exact, so it equals plain float64 backprop:
+    dfc2x = dy W2, dh = dfc2x * 2 relu(h), dx = dh W1, dprob = sum dfc2x relu(h)^2."""
+    rng = np.random.default_rng(9)
+    G, K, N = 3, 64, 64
+    splits = np.array([5, 0, 9])
+    M = splits.sum()
+    offs = np.concatenate([[0], np.cumsum(splits)])
+    dy = rng.choice([0.0, 1.0, -1.0], size=(M, K))
+    W2 = np.zeros((G, K, N))
+    W1 = np.zeros((G, N, K))
+    for g in range(G):
+        W2[g, rng.integers(0, K, N), np.arange(N)] = 1.0     # each fc2_x column reads one output row
+        W1[g, np.arange(N), rng.integers(0, K, N)] = 1.0
+    h = rng.choice([0.0, 1.0, -1.0, 2.0], size=(M, N))
+    out = orc.backward_dgrad(as_bits(dy), splits, as_bits(W1), as_bits(W2), as_bits(h), None, orc.SRELU)
+    for g in range(G):
+        sl = slice(offs[g], offs[g + 1])
+        d = dy[sl] @ W2[g]
+        dh = d * 2 * np.maximum(h[sl], 0)
+        assert np.array_equal(out["dfc2x"][sl], bf16_of(d))
+        assert np.array_equal(out["fc1_dy"][sl], bf16_of(dh))
+        assert np.array_equal(out["dx"][sl], bf16_of(dh @ W1[g])), g
+        np.testing.assert_array_equal(out["dprob"][sl], (d * np.maximum(h[sl], 0) ** 2).sum(axis=1))
