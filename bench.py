@@ -171,7 +171,8 @@ def run_gpu(args, rank: int, world: int) -> dict:
     probs = d["probs"].to(dev)
     W1 = gmlp.prepare_weights(d["W1"].to(dev), fmt, swiglu_interleave=(act == gmlp.SWIGLU))
     W2 = gmlp.prepare_weights(d["W2"].to(dev), fmt)
-    del d["W1"], d["W2"]
+    if not args.backward:
+        del d["W1"], d["W2"]
     y = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(gmlp.forward_workspace_size(w.M, w.K, w.N, w.G, act, rec), dtype=torch.uint8, device=dev)
     colwise = None
@@ -312,6 +313,9 @@ def run_gpu(args, rank: int, world: int) -> dict:
         out["fc2x_cast"] = {"ms": round(stage_ms[3], 5), "bytes": f_bytes, "columnwise": bool(colwise),
                             "GB_s": round(f_bytes / (stage_ms[3] * 1e-3) / 1e9, 1),
                             "frac_hbm": round(f_bytes / (stage_ms[3] * 1e-3) / 1e9 / hbm, 4)}
+    if args.backward and fmt == gmlp.MXFP8 and w.act != gmlp.TANH_SRELU:
+        out["backward_dgrad"] = bench_backward(gmlp, d, w, d["W1"].to(dev), d["W2"].to(dev), x, splits, probs,
+                                               K_steps, W_steps, dev)
     ceiling = mma_ceiling(gmlp, fmt)
     out["roofline"]["mma_loop_tflops"] = ceiling
     # the loop with the copy mix the forward's GEMM issues (NVFP4 weights carry X4 scales)
@@ -344,6 +348,42 @@ def mma_ceiling(gmlp, fmt: int, iters: int = 32768, reps: int = 5) -> dict:
         tf = gmlp.mma_peak_flops(fmt, iters, n_sm) / (ms * 1e-3) / 1e12
         out[names[copy]] = round(tf, 1)
     return out
+
+
+def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps: int, dev) -> dict:
+    """Data-gradient backward (MXFP8): dy quantise -> fc2 dGLU GEMM (dSwiGLU /
+    dSReLU x prob, dprob, MXFP8 fc1_dy) -> fc1 dgrad GEMM, on the forward's own
+    saved activation input; L2 flushed between steps, per-step events."""
+    rec = gmlp.recipe(w.fmt)
+    w1 = gmlp.prepare_weights(W1b, w.fmt, swiglu_interleave=(w.act == gmlp.SWIGLU))
+    w2 = gmlp.prepare_weights(W2b, w.fmt)
+    h = torch.empty((w.M, w.n1), dtype=torch.bfloat16, device=dev)
+    gmlp.forward(x, splits, w1, w2, probs, w.act, rec, aux={"fc1_pre_act": h})
+    w2t = gmlp.prepare_transposed_weights(W2b)
+    w1t = gmlp.prepare_transposed_weights(W1b)
+    gen = torch.Generator().manual_seed(w.seed + 77)
+    dy = torch.randn((w.M, w.K), generator=gen, dtype=torch.float32).to(torch.bfloat16).to(dev)
+    dx = torch.empty_like(dy)
+    ws = torch.empty(gmlp.load().gmlp_backward_workspace_size(w.M, w.K, w.N, w.G, w.act), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(W_steps):
+        flush.zero_()
+        gmlp.backward_dgrad(dy, splits, w2t, w1t, h, probs, w.act, rec, dx=dx, workspace=ws)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record()
+        gmlp.backward_dgrad(dy, splits, w2t, w1t, h, probs, w.act, rec, dx=dx, workspace=ws)
+        e1.record()
+    torch.cuda.synchronize()
+    gmlp.check_device_status()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    flops = 2.0 * w.M * w.K * w.N + 2.0 * w.M * w.n1 * w.K
+    return {"what": "dx and dprob: dy MXFP8 cast, fc2 dGLU GEMM (fused dact x prob, dprob, MXFP8 fc1_dy), "
+                    "fc1 dgrad GEMM; weight gradients not included",
+            "ms_per_step": round(ms, 5), "flops_per_step": flops, "TFLOP_s": round(flops / (ms * 1e-3) / 1e12, 2)}
 
 
 def bench_quantizer(gmlp, dev, hbm) -> dict:
@@ -471,6 +511,8 @@ def main():
     ap.add_argument("--workload", default="mx_swiglu", choices=[k for k in WORKLOADS if k != "nv_quant"])
     ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 2],
                     help="0: one CTA per 128x256 tile; 2: CTA pairs on 256x256 tiles")
+    ap.add_argument("--backward", action="store_true",
+                    help="MXFP8: also time the data-gradient backward (dy -> dx, dprob)")
     ap.add_argument("--fc2x-colwise", action="store_true",
                     help="NVFP4: also write the columnwise (RHT) NVFP4 fc2_x each step (no-recompute training path)")
     ap.add_argument("--l2-flush", default="write", choices=["write", "clean"],
