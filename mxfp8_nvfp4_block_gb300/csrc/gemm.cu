@@ -222,55 +222,51 @@ __device__ __forceinline__ int mx_block_packed(const uint32_t* w, uint8_t* dst) 
   return e;
 }
 
+// One 32-column block b of the dGLU epilogue: acc32 = dfc2x of columns
+// n0 + 32 b .. + 31 of this thread's row; returns sum d * act over them.
 template <int EPI>
-__device__ __forceinline__ void dglu_epilogue(const GemmArgs& a, const float* acc, const Tile& t, const int* tb,
-                                              int lr, int64_t grow, bool valid, int q, int lane, int slice,
-                                              float prob) {
-  if (!valid) return;
+__device__ __forceinline__ float dglu_block(const GemmArgs& a, const float* acc32, const Tile& t, const int* tb,
+                                            int lr, int64_t grow, int q, int lane, int slice, float prob, int b) {
   constexpr bool kGlu = EPI == EPI_DGLU_SWIGLU;
-  const int n0 = t.nt * kBN + slice * kSliceCols;
+  const int n0 = t.nt * kBN + slice * kSliceCols + 32 * b;
   const int64_t N1 = a.n_cols_out;
   const int64_t N = kGlu ? N1 / 2 : N1;
   const uint16_t* hrow = a.act_in + grow * N1;
   uint8_t* crow = a.out_codes + grow * N1;
   const int nscale = (int)(N1 / 32);
   const int64_t sbase = (int64_t)(tb[t.g] + (lr >> 7)) * (nscale >> 2) * 512 + lane * 16 + q * 4;
-  uint32_t dw[32];  // d = bf16(dfc2x), packed pairs (the accumulator registers die here)
-#pragma unroll
-  for (int i = 0; i < 32; ++i) dw[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
   float dsum = 0.0f;
-  constexpr int kOuts = kGlu ? 2 : 1;  // fc1_dy outputs per fc2_x column (gate and up, or h)
+  // fc1_dy values (bf16, packed pairs) of the gate half (or h) and of the up half;
+  // one pass over the accumulator so each of its values dies once it is used
+  uint32_t ow0[16], ow1[kGlu ? 16 : 1];
 #pragma unroll
-  for (int b = 0; b < 2; ++b) {  // the slice's two 32-column blocks
+  for (int c = 0; c < 32; c += 8) {
+    const uint4 g8 = __ldg(reinterpret_cast<const uint4*>(hrow + n0 + c));
+    const uint4 u8 = kGlu ? __ldg(reinterpret_cast<const uint4*>(hrow + N + n0 + c)) : g8;
+    const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w}, uw[4] = {u8.x, u8.y, u8.z, u8.w};
 #pragma unroll
-    for (int o = 0; o < kOuts; ++o) {
-      uint32_t ow[16];  // fc1_dy values of output o (bf16), packed pairs
+    for (int k = 0; k < 8; k += 2) {
+      float v0[2], v1[2];
 #pragma unroll
-      for (int c = 0; c < 32; c += 8) {
-        const uint4 g8 = __ldg(reinterpret_cast<const uint4*>(hrow + n0 + 32 * b + c));
-        const uint4 u8 = kGlu ? __ldg(reinterpret_cast<const uint4*>(hrow + N + n0 + 32 * b + c)) : g8;
-        const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w}, uw[4] = {u8.x, u8.y, u8.z, u8.w};
-#pragma unroll
-        for (int k = 0; k < 8; k += 2) {
-          float v[2];
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            float v0, v1, ad;
-            dglu_values<EPI>(bf16_half(dw[(32 * b + c + k) >> 1], kk), bf16_half(gw[k >> 1], kk),
-                             bf16_half(uw[k >> 1], kk), prob, v0, v1, ad);
-            v[kk] = o == 0 ? v0 : v1;
-            if (o == 0) dsum += ad;
-          }
-          ow[(c + k) >> 1] = pack_bf16x2(v[0], v[1]);
-        }
+      for (int kk = 0; kk < 2; ++kk) {
+        float ad;
+        dglu_values<EPI>(round_bf16(acc32[c + k + kk]), bf16_half(gw[k >> 1], kk), bf16_half(uw[k >> 1], kk), prob,
+                         v0[kk], v1[kk], ad);
+        dsum += ad;
       }
-      const int64_t col = (o == 0 ? 0 : N) + n0 + 32 * b;
-      const int e = mx_block_packed(ow, crow + col);
-      const int kidx = (int)(col / 32);
-      a.out_scales[sbase + (int64_t)(kidx >> 2) * 512 + (kidx & 3)] = (uint8_t)(e + 127);
+      ow0[(c + k) >> 1] = pack_bf16x2(v0[0], v0[1]);
+      if (kGlu) ow1[((c + k) >> 1) & (kGlu ? 15 : 0)] = pack_bf16x2(v1[0], v1[1]);
     }
   }
-  if (a.dprob) atomicAdd(a.dprob + grow, dsum);
+  constexpr int kOuts = kGlu ? 2 : 1;  // fc1_dy outputs per fc2_x column (gate and up, or h)
+#pragma unroll
+  for (int o = 0; o < kOuts; ++o) {
+    const int64_t col = (o == 0 ? 0 : N) + n0;
+    const int e = mx_block_packed(o == 0 ? ow0 : ow1, crow + col);
+    const int kidx = (int)(col / 32);
+    a.out_scales[sbase + (int64_t)(kidx >> 2) * 512 + (kidx & 3)] = (uint8_t)(e + 127);
+  }
+  return dsum;
 }
 
 template <int FMT, int EPI, bool XT>
@@ -307,11 +303,6 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
                                bf16_bits_to_float((k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu)));
     }
     alpha = 1.0f;
-  }
-
-  if (EPI == EPI_DGLU_SWIGLU || EPI == EPI_DSRELU) {
-    dglu_epilogue<EPI>(a, acc, t, tb, lr, grow, valid, q, lane, slice, prob);
-    return;
   }
 
   if (EPI == EPI_FC2) {
@@ -777,8 +768,30 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       }
       if (!mbar_wait(tfull, acc_phase, abort_flag)) break;
       tc_fence_after();
-      float acc[kSliceCols];
       const uint32_t taddr = tbase + (uint32_t(32 * q) << 16) + uint32_t(slice * kSliceCols);
+      if (EPI == EPI_DGLU_SWIGLU || EPI == EPI_DSRELU) {
+        // backward dGLU: one 32-column half of the accumulator at a time (the
+        // accumulator is released after the second load)
+        const int lr = row_base + 32 * q + lane;
+        const bool valid = lr < off[t.g + 1] - off[t.g];
+        const int64_t grow = (int64_t)off[t.g] + lr;
+        float acc32[32];
+        tmem_ld32(taddr, acc32);
+        tmem_wait_ld();
+        float dsum = valid ? dglu_block<EPI>(a, acc32, t, tb, lr, grow, q, lane, slice, prob, 0) : 0.0f;
+        tmem_ld32(taddr + 32, acc32);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty);
+        acc_phase ^= 1;
+        if (valid) {
+          dsum += dglu_block<EPI>(a, acc32, t, tb, lr, grow, q, lane, slice, prob, 1);
+          if (a.dprob) atomicAdd(a.dprob + grow, dsum);
+        }
+        continue;
+      }
+      float acc[kSliceCols];
       tmem_ld32(taddr, acc);
       tmem_ld32(taddr + 32, acc + 32);
       tmem_wait_ld();
