@@ -380,10 +380,24 @@ def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps
     torch.cuda.synchronize()
     gmlp.check_device_status()
     ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    # second pass: an event after every kernel (dy quantise, dGLU GEMM, dgrad GEMM)
+    st = [0.0, 0.0, 0.0]
+    for _ in range(K_steps):
+        flush.zero_()
+        se = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        se[0].record()
+        gmlp.backward_dgrad(dy, splits, w2t, w1t, h, probs, w.act, rec, dx=dx, workspace=ws, events=se[1:])
+        torch.cuda.synchronize()
+        for i in range(3):
+            st[i] += se[i].elapsed_time(se[i + 1]) / K_steps
+    gmlp.check_device_status()
     flops = 2.0 * w.M * w.K * w.N + 2.0 * w.M * w.n1 * w.K
     return {"what": "dx and dprob: dy MXFP8 cast, fc2 dGLU GEMM (fused dact x prob, dprob, MXFP8 fc1_dy), "
                     "fc1 dgrad GEMM; weight gradients not included",
-            "ms_per_step": round(ms, 5), "flops_per_step": flops, "TFLOP_s": round(flops / (ms * 1e-3) / 1e12, 2)}
+            "ms_per_step": round(ms, 5), "flops_per_step": flops, "TFLOP_s": round(flops / (ms * 1e-3) / 1e12, 2),
+            "stages_ms": [round(t, 5) for t in st],
+            "stage_tflops": {"dglu": round(2.0 * w.M * w.K * w.N / (st[1] * 1e-3) / 1e12, 1),
+                             "dgrad": round(2.0 * w.M * w.n1 * w.K / (st[2] * 1e-3) / 1e12, 1)}}
 
 
 def bench_quantizer(gmlp, dev, hbm) -> dict:

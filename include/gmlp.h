@@ -21,7 +21,9 @@
  * Conventions (all calls):
  *   - Every pointer argument named as device memory is a device pointer owned
  *     by the caller; the library never allocates, frees or keeps it.  Device
- *     pointers must be 16-byte aligned.
+ *     pointers must be 16-byte aligned; the bf16 outputs y and dx and the
+ *     activation input h (fc1_pre_act, pre_act), which move in 32-byte
+ *     vectors, 32-byte aligned.
  *   - Calls are asynchronous on `stream` and never synchronise the host,
  *     except gmlp_check_device_status.  Host structs are read during the call
  *     only.
@@ -262,7 +264,7 @@ typedef struct gmlp_fwd_aux {
   /* out, optional: the activation input h = bf16(fc1 accumulator) [M][N1] in
    * logical column order (SwiGLU: gate columns [0,N), up [N,2N)), the tensor
    * the backward's dGLU step reads (PR #2769 sequence diagram: c_tensor,
-   * swiglu_in).  16-byte aligned. */
+   * swiglu_in).  32-byte aligned. */
   uint16_t* fc1_pre_act;
 } gmlp_fwd_aux;
 
@@ -342,13 +344,16 @@ GMLP_API size_t gmlp_backward_workspace_size(int64_t M, int64_t K, int64_t N, in
  *      gate/up order, [K][N1] per expert, quantised along N1).
  * W2t / W1t come from gmlp_prepare_weights on the transposed bf16 weights
  * (no interleave).  probs NULL = 1; dprob NULL skips it.  act: SWIGLU or SRELU.
+ * stage_events (n_stage_events of them, at most 3, NULL when 0) are recorded
+ * on `stream` after the dy quantise, the dGLU GEMM and the dgrad GEMM.
  * Limits: K % 256 == 0, N % 256 == 0. */
 GMLP_API gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_t N,
                                          const int64_t* split_sizes, int32_t G, const gmlp_qweight* W2t,
                                          const gmlp_qweight* W1t, const uint16_t* pre_act, const float* probs,
                                          int32_t act, const gmlp_recipe* recipe, uint16_t* dx, float* dprob,
                                          uint8_t* fc1_dy_codes, uint8_t* fc1_dy_scales, void* workspace,
-                                         size_t workspace_bytes, gmlp_stream stream);
+                                         size_t workspace_bytes, gmlp_event* stage_events,
+                                         int32_t n_stage_events, gmlp_stream stream);
 
 /* Self-test of the device failure path (no counterpart on the pages): one
  * warp waits, through the same bounded mbarrier wait the kernels use, on a

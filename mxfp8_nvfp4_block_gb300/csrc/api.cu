@@ -33,6 +33,8 @@ gmlp_status cuda_fail(cudaError_t e, const char* where) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+// y, dx and the activation input are written or read in 32-byte vectors
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 0; }
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
@@ -409,8 +411,8 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   if (!aligned16(W1->bias) || !aligned16(W2->bias)) return fail(GMLP_ERR_INVALID_ARG, "weight bias not 16-byte aligned");
   if (fmt == GMLP_NVFP4 && (!W1->global_scale || !W2->global_scale))
     return fail(GMLP_ERR_INVALID_ARG, "NVFP4 weights need global_scale");
-  if ((M > 0 && (!x || !y)) || !aligned16(x) || !aligned16(y))
-    return fail(GMLP_ERR_INVALID_ARG, "x / y NULL or not 16-byte aligned");
+  if ((M > 0 && (!x || !y)) || !aligned16(x) || !aligned32(y))
+    return fail(GMLP_ERR_INVALID_ARG, "x / y NULL, or x not 16-byte or y not 32-byte aligned");
   if (probs && (reinterpret_cast<uintptr_t>(probs) & 3)) return fail(GMLP_ERR_INVALID_ARG, "probs misaligned");
   const FwdLayout L = fwd_layout(M, K, N, G, fmt);
   if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
@@ -422,7 +424,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
         !aligned16(aux->fc2x_col_scales))
       return fail(GMLP_ERR_INVALID_ARG, "fc2x_col_codes / fc2x_col_scales: both, 16-byte aligned");
   }
-  if (aux && !aligned16(aux->fc1_pre_act)) return fail(GMLP_ERR_INVALID_ARG, "fc1_pre_act not 16-byte aligned");
+  if (aux && !aligned32(aux->fc1_pre_act)) return fail(GMLP_ERR_INVALID_ARG, "fc1_pre_act not 32-byte aligned");
   if (aux && aux->gemm_mode == 2 && (aux->fc1_pre_act || W1->bias || W2->bias))
     return fail(GMLP_ERR_INVALID_ARG, "gemm_mode 2 (CTA pairs) takes no biases and saves no activation input");
   if (aux && aux->gemm_mode != 0 && aux->gemm_mode != 2)
@@ -634,7 +636,8 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
                                 int32_t G, const gmlp_qweight* W2t, const gmlp_qweight* W1t,
                                 const uint16_t* pre_act, const float* probs, int32_t act, const gmlp_recipe* recipe,
                                 uint16_t* dx, float* dprob, uint8_t* fc1_dy_codes, uint8_t* fc1_dy_scales,
-                                void* workspace, size_t workspace_bytes, gmlp_stream stream) {
+                                void* workspace, size_t workspace_bytes, gmlp_event* stage_events,
+                                int32_t n_stage_events, gmlp_stream stream) {
   g_last_error[0] = 0;
   GMLP_TRY(check_groups(G, M, split_sizes));
   GMLP_TRY(check_recipe(recipe));
@@ -655,12 +658,14 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
   if (!W2t->codes || !W2t->scales || !W1t->codes || !W1t->scales || !aligned16(W2t->codes) ||
       !aligned16(W2t->scales) || !aligned16(W1t->codes) || !aligned16(W1t->scales))
     return fail(GMLP_ERR_INVALID_ARG, "weight codes/scales NULL or not 16-byte aligned");
-  if ((M > 0 && (!dy || !dx || !pre_act)) || !aligned16(dy) || !aligned16(dx) || !aligned16(pre_act))
-    return fail(GMLP_ERR_INVALID_ARG, "dy / dx / pre_act NULL or not 16-byte aligned");
+  if ((M > 0 && (!dy || !dx || !pre_act)) || !aligned16(dy) || !aligned32(dx) || !aligned32(pre_act))
+    return fail(GMLP_ERR_INVALID_ARG, "dy / dx / pre_act NULL, or dy not 16-byte or dx / pre_act not 32-byte aligned");
   if ((fc1_dy_codes == nullptr) != (fc1_dy_scales == nullptr) || !aligned16(fc1_dy_codes) ||
       !aligned16(fc1_dy_scales))
     return fail(GMLP_ERR_INVALID_ARG, "fc1_dy_codes / fc1_dy_scales: both or neither, 16-byte aligned");
   if (probs && (reinterpret_cast<uintptr_t>(probs) & 3)) return fail(GMLP_ERR_INVALID_ARG, "probs misaligned");
+  if (n_stage_events < 0 || n_stage_events > 3 || (n_stage_events > 0 && !stage_events))
+    return fail(GMLP_ERR_INVALID_ARG, "n_stage_events = %d: 0..3, stage_events non-NULL", n_stage_events);
   const BwdLayout L = bwd_layout(M, K, N1, G);
   if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
     return fail(GMLP_ERR_WORKSPACE, "workspace %zu bytes, need %zu (16-byte aligned)", workspace_bytes, L.total);
@@ -673,6 +678,10 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
   uint8_t* g_codes = fc1_dy_codes ? fc1_dy_codes : ws + L.g_codes;
   uint8_t* g_scales = fc1_dy_scales ? fc1_dy_scales : ws + L.g_scales;
   GroupSrc gs{split_sizes, 0, G, M};
+  auto stage_done = [&](int i) -> gmlp_status {
+    if (i < n_stage_events) GMLP_CUDA(cudaEventRecord((cudaEvent_t)stage_events[i], s), "stage event record");
+    return GMLP_OK;
+  };
   if (dprob) GMLP_CUDA(cudaMemsetAsync(dprob, 0, sizeof(float) * M, s), "dprob memset");
   {
     RowQuantArgs q{};
@@ -686,6 +695,7 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
     q.scales = dy_scales;
     GMLP_CUDA(launch_row_quant(q, s), "dy quantise launch");
   }
+  GMLP_TRY(stage_done(0));
   GemmArgs g1{};  // FC2 dGLU: dfc2x = dy W2 per expert, then dGLU x prob -> fc1_dy (MXFP8), dprob
   g1.format = GMLP_MXFP8;
   g1.epi = act == GMLP_ACT_SWIGLU ? EPI_DGLU_SWIGLU : EPI_DSRELU;
@@ -706,6 +716,7 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
   g1.pair = 1;
   g1.pdl = 1;
   GMLP_CUDA(launch_gemm(g1, s), "dGLU launch");
+  GMLP_TRY(stage_done(1));
   GemmArgs g2{};  // FC1 dgrad: dx = fc1_dy W1 per expert
   g2.format = GMLP_MXFP8;
   g2.epi = EPI_FC2;
@@ -722,6 +733,7 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
   g2.pair = 1;
   g2.pdl = 1;
   GMLP_CUDA(launch_gemm(g2, s), "fc1 dgrad launch");
+  GMLP_TRY(stage_done(2));
   return GMLP_OK;
 }
 

@@ -166,8 +166,9 @@ __device__ __forceinline__ float dsilu(float g, float sg) { return sg * (1.0f + 
 //   SReLU:  a = max(h,0)^2; dh = d prob 2 max(h,0)
 // fc1_dy = bf16(dg | du | dh) quantised to MXFP8 in 1x32 blocks (codes
 // [M][N1], scales GEMM_TILED for the fc1 dgrad), and dprob[row] += sum d a.
-// Each 32-column block is evaluated twice (block max, then codes) so that only
-// the packed d values stay in registers.
+// The accumulator is read one 32-column half at a time; each half yields the
+// gate and up fc1_dy blocks (bf16 pairs in registers) in one pass, then both
+// are quantised.
 // The dGLU values of one element: v0 = fc1_dy of the gate (or of h), v1 =
 // fc1_dy of the up column (SwiGLU), act_d = d * a for dprob.
 template <int EPI>
@@ -187,6 +188,16 @@ __device__ __forceinline__ void dglu_values(float d, float g, float u, float pro
     v1 = 0.0f;
   }
 }
+
+// 32 bytes from global memory through the read-only path without allocating
+// in L1 (p 32-byte aligned).
+__device__ __forceinline__ void ld_global_nc_v8(const void* p, uint32_t* w) {
+  asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 __device__ __forceinline__ float bf16_half(uint32_t w, int hi) {
   return bf16_bits_to_float(hi ? (w >> 16) : (w & 0xFFFFu));
@@ -240,18 +251,20 @@ __device__ __forceinline__ float dglu_block(const GemmArgs& a, const float* acc3
   // one pass over the accumulator so each of its values dies once it is used
   uint32_t ow0[16], ow1[kGlu ? 16 : 1];
 #pragma unroll
-  for (int c = 0; c < 32; c += 8) {
-    const uint4 g8 = __ldg(reinterpret_cast<const uint4*>(hrow + n0 + c));
-    const uint4 u8 = kGlu ? __ldg(reinterpret_cast<const uint4*>(hrow + N + n0 + c)) : g8;
-    const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w}, uw[4] = {u8.x, u8.y, u8.z, u8.w};
+  for (int c = 0; c < 32; c += 16) {
+    // one whole 32-byte sector per load (each is read once: no L1 allocation)
+    uint32_t gw[8], uw[8];
+    ld_global_nc_v8(hrow + n0 + c, gw);
+    if (kGlu) ld_global_nc_v8(hrow + N + n0 + c, uw);
 #pragma unroll
-    for (int k = 0; k < 8; k += 2) {
+    for (int k = 0; k < 16; k += 2) {
       float v0[2], v1[2];
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         float ad;
-        dglu_values<EPI>(round_bf16(acc32[c + k + kk]), bf16_half(gw[k >> 1], kk), bf16_half(uw[k >> 1], kk), prob,
-                         v0[kk], v1[kk], ad);
+        const float g = bf16_half(gw[k >> 1], kk);
+        dglu_values<EPI>(round_bf16(acc32[c + k + kk]), g, kGlu ? bf16_half(uw[k >> 1], kk) : g, prob, v0[kk], v1[kk],
+                         ad);
         dsum += ad;
       }
       ow0[(c + k) >> 1] = pack_bf16x2(v0[0], v0[1]);
@@ -765,6 +778,17 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       if (EPI != EPI_FC2 && a.probs) {
         const int lr = row_base + 32 * q + lane;
         if (lr < off[t.g + 1] - off[t.g]) prob = __ldg(a.probs + off[t.g] + lr);
+      }
+      if (EPI == EPI_DGLU_SWIGLU || EPI == EPI_DSRELU) {
+        // start this row's activation-input lines (gate and up) on their way to
+        // L2 while the tile's MMAs run
+        const int lr = row_base + 32 * q + lane;
+        if (lr < off[t.g + 1] - off[t.g]) {
+          const int64_t N1 = a.n_cols_out;
+          const uint16_t* hp = a.act_in + ((int64_t)off[t.g] + lr) * N1 + t.nt * kBN + slice * kSliceCols;
+          prefetch_l2(hp);
+          if (EPI == EPI_DGLU_SWIGLU) prefetch_l2(hp + N1 / 2);
+        }
       }
       if (!mbar_wait(tfull, acc_phase, abort_flag)) break;
       tc_fence_after();

@@ -90,7 +90,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gmlp_backward_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
         "gmlp_backward_dgrad": (_i32, [_vp, _i64, _i64, _i64, _vp, _i32, ctypes.POINTER(QWeightC),
                                        ctypes.POINTER(QWeightC), _vp, _vp, _i32, ctypes.POINTER(Recipe), _vp, _vp,
-                                       _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+                                       _vp, _vp, _vp, ctypes.c_size_t, _vp, _i32, _vp]),
         "gmlp_last_error": (ctypes.c_char_p, []),
         "gmlp_version": (ctypes.c_char_p, []),
     }
@@ -298,7 +298,7 @@ def forward(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *
                        _p(aux.get("fc2x_col_codes")), _p(aux.get("fc2x_col_scales")), float(tanh_clamp_scale),
                        _p(aux.get("fc1_pre_act")))
         if events:
-            ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+            ev_arr = _event_handles(events)
             aux_c.stage_events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))
             aux_c.n_stage_events = len(events)
     w1c, w2c = W1.c(), W2.c()
@@ -334,9 +334,21 @@ def prepare_transposed_weights(W: torch.Tensor, fmt: int = MXFP8, stream=None) -
     return prepare_weights(_bits(W).transpose(1, 2).contiguous(), fmt, x4=False, stream=stream)
 
 
+def _event_handles(events):
+    """cudaEvent_t handles of torch.cuda.Events; torch creates an event's
+    handle at its first record, so an event not yet recorded is recorded once
+    here (the library records it again)."""
+    for e in events:
+        if not e.cuda_event:
+            e.record()
+    return (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+
+
 def backward_dgrad(dy, splits, W2t: "QWeight", W1t: "QWeight", pre_act, probs, act: int, rec: Recipe, *,
-                   dx=None, want_dprob: bool = True, fc1_dy: dict | None = None, workspace=None, stream=None):
-    """dx (and dprob) of the fused grouped MLP (see gmlp_backward_dgrad)."""
+                   dx=None, want_dprob: bool = True, fc1_dy: dict | None = None, workspace=None, events=None,
+                   stream=None):
+    """dx (and dprob) of the fused grouped MLP (see gmlp_backward_dgrad).
+    events: up to 3 torch.cuda.Event recorded after each kernel."""
     dy = _bits(dy)
     M, K = dy.shape
     N = W2t.rows
@@ -348,10 +360,11 @@ def backward_dgrad(dy, splits, W2t: "QWeight", W1t: "QWeight", pre_act, probs, a
     if workspace is None:
         workspace = _u8(need, dy.device)
     fc1_dy = fc1_dy or {}
+    ev_arr = _event_handles(events) if events else None
     _check(load().gmlp_backward_dgrad(_p(dy), M, K, N, _p(splits), G, ctypes.byref(W2t.c()), ctypes.byref(W1t.c()),
                                       _p(pre_act), _p(probs), act, ctypes.byref(rec), _p(dx), _p(dprob),
                                       _p(fc1_dy.get("codes")), _p(fc1_dy.get("scales")), _p(workspace),
-                                      workspace.numel(), _stream(stream)))
+                                      workspace.numel(), ev_arr, len(events or ()), _stream(stream)))
     return dx, dprob
 
 

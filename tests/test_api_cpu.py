@@ -94,13 +94,17 @@ def test_forward_argument_checks(lib):
     w2 = g.QWeightC(FAKE, FAKE, None, 256, 256, 4, g.MXFP8, 0, 0)
     need = g.forward_workspace_size(512, 256, 256, 4, g.SWIGLU, r)
 
-    def call(M=512, K=256, N=256, G=4, W1=w1, W2=w2, act=g.SWIGLU, rec=r, ws=FAKE, wsb=need):
+    def call(M=512, K=256, N=256, G=4, W1=w1, W2=w2, act=g.SWIGLU, rec=r, ws=FAKE, wsb=need, y=FAKE):
         return L.gmlp_forward(FAKE, M, K, N, FAKE, G, ctypes.byref(W1), ctypes.byref(W2), None, act,
-                              ctypes.byref(rec), FAKE, None, ws, wsb, None)
+                              ctypes.byref(rec), y, None, ws, wsb, None)
 
     bad_aux = g.FwdAux(None, None, None, None, None, None, 0, 1)
     assert L.gmlp_forward(FAKE, 512, 256, 256, FAKE, 4, ctypes.byref(w1), ctypes.byref(w2), None, g.SWIGLU,
                           ctypes.byref(r), FAKE, ctypes.byref(bad_aux), FAKE, need, None) == g.ERR_INVALID_ARG
+    assert call(y=FAKE + 16) == g.ERR_INVALID_ARG                   # y is stored in 32-byte vectors
+    pre16 = g.FwdAux(None, None, None, None, None, None, 0, 0, None, None, 0.0, FAKE + 16)
+    assert L.gmlp_forward(FAKE, 512, 256, 256, FAKE, 4, ctypes.byref(w1), ctypes.byref(w2), None, g.SWIGLU,
+                          ctypes.byref(r), FAKE, ctypes.byref(pre16), FAKE, need, None) == g.ERR_INVALID_ARG
     assert call(K=128) == g.ERR_INVALID_DIMS                        # K % 256
     assert call(N=192) == g.ERR_INVALID_DIMS                        # N % 128
     assert call(G=3) == g.ERR_INVALID_DIMS                          # weights have 4 experts
@@ -224,12 +228,16 @@ def test_backward_dgrad_checks(lib):
     w1t = g.QWeightC(FAKE, FAKE, None, 512, 256, 4, g.MXFP8, 0, 0)   # [K x N1] (SReLU)
     need = L.gmlp_backward_workspace_size(512, 512, 256, 4, g.SRELU)
 
-    def call(K=512, N=256, act=g.SRELU, rec=r, W2t=w2t, W1t=w1t, pre=FAKE):
+    def call(K=512, N=256, act=g.SRELU, rec=r, W2t=w2t, W1t=w1t, pre=FAKE, ev=None, n_ev=0, dx=FAKE):
         return L.gmlp_backward_dgrad(FAKE, 512, K, N, FAKE, 4, ctypes.byref(W2t), ctypes.byref(W1t), pre, None, act,
-                                     ctypes.byref(rec), FAKE, None, None, None, FAKE, need, None)
+                                     ctypes.byref(rec), dx, None, None, None, FAKE, need, ev, n_ev, None)
 
     assert call(rec=g.recipe(g.NVFP4)) == g.ERR_UNSUPPORTED_RECIPE
     assert call(act=g.TANH_SRELU) == g.ERR_INVALID_ARG
     assert call(N=128) == g.ERR_INVALID_DIMS
     assert call(W2t=w1t) == g.ERR_INVALID_DIMS          # shapes swapped
     assert call(pre=None) == g.ERR_INVALID_ARG
+    assert call(pre=FAKE + 16) == g.ERR_INVALID_ARG      # read in 32-byte vectors
+    assert call(dx=FAKE + 16) == g.ERR_INVALID_ARG       # stored in 32-byte vectors
+    assert call(n_ev=4, ev=FAKE) == g.ERR_INVALID_ARG    # at most 3 stage events
+    assert call(n_ev=1) == g.ERR_INVALID_ARG             # events NULL
