@@ -114,8 +114,19 @@ __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
                : "memory");
 }
 
+__device__ __forceinline__ float bf16_half(uint32_t w, int hi) {
+  return bf16_bits_to_float(hi ? (w >> 16) : (w & 0xFFFFu));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return bf16_bits(lo) | (bf16_bits(hi) << 16);
+}
+
+// The same value as pack_bf16x2 in one paired conversion (fewer conversion
+// instructions; used where the epilogue is conversion-bound).
+__device__ __forceinline__ uint32_t pack2_bf16_rn(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Max |f| over n values as a balanced tree (short dependency chains).
@@ -169,24 +180,34 @@ __device__ __forceinline__ float dsilu(float g, float sg) { return sg * (1.0f + 
 // The accumulator is read one 32-column half at a time; each half yields the
 // gate and up fc1_dy blocks (bf16 pairs in registers) in one pass, then both
 // are quantised.
-// The dGLU values of one element: v0 = fc1_dy of the gate (or of h), v1 =
-// fc1_dy of the up column (SwiGLU), act_d = d * a for dprob.
+// The dGLU values of two adjacent columns, all operands bf16 pairs (d =
+// bf16(dfc2x), g / u the activation input; SReLU: g = h): w0 = fc1_dy of the
+// gate (or of h), w1 = fc1_dy of the up columns (SwiGLU), both rounded to bf16
+// once, in the packing; dsum += d * a per column, in column order.
 template <int EPI>
-__device__ __forceinline__ void dglu_values(float d, float g, float u, float prob, float& v0, float& v1,
-                                            float& act_d) {
-  const float da = d * prob;
-  if (EPI == EPI_DGLU_SWIGLU) {
-    const float sg = __fdividef(1.0f, 1.0f + __expf(fminf(-g, 80.0f)));
-    const float silu = g * sg;
-    act_d = d * (silu * u);
-    v0 = round_bf16(da * u * dsilu(g, sg));
-    v1 = round_bf16(da * silu);
-  } else {
-    const float r = fmaxf(g, 0.0f);
-    act_d = d * (r * r);
-    v0 = round_bf16(da * 2.0f * r);
-    v1 = 0.0f;
+__device__ __forceinline__ void dglu_pair(uint32_t dp, uint32_t gp, uint32_t up, float prob, uint32_t& w0,
+                                          uint32_t& w1, float& dsum) {
+  float v0[2], v1[2];
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    const float d = bf16_half(dp, kk), g = bf16_half(gp, kk);
+    const float da = d * prob;
+    if (EPI == EPI_DGLU_SWIGLU) {
+      const float u = bf16_half(up, kk);
+      const float sg = __fdividef(1.0f, 1.0f + __expf(fminf(-g, 80.0f)));
+      const float silu = g * sg;
+      dsum += d * (silu * u);
+      v0[kk] = da * u * dsilu(g, sg);
+      v1[kk] = da * silu;
+    } else {
+      const float r = fmaxf(g, 0.0f);
+      dsum += d * (r * r);
+      v0[kk] = da * 2.0f * r;
+      v1[kk] = 0.0f;
+    }
   }
+  w0 = pack2_bf16_rn(v0[0], v0[1]);
+  w1 = EPI == EPI_DGLU_SWIGLU ? pack2_bf16_rn(v1[0], v1[1]) : 0u;
 }
 
 // 32 bytes from global memory through the read-only path without allocating
@@ -198,10 +219,6 @@ __device__ __forceinline__ void ld_global_nc_v8(const void* p, uint32_t* w) {
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
-
-__device__ __forceinline__ float bf16_half(uint32_t w, int hi) {
-  return bf16_bits_to_float(hi ? (w >> 16) : (w & 0xFFFFu));
-}
 
 // max(|a|, |b|) of packed bf16 pairs (sign bits are the xor of the inputs').
 __device__ __forceinline__ uint32_t bmax_abs2_g(uint32_t a, uint32_t b) {
@@ -258,17 +275,11 @@ __device__ __forceinline__ float dglu_block(const GemmArgs& a, const float* acc3
     if (kGlu) ld_global_nc_v8(hrow + N + n0 + c, uw);
 #pragma unroll
     for (int k = 0; k < 16; k += 2) {
-      float v0[2], v1[2];
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        float ad;
-        const float g = bf16_half(gw[k >> 1], kk);
-        dglu_values<EPI>(round_bf16(acc32[c + k + kk]), g, kGlu ? bf16_half(uw[k >> 1], kk) : g, prob, v0[kk], v1[kk],
-                         ad);
-        dsum += ad;
-      }
-      ow0[(c + k) >> 1] = pack_bf16x2(v0[0], v0[1]);
-      if (kGlu) ow1[((c + k) >> 1) & (kGlu ? 15 : 0)] = pack_bf16x2(v1[0], v1[1]);
+      uint32_t w0, w1;
+      dglu_pair<EPI>(pack2_bf16_rn(acc32[c + k], acc32[c + k + 1]), gw[k >> 1], kGlu ? uw[k >> 1] : 0u, prob, w0, w1,
+                     dsum);
+      ow0[(c + k) >> 1] = w0;
+      if (kGlu) ow1[((c + k) >> 1) & (kGlu ? 15 : 0)] = w1;
     }
   }
   constexpr int kOuts = kGlu ? 2 : 1;  // fc1_dy outputs per fc2_x column (gate and up, or h)
