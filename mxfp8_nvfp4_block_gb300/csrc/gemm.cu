@@ -177,9 +177,9 @@ __device__ __forceinline__ float dsilu(float g, float sg) { return sg * (1.0f + 
 //   SReLU:  a = max(h,0)^2; dh = d prob 2 max(h,0)
 // fc1_dy = bf16(dg | du | dh) quantised to MXFP8 in 1x32 blocks (codes
 // [M][N1], scales GEMM_TILED for the fc1 dgrad), and dprob[row] += sum d a.
-// The accumulator is read one 32-column half at a time; each half yields the
-// gate and up fc1_dy blocks (bf16 pairs in registers) in one pass, then both
-// are quantised.
+// The accumulator is read as bf16 pairs and released at once; each 32-column
+// half then yields the gate and up fc1_dy blocks (bf16 pairs in registers) in
+// one pass, and both are quantised.
 // The dGLU values of two adjacent columns, all operands bf16 pairs (d =
 // bf16(dfc2x), g / u the activation input; SReLU: g = h): w0 = fc1_dy of the
 // gate (or of h), w1 = fc1_dy of the up columns (SwiGLU), both rounded to bf16
@@ -250,10 +250,11 @@ __device__ __forceinline__ int mx_block_packed(const uint32_t* w, uint8_t* dst) 
   return e;
 }
 
-// One 32-column block b of the dGLU epilogue: acc32 = dfc2x of columns
-// n0 + 32 b .. + 31 of this thread's row; returns sum d * act over them.
+// One 32-column block b of the dGLU epilogue: d16 = bf16(dfc2x) of columns
+// n0 + 32 b .. + 31 of this thread's row as packed pairs; returns sum d * act
+// over them.
 template <int EPI>
-__device__ __forceinline__ float dglu_block(const GemmArgs& a, const float* acc32, const Tile& t, const int* tb,
+__device__ __forceinline__ float dglu_block(const GemmArgs& a, const uint32_t* d16, const Tile& t, const int* tb,
                                             int lr, int64_t grow, int q, int lane, int slice, float prob, int b) {
   constexpr bool kGlu = EPI == EPI_DGLU_SWIGLU;
   const int n0 = t.nt * kBN + slice * kSliceCols + 32 * b;
@@ -276,8 +277,7 @@ __device__ __forceinline__ float dglu_block(const GemmArgs& a, const float* acc3
 #pragma unroll
     for (int k = 0; k < 16; k += 2) {
       uint32_t w0, w1;
-      dglu_pair<EPI>(pack2_bf16_rn(acc32[c + k], acc32[c + k + 1]), gw[k >> 1], kGlu ? uw[k >> 1] : 0u, prob, w0, w1,
-                     dsum);
+      dglu_pair<EPI>(d16[(c + k) >> 1], gw[k >> 1], kGlu ? uw[k >> 1] : 0u, prob, w0, w1, dsum);
       ow0[(c + k) >> 1] = w0;
       if (kGlu) ow1[((c + k) >> 1) & (kGlu ? 15 : 0)] = w1;
     }
@@ -805,23 +805,27 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       tc_fence_after();
       const uint32_t taddr = tbase + (uint32_t(32 * q) << 16) + uint32_t(slice * kSliceCols);
       if (EPI == EPI_DGLU_SWIGLU || EPI == EPI_DSRELU) {
-        // backward dGLU: one 32-column half of the accumulator at a time (the
-        // accumulator is released after the second load)
+        // backward dGLU: the accumulator is read as bf16 pairs (the epilogue's
+        // first rounding) and released before any of the math
         const int lr = row_base + 32 * q + lane;
         const bool valid = lr < off[t.g + 1] - off[t.g];
         const int64_t grow = (int64_t)off[t.g] + lr;
-        float acc32[32];
-        tmem_ld32(taddr, acc32);
-        tmem_wait_ld();
-        float dsum = valid ? dglu_block<EPI>(a, acc32, t, tb, lr, grow, q, lane, slice, prob, 0) : 0.0f;
-        tmem_ld32(taddr + 32, acc32);
-        tmem_wait_ld();
+        uint32_t d16[32];  // bf16(dfc2x) of the 64 columns, packed pairs
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float acc32[32];
+          tmem_ld32(taddr + 32 * h, acc32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) d16[16 * h + i] = pack2_bf16_rn(acc32[2 * i], acc32[2 * i + 1]);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty);
         acc_phase ^= 1;
         if (valid) {
-          dsum += dglu_block<EPI>(a, acc32, t, tb, lr, grow, q, lane, slice, prob, 1);
+          float dsum = dglu_block<EPI>(a, d16, t, tb, lr, grow, q, lane, slice, prob, 0);
+          dsum += dglu_block<EPI>(a, d16 + 16, t, tb, lr, grow, q, lane, slice, prob, 1);
           if (a.dprob) atomicAdd(a.dprob + grow, dsum);
         }
         continue;
