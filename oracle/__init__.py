@@ -14,12 +14,15 @@ Layout:
   quant.py   -- group quantisers (``group_quantize``, ``group_hadamard_amax``,
                 ``group_quantize_with_amax``)
   forward.py -- the forward (``forward``) and per-expert weight quantisation
+  backward.py -- the backward's data gradients (``backward_dgrad``) and weight
+                gradients (``backward_wgrad``, columnwise MXFP8 ``mxfp8_colwise``)
   layout.py  -- the boundary's scale layouts (COMPACT, GEMM_TILED)
 
 Parity pins live in tests/test_oracle_*.py.  Functions without a pin: none.
 """
 from ._lib import build, lib  # noqa: F401
-from .backward import backward_dgrad, dact  # noqa: F401
+from .backward import (backward_dgrad, backward_wgrad, dact, mxfp8_colwise, padded_offsets,  # noqa: F401
+                       recompute_fc2x)
 from .forward import SRELU, SWIGLU, TANH_SRELU, activation, dequant_weight, forward, quantize_weights  # noqa: F401
 from .layout import (compact_to_tiled, group_offsets, tile_bases, tiled_index, tiled_size,  # noqa: F401
                      tiled_to_compact, tiled_to_x4)

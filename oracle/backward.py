@@ -82,3 +82,78 @@ def backward_dgrad(dy, splits, W1, W2, h, probs, act: int, *, qw1t=None, qw2t=No
         fd = mxfp8_dequant_rows(fq, fs)
         out["dx"][r0:r1] = f64_to_bf16(fd @ dequant_weight(qw1t, g, MXFP8).T)
     return out
+
+
+def padded_offsets(splits) -> np.ndarray:
+    """Token offsets of the groups in a columnwise (wgrad) operand: each group's
+    token count rounded up to a multiple of 128 (zero tokens in the padding),
+    groups side by side; the last entry is the total T."""
+    p = (np.asarray(splits, dtype=np.int64) + 127) // 128 * 128
+    return np.concatenate([[0], np.cumsum(p)]).astype(np.int64)
+
+
+def mxfp8_colwise(x, splits) -> tuple[np.ndarray, np.ndarray]:
+    """Columnwise MXFP8 of a token-sorted bf16 matrix x [M, C] (bits), the
+    weight-gradient operand layout: per group g the transpose x_g^T [C, m_g],
+    zero-padded to T_g = 128 ceil(m_g / 128) tokens, is quantised in 1x32 blocks
+    along the tokens (blocks counted from the group's first token); groups sit
+    side by side.  Returns codes [C, T] and E8M0 scales [C, T / 32] (compact)."""
+    x = np.ascontiguousarray(x).view(np.uint16)
+    C = x.shape[1]
+    offs, pofs = group_offsets(splits), padded_offsets(splits)
+    T = int(pofs[-1])
+    codes = np.zeros((C, T), np.uint8)
+    scales = np.zeros((C, T // 32), np.uint8)
+    for g in range(len(offs) - 1):
+        r0, r1, p0, p1 = int(offs[g]), int(offs[g + 1]), int(pofs[g]), int(pofs[g + 1])
+        if p1 == p0:
+            continue
+        xt = np.zeros((C, p1 - p0), np.uint16)
+        xt[:, :r1 - r0] = x[r0:r1].T
+        codes[:, p0:p1], scales[:, p0 // 32:p1 // 32] = mxfp8_quantize_rows(xt)
+    return codes, scales
+
+
+def recompute_fc2x(h, probs, act: int) -> np.ndarray:
+    """fc2_x rebuilt from the saved activation input: bf16(act(h) * prob), the
+    forward's own definition (h [M, N1] bf16 bits, probs [M] or None = 1)."""
+    hb = bf16_to_f64(np.ascontiguousarray(h).view(np.uint16))
+    p = np.ones(hb.shape[0]) if probs is None else np.asarray(probs, dtype=np.float64)
+    return f64_to_bf16(activation(hb, act) * p[:, None])
+
+
+def backward_wgrad(x, dy, h, probs, fc1_dy, splits, act: int) -> dict:
+    """Oracle of gmlp_backward_wgrad (MXFP8).
+
+    PR #2769 "GEMM + Swiglu fused Grouped MLP for MXFP8", sequence diagram,
+    backward pass: the weight gradients come from grouped GEMMs ("wgrad via
+    general_grouped_gemm") beside the dGLU and dgrad kernels, on the columnwise
+    MXFP8 operands (the forward's `d_col_tensor`, the dGLU's columnwise
+    fc1_dy).  Per group g (m_g tokens; an empty group has zero gradients):
+      fc2_x = bf16(act(h) * prob)                                   [M, N]
+      dW2_g = dq(colq(dy_g)) @ dq(colq(fc2_x_g))^T                  [K, N]
+      dW1_g = dq(colq(fc1_dy_g)) @ dq(colq(x_g))^T                  [N1, K]
+      dbias1_g = sum_t fc1_dy[t, :],  dbias2_g = sum_t dy[t, :]      (bf16 values)
+    colq = mxfp8_colwise (1x32 blocks along the tokens); float64 products.
+    x [M, K], dy [M, K], h [M, N1], fc1_dy [M, N1] bf16 bits; dW1 rows in the
+    logical order of fc1's outputs (SwiGLU: gate rows, then up rows)."""
+    x, dy = np.ascontiguousarray(x).view(np.uint16), np.ascontiguousarray(dy).view(np.uint16)
+    fc1_dy = np.ascontiguousarray(fc1_dy).view(np.uint16)
+    K, N1 = x.shape[1], fc1_dy.shape[1]
+    fc2x = recompute_fc2x(h, probs, act)
+    N = fc2x.shape[1]
+    G = len(splits)
+    offs, pofs = group_offsets(splits), padded_offsets(splits)
+    deq = {}
+    for name, m in (("dy", dy), ("fc2x", fc2x), ("fc1_dy", fc1_dy), ("x", x)):
+        deq[name] = mxfp8_dequant_rows(*mxfp8_colwise(m, splits))
+    out = dict(dW1=np.zeros((G, N1, K)), dW2=np.zeros((G, K, N)), dbias1=np.zeros((G, N1)),
+               dbias2=np.zeros((G, K)), fc2x=fc2x)
+    for g in range(G):
+        p0, p1 = int(pofs[g]), int(pofs[g + 1])
+        r0, r1 = int(offs[g]), int(offs[g + 1])
+        out["dW2"][g] = deq["dy"][:, p0:p1] @ deq["fc2x"][:, p0:p1].T
+        out["dW1"][g] = deq["fc1_dy"][:, p0:p1] @ deq["x"][:, p0:p1].T
+        out["dbias1"][g] = bf16_to_f64(fc1_dy[r0:r1]).sum(axis=0)
+        out["dbias2"][g] = bf16_to_f64(dy[r0:r1]).sum(axis=0)
+    return out

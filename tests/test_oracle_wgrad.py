@@ -1,0 +1,94 @@
+"""Pins of the oracle's weight-gradient backward (columnwise MXFP8 operands and
+grouped wgrad GEMMs) against closed forms and brute force (CPU)."""
+import numpy as np
+import torch
+
+
+def as_bits(a):
+    """bf16 bits of exactly representable values (torch rounding)."""
+    return torch.from_numpy(np.asarray(a, np.float64).astype(np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def test_colwise_blocks_run_along_the_tokens_of_each_group(orc):
+    """x[t, c] = s_c 2^(j + c mod 3), j = the 32-token block of t counted from
+    its group's first token: every block along the tokens holds one magnitude,
+    so its E8M0 byte is (j + c mod 3) - 8 + 127 and every code is E4M3(+-256) =
+    0x78 | sign; tokens past a group's end are zero codes and a block with no
+    tokens has byte 0.  Blocks taken along the columns, or counted from row 0
+    of x, give other bytes."""
+    splits = np.array([40, 0, 70, 128])
+    C = 12
+    offs = orc.group_offsets(splits)
+    x = np.zeros((int(offs[-1]), C))
+    sign = np.where(np.arange(C) % 2 == 0, 1.0, -1.0)
+    for g in range(len(splits)):
+        for t in range(offs[g], offs[g + 1]):
+            j = (t - offs[g]) // 32
+            x[t] = sign * 2.0 ** (j + np.arange(C) % 3)
+    codes, scales = orc.mxfp8_colwise(as_bits(x), splits)
+    pofs = orc.padded_offsets(splits)
+    assert list(pofs) == [0, 128, 128, 256, 384]
+    assert codes.shape == (C, 384) and scales.shape == (C, 12)
+    for g in range(len(splits)):
+        m = int(splits[g])
+        for c in range(C):
+            seg = codes[c, pofs[g]:pofs[g + 1]]
+            want = 0x78 | (0x80 if sign[c] < 0 else 0)
+            assert np.all(seg[:m] == want) and np.all(seg[m:] == 0), (g, c)
+            for jb in range((pofs[g + 1] - pofs[g]) // 32):
+                byte = scales[c, pofs[g] // 32 + jb]
+                expect = (jb + c % 3) - 8 + 127 if 32 * jb < m else 0
+                assert byte == expect, (g, c, jb)
+
+
+def _loops_matmul_t(a, b):
+    """sum_t a[t, i] b[t, j] by explicit loops (float64)."""
+    out = np.zeros((a.shape[1], b.shape[1]))
+    for t in range(a.shape[0]):
+        for i in range(a.shape[1]):
+            if a[t, i] != 0.0:
+                for j in range(b.shape[1]):
+                    out[i, j] += a[t, i] * b[t, j]
+    return out
+
+
+def test_wgrad_lossless_equals_brute_force():
+    """SReLU, operands from {0, +-1, +-2, +-4} and probs from {1, 0.5}: every
+    columnwise MXFP8 block is exact (block max 1, 2 or 4), so the weight
+    gradients equal plain float64 sums over each expert's tokens, computed here
+    by loops: dW2_g[k, n] = sum_t dy[t, k] relu(h)^2 p, dW1_g[j, k] = sum_t
+    fc1_dy[t, j] x[t, k], and the bias gradients the token sums.  An empty
+    expert gets zeros; K != N1 fixes the orientation of each gradient."""
+    import oracle as orc
+
+    rng = np.random.default_rng(21)
+    splits = np.array([40, 0, 70])
+    K, N = 48, 16
+    offs = orc.group_offsets(splits)
+    M = int(offs[-1])
+    x = rng.choice([0.0, 1.0, -1.0], size=(M, K))
+    dy = rng.choice([0.0, 1.0, -1.0, 2.0, -2.0], size=(M, K))
+    h = rng.choice([0.0, 1.0, -1.0, 2.0], size=(M, N))
+    fc1_dy = rng.choice([0.0, 1.0, -4.0, 2.0], size=(M, N))
+    probs = rng.choice([1.0, 0.5], size=M).astype(np.float32)
+    out = orc.backward_wgrad(as_bits(x), as_bits(dy), as_bits(h), probs, as_bits(fc1_dy), splits, orc.SRELU)
+    fc2x = np.maximum(h, 0.0) ** 2 * probs[:, None]
+    assert out["dW2"].shape == (3, K, N) and out["dW1"].shape == (3, N, K)
+    for g in range(3):
+        sl = slice(offs[g], offs[g + 1])
+        np.testing.assert_array_equal(out["dW2"][g], _loops_matmul_t(dy[sl], fc2x[sl]))
+        np.testing.assert_array_equal(out["dW1"][g], _loops_matmul_t(fc1_dy[sl], x[sl]))
+        np.testing.assert_array_equal(out["dbias1"][g], fc1_dy[sl].sum(axis=0))
+        np.testing.assert_array_equal(out["dbias2"][g], dy[sl].sum(axis=0))
+    assert not out["dW2"][1].any() and not out["dW1"][1].any()
+
+
+def test_recompute_fc2x_swiglu_closed_form(orc):
+    """SwiGLU fc2_x from h = [gate | up]: gate 0 gives silu 0; gate 2, up 1,
+    prob 1 gives bf16(2 / (1 + e^-2))."""
+    h = np.array([[0.0, 2.0, 3.0, 1.0]])
+    f = orc.recompute_fc2x(as_bits(h), np.array([1.0]), orc.SWIGLU)
+    assert f[0, 0] == 0
+    want = as_bits(np.array([2.0 / (1.0 + np.exp(-2.0))]))[0]
+    assert f[0, 1] == want
