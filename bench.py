@@ -392,8 +392,35 @@ def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps
             st[i] += se[i].elapsed_time(se[i + 1]) / K_steps
     gmlp.check_device_status()
     flops = 2.0 * w.M * w.K * w.N + 2.0 * w.M * w.n1 * w.K
+    # weight gradients on the dgrad's own bf16 fc1_dy: columnwise MXFP8 of dy,
+    # fc2_x (rebuilt from h), fc1_dy and x, the two grouped wgrad GEMMs (FP32
+    # dW) and the bias gradients
+    f1 = torch.empty((w.M, w.n1), dtype=torch.bfloat16, device=dev)
+    gmlp.backward_dgrad(dy, splits, w2t, w1t, h, probs, w.act, rec, dx=dx, workspace=ws, fc1_dy_bf16=f1)
+    xin = x
+    wws = torch.empty(gmlp.load().gmlp_backward_wgrad_workspace_size(w.M, w.K, w.N, w.G, w.act), dtype=torch.uint8,
+                      device=dev)
+    grads = gmlp.backward_wgrad(xin, dy, h, probs, f1, splits, w.act, workspace=wws)
+    for _ in range(W_steps):
+        flush.zero_()
+        gmlp.backward_wgrad(xin, dy, h, probs, f1, splits, w.act, workspace=wws, **grads)
+    torch.cuda.synchronize()
+    ew = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
+    for e0, e1 in ew:
+        flush.zero_()
+        e0.record()
+        gmlp.backward_wgrad(xin, dy, h, probs, f1, splits, w.act, workspace=wws, **grads)
+        e1.record()
+    torch.cuda.synchronize()
+    gmlp.check_device_status()
+    wms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ew)
+    del grads, wws, f1
+    wgrad = {"what": "dW1, dW2 (FP32) and dbias1, dbias2: columnwise MXFP8 of dy, fc2_x (rebuilt from the saved "
+                     "activation input), fc1_dy and x, two grouped wgrad GEMMs over each expert's tokens",
+             "ms_per_step": round(wms, 5), "flops_per_step": flops, "TFLOP_s": round(flops / (wms * 1e-3) / 1e12, 2)}
     return {"what": "dx and dprob: dy MXFP8 cast, fc2 dGLU GEMM (fused dact x prob, dprob, MXFP8 fc1_dy), "
-                    "fc1 dgrad GEMM; weight gradients not included",
+                    "fc1 dgrad GEMM",
+            "wgrad": wgrad,
             "ms_per_step": round(ms, 5), "flops_per_step": flops, "TFLOP_s": round(flops / (ms * 1e-3) / 1e12, 2),
             "stages_ms": [round(t, 5) for t in st],
             "stage_tflops": {"dglu": round(2.0 * w.M * w.K * w.N / (st[1] * 1e-3) / 1e12, 1),

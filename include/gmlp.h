@@ -65,6 +65,16 @@
  *     a multiple of 4.
  * Columnwise NVFP4 output (per group, groups concatenated in order): codes
  *   [cols][Mpad_g/2] and scales [cols][Mpad_g/16], Mpad_g = 16*ceil(m_g/16).
+ * Columnwise MXFP8 output (the weight-gradient GEMM operand): one code matrix
+ *   [cols][T], T = gmlp_colwise_tokens(M, G) = 128 (ceil(M/128) + G); group g's
+ *   tokens, cut into 128-token chunks from its first token, fill columns
+ *   128 c_g .. 128 (c_g + ceil(m_g/128)) - 1 with c_g = sum_{h<g} ceil(m_h/128)
+ *   (zero codes past the group's end; columns past the last chunk are not
+ *   written); one E8M0 scale per 32 tokens, in the GEMM_TILED form of a
+ *   [cols]-row operand with T/32 scales per row: the 512-byte block of column
+ *   tile r (128 columns) and chunk c at byte (r * (T/128) + c) * 512, the scale
+ *   of column 128 r + i, block j of the chunk at (i % 32) * 16 + (i / 32) * 4 + j.
+ *   Scales buffer: cols * T / 32 bytes.
  */
 #ifndef GMLP_H_
 #define GMLP_H_
@@ -127,6 +137,9 @@ typedef struct gmlp_qtensor {
   uint8_t* scales;
 } gmlp_qtensor;
 
+/* T of the columnwise MXFP8 layout: 128 (ceil(M / 128) + G) (0 if M < 0 or G < 1). */
+GMLP_API int64_t gmlp_colwise_tokens(int64_t M, int32_t G);
+
 /* Bytes of a GEMM_TILED scale buffer for M rows in G groups with `nscale`
  * scale columns per row (cols/32 for MXFP8, cols/16 for NVFP4). */
 GMLP_API size_t gmlp_tiled_scales_bytes(int64_t M, int32_t G, int64_t nscale);
@@ -153,8 +166,8 @@ GMLP_API gmlp_status gmlp_group_hadamard_amax(const uint16_t* x, int64_t M, int6
  *     the RHT-transformed chunks with S_g from amax_post[g] when
  *     recipe->use_rht, else of the plain chunks with S_g from amax_pre[g].
  *   amax_pre / amax_post: device float [G] (NVFP4; ignored for MXFP8).
- * Limits: 1 <= G <= 512, K % 128 == 0.  MXFP8 with col_out is
- * GMLP_ERR_UNSUPPORTED_RECIPE.  At least one of row_out / col_out. */
+ *   col_out with MXFP8: the columnwise MXFP8 layout above (no amax needed).
+ * Limits: 1 <= G <= 512, K % 128 == 0.  At least one of row_out / col_out. */
 GMLP_API gmlp_status gmlp_group_quantize_with_amax(const uint16_t* x, int64_t M, int64_t K,
                                           const int64_t* split_sizes, int32_t G,
                                           const gmlp_recipe* recipe, const float* amax_pre,
@@ -338,7 +351,9 @@ GMLP_API size_t gmlp_backward_workspace_size(int64_t M, int64_t K, int64_t N, in
  *      and prob p: SwiGLU (g = h[:, :N], u = h[:, N:]): dg = dfc2x p u silu'(g),
  *      du = dfc2x p silu(g); SReLU: dh = dfc2x p 2 max(h,0); fc1_dy =
  *      bf16(dg | du) or bf16(dh) [M, N1], quantised to MXFP8 rowwise (codes and
- *      GEMM_TILED scales to fc1_dy_codes / fc1_dy_scales when given);
+ *      GEMM_TILED scales to fc1_dy_codes / fc1_dy_scales when given; the bf16
+ *      values to fc1_dy_bf16 [M, N1] when given, 32-byte aligned: the operand
+ *      gmlp_backward_wgrad takes);
  *      dprob[t] = sum_n dfc2x[t,n] act(h)[t,n] (zeroed, then accumulated);
  *   4. dx = bf16(dq(fc1_dy_g) dq(W1t_g)^T) [m_g, K] (W1t = W1^T in logical
  *      gate/up order, [K][N1] per expert, quantised along N1).
@@ -351,9 +366,40 @@ GMLP_API gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t 
                                          const int64_t* split_sizes, int32_t G, const gmlp_qweight* W2t,
                                          const gmlp_qweight* W1t, const uint16_t* pre_act, const float* probs,
                                          int32_t act, const gmlp_recipe* recipe, uint16_t* dx, float* dprob,
-                                         uint8_t* fc1_dy_codes, uint8_t* fc1_dy_scales, void* workspace,
-                                         size_t workspace_bytes, gmlp_event* stage_events,
+                                         uint8_t* fc1_dy_codes, uint8_t* fc1_dy_scales, uint16_t* fc1_dy_bf16,
+                                         void* workspace, size_t workspace_bytes, gmlp_event* stage_events,
                                          int32_t n_stage_events, gmlp_stream stream);
+
+/* Workspace bytes gmlp_backward_wgrad needs: four columnwise MXFP8 operands
+ * of T = 128 (ceil(M / 128) + G) padded tokens (about (2K + N + N1) T bytes). */
+GMLP_API size_t gmlp_backward_wgrad_workspace_size(int64_t M, int64_t K, int64_t N, int32_t G, int32_t act);
+
+/* gmlp_backward_wgrad -- the weight-gradient half of the fused grouped-MLP
+ * backward, MXFP8 (PR #2769 sequence diagram, backward pass: "wgrad via
+ * general_grouped_gemm" beside the dGLU and dGrad kernels, on columnwise
+ * MXFP8 operands):
+ *   colq(A) = per expert g, A_g^T zero-padded to 128 ceil(m_g / 128) tokens and
+ *             quantised to MXFP8 in 1x32 blocks along the tokens (counted from
+ *             the expert's first token);
+ *   fc2_x   = bf16(act(h) p), rebuilt from pre_act exactly as the forward's
+ *             fc1 epilogue computes it;
+ *   dW2_g   = dq(colq(dy_g)) dq(colq(fc2_x_g))^T      [K, N]  (FP32, per expert)
+ *   dW1_g   = dq(colq(fc1_dy_g)) dq(colq(x_g))^T      [N1, K] (logical gate/up order)
+ *   dbias2_g = sum over g's tokens of dy [K];  dbias1_g = sum of fc1_dy [N1].
+ * x [M,K] (the forward input), dy [M,K], fc1_dy [M,N1] (gmlp_backward_dgrad's
+ * fc1_dy_bf16) bf16, 16-byte aligned; pre_act [M,N1] (gmlp_fwd_aux.fc1_pre_act)
+ * 32-byte aligned; probs [M] or NULL (= 1).  Outputs on the device, FP32:
+ * dW1 [G][N1][K] and dW2 [G][K][N] (32-byte aligned), dbias1 [G][N1],
+ * dbias2 [G][K]; any of them may be NULL (its work is skipped; an input only
+ * it needs may then be NULL).  accumulate = 0 overwrites them (an expert with
+ * no tokens gets zeros); 1 adds the new gradients into them.  The GEMMs
+ * accumulate in FP32 on the tensor cores; the bias sums are FP32 atomics.
+ * act: SWIGLU or SRELU.  Limits: K % 256 == 0, N % 256 == 0. */
+GMLP_API gmlp_status gmlp_backward_wgrad(const uint16_t* x, const uint16_t* dy, const uint16_t* pre_act,
+                                         const float* probs, const uint16_t* fc1_dy, int64_t M, int64_t K, int64_t N,
+                                         const int64_t* split_sizes, int32_t G, int32_t act, float* dW1, float* dW2,
+                                         float* dbias1, float* dbias2, int32_t accumulate, void* workspace,
+                                         size_t workspace_bytes, gmlp_stream stream);
 
 /* Self-test of the device failure path (no counterpart on the pages): one
  * warp waits, through the same bounded mbarrier wait the kernels use, on a

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgmlp.so")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "noalloc.cu", "peak.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "noalloc.cu", "peak.cu", "wgrad.cu"]
 HEADERS = ["device.cuh", "internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

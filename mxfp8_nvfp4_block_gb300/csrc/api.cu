@@ -15,6 +15,7 @@ namespace gmlp {
 int quant_read_clear_status();
 int gemm_read_clear_status();
 int peak_read_clear_status();
+int wgrad_read_clear_status();
 
 namespace {
 
@@ -122,6 +123,34 @@ BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N1, int32_t G) {
   L.dy_scales = take(tiled_bytes(M, G, K / 32));
   L.g_codes = take((size_t)M * N1);
   L.g_scales = take(tiled_bytes(M, G, N1 / 32));
+  L.total = cur;
+  return L;
+}
+
+// weight-gradient workspace: four columnwise MXFP8 operands ([C][T] codes and
+// their GEMM_TILED scales) with T = 128 x (chunk capacity of M tokens in G groups)
+struct WgradLayout {
+  int64_t T;
+  size_t dy_c, dy_s, f_c, f_s, g_c, g_s, x_c, x_s, total;
+};
+
+WgradLayout wgrad_layout(int64_t M, int64_t K, int64_t N, int64_t N1, int32_t G) {
+  WgradLayout L{};
+  L.T = gmlp_colwise_tokens(M, G);
+  size_t cur = 0;
+  auto take = [&](size_t b) {
+    size_t o = cur;
+    cur += align256(b);
+    return o;
+  };
+  L.dy_c = take((size_t)K * L.T);
+  L.dy_s = take((size_t)K * L.T / 32);
+  L.f_c = take((size_t)N * L.T);
+  L.f_s = take((size_t)N * L.T / 32);
+  L.g_c = take((size_t)N1 * L.T);
+  L.g_s = take((size_t)N1 * L.T / 32);
+  L.x_c = take((size_t)K * L.T);
+  L.x_s = take((size_t)K * L.T / 32);
   L.total = cur;
   return L;
 }
@@ -246,16 +275,30 @@ static gmlp_status quantize_with_amax_impl(const uint16_t* x, int64_t M, int64_t
                                            const gmlp_qtensor* col_out, cudaStream_t s) {
   GroupSrc gs{split_sizes, 0, G, M};
   if (r->format == GMLP_MXFP8) {
-    RowQuantArgs a{};
-    a.x = x;
-    a.M = M;
-    a.K = K;
-    a.grp = gs;
-    a.format = GMLP_MXFP8;
-    a.tiled = r->scale_layout == GMLP_SCALES_GEMM_TILED;
-    a.codes = row_out->codes;
-    a.scales = row_out->scales;
-    GMLP_CUDA(launch_row_quant(a, s), "row_quant launch");
+    if (row_out) {
+      RowQuantArgs a{};
+      a.x = x;
+      a.M = M;
+      a.K = K;
+      a.grp = gs;
+      a.format = GMLP_MXFP8;
+      a.tiled = r->scale_layout == GMLP_SCALES_GEMM_TILED;
+      a.codes = row_out->codes;
+      a.scales = row_out->scales;
+      GMLP_CUDA(launch_row_quant(a, s), "row_quant launch");
+    }
+    if (col_out) {
+      ColqArgs q{};
+      q.src = x;
+      q.ld = K;
+      q.C = K;
+      q.grp = gs;
+      q.T = gmlp_colwise_tokens(M, G);
+      q.codes = col_out->codes;
+      q.scales = col_out->scales;
+      q.mode = COLQ_PLAIN;
+      GMLP_CUDA(launch_colq(q, s), "columnwise MXFP8 launch");
+    }
     return GMLP_OK;
   }
   if (col_out) {
@@ -299,8 +342,8 @@ static gmlp_status check_quant_args(const uint16_t* x, int64_t M, int64_t K, con
   if (M > 0 && !x) return fail(GMLP_ERR_INVALID_ARG, "x is NULL");
   if (!aligned16(x)) return fail(GMLP_ERR_INVALID_ARG, "x not 16-byte aligned");
   if (!row_out && !col_out) return fail(GMLP_ERR_INVALID_ARG, "neither row_out nor col_out given");
-  if (recipe->format == GMLP_MXFP8 && col_out)
-    return fail(GMLP_ERR_UNSUPPORTED_RECIPE, "columnwise MXFP8 output is not part of this path");
+  if (recipe->format == GMLP_MXFP8 && col_out && (!aligned32(col_out->codes) || !aligned32(col_out->scales)))
+    return fail(GMLP_ERR_INVALID_ARG, "columnwise MXFP8 codes / scales not 32-byte aligned");
   GMLP_TRY(check_qtensor(row_out, "row_out"));
   GMLP_TRY(check_qtensor(col_out, "col_out"));
   return GMLP_OK;
@@ -636,7 +679,8 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
                                 int32_t G, const gmlp_qweight* W2t, const gmlp_qweight* W1t,
                                 const uint16_t* pre_act, const float* probs, int32_t act, const gmlp_recipe* recipe,
                                 uint16_t* dx, float* dprob, uint8_t* fc1_dy_codes, uint8_t* fc1_dy_scales,
-                                void* workspace, size_t workspace_bytes, gmlp_event* stage_events,
+                                uint16_t* fc1_dy_bf16, void* workspace, size_t workspace_bytes,
+                                gmlp_event* stage_events,
                                 int32_t n_stage_events, gmlp_stream stream) {
   g_last_error[0] = 0;
   GMLP_TRY(check_groups(G, M, split_sizes));
@@ -664,6 +708,7 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
       !aligned16(fc1_dy_scales))
     return fail(GMLP_ERR_INVALID_ARG, "fc1_dy_codes / fc1_dy_scales: both or neither, 16-byte aligned");
   if (probs && (reinterpret_cast<uintptr_t>(probs) & 3)) return fail(GMLP_ERR_INVALID_ARG, "probs misaligned");
+  if (!aligned32(fc1_dy_bf16)) return fail(GMLP_ERR_INVALID_ARG, "fc1_dy_bf16 not 32-byte aligned");
   if (n_stage_events < 0 || n_stage_events > 3 || (n_stage_events > 0 && !stage_events))
     return fail(GMLP_ERR_INVALID_ARG, "n_stage_events = %d: 0..3, stage_events non-NULL", n_stage_events);
   const BwdLayout L = bwd_layout(M, K, N1, G);
@@ -712,6 +757,7 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
   g1.dprob = dprob;
   g1.out_codes = g_codes;
   g1.out_scales = g_scales;
+  g1.out_bf16 = fc1_dy_bf16;
   g1.n_cols_out = N1;
   g1.pair = 1;
   g1.pdl = 1;
@@ -734,6 +780,102 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
   g2.pdl = 1;
   GMLP_CUDA(launch_gemm(g2, s), "fc1 dgrad launch");
   GMLP_TRY(stage_done(2));
+  return GMLP_OK;
+}
+
+int64_t gmlp_colwise_tokens(int64_t M, int32_t G) {
+  if (M < 0 || G < 1) return 0;
+  return 128 * ((M + 127) / 128 + G);
+}
+
+size_t gmlp_backward_wgrad_workspace_size(int64_t M, int64_t K, int64_t N, int32_t G, int32_t act) {
+  if (M < 0 || K <= 0 || N <= 0 || G < 1) return 0;
+  return wgrad_layout(M, K, N, act == GMLP_ACT_SWIGLU ? 2 * N : N, G).total;
+}
+
+gmlp_status gmlp_backward_wgrad(const uint16_t* x, const uint16_t* dy, const uint16_t* pre_act, const float* probs,
+                                const uint16_t* fc1_dy, int64_t M, int64_t K, int64_t N, const int64_t* split_sizes,
+                                int32_t G, int32_t act, float* dW1, float* dW2, float* dbias1, float* dbias2,
+                                int32_t accumulate, void* workspace, size_t workspace_bytes, gmlp_stream stream) {
+  g_last_error[0] = 0;
+  GMLP_TRY(check_groups(G, M, split_sizes));
+  if (act != GMLP_ACT_SWIGLU && act != GMLP_ACT_SRELU)
+    return fail(GMLP_ERR_INVALID_ARG, "wgrad act = %d: SwiGLU or SReLU", act);
+  if (accumulate != 0 && accumulate != 1) return fail(GMLP_ERR_INVALID_ARG, "accumulate = %d: 0 or 1", accumulate);
+  const int64_t N1 = act == GMLP_ACT_SWIGLU ? 2 * N : N;
+  if (K <= 0 || K % 256 || N <= 0 || N % 256)
+    return fail(GMLP_ERR_INVALID_DIMS, "K = %lld, N = %lld: both positive multiples of 256", (long long)K,
+                (long long)N);
+  const bool want1 = dW1 || dbias1, want2 = dW2 || dbias2;
+  if (M > 0 && ((want2 && !dy) || (dW2 && !pre_act) || (want1 && !fc1_dy) || (dW1 && !x)))
+    return fail(GMLP_ERR_INVALID_ARG, "an input a requested gradient needs is NULL");
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(fc1_dy) || !aligned32(pre_act))
+    return fail(GMLP_ERR_INVALID_ARG, "x / dy / fc1_dy not 16-byte or pre_act not 32-byte aligned");
+  if (!aligned32(dW1) || !aligned32(dW2) || (reinterpret_cast<uintptr_t>(dbias1) & 3) ||
+      (reinterpret_cast<uintptr_t>(dbias2) & 3))
+    return fail(GMLP_ERR_INVALID_ARG, "dW1 / dW2 not 32-byte or dbias1 / dbias2 not 4-byte aligned");
+  if (probs && (reinterpret_cast<uintptr_t>(probs) & 3)) return fail(GMLP_ERR_INVALID_ARG, "probs misaligned");
+  const WgradLayout L = wgrad_layout(M, K, N, N1, G);
+  if (!workspace || workspace_bytes < L.total || !aligned16(workspace))
+    return fail(GMLP_ERR_WORKSPACE, "workspace %zu bytes, need %zu (16-byte aligned)", workspace_bytes, L.total);
+  GMLP_TRY(check_device());
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!accumulate) {
+    // an empty batch still has (zero) gradients; the kernels overwrite the rest
+    if (M == 0 && dW1) GMLP_CUDA(cudaMemsetAsync(dW1, 0, sizeof(float) * G * N1 * K, s), "dW1 memset");
+    if (M == 0 && dW2) GMLP_CUDA(cudaMemsetAsync(dW2, 0, sizeof(float) * G * K * N, s), "dW2 memset");
+    if (dbias1) GMLP_CUDA(cudaMemsetAsync(dbias1, 0, sizeof(float) * G * N1, s), "dbias1 memset");
+    if (dbias2) GMLP_CUDA(cudaMemsetAsync(dbias2, 0, sizeof(float) * G * K, s), "dbias2 memset");
+  }
+  if (M == 0) return GMLP_OK;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const GroupSrc gs{split_sizes, 0, G, M};
+  auto colq = [&](const uint16_t* src, int64_t ld, int64_t C, int mode, size_t c_off, size_t s_off,
+                  float* colsum) -> gmlp_status {
+    ColqArgs q{};
+    q.src = src;
+    q.ld = ld;
+    q.C = C;
+    q.up_off = N;
+    q.probs = probs;
+    q.grp = gs;
+    q.T = L.T;
+    q.codes = ws + c_off;
+    q.scales = ws + s_off;
+    q.colsum = colsum;
+    q.mode = mode;
+    GMLP_CUDA(launch_colq(q, s), "columnwise quantise launch");
+    return GMLP_OK;
+  };
+  auto wgrad = [&](size_t ac, size_t as, size_t bc, size_t bs, int64_t RA, int64_t RB, float* out) -> gmlp_status {
+    WgradArgs w{};
+    w.a_codes = ws + ac;
+    w.a_scales = ws + as;
+    w.b_codes = ws + bc;
+    w.b_scales = ws + bs;
+    w.RA = RA;
+    w.RB = RB;
+    w.T = L.T;
+    w.grp = gs;
+    w.out = out;
+    w.accumulate = accumulate;
+    GMLP_CUDA(launch_wgrad(w, s), "wgrad launch");
+    return GMLP_OK;
+  };
+  if (want2) {  // FC2: dW2_g = dy_g^T fc2_x_g over the group's tokens, dbias2 = token sums of dy
+    GMLP_TRY(colq(dy, K, K, COLQ_PLAIN, L.dy_c, L.dy_s, dbias2));
+    if (dW2) {
+      GMLP_TRY(colq(pre_act, N1, N, act == GMLP_ACT_SWIGLU ? COLQ_SWIGLU : COLQ_SRELU, L.f_c, L.f_s, nullptr));
+      GMLP_TRY(wgrad(L.dy_c, L.dy_s, L.f_c, L.f_s, K, N, dW2));
+    }
+  }
+  if (want1) {  // FC1: dW1_g = fc1_dy_g^T x_g, dbias1 = token sums of fc1_dy
+    GMLP_TRY(colq(fc1_dy, N1, N1, COLQ_PLAIN, L.g_c, L.g_s, dbias1));
+    if (dW1) {
+      GMLP_TRY(colq(x, K, K, COLQ_PLAIN, L.x_c, L.x_s, nullptr));
+      GMLP_TRY(wgrad(L.g_c, L.g_s, L.x_c, L.x_s, N1, K, dW1));
+    }
+  }
   return GMLP_OK;
 }
 
@@ -772,7 +914,8 @@ gmlp_status gmlp_check_device_status(gmlp_stream stream) {
   const int a = quant_read_clear_status();
   const int b = gemm_read_clear_status();
   const int c = peak_read_clear_status();
-  const int code = a ? a : (b ? b : c);
+  const int d = wgrad_read_clear_status();
+  const int code = a ? a : (b ? b : (c ? c : d));
   if (code < 0) return fail(GMLP_ERR_CUDA, "reading the device status word failed");
   if (code == GMLP_ERR_DEVICE_TIMEOUT) return fail(GMLP_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait");
   if (code == GMLP_ERR_DEVICE_BOUNDS)

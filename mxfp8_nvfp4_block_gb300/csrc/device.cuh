@@ -161,6 +161,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Bounded wait used only while shutting down after an abort (no new report).
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > 500000000ull) return;
+}
+
 // ----------------------------------------------------------------- TMA / bulk copies
 
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int32_t x, int32_t y,
@@ -284,6 +291,31 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)(swizzle & 7) << 61;
   return d;
+}
+
+// ----------------------------------------------------------------- global memory
+
+// 32-byte store (one full sector per lane); dst must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// 32 bytes from global memory through the read-only path without allocating
+// in L1 (p 32-byte aligned).
+__device__ __forceinline__ void ld_global_nc_v8(const void* p, uint32_t* w) {
+  asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
+}
+
+// ----------------------------------------------------------------- activations
+
+// silu(gate) * up in FP32 with the fast exponential and division (their
+// error is far below the bf16 rounding that follows).
+__device__ __forceinline__ float silu_times(float gate, float up) {
+  return __fdividef(gate, 1.0f + __expf(fminf(-gate, 80.0f))) * up;
 }
 
 }  // namespace gmlp

@@ -100,20 +100,6 @@ __device__ __forceinline__ Tile decode_tile(const int* off, const int* ip, int G
   return t;
 }
 
-// Bounded wait used only while shutting down after an abort (no new report).
-__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > 500000000ull) return;
-}
-
-// 32-byte store (one full sector per lane); dst must be 32-byte aligned.
-__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
-  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-               : "memory");
-}
-
 __device__ __forceinline__ float bf16_half(uint32_t w, int hi) {
   return bf16_bits_to_float(hi ? (w >> 16) : (w & 0xFFFFu));
 }
@@ -152,12 +138,6 @@ __device__ __forceinline__ int mx_block(const float* f, uint32_t* words) {
     words[i] = e4m3x2(__fmul_rn(f[4 * i], mul), __fmul_rn(f[4 * i + 1], mul)) |
                (e4m3x2(__fmul_rn(f[4 * i + 2], mul), __fmul_rn(f[4 * i + 3], mul)) << 16);
   return e;
-}
-
-// silu(gate) * up in FP32 with the fast exponential and division (their
-// error is far below the bf16 rounding that follows).
-__device__ __forceinline__ float silu_times(float gate, float up) {
-  return __fdividef(gate, 1.0f + __expf(fminf(-gate, 80.0f))) * up;
 }
 
 // ------------------------------------------------------------------ epilogues
@@ -208,14 +188,6 @@ __device__ __forceinline__ void dglu_pair(uint32_t dp, uint32_t gp, uint32_t up,
   }
   w0 = pack2_bf16_rn(v0[0], v0[1]);
   w1 = EPI == EPI_DGLU_SWIGLU ? pack2_bf16_rn(v1[0], v1[1]) : 0u;
-}
-
-// 32 bytes from global memory through the read-only path without allocating
-// in L1 (p 32-byte aligned).
-__device__ __forceinline__ void ld_global_nc_v8(const void* p, uint32_t* w) {
-  asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-               : "l"(p));
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
@@ -286,6 +258,11 @@ __device__ __forceinline__ float dglu_block(const GemmArgs& a, const uint32_t* d
 #pragma unroll
   for (int o = 0; o < kOuts; ++o) {
     const int64_t col = (o == 0 ? 0 : N) + n0;
+    if (a.out_bf16) {  // fc1_dy in bf16 as well (the weight gradient's operand)
+      uint16_t* brow = a.out_bf16 + grow * N1 + col;
+      st_global_v8(brow, o == 0 ? ow0 : ow1);
+      st_global_v8(brow + 16, (o == 0 ? ow0 : ow1) + 8);
+    }
     const int e = mx_block_packed(o == 0 ? ow0 : ow1, crow + col);
     const int kidx = (int)(col / 32);
     a.out_scales[sbase + (int64_t)(kidx >> 2) * 512 + (kidx & 3)] = (uint8_t)(e + 127);
@@ -856,34 +833,6 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 2D uint8 tensor map over [rows][row_bytes] with a box of box_rows x box_bytes.
-bool make_tmap(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows, int box_bytes, int box_rows,
-               CUtensorMapSwizzle swz) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int FMT, int EPI, int PAIR, bool X4 = false, bool XT = false>
 cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
   using C = Cfg<FMT, PAIR, X4>;
@@ -946,6 +895,33 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool make_tmap(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows, int box_bytes, int box_rows,
+               CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 int gemm_read_clear_status() { return read_clear_status(); }
 

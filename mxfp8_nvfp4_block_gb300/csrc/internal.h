@@ -111,7 +111,49 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 
+// ---- weight gradients (wgrad.cu) ----
+
+// Columnwise MXFP8 of a token-sorted bf16 matrix (or of fc2_x rebuilt from the
+// saved activation input): per group, 128-token chunks become 128-column
+// slabs of a [C][T] code matrix (1x32 blocks along the tokens, zero past the
+// group's end), scales GEMM_TILED for a [C]-row operand with T/32 per row.
+enum ColqMode { COLQ_PLAIN = 0, COLQ_SWIGLU = 1, COLQ_SRELU = 2 };
+struct ColqArgs {
+  const uint16_t* src;  // [M][ld] bf16 (COLQ_SWIGLU / COLQ_SRELU: the activation input h)
+  int64_t ld;           // row stride of src (elements)
+  int64_t C;            // output columns (multiple of 128)
+  int64_t up_off;       // COLQ_SWIGLU: column of the first up value (N)
+  const float* probs;   // COLQ_SWIGLU / COLQ_SRELU: [M] routing probabilities, null = 1
+  GroupSrc grp;
+  int64_t T;            // columns of `codes` = 128 x (chunk capacity), multiple of 128
+  uint8_t* codes;       // [C][T]
+  uint8_t* scales;      // (C / 128) x (T / 128) blocks of 512 bytes
+  float* colsum;        // [G][C] per-group column sums (accumulated), or null
+  int mode;             // ColqMode
+};
+cudaError_t launch_colq(const ColqArgs& a, cudaStream_t s);
+
+// Per group g: out_g [RA][RB] (FP32) = A_g B_g^T over the group's padded
+// tokens, A [RA][T] and B [RB][T] columnwise MXFP8 operands from launch_colq.
+struct WgradArgs {
+  const uint8_t* a_codes;
+  const uint8_t* a_scales;
+  const uint8_t* b_codes;
+  const uint8_t* b_scales;
+  int64_t RA, RB;       // RA % 128 == 0, RB % 256 == 0
+  int64_t T;            // as ColqArgs::T
+  GroupSrc grp;
+  float* out;           // [G][RA][RB], 32-byte aligned
+  int accumulate;       // 1: out += result; 0: out = result
+};
+cudaError_t launch_wgrad(const WgradArgs& a, cudaStream_t s);
+
 int num_sms();
+
+// 2D uint8 tensor map over [rows][row_bytes] with a box of box_rows x
+// box_bytes (gemm.cu); false if the driver entry point or the encode fails.
+bool make_tmap(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows, int box_bytes, int box_rows,
+               CUtensorMapSwizzle swz);
 
 cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_mma_peak(int format, int scale_copy, int64_t iters, int ctas, cudaStream_t s);

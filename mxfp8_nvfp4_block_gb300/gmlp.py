@@ -26,7 +26,8 @@ EXPORTS = ["gmlp_tiled_scales_bytes", "gmlp_group_hadamard_amax", "gmlp_group_qu
            "gmlp_group_quantize", "gmlp_prepare_weights", "gmlp_forward_workspace_size", "gmlp_forward",
            "gmlp_check_device_status", "gmlp_last_error", "gmlp_version", "gmlp_forward_noalloc",
            "gmlp_selftest_bounded_wait", "gmlp_mma_peak", "gmlp_replicate_weight_scales",
-           "gmlp_prepare_weights_discrete", "gmlp_backward_workspace_size", "gmlp_backward_dgrad"]
+           "gmlp_prepare_weights_discrete", "gmlp_backward_workspace_size", "gmlp_backward_dgrad",
+           "gmlp_backward_wgrad_workspace_size", "gmlp_backward_wgrad", "gmlp_colwise_tokens"]
 
 
 class Recipe(ctypes.Structure):
@@ -90,7 +91,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gmlp_backward_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
         "gmlp_backward_dgrad": (_i32, [_vp, _i64, _i64, _i64, _vp, _i32, ctypes.POINTER(QWeightC),
                                        ctypes.POINTER(QWeightC), _vp, _vp, _i32, ctypes.POINTER(Recipe), _vp, _vp,
-                                       _vp, _vp, _vp, ctypes.c_size_t, _vp, _i32, _vp]),
+                                       _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _i32, _vp]),
+        "gmlp_backward_wgrad_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
+        "gmlp_colwise_tokens": (_i64, [_i64, _i32]),
+        "gmlp_backward_wgrad": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp,
+                                       _vp, _i32, _vp, ctypes.c_size_t, _vp]),
         "gmlp_last_error": (ctypes.c_char_p, []),
         "gmlp_version": (ctypes.c_char_p, []),
     }
@@ -160,10 +165,18 @@ def alloc_quant_outputs(M: int, K: int, G: int, fmt: int, layout: int, rowwise: 
         ns = K // blk
         sbytes = tiled_scales_bytes(M, G, ns) if layout == GEMM_TILED else M * ns
         out["row"] = (_u8(M * K // cdiv, device), _u8(sbytes, device))
-    if columnwise:
+    if columnwise and fmt == MXFP8:
+        T = colwise_tokens(M, G)   # the weight-gradient operand layout: [K][T] codes
+        out["col"] = (_u8(K * T, device), _u8(K * T // 32, device))
+    elif columnwise:
         mp = sum((int(m) + 15) // 16 * 16 for m in splits_host)
         out["col"] = (_u8(K * mp // 2, device), _u8(K * mp // 16, device))
     return out
+
+
+def colwise_tokens(M: int, G: int) -> int:
+    """T of the columnwise MXFP8 layout (see gmlp_colwise_tokens)."""
+    return int(load().gmlp_colwise_tokens(M, G))
 
 
 def group_quantize_with_amax(x, splits, rec: Recipe, amax_pre=None, amax_post=None, *, rowwise=True,
@@ -345,10 +358,12 @@ def _event_handles(events):
 
 
 def backward_dgrad(dy, splits, W2t: "QWeight", W1t: "QWeight", pre_act, probs, act: int, rec: Recipe, *,
-                   dx=None, want_dprob: bool = True, fc1_dy: dict | None = None, workspace=None, events=None,
-                   stream=None):
+                   dx=None, want_dprob: bool = True, fc1_dy: dict | None = None, fc1_dy_bf16=None, workspace=None,
+                   events=None, stream=None):
     """dx (and dprob) of the fused grouped MLP (see gmlp_backward_dgrad).
-    events: up to 3 torch.cuda.Event recorded after each kernel."""
+    fc1_dy: optional {"codes", "scales"} outputs; fc1_dy_bf16: optional [M, N1]
+    bf16 output (the weight gradient's operand); events: up to 3
+    torch.cuda.Event recorded after each kernel."""
     dy = _bits(dy)
     M, K = dy.shape
     N = W2t.rows
@@ -363,9 +378,37 @@ def backward_dgrad(dy, splits, W2t: "QWeight", W1t: "QWeight", pre_act, probs, a
     ev_arr = _event_handles(events) if events else None
     _check(load().gmlp_backward_dgrad(_p(dy), M, K, N, _p(splits), G, ctypes.byref(W2t.c()), ctypes.byref(W1t.c()),
                                       _p(pre_act), _p(probs), act, ctypes.byref(rec), _p(dx), _p(dprob),
-                                      _p(fc1_dy.get("codes")), _p(fc1_dy.get("scales")), _p(workspace),
+                                      _p(fc1_dy.get("codes")), _p(fc1_dy.get("scales")), _p(fc1_dy_bf16),
+                                      _p(workspace),
                                       workspace.numel(), ev_arr, len(events or ()), _stream(stream)))
     return dx, dprob
+
+
+def backward_wgrad(x, dy, pre_act, probs, fc1_dy, splits, act: int, *, dW1=None, dW2=None, dbias1=None,
+                   dbias2=None, want=("dW1", "dW2", "dbias1", "dbias2"), accumulate: bool = False, workspace=None,
+                   stream=None) -> dict:
+    """Weight and bias gradients of the fused grouped MLP (see
+    gmlp_backward_wgrad); outputs FP32, allocated when not given for the names
+    in `want`.  Returns {"dW1", "dW2", "dbias1", "dbias2"} (None where skipped)."""
+    x, dy, fc1_dy = _bits(x), _bits(dy), _bits(fc1_dy)
+    M, K = dy.shape
+    N1 = fc1_dy.shape[1]
+    N = N1 // 2 if act == SWIGLU else N1
+    G = splits.numel()
+    dev = dy.device
+    shapes = {"dW1": (G, N1, K), "dW2": (G, K, N), "dbias1": (G, N1), "dbias2": (G, K)}
+    out = {"dW1": dW1, "dW2": dW2, "dbias1": dbias1, "dbias2": dbias2}
+    for k in shapes:
+        if out[k] is None and k in want:
+            out[k] = torch.empty(shapes[k], dtype=torch.float32, device=dev)
+    need = load().gmlp_backward_wgrad_workspace_size(M, K, N, G, act)
+    if workspace is None:
+        workspace = _u8(need, dev)
+    _check(load().gmlp_backward_wgrad(_p(x), _p(dy), _p(_bits(pre_act) if pre_act is not None else None), _p(probs),
+                                      _p(fc1_dy), M, K, N, _p(splits), G, act, _p(out["dW1"]), _p(out["dW2"]),
+                                      _p(out["dbias1"]), _p(out["dbias2"]), int(bool(accumulate)), _p(workspace),
+                                      workspace.numel(), _stream(stream)))
+    return out
 
 
 def selftest_bounded_wait(limit_ns: int, stream=None) -> None:

@@ -76,7 +76,9 @@ def forward(x, splits, W1, W2, probs, act: int, fmt: int, *, rows=None, qw1=None
       1. xq = rowwise quantisation of x (MXFP8 blocks are row-local; NVFP4 takes
          S_x,g from the group's amax).
       2. acc = dq(xq_g) @ dq(W1q_g)^T in float64 (NVFP4's 1/S factors are part of dq).
-      3. h = bf16(acc)  ("rounds the accumulator through C dtype before the activation").
+      3. h = bf16(acc)  ("rounds the accumulator through C dtype before the activation");
+         returned as ``h`` [M, N1] in logical column order, the activation input
+         the backward reads (PR #2769 sequence diagram: c_tensor, swiglu_in).
       4. a = act(h) in float64; f = bf16(a * prob)  (fc2_x).
       5. fc2_x quantisation: MXFP8 rowwise; NVFP4 rowwise with S_f,g from the
          group's amax of f; the post-RHT amax of f (16-row column chunks, sign
@@ -108,6 +110,7 @@ def forward(x, splits, W1, W2, probs, act: int, fmt: int, *, rows=None, qw1=None
     out = dict(
         y=np.zeros((M, K), dtype=np.uint16),
         fc2x=np.zeros((M, N), dtype=np.uint16),
+        h=np.zeros((M, W1.shape[1]), dtype=np.uint16),
         fc2x_codes=np.zeros((M, N // cdiv), dtype=np.uint8),
         fc2x_scales=np.zeros((M, N // blk), dtype=np.uint8),
         rows=sel_all,
@@ -138,7 +141,8 @@ def forward(x, splits, W1, W2, probs, act: int, fmt: int, *, rows=None, qw1=None
         acc = xd @ dequant_weight(qw1, g, fmt).T
         if b1 is not None:
             acc = acc + np.asarray(b1, np.float64)[g][None, :]
-        h = bf16_to_f64(f64_to_bf16(acc))
+        out["h"][sel] = f64_to_bf16(acc)
+        h = bf16_to_f64(out["h"][sel])
         a = activation(h, act, tanh_clamp_scale)
         f = f64_to_bf16(a * probs[sel].astype(np.float64)[:, None])
         out["fc2x"][sel] = f

@@ -72,9 +72,12 @@ def test_quantize_argument_checks(lib):
     # misaligned x
     assert L.gmlp_group_quantize(FAKE + 2, 64, 128, FAKE, 2, ctypes.byref(r), ctypes.byref(qt), None, None, None,
                                  None) == g.ERR_INVALID_ARG
-    # MXFP8 has no columnwise output here
-    assert L.gmlp_group_quantize(FAKE, 64, 128, FAKE, 2, ctypes.byref(r), ctypes.byref(qt), ctypes.byref(qt),
-                                 None, None, None) == g.ERR_UNSUPPORTED_RECIPE
+    # MXFP8 columnwise codes / scales are written in 32-byte vectors
+    q16 = g.QTensor(FAKE + 16, FAKE)
+    assert L.gmlp_group_quantize(FAKE, 64, 128, FAKE, 2, ctypes.byref(r), None, ctypes.byref(q16),
+                                 None, None, None) == g.ERR_INVALID_ARG
+    assert L.gmlp_colwise_tokens(300, 3) == 128 * (3 + 3)
+    assert L.gmlp_colwise_tokens(0, 1) == 128 and L.gmlp_colwise_tokens(-1, 1) == 0
     # unknown format
     bad = g.Recipe(7, 0, 0, 1)
     assert L.gmlp_group_quantize(FAKE, 64, 128, FAKE, 2, ctypes.byref(bad), ctypes.byref(qt), None, None, None,
@@ -228,9 +231,9 @@ def test_backward_dgrad_checks(lib):
     w1t = g.QWeightC(FAKE, FAKE, None, 512, 256, 4, g.MXFP8, 0, 0)   # [K x N1] (SReLU)
     need = L.gmlp_backward_workspace_size(512, 512, 256, 4, g.SRELU)
 
-    def call(K=512, N=256, act=g.SRELU, rec=r, W2t=w2t, W1t=w1t, pre=FAKE, ev=None, n_ev=0, dx=FAKE):
+    def call(K=512, N=256, act=g.SRELU, rec=r, W2t=w2t, W1t=w1t, pre=FAKE, ev=None, n_ev=0, dx=FAKE, bf=None):
         return L.gmlp_backward_dgrad(FAKE, 512, K, N, FAKE, 4, ctypes.byref(W2t), ctypes.byref(W1t), pre, None, act,
-                                     ctypes.byref(rec), dx, None, None, None, FAKE, need, ev, n_ev, None)
+                                     ctypes.byref(rec), dx, None, None, None, bf, FAKE, need, ev, n_ev, None)
 
     assert call(rec=g.recipe(g.NVFP4)) == g.ERR_UNSUPPORTED_RECIPE
     assert call(act=g.TANH_SRELU) == g.ERR_INVALID_ARG
@@ -239,5 +242,32 @@ def test_backward_dgrad_checks(lib):
     assert call(pre=None) == g.ERR_INVALID_ARG
     assert call(pre=FAKE + 16) == g.ERR_INVALID_ARG      # read in 32-byte vectors
     assert call(dx=FAKE + 16) == g.ERR_INVALID_ARG       # stored in 32-byte vectors
+    assert call(bf=FAKE + 16) == g.ERR_INVALID_ARG       # bf16 fc1_dy too
     assert call(n_ev=4, ev=FAKE) == g.ERR_INVALID_ARG    # at most 3 stage events
     assert call(n_ev=1) == g.ERR_INVALID_ARG             # events NULL
+
+
+def test_backward_wgrad_checks(lib):
+    L, g = lib
+    M, K, N, G = 512, 512, 256, 4
+    need = L.gmlp_backward_wgrad_workspace_size(M, K, N, G, g.SWIGLU)
+    T = L.gmlp_colwise_tokens(M, G)
+    assert need >= (2 * K + N + 2 * N) * T
+
+    def call(K=K, N=N, act=g.SWIGLU, x=FAKE, dy=FAKE, pre=FAKE, f=FAKE, dW1=FAKE, dW2=FAKE, db1=None, db2=None,
+             acc=0, ws=FAKE, wsb=need):
+        return L.gmlp_backward_wgrad(x, dy, pre, None, f, M, K, N, FAKE, G, act, dW1, dW2, db1, db2, acc, ws, wsb,
+                                     None)
+
+    assert call(act=g.TANH_SRELU) == g.ERR_INVALID_ARG
+    assert call(K=384) == g.ERR_INVALID_DIMS
+    assert call(N=128) == g.ERR_INVALID_DIMS
+    assert call(acc=2) == g.ERR_INVALID_ARG
+    assert call(pre=None) == g.ERR_INVALID_ARG            # dW2 rebuilds fc2_x from pre_act
+    assert call(x=None) == g.ERR_INVALID_ARG              # dW1 needs x
+    assert call(f=None) == g.ERR_INVALID_ARG
+    assert call(dW1=FAKE + 16) == g.ERR_INVALID_ARG       # 32-byte vector stores
+    assert call(pre=FAKE + 16) == g.ERR_INVALID_ARG
+    assert call(db1=FAKE + 2) == g.ERR_INVALID_ARG
+    assert call(wsb=need - 1) == g.ERR_WORKSPACE
+    assert call(ws=None) == g.ERR_WORKSPACE

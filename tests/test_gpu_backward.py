@@ -1,6 +1,7 @@
 """Parity of the data-gradient backward (CUDA path, through the C ABI) with the
-oracle: fc2 dGLU (dSwiGLU / dSReLU x prob, dprob, fc1_dy in MXFP8) and the fc1
-dgrad, on the forward's own saved activation input."""
+oracle: fc2 dGLU (dSwiGLU / dSReLU x prob, dprob, fc1_dy in MXFP8 and bf16)
+and the fc1 dgrad, on seeded inputs shared by both sides; and the forward's
+saved activation input against the oracle forward's."""
 import numpy as np
 import pytest
 import torch
@@ -33,10 +34,35 @@ def run_backward(gm, dy, splits, W1, W2, h, probs, act):
     w2t = gm.prepare_transposed_weights(W2.cuda())
     w1t = gm.prepare_transposed_weights(W1.cuda())
     fc1 = {"codes": torch.zeros(M * N1 + 16, dtype=torch.uint8, device="cuda"),
-           "scales": torch.zeros(gm.tiled_scales_bytes(M, G, N1 // 32) + 16, dtype=torch.uint8, device="cuda")}
-    dx, dprob = gm.backward_dgrad(dy.cuda(), splits.cuda(), w2t, w1t, h, probs, act, gm.recipe(gm.MXFP8), fc1_dy=fc1)
+           "scales": torch.zeros(gm.tiled_scales_bytes(M, G, N1 // 32) + 16, dtype=torch.uint8, device="cuda"),
+           "bf16": torch.full((M, N1), float("nan"), dtype=torch.bfloat16, device="cuda")}
+    dx, dprob = gm.backward_dgrad(dy.cuda(), splits.cuda(), w2t, w1t, h, probs, act, gm.recipe(gm.MXFP8),
+                                  fc1_dy={"codes": fc1["codes"], "scales": fc1["scales"]}, fc1_dy_bf16=fc1["bf16"])
     gm.check_device_status()
     return dx, dprob, fc1
+
+
+@pytest.mark.parametrize("act", [0, 1], ids=["swiglu", "srelu"])
+def test_forward_saves_activation_input(orc, gm, act):
+    """gmlp_fwd_aux.fc1_pre_act = bf16(fc1 accumulator) in logical column order
+    (SwiGLU: gate then up), against the oracle forward's h."""
+    rng = np.random.default_rng(41 + act)
+    splits_l, K, N = [130, 0, 257, 5, 1, 128], 512, 256
+    G, M = len(splits_l), sum(splits_l)
+    n1 = 2 * N if act == 0 else N
+    splits = torch.tensor(splits_l, dtype=torch.int64)
+    x = bf16_cpu(rng.standard_normal((M, K)))
+    W1 = bf16_cpu(rng.standard_normal((G, n1, K)) / np.sqrt(K))
+    W2 = bf16_cpu(rng.standard_normal((G, K, N)) / np.sqrt(N))
+    probs = torch.from_numpy(rng.uniform(0.1, 1, M).astype(np.float32))
+    _, h = forward_with_h(gm, x, splits, W1, W2, probs.cuda(), act)
+    ref = orc.forward(bits(x), np.array(splits_l), bits(W1), bits(W2), probs.numpy(), act, orc.MXFP8)
+    hb = np_bits(h)
+    match = float(np.mean(hb == ref["h"]))
+    err = frob(orc.bf16_to_f64(hb), orc.bf16_to_f64(ref["h"]))
+    print(f"fc1_pre_act bf16 match {match:.6f}, relative error {err:.2e}")
+    # FP32 tensor-core sums against float64: a bf16 rounding may flip by one step
+    assert match >= 0.99 and err <= 1e-2
 
 
 @pytest.mark.parametrize("act", [0, 1], ids=["swiglu", "srelu"])
@@ -46,16 +72,18 @@ def test_backward_dgrad_parity(orc, gm, act):
     G, M = len(splits_l), sum(splits_l)
     n1 = 2 * N if act == 0 else N
     splits = torch.tensor(splits_l, dtype=torch.int64)
-    x = bf16_cpu(rng.standard_normal((M, K)))
     W1 = bf16_cpu(rng.standard_normal((G, n1, K)) / np.sqrt(K))
     W2 = bf16_cpu(rng.standard_normal((G, K, N)) / np.sqrt(N))
     probs = torch.from_numpy(rng.uniform(0.1, 1, M).astype(np.float32)).cuda()
-    _, h = forward_with_h(gm, x, splits, W1, W2, probs, act)
-    assert not torch.isnan(h.float()).any()
+    h = bf16_cpu(1.5 * rng.standard_normal((M, n1))).cuda()   # the saved activation input (pre-activations)
     dy = bf16_cpu(rng.standard_normal((M, K)))
     dx, dprob, fc1 = run_backward(gm, dy, splits, W1, W2, h, probs, act)
-    hb = h.cpu().view(torch.int16).numpy().view(np.uint16)
+    hb = np_bits(h)
     ref = orc.backward_dgrad(bits(dy), np.array(splits_l), bits(W1), bits(W2), hb, probs.cpu().numpy(), act)
+    fb = np_bits(fc1["bf16"])
+    bmatch = float(np.mean(fb == ref["fc1_dy"]))
+    print(f"fc1_dy bf16 match {bmatch:.6f}")
+    assert bmatch >= 0.99 and frob(orc.bf16_to_f64(fb), orc.bf16_to_f64(ref["fc1_dy"])) <= 1e-2
     frac, steps = code_match_report(0, np_u8(fc1["codes"], M * n1).reshape(M, n1), ref["fc1_dy_codes"],
                                     orc.tiled_to_compact(np_u8(fc1["scales"]), np.array(splits_l), n1 // 32),
                                     ref["fc1_dy_scales"])
