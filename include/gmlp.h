@@ -65,12 +65,14 @@
  *     a multiple of 4.
  * Columnwise NVFP4 output (per group, groups concatenated in order): codes
  *   [cols][Mpad_g/2] and scales [cols][Mpad_g/16], Mpad_g = 16*ceil(m_g/16).
- * Columnwise MXFP8 output (the weight-gradient GEMM operand): one code matrix
- *   [cols][T], T = gmlp_colwise_tokens(M, G) = 128 (ceil(M/128) + G); group g's
- *   tokens, cut into 128-token chunks from its first token, fill columns
- *   128 c_g .. 128 (c_g + ceil(m_g/128)) - 1 with c_g = sum_{h<g} ceil(m_h/128)
- *   (zero codes past the group's end; columns past the last chunk are not
- *   written); one E8M0 scale per 32 tokens, in the GEMM_TILED form of a
+ * Columnwise MXFP8 output (the weight-gradient GEMM operand): chunk-major
+ *   codes [T/128][cols][128], T = gmlp_colwise_tokens(M, G) = 128 (ceil(M/128)
+ *   + G); group g's tokens, cut into 128-token chunks from its first token,
+ *   are chunks c_g .. c_g + ceil(m_g/128) - 1 with c_g = sum_{h<g}
+ *   ceil(m_h/128); chunk c holds, for every column i, the 128 codes of its
+ *   tokens at byte (c * cols + i) * 128 (zero codes past the group's end;
+ *   chunks past the last are not written); one E8M0 scale per 32 tokens, in
+ *   the GEMM_TILED form of a
  *   [cols]-row operand with T/32 scales per row: the 512-byte block of column
  *   tile r (128 columns) and chunk c at byte (r * (T/128) + c) * 512, the scale
  *   of column 128 r + i, block j of the chunk at (i % 32) * 16 + (i / 32) * 4 + j.

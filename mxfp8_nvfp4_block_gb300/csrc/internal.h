@@ -114,9 +114,10 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s);
 // ---- weight gradients (wgrad.cu) ----
 
 // Columnwise MXFP8 of a token-sorted bf16 matrix (or of fc2_x rebuilt from the
-// saved activation input): per group, 128-token chunks become 128-column
-// slabs of a [C][T] code matrix (1x32 blocks along the tokens, zero past the
-// group's end), scales GEMM_TILED for a [C]-row operand with T/32 per row.
+// saved activation input): per group, 128-token chunks become [C][128] slabs
+// of a chunk-major code array [T/128][C][128] (1x32 blocks along the tokens,
+// zero past the group's end), scales GEMM_TILED for a [C]-row operand with
+// T/32 per row.
 enum ColqMode { COLQ_PLAIN = 0, COLQ_SWIGLU = 1, COLQ_SRELU = 2 };
 struct ColqArgs {
   const uint16_t* src;  // [M][ld] bf16 (COLQ_SWIGLU / COLQ_SRELU: the activation input h)
@@ -125,8 +126,8 @@ struct ColqArgs {
   int64_t up_off;       // COLQ_SWIGLU: column of the first up value (N)
   const float* probs;   // COLQ_SWIGLU / COLQ_SRELU: [M] routing probabilities, null = 1
   GroupSrc grp;
-  int64_t T;            // columns of `codes` = 128 x (chunk capacity), multiple of 128
-  uint8_t* codes;       // [C][T]
+  int64_t T;            // 128 x (chunk capacity)
+  uint8_t* codes;       // [T / 128][C][128]
   uint8_t* scales;      // (C / 128) x (T / 128) blocks of 512 bytes
   float* colsum;        // [G][C] per-group column sums (accumulated), or null
   int mode;             // ColqMode

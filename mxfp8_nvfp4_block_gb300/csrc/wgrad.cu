@@ -10,18 +10,21 @@
 //
 // Columnwise operand (colq_kernel): group g's m_g tokens are cut into
 // 128-token chunks counted from its first token; chunk w of all groups
-// (groups in order) becomes columns 128w .. 128w + 127 of a [C][T] code
-// matrix, i.e. the group's transpose zero-padded to a multiple of 128 tokens,
-// with one E8M0 scale per 32 tokens.  The scales sit in the GEMM_TILED layout
-// of a [C]-row operand with T/32 scales per row, so chunk w of column tile r
-// is the 512-byte block r * (T / 128) + w, exactly what one GEMM stage loads.
+// (groups in order) becomes the slab [C][128] at w * C * 128 of a chunk-major
+// code array [T/128][C][128] (the group's transpose zero-padded to a multiple
+// of 128 tokens), with one E8M0 scale per 32 tokens.  A GEMM stage's operand
+// tile is then one contiguous block (128 or 256 rows x 128 bytes), where a
+// token-contiguous [C][T] matrix would put its rows T bytes apart and halve
+// the TMA unit's row rate.  The scales sit in the GEMM_TILED layout of a
+// [C]-row operand with T/32 scales per row, so chunk w of column tile r is the
+// 512-byte block r * (T / 128) + w, exactly what one GEMM stage loads.
 //
 // Grouped GEMM (wgrad_kernel; one CTA per SM, 576 threads, as gemm.cu):
 // tile (g, 128-row tile of A, 256-row tile of B) accumulates over the group's
 // chunks (one 128-token stage each) into 256 TMEM columns; the epilogue writes
 // FP32 (or adds into it).  A group with no tokens gets zeros without an MMA.
-// Tiles are ordered by their groups' chunk counts, longest first, and handed
-// round-robin to the persistent CTAs, so the ragged groups balance.
+// Tiles are ordered by their groups' chunk counts, longest first, and dealt to
+// the persistent CTAs in alternating directions, so the ragged groups balance.
 #include <cudaTypedefs.h>
 
 #include "device.cuh"
@@ -33,6 +36,15 @@ namespace {
 // ------------------------------------------------------------------ columnwise MXFP8
 
 constexpr int kColThreads = 128;  // one thread per output column of a 128-column tile
+
+// 16-byte global -> shared copy; the bytes past src_bytes (0 or 16) are zeros
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(kColThreads) colq_kernel(const ColqArgs a) {
@@ -95,49 +107,66 @@ __global__ void __launch_bounds__(kColThreads) colq_kernel(const ColqArgs a) {
   const int64_t t0 = (int64_t)off[g] + 128 * local;
   const int64_t c0 = (int64_t)blockIdx.y * 128;
 
-  // 1. the chunk's 128 tokens x 128 columns as bf16 (zero past the group's end)
-  for (int i = tid; i < 128 * 16; i += kColThreads) {
-    const int t = i >> 4, v = i & 15;
-    uint4 o = make_uint4(0, 0, 0, 0);
-    if (t < valid) {
-      const uint16_t* row = a.src + (t0 + t) * a.ld + c0 + 8 * v;
-      if (MODE == COLQ_PLAIN) {
-        o = __ldg(reinterpret_cast<const uint4*>(row));
-      } else {
-        // fc2_x = bf16(act(h) * prob), the fc1 epilogue's own arithmetic
-        const float p = a.probs ? __ldg(a.probs + t0 + t) : 1.0f;
-        const uint4 h8 = __ldg(reinterpret_cast<const uint4*>(row));
-        const uint32_t hw[4] = {h8.x, h8.y, h8.z, h8.w};
-        uint32_t ow[4];
-        if (MODE == COLQ_SWIGLU) {
-          const uint4 u8 = __ldg(reinterpret_cast<const uint4*>(row + a.up_off));
-          const uint32_t uw[4] = {u8.x, u8.y, u8.z, u8.w};
+  // 1. the chunk's 128 tokens x 128 columns as bf16 (zero past the group's end);
+  // thread tid moves 16-byte vector vc = tid % 16 of rows tid / 16 + 8 i
+  const int vc = tid & 15, r0 = tid >> 4;
+  if (MODE == COLQ_PLAIN) {
+    // all 16 copies in flight at once; rows past the group's end are zero-filled
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float f0 = round_bf16(silu_times(bf16_bits_to_float(hw[k] & 0xFFFFu),
-                                                   bf16_bits_to_float(uw[k] & 0xFFFFu)) * p);
-            const float f1 = round_bf16(silu_times(bf16_bits_to_float(hw[k] >> 16), bf16_bits_to_float(uw[k] >> 16)) *
-                                        p);
-            ow[k] = bf16_bits(f0) | (bf16_bits(f1) << 16);
-          }
-        } else {
+    for (int i = 0; i < 16; ++i) {
+      const int t = r0 + 8 * i;
+      const uint16_t* src = a.src + (t0 + (t < valid ? t : 0)) * a.ld + c0 + 8 * vc;
+      cp_async16(smem_u32(&tile[t][8 * vc]), src, t < valid ? 16u : 0u);
+    }
+    cp_async_wait_all();
+  } else {
+#pragma unroll 1
+    for (int i0 = 0; i0 < 16; i0 += 4) {
+      uint4 hv[4], uv[4];
+      float pv[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float h0 = fmaxf(bf16_bits_to_float(hw[k] & 0xFFFFu), 0.0f);
-            const float h1 = fmaxf(bf16_bits_to_float(hw[k] >> 16), 0.0f);
-            ow[k] = bf16_bits(round_bf16(h0 * h0 * p)) | (bf16_bits(round_bf16(h1 * h1 * p)) << 16);
-          }
+      for (int k = 0; k < 4; ++k) {
+        const int t = r0 + 8 * (i0 + k);
+        hv[k] = uv[k] = make_uint4(0, 0, 0, 0);
+        pv[k] = 0.0f;
+        if (t < valid) {
+          const uint16_t* row = a.src + (t0 + t) * a.ld + c0 + 8 * vc;
+          hv[k] = __ldg(reinterpret_cast<const uint4*>(row));
+          if (MODE == COLQ_SWIGLU) uv[k] = __ldg(reinterpret_cast<const uint4*>(row + a.up_off));
+          pv[k] = a.probs ? __ldg(a.probs + t0 + t) : 1.0f;
         }
-        o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        // fc2_x = bf16(act(h) * prob), the fc1 epilogue's own arithmetic (an
+        // invalid row has h = 0, prob = 0: zero)
+        const uint32_t hw[4] = {hv[k].x, hv[k].y, hv[k].z, hv[k].w};
+        const uint32_t uw[4] = {uv[k].x, uv[k].y, uv[k].z, uv[k].w};
+        const float p = pv[k];
+        uint32_t ow[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float f0, f1;
+          if (MODE == COLQ_SWIGLU) {
+            f0 = round_bf16(silu_times(bf16_bits_to_float(hw[e] & 0xFFFFu), bf16_bits_to_float(uw[e] & 0xFFFFu)) * p);
+            f1 = round_bf16(silu_times(bf16_bits_to_float(hw[e] >> 16), bf16_bits_to_float(uw[e] >> 16)) * p);
+          } else {
+            const float h0 = fmaxf(bf16_bits_to_float(hw[e] & 0xFFFFu), 0.0f);
+            const float h1 = fmaxf(bf16_bits_to_float(hw[e] >> 16), 0.0f);
+            f0 = round_bf16(h0 * h0 * p);
+            f1 = round_bf16(h1 * h1 * p);
+          }
+          ow[e] = bf16_bits(f0) | (bf16_bits(f1) << 16);
+        }
+        *reinterpret_cast<uint4*>(&tile[r0 + 8 * (i0 + k)][8 * vc]) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
       }
     }
-    *reinterpret_cast<uint4*>(&tile[t][8 * v]) = o;
   }
   __syncthreads();
 
   // 2. thread c: column c0 + c, four 32-token blocks -> 4 x 32 codes, 4 scales
   const int c = tid;
-  uint8_t* crow = a.codes + (c0 + c) * a.T + (int64_t)w * 128;
+  uint8_t* crow = a.codes + ((int64_t)w * a.C + c0 + c) * 128;
   uint32_t sc = 0;
   float csum = 0.0f;
 #pragma unroll 1
@@ -284,6 +313,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
   __syncthreads();
   const uint32_t tbase = *tslot;
   const int total = *bad ? 0 : G * TPG;
+  // round i of the tile list goes left to right when i is even and right to
+  // left when odd, so a CTA that drew a long tile draws a short one next
+  auto snake_tile = [&](int i) {
+    return i * (int)gridDim.x + ((i & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
+  };
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
@@ -291,7 +325,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const uint64_t pol_b = policy_evict_last();
     int stage = 0;
     uint32_t phase = 0, armed = 0, armed_parity = 0;
-    for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+    for (int i = 0; i * (int)gridDim.x < total && !*abort_flag; ++i) {
+      const int w = snake_tile(i);
+      if (w >= total) continue;
       const int g = ord[w / TPG], local = w % TPG;
       const int mt = local % MT, nt = local / MT;
       for (int kb = 0; kb < nkb[g]; ++kb) {
@@ -300,8 +336,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
         armed |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         const int64_t chunk = (int64_t)cb[g] + kb;
-        tma_load_2d(sA + stage * kWATile, &tmA, (int32_t)(chunk * 128), mt * 128, &full[stage], pol_a);
-        tma_load_2d(sB + stage * kWBTile, &tmB, (int32_t)(chunk * 128), nt * 256, &full[stage], pol_b);
+        tma_load_2d(sA + stage * kWATile, &tmA, 0, (int32_t)(chunk * a.RA + mt * 128), &full[stage], pol_a);
+        tma_load_2d(sB + stage * kWBTile, &tmB, 0, (int32_t)(chunk * a.RB + nt * 256), &full[stage], pol_b);
         bulk_load(sSFA + stage * kWSfA, a.a_scales + ((int64_t)mt * KBT + chunk) * 512, 512, &full[stage]);
         bulk_load(sSFB + stage * kWSfB, a.b_scales + ((int64_t)(2 * nt) * KBT + chunk) * 512, 512, &full[stage]);
         bulk_load(sSFB + stage * kWSfB + 512, a.b_scales + ((int64_t)(2 * nt + 1) * KBT + chunk) * 512, 512,
@@ -320,7 +356,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
     const uint32_t sf_base = tbase + kWAccCols;
-    for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+    for (int i = 0; i * (int)gridDim.x < total && !*abort_flag; ++i) {
+      const int w = snake_tile(i);
+      if (w >= total) continue;
       const int g = ord[w / TPG];
       if (!mbar_wait(tempty, acc_phase ^ 1, abort_flag)) break;
       tc_fence_after();
@@ -365,7 +403,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const int q = warp & 3;
     const int slice = (warp - 2) >> 2;
     uint32_t acc_phase = 0;
-    for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+    for (int i = 0; i * (int)gridDim.x < total && !*abort_flag; ++i) {
+      const int w = snake_tile(i);
+      if (w >= total) continue;
       const int g = ord[w / TPG], local = w % TPG;
       const int mt = local % MT, nt = local / MT;
       if (!mbar_wait(tfull, acc_phase, abort_flag)) break;
@@ -386,20 +426,48 @@ __global__ void __launch_bounds__(kWThreads, 1)
       if (lane == 0) mbar_arrive(tempty);
       acc_phase ^= 1;
       if (!has && a.accumulate) continue;
-      const int64_t row = (int64_t)g * a.RA + (int64_t)mt * 128 + 32 * q + lane;
-      float* orow = a.out + row * a.RB + (int64_t)nt * 256 + slice * 64;
+      // 4 x 4 transpose of 8-column chunks inside each quad of lanes (two
+      // xor-shuffle rounds): afterwards chunk s of each 32-column block of lane
+      // 4a + b holds row 4a + s, columns 8b .. 8b + 7, so one store instruction
+      // writes whole 128-byte lines (a row per quad) rather than a 32-byte
+      // sector per lane and row, a quarter of the L2 write requests.
+      const int b = lane & 3;
 #pragma unroll
-      for (int j = 0; j < 64; j += 8) {
-        uint32_t o[8];
-        if (a.accumulate) {
-          ld_global_v8(orow + j, o);
+      for (int u = 0; u < 2; ++u) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) + acc[j + k]);
-        } else {
+        for (int m = 1; m <= 2; m <<= 1) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) o[k] = __float_as_uint(acc[j + k]);
+          for (int c = 0; c < 4; ++c) {
+            if (c & m) continue;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float& lo = acc[32 * u + 8 * c + e];
+              float& hi = acc[32 * u + 8 * (c | m) + e];
+              const float recv = __shfl_xor_sync(0xffffffffu, (b & m) ? lo : hi, m);
+              if (b & m) lo = recv; else hi = recv;
+            }
+          }
         }
-        st_global_v8(orow + j, o);
+      }
+      const int64_t row0 = (int64_t)g * a.RA + (int64_t)mt * 128 + 32 * q + (lane & ~3);
+      float* obase = a.out + row0 * a.RB + (int64_t)nt * 256 + slice * 64 + 8 * b;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4) {
+          float* op = obase + (int64_t)s4 * a.RB + 32 * u;
+          const float* v = acc + 32 * u + 8 * s4;
+          uint32_t o[8];
+          if (a.accumulate) {
+            ld_global_v8(op, o);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) + v[k]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = __float_as_uint(v[k]);
+          }
+          st_global_v8(op, o);
+        }
       }
     }
   }
@@ -439,8 +507,9 @@ cudaError_t launch_wgrad(const WgradArgs& a, cudaStream_t s) {
     attr_set[dev & 63] = true;
   }
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, a.a_codes, a.T, a.RA, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&tb, a.b_codes, a.T, a.RB, 128, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+  // chunk-major codes: rows (chunk, operand row) of 128 token bytes
+  if (!make_tmap(&ta, a.a_codes, 128, a.T / 128 * a.RA, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tb, a.b_codes, 128, a.T / 128 * a.RB, 128, 256, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const int64_t tiles = (int64_t)a.grp.G * (a.RA / 128) * (a.RB / 256);
   int64_t units = num_sms();

@@ -53,7 +53,7 @@ def test_colwise_mxfp8_bitexact(orc, gm):
     T = gm.colwise_tokens(M, G)
     codes, scales = orc.mxfp8_colwise(bits(d["x"]), np.array(splits_l))
     used = codes.shape[1]
-    g_codes = np_u8(out["col"][0], K * T).reshape(K, T)[:, :used]
+    g_codes = np_u8(out["col"][0], K * T).reshape(T // 128, K, 128).transpose(1, 0, 2).reshape(K, T)[:, :used]
     g_scales = orc.tiled_to_compact(np_u8(out["col"][1]), np.array([K]), T // 32)[:, :used // 32]
     assert np.array_equal(g_codes, codes)
     assert np.array_equal(g_scales, scales)
