@@ -46,10 +46,9 @@ WORKLOAD_TEXT = {
     "tiny": "MXFP8 SwiGLU grouped MLP: 4 experts, K=256, N=256, 512 tokens, seed 0",
 }
 NOMINAL_RATIO = {0: 2.0, 1: 6.0}   # dense FP8 / bf16 and FP4 / bf16 (4.5 and 13.5 vs 2.25 PFLOP/s)
-# DRAM bytes (read + write) per fc1 launch from one ncu capture
-# (profiles/gemm_mx_swiglu.md), valid only for the gemm.cu it was taken on.
-FC1_TRAFFIC = {("mx_swiglu", "c1e1067c12d12aa78d485ffa9be7e7c889c6d6d8"): 65025280 + 4927232,
-               ("nv_srelu", "c1e1067c12d12aa78d485ffa9be7e7c889c6d6d8"): 126107136 + 98628864}
+# DRAM bytes (read + write) per fc1 launch from one ncu capture of the gemm.cu
+# whose sha1 is in the key, valid only for that source.
+FC1_TRAFFIC = {("mx_swiglu", "b0e8fcf872c3051bf7b3c4106ed692b23271c65a"): 65024256 + 4080384}
 
 
 def fc1_traffic(workload: str):

@@ -16,7 +16,9 @@
  * The pages give no rounding rules.  The format facts used here are those the
  * method statement fixes: E2M1 values {0,0.5,1,1.5,2,3,4,6}; E4M3 max 448 (no
  * infinity, S.1111.111 is NaN); MXFP8 block scale 2^(floor(log2 amax) - 8) in
- * E8M0; H16 * H16^T = 16 I.  Every reading beyond those is listed in the design doc.
+ * E8M0; H16 * H16^T = 16 I.  Every reading beyond those is stated at the
+ * function that takes it (round-to-nearest-even, saturation, the NVFP4 scale
+ * chain and its FLT_MAX caps).
  *
  * Arithmetic: exact values are carried in double; wherever the method fixes an
  * FP32 operation (the NVFP4 scale chain, the RHT butterfly) it is done in
