@@ -400,6 +400,7 @@ def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps
     wws = torch.empty(gmlp.load().gmlp_backward_wgrad_workspace_size(w.M, w.K, w.N, w.G, w.act), dtype=torch.uint8,
                       device=dev)
     grads = gmlp.backward_wgrad(xin, dy, h, probs, f1, splits, w.act, workspace=wws)
+    kern = {}
     for _ in range(W_steps):
         flush.zero_()
         gmlp.backward_wgrad(xin, dy, h, probs, f1, splits, w.act, workspace=wws, **grads)
@@ -413,17 +414,60 @@ def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps
     torch.cuda.synchronize()
     gmlp.check_device_status()
     wms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ew)
+    # second pass: an event after every kernel (dy cast, fc2_x cast, dW2 GEMM,
+    # fc1_dy cast, x cast, dW1 GEMM)
+    wst = [0.0] * 6
+    for _ in range(K_steps):
+        flush.zero_()
+        se = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        se[0].record()
+        gmlp.backward_wgrad(xin, dy, h, probs, f1, splits, w.act, workspace=wws, events=se[1:], **grads)
+        torch.cuda.synchronize()
+        for i in range(6):
+            wst[i] += se[i].elapsed_time(se[i + 1]) / K_steps
+    gmlp.check_device_status()
     del grads, wws, f1
+    hbm, bf16_burst, _, _ = peaks()
+    fp8 = bf16_burst * NOMINAL_RATIO[gmlp.MXFP8]
+    M, K, N, N1 = w.M, w.K, w.N, w.n1
+
+    def tensor(name, flops, ms):
+        tf = flops / (ms * 1e-3) / 1e12
+        kern[name] = {"bound": "tensor", "ms": round(ms, 5), "TFLOP_s": round(tf, 1), "frac": round(tf / fp8, 4)}
+
+    def mem(name, nbytes, ms):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        kern[name] = {"bound": "hbm", "ms": round(ms, 5), "GB_s": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+
+    colq = M * (1 + 1 / 32)  # codes + scales written per column (padding excluded)
+    mem("dy columnwise cast", M * K * 2 + K * colq, wst[0])
+    mem("fc2_x rebuild + columnwise cast", M * N1 * 2 + M * 4 + N * colq, wst[1])
+    tensor("dW2 GEMM", 2.0 * M * K * N, wst[2])
+    mem("fc1_dy columnwise cast", M * N1 * 2 + N1 * colq, wst[3])
+    mem("x columnwise cast", M * K * 2 + K * colq, wst[4])
+    tensor("dW1 GEMM", 2.0 * M * N1 * K, wst[5])
     wgrad = {"what": "dW1, dW2 (FP32) and dbias1, dbias2: columnwise MXFP8 of dy, fc2_x (rebuilt from the saved "
                      "activation input), fc1_dy and x, two grouped wgrad GEMMs over each expert's tokens",
-             "ms_per_step": round(wms, 5), "flops_per_step": flops, "TFLOP_s": round(flops / (wms * 1e-3) / 1e12, 2)}
+             "ms_per_step": round(wms, 5), "flops_per_step": flops, "TFLOP_s": round(flops / (wms * 1e-3) / 1e12, 2),
+             "kernels": kern,
+             "roofline_note": "per kernel, from a second pass with an event after every kernel; tensor kernels "
+                              f"against the measured bf16 burst x {NOMINAL_RATIO[gmlp.MXFP8]} (FP8), casts "
+                              "against the measured HBM copy bandwidth; algorithmic bytes"}
     return {"what": "dx and dprob: dy MXFP8 cast, fc2 dGLU GEMM (fused dact x prob, dprob, MXFP8 fc1_dy), "
                     "fc1 dgrad GEMM",
             "wgrad": wgrad,
             "ms_per_step": round(ms, 5), "flops_per_step": flops, "TFLOP_s": round(flops / (ms * 1e-3) / 1e12, 2),
             "stages_ms": [round(t, 5) for t in st],
             "stage_tflops": {"dglu": round(2.0 * w.M * w.K * w.N / (st[1] * 1e-3) / 1e12, 1),
-                             "dgrad": round(2.0 * w.M * w.n1 * w.K / (st[2] * 1e-3) / 1e12, 1)}}
+                             "dgrad": round(2.0 * w.M * w.n1 * w.K / (st[2] * 1e-3) / 1e12, 1)},
+            "kernels": {
+                "dy cast (+ dprob memset)": {"bound": "hbm", "ms": round(st[0], 5),
+                                             "GB_s": round((M * K * (3 + 1 / 32)) / (st[0] * 1e-3) / 1e9, 1),
+                                             "frac": round((M * K * (3 + 1 / 32)) / (st[0] * 1e-3) / 1e9 / hbm, 4)},
+                "dGLU GEMM": {"bound": "tensor", "ms": round(st[1], 5),
+                              "frac": round(2.0 * M * K * N / (st[1] * 1e-3) / 1e12 / fp8, 4)},
+                "dgrad GEMM": {"bound": "tensor", "ms": round(st[2], 5),
+                               "frac": round(2.0 * M * N1 * K / (st[2] * 1e-3) / 1e12 / fp8, 4)}}}
 
 
 def bench_quantizer(gmlp, dev, hbm) -> dict:

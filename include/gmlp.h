@@ -396,12 +396,17 @@ GMLP_API size_t gmlp_backward_wgrad_workspace_size(int64_t M, int64_t K, int64_t
  * it needs may then be NULL).  accumulate = 0 overwrites them (an expert with
  * no tokens gets zeros); 1 adds the new gradients into them.  The GEMMs
  * accumulate in FP32 on the tensor cores; the bias sums are FP32 atomics.
+ * stage_events (n_stage_events of them, at most 6, NULL when 0) are recorded
+ * on `stream` after each launched kernel in order: the dy cast, the fc2_x
+ * cast, the dW2 GEMM, the fc1_dy cast, the x cast, the dW1 GEMM (those that
+ * the requested outputs need).
  * act: SWIGLU or SRELU.  Limits: K % 256 == 0, N % 256 == 0. */
 GMLP_API gmlp_status gmlp_backward_wgrad(const uint16_t* x, const uint16_t* dy, const uint16_t* pre_act,
                                          const float* probs, const uint16_t* fc1_dy, int64_t M, int64_t K, int64_t N,
                                          const int64_t* split_sizes, int32_t G, int32_t act, float* dW1, float* dW2,
                                          float* dbias1, float* dbias2, int32_t accumulate, void* workspace,
-                                         size_t workspace_bytes, gmlp_stream stream);
+                                         size_t workspace_bytes, gmlp_event* stage_events, int32_t n_stage_events,
+                                         gmlp_stream stream);
 
 /* Self-test of the device failure path (no counterpart on the pages): one
  * warp waits, through the same bounded mbarrier wait the kernels use, on a

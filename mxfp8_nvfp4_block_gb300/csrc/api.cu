@@ -796,11 +796,14 @@ size_t gmlp_backward_wgrad_workspace_size(int64_t M, int64_t K, int64_t N, int32
 gmlp_status gmlp_backward_wgrad(const uint16_t* x, const uint16_t* dy, const uint16_t* pre_act, const float* probs,
                                 const uint16_t* fc1_dy, int64_t M, int64_t K, int64_t N, const int64_t* split_sizes,
                                 int32_t G, int32_t act, float* dW1, float* dW2, float* dbias1, float* dbias2,
-                                int32_t accumulate, void* workspace, size_t workspace_bytes, gmlp_stream stream) {
+                                int32_t accumulate, void* workspace, size_t workspace_bytes, gmlp_event* stage_events,
+                                int32_t n_stage_events, gmlp_stream stream) {
   g_last_error[0] = 0;
   GMLP_TRY(check_groups(G, M, split_sizes));
   if (act != GMLP_ACT_SWIGLU && act != GMLP_ACT_SRELU)
     return fail(GMLP_ERR_INVALID_ARG, "wgrad act = %d: SwiGLU or SReLU", act);
+  if (n_stage_events < 0 || n_stage_events > 6 || (n_stage_events > 0 && !stage_events))
+    return fail(GMLP_ERR_INVALID_ARG, "n_stage_events = %d: 0..6, stage_events non-NULL", n_stage_events);
   if (accumulate != 0 && accumulate != 1) return fail(GMLP_ERR_INVALID_ARG, "accumulate = %d: 0 or 1", accumulate);
   const int64_t N1 = act == GMLP_ACT_SWIGLU ? 2 * N : N;
   if (K <= 0 || K % 256 || N <= 0 || N % 256)
@@ -830,6 +833,12 @@ gmlp_status gmlp_backward_wgrad(const uint16_t* x, const uint16_t* dy, const uin
   if (M == 0) return GMLP_OK;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const GroupSrc gs{split_sizes, 0, G, M};
+  int n_ev = 0;  // stage events go out in launch order
+  auto stage_done = [&]() -> gmlp_status {
+    if (n_ev < n_stage_events) GMLP_CUDA(cudaEventRecord((cudaEvent_t)stage_events[n_ev], s), "stage event record");
+    ++n_ev;
+    return GMLP_OK;
+  };
   auto colq = [&](const uint16_t* src, int64_t ld, int64_t C, int mode, size_t c_off, size_t s_off,
                   float* colsum) -> gmlp_status {
     ColqArgs q{};
@@ -845,7 +854,7 @@ gmlp_status gmlp_backward_wgrad(const uint16_t* x, const uint16_t* dy, const uin
     q.colsum = colsum;
     q.mode = mode;
     GMLP_CUDA(launch_colq(q, s), "columnwise quantise launch");
-    return GMLP_OK;
+    return stage_done();
   };
   auto wgrad = [&](size_t ac, size_t as, size_t bc, size_t bs, int64_t RA, int64_t RB, float* out) -> gmlp_status {
     WgradArgs w{};
@@ -860,7 +869,7 @@ gmlp_status gmlp_backward_wgrad(const uint16_t* x, const uint16_t* dy, const uin
     w.out = out;
     w.accumulate = accumulate;
     GMLP_CUDA(launch_wgrad(w, s), "wgrad launch");
-    return GMLP_OK;
+    return stage_done();
   };
   if (want2) {  // FC2: dW2_g = dy_g^T fc2_x_g over the group's tokens, dbias2 = token sums of dy
     GMLP_TRY(colq(dy, K, K, COLQ_PLAIN, L.dy_c, L.dy_s, dbias2));

@@ -95,7 +95,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gmlp_backward_wgrad_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
         "gmlp_colwise_tokens": (_i64, [_i64, _i32]),
         "gmlp_backward_wgrad": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp,
-                                       _vp, _i32, _vp, ctypes.c_size_t, _vp]),
+                                       _vp, _i32, _vp, ctypes.c_size_t, _vp, _i32, _vp]),
         "gmlp_last_error": (ctypes.c_char_p, []),
         "gmlp_version": (ctypes.c_char_p, []),
     }
@@ -386,10 +386,11 @@ def backward_dgrad(dy, splits, W2t: "QWeight", W1t: "QWeight", pre_act, probs, a
 
 def backward_wgrad(x, dy, pre_act, probs, fc1_dy, splits, act: int, *, dW1=None, dW2=None, dbias1=None,
                    dbias2=None, want=("dW1", "dW2", "dbias1", "dbias2"), accumulate: bool = False, workspace=None,
-                   stream=None) -> dict:
+                   events=None, stream=None) -> dict:
     """Weight and bias gradients of the fused grouped MLP (see
     gmlp_backward_wgrad); outputs FP32, allocated when not given for the names
-    in `want`.  Returns {"dW1", "dW2", "dbias1", "dbias2"} (None where skipped)."""
+    in `want`; events: up to 6 torch.cuda.Event recorded after each kernel.
+    Returns {"dW1", "dW2", "dbias1", "dbias2"} (None where skipped)."""
     x, dy, fc1_dy = _bits(x), _bits(dy), _bits(fc1_dy)
     M, K = dy.shape
     N1 = fc1_dy.shape[1]
@@ -407,7 +408,8 @@ def backward_wgrad(x, dy, pre_act, probs, fc1_dy, splits, act: int, *, dW1=None,
     _check(load().gmlp_backward_wgrad(_p(x), _p(dy), _p(_bits(pre_act) if pre_act is not None else None), _p(probs),
                                       _p(fc1_dy), M, K, N, _p(splits), G, act, _p(out["dW1"]), _p(out["dW2"]),
                                       _p(out["dbias1"]), _p(out["dbias2"]), int(bool(accumulate)), _p(workspace),
-                                      workspace.numel(), _stream(stream)))
+                                      workspace.numel(), _event_handles(events) if events else None,
+                                      len(events or ()), _stream(stream)))
     return out
 
 

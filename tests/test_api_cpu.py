@@ -255,9 +255,9 @@ def test_backward_wgrad_checks(lib):
     assert need >= (2 * K + N + 2 * N) * T
 
     def call(K=K, N=N, act=g.SWIGLU, x=FAKE, dy=FAKE, pre=FAKE, f=FAKE, dW1=FAKE, dW2=FAKE, db1=None, db2=None,
-             acc=0, ws=FAKE, wsb=need):
+             acc=0, ws=FAKE, wsb=need, ev=None, n_ev=0):
         return L.gmlp_backward_wgrad(x, dy, pre, None, f, M, K, N, FAKE, G, act, dW1, dW2, db1, db2, acc, ws, wsb,
-                                     None)
+                                     ev, n_ev, None)
 
     assert call(act=g.TANH_SRELU) == g.ERR_INVALID_ARG
     assert call(K=384) == g.ERR_INVALID_DIMS
@@ -271,3 +271,5 @@ def test_backward_wgrad_checks(lib):
     assert call(db1=FAKE + 2) == g.ERR_INVALID_ARG
     assert call(wsb=need - 1) == g.ERR_WORKSPACE
     assert call(ws=None) == g.ERR_WORKSPACE
+    assert call(n_ev=7, ev=FAKE) == g.ERR_INVALID_ARG      # at most 6 stage events
+    assert call(n_ev=2) == g.ERR_INVALID_ARG               # events NULL
