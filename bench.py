@@ -539,6 +539,40 @@ def oracle_sample(name: str, target_s: float = 10.0, max_reps: int = 3) -> dict:
                       f"{el:.1f} s, numpy float64 GEMMs + C format arithmetic"}
 
 
+def oracle_backward_sample(name: str, max_tokens: int = 8000) -> dict:
+    """The oracle's backward (data, weight and bias gradients) on the host
+    cores, on a bounded sample of whole experts of the workload (the weight
+    gradients contract over each expert's tokens, so experts are not cut)."""
+    import oracle
+    d = make_inputs(name)
+    w = d["workload"]
+    sp = d["splits"].numpy()
+    offs = np.concatenate([[0], np.cumsum(sp)])
+    picked, tok = [], 0
+    for g in np.argsort(sp):                      # smallest non-empty experts first
+        if sp[g] > 0 and tok + sp[g] <= max_tokens:
+            picked.append(int(g))
+            tok += int(sp[g])
+    picked.sort()
+    rows = np.concatenate([np.arange(offs[g], offs[g + 1]) for g in picked])
+    ssp = np.array([sp[g] for g in picked])
+    gen = torch.Generator().manual_seed(w.seed + 77)
+    dy = torch.randn((len(rows), w.K), generator=gen).to(torch.bfloat16)
+    h = (1.5 * torch.randn((len(rows), w.n1), generator=gen)).to(torch.bfloat16)
+    xs, W1, W2 = bits(d["x"])[rows], bits(d["W1"])[picked], bits(d["W2"])[picked]
+    probs = d["probs"].numpy()[rows]
+    t0 = time.time()
+    rb = oracle.backward_dgrad(bits(dy), ssp, W1, W2, bits(h), probs, w.act)
+    oracle.backward_wgrad(xs, bits(dy), bits(h), probs, rb["fc1_dy"], ssp, w.act)
+    el = time.time() - t0
+    m = len(rows)
+    flops = 2 * (2.0 * m * w.K * w.N + 2.0 * m * w.n1 * w.K)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"experts {picked} of {name} ({m} tokens): backward_dgrad + backward_wgrad (weights "
+                      f"quantised inside), {el:.1f} s, numpy float64 GEMMs + C format arithmetic"}
+
+
 def run_reference(args) -> dict:
     """The reference arm: the oracle on the host, each step a bounded row
     sample (MXFP8 rows are independent) of the same workload."""
@@ -629,6 +663,8 @@ def main():
     if rank == 0:
         if args.cpu:
             out["cpu_baseline"] = oracle_sample(args.workload)
+            if "backward_dgrad" in out:
+                out["backward_dgrad"]["cpu_baseline"] = oracle_backward_sample(args.workload)
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.barrier()
