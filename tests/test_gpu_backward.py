@@ -114,3 +114,24 @@ def test_backward_dgrad_lossless_bitexact(orc, gm):
     assert np.array_equal(np_u8(fc1["codes"], M * N).reshape(M, N), ref["fc1_dy_codes"])
     assert np.array_equal(np_bits(dx), ref["dx"])
     assert np.array_equal(dprob.cpu().numpy().astype(np.float64), ref["dprob"])
+
+
+def test_backward_dgrad_many_tiny_groups(orc, gm):
+    """64 experts, most empty or of 1-8 tokens, a few large: every tile of the
+    dGLU and dgrad GEMMs is a ragged one."""
+    rng = np.random.default_rng(81)
+    splits_l = [int(v) for v in rng.integers(0, 9, 64)]
+    splits_l[5], splits_l[50] = 260, 131
+    K, N = 256, 256
+    G, M = len(splits_l), sum(splits_l)
+    splits = torch.tensor(splits_l, dtype=torch.int64)
+    W1 = bf16_cpu(rng.standard_normal((G, 2 * N, K)) / np.sqrt(K))
+    W2 = bf16_cpu(rng.standard_normal((G, K, N)) / np.sqrt(N))
+    probs = torch.from_numpy(rng.uniform(0.1, 1, M).astype(np.float32)).cuda()
+    h = bf16_cpu(1.5 * rng.standard_normal((M, 2 * N))).cuda()
+    dy = bf16_cpu(rng.standard_normal((M, K)))
+    dx, dprob, fc1 = run_backward(gm, dy, splits, W1, W2, h, probs, 0)
+    ref = orc.backward_dgrad(bits(dy), np.array(splits_l), bits(W1), bits(W2), np_bits(h), probs.cpu().numpy(), 0)
+    assert frob(dx.float().cpu().numpy(), orc.bf16_to_f64(ref["dx"])) <= 1e-2
+    assert frob(dprob.cpu().numpy(), ref["dprob"]) <= 1e-2
+    assert float(np.mean(np_bits(fc1["bf16"]) == ref["fc1_dy"])) >= 0.99

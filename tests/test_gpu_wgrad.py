@@ -155,3 +155,31 @@ def test_wgrad_full_size_sampled(orc, gm):
     for g in empty:
         assert not out["dW1"][g].any() and not out["dW2"][g].any()
     print(f"full-size wgrad: worst sampled error {worst:.2e} of sum |a b|")
+
+
+@pytest.mark.parametrize("case", ["many_tiny", "one_group", "under_one_chunk"])
+def test_wgrad_group_edge_cases(orc, gm, case):
+    """Ragged extremes: 64 experts, most empty or of 1-8 tokens with a few large
+    ones (the skewed workload's tail); one expert holding every token; fewer
+    tokens than one 128-token chunk.  SReLU keeps the fc2_x rebuild exact, so
+    only FP32 summation order separates the two sides."""
+    rng = np.random.default_rng(31)
+    if case == "many_tiny":
+        splits_l = [int(v) for v in rng.integers(0, 9, 64)]
+        splits_l[3], splits_l[40], splits_l[63] = 300, 129, 0
+    elif case == "one_group":
+        splits_l = [777]
+    else:
+        splits_l = [0, 37, 0, 60]
+    K, N = 256, 256
+    d = seeded_inputs(41, splits_l, K, N, 1)
+    splits = torch.tensor(splits_l, dtype=torch.int64)
+    out = run_wgrad(gm, d, splits, 1)
+    ref = orc.backward_wgrad(bits(d["x"]), bits(d["dy"]), bits(d["h"]), d["probs"].numpy(), bits(d["fc1_dy"]),
+                             np.array(splits_l), 1)
+    for k in ("dW1", "dW2", "dbias1", "dbias2"):
+        err = frob(out[k].cpu().numpy(), ref[k])
+        assert err <= 1e-5, (k, err)
+    for g, m in enumerate(splits_l):
+        if m == 0:
+            assert not out["dW1"][g].any() and not out["dW2"][g].any() and not out["dbias1"][g].any()
