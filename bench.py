@@ -608,11 +608,13 @@ def oracle_sample(name: str, target_s: float = 10.0, max_reps: int = 3) -> dict:
                       f"{el:.1f} s, numpy float64 GEMMs + C format arithmetic"}
 
 
-def oracle_backward_sample(name: str, max_tokens: int = 1 << 30, target_s: float = 10.0, max_reps: int = 3) -> dict:
+def oracle_backward_sample(name: str, max_tokens: int = 16384, max_experts: int = 8, target_s: float = 10.0,
+                           max_reps: int = 3) -> dict:
     """The oracle's backward (data, weight and bias gradients) on the host
-    cores, on whole experts of the workload up to max_tokens (the weight
-    gradients contract over each expert's tokens, so experts are not cut),
-    repeated until about target_s of CPU work."""
+    cores, on whole experts of the workload, smallest first, up to max_tokens
+    tokens and max_experts experts (the weight gradients contract over each
+    expert's tokens, so experts are not cut), repeated until about target_s of
+    CPU work."""
     import oracle
     d = make_inputs(name)
     w = d["workload"]
@@ -620,7 +622,7 @@ def oracle_backward_sample(name: str, max_tokens: int = 1 << 30, target_s: float
     offs = np.concatenate([[0], np.cumsum(sp)])
     picked, tok = [], 0
     for g in np.argsort(sp):                      # smallest non-empty experts first
-        if sp[g] > 0 and tok + sp[g] <= max_tokens:
+        if sp[g] > 0 and tok + sp[g] <= max_tokens and len(picked) < max_experts:
             picked.append(int(g))
             tok += int(sp[g])
     picked.sort()
@@ -705,8 +707,9 @@ def main():
     ap.add_argument("--workload", default="mx_swiglu", choices=[k for k in WORKLOADS if k != "nv_quant"])
     ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 2],
                     help="0: one CTA per 128x256 tile; 2: CTA pairs on 256x256 tiles")
-    ap.add_argument("--backward", action="store_true",
-                    help="MXFP8: also time the data-gradient backward (dy -> dx, dprob)")
+    ap.add_argument("--backward", dest="backward", action="store_true", default=True,
+                    help="MXFP8 SwiGLU / SReLU: also time the backward, data and weight gradients (the default)")
+    ap.add_argument("--no-backward", dest="backward", action="store_false", help="skip the backward leg")
     ap.add_argument("--fc2x-colwise", action="store_true",
                     help="NVFP4: also write the columnwise (RHT) NVFP4 fc2_x each step (no-recompute training path)")
     ap.add_argument("--l2-flush", default="write", choices=["write", "clean"],
