@@ -146,6 +146,31 @@ GMLP_API int64_t gmlp_colwise_tokens(int64_t M, int32_t G);
  * scale columns per row (cols/32 for MXFP8, cols/16 for NVFP4). */
 GMLP_API size_t gmlp_tiled_scales_bytes(int64_t M, int32_t G, int64_t nscale);
 
+/* Layout queries (host only: no CUDA call, no device memory, callable without a
+ * GPU).  The machine-readable form of the two swizzled layouts described at the
+ * top of this file, so that a caller can de-swizzle scales and codes without
+ * re-deriving them.  split_sizes_host: host int64 [G], each >= 0; M is their
+ * sum.
+ *
+ * gmlp_query_layout(GMLP_LAYOUT_TILED_SCALE, ...): byte offset, inside a
+ *   GEMM_TILED scale buffer with `ncols` scale columns per row (a multiple of
+ *   4), of the scale of row `row` (0 <= row < M), scale column `col`.
+ * gmlp_query_layout(GMLP_LAYOUT_COLWISE_CODE, ...): byte offset, inside a
+ *   columnwise MXFP8 code buffer of an [M, ncols] tensor, of the code of token
+ *   `row`, column `col`.
+ * gmlp_query_layout(GMLP_LAYOUT_COLWISE_SCALE, ...): byte offset, inside that
+ *   tensor's columnwise scale buffer, of the E8M0 scale of the 32-token block
+ *   holding token `row`, column `col` (ncols a multiple of 128).
+ * Returns -1 for an unknown kind, a NULL split_sizes_host with G > 0, a
+ * negative size, or row / col out of range. */
+typedef enum gmlp_layout_kind {
+  GMLP_LAYOUT_TILED_SCALE = 0,
+  GMLP_LAYOUT_COLWISE_CODE = 1,
+  GMLP_LAYOUT_COLWISE_SCALE = 2
+} gmlp_layout_kind;
+GMLP_API int64_t gmlp_query_layout(int32_t kind, const int64_t* split_sizes_host, int32_t G, int64_t ncols,
+                                   int64_t row, int64_t col);
+
 /* gmlp_group_hadamard_amax -- nvfp4_group_hadamard_amax (PR #3837, Changes:
  * the binding exposes the group Hadamard-amax pass on its own; the sign-mask
  * fix makes the mask part of the post-RHT amax).  One read-only pass over a

@@ -788,6 +788,41 @@ int64_t gmlp_colwise_tokens(int64_t M, int32_t G) {
   return 128 * ((M + 127) / 128 + G);
 }
 
+int64_t gmlp_query_layout(int32_t kind, const int64_t* split_sizes_host, int32_t G, int64_t ncols, int64_t row,
+                          int64_t col) {
+  if (G < 1 || !split_sizes_host || ncols <= 0 || row < 0 || col < 0 || col >= ncols) return -1;
+  // find row's group: its first row and the number of 128-row tiles before it
+  int64_t off = 0, tiles = 0, M = 0;
+  int32_t g = -1;
+  for (int32_t h = 0; h < G; ++h) {
+    const int64_t m = split_sizes_host[h];
+    if (m < 0) return -1;
+    if (g < 0 && row < M + m) {
+      g = h;
+      off = M;
+    }
+    if (g < 0) tiles += (m + 127) / 128;
+    M += m;
+  }
+  if (g < 0) return -1;  // row >= M
+  const int64_t lr = row - off;
+  const int64_t tile = tiles + lr / 128, rr = lr % 128;
+  switch (kind) {
+    case GMLP_LAYOUT_TILED_SCALE:
+      if (ncols % 4) return -1;
+      return (tile * (ncols / 4) + col / 4) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + col % 4;
+    case GMLP_LAYOUT_COLWISE_CODE:
+      return (tile * ncols + col) * 128 + rr;
+    case GMLP_LAYOUT_COLWISE_SCALE: {
+      if (ncols % 128) return -1;
+      const int64_t chunks = gmlp_colwise_tokens(M, G) / 128, i = col % 128;
+      return ((col / 128) * chunks + tile) * 512 + (i % 32) * 16 + (i / 32) * 4 + rr / 32;
+    }
+    default:
+      return -1;
+  }
+}
+
 size_t gmlp_backward_wgrad_workspace_size(int64_t M, int64_t K, int64_t N, int32_t G, int32_t act) {
   if (M < 0 || K <= 0 || N <= 0 || G < 1) return 0;
   return wgrad_layout(M, K, N, act == GMLP_ACT_SWIGLU ? 2 * N : N, G).total;

@@ -27,7 +27,8 @@ EXPORTS = ["gmlp_tiled_scales_bytes", "gmlp_group_hadamard_amax", "gmlp_group_qu
            "gmlp_check_device_status", "gmlp_last_error", "gmlp_version", "gmlp_forward_noalloc",
            "gmlp_selftest_bounded_wait", "gmlp_mma_peak", "gmlp_replicate_weight_scales",
            "gmlp_prepare_weights_discrete", "gmlp_backward_workspace_size", "gmlp_backward_dgrad",
-           "gmlp_backward_wgrad_workspace_size", "gmlp_backward_wgrad", "gmlp_colwise_tokens"]
+           "gmlp_backward_wgrad_workspace_size", "gmlp_backward_wgrad", "gmlp_colwise_tokens",
+           "gmlp_query_layout"]
 
 
 class Recipe(ctypes.Structure):
@@ -94,6 +95,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                        _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _i32, _vp]),
         "gmlp_backward_wgrad_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
         "gmlp_colwise_tokens": (_i64, [_i64, _i32]),
+        "gmlp_query_layout": (_i64, [_i32, ctypes.c_void_p, _i32, _i64, _i64, _i64]),
         "gmlp_backward_wgrad": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp,
                                        _vp, _i32, _vp, ctypes.c_size_t, _vp, _i32, _vp]),
         "gmlp_last_error": (ctypes.c_char_p, []),
@@ -177,6 +179,16 @@ def alloc_quant_outputs(M: int, K: int, G: int, fmt: int, layout: int, rowwise: 
 def colwise_tokens(M: int, G: int) -> int:
     """T of the columnwise MXFP8 layout (see gmlp_colwise_tokens)."""
     return int(load().gmlp_colwise_tokens(M, G))
+
+
+LAYOUT_TILED_SCALE, LAYOUT_COLWISE_CODE, LAYOUT_COLWISE_SCALE = 0, 1, 2
+
+
+def query_layout(kind: int, splits_host, ncols: int, row: int, col: int) -> int:
+    """Byte offset of one scale or code in a swizzled layout (gmlp_query_layout;
+    host only, -1 when out of range)."""
+    sp = (ctypes.c_int64 * len(splits_host))(*[int(m) for m in splits_host])
+    return int(load().gmlp_query_layout(kind, ctypes.cast(sp, ctypes.c_void_p), len(splits_host), ncols, row, col))
 
 
 def group_quantize_with_amax(x, splits, rec: Recipe, amax_pre=None, amax_post=None, *, rowwise=True,

@@ -273,3 +273,41 @@ def test_backward_wgrad_checks(lib):
     assert call(ws=None) == g.ERR_WORKSPACE
     assert call(n_ev=7, ev=FAKE) == g.ERR_INVALID_ARG      # at most 6 stage events
     assert call(n_ev=2) == g.ERR_INVALID_ARG               # events NULL
+
+
+def test_query_layout_matches_the_oracles_layouts(lib, orc):
+    """gmlp_query_layout against the oracle's own restatement of the layouts
+    (oracle/layout.py for GEMM_TILED; the chunk-major columnwise MXFP8 layout
+    as the weight-gradient parity tests de-swizzle it): every owned scale and
+    code of a ragged split with empty groups, and -1 outside the tensor."""
+    import numpy as np
+    L, g = lib
+    splits = [130, 0, 257, 5, 1, 128]
+    M, G = sum(splits), len(splits)
+    ks = 8
+    want = orc.tiled_index(np.array(splits), ks)
+    got = np.array([[g.query_layout(g.LAYOUT_TILED_SCALE, splits, ks, r, j) for j in range(ks)] for r in range(M)])
+    assert np.array_equal(got, want)
+
+    C = 256
+    T = g.colwise_tokens(M, G)
+    # code buffer [T/128][C][128] viewed as the logical [C][T] operand
+    code_pos = np.arange(C * T).reshape(T // 128, C, 128).transpose(1, 0, 2).reshape(C, T)
+    scale_pos = orc.tiled_index(np.array([C]), T // 32)           # a [C]-row operand, T/32 scales per row
+    offs, pofs = orc.group_offsets(np.array(splits)), orc.padded_offsets(np.array(splits))
+    rng = np.random.default_rng(3)
+    for t in rng.integers(0, M, 64):
+        grp = int(np.searchsorted(offs, t, side="right") - 1)
+        p = int(pofs[grp] + t - offs[grp])
+        for c in rng.integers(0, C, 8):
+            assert g.query_layout(g.LAYOUT_COLWISE_CODE, splits, C, int(t), int(c)) == code_pos[c, p]
+            assert g.query_layout(g.LAYOUT_COLWISE_SCALE, splits, C, int(t), int(c)) == scale_pos[c, p // 32]
+
+    for kind, nc in ((g.LAYOUT_TILED_SCALE, ks), (g.LAYOUT_COLWISE_CODE, C), (g.LAYOUT_COLWISE_SCALE, C)):
+        assert g.query_layout(kind, splits, nc, M, 0) == -1
+        assert g.query_layout(kind, splits, nc, 0, nc) == -1
+        assert g.query_layout(kind, splits, nc, -1, 0) == -1
+    assert g.query_layout(g.LAYOUT_TILED_SCALE, splits, 6, 0, 0) == -1        # not a multiple of 4
+    assert g.query_layout(g.LAYOUT_COLWISE_SCALE, splits, 96, 0, 0) == -1     # not a multiple of 128
+    assert g.query_layout(7, splits, ks, 0, 0) == -1
+    assert g.query_layout(g.LAYOUT_TILED_SCALE, [4, -1], ks, 0, 0) == -1
