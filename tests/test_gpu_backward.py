@@ -135,3 +135,44 @@ def test_backward_dgrad_many_tiny_groups(orc, gm):
     assert frob(dx.float().cpu().numpy(), orc.bf16_to_f64(ref["dx"])) <= 1e-2
     assert frob(dprob.cpu().numpy(), ref["dprob"]) <= 1e-2
     assert float(np.mean(np_bits(fc1["bf16"]) == ref["fc1_dy"])) >= 0.99
+
+
+def test_backward_dgrad_full_size_sampled(orc, gm):
+    """The full headline workload (MXFP8 SwiGLU, 8 experts, K=2048, N=1024,
+    16384 tokens, Dirichlet splits with an empty expert) in the launch
+    configuration the benchmark times.  Each row of dx, dprob and fc1_dy
+    depends only on its own dy and h rows and its expert's weights, and every
+    MXFP8 block lies along a row, so the oracle evaluates a row sample covering
+    every non-empty expert (its first and last rows included)."""
+    from mxfp8_nvfp4_block_gb300.inputs import make_inputs
+    w = make_inputs("mx_swiglu")
+    wl = w["workload"]
+    sp = w["splits"].numpy()
+    M, K, N = wl.M, wl.K, wl.N
+    gen = torch.Generator().manual_seed(99)
+    dy = torch.randn((M, K), generator=gen).to(torch.bfloat16)
+    h = (1.5 * torch.randn((M, 2 * N), generator=gen)).to(torch.bfloat16)
+    probs = w["probs"]
+    dx, dprob, fc1 = run_backward(gm, dy, w["splits"], w["W1"], w["W2"], h.cuda(), probs.cuda(), 0)
+    offs = orc.group_offsets(sp)
+    rng = np.random.default_rng(9)
+    rows = []
+    for g in range(len(sp)):
+        if sp[g]:
+            pick = [offs[g], offs[g + 1] - 1] + list(rng.integers(offs[g], offs[g + 1], min(16, int(sp[g]))))
+            rows += sorted(set(int(r) for r in pick))
+    rows = np.array(rows, dtype=np.int64)
+    sub = np.array([np.count_nonzero((rows >= offs[g]) & (rows < offs[g + 1])) for g in range(len(sp))])
+    ref = orc.backward_dgrad(bits(dy)[rows], sub, bits(w["W1"]), bits(w["W2"]), bits(h)[rows], probs.numpy()[rows],
+                             0)
+    fb = np_bits(fc1["bf16"])[rows]
+    bmatch = float(np.mean(fb == ref["fc1_dy"]))
+    frac, steps = code_match_report(0, np_u8(fc1["codes"], M * 2 * N).reshape(M, 2 * N)[rows], ref["fc1_dy_codes"],
+                                    orc.tiled_to_compact(np_u8(fc1["scales"]), sp, 2 * N // 32)[rows],
+                                    ref["fc1_dy_scales"])
+    err = frob(dx.float().cpu().numpy()[rows], orc.bf16_to_f64(ref["dx"]))
+    perr = frob(dprob.cpu().numpy()[rows], ref["dprob"])
+    print(f"full-size dgrad, {len(rows)} rows: fc1_dy bf16 match {bmatch:.6f}, code match {frac:.6f} "
+          f"(max {steps:.2f} steps), dx error {err:.3e}, dprob error {perr:.3e}")
+    assert bmatch >= 0.99 and frac >= 0.999 and steps <= 1.0 + 1e-9, (bmatch, frac, steps)
+    assert err <= 1e-2 and perr <= 1e-2
