@@ -295,8 +295,10 @@ def run_gpu(args, rank: int, world: int) -> dict:
                    "fc2x_columnwise": bool(colwise)},
         "e2e": {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "double-buffered across steps: step i's inputs copy in on one stream while step i-1 "
-                       "computes on a second and step i-2's y copies out on a third",
+                "how": "double-buffered across steps: step i's inputs copy in while step i-1 computes and "
+                       "step i-2's y copies out, on separate streams",
+                "copy_streams_per_direction": args.e2e_streams,
+                "copy_GB_s_per_direction": round(h2d / (e2e_ms * 1e-3) / 1e9, 1),
                 "sequential": {"value": round(world * w.flops / (e2e_seq_ms * 1e-3) / 1e12, 3),
                                "ms_per_step": round(e2e_seq_ms, 5)}},
         "gpu_launches": K_steps * n_stage,
@@ -354,14 +356,21 @@ def e2e_pipelined(gmlp, args, w, x, probs, splits, y, x_h, p_h, s_h, W1, W2, act
                   K_steps: int, W_steps: int) -> float:
     """ms per step of the host-to-host forward with two slots of device and
     pinned host buffers: every step copies its x, probs and split sizes in
-    and its y out inside the timed region, on three streams (in, compute,
-    out) ordered by events, so the copies of neighbouring steps overlap."""
+    and its y out inside the timed region, on copy streams ordered by events
+    around one compute stream, so the copies of neighbouring steps overlap.
+    With args.e2e_streams = S > 1, x and y move as S row slices on S streams
+    per direction (concurrent copies)."""
+    S = max(1, int(args.e2e_streams))
+    M = x.shape[0]
+    cuts = [M * k // S for k in range(S + 1)]
     xs, ps, ss, ys = [x, x.clone()], [probs, probs.clone()], [splits, splits.clone()], [y, torch.empty_like(y)]
     yh = [torch.empty(y.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]
+    s_in = [torch.cuda.Stream() for _ in range(S)]
+    s_out = [torch.cuda.Stream() for _ in range(S)]
+    s_cmp = torch.cuda.Stream()
+    ev_in = [[torch.cuda.Event() for _ in range(S)] for _ in range(2)]
+    ev_out = [[torch.cuda.Event() for _ in range(S)] for _ in range(2)]
     ev_cmp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
     started = [False, False]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -369,26 +378,35 @@ def e2e_pipelined(gmlp, args, w, x, probs, splits, y, x_h, p_h, s_h, W1, W2, act
         b = it & 1
         if it == W_steps:
             torch.cuda.synchronize()
-            e0.record(s_in)
-        with torch.cuda.stream(s_in):
+            e0.record(s_in[0])
+            for st in s_in[1:] + s_out:
+                st.wait_event(e0)
+        for k, st in enumerate(s_in):
+            with torch.cuda.stream(st):
+                if started[b]:
+                    st.wait_event(ev_cmp[b])      # the slot's previous forward has read its inputs
+                xs[b][cuts[k]:cuts[k + 1]].copy_(x_h[cuts[k]:cuts[k + 1]], non_blocking=True)
+                if k == 0:
+                    ps[b].copy_(p_h, non_blocking=True)
+                    ss[b].copy_(s_h, non_blocking=True)
+                ev_in[b][k].record(st)
+        for k in range(S):
+            s_cmp.wait_event(ev_in[b][k])
             if started[b]:
-                s_in.wait_event(ev_cmp[b])        # the slot's previous forward has read its inputs
-            xs[b].copy_(x_h, non_blocking=True)
-            ps[b].copy_(p_h, non_blocking=True)
-            ss[b].copy_(s_h, non_blocking=True)
-            ev_in[b].record(s_in)
-        s_cmp.wait_event(ev_in[b])
-        if started[b]:
-            s_cmp.wait_event(ev_out[b])           # the slot's previous y has been read out
+                s_cmp.wait_event(ev_out[b][k])    # the slot's previous y has been read out
         gmlp.forward(xs[b], ss[b], W1, W2, ps[b], act, rec, y=ys[b], workspace=ws, gemm_mode=args.gemm_mode,
                      aux=colwise, tanh_clamp_scale=w.tanh_clamp_scale, stream=s_cmp)
         ev_cmp[b].record(s_cmp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_cmp[b])
-            yh[b].copy_(ys[b], non_blocking=True)
-            ev_out[b].record(s_out)
+        for k, st in enumerate(s_out):
+            with torch.cuda.stream(st):
+                st.wait_event(ev_cmp[b])
+                yh[b][cuts[k]:cuts[k + 1]].copy_(ys[b][cuts[k]:cuts[k + 1]], non_blocking=True)
+                ev_out[b][k].record(st)
         started[b] = True
-    e1.record(s_out)
+    b = (W_steps + K_steps - 1) & 1
+    for k in range(1, S):
+        s_out[0].wait_event(ev_out[b][k])
+    e1.record(s_out[0])
     torch.cuda.synchronize()
     gmlp.check_device_status(stream=s_cmp)
     return e0.elapsed_time(e1) / K_steps
@@ -714,6 +732,8 @@ def main():
                     help="NVFP4: also write the columnwise (RHT) NVFP4 fc2_x each step (no-recompute training path)")
     ap.add_argument("--l2-flush", default="write", choices=["write", "clean"],
                     help="between timed steps: write 256 MiB, or write 256 MiB then read another 256 MiB")
+    ap.add_argument("--e2e-streams", type=int, default=1,
+                    help="e2e leg: copy x and y as this many row slices on as many streams per direction")
     ap.add_argument("--no-quant", dest="quant", action="store_false", help="skip the standalone quantiser leg")
     ap.add_argument("--quant-only", action="store_true",
                     help="run only the standalone NVFP4 quantiser leg and print its JSON")
