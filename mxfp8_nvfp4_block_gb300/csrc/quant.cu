@@ -91,15 +91,6 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return r;
 }
 
-__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = bf16_bits_to_float(w[i] & 0xFFFF);
-    f[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
-  }
-}
-
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
@@ -182,12 +173,14 @@ __device__ __forceinline__ f32x2 pk2(float a, float b) {
   return r;
 }
 __device__ __forceinline__ float lo2(f32x2 v) {
-  float a, b;
+  float a;
+  [[maybe_unused]] float b;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
   return a;
 }
 __device__ __forceinline__ float hi2(f32x2 v) {
-  float a, b;
+  [[maybe_unused]] float a;
+  float b;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
   return b;
 }
@@ -563,19 +556,6 @@ __global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const uint16_t*
 constexpr int kTileR = 64, kTileC = 256, kChunks = kTileR / 16;
 constexpr size_t kColSmem = (size_t)kTileR * kTileC * 2 + kTileC * 8 * kChunks + kTileC * kChunks;
 
-
-// 16 values -> 8 bytes of E2M1 codes (even element in the low nibble)
-__device__ __forceinline__ uint2 e2m1_pack16(const float* v, float enc) {
-  float p[16];
-  const f32x2 e2 = pk2(enc, enc);
-#pragma unroll
-  for (int k = 0; k < 16; k += 2) {
-    const f32x2 q = mul2(pk2(v[k], v[k + 1]), e2);
-    p[k] = lo2(q);
-    p[k + 1] = hi2(q);
-  }
-  return make_uint2(e2m1_pack8(p), e2m1_pack8(p + 8));
-}
 
 // The 16-point FWHT stages of fwht16 on two columns at once.
 __device__ __forceinline__ void fwht16x2(f32x2* w) {
