@@ -92,3 +92,26 @@ def test_recompute_fc2x_swiglu_closed_form(orc):
     assert f[0, 0] == 0
     want = as_bits(np.array([2.0 / (1.0 + np.exp(-2.0))]))[0]
     assert f[0, 1] == want
+
+
+def test_colwise_equals_rowwise_of_the_transposed_groups(orc):
+    """Random bf16 x: the columnwise MXFP8 operand of each group is the rowwise
+    MXFP8 quantiser applied to that group's transpose, zero-padded to a
+    multiple of 128 tokens (blocks of 32 tokens from the group's first)."""
+    rng = np.random.default_rng(27)
+    splits = np.array([40, 0, 130, 128, 1])
+    M, C = int(splits.sum()), 96
+    xb = torch.from_numpy(rng.standard_normal((M, C)).astype(np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+    codes, scales = orc.mxfp8_colwise(xb, splits)
+    offs, pofs = orc.group_offsets(splits), orc.padded_offsets(splits)
+    for g in range(len(splits)):
+        m, mp = int(splits[g]), int(pofs[g + 1] - pofs[g])
+        assert mp == (m + 127) // 128 * 128
+        if mp == 0:
+            continue
+        t = np.zeros((C, mp), np.uint16)
+        t[:, :m] = xb[offs[g]:offs[g + 1]].T
+        rc, rs = orc.mxfp8_quantize_rows(t)
+        assert np.array_equal(codes[:, pofs[g]:pofs[g + 1]], rc), g
+        assert np.array_equal(scales[:, pofs[g] // 32:pofs[g + 1] // 32], rs), g
