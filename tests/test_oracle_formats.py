@@ -12,7 +12,8 @@ import torch
 
 def all_finite_bf16():
     b = np.arange(65536, dtype=np.uint32).astype(np.uint16)
-    f = (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):      # NaN patterns, dropped below
+        f = (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     ok = np.isfinite(f)
     return b[ok], f[ok]
 
@@ -125,8 +126,9 @@ def test_e2m1_encode_bruteforce(orc):
 
 def test_bf16_round_matches_torch_for_float_values(orc):
     rng = np.random.default_rng(1)
-    v = np.concatenate([rng.standard_normal(50000), rng.standard_normal(5000) * 1e-39,
-                        rng.standard_normal(5000) * 1e38]).astype(np.float32)
+    with np.errstate(over="ignore"):         # values past FLT_MAX become inf on purpose
+        v = np.concatenate([rng.standard_normal(50000), rng.standard_normal(5000) * 1e-39,
+                            rng.standard_normal(5000) * 1e38]).astype(np.float32)
     mine = orc.f64_to_bf16(v.astype(np.float64))
     ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(mine, ref)
