@@ -34,6 +34,8 @@
  *     M; a negative size or a sum above M is detected on the device and
  *     reported by gmlp_check_device_status as GMLP_ERR_DEVICE_BOUNDS (no
  *     output written past M).
+ *   - Feature counts (K, N, weight rows and cols) are at most 2^20 and token
+ *     counts M below 2^31; larger values are GMLP_ERR_INVALID_DIMS.
  *   - Host-side argument checks return a status before anything is launched.
  *     No C++ exception crosses the ABI.  gmlp_last_error() describes the last
  *     non-OK status of the calling thread.

@@ -39,6 +39,12 @@ bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
+// Largest feature count (K, N, weight rows / cols) a call accepts: far past
+// any model's hidden or ffn size, and small enough that every per-row count
+// the kernels keep in 32 bits (16-byte chunks, scale blocks, TMA coordinates)
+// cannot overflow.
+constexpr int64_t kMaxFeatures = int64_t(1) << 20;
+
 gmlp_status check_device() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -202,11 +208,12 @@ static gmlp_status prepare_weights_impl(const uint16_t* const* Wp, bool discrete
                                         uint8_t* scales, float* global_scale, float* amax, cudaStream_t s) {
   if (G < 1 || G > kMaxGroups) return fail(GMLP_ERR_INVALID_DIMS, "G = %d outside [1, %d]", G, kMaxGroups);
   if (format != GMLP_MXFP8 && format != GMLP_NVFP4) return fail(GMLP_ERR_UNSUPPORTED_RECIPE, "format %d", format);
-  if (rows <= 0 || rows % 128 || (int64_t)G * rows > 0x7FFFFFFF)
-    return fail(GMLP_ERR_INVALID_DIMS, "rows = %lld must be a positive multiple of 128", (long long)rows);
+  if (rows <= 0 || rows % 128 || rows > kMaxFeatures || (int64_t)G * rows > 0x7FFFFFFF)
+    return fail(GMLP_ERR_INVALID_DIMS, "rows = %lld must be a positive multiple of 128, at most 2^20", (long long)rows);
   const int64_t cmod = format == GMLP_MXFP8 ? 128 : 256;
-  if (cols <= 0 || cols % cmod)
-    return fail(GMLP_ERR_INVALID_DIMS, "cols = %lld must be a positive multiple of %lld", (long long)cols, (long long)cmod);
+  if (cols <= 0 || cols % cmod || cols > kMaxFeatures)
+    return fail(GMLP_ERR_INVALID_DIMS, "cols = %lld must be a positive multiple of %lld, at most 2^20", (long long)cols,
+                (long long)cmod);
   if (swiglu_interleave && rows % 64) return fail(GMLP_ERR_INVALID_DIMS, "SwiGLU interleave needs rows %% 64 == 0");
   const int n_src = discrete ? G : 1;
   for (int i = 0; i < n_src; ++i)
@@ -258,7 +265,8 @@ gmlp_status gmlp_group_hadamard_amax(const uint16_t* x, int64_t M, int64_t K, co
                                      gmlp_stream stream) {
   g_last_error[0] = 0;
   GMLP_TRY(check_groups(G, M, split_sizes));
-  if (K <= 0 || K % 128) return fail(GMLP_ERR_INVALID_DIMS, "K = %lld must be a positive multiple of 128", (long long)K);
+  if (K <= 0 || K % 128 || K > kMaxFeatures)
+    return fail(GMLP_ERR_INVALID_DIMS, "K = %lld must be a positive multiple of 128, at most 2^20", (long long)K);
   if ((M > 0 && !x) || !amax_pre || !amax_post) return fail(GMLP_ERR_INVALID_ARG, "NULL pointer argument");
   if (!aligned16(x) || !aligned16(amax_pre) || !aligned16(amax_post))
     return fail(GMLP_ERR_INVALID_ARG, "pointer not 16-byte aligned");
@@ -338,7 +346,8 @@ static gmlp_status check_quant_args(const uint16_t* x, int64_t M, int64_t K, con
                                     const gmlp_qtensor* col_out) {
   GMLP_TRY(check_groups(G, M, split_sizes));
   GMLP_TRY(check_recipe(recipe));
-  if (K <= 0 || K % 128) return fail(GMLP_ERR_INVALID_DIMS, "K = %lld must be a positive multiple of 128", (long long)K);
+  if (K <= 0 || K % 128 || K > kMaxFeatures)
+    return fail(GMLP_ERR_INVALID_DIMS, "K = %lld must be a positive multiple of 128, at most 2^20", (long long)K);
   if (M > 0 && !x) return fail(GMLP_ERR_INVALID_ARG, "x is NULL");
   if (!aligned16(x)) return fail(GMLP_ERR_INVALID_ARG, "x not 16-byte aligned");
   if (!row_out && !col_out) return fail(GMLP_ERR_INVALID_ARG, "neither row_out nor col_out given");
@@ -424,8 +433,9 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     return fail(GMLP_ERR_INVALID_ARG, "tanh-SReLU needs aux->tanh_clamp_scale > 0 and finite");
   const int fmt = recipe->format;
   const int64_t n1 = act == GMLP_ACT_SWIGLU ? 2 * N : N;
-  if (K <= 0 || K % 256) return fail(GMLP_ERR_INVALID_DIMS, "K = %lld must be a positive multiple of 256", (long long)K);
-  if (N <= 0 || n1 % 256 || N % (fmt == GMLP_NVFP4 ? 256 : 128))
+  if (K <= 0 || K % 256 || K > kMaxFeatures)
+    return fail(GMLP_ERR_INVALID_DIMS, "K = %lld must be a positive multiple of 256, at most 2^20", (long long)K);
+  if (N <= 0 || n1 % 256 || N % (fmt == GMLP_NVFP4 ? 256 : 128) || N > kMaxFeatures)
     return fail(GMLP_ERR_INVALID_DIMS, "N = %lld: need fc1 width %% 256 == 0 and N %% %d == 0", (long long)N,
                 fmt == GMLP_NVFP4 ? 256 : 128);
   if (!W1 || !W2) return fail(GMLP_ERR_INVALID_ARG, "W1 / W2 NULL");
@@ -690,8 +700,8 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
   if (act != GMLP_ACT_SWIGLU && act != GMLP_ACT_SRELU)
     return fail(GMLP_ERR_INVALID_ARG, "backward act = %d: SwiGLU or SReLU", act);
   const int64_t N1 = act == GMLP_ACT_SWIGLU ? 2 * N : N;
-  if (K <= 0 || K % 256 || N <= 0 || N % 256)
-    return fail(GMLP_ERR_INVALID_DIMS, "K = %lld, N = %lld: both positive multiples of 256", (long long)K,
+  if (K <= 0 || K % 256 || N <= 0 || N % 256 || K > kMaxFeatures || N > kMaxFeatures)
+    return fail(GMLP_ERR_INVALID_DIMS, "K = %lld, N = %lld: both positive multiples of 256, at most 2^20", (long long)K,
                 (long long)N);
   if (!W2t || !W1t || W2t->G != G || W1t->G != G || W2t->format != GMLP_MXFP8 || W1t->format != GMLP_MXFP8)
     return fail(GMLP_ERR_INVALID_ARG, "W2t / W1t: MXFP8 weights of G experts");
@@ -841,8 +851,8 @@ gmlp_status gmlp_backward_wgrad(const uint16_t* x, const uint16_t* dy, const uin
     return fail(GMLP_ERR_INVALID_ARG, "n_stage_events = %d: 0..6, stage_events non-NULL", n_stage_events);
   if (accumulate != 0 && accumulate != 1) return fail(GMLP_ERR_INVALID_ARG, "accumulate = %d: 0 or 1", accumulate);
   const int64_t N1 = act == GMLP_ACT_SWIGLU ? 2 * N : N;
-  if (K <= 0 || K % 256 || N <= 0 || N % 256)
-    return fail(GMLP_ERR_INVALID_DIMS, "K = %lld, N = %lld: both positive multiples of 256", (long long)K,
+  if (K <= 0 || K % 256 || N <= 0 || N % 256 || K > kMaxFeatures || N > kMaxFeatures)
+    return fail(GMLP_ERR_INVALID_DIMS, "K = %lld, N = %lld: both positive multiples of 256, at most 2^20", (long long)K,
                 (long long)N);
   const bool want1 = dW1 || dbias1, want2 = dW2 || dbias2;
   if (M > 0 && ((want2 && !dy) || (dW2 && !pre_act) || (want1 && !fc1_dy) || (dW1 && !x)))
@@ -928,7 +938,8 @@ gmlp_status gmlp_replicate_weight_scales(const uint8_t* tiled, int32_t G, int64_
   g_last_error[0] = 0;
   if (!tiled || !out || !aligned16(tiled) || !aligned16(out))
     return fail(GMLP_ERR_INVALID_ARG, "tiled / out NULL or not 16-byte aligned");
-  if (G < 1 || G > kMaxGroups || rows <= 0 || cols <= 0 || rows % 256 || cols % 256)
+  if (G < 1 || G > kMaxGroups || rows <= 0 || cols <= 0 || rows % 256 || cols % 256 || rows > kMaxFeatures ||
+      cols > kMaxFeatures)
     return fail(GMLP_ERR_INVALID_DIMS, "G = %d, rows = %lld, cols = %lld: need 1 <= G <= %d, rows and cols %% 256 == 0",
                 G, (long long)rows, (long long)cols, kMaxGroups);
   GMLP_TRY(check_device());

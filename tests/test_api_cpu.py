@@ -311,3 +311,40 @@ def test_query_layout_matches_the_oracles_layouts(lib, orc):
     assert g.query_layout(g.LAYOUT_COLWISE_SCALE, splits, 96, 0, 0) == -1     # not a multiple of 128
     assert g.query_layout(7, splits, ks, 0, 0) == -1
     assert g.query_layout(g.LAYOUT_TILED_SCALE, [4, -1], ks, 0, 0) == -1
+
+
+def test_feature_counts_above_2_to_20_are_rejected(lib):
+    """K, N and weight rows / cols above 2^20 are INVALID_DIMS in every call
+    that takes them; 2^20 itself passes the dimension checks (the call then
+    stops at a later check, never at the size)."""
+    L, g = lib
+    big, top = (1 << 20) + 256, 1 << 20
+    r = g.recipe(g.MXFP8)
+    qt = g.QTensor(FAKE, FAKE)
+    assert L.gmlp_group_quantize(FAKE, 64, big, FAKE, 2, ctypes.byref(r), ctypes.byref(qt), None, None, None,
+                                 None) == g.ERR_INVALID_DIMS
+    assert L.gmlp_group_quantize(FAKE, 64, top, FAKE, 2, ctypes.byref(r), ctypes.byref(qt), None, None, None,
+                                 None) != g.ERR_INVALID_DIMS
+    assert L.gmlp_group_quantize_with_amax(FAKE, 64, big, FAKE, 2, ctypes.byref(r), None, None, ctypes.byref(qt),
+                                           None, None) == g.ERR_INVALID_DIMS
+    assert L.gmlp_group_hadamard_amax(FAKE, 64, big, FAKE, 2, 0, FAKE, FAKE, None) == g.ERR_INVALID_DIMS
+    assert L.gmlp_group_hadamard_amax(FAKE, 64, top, FAKE, 2, 0, FAKE, FAKE, None) != g.ERR_INVALID_DIMS
+    assert L.gmlp_prepare_weights(FAKE, 1, big, 256, 0, g.MXFP8, FAKE, FAKE, None, None, None) == g.ERR_INVALID_DIMS
+    assert L.gmlp_prepare_weights(FAKE, 1, 256, big, 0, g.MXFP8, FAKE, FAKE, None, None, None) == g.ERR_INVALID_DIMS
+    assert L.gmlp_prepare_weights(FAKE, 1, top, top, 0, g.MXFP8, FAKE, FAKE, None, None, None) != g.ERR_INVALID_DIMS
+    assert L.gmlp_replicate_weight_scales(FAKE, 1, big, 256, FAKE, None) == g.ERR_INVALID_DIMS
+    assert L.gmlp_replicate_weight_scales(FAKE, 1, 256, top, FAKE, None) != g.ERR_INVALID_DIMS
+    for K, N in ((big, 256), (256, big)):
+        w1 = g.QWeightC(FAKE, FAKE, None, 2 * N, K, 1, g.MXFP8, 1, 0)
+        w2 = g.QWeightC(FAKE, FAKE, None, K, N, 1, g.MXFP8, 0, 0)
+        assert L.gmlp_forward(FAKE, 64, K, N, FAKE, 1, ctypes.byref(w1), ctypes.byref(w2), None, g.SWIGLU,
+                              ctypes.byref(r), FAKE, None, FAKE, 1 << 40, None) == g.ERR_INVALID_DIMS
+        assert L.gmlp_backward_dgrad(FAKE, 64, K, N, FAKE, 1, ctypes.byref(w2), ctypes.byref(w1), FAKE, None,
+                                     g.SWIGLU, ctypes.byref(r), FAKE, None, None, None, None, FAKE, 1 << 40, None, 0,
+                                     None) == g.ERR_INVALID_DIMS
+        assert L.gmlp_backward_wgrad(FAKE, FAKE, FAKE, None, FAKE, 64, K, N, FAKE, 1, g.SWIGLU, FAKE, FAKE, None,
+                                     None, 0, FAKE, 1 << 40, None, 0, None) == g.ERR_INVALID_DIMS
+    w1 = g.QWeightC(FAKE, FAKE, None, 2 * top, top, 1, g.MXFP8, 1, 0)
+    w2 = g.QWeightC(FAKE, FAKE, None, top, top, 1, g.MXFP8, 0, 0)
+    assert L.gmlp_forward(FAKE, 64, top, top, FAKE, 1, ctypes.byref(w1), ctypes.byref(w2), None, g.SWIGLU,
+                          ctypes.byref(r), FAKE, None, FAKE, 1 << 40, None) != g.ERR_INVALID_DIMS
