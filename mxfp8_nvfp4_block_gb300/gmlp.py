@@ -120,7 +120,32 @@ def _check(st: int) -> None:
 
 
 def _p(t) -> int | None:
-    return None if t is None else t.data_ptr()
+    """Device address of a CUDA tensor (None stays NULL).  A host tensor is
+    refused here: the kernels would dereference its host address."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"expected a torch.Tensor, got {type(t).__name__}")
+    if not t.is_cuda:
+        raise ValueError("gmlp takes device tensors: got a tensor on " + str(t.device))
+    return t.data_ptr()
+
+
+def _splits_p(splits: torch.Tensor) -> int:
+    """split_sizes: a contiguous 1-D int64 CUDA tensor (it stays on the device)."""
+    if not isinstance(splits, torch.Tensor) or splits.dtype != torch.int64 or splits.dim() != 1 \
+            or not splits.is_contiguous():
+        raise ValueError("split sizes must be a contiguous 1-D int64 tensor on the device")
+    return _p(splits)
+
+
+def _probs_p(probs, M: int) -> int | None:
+    """probs: None (all ones) or a contiguous float32 CUDA tensor of at least M values."""
+    if probs is None:
+        return None
+    if probs.dtype != torch.float32 or not probs.is_contiguous() or probs.numel() < M:
+        raise ValueError(f"probs must be a contiguous float32 tensor of at least {M} values")
+    return _p(probs)
 
 
 def _stream(stream=None) -> int:
@@ -141,7 +166,10 @@ def _u8(n, device):
 
 
 def _bits(x: torch.Tensor) -> torch.Tensor:
-    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous()
+    """A bf16 operand: contiguous, on the device."""
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or not x.is_contiguous():
+        raise ValueError("expected a contiguous bf16 tensor")
+    _p(x)
     return x
 
 
@@ -154,7 +182,7 @@ def group_hadamard_amax(x: torch.Tensor, splits: torch.Tensor, mask: int, stream
     G = splits.numel()
     pre = torch.empty(G, dtype=torch.float32, device=x.device)
     post = torch.empty(G, dtype=torch.float32, device=x.device)
-    _check(load().gmlp_group_hadamard_amax(_p(x), M, K, _p(splits), G, mask, _p(pre), _p(post), _stream(stream)))
+    _check(load().gmlp_group_hadamard_amax(_p(x), M, K, _splits_p(splits), G, mask, _p(pre), _p(post), _stream(stream)))
     return pre, post
 
 
@@ -200,7 +228,7 @@ def group_quantize_with_amax(x, splits, rec: Recipe, amax_pre=None, amax_post=No
     row = QTensor(bufs["row"][0].data_ptr(), bufs["row"][1].data_ptr()) if rowwise else None
     col = QTensor(bufs["col"][0].data_ptr(), bufs["col"][1].data_ptr()) if columnwise else None
     _check(load().gmlp_group_quantize_with_amax(
-        _p(x), M, K, _p(splits), G, ctypes.byref(rec), _p(amax_pre), _p(amax_post),
+        _p(x), M, K, _splits_p(splits), G, ctypes.byref(rec), _p(amax_pre), _p(amax_post),
         ctypes.byref(row) if row else None, ctypes.byref(col) if col else None, _stream(stream)))
     return bufs
 
@@ -219,7 +247,7 @@ def group_quantize(x, splits, rec: Recipe, *, rowwise=True, columnwise=False, sp
     row = QTensor(bufs["row"][0].data_ptr(), bufs["row"][1].data_ptr()) if rowwise else None
     col = QTensor(bufs["col"][0].data_ptr(), bufs["col"][1].data_ptr()) if columnwise else None
     _check(load().gmlp_group_quantize(
-        _p(x), M, K, _p(splits), G, ctypes.byref(rec), ctypes.byref(row) if row else None,
+        _p(x), M, K, _splits_p(splits), G, ctypes.byref(rec), ctypes.byref(row) if row else None,
         ctypes.byref(col) if col else None, _p(pre), _p(post), _stream(stream)))
     return bufs
 
@@ -327,7 +355,7 @@ def forward(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *
             aux_c.stage_events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))
             aux_c.n_stage_events = len(events)
     w1c, w2c = W1.c(), W2.c()
-    _check(load().gmlp_forward(_p(x), M, K, N, _p(splits), G, ctypes.byref(w1c), ctypes.byref(w2c), _p(probs),
+    _check(load().gmlp_forward(_p(x), M, K, N, _splits_p(splits), G, ctypes.byref(w1c), ctypes.byref(w2c), _probs_p(probs, M),
                                act, ctypes.byref(rec), _p(y), ctypes.byref(aux_c) if aux_c else None,
                                _p(workspace), workspace.numel(), _stream(stream)))
     return y
@@ -344,8 +372,8 @@ def forward_noalloc(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: R
         y = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
     w1c, w2c = W1.c(), W2.c()
     aux_c = FwdAux(tanh_clamp_scale=float(tanh_clamp_scale)) if act == TANH_SRELU else None
-    _check(load().gmlp_forward_noalloc(_p(x), M, K, W2.cols, _p(splits), G, ctypes.byref(w1c), ctypes.byref(w2c),
-                                       _p(probs), act, ctypes.byref(rec), _p(y),
+    _check(load().gmlp_forward_noalloc(_p(x), M, K, W2.cols, _splits_p(splits), G, ctypes.byref(w1c), ctypes.byref(w2c),
+                                       _probs_p(probs, M), act, ctypes.byref(rec), _p(y),
                                        ctypes.byref(aux_c) if aux_c else None, _stream(stream)))
     return y
 
@@ -388,8 +416,8 @@ def backward_dgrad(dy, splits, W2t: "QWeight", W1t: "QWeight", pre_act, probs, a
         workspace = _u8(need, dy.device)
     fc1_dy = fc1_dy or {}
     ev_arr = _event_handles(events) if events else None
-    _check(load().gmlp_backward_dgrad(_p(dy), M, K, N, _p(splits), G, ctypes.byref(W2t.c()), ctypes.byref(W1t.c()),
-                                      _p(pre_act), _p(probs), act, ctypes.byref(rec), _p(dx), _p(dprob),
+    _check(load().gmlp_backward_dgrad(_p(dy), M, K, N, _splits_p(splits), G, ctypes.byref(W2t.c()), ctypes.byref(W1t.c()),
+                                      _p(pre_act), _probs_p(probs, M), act, ctypes.byref(rec), _p(dx), _p(dprob),
                                       _p(fc1_dy.get("codes")), _p(fc1_dy.get("scales")), _p(fc1_dy_bf16),
                                       _p(workspace),
                                       workspace.numel(), ev_arr, len(events or ()), _stream(stream)))
@@ -417,8 +445,8 @@ def backward_wgrad(x, dy, pre_act, probs, fc1_dy, splits, act: int, *, dW1=None,
     need = load().gmlp_backward_wgrad_workspace_size(M, K, N, G, act)
     if workspace is None:
         workspace = _u8(need, dev)
-    _check(load().gmlp_backward_wgrad(_p(x), _p(dy), _p(_bits(pre_act) if pre_act is not None else None), _p(probs),
-                                      _p(fc1_dy), M, K, N, _p(splits), G, act, _p(out["dW1"]), _p(out["dW2"]),
+    _check(load().gmlp_backward_wgrad(_p(x), _p(dy), _p(_bits(pre_act) if pre_act is not None else None), _probs_p(probs, M),
+                                      _p(fc1_dy), M, K, N, _splits_p(splits), G, act, _p(out["dW1"]), _p(out["dW2"]),
                                       _p(out["dbias1"]), _p(out["dbias2"]), int(bool(accumulate)), _p(workspace),
                                       workspace.numel(), _event_handles(events) if events else None,
                                       len(events or ()), _stream(stream)))

@@ -348,3 +348,28 @@ def test_feature_counts_above_2_to_20_are_rejected(lib):
     w2 = g.QWeightC(FAKE, FAKE, None, top, top, 1, g.MXFP8, 0, 0)
     assert L.gmlp_forward(FAKE, 64, top, top, FAKE, 1, ctypes.byref(w1), ctypes.byref(w2), None, g.SWIGLU,
                           ctypes.byref(r), FAKE, None, FAKE, 1 << 40, None) != g.ERR_INVALID_DIMS
+
+
+def test_binding_refuses_host_and_mistyped_tensors(lib):
+    """The binding passes device addresses only: a host tensor, split sizes
+    that are not int64, or probs that are not float32 (or too short) raise
+    before anything reaches the library (a kernel would otherwise dereference
+    a host address or misread the buffer)."""
+    import torch
+    _, g = lib
+    x = torch.zeros((64, 128), dtype=torch.bfloat16)          # host memory
+    with pytest.raises(ValueError, match="device"):
+        g.group_hadamard_amax(x, torch.tensor([64]), 0)
+    with pytest.raises(ValueError):
+        g.forward(x.float(), torch.tensor([64]), None, None, None, g.SWIGLU, g.recipe(g.MXFP8))
+    with pytest.raises(ValueError, match="int64"):
+        g._splits_p(torch.tensor([64], dtype=torch.int32))
+    with pytest.raises(ValueError, match="device"):
+        g._splits_p(torch.tensor([64]))
+    with pytest.raises(ValueError, match="float32"):
+        g._probs_p(torch.ones(64, dtype=torch.float64), 64)
+    with pytest.raises(ValueError, match="at least 64"):
+        g._probs_p(torch.ones(32), 64)
+    with pytest.raises(TypeError):
+        g._p([1, 2, 3])
+    assert g._p(None) is None and g._probs_p(None, 64) is None
