@@ -59,6 +59,15 @@ def fc1_traffic(workload: str):
     return FC1_TRAFFIC.get((workload, digest))
 
 
+def oracle_threads() -> int:
+    """Threads the oracle runs on: the host cores this process may use, capped
+    by OMP_NUM_THREADS when it is set (torchrun sets it to 1 per rank), which
+    both numpy's BLAS and the oracle's OpenMP loops follow."""
+    n = len(os.sched_getaffinity(0))
+    v = os.environ.get("OMP_NUM_THREADS", "")
+    return min(n, int(v)) if v.isdigit() and int(v) > 0 else n
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -620,7 +629,7 @@ def oracle_sample(name: str, target_s: float = 10.0, max_reps: int = 3) -> dict:
         el = time.time() - t0
         if el >= target_s or reps >= max_reps:
             break
-    cores = len(os.sched_getaffinity(0))
+    cores = oracle_threads()
     return {"value": round(reps * w.flops / el / 1e12, 5), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{reps} full forward(s) of {name} (all {w.M} tokens; weights pre-quantised), "
                       f"{el:.1f} s, numpy float64 GEMMs + C format arithmetic"}
@@ -662,7 +671,7 @@ def oracle_backward_sample(name: str, max_tokens: int = 16384, max_experts: int 
             break
     m = len(rows)
     flops = reps * 2 * (2.0 * m * w.K * w.N + 2.0 * m * w.n1 * w.K)
-    cores = len(os.sched_getaffinity(0))
+    cores = oracle_threads()
     return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{reps} backward(s) of experts {picked} of {name} ({m} tokens): backward_dgrad + "
                       f"backward_wgrad (weights quantised inside), {el:.1f} s, numpy float64 GEMMs + C format "
@@ -704,7 +713,7 @@ def run_reference(args) -> dict:
         step()
     el = time.time() - t0
     v = flops * args.steps / el / 1e12
-    cores = len(os.sched_getaffinity(0))
+    cores = oracle_threads()
     sample = (f"{len(rows)} random rows of the {w.M} tokens per step" if rows is not None
               else f"all {w.M} tokens per step")
     return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,

@@ -67,3 +67,5 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     for k in ("metric", "value", "unit", "ms_per_step", "higher_is_better", "config", "cpu_baseline", "e2e"):
         assert k in d, k
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    # torchrun limits each rank to one OpenMP / BLAS thread, and the line says so
+    assert d["cpu_baseline"]["cores"] == 1
