@@ -17,7 +17,7 @@ HEADERS = ["device.cuh", "internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
-         "-I", os.path.join(ROOT, "include")]
+         "-Xcompiler", "-Wall", "-Xcompiler", "-Wextra", "-I", os.path.join(ROOT, "include")]
 
 
 def nvcc() -> str:
