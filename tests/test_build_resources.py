@@ -1,7 +1,8 @@
 """Resource use of the kernels on the measured path, from ptxas's own report of
 this build (CPU: nvcc cross-compiles for sm_103a): the sources compile without
-warnings (device code, and host code under -Wall -Wextra), and the GEMM, dGLU and NVFP4 cast instantiations that the forward
-and backward time keep every value in registers (no spill stores or loads)."""
+warnings (device code, and host code under -Wall -Wextra), and the GEMM, dGLU
+and NVFP4 cast instantiations that the forward and backward time keep every
+value in registers (no spill stores or loads)."""
 import os
 import re
 import subprocess
