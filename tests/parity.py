@@ -42,6 +42,18 @@ def nv_dequant(codes: np.ndarray, scales: np.ndarray, S) -> np.ndarray:
     return e2m1_value(nib) * sf / np.asarray(S, np.float64).reshape(-1, 1)
 
 
+def nvfp4_scale_of(amax) -> np.float32:
+    """The FP32 global scale a GPU-side amax implies (448 * 6 / amax, 1 for a zero
+    amax, FLT_MAX past the range), to dequantise the CUDA path's NVFP4 codes with
+    its own scale; the oracle's scales come from the oracle alone."""
+    a = np.float32(amax)
+    if a == 0:
+        return np.float32(1.0)
+    with np.errstate(over="ignore", divide="ignore"):
+        S = np.float32(2688.0) / a
+    return np.float32(np.finfo(np.float32).max) if np.isinf(S) else np.float32(S)
+
+
 def code_match_report(fmt: int, g_codes, o_codes, g_scales, o_scales, g_S=None, o_S=None, rows=None):
     """Fraction of identical codes, and the largest distance of a mismatched
     value in code steps at the coarser of the two block scales (c18 reading:

@@ -74,12 +74,11 @@ def test_backward_dgrad_parity(orc, gm, act):
     splits = torch.tensor(splits_l, dtype=torch.int64)
     W1 = bf16_cpu(rng.standard_normal((G, n1, K)) / np.sqrt(K))
     W2 = bf16_cpu(rng.standard_normal((G, K, N)) / np.sqrt(N))
-    probs = torch.from_numpy(rng.uniform(0.1, 1, M).astype(np.float32)).cuda()
-    h = bf16_cpu(1.5 * rng.standard_normal((M, n1))).cuda()   # the saved activation input (pre-activations)
+    probs_h = torch.from_numpy(rng.uniform(0.1, 1, M).astype(np.float32))
+    h_host = bf16_cpu(1.5 * rng.standard_normal((M, n1)))   # the saved activation input (pre-activations)
     dy = bf16_cpu(rng.standard_normal((M, K)))
-    dx, dprob, fc1 = run_backward(gm, dy, splits, W1, W2, h, probs, act)
-    hb = np_bits(h)
-    ref = orc.backward_dgrad(bits(dy), np.array(splits_l), bits(W1), bits(W2), hb, probs.cpu().numpy(), act)
+    dx, dprob, fc1 = run_backward(gm, dy, splits, W1, W2, h_host.cuda(), probs_h.cuda(), act)
+    ref = orc.backward_dgrad(bits(dy), np.array(splits_l), bits(W1), bits(W2), bits(h_host), probs_h.numpy(), act)
     fb = np_bits(fc1["bf16"])
     bmatch = float(np.mean(fb == ref["fc1_dy"]))
     print(f"fc1_dy bf16 match {bmatch:.6f}")
@@ -106,11 +105,11 @@ def test_backward_dgrad_lossless_bitexact(orc, gm):
     for g in range(G):
         W2[g, rng.integers(0, K, N), np.arange(N)] = 1.0
         W1[g, np.arange(N), rng.integers(0, K, N)] = 1.0
-    h = bf16_cpu(rng.choice([0.0, 1.0, -1.0, 2.0], size=(M, N))).cuda()
+    h_host = bf16_cpu(rng.choice([0.0, 1.0, -1.0, 2.0], size=(M, N)))
     dy = bf16_cpu(rng.choice([0.0, 1.0, -1.0], size=(M, K)))
-    dx, dprob, fc1 = run_backward(gm, dy, splits, bf16_cpu(W1), bf16_cpu(W2), h, None, 1)
-    hb = h.cpu().view(torch.int16).numpy().view(np.uint16)
-    ref = orc.backward_dgrad(bits(dy), np.array(splits_l), bits(bf16_cpu(W1)), bits(bf16_cpu(W2)), hb, None, 1)
+    dx, dprob, fc1 = run_backward(gm, dy, splits, bf16_cpu(W1), bf16_cpu(W2), h_host.cuda(), None, 1)
+    ref = orc.backward_dgrad(bits(dy), np.array(splits_l), bits(bf16_cpu(W1)), bits(bf16_cpu(W2)), bits(h_host),
+                             None, 1)
     assert np.array_equal(np_u8(fc1["codes"], M * N).reshape(M, N), ref["fc1_dy_codes"])
     assert np.array_equal(np_bits(dx), ref["dx"])
     assert np.array_equal(dprob.cpu().numpy().astype(np.float64), ref["dprob"])
@@ -127,11 +126,11 @@ def test_backward_dgrad_many_tiny_groups(orc, gm):
     splits = torch.tensor(splits_l, dtype=torch.int64)
     W1 = bf16_cpu(rng.standard_normal((G, 2 * N, K)) / np.sqrt(K))
     W2 = bf16_cpu(rng.standard_normal((G, K, N)) / np.sqrt(N))
-    probs = torch.from_numpy(rng.uniform(0.1, 1, M).astype(np.float32)).cuda()
-    h = bf16_cpu(1.5 * rng.standard_normal((M, 2 * N))).cuda()
+    probs_h = torch.from_numpy(rng.uniform(0.1, 1, M).astype(np.float32))
+    h_host = bf16_cpu(1.5 * rng.standard_normal((M, 2 * N)))
     dy = bf16_cpu(rng.standard_normal((M, K)))
-    dx, dprob, fc1 = run_backward(gm, dy, splits, W1, W2, h, probs, 0)
-    ref = orc.backward_dgrad(bits(dy), np.array(splits_l), bits(W1), bits(W2), np_bits(h), probs.cpu().numpy(), 0)
+    dx, dprob, fc1 = run_backward(gm, dy, splits, W1, W2, h_host.cuda(), probs_h.cuda(), 0)
+    ref = orc.backward_dgrad(bits(dy), np.array(splits_l), bits(W1), bits(W2), bits(h_host), probs_h.numpy(), 0)
     assert frob(dx.float().cpu().numpy(), orc.bf16_to_f64(ref["dx"])) <= 1e-2
     assert frob(dprob.cpu().numpy(), ref["dprob"]) <= 1e-2
     assert float(np.mean(np_bits(fc1["bf16"]) == ref["fc1_dy"])) >= 0.99

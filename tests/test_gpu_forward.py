@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from mxfp8_nvfp4_block_gb300.inputs import WORKLOADS, bits, make_inputs
-from parity import code_match_report, frob, np_bits, np_u8
+from parity import code_match_report, frob, np_bits, np_u8, nvfp4_scale_of
 
 pytestmark = pytest.mark.gpu
 
@@ -107,7 +107,7 @@ def test_forward_lossless_bitexact(orc, gm, fmt, act, gemm_mode):
                                         orc.tiled_to_compact(np_u8(aux["fc2x_scales"]), splits, N // (32 if fmt == 0 else 16)),
                                         ref["fc2x_scales"],
                                         g_S=None if fmt == 0 else np.repeat(
-                                            [orc.nvfp4_global_scale(a) for a in aux["fc2x_amax_pre"].cpu().numpy()], splits),
+                                            [nvfp4_scale_of(a) for a in aux["fc2x_amax_pre"].cpu().numpy()], splits),
                                         o_S=None if fmt == 0 else np.repeat(ref["fc2x_S"], splits))
         assert frac >= CODE_MATCH and steps <= 1.0 + 1e-9, (frac, steps)
         assert frob(y.float().cpu().numpy(), orc.bf16_to_f64(ref["y"])) <= Y_TOL
@@ -136,15 +136,14 @@ def test_forward_nvfp4_x4_scales_match_tiled(gm, act):
 @pytest.mark.parametrize("use_rht", [True, False])
 def test_forward_nvfp4_columnwise_fc2x(orc, gm, use_rht):
     """The forward's optional columnwise NVFP4 fc2_x (no-recompute training
-    path): bit-exact against the oracle's quantize-with-amax of the GPU's own
-    bf16 fc2_x and fused amaxes; fc2's rowwise operand and y are unchanged."""
-    rng = np.random.default_rng(31)
+    path) on lossless operands (one-hot fc1 weights, x from {0, +-2, +-4},
+    prob 1: fc2_x is exact, and so are its amaxes and every RHT value):
+    bit-exact against the oracle's quantize-with-amax of the oracle forward's
+    own fc2_x and amaxes; fc2's rowwise operand and y are unchanged by the
+    extra output."""
     splits, K, N = [130, 0, 257, 5, 1, 128, 700], 512, 512
     G, M = len(splits), sum(splits)
-    d = dict(x=bf16_cpu(rng.standard_normal((M, K))), splits=torch.tensor(splits, dtype=torch.int64),
-             W1=bf16_cpu(rng.standard_normal((G, N, K)) / np.sqrt(K)),
-             W2=bf16_cpu(rng.standard_normal((G, K, N)) / np.sqrt(N)),
-             probs=torch.from_numpy(rng.uniform(0, 1, M).astype(np.float32)))
+    d = onehot_case(1, 1, splits, K, N, seed=31)
     mask = 0x5AC3
     y0, a0 = run_gpu(gm, d, 1, 1, mask=mask)
     w1 = gm.prepare_weights(d["W1"].cuda(), gm.NVFP4)
@@ -159,11 +158,14 @@ def test_forward_nvfp4_columnwise_fc2x(orc, gm, use_rht):
     gm.check_device_status()
     assert np.array_equal(np_bits(y), np_bits(y0))
     assert torch.equal(aux["fc2x_codes"], a0["fc2x_codes"]) and torch.equal(aux["fc2x_scales"], a0["fc2x_scales"])
-    fx = aux["fc2x_bf16"].cpu().view(torch.int16).numpy().view(np.uint16)
-    pre = aux["fc2x_amax_pre"].cpu().numpy()
-    post = aux["fc2x_amax_post"].cpu().numpy()
-    ref = orc.group_quantize_with_amax(fx, np.array(splits), orc.NVFP4, pre, post, rowwise=False, columnwise=True,
-                                       use_rht=use_rht, mask=mask)
+    fwd = orc.forward(bits(d["x"]), np.array(splits), bits(d["W1"]), bits(d["W2"]), d["probs"].numpy(), 1, 1,
+                      rht_mask=mask)
+    assert np.array_equal(np_bits(aux["fc2x_bf16"]), fwd["fc2x"])             # the lossless premise
+    assert np.array_equal(aux["fc2x_amax_pre"].cpu().numpy(), fwd["fc2x_amax_pre"])
+    assert np.array_equal(aux["fc2x_amax_post"].cpu().numpy(), fwd["fc2x_amax_post"])
+    ref = orc.group_quantize_with_amax(fwd["fc2x"], np.array(splits), orc.NVFP4, fwd["fc2x_amax_pre"],
+                                       fwd["fc2x_amax_post"], rowwise=False, columnwise=True, use_rht=use_rht,
+                                       mask=mask)
     nb = len(ref["col_codes"])
     assert np.array_equal(np_u8(aux["fc2x_col_codes"], nb), ref["col_codes"])
     assert np.array_equal(np_u8(aux["fc2x_col_scales"], len(ref["col_scales"])), ref["col_scales"])
@@ -273,7 +275,7 @@ def forward_parity(orc, gm, name, rows=None, gemm_mode=0):
     gS = oS = None
     if w.fmt == 1:
         gpre = aux["fc2x_amax_pre"].cpu().numpy()
-        gS = np.repeat([orc.nvfp4_global_scale(a) for a in gpre], splits)
+        gS = np.repeat([nvfp4_scale_of(a) for a in gpre], splits)
         oS = np.repeat(ref["fc2x_S"], splits)
     frac, steps = code_match_report(w.fmt, g_codes, ref["fc2x_codes"], g_scales, ref["fc2x_scales"], gS, oS, rows=sel)
     err = frob(y.float().cpu().numpy()[sel], orc.bf16_to_f64(ref["y"])[sel])
@@ -328,7 +330,7 @@ def test_forward_tanh_srelu_small(orc, gm, fmt):
     cdiv, blk = (1, 32) if fmt == 0 else (2, 16)
     gS = oS = None
     if fmt == 1:
-        gS = np.repeat([orc.nvfp4_global_scale(a) for a in aux["fc2x_amax_pre"].cpu().numpy()], splits)
+        gS = np.repeat([nvfp4_scale_of(a) for a in aux["fc2x_amax_pre"].cpu().numpy()], splits)
         oS = np.repeat(ref["fc2x_S"], splits)
     frac, steps = code_match_report(fmt, np_u8(aux["fc2x_codes"], M * N // cdiv).reshape(M, -1), ref["fc2x_codes"],
                                     orc.tiled_to_compact(np_u8(aux["fc2x_scales"]), splits, N // blk),
