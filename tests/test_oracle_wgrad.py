@@ -115,3 +115,19 @@ def test_colwise_equals_rowwise_of_the_transposed_groups(orc):
         rc, rs = orc.mxfp8_quantize_rows(t)
         assert np.array_equal(codes[:, pofs[g]:pofs[g + 1]], rc), g
         assert np.array_equal(scales[:, pofs[g] // 32:pofs[g + 1] // 32], rs), g
+
+
+def test_recompute_fc2x_equals_the_forward_fc2x(orc):
+    """The weight gradient's fc2_x, rebuilt from the forward's saved activation
+    input h, is the forward's own fc2_x bit for bit (SwiGLU and SReLU, MXFP8,
+    random operands): the rebuild reads h in logical column order and applies
+    the prob and the bf16 rounding exactly where the forward does."""
+    from mxfp8_nvfp4_block_gb300.inputs import bits, make_inputs
+    d = make_inputs("tiny")
+    for act in (orc.SWIGLU, orc.SRELU):
+        W1 = d["W1"] if act == orc.SWIGLU else d["W1"][:, :d["W2"].shape[2]].contiguous()
+        fwd = orc.forward(bits(d["x"]), d["splits"].numpy(), bits(W1), bits(d["W2"]), d["probs"].numpy(), act,
+                          orc.MXFP8)
+        again = orc.recompute_fc2x(fwd["h"], d["probs"].numpy(), act)
+        assert np.array_equal(again, fwd["fc2x"]), act
+        assert np.count_nonzero(fwd["fc2x"]) > fwd["fc2x"].size // 4
