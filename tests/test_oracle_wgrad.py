@@ -118,16 +118,27 @@ def test_colwise_equals_rowwise_of_the_transposed_groups(orc):
 
 
 def test_recompute_fc2x_equals_the_forward_fc2x(orc):
-    """The weight gradient's fc2_x, rebuilt from the forward's saved activation
-    input h, is the forward's own fc2_x bit for bit (SwiGLU and SReLU, MXFP8,
-    random operands): the rebuild reads h in logical column order and applies
-    the prob and the bf16 rounding exactly where the forward does."""
+    """fc2_x rebuilt from the forward's saved activation input h is the
+    forward's own fc2_x bit for bit (SwiGLU and SReLU, MXFP8 and NVFP4, random
+    operands): the rebuild reads h in logical column order and applies the prob
+    and the bf16 rounding exactly where the forward does.  For NVFP4 this is
+    the pages' recompute on / off equality (PR #3837, Description): the rebuilt
+    tensor, cast column-wise with the forward's saved amaxes, gives the same
+    codes and scales as the forward's own fc2_x."""
     from mxfp8_nvfp4_block_gb300.inputs import bits, make_inputs
     d = make_inputs("tiny")
-    for act in (orc.SWIGLU, orc.SRELU):
-        W1 = d["W1"] if act == orc.SWIGLU else d["W1"][:, :d["W2"].shape[2]].contiguous()
-        fwd = orc.forward(bits(d["x"]), d["splits"].numpy(), bits(W1), bits(d["W2"]), d["probs"].numpy(), act,
-                          orc.MXFP8)
-        again = orc.recompute_fc2x(fwd["h"], d["probs"].numpy(), act)
-        assert np.array_equal(again, fwd["fc2x"]), act
-        assert np.count_nonzero(fwd["fc2x"]) > fwd["fc2x"].size // 4
+    sp = d["splits"].numpy()
+    for fmt in (orc.MXFP8, orc.NVFP4):
+        for act in (orc.SWIGLU, orc.SRELU):
+            W1 = d["W1"] if act == orc.SWIGLU else d["W1"][:, :d["W2"].shape[2]].contiguous()
+            fwd = orc.forward(bits(d["x"]), sp, bits(W1), bits(d["W2"]), d["probs"].numpy(), act, fmt,
+                              rht_mask=0x2D4B)
+            again = orc.recompute_fc2x(fwd["h"], d["probs"].numpy(), act)
+            assert np.array_equal(again, fwd["fc2x"]), (fmt, act)
+            assert np.count_nonzero(fwd["fc2x"]) > fwd["fc2x"].size // 4
+            if fmt == orc.NVFP4:
+                on, off = (orc.group_quantize_with_amax(t, sp, orc.NVFP4, fwd["fc2x_amax_pre"],
+                                                        fwd["fc2x_amax_post"], rowwise=True, columnwise=True,
+                                                        use_rht=True, mask=0x2D4B) for t in (again, fwd["fc2x"]))
+                for k in ("row_codes", "row_scales", "col_codes", "col_scales"):
+                    assert np.array_equal(on[k], off[k]), k
