@@ -352,6 +352,9 @@ GMLP_API gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64
  * nothing: the caller still provides x, y, the weights and the aux outputs.
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.
+ * The address is kept for the life of the process: after cudaDeviceReset (or
+ * anything else that destroys the device's primary context) it is stale, so
+ * do not call the library on that device again in that process.
  * All calls share the one array and it keeps the previous call's contents
  * (the forward zeroes what it accumulates into), so calls whose work overlaps
  * on the GPU -- on different streams, or from different threads -- race; keep

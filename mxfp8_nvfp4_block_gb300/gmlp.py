@@ -10,6 +10,7 @@ import ctypes
 import os
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -146,6 +147,40 @@ def _probs_p(probs, M: int) -> int | None:
     if probs.dtype != torch.float32 or not probs.is_contiguous() or probs.numel() < M:
         raise ValueError(f"probs must be a contiguous float32 tensor of at least {M} values")
     return _p(probs)
+
+
+def _out_p(t, name: str, dtype, min_numel: int, device, shape=None) -> int | None:
+    """A caller-supplied output buffer the library writes into: None stays
+    NULL; otherwise a contiguous tensor of `dtype` on `device` (the input's
+    device) holding at least `min_numel` elements (exactly `shape` when given).
+    Anything else is refused here, before the kernels could write past it."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the inputs on {device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, the call writes {min_numel}")
+    return _p(t)
+
+
+def _fwd_aux_ptrs(aux: dict, M: int, K: int, N: int, G: int, act: int, fmt: int, device) -> dict:
+    """Checked device addresses of the forward's optional outputs (sizes as
+    include/gmlp.h states them for gmlp_fwd_aux)."""
+    blk, cdiv = (32, 1) if fmt == MXFP8 else (16, 2)
+    n1 = 2 * N if act == SWIGLU else N
+    ncol = N * (M + 16 * G)
+    spec = {"fc2x_codes": (torch.uint8, M * N // cdiv), "fc2x_scales": (torch.uint8, tiled_scales_bytes(M, G, N // blk)),
+            "fc2x_bf16": (torch.bfloat16, M * N), "fc2x_amax_pre": (torch.float32, G),
+            "fc2x_amax_post": (torch.float32, G), "fc2x_col_codes": (torch.uint8, ncol // 2),
+            "fc2x_col_scales": (torch.uint8, ncol // 16), "fc1_pre_act": (torch.bfloat16, M * n1)}
+    unknown = set(aux) - set(spec)
+    if unknown:
+        raise ValueError(f"unknown forward outputs {sorted(unknown)}")
+    return {k: _out_p(aux.get(k), k, dt, n, device) for k, (dt, n) in spec.items()}
 
 
 def _stream(stream=None) -> int:
@@ -339,25 +374,26 @@ def forward(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: Recipe, *
     G = splits.numel()
     if y is None:
         y = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    y_p = _out_p(y, "y", torch.bfloat16, M * K, x.device, shape=(M, K))
     need = forward_workspace_size(M, K, N, G, act, rec)
     if workspace is None:
         workspace = _u8(need, x.device)
+    ws_p = _out_p(workspace, "workspace", torch.uint8, need, x.device)
     aux_c = None
     ev_arr = None
     if aux is not None or events is not None or gemm_mode or act == TANH_SRELU:
-        aux = aux or {}
-        aux_c = FwdAux(_p(aux.get("fc2x_codes")), _p(aux.get("fc2x_scales")), _p(aux.get("fc2x_bf16")),
-                       _p(aux.get("fc2x_amax_pre")), _p(aux.get("fc2x_amax_post")), None, 0, int(gemm_mode),
-                       _p(aux.get("fc2x_col_codes")), _p(aux.get("fc2x_col_scales")), float(tanh_clamp_scale),
-                       _p(aux.get("fc1_pre_act")))
+        a = _fwd_aux_ptrs(aux or {}, M, K, N, G, act, rec.format, x.device)
+        aux_c = FwdAux(a["fc2x_codes"], a["fc2x_scales"], a["fc2x_bf16"], a["fc2x_amax_pre"], a["fc2x_amax_post"],
+                       None, 0, int(gemm_mode), a["fc2x_col_codes"], a["fc2x_col_scales"], float(tanh_clamp_scale),
+                       a["fc1_pre_act"])
         if events:
             ev_arr = _event_handles(events)
             aux_c.stage_events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))
             aux_c.n_stage_events = len(events)
     w1c, w2c = W1.c(), W2.c()
     _check(load().gmlp_forward(_p(x), M, K, N, _splits_p(splits), G, ctypes.byref(w1c), ctypes.byref(w2c), _probs_p(probs, M),
-                               act, ctypes.byref(rec), _p(y), ctypes.byref(aux_c) if aux_c else None,
-                               _p(workspace), workspace.numel(), _stream(stream)))
+                               act, ctypes.byref(rec), y_p, ctypes.byref(aux_c) if aux_c else None,
+                               ws_p, workspace.numel(), _stream(stream)))
     return y
 
 
@@ -370,10 +406,11 @@ def forward_noalloc(x, splits, W1: QWeight, W2: QWeight, probs, act: int, rec: R
     G = splits.numel()
     if y is None:
         y = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    y_p = _out_p(y, "y", torch.bfloat16, M * K, x.device, shape=(M, K))
     w1c, w2c = W1.c(), W2.c()
     aux_c = FwdAux(tanh_clamp_scale=float(tanh_clamp_scale)) if act == TANH_SRELU else None
     _check(load().gmlp_forward_noalloc(_p(x), M, K, W2.cols, _splits_p(splits), G, ctypes.byref(w1c), ctypes.byref(w2c),
-                                       _probs_p(probs, M), act, ctypes.byref(rec), _p(y),
+                                       _probs_p(probs, M), act, ctypes.byref(rec), y_p,
                                        ctypes.byref(aux_c) if aux_c else None, _stream(stream)))
     return y
 
@@ -410,16 +447,25 @@ def backward_dgrad(dy, splits, W2t: "QWeight", W1t: "QWeight", pre_act, probs, a
     G = splits.numel()
     if dx is None:
         dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
+    n1 = 2 * N if act == SWIGLU else N
+    dx_p = _out_p(dx, "dx", torch.bfloat16, M * K, dy.device, shape=(M, K))
     dprob = torch.empty(M, dtype=torch.float32, device=dy.device) if want_dprob else None
     need = load().gmlp_backward_workspace_size(M, K, N, G, act)
     if workspace is None:
         workspace = _u8(need, dy.device)
+    ws_p = _out_p(workspace, "workspace", torch.uint8, need, dy.device)
     fc1_dy = fc1_dy or {}
+    g_codes = _out_p(fc1_dy.get("codes"), "fc1_dy codes", torch.uint8, M * n1, dy.device)
+    g_scales = _out_p(fc1_dy.get("scales"), "fc1_dy scales", torch.uint8, tiled_scales_bytes(M, G, n1 // 32), dy.device)
+    g_bf16 = _out_p(fc1_dy_bf16, "fc1_dy_bf16", torch.bfloat16, M * n1, dy.device)
+    h_p = _p(_bits(pre_act)) if pre_act is not None else None
+    if pre_act is not None and pre_act.numel() < M * n1:
+        raise ValueError(f"pre_act holds {pre_act.numel()} values, the call reads {M * n1}")
     ev_arr = _event_handles(events) if events else None
     _check(load().gmlp_backward_dgrad(_p(dy), M, K, N, _splits_p(splits), G, ctypes.byref(W2t.c()), ctypes.byref(W1t.c()),
-                                      _p(pre_act), _probs_p(probs, M), act, ctypes.byref(rec), _p(dx), _p(dprob),
-                                      _p(fc1_dy.get("codes")), _p(fc1_dy.get("scales")), _p(fc1_dy_bf16),
-                                      _p(workspace),
+                                      h_p, _probs_p(probs, M), act, ctypes.byref(rec), dx_p, _p(dprob),
+                                      g_codes, g_scales, g_bf16,
+                                      ws_p,
                                       workspace.numel(), ev_arr, len(events or ()), _stream(stream)))
     return dx, dprob
 
@@ -442,12 +488,17 @@ def backward_wgrad(x, dy, pre_act, probs, fc1_dy, splits, act: int, *, dW1=None,
     for k in shapes:
         if out[k] is None and k in want:
             out[k] = torch.empty(shapes[k], dtype=torch.float32, device=dev)
+    op = {k: _out_p(out[k], k, torch.float32, int(np.prod(shapes[k])), dev) for k in shapes}
     need = load().gmlp_backward_wgrad_workspace_size(M, K, N, G, act)
     if workspace is None:
         workspace = _u8(need, dev)
+    ws_p = _out_p(workspace, "workspace", torch.uint8, need, dev)
+    for t, nm, n in ((x, "x", M * K), (pre_act, "pre_act", M * N1)):
+        if t is not None and t.numel() < n:
+            raise ValueError(f"{nm} holds {t.numel()} values, the call reads {n}")
     _check(load().gmlp_backward_wgrad(_p(x), _p(dy), _p(_bits(pre_act) if pre_act is not None else None), _probs_p(probs, M),
-                                      _p(fc1_dy), M, K, N, _splits_p(splits), G, act, _p(out["dW1"]), _p(out["dW2"]),
-                                      _p(out["dbias1"]), _p(out["dbias2"]), int(bool(accumulate)), _p(workspace),
+                                      _p(fc1_dy), M, K, N, _splits_p(splits), G, act, op["dW1"], op["dW2"],
+                                      op["dbias1"], op["dbias2"], int(bool(accumulate)), ws_p,
                                       workspace.numel(), _event_handles(events) if events else None,
                                       len(events or ()), _stream(stream)))
     return out

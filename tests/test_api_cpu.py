@@ -373,3 +373,40 @@ def test_binding_refuses_host_and_mistyped_tensors(lib):
     with pytest.raises(TypeError):
         g._p([1, 2, 3])
     assert g._p(None) is None and g._probs_p(None, 64) is None
+
+
+def test_binding_refuses_wrong_output_buffers(lib):
+    """Output buffers are checked before their addresses reach the library:
+    y must be a contiguous bf16 [M, K] tensor on the inputs' device, and every
+    optional forward output must hold what the forward writes into it (a short
+    or mistyped buffer would otherwise be written past its end)."""
+    import torch
+    _, g = lib
+    cpu = torch.device("cpu")
+    M, K, N, G = 64, 256, 256, 2
+    with pytest.raises(ValueError, match="bfloat16"):
+        g._out_p(torch.zeros((M, K), dtype=torch.float32), "y", torch.bfloat16, M * K, cpu, shape=(M, K))
+    with pytest.raises(ValueError, match="shape"):
+        g._out_p(torch.zeros((M, K // 2), dtype=torch.bfloat16), "y", torch.bfloat16, M * K, cpu, shape=(M, K))
+    with pytest.raises(ValueError, match="contiguous"):
+        g._out_p(torch.zeros((K, M), dtype=torch.bfloat16).t(), "y", torch.bfloat16, M * K, cpu, shape=(M, K))
+    with pytest.raises(ValueError, match="is on"):
+        g._out_p(torch.zeros((M, K), dtype=torch.bfloat16), "y", torch.bfloat16, M * K, torch.device("cuda", 0),
+                 shape=(M, K))
+    assert g._out_p(None, "y", torch.bfloat16, 1, cpu) is None
+    for fmt, act in ((g.MXFP8, g.SWIGLU), (g.NVFP4, g.SRELU)):
+        cdiv = 1 if fmt == g.MXFP8 else 2
+        short = {"fc2x_codes": torch.zeros(M * N // cdiv - 1, dtype=torch.uint8),
+                 "fc2x_scales": torch.zeros(16, dtype=torch.uint8),
+                 "fc2x_amax_pre": torch.zeros(G - 1, dtype=torch.float32),
+                 "fc2x_col_codes": torch.zeros(N * M // 2, dtype=torch.uint8),   # no room for group padding
+                 "fc1_pre_act": torch.zeros((M, N), dtype=torch.bfloat16)}
+        for k, v in short.items():
+            if k == "fc1_pre_act" and act == g.SRELU:
+                continue                                    # [M, N] is the SReLU size
+            with pytest.raises(ValueError, match=k):
+                g._fwd_aux_ptrs({k: v}, M, K, N, G, act, fmt, cpu)
+        with pytest.raises(ValueError, match="float32"):
+            g._fwd_aux_ptrs({"fc2x_amax_post": torch.zeros(G, dtype=torch.float64)}, M, K, N, G, act, fmt, cpu)
+        with pytest.raises(ValueError, match="unknown"):
+            g._fwd_aux_ptrs({"fc2x_code": torch.zeros(M * N, dtype=torch.uint8)}, M, K, N, G, act, fmt, cpu)

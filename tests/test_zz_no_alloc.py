@@ -8,8 +8,6 @@ Checked through the C ABI against gmlp_forward (with a caller workspace) on
 two calls in a row with different formats, so the second call starts from the
 scratch contents the first one left behind.  This file is collected last so
 that a run stopping at its first failure has run every other test already."""
-import ctypes
-
 import numpy as np
 import pytest
 import torch
@@ -50,11 +48,18 @@ def test_noalloc_matches_forward_two_calls(gm):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(gm):
+    """131072 tokens at K = N = 256 need about 66 MB of scratch, above the fixed
+    64 MiB: the call is refused before any launch.  Every buffer is a real
+    device tensor of the right size, so a regression in the size check would
+    still only touch valid memory."""
     d, w1, w2, rec = case(gm, gm.MXFP8, gm.SWIGLU)
-    L = gm.load()
-    M = 1 << 20            # a workspace of ~1.3 GB, far above the fixed scratch
-    w1c, w2c = w1.c(), w2.c()
-    st = L.gmlp_forward_noalloc(1 << 20, M, 256, 256, 1 << 20, 4, ctypes.byref(w1c), ctypes.byref(w2c), None,
-                                gm.SWIGLU, ctypes.byref(rec), 1 << 20, None, None)
-    assert st == gm.ERR_WORKSPACE
-    assert b"scratch" in L.gmlp_last_error()
+    M, K, N, G = 1 << 17, 256, 256, 4
+    assert gm.forward_workspace_size(M, K, N, G, gm.SWIGLU, rec) > 64 << 20
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    s = torch.tensor([M // 4] * 4, dtype=torch.int64, device="cuda")
+    with pytest.raises(gm.GmlpError) as e:
+        gm.forward_noalloc(x, s, w1, w2, None, gm.SWIGLU, rec, y=y)
+    assert e.value.status == gm.ERR_WORKSPACE
+    assert "scratch" in str(e.value)
+    gm.check_device_status()
