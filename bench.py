@@ -5,16 +5,20 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gmlp|reference] [--w
 One step = one gmlp_forward over the workload's synthetic batch: x quantise,
 fc1 grouped GEMM with the fused activation x prob and fc2_x requantisation,
 fc2 grouped GEMM (NVFP4 adds the x amax pass and the fc2_x cast).  Weights are
-quantised once before timing.  The default workload is the MXFP8 SwiGLU MoE
-layer with 8 experts, K=2048, N=1024 and 16384 tokens.
+quantised once before timing.  The default workload is the largest
+configuration: the MXFP8 SwiGLU MoE layer with 64 Zipf-routed experts,
+K=7168, N=2048 and 65536 tokens.
 
 Prints one JSON line (rank 0).  value = TFLOP/s of the GEMMs (2*M*K*N1 +
 2*M*N*K) over the device-timed steps, inputs resident in HBM, L2 flushed
 between steps.  e2e = the same metric through the C ABI with the step's x,
 probs and split sizes copied from pinned host memory and y copied back inside
 the timed region, double-buffered across steps (the sequential figure is
-reported beside it).  --impl reference times the oracle (the CPU restatement)
-on the host cores instead.
+reported beside it).  The same line carries, under "workloads", the NVFP4 SReLU
+forward and the MXFP8 SwiGLU forward + backward legs, and under
+"group_quantize" the standalone NVFP4 quantiser (--no-extra / --no-quant skip
+them).  --impl reference times the oracle (the CPU restatement) on the host
+cores instead.
 """
 from __future__ import annotations
 
@@ -165,11 +169,25 @@ L2_TEXT = {"write": "flushed between timed steps (256 MiB write, outside the ste
                     "step starts on a cold L2 without the write's dirty lines; outside the step events)"}
 
 
-def run_gpu(args, rank: int, world: int) -> dict:
-    from mxfp8_nvfp4_block_gb300 import gmlp
-    gmlp.load()
-    dev = torch.device("cuda", torch.cuda.current_device())
-    name = args.workload
+class L2Flush:
+    """Flush L2 between timed steps: write 256 MiB; in "clean" mode then read
+    another 256 MiB, so the write's dirty lines are written back here and the
+    step starts on a cold, clean L2 (it does not pay for the flush's write-back)."""
+
+    def __init__(self, mode: str, dev):
+        self.buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > 129 MB of L2
+        self.sweep = torch.zeros(64 * 1024 * 1024, dtype=torch.int32, device=dev) if mode == "clean" else None
+
+    def __call__(self):
+        self.buf.zero_()
+        if self.sweep is not None:
+            torch.amax(self.sweep)
+
+
+def forward_leg(gmlp, name: str, args, dev, world: int, steps: int, warmup: int, *, e2e: bool, rank: int = 0,
+                keep_weights: bool = False) -> dict:
+    """The forward of one workload: per-step time (value), per-kernel times,
+    the fc1 roofline, and (e2e) the host-to-host figure through the C ABI."""
     d = make_inputs(name)
     w = d["workload"]
     fmt, act = w.fmt, w.act
@@ -180,7 +198,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
     probs = d["probs"].to(dev)
     W1 = gmlp.prepare_weights(d["W1"].to(dev), fmt, swiglu_interleave=(act == gmlp.SWIGLU))
     W2 = gmlp.prepare_weights(d["W2"].to(dev), fmt)
-    if not args.backward:
+    if not keep_weights:
         del d["W1"], d["W2"]
     y = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(gmlp.forward_workspace_size(w.M, w.K, w.N, w.G, act, rec), dtype=torch.uint8, device=dev)
@@ -190,32 +208,27 @@ def run_gpu(args, rank: int, world: int) -> dict:
         ncol = w.N * (w.M + 16 * w.G)
         colwise = {"fc2x_col_codes": torch.empty(ncol // 2, dtype=torch.uint8, device=dev),
                    "fc2x_col_scales": torch.empty(ncol // 16, dtype=torch.uint8, device=dev)}
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > 129 MB of L2
-    sweep = torch.zeros(64 * 1024 * 1024, dtype=torch.int32, device=dev) if args.l2_flush == "clean" else None
-
-    def flush_l2():
-        # write 256 MiB; "clean" then reads another 256 MiB so that the write's
-        # dirty lines are written back here and the step starts on a cold, clean L2
-        flush.zero_()
-        if sweep is not None:
-            torch.amax(sweep)
+    flush_l2 = L2Flush(args.l2_flush, dev)
     n_stage = 3 if fmt == gmlp.MXFP8 else 5
-    K_steps, W_steps = args.steps, args.warmup
+
+    def fwd(**kw):
+        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise,
+                     tanh_clamp_scale=w.tanh_clamp_scale, **kw)
 
     def ev():
         e = torch.cuda.Event(enable_timing=True)
         e.record()
         return e
 
-    starts = [ev() for _ in range(K_steps)]
-    ends = [ev() for _ in range(K_steps)]
-    starts2 = [ev() for _ in range(K_steps)]
-    stages = [[ev() for _ in range(n_stage)] for _ in range(K_steps)]
+    starts = [ev() for _ in range(steps)]
+    ends = [ev() for _ in range(steps)]
+    starts2 = [ev() for _ in range(steps)]
+    stages = [[ev() for _ in range(n_stage)] for _ in range(steps)]
     torch.cuda.synchronize()
 
-    for _ in range(W_steps):
+    for _ in range(warmup):
         flush_l2()
-        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise, tanh_clamp_scale=w.tanh_clamp_scale)
+        fwd()
     gmlp.check_device_status()
     torch.cuda.synchronize()
     if world > 1:
@@ -224,54 +237,29 @@ def run_gpu(args, rank: int, world: int) -> dict:
     with ClockSampler(dev.index) as clk:
         # pass 1 (the reported steps): one event before and after each step, so the
         # kernels of a step overlap their neighbours' prologues as in normal use
-        for i in range(K_steps):
+        for i in range(steps):
             flush_l2()
             starts[i].record(stream)
-            gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise, tanh_clamp_scale=w.tanh_clamp_scale)
+            fwd()
             ends[i].record(stream)
         torch.cuda.synchronize()
         # pass 2: events after every kernel of the step, for per-kernel times
         # (an event between kernels stops that overlap, so these steps run slightly longer)
-        for i in range(K_steps):
+        for i in range(steps):
             flush_l2()
             starts2[i].record(stream)
-            gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, events=stages[i],
-                         gemm_mode=args.gemm_mode, aux=colwise, tanh_clamp_scale=w.tanh_clamp_scale)
+            fwd(events=stages[i])
         torch.cuda.synchronize()
         clk.mark_end()
     if world > 1:
         torch.distributed.barrier()
     gmlp.check_device_status()
-    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(K_steps)]
-    bounds = [[starts2[i]] + stages[i] for i in range(K_steps)]
+    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(steps)]
+    bounds = [[starts2[i]] + stages[i] for i in range(steps)]
     stage_ms = [statistics.mean(b[j].elapsed_time(b[j + 1]) for b in bounds) for j in range(n_stage)]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
-    ms_per_step = total_ms / K_steps
+    ms_per_step = total_ms / steps
     value = job_tflops(w.flops, world, ms_per_step)
-
-    # ---- end to end through the C ABI with host buffers
-    x_h = d["x"].pin_memory()
-    p_h = d["probs"].pin_memory()
-    s_h = d["splits"].pin_memory()
-    y_h = torch.empty((w.M, w.K), dtype=torch.bfloat16).pin_memory()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for it in range(W_steps + K_steps):
-        if it == W_steps:
-            torch.cuda.synchronize()
-            e0.record()
-        x.copy_(x_h, non_blocking=True)
-        probs.copy_(p_h, non_blocking=True)
-        splits.copy_(s_h, non_blocking=True)
-        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise, tanh_clamp_scale=w.tanh_clamp_scale)
-        y_h.copy_(y, non_blocking=True)
-    e1.record()
-    torch.cuda.synchronize()
-    gmlp.check_device_status()
-    e2e_seq_ms = e0.elapsed_time(e1) / K_steps
-    e2e_ms = e2e_pipelined(gmlp, args, w, x, probs, splits, y, x_h, p_h, s_h, W1, W2, act, rec, ws, colwise,
-                           K_steps, W_steps)
-    h2d = x_h.numel() * 2 + p_h.numel() * 4 + s_h.numel() * 8
-    d2h = y_h.numel() * 2
 
     hbm, bf16_burst, _, src = peaks()
     fc1_idx = 1 if fmt == gmlp.MXFP8 else 2
@@ -282,19 +270,12 @@ def run_gpu(args, rank: int, world: int) -> dict:
     cdiv, blk = (1, 32) if fmt == gmlp.MXFP8 else (2, 16)
     q_bytes = w.M * w.K * 2 + w.M * w.K // cdiv + w.M * w.K // blk
     achieved = fc1_flops / (fc1_ms * 1e-3) / 1e12
+    # the GEMM path alone: from the quantised x to y (fc1, NVFP4's fc2_x cast, fc2)
+    gemm_ms = sum(stage_ms[quant_idx + 1:])
     out = {
-        "metric": METRIC,
         "value": round(value, 3),
-        "unit": "TFLOP/s",
-        "n_gpus": world,
-        "steps": K_steps,
-        "warmup": W_steps,
         "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
         "dtype": "mxfp8" if fmt == gmlp.MXFP8 else "nvfp4",
-        "data": "synthetic",
         "config": {"workload": f"{name}: {WORKLOAD_TEXT.get(name, name)}",
                    "l2": L2_TEXT[args.l2_flush],
                    "timing": "value: per-step start/end events; stages_ms and roofline: a second timed pass with "
@@ -302,16 +283,11 @@ def run_gpu(args, rank: int, world: int) -> dict:
                    "weights": "quantised once before timing", "flops_per_step": w.flops,
                    "gemm_mode": args.gemm_mode,
                    "fc2x_columnwise": bool(colwise)},
-        "e2e": {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "double-buffered across steps: step i's inputs copy in while step i-1 computes and "
-                       "step i-2's y copies out, on separate streams",
-                "copy_streams_per_direction": args.e2e_streams,
-                "copy_GB_s_per_direction": round(h2d / (e2e_ms * 1e-3) / 1e9, 1),
-                "sequential": {"value": round(world * w.flops / (e2e_seq_ms * 1e-3) / 1e12, 3),
-                               "ms_per_step": round(e2e_seq_ms, 5)}},
-        "gpu_launches": K_steps * n_stage,
-        "stages_ms": [round(s, 5) for s in stage_ms],
+        "gpu_launches": steps * n_stage,
+        "stages_ms": [round(t, 5) for t in stage_ms],
+        "gemm_path": {"ms": round(gemm_ms, 5), "TFLOP_s": round(w.flops / (gemm_ms * 1e-3) / 1e12, 1),
+                      "frac": round(w.flops / (gemm_ms * 1e-3) / 1e12 / peak, 4),
+                      "what": "the step's kernels after the x cast (quantised x to bf16 y), per-kernel events"},
         "roofline": {"kernel": "fc1 grouped GEMM (gemm_kernel, fused activation + requant epilogue)",
                      "bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
@@ -324,12 +300,13 @@ def run_gpu(args, rank: int, world: int) -> dict:
                        "frac_hbm": round(q_bytes / (stage_ms[quant_idx] * 1e-3) / 1e9 / hbm, 4)},
         "clocks": clk.summary(),
     }
+    f_bytes = w.M * w.N * 2 + (w.M * w.N // 2 + w.M * w.N // 16) * (2 if colwise else 1)
     if fmt == gmlp.NVFP4:
         # fc2_x cast: bf16 in, rowwise NVFP4 out (+ the columnwise copy with --fc2x-colwise)
-        f_bytes = w.M * w.N * 2 + (w.M * w.N // 2 + w.M * w.N // 16) * (2 if colwise else 1)
         out["fc2x_cast"] = {"ms": round(stage_ms[3], 5), "bytes": f_bytes, "columnwise": bool(colwise),
                             "GB_s": round(f_bytes / (stage_ms[3] * 1e-3) / 1e9, 1),
                             "frac_hbm": round(f_bytes / (stage_ms[3] * 1e-3) / 1e9 / hbm, 4)}
+
     # every kernel of the step against its own roofline (algorithmic bytes or FLOPs / event time)
     def k_mem(nbytes, ms):
         gbs = nbytes / (ms * 1e-3) / 1e9
@@ -348,16 +325,90 @@ def run_gpu(args, rank: int, world: int) -> dict:
         kern["fc2_x cast"] = k_mem(f_bytes, stage_ms[3])
     kern["fc2 GEMM"] = k_tensor(2.0 * w.M * w.N * w.K, stage_ms[-1])
     out["kernels"] = kern
-    if args.backward and fmt == gmlp.MXFP8 and w.act != gmlp.TANH_SRELU:
-        out["backward_dgrad"] = bench_backward(gmlp, d, w, d["W1"].to(dev), d["W2"].to(dev), x, splits, probs,
-                                               K_steps, W_steps, dev)
     ceiling = mma_ceiling(gmlp, fmt)
     out["roofline"]["mma_loop_tflops"] = ceiling
     # the loop with the copy mix the forward's GEMM issues (NVFP4 weights carry X4 scales)
     loop = ceiling["with_x4_scale_copies" if fmt == gmlp.NVFP4 else "with_scale_copies"]
     out["roofline"]["frac_of_mma_loop"] = round(achieved / loop, 4)
+
+    if e2e:
+        # ---- end to end through the C ABI with host buffers
+        x_h = d["x"].pin_memory()
+        p_h = d["probs"].pin_memory()
+        s_h = d["splits"].pin_memory()
+        y_h = torch.empty((w.M, w.K), dtype=torch.bfloat16).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for it in range(warmup + steps):
+            if it == warmup:
+                torch.cuda.synchronize()
+                e0.record()
+            x.copy_(x_h, non_blocking=True)
+            probs.copy_(p_h, non_blocking=True)
+            splits.copy_(s_h, non_blocking=True)
+            fwd()
+            y_h.copy_(y, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        gmlp.check_device_status()
+        e2e_seq_ms = e0.elapsed_time(e1) / steps
+        e2e_ms = e2e_pipelined(gmlp, args, w, x, probs, splits, y, x_h, p_h, s_h, W1, W2, act, rec, ws, colwise,
+                               steps, warmup)
+        h2d = x_h.numel() * 2 + p_h.numel() * 4 + s_h.numel() * 8
+        d2h = y_h.numel() * 2
+        out["e2e"] = {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                      "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "how": "double-buffered across steps: step i's inputs copy in while step i-1 computes and "
+                             "step i-2's y copies out, on separate streams",
+                      "copy_streams_per_direction": args.e2e_streams,
+                      "copy_GB_s_per_direction": round(h2d / (e2e_ms * 1e-3) / 1e9, 1),
+                      "sequential": {"value": round(world * w.flops / (e2e_seq_ms * 1e-3) / 1e12, 3),
+                                     "ms_per_step": round(e2e_seq_ms, 5)}}
+    if keep_weights:
+        out["_inputs"] = (d, x, splits, probs)
+    return out
+
+
+def run_gpu(args, rank: int, world: int) -> dict:
+    from mxfp8_nvfp4_block_gb300 import gmlp
+    gmlp.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    name = args.workload
+    main_bwd = args.backward and name == "mx_swiglu"
+    main = forward_leg(gmlp, name, args, dev, world, args.steps, args.warmup, e2e=True, rank=rank,
+                       keep_weights=main_bwd)
+    if main_bwd:
+        d, x, splits, probs = main.pop("_inputs")
+        main["backward_dgrad"] = bench_backward(gmlp, d, d["workload"], d["W1"].to(dev), d["W2"].to(dev), x, splits,
+                                                probs, args.steps, args.warmup, dev, args.l2_flush)
+        del d, x, splits, probs
+    out = {"metric": METRIC, "value": main.pop("value"), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": main.pop("ms_per_step"), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": main.pop("dtype"), "data": "synthetic",
+           "config": main.pop("config"), "e2e": main.pop("e2e"), "gpu_launches": main.pop("gpu_launches")}
+    out.update(main)
+    torch.cuda.empty_cache()
+    if args.extra:
+        # the other configurations of the path, each its own forward leg on this GPU
+        # (fewer steps; no host copies); the MXFP8 SwiGLU leg also times the backward
+        steps = max(3, min(args.steps, args.extra_steps))
+        legs = {}
+        for leg in ("nv_srelu", "mx_swiglu"):
+            if leg == name:
+                continue
+            want_bwd = args.backward and leg == "mx_swiglu"
+            r = forward_leg(gmlp, leg, args, dev, world, steps, args.warmup, e2e=False, rank=rank,
+                            keep_weights=want_bwd)
+            if want_bwd:
+                d, x, splits, probs = r.pop("_inputs")
+                w = d["workload"]
+                r["backward_dgrad"] = bench_backward(gmlp, d, w, d["W1"].to(dev), d["W2"].to(dev), x, splits, probs,
+                                                     steps, args.warmup, dev, args.l2_flush)
+                del d, x, splits, probs
+            legs[leg] = r
+            torch.cuda.empty_cache()
+        out["workloads"] = legs
     if args.quant and rank == 0:
-        out["group_quantize"] = bench_quantizer(gmlp, dev, hbm)
+        out["group_quantize"] = bench_quantizer(gmlp, dev, peaks()[0], args.quant_rows)
     return out
 
 
@@ -445,7 +496,7 @@ def mma_ceiling(gmlp, fmt: int, iters: int = 32768, reps: int = 5) -> dict:
     return out
 
 
-def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps: int, dev) -> dict:
+def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps: int, dev, l2_mode: str) -> dict:
     """Data-gradient backward (MXFP8): dy quantise -> fc2 dGLU GEMM (dSwiGLU /
     dSReLU x prob, dprob, MXFP8 fc1_dy) -> fc1 dgrad GEMM, on the forward's own
     saved activation input; L2 flushed between steps, per-step events."""
@@ -461,14 +512,14 @@ def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps
     dx = torch.empty_like(dy)
     ws = torch.empty(gmlp.load().gmlp_backward_workspace_size(w.M, w.K, w.N, w.G, w.act), dtype=torch.uint8,
                      device=dev)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = L2Flush(l2_mode, dev)
     for _ in range(W_steps):
-        flush.zero_()
+        flush()
         gmlp.backward_dgrad(dy, splits, w2t, w1t, h, probs, w.act, rec, dx=dx, workspace=ws)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
     for e0, e1 in ev:
-        flush.zero_()
+        flush()
         e0.record()
         gmlp.backward_dgrad(dy, splits, w2t, w1t, h, probs, w.act, rec, dx=dx, workspace=ws)
         e1.record()
@@ -478,7 +529,7 @@ def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps
     # second pass: an event after every kernel (dy quantise, dGLU GEMM, dgrad GEMM)
     st = [0.0, 0.0, 0.0]
     for _ in range(K_steps):
-        flush.zero_()
+        flush()
         se = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         se[0].record()
         gmlp.backward_dgrad(dy, splits, w2t, w1t, h, probs, w.act, rec, dx=dx, workspace=ws, events=se[1:])
@@ -498,12 +549,12 @@ def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps
     grads = gmlp.backward_wgrad(xin, dy, h, probs, f1, splits, w.act, workspace=wws)
     kern = {}
     for _ in range(W_steps):
-        flush.zero_()
+        flush()
         gmlp.backward_wgrad(xin, dy, h, probs, f1, splits, w.act, workspace=wws, **grads)
     torch.cuda.synchronize()
     ew = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
     for e0, e1 in ew:
-        flush.zero_()
+        flush()
         e0.record()
         gmlp.backward_wgrad(xin, dy, h, probs, f1, splits, w.act, workspace=wws, **grads)
         e1.record()
@@ -514,7 +565,7 @@ def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps
     # fc1_dy cast, x cast, dW1 GEMM)
     wst = [0.0] * 6
     for _ in range(K_steps):
-        flush.zero_()
+        flush()
         se = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
         se[0].record()
         gmlp.backward_wgrad(xin, dy, h, probs, f1, splits, w.act, workspace=wws, events=se[1:], **grads)
@@ -566,14 +617,22 @@ def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps
                                "frac": round(2.0 * M * N1 * K / (st[2] * 1e-3) / 1e12 / fp8, 4)}}}
 
 
-def bench_quantizer(gmlp, dev, hbm) -> dict:
+def bench_quantizer(gmlp, dev, hbm, rows: int = 0) -> dict:
     """Standalone NVFP4 group Hadamard-amax + quantize-with-amax (row + column,
-    RHT) on bf16 [131072, 4096], 8 groups (inputs 1 GiB, larger than L2)."""
+    RHT) on bf16 [131072, 4096], 8 groups (inputs 1 GiB, larger than L2).
+    rows > 0 takes only the first `rows` tokens (the groups cut to fit; a
+    smaller case for profiling)."""
     d = make_inputs("nv_quant")
     w = d["workload"]
-    x = d["x"].to(dev)
-    splits = d["splits"].to(dev)
-    sh = d["splits"].tolist()
+    x, sp = d["x"], d["splits"]
+    if 0 < rows < w.M:
+        cut = np.minimum(np.cumsum(sp.numpy()), rows)
+        sp = torch.from_numpy(np.diff(np.concatenate([[0], cut])))
+        x = x[:rows].contiguous()
+    M, K = x.shape
+    x = x.to(dev)
+    splits = sp.to(dev)
+    sh = sp.tolist()
     rec = gmlp.recipe(gmlp.NVFP4, use_rht=True, mask=d["mask"])
     reps = 10
     for _ in range(2):
@@ -596,13 +655,13 @@ def bench_quantizer(gmlp, dev, hbm) -> dict:
     torch.cuda.synchronize()
     gmlp.check_device_status()
     t_cast = e[0].elapsed_time(e[1]) / reps
-    M, K = w.M, w.K
     mpad = sum((m + 15) // 16 * 16 for m in sh)
     rd = M * K * 2
     wr = M * K // 2 + M * K // 16 + K * mpad // 2 + K * mpad // 16
     del out, x
-    return {"workload": "nv_quant: NVFP4 group quantise, bf16 [131072, 4096], 8 groups Dirichlet(0.5), "
+    return {"workload": f"nv_quant: NVFP4 group quantise, bf16 [{M}, {K}], 8 groups Dirichlet(0.5), "
                         "row + column (RHT)",
+            "timing": "mean of 10 back-to-back launches (inputs of 1 GiB, larger than L2)",
             "hadamard_amax": {"ms": round(t_amax, 4), "bytes": rd, "GB_s": round(rd / t_amax / 1e6, 1),
                               "frac_hbm": round(rd / t_amax / 1e6 / hbm, 4)},
             "quantize_with_amax": {"ms": round(t_cast, 4), "bytes": rd + wr,
@@ -612,27 +671,70 @@ def bench_quantizer(gmlp, dev, hbm) -> dict:
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_sample(name: str, target_s: float = 10.0, max_reps: int = 3) -> dict:
-    """The oracle as it stands on the host cores, on the full workload (repeated
-    until about target_s of CPU work)."""
-    import oracle
-    d = make_inputs(name)
-    w = d["workload"]
-    xb, W1, W2 = bits(d["x"]), bits(d["W1"]), bits(d["W2"])
-    qw1, qw2 = oracle.quantize_weights(W1, w.fmt), oracle.quantize_weights(W2, w.fmt)
-    t0 = time.time()
-    reps = 0
-    while True:
-        oracle.forward(xb, d["splits"].numpy(), W1, W2, d["probs"].numpy(), w.act, w.fmt, qw1=qw1, qw2=qw2,
-                       rht_mask=d["mask"], tanh_clamp_scale=w.tanh_clamp_scale)
-        reps += 1
-        el = time.time() - t0
-        if el >= target_s or reps >= max_reps:
-            break
-    cores = oracle_threads()
-    return {"value": round(reps * w.flops / el / 1e12, 5), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{reps} full forward(s) of {name} (all {w.M} tokens; weights pre-quantised), "
-                      f"{el:.1f} s, numpy float64 GEMMs + C format arithmetic"}
+class OracleSteps:
+    """Bounded samples of a workload for the oracle on the host cores.  Step i
+    runs the oracle's forward on one expert, rotating over the non-empty
+    experts: all of its tokens for NVFP4 (its amaxes need the whole group),
+    at most `rows` random tokens of it for MXFP8 (MXFP8 rows are independent,
+    so a row's result does not depend on the others).  An expert's weights are
+    quantised by the oracle the first time the expert is used, before its step
+    is timed (the GPU arm also quantises weights before timing)."""
+
+    def __init__(self, name: str, rows: int = 128):
+        import oracle
+        self.oracle = oracle
+        self.d = make_inputs(name)
+        self.w = self.d["workload"]
+        self.xb, self.W1, self.W2 = bits(self.d["x"]), bits(self.d["W1"]), bits(self.d["W2"])
+        self.probs = self.d["probs"].numpy()
+        sp = self.d["splits"].numpy()
+        self.offs = np.concatenate([[0], np.cumsum(sp)])
+        self.experts = [g for g in range(self.w.G) if sp[g] > 0]
+        self.rows = rows
+        self.qw = {}
+        self.rng = np.random.default_rng(0)
+
+    def prepare(self, i: int):
+        """(expert, token indices) of step i, with the expert's weights quantised."""
+        w, o = self.w, self.oracle
+        e = self.experts[i % len(self.experts)]
+        if e not in self.qw:
+            self.qw[e] = (o.quantize_weights(self.W1[e:e + 1], w.fmt), o.quantize_weights(self.W2[e:e + 1], w.fmt))
+        lo, hi = int(self.offs[e]), int(self.offs[e + 1])
+        idx = np.arange(lo, hi)
+        if w.fmt == 0 and hi - lo > self.rows:
+            idx = np.sort(self.rng.choice(idx, self.rows, replace=False))
+        return e, idx
+
+    def run(self, e: int, idx) -> float:
+        """One oracle forward of expert e on tokens idx; returns its GEMM FLOPs."""
+        w = self.w
+        q1, q2 = self.qw[e]
+        self.oracle.forward(np.ascontiguousarray(self.xb[idx]), [len(idx)], self.W1[e:e + 1], self.W2[e:e + 1],
+                            self.probs[idx], w.act, w.fmt, qw1=q1, qw2=q2, rht_mask=self.d["mask"],
+                            tanh_clamp_scale=w.tanh_clamp_scale)
+        return 2.0 * len(idx) * w.K * w.n1 + 2.0 * len(idx) * w.N * w.K
+
+    def describe(self) -> str:
+        what = "all tokens of one expert" if self.w.fmt == 1 else f"at most {self.rows} random tokens of one expert"
+        return (f"per step {what}, experts in turn ({len(self.experts)} non-empty of {self.w.G}); numpy float64 "
+                "GEMMs + C format arithmetic; weights quantised before timing")
+
+
+def oracle_sample(name: str, target_s: float = 15.0) -> dict:
+    """The oracle as it stands on the host cores, on bounded samples of the
+    workload (OracleSteps), repeated until about target_s of CPU work."""
+    st = OracleSteps(name)
+    flops = el = 0.0
+    i = 0
+    while el < target_s and i < 4 * len(st.experts):
+        e, idx = st.prepare(i)
+        t0 = time.time()
+        flops += st.run(e, idx)
+        el += time.time() - t0
+        i += 1
+    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{i} oracle forward steps of {name} ({flops / 1e9:.1f} GFLOP, {el:.1f} s): {st.describe()}"}
 
 
 def oracle_backward_sample(name: str, max_tokens: int = 16384, max_experts: int = 8, target_s: float = 10.0,
@@ -679,49 +781,28 @@ def oracle_backward_sample(name: str, max_tokens: int = 16384, max_experts: int 
 
 
 def run_reference(args) -> dict:
-    """The reference arm: the oracle on the host, each step a bounded row
-    sample (MXFP8 rows are independent) of the same workload."""
-    import oracle
-    d = make_inputs(args.workload)
-    w = d["workload"]
-    xb, W1, W2 = bits(d["x"]), bits(d["W1"]), bits(d["W2"])
-    qw1, qw2 = oracle.quantize_weights(W1, w.fmt), oracle.quantize_weights(W2, w.fmt)
-    splits = d["splits"].numpy()
-    rng = np.random.default_rng(0)
-    frac = 1.0
-    rows = None
-    if w.fmt == 0:
-        # size the per-step row sample so the whole run stays near two minutes
-        probe = np.sort(rng.choice(w.M, max(64, w.M // 64), replace=False))
-        t0 = time.time()
-        oracle.forward(xb, splits, W1, W2, d["probs"].numpy(), w.act, w.fmt, rows=probe, qw1=qw1, qw2=qw2,
-                       tanh_clamp_scale=w.tanh_clamp_scale)
-        per_row = (time.time() - t0) / len(probe)
-        n = int(min(w.M // 8, max(64, 120.0 / (args.steps + args.warmup) / per_row)))
-        rows = np.sort(rng.choice(w.M, n, replace=False))
-        frac = n / w.M
-    flops = w.flops * frac
-
-    def step():
-        oracle.forward(xb, splits, W1, W2, d["probs"].numpy(), w.act, w.fmt, rows=rows, qw1=qw1, qw2=qw2,
-                       rht_mask=d["mask"], tanh_clamp_scale=w.tanh_clamp_scale)
-
-    for _ in range(args.warmup):
-        step()
+    """The reference arm: the oracle on the host, each step a bounded sample of
+    the same workload (OracleSteps: one expert per step)."""
+    st = OracleSteps(args.workload)
+    w = st.w
+    n = args.warmup + args.steps
+    plan = [st.prepare(i) for i in range(n)]
+    for e, idx in plan[:args.warmup]:
+        st.run(e, idx)
+    flops = 0.0
     t0 = time.time()
-    for _ in range(args.steps):
-        step()
+    for e, idx in plan[args.warmup:]:
+        flops += st.run(e, idx)
     el = time.time() - t0
-    v = flops * args.steps / el / 1e12
+    v = flops / el / 1e12
     cores = oracle_threads()
-    sample = (f"{len(rows)} random rows of the {w.M} tokens per step" if rows is not None
-              else f"all {w.M} tokens per step")
     return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload)}"},
+            "data": "synthetic", "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload)}",
+                                            "flops_per_step": w.flops},
             "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "sample": st.describe()},
             "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -731,21 +812,26 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gmlp", choices=["gmlp", "reference"])
-    ap.add_argument("--workload", default="mx_swiglu", choices=[k for k in WORKLOADS if k != "nv_quant"])
+    ap.add_argument("--workload", default="mx_skew", choices=[k for k in WORKLOADS if k != "nv_quant"])
     ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 2],
                     help="0: one CTA per 128x256 tile; 2: CTA pairs on 256x256 tiles")
     ap.add_argument("--backward", dest="backward", action="store_true", default=True,
-                    help="MXFP8 SwiGLU / SReLU: also time the backward, data and weight gradients (the default)")
+                    help="time the backward (data and weight gradients) on the MXFP8 SwiGLU leg (the default)")
     ap.add_argument("--no-backward", dest="backward", action="store_false", help="skip the backward leg")
+    ap.add_argument("--no-extra", dest="extra", action="store_false",
+                    help="skip the other workloads' forward legs (nv_srelu, mx_swiglu)")
+    ap.add_argument("--extra-steps", type=int, default=50, help="timed steps of each extra leg (at most --steps)")
     ap.add_argument("--fc2x-colwise", action="store_true",
                     help="NVFP4: also write the columnwise (RHT) NVFP4 fc2_x each step (no-recompute training path)")
-    ap.add_argument("--l2-flush", default="write", choices=["write", "clean"],
+    ap.add_argument("--l2-flush", default="clean", choices=["write", "clean"],
                     help="between timed steps: write 256 MiB, or write 256 MiB then read another 256 MiB")
     ap.add_argument("--e2e-streams", type=int, default=1,
                     help="e2e leg: copy x and y as this many row slices on as many streams per direction")
     ap.add_argument("--no-quant", dest="quant", action="store_false", help="skip the standalone quantiser leg")
     ap.add_argument("--quant-only", action="store_true",
                     help="run only the standalone NVFP4 quantiser leg and print its JSON")
+    ap.add_argument("--quant-rows", type=int, default=0,
+                    help="standalone quantiser leg on the first N tokens only (a smaller case for profiling)")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false", help="skip the oracle CPU-baseline leg")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -765,14 +851,16 @@ def main():
         from mxfp8_nvfp4_block_gb300 import gmlp
         gmlp.load()
         if rank == 0:
-            print(json.dumps(bench_quantizer(gmlp, torch.device("cuda", torch.cuda.current_device()), peaks()[0])))
+            print(json.dumps(bench_quantizer(gmlp, torch.device("cuda", torch.cuda.current_device()), peaks()[0],
+                                             args.quant_rows)))
         return
     out = run_gpu(args, rank, world)
     if rank == 0:
         if args.cpu:
             out["cpu_baseline"] = oracle_sample(args.workload)
-            if "backward_dgrad" in out:
-                out["backward_dgrad"]["cpu_baseline"] = oracle_backward_sample(args.workload)
+            bwd = out.get("backward_dgrad") or out.get("workloads", {}).get("mx_swiglu", {}).get("backward_dgrad")
+            if bwd is not None:
+                bwd["cpu_baseline"] = oracle_backward_sample("mx_swiglu")
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.barrier()
