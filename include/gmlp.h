@@ -238,8 +238,8 @@ GMLP_API gmlp_status gmlp_prepare_weights_discrete(const uint16_t* const* W_expe
  * (tile 2P+1, run 4kb+k) four times: the image the GEMM copies into tensor
  * memory with one 128-row copy per MMA instead of two.  out: 4 * G * rows *
  * (cols / 16) bytes, device, 16-byte aligned; neither buffer is kept.  Limits: rows % 256 == 0, cols % 256 == 0.
- * gmlp_forward reads it when a weight's scale_layout is GEMM_TILED_X4 (not in
- * CTA-pair mode). */
+ * gmlp_forward reads it when a weight's scale_layout is GEMM_TILED_X4 (in both
+ * GEMM modes). */
 GMLP_API gmlp_status gmlp_replicate_weight_scales(const uint8_t* tiled, int32_t G, int64_t rows, int64_t cols,
                                                   uint8_t* out, gmlp_stream stream);
 
@@ -365,6 +365,23 @@ GMLP_API gmlp_status gmlp_forward_noalloc(const uint16_t* x, int64_t M, int64_t 
                                           const gmlp_qweight* W2, const float* probs, int32_t act,
                                           const gmlp_recipe* recipe, uint16_t* y, const gmlp_fwd_aux* aux,
                                           gmlp_stream stream);
+
+/* gmlp_fc2x_recompute -- the fc2 input rebuilt from the saved activation
+ * input, for a backward that recomputes fc2_x instead of keeping it (PR #3837,
+ * Description and Changes: with activation recompute the backward regenerates
+ * fc2_x, and the column-wise NVFP4 cast of it reuses the forward's amaxes
+ * through gmlp_group_quantize_with_amax; recompute on and off give bitwise
+ * equal results).
+ *   fc2x[t, n] = bf16(act(h[t, :])[n] * probs[t])  (probs NULL = 1)
+ * with exactly the arithmetic of gmlp_forward's fc1 epilogue (step 3 there),
+ * so it equals the forward's fc2_x bit for bit.
+ * pre_act: device bf16 [M][N1], the forward's gmlp_fwd_aux.fc1_pre_act (N1 =
+ * 2N for SwiGLU, gate columns then up columns; N otherwise), 32-byte aligned;
+ * probs: device float [M] or NULL; fc2x: device bf16 [M][N] out, 32-byte
+ * aligned.  act: SWIGLU, SRELU or TANH_SRELU (tanh_clamp_scale > 0, finite;
+ * ignored otherwise).  Limits: N % 16 == 0, N <= 2^20, 0 <= M < 2^31. */
+GMLP_API gmlp_status gmlp_fc2x_recompute(const uint16_t* pre_act, const float* probs, int64_t M, int64_t N,
+                                         int32_t act, float tanh_clamp_scale, uint16_t* fc2x, gmlp_stream stream);
 
 /* Synchronises `stream`, then reads and clears the device status word the
  * kernels set on a bounded-wait timeout or inconsistent split sizes. */

@@ -456,8 +456,6 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
       return fail(GMLP_ERR_INVALID_ARG, "weight scale_layout %d: GEMM_TILED, or GEMM_TILED_X4 for NVFP4",
                   W->scale_layout);
   const bool x4_1 = W1->scale_layout == GMLP_SCALES_GEMM_TILED_X4, x4_2 = W2->scale_layout == GMLP_SCALES_GEMM_TILED_X4;
-  if (aux && aux->gemm_mode == 2 && (x4_1 || x4_2))
-    return fail(GMLP_ERR_INVALID_ARG, "gemm_mode 2 (CTA pairs) reads GEMM_TILED weight scales, not GEMM_TILED_X4");
   if (!W1->codes || !W1->scales || !W2->codes || !W2->scales || !aligned16(W1->codes) || !aligned16(W1->scales) ||
       !aligned16(W2->codes) || !aligned16(W2->scales))
     return fail(GMLP_ERR_INVALID_ARG, "weight codes/scales NULL or not 16-byte aligned");
@@ -668,6 +666,25 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     g2.pdl = 1;
   GMLP_CUDA(launch_gemm(g2, s), "fc2 launch");
   GMLP_TRY(mark());
+  return GMLP_OK;
+}
+
+gmlp_status gmlp_fc2x_recompute(const uint16_t* pre_act, const float* probs, int64_t M, int64_t N, int32_t act,
+                                float tanh_clamp_scale, uint16_t* fc2x, gmlp_stream stream) {
+  g_last_error[0] = 0;
+  if (act != GMLP_ACT_SWIGLU && act != GMLP_ACT_SRELU && act != GMLP_ACT_TANH_SRELU)
+    return fail(GMLP_ERR_INVALID_ARG, "act = %d unknown", act);
+  if (act == GMLP_ACT_TANH_SRELU && !(tanh_clamp_scale > 0.0f && std::isfinite(tanh_clamp_scale)))
+    return fail(GMLP_ERR_INVALID_ARG, "tanh-SReLU needs tanh_clamp_scale > 0 and finite");
+  if (M < 0 || M > (int64_t)0x7FFFFFFF) return fail(GMLP_ERR_INVALID_DIMS, "M = %lld outside [0, 2^31)", (long long)M);
+  if (N <= 0 || N % 16 || N > kMaxFeatures)
+    return fail(GMLP_ERR_INVALID_DIMS, "N = %lld must be a positive multiple of 16, at most 2^20", (long long)N);
+  if ((M > 0 && (!pre_act || !fc2x)) || !aligned32(pre_act) || !aligned32(fc2x))
+    return fail(GMLP_ERR_INVALID_ARG, "pre_act / fc2x NULL or not 32-byte aligned");
+  if (probs && (reinterpret_cast<uintptr_t>(probs) & 3)) return fail(GMLP_ERR_INVALID_ARG, "probs misaligned");
+  GMLP_TRY(check_device());
+  GMLP_CUDA(launch_fc2x_recompute(pre_act, probs, M, N, act, tanh_clamp_scale, fc2x, (cudaStream_t)stream),
+            "fc2_x recompute launch");
   return GMLP_OK;
 }
 

@@ -318,4 +318,22 @@ __device__ __forceinline__ float silu_times(float gate, float up) {
   return __fdividef(gate, 1.0f + __expf(fminf(-gate, 80.0f))) * up;
 }
 
+// fc2_x = bf16(act(h) * prob) from bf16 activation-input values (FP32
+// arithmetic).  The fc1 epilogue and every rebuild of fc2_x from the saved
+// activation input call these, so the two give the same bits.
+//   SwiGLU:     silu(g) * u          (g gate, u up)
+//   SReLU:      max(h, 0)^2
+//   tanh-SReLU: c * tanh(max(h, 0)^2 / c), with inv_c = 1 / c rounded once
+__device__ __forceinline__ float fc2x_swiglu(float g, float u, float prob) { return round_bf16(silu_times(g, u) * prob); }
+
+__device__ __forceinline__ float fc2x_srelu(float h, float prob) {
+  const float r = fmaxf(h, 0.0f);
+  return round_bf16(r * r * prob);
+}
+
+__device__ __forceinline__ float fc2x_tanh_srelu(float h, float prob, float c, float inv_c) {
+  const float r = fmaxf(h, 0.0f);
+  return round_bf16(c * tanhf(r * r * inv_c) * prob);
+}
+
 }  // namespace gmlp

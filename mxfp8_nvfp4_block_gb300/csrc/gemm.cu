@@ -45,12 +45,12 @@ constexpr uint32_t kTmemCols = 512;
 // 256 x 256 tile with cta_group::2 MMAs; each CTA loads its own 128 A rows and
 // one 128-row half of the B tile, so each SM takes in a third fewer bytes.
 //
-// X4 (NVFP4, single CTA): the B scales come replicated four times (weight
-// layout GEMM_TILED_X4), so one 128x256b copy places the scales of both
-// 128-row halves of the B tile for one MMA, replacing two 32x128b.warpx4
-// copies; each copy instruction costs the same tensor-pipe time whatever its
-// size, and NVFP4 needs 12 of the small ones per stage.  A stage is then
-// 66 KB, so 3 stages fit.
+// X4 (NVFP4): the B scales come replicated four times (weight layout
+// GEMM_TILED_X4), so one 128x256b copy places the scales of both 128-row
+// halves of the B tile for one MMA, replacing two 32x128b.warpx4 copies; each
+// copy instruction costs the same tensor-pipe time whatever its size, and
+// NVFP4 needs 12 of the small ones per stage.  A single-CTA stage is then
+// 66 KB (3 stages fit); a CTA-pair stage, with half the B tile, 50 KB (4).
 template <int FMT, int PAIR, bool X4 = false>
 struct Cfg {
   // bytes of scale factors per 128 rows per stage: MXFP8 4 scales/row (one
@@ -60,7 +60,7 @@ struct Cfg {
   static constexpr int kBRows = kBN / PAIR;                   // B rows held per CTA
   static constexpr int kBTileBytes = kBRows * kBKBytes;
   static constexpr int kStageBytes = kATileBytes + kBTileBytes + kSfBytes + kSfBBytes;
-  static constexpr int kStages = X4 ? 3 : PAIR == 1 ? 4 : (FMT == GMLP_MXFP8 ? 6 : 5);
+  static constexpr int kStages = X4 ? (PAIR == 1 ? 3 : 4) : PAIR == 1 ? 4 : (FMT == GMLP_MXFP8 ? 6 : 5);
   static constexpr uint32_t kSfCols = FMT == GMLP_MXFP8 ? 16 : 48;  // TMEM columns per stage
   static constexpr uint32_t kSfbOff = FMT == GMLP_MXFP8 ? 4 : 16;   // SFB after SFA within a stage
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes;
@@ -338,25 +338,15 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
   if (EPI == EPI_FC1_SWIGLU) {
     // a 64-column slice holds 32 gate then 32 up columns of the same 32 outputs
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float hg = round_bf16(acc[i] * alpha);
-      const float hu = round_bf16(acc[32 + i] * alpha);
-      acc[i] = round_bf16(silu_times(hg, hu) * prob);
-    }
+    for (int i = 0; i < 32; ++i) acc[i] = fc2x_swiglu(round_bf16(acc[i] * alpha), round_bf16(acc[32 + i] * alpha), prob);
   } else if (EPI == EPI_FC1_TANH_SRELU) {
     // soft clamp of the squared ReLU at c: c * tanh(h^2 / c)
     const float c = a.tanh_c, inv_c = __frcp_rn(a.tanh_c);
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const float h = fmaxf(round_bf16(acc[i] * alpha), 0.0f);
-      acc[i] = round_bf16(c * tanhf(h * h * inv_c) * prob);
-    }
+    for (int i = 0; i < 64; ++i) acc[i] = fc2x_tanh_srelu(round_bf16(acc[i] * alpha), prob, c, inv_c);
   } else {
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const float h = fmaxf(round_bf16(acc[i] * alpha), 0.0f);
-      acc[i] = round_bf16(h * h * prob);
-    }
+    for (int i = 0; i < 64; ++i) acc[i] = fc2x_srelu(round_bf16(acc[i] * alpha), prob);
   }
 
   if (FMT == GMLP_MXFP8) {
@@ -494,6 +484,16 @@ __device__ __forceinline__ void tc_cp_g(uint32_t taddr, uint64_t sdesc) {
     tc_cp_32x128b_x4(taddr, sdesc);
   else
     asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// 128 rows x 32 bytes of shared memory into TMEM lanes 0..127, columns taddr ..
+// taddr + 7 (a CTA pair: each CTA from its own shared memory into its own TMEM).
+template <int PAIR>
+__device__ __forceinline__ void tc_cp_wide_g(uint32_t taddr, uint64_t sdesc) {
+  if (PAIR == 1)
+    tc_cp_128x256b(taddr, sdesc);
+  else
+    asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 template <int FMT, int PAIR>
@@ -674,9 +674,14 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           tma_load_2d_pair(sB + stage * C::kBTileBytes, &tmB, kb * kBKBytes, rowB, bar, pol_b);
           tma_load_2d_pair(sSFA + stage * C::kSfBytes, &tmSFA, 0, (int32_t)((tileA * KB + kb) * kSfRows), bar,
                            pol_a);
-          tma_load_2d_pair(sfb, &tmSFB, 0, (int32_t)((tileB * KB + kb) * kSfRows), bar, pol_b);
-          tma_load_2d_pair(sfb + C::kSfBytes, &tmSFB, 0, (int32_t)(((tileB + 1) * KB + kb) * kSfRows), bar,
-                           pol_b);
+          if (X4) {  // the stage's 16 KB GEMM_TILED_X4 block of the B tile pair, whole in each CTA
+            tma_load_2d_pair(sfb, &tmSFB, 0, (int32_t)(((tileB >> 1) * KB + kb) * (C::kSfBBytes / 256)), bar,
+                             pol_b);
+          } else {
+            tma_load_2d_pair(sfb, &tmSFB, 0, (int32_t)((tileB * KB + kb) * kSfRows), bar, pol_b);
+            tma_load_2d_pair(sfb + C::kSfBytes, &tmSFB, 0, (int32_t)(((tileB + 1) * KB + kb) * kSfRows), bar,
+                             pol_b);
+          }
         }
         if (++stage == S) {
           stage = 0;
@@ -715,10 +720,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         } else if (X4) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            tc_cp_32x128b_x4(sfa_t + 4 * k, smem_desc(sfa_addr + 512 * k, 0, 128, 0));
+            tc_cp_g<PAIR>(sfa_t + 4 * k, smem_desc(sfa_addr + 512 * k, 0, 128, 0));
             // [4 x half-0 block | 4 x half-1 block]: 128 rows x 32 bytes, the two
             // 16-byte column halves 2048 bytes apart, 8-row groups 128 apart
-            tc_cp_128x256b(sfb_t + 8 * k, smem_desc(sfb_addr + 4096 * k, 2048, 128, 0));
+            tc_cp_wide_g<PAIR>(sfb_t + 8 * k, smem_desc(sfb_addr + 4096 * k, 2048, 128, 0));
           }
         } else {
 #pragma unroll
@@ -872,13 +877,14 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
   }
   const int nscale = (int)(FMT == GMLP_MXFP8 ? a.kbytes / 32 : a.kbytes / 8);
   const int64_t sfa_bytes = ((a.M + 127) / 128 + a.grp.G) * 128LL * nscale;
-  const int64_t sfb_bytes = (int64_t)a.grp.G * a.n_out * nscale;
+  const int64_t sfb_bytes = (int64_t)a.grp.G * a.n_out * nscale * (X4 ? 4 : 1);
   CUtensorMap ta, tbm, tsa, tsb;
   if (!make_tmap(&ta, a.a_codes, a.kbytes, a.M, kBKBytes, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap(&tbm, a.b_codes, a.kbytes, (int64_t)a.grp.G * a.n_out, kBKBytes, C::kBRows,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap(&tsa, a.a_scales, 256, sfa_bytes / 256, 256, C::kSfBytes / 256, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_tmap(&tsb, a.b_scales, 256, sfb_bytes / 256, 256, C::kSfBytes / 256, CU_TENSOR_MAP_SWIZZLE_NONE))
+      !make_tmap(&tsb, a.b_scales, 256, sfb_bytes / 256, 256, (X4 ? C::kSfBBytes : C::kSfBytes) / 256,
+                 CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   const int64_t max_tiles = ((a.M + C::kTileRows - 1) / C::kTileRows + a.grp.G) * (a.n_out / kBN);
   int64_t units = max_units[dev & 63];
@@ -946,11 +952,15 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
     if (a.epi == EPI_DSRELU) return launch_t<GMLP_MXFP8, EPI_DSRELU, 1>(a, s);
     GMLP_LAUNCH(GMLP_MXFP8, EPI_FC2);
   }
-  if (a.b_x4) {  // replicated B scales: single-CTA tiles only
-    if (a.epi == EPI_FC1_SWIGLU) { GMLP_ONE(GMLP_NVFP4, EPI_FC1_SWIGLU, true); }
-    if (a.epi == EPI_FC1_SRELU) { GMLP_ONE(GMLP_NVFP4, EPI_FC1_SRELU, true); }
-    if (a.epi == EPI_FC1_TANH_SRELU) { GMLP_ONE(GMLP_NVFP4, EPI_FC1_TANH_SRELU, true); }
-    GMLP_ONE(GMLP_NVFP4, EPI_FC2, true);
+  if (a.b_x4) {  // replicated B scales
+#define GMLP_X4(E)                                                 \
+  if (pair) return launch_t<GMLP_NVFP4, E, 2, true, false>(a, s); \
+  GMLP_ONE(GMLP_NVFP4, E, true)
+    if (a.epi == EPI_FC1_SWIGLU) { GMLP_X4(EPI_FC1_SWIGLU); }
+    if (a.epi == EPI_FC1_SRELU) { GMLP_X4(EPI_FC1_SRELU); }
+    if (a.epi == EPI_FC1_TANH_SRELU) { GMLP_X4(EPI_FC1_TANH_SRELU); }
+    GMLP_X4(EPI_FC2);
+#undef GMLP_X4
   }
   if (a.epi == EPI_FC1_SWIGLU) { GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SWIGLU); }
   if (a.epi == EPI_FC1_SRELU) { GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SRELU); }

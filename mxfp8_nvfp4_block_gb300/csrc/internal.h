@@ -63,8 +63,13 @@ struct ColQuantArgs {
   int row_tiled;
   uint8_t* col_codes;
   uint8_t* col_scales;
+  uint32_t sgn[16];         // set by the launcher: 0x80008000 for the rows the sign mask negates
 };
 cudaError_t launch_col_quant(const ColQuantArgs& a, cudaStream_t s);
+
+// fc2_x = bf16(act(h) * prob) from the saved activation input h [M][N1]
+cudaError_t launch_fc2x_recompute(const uint16_t* h, const float* probs, int64_t M, int64_t N, int act, float c,
+                                  uint16_t* out, cudaStream_t s);
 
 // ---- grouped GEMM (gemm.cu) ----
 

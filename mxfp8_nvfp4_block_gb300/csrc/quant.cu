@@ -101,16 +101,6 @@ __device__ __forceinline__ void atomic_max_nonneg(float* p, float v) {
   atomicMax(reinterpret_cast<int*>(p), __float_as_int(v));
 }
 
-// Byte offset of the scale (row r of group g, scale column kidx).
-__device__ __forceinline__ int64_t scale_offset(bool tiled, const SmemGroups& t, int g, int64_t r, int kidx,
-                                                int nscale) {
-  if (!tiled) return r * nscale + kidx;
-  const int lr = (int)(r - t.off[g]);
-  const int rr = lr & 127;
-  const int64_t blk = (int64_t)(t.tb[g] + (lr >> 7)) * (nscale >> 2) + (kidx >> 2);
-  return blk * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (kidx & 3);
-}
-
 // Group containing row r, searching forward from g.
 __device__ __forceinline__ int find_group(const SmemGroups& t, int G, int64_t r) {
   int lo = 0, hi = G - 1;  // largest g with off[g] <= r
@@ -132,22 +122,10 @@ __device__ __forceinline__ int find_unit_group(const SmemGroups& t, int G, int64
 
 // ------------------------------------------------------------------ rowwise cast
 
-// E4M3 scale byte of an NVFP4 block with max b under global scale S:
-// E4M3(fp32(fp32(b / 6) * S)).
-__device__ __forceinline__ uint32_t nvfp4_block_sf(float b, float S) {
-  return e4m3x2(__fmul_rn(__fdiv_rn(b, 6.0f), S), 0.0f) & 0xFF;
-}
-
 // NVFP4 encode factor for block scale byte c under global scale S:
 // fp32(S / E4M3(c)), saturated at FLT_MAX as S is (0 for c = 0).
 __device__ __forceinline__ float nvfp4_enc(float S, uint32_t c) {
   return (c == 0 || c == 127) ? 0.0f : fminf(__fdiv_rn(S, e4m3_to_float(c)), 3.402823466e38f);
-}
-
-// enc[c] for every scale byte c a block can take: the block encode's IEEE
-// division, once per code.
-__device__ __forceinline__ void fill_enc_table(float* enc, float S, int tid) {
-  if (tid < 128) enc[tid] = nvfp4_enc(S, (uint32_t)tid);
 }
 
 // Eight FP32 values (already multiplied by the encode factor) -> four E2M1
@@ -551,12 +529,6 @@ __global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const uint16_t*
 
 // ------------------------------------------------------------------ row + column NVFP4 cast
 
-// Tiles of 64 rows x 256 columns of one group, staged in shared memory
-// (4 column chunks of 16 rows each).
-constexpr int kTileR = 64, kTileC = 256, kChunks = kTileR / 16;
-constexpr size_t kColSmem = (size_t)kTileR * kTileC * 2 + kTileC * 8 * kChunks + kTileC * kChunks;
-
-
 // The 16-point FWHT stages of fwht16 on two columns at once.
 __device__ __forceinline__ void fwht16x2(f32x2* w) {
 #pragma unroll
@@ -570,152 +542,148 @@ __device__ __forceinline__ void fwht16x2(f32x2* w) {
       }
 }
 
-__global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
+// fp32(b / 6) for an FP32 block max b: the product with fp32(1/6) and one
+// residual correction equals the IEEE quotient for every b in [2^-125,
+// FLT_MAX] (checked exhaustively on the CPU); tiny, infinite or NaN b take the
+// IEEE division.
+__device__ __forceinline__ float div6(float b) {
+  const float r6 = __uint_as_float(0x3e2aaaabu);  // fp32(1/6)
+  if (b >= __uint_as_float(0x01000000u) && b <= 3.402823466e38f) {
+    const float q1 = __fmul_rn(b, r6);
+    return __fmaf_rn(__fmaf_rn(-6.0f, q1, b), r6, q1);
+  }
+  return __fdiv_rn(b, 6.0f);
+}
+
+// Word k (0..3) of a 16-byte vector.
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
+  return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+}
+
+// Row + column NVFP4 cast.  Work units are (group, 256-column slab, 16-row
+// chunk counted from the group's first row), chunk fastest; each warp takes a
+// contiguous range of units, so consecutive chunks of one slab (the adjacent
+// 8-byte pieces of each column's columnwise codes) go out back to back.  Lane
+// l holds 16 rows x 8 columns (col0 = slab * 256 + 8 l) in registers, rows
+// past the group's end as zeros:
+//   rowwise (ROW): a 16-column block spans lanes 2m, 2m+1; the lanes' row
+//     codes make a contiguous 128-byte run per row;
+//   columnwise: each of the lane's 8 columns is one 16-row block: sign mask
+//     and 16-point FWHT (RHT) in packed FP32 pairs of columns, x 1/4, block
+//     scale, codes; 8 code bytes and 1 scale byte per column and chunk.
+// No shared memory but the per-warp encode tables, no block-wide barrier.
+template <bool ROW, bool RHT, bool TILED>
+__global__ void __launch_bounds__(kThreads, 2) rowcol_quant_kernel(ColQuantArgs a) {
   __shared__ SmemGroups t;
-  __shared__ float enc_row[128], enc_col[128];
-  extern __shared__ uint4 dyn_smem[];
-  uint16_t* tile = reinterpret_cast<uint16_t*>(dyn_smem);             // [kTileR][256] bf16
-  const uint32_t* tile32 = reinterpret_cast<const uint32_t*>(tile);   // [kTileR][128] bf16 pairs
-  uint8_t* ccode = reinterpret_cast<uint8_t*>(tile + kTileR * kTileC);  // [256 columns][kChunks x 8 B]
-  uint8_t* cscale = ccode + kTileC * 8 * kChunks;                       // [256 columns][kChunks]
+  __shared__ float enc_tab[kWarps][2][128];  // per warp: row and column encode factors of its current group
   const int64_t K = a.K;
-  const int slabs = (int)((K + kTileC - 1) / kTileC);
-  build_group_tables(a.grp, slabs, t, kTileR);
+  const int slabs = (int)((K + 255) / 256);
+  build_group_tables(a.grp, slabs, t, 16);
   griddep_wait();
   griddep_launch_dependents();
   if (t.bad) return;
   const int G = a.grp.G;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int64_t units = t.up[G];
+  const int64_t warps = (int64_t)gridDim.x * kWarps;
+  const int64_t w = (int64_t)blockIdx.x * kWarps + wib;
+  const int64_t u0 = units * w / warps, u1 = units * (w + 1) / warps;
+  if (u0 >= u1) return;
+  float* enc_row = enc_tab[wib][0];
+  float* enc_col = enc_tab[wib][1];
   const int nscale_row = (int)(K / 16);
-  int cur_g = -1;
+  int g = find_unit_group(t, G, u0), g_tab = -1;
   float S_row = 0.0f, S_col = 0.0f;
-  for (int64_t u = blockIdx.x; u < t.up[G]; u += gridDim.x) {
-    const int g = find_unit_group(t, G, u);
-    const int m = t.off[g + 1] - t.off[g];
-    const int ntile = (m + kTileR - 1) / kTileR;
-    const int local = (int)(u - t.up[g]);
-    const int slab = local / ntile, b = local % ntile;
-    const int64_t row0 = (int64_t)t.off[g] + (int64_t)b * kTileR;
-    const int nvalid = min(kTileR, m - b * kTileR);
-    const int64_t col0 = (int64_t)slab * kTileC;
-    const int ncols = (int)min((int64_t)kTileC, K - col0);
-
-    __syncthreads();  // the previous tile is done with shared memory
-    if (g != cur_g) {
-      cur_g = g;
-      S_row = a.row_codes ? nvfp4_global_scale(a.amax_row[g]) : 0.0f;
-      S_col = a.col_codes ? nvfp4_global_scale(a.amax_col[g]) : 0.0f;
-      fill_enc_table(enc_row, S_row, tid);
-      fill_enc_table(enc_col, S_col, tid);
-    }
-    // phase 1: the tile into shared memory (rows past the group end as zeros)
-    {
-      constexpr int kIt = kTileR / kWarps;
-      uint4 v[kIt];
+  for (int64_t u = u0; u < u1; ++u) {
+    while (t.up[g + 1] <= u) ++g;
+    if (g != g_tab) {
+      S_row = ROW ? nvfp4_global_scale(a.amax_row[g]) : 0.0f;
+      S_col = nvfp4_global_scale(a.amax_col[g]);
+      __syncwarp();
 #pragma unroll
-      for (int it = 0; it < kIt; ++it) {
-        const int r = it * 8 + (tid >> 5), c8 = (tid & 31) * 8;
-        v[it] = (r < nvalid && c8 < ncols) ? ld_stream(a.x + (row0 + r) * K + col0 + c8) : make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < 4; ++i) {
+        if (ROW) enc_row[lane + 32 * i] = nvfp4_enc(S_row, (uint32_t)(lane + 32 * i));
+        enc_col[lane + 32 * i] = nvfp4_enc(S_col, (uint32_t)(lane + 32 * i));
+      }
+      __syncwarp();
+      g_tab = g;
+    }
+    const Unit un = decode_unit(t, g, u, K, lane);
+    uint4 v[16];
+    load_unit(a.x, K, un, v);
+
+    if (ROW) {
+      // rowwise NVFP4: lanes 2m, 2m+1 share block m of the slab (16 columns)
+      const int kblk = (int)(un.col0 >> 4);  // this lane pair's block column
+      uint8_t* crow = a.row_codes + un.row0 * (K / 2) + (un.col0 >> 1);
+      uint8_t* srow;
+      int64_t sstep;
+      if (TILED) {
+        const int lr0 = 16 * un.j, rr0 = lr0 & 127;
+        srow = a.row_scales + ((int64_t)(t.tb[g] + (lr0 >> 7)) * (nscale_row >> 2) + (kblk >> 2)) * 512 +
+               (rr0 & 31) * 16 + (rr0 >> 5) * 4;
+        sstep = 16;
+      } else {
+        srow = a.row_scales + un.row0 * nscale_row + kblk;
+        sstep = nscale_row;
       }
 #pragma unroll
-      for (int it = 0; it < kIt; ++it) {
-        const int r = it * 8 + (tid >> 5), c8 = (tid & 31) * 8;
-        *reinterpret_cast<uint4*>(tile + r * kTileC + c8) = v[it];
-      }
-    }
-    __syncthreads();
-
-    // phase 2: rowwise NVFP4, one thread per 16-column block (16 threads per
-    // row): packed bf16 max, the exact division-free b / 6, encode table
-    if (a.row_codes) {
-      const int nblk = ncols / 16;
-      for (int base = warp * 32; base < nvalid * 16; base += kThreads) {
-        const int i = base + lane, r = i >> 4, bb = i & 15;
-        const bool ok = r < nvalid && bb < nblk;
-        const uint4 v0 = *reinterpret_cast<const uint4*>(tile + r * kTileC + 16 * bb);
-        const uint4 v1 = *reinterpret_cast<const uint4*>(tile + r * kTileC + 16 * bb + 8);
-        const uint32_t sf = nvfp4_block_sf_bf16(max(amax8_bits(v0), amax8_bits(v1)), S_row);
-        const float enc = enc_row[sf];
-        float q0[8], q1[8];
-        scale8(v0, enc, q0);
-        scale8(v1, enc, q1);
-        const uint32_t sw = gather4_bytes(sf, 1);
-        if (ok) {
-          const int64_t rg = row0 + r;
-          *reinterpret_cast<uint2*>(a.row_codes + rg * (K / 2) + (col0 >> 1) + 8 * bb) =
-              make_uint2(e2m1_pack8(q0), e2m1_pack8(q1));
-          if ((bb & 3) == 0)
-            *reinterpret_cast<uint32_t*>(a.row_scales + scale_offset(a.row_tiled, t, g, rg,
-                                                                     (int)(col0 >> 4) + bb, nscale_row)) = sw;
+      for (int i = 0; i < 16; ++i) {
+        if (i < un.nvalid) {
+          uint32_t m = amax8_bits(v[i]);
+          m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          const uint32_t sf = nvfp4_block_sf_bf16(m, S_row);
+          float q[8];
+          scale8(v[i], enc_row[sf], q);
+          const uint32_t sw = gather4_bytes(sf, 2);
+          if (un.active) {
+            *reinterpret_cast<uint32_t*>(crow + i * (K / 2)) = e2m1_pack8(q);
+            if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(srow + i * sstep) = sw;
+          }
         }
       }
     }
 
-    // phase 3: columnwise NVFP4 (16 consecutive rows per block, RHT first):
-    // thread = two adjacent columns (packed FP32 pairs) x two chunks; results
-    // staged in shared memory
-    const int nch = min(kChunks, (nvalid + 15) >> 4);
-    if (a.col_codes) {
-      const int cp = tid & 127;
-      const uint32_t sm = a.use_rht ? a.mask : 0u;
+    // columnwise NVFP4: per column pair, the 16 rows as packed FP32 pairs
+    const int64_t mpad = (int64_t)(t.mp[g + 1] - t.mp[g]);
+    uint8_t* ccol = a.col_codes + K * (int64_t)t.mp[g] / 2 + un.col0 * (mpad / 2) + 8 * un.j;
+    uint8_t* scol = a.col_scales + K * (int64_t)t.mp[g] / 16 + un.col0 * (mpad / 16) + un.j;
 #pragma unroll
-      for (int jq = 0; jq < 2; ++jq) {
-        const int j = (tid >> 7) * 2 + jq;
-        if (j < nch && 2 * cp < ncols) {
-          f32x2 y[16];
+    for (int cp = 0; cp < 4; ++cp) {
+      f32x2 y[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            // bf16 pair -> FP32 pair, the sign of row i flipped through its sign bit
-            const uint32_t w = tile32[(16 * j + i) * (kTileC / 2) + cp];
-            const uint32_t sb = (sm << (31 - i)) & 0x80000000u;
-            y[i] = pk2(__uint_as_float((w << 16) ^ sb), __uint_as_float((w & 0xFFFF0000u) ^ sb));
-          }
-          if (a.use_rht) {
-            fwht16x2(y);
-            const f32x2 quarter = pk2(0.25f, 0.25f);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = mul2(y[i], quarter);
-          }
-          float b0 = 0.0f, b1 = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            b0 = fmaxf(b0, fabsf(lo2(y[i])));
-            b1 = fmaxf(b1, fabsf(hi2(y[i])));
-          }
-          const uint32_t sf0 = nvfp4_block_sf(b0, S_col), sf1 = nvfp4_block_sf(b1, S_col);
-          const f32x2 enc = pk2(enc_col[sf0], enc_col[sf1]);
-          float p0[16], p1[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const f32x2 q = mul2(y[i], enc);
-            p0[i] = lo2(q);
-            p1[i] = hi2(q);
-          }
-          *reinterpret_cast<uint2*>(ccode + (2 * cp) * 8 * kChunks + 8 * j) =
-              make_uint2(e2m1_pack8(p0), e2m1_pack8(p0 + 8));
-          *reinterpret_cast<uint2*>(ccode + (2 * cp + 1) * 8 * kChunks + 8 * j) =
-              make_uint2(e2m1_pack8(p1), e2m1_pack8(p1 + 8));
-          cscale[(2 * cp) * kChunks + j] = (uint8_t)sf0;
-          cscale[(2 * cp + 1) * kChunks + j] = (uint8_t)sf1;
-        }
+      for (int i = 0; i < 16; ++i) {
+        uint32_t wd = word_of(v[i], cp);
+        if (RHT) wd ^= a.sgn[i];  // the sign mask on row i of both columns
+        y[i] = pk2(__uint_as_float(wd << 16), __uint_as_float(wd & 0xFFFF0000u));
       }
-    }
-    __syncthreads();
-
-    // phase 4: each column's run of nch chunks is contiguous in the columnwise
-    // layout; kChunks lanes write one column (32 / kChunks columns per warp instruction)
-    if (a.col_codes) {
-      const int64_t mpad = (int64_t)(t.mp[g + 1] - t.mp[g]);
-      const int64_t cbase = K * (int64_t)t.mp[g] / 2, sbase = K * (int64_t)t.mp[g] / 16;
-      constexpr int kColsPerWarp = 32 / kChunks;
-      const int j = lane % kChunks;
-      for (int cc = warp * kColsPerWarp + lane / kChunks; cc < ncols; cc += kWarps * kColsPerWarp) {
-        if (j < nch) {
-          const int64_t col = col0 + cc;
-          *reinterpret_cast<uint2*>(a.col_codes + cbase + col * (mpad / 2) + 8LL * (kChunks * b + j)) =
-              *reinterpret_cast<const uint2*>(ccode + cc * 8 * kChunks + 8 * j);
-          a.col_scales[sbase + col * (mpad / 16) + kChunks * b + j] = cscale[cc * kChunks + j];
-        }
+      if (RHT) {
+        fwht16x2(y);
+        const f32x2 quarter = pk2(0.25f, 0.25f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = mul2(y[i], quarter);
+      }
+      float b0 = 0.0f, b1 = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        b0 = fmaxf(b0, fabsf(lo2(y[i])));
+        b1 = fmaxf(b1, fabsf(hi2(y[i])));
+      }
+      const uint32_t sf0 = e4m3x2(__fmul_rn(div6(b0), S_col), 0.0f) & 0xFF;
+      const uint32_t sf1 = e4m3x2(__fmul_rn(div6(b1), S_col), 0.0f) & 0xFF;
+      const f32x2 enc = pk2(enc_col[sf0], enc_col[sf1]);
+      float p0[16], p1[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const f32x2 q = mul2(y[i], enc);
+        p0[i] = lo2(q);
+        p1[i] = hi2(q);
+      }
+      if (un.active) {
+        *reinterpret_cast<uint2*>(ccol + (2 * cp) * (mpad / 2)) = make_uint2(e2m1_pack8(p0), e2m1_pack8(p0 + 8));
+        *reinterpret_cast<uint2*>(ccol + (2 * cp + 1) * (mpad / 2)) = make_uint2(e2m1_pack8(p1), e2m1_pack8(p1 + 8));
+        scol[(2 * cp) * (mpad / 16)] = (uint8_t)sf0;
+        scol[(2 * cp + 1) * (mpad / 16)] = (uint8_t)sf1;
       }
     }
   }
@@ -725,17 +693,17 @@ __global__ void __launch_bounds__(kThreads) col_quant_kernel(ColQuantArgs a) {
 // fewer when there is less work.
 template <typename Kern>
 int grid_for(Kern kern, int64_t work_warps, size_t smem = 0) {
-  static int per_sm_cache[64][8] = {};
-  static const void* keys[64][8] = {};
+  static int per_sm_cache[64][32] = {};
+  static const void* keys[64][32] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   int per_sm = 0;
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 32; ++i)
     if (keys[dev & 63][i] == (const void*)kern) per_sm = per_sm_cache[dev & 63][i];
   if (!per_sm) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
       per_sm = 1;
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 32; ++i)
       if (!keys[dev & 63][i]) {
         keys[dev & 63][i] = (const void*)kern;
         per_sm_cache[dev & 63][i] = per_sm;
@@ -746,6 +714,54 @@ int grid_for(Kern kern, int64_t work_warps, size_t smem = 0) {
   int64_t blocks = (work_warps + kWarps - 1) / kWarps;
   if (blocks > max_blocks) blocks = max_blocks;
   return (int)(blocks < 1 ? 1 : blocks);
+}
+
+// ------------------------------------------------------------------ fc2_x rebuild
+
+// fc2_x = bf16(act(h) * prob) from the saved activation input h [M][N1]
+// (SwiGLU: N1 = 2N, gate columns then up columns; otherwise N1 = N), with the
+// fc1 epilogue's own arithmetic (fc2x_* of device.cuh).  One thread makes 16
+// outputs of a row per step (32-byte loads and stores), grid-stride.
+template <int ACT>
+__global__ void __launch_bounds__(kThreads) fc2x_recompute_kernel(const uint16_t* h, const float* probs, int64_t M,
+                                                                  int64_t N, float c, uint16_t* out) {
+  const int64_t per_row = N / 16, N1 = ACT == GMLP_ACT_SWIGLU ? 2 * N : N;
+  const int64_t total = M * per_row;
+  const float inv_c = ACT == GMLP_ACT_TANH_SRELU ? __frcp_rn(c) : 0.0f;
+  int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  const int64_t st_t = stride / per_row, st_c = stride - st_t * per_row;
+  int64_t t = i / per_row, ch = i - t * per_row;
+  for (; i < total; i += stride) {
+    const float p = probs ? __ldg(probs + t) : 1.0f;
+    const uint16_t* row = h + t * N1 + ch * 16;
+    uint32_t gw[8], uw[8], ow[8];
+    ld_global_nc_v8(row, gw);
+    if (ACT == GMLP_ACT_SWIGLU) ld_global_nc_v8(row + N, uw);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float g0 = bf16_bits_to_float(gw[k] & 0xFFFFu), g1 = bf16_bits_to_float(gw[k] >> 16);
+      float f0, f1;
+      if (ACT == GMLP_ACT_SWIGLU) {
+        f0 = fc2x_swiglu(g0, bf16_bits_to_float(uw[k] & 0xFFFFu), p);
+        f1 = fc2x_swiglu(g1, bf16_bits_to_float(uw[k] >> 16), p);
+      } else if (ACT == GMLP_ACT_TANH_SRELU) {
+        f0 = fc2x_tanh_srelu(g0, p, c, inv_c);
+        f1 = fc2x_tanh_srelu(g1, p, c, inv_c);
+      } else {
+        f0 = fc2x_srelu(g0, p);
+        f1 = fc2x_srelu(g1, p);
+      }
+      ow[k] = bf16_bits(f0) | (bf16_bits(f1) << 16);
+    }
+    st_global_v8(out + t * N + ch * 16, ow);
+    t += st_t;
+    ch += st_c;
+    if (ch >= per_row) {
+      ch -= per_row;
+      ++t;
+    }
+  }
 }
 
 // One warp waits, through the kernels' bounded wait, on an mbarrier that
@@ -849,18 +865,42 @@ cudaError_t launch_hadamard_amax(const uint16_t* x, int64_t M, int64_t K, GroupS
   return cudaGetLastError();
 }
 
-cudaError_t launch_col_quant(const ColQuantArgs& a, cudaStream_t s) {
-  static bool attr[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!attr[dev & 63]) {
-    cudaError_t e = cudaFuncSetAttribute(col_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kColSmem);
-    if (e != cudaSuccess) return e;
-    attr[dev & 63] = true;
+cudaError_t launch_fc2x_recompute(const uint16_t* h, const float* probs, int64_t M, int64_t N, int act, float c,
+                                  uint16_t* out, cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  const int64_t work = M * (N / 16);
+  if (act == GMLP_ACT_SWIGLU) {
+    fc2x_recompute_kernel<GMLP_ACT_SWIGLU>
+        <<<grid_for(fc2x_recompute_kernel<GMLP_ACT_SWIGLU>, work / 32), kThreads, 0, s>>>(h, probs, M, N, c, out);
+  } else if (act == GMLP_ACT_TANH_SRELU) {
+    fc2x_recompute_kernel<GMLP_ACT_TANH_SRELU>
+        <<<grid_for(fc2x_recompute_kernel<GMLP_ACT_TANH_SRELU>, work / 32), kThreads, 0, s>>>(h, probs, M, N, c, out);
+  } else {
+    fc2x_recompute_kernel<GMLP_ACT_SRELU>
+        <<<grid_for(fc2x_recompute_kernel<GMLP_ACT_SRELU>, work / 32), kThreads, 0, s>>>(h, probs, M, N, c, out);
   }
-  const int64_t units = ((a.M + kTileR - 1) / kTileR + a.grp.G) * ((a.K + kTileC - 1) / kTileC);
-  col_quant_kernel<<<grid_for(col_quant_kernel, units * kWarps, kColSmem), kThreads, kColSmem, s>>>(a);
   return cudaGetLastError();
+}
+
+template <bool ROW, bool RHT, bool TILED>
+cudaError_t launch_rowcol_t(const ColQuantArgs& a, cudaStream_t s) {
+  auto kern = rowcol_quant_kernel<ROW, RHT, TILED>;
+  const int64_t units = ((a.M + 15) / 16 + a.grp.G) * ((a.K + 255) / 256);
+  kern<<<grid_for(kern, units), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_col_quant(const ColQuantArgs& a0, cudaStream_t s) {
+  if (a0.M == 0 && a0.grp.G == 0) return cudaSuccess;
+  ColQuantArgs a = a0;
+  for (int i = 0; i < 16; ++i) a.sgn[i] = ((a.mask >> i) & 1u) ? 0x80008000u : 0u;
+  const bool row = a.row_codes != nullptr;
+  if (a.use_rht) {
+    if (!row) return launch_rowcol_t<false, true, false>(a, s);
+    return a.row_tiled ? launch_rowcol_t<true, true, true>(a, s) : launch_rowcol_t<true, true, false>(a, s);
+  }
+  if (!row) return launch_rowcol_t<false, false, false>(a, s);
+  return a.row_tiled ? launch_rowcol_t<true, false, true>(a, s) : launch_rowcol_t<true, false, false>(a, s);
 }
 
 }  // namespace gmlp

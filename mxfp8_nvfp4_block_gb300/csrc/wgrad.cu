@@ -148,13 +148,11 @@ __global__ void __launch_bounds__(kColThreads) colq_kernel(const ColqArgs a) {
         for (int e = 0; e < 4; ++e) {
           float f0, f1;
           if (MODE == COLQ_SWIGLU) {
-            f0 = round_bf16(silu_times(bf16_bits_to_float(hw[e] & 0xFFFFu), bf16_bits_to_float(uw[e] & 0xFFFFu)) * p);
-            f1 = round_bf16(silu_times(bf16_bits_to_float(hw[e] >> 16), bf16_bits_to_float(uw[e] >> 16)) * p);
+            f0 = fc2x_swiglu(bf16_bits_to_float(hw[e] & 0xFFFFu), bf16_bits_to_float(uw[e] & 0xFFFFu), p);
+            f1 = fc2x_swiglu(bf16_bits_to_float(hw[e] >> 16), bf16_bits_to_float(uw[e] >> 16), p);
           } else {
-            const float h0 = fmaxf(bf16_bits_to_float(hw[e] & 0xFFFFu), 0.0f);
-            const float h1 = fmaxf(bf16_bits_to_float(hw[e] >> 16), 0.0f);
-            f0 = round_bf16(h0 * h0 * p);
-            f1 = round_bf16(h1 * h1 * p);
+            f0 = fc2x_srelu(bf16_bits_to_float(hw[e] & 0xFFFFu), p);
+            f1 = fc2x_srelu(bf16_bits_to_float(hw[e] >> 16), p);
           }
           ow[e] = bf16_bits(f0) | (bf16_bits(f1) << 16);
         }

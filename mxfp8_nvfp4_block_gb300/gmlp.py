@@ -29,7 +29,7 @@ EXPORTS = ["gmlp_tiled_scales_bytes", "gmlp_group_hadamard_amax", "gmlp_group_qu
            "gmlp_selftest_bounded_wait", "gmlp_mma_peak", "gmlp_replicate_weight_scales",
            "gmlp_prepare_weights_discrete", "gmlp_backward_workspace_size", "gmlp_backward_dgrad",
            "gmlp_backward_wgrad_workspace_size", "gmlp_backward_wgrad", "gmlp_colwise_tokens",
-           "gmlp_query_layout"]
+           "gmlp_query_layout", "gmlp_fc2x_recompute"]
 
 
 class Recipe(ctypes.Structure):
@@ -99,6 +99,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gmlp_query_layout": (_i64, [_i32, ctypes.c_void_p, _i32, _i64, _i64, _i64]),
         "gmlp_backward_wgrad": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp,
                                        _vp, _i32, _vp, ctypes.c_size_t, _vp, _i32, _vp]),
+        "gmlp_fc2x_recompute": (_i32, [_vp, _vp, _i64, _i64, _i32, ctypes.c_float, _vp, _vp]),
         "gmlp_last_error": (ctypes.c_char_p, []),
         "gmlp_version": (ctypes.c_char_p, []),
     }
@@ -501,6 +502,20 @@ def backward_wgrad(x, dy, pre_act, probs, fc1_dy, splits, act: int, *, dW1=None,
                                       op["dbias1"], op["dbias2"], int(bool(accumulate)), ws_p,
                                       workspace.numel(), _event_handles(events) if events else None,
                                       len(events or ()), _stream(stream)))
+    return out
+
+
+def fc2x_recompute(pre_act, probs, act: int, *, tanh_clamp_scale: float = 0.0, out=None, stream=None):
+    """fc2_x = bf16(act(h) * prob) rebuilt from the saved activation input h
+    [M, N1] (see gmlp_fc2x_recompute); returns bf16 [M, N]."""
+    h = _bits(pre_act)
+    M, N1 = h.shape
+    N = N1 // 2 if act == SWIGLU else N1
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=h.device)
+    o = _out_p(out, "out", torch.bfloat16, M * N, h.device, shape=(M, N))
+    _check(load().gmlp_fc2x_recompute(_p(h), _probs_p(probs, M), M, N, act, float(tanh_clamp_scale), o,
+                                      _stream(stream)))
     return out
 
 

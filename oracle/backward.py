@@ -114,12 +114,13 @@ def mxfp8_colwise(x, splits) -> tuple[np.ndarray, np.ndarray]:
     return codes, scales
 
 
-def recompute_fc2x(h, probs, act: int) -> np.ndarray:
+def recompute_fc2x(h, probs, act: int, tanh_clamp_scale: float | None = None) -> np.ndarray:
     """fc2_x rebuilt from the saved activation input: bf16(act(h) * prob), the
-    forward's own definition (h [M, N1] bf16 bits, probs [M] or None = 1)."""
+    forward's own definition (h [M, N1] bf16 bits, probs [M] or None = 1;
+    tanh_clamp_scale for tanh-SReLU)."""
     hb = bf16_to_f64(np.ascontiguousarray(h).view(np.uint16))
     p = np.ones(hb.shape[0]) if probs is None else np.asarray(probs, dtype=np.float64)
-    return f64_to_bf16(activation(hb, act) * p[:, None])
+    return f64_to_bf16(activation(hb, act, tanh_clamp_scale) * p[:, None])
 
 
 def backward_wgrad(x, dy, h, probs, fc1_dy, splits, act: int) -> dict:

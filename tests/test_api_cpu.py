@@ -173,7 +173,8 @@ def test_forward_weight_scale_layout_checks(lib):
     assert call(l1=3) == g.ERR_INVALID_ARG
     assert call(l2=g.GEMM_TILED_X4, fmt=g.MXFP8) == g.ERR_INVALID_ARG    # X4 is an NVFP4 layout
     pair = g.FwdAux(None, None, None, None, None, None, 0, 2)
-    assert call(l1=g.GEMM_TILED_X4, aux=ctypes.byref(pair)) == g.ERR_INVALID_ARG   # CTA pairs read GEMM_TILED
+    # CTA pairs read GEMM_TILED_X4 too: the call passes the argument checks (then needs a device)
+    assert call(l1=g.GEMM_TILED_X4, aux=ctypes.byref(pair)) in (g.ERR_CUDA, g.ERR_UNSUPPORTED_DEVICE)
 
 
 def test_forward_columnwise_fc2x_checks(lib):

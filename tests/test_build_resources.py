@@ -26,7 +26,9 @@ SPILL_FREE = [
     "gemm_kernel<1, 2, 1, true, false>",    # NVFP4 fc2
     "row_quant_kernel<1, true>",            # NVFP4 casts (x, fc2_x)
     "hadamard_amax_kernel",
-    "col_quant_kernel",
+    "rowcol_quant_kernel<true, true, true>",    # NVFP4 row + column (RHT) cast, GEMM_TILED row scales
+    "rowcol_quant_kernel<true, true, false>",   # the same, compact row scales
+    "rowcol_quant_kernel<false, true, false>",  # column (RHT) only
     "colq_kernel<0>", "colq_kernel<1>", "colq_kernel<2>",
 ]
 

@@ -14,6 +14,7 @@ import pytest
 import torch
 
 from mxfp8_nvfp4_block_gb300.inputs import WORKLOADS, bits, make_inputs
+from oracle.layout import tiled_index
 from parity import code_match_report, frob, np_bits, np_u8, nvfp4_scale_of
 
 pytestmark = pytest.mark.gpu
@@ -27,10 +28,7 @@ def bf16_cpu(a):
 
 
 def run_gpu(gm, d, fmt, act, mask=0, probs=True, gemm_mode=0, x4=None, tanh_c=0.0):
-    # NVFP4 weights carry the replicated (GEMM_TILED_X4) scales by default; the
-    # CTA-pair mode reads GEMM_TILED ones
-    if gemm_mode == 2:
-        x4 = False
+    # NVFP4 weights carry the replicated (GEMM_TILED_X4) scales by default
     w1 = gm.prepare_weights(d["W1"].cuda(), fmt, swiglu_interleave=(act == gm.SWIGLU), x4=x4)
     w2 = gm.prepare_weights(d["W2"].cuda(), fmt, x4=x4)
     M, N = d["x"].shape[0], d["W2"].shape[2]
@@ -116,7 +114,8 @@ def test_forward_lossless_bitexact(orc, gm, fmt, act, gemm_mode):
 @pytest.mark.parametrize("act", [0, 1], ids=["swiglu", "srelu"])
 def test_forward_nvfp4_x4_scales_match_tiled(gm, act):
     """The GEMM reading replicated weight scales (one 128x256b tensor-memory copy
-    per MMA) gives bit-identical outputs to the one reading GEMM_TILED scales."""
+    per MMA) gives bit-identical outputs to the one reading GEMM_TILED scales,
+    in single-CTA and CTA-pair mode."""
     rng = np.random.default_rng(21 + act)
     splits, K, N = [130, 0, 257, 5, 128, 700], 512, 512
     G, M = len(splits), sum(splits)
@@ -125,12 +124,15 @@ def test_forward_nvfp4_x4_scales_match_tiled(gm, act):
              W1=bf16_cpu(rng.standard_normal((G, n1, K)) / np.sqrt(K)),
              W2=bf16_cpu(rng.standard_normal((G, K, N)) / np.sqrt(N)),
              probs=torch.from_numpy(rng.uniform(0, 1, M).astype(np.float32)))
-    y4, a4 = run_gpu(gm, d, 1, act, mask=0x3C5A, x4=True)
     yt, at = run_gpu(gm, d, 1, act, mask=0x3C5A, x4=False)
-    assert np.array_equal(np_bits(y4), np_bits(yt))
-    for key in ("fc2x_codes", "fc2x_scales", "fc2x_amax_pre", "fc2x_amax_post"):
-        assert torch.equal(a4[key], at[key]), key
-    assert torch.equal(a4["fc2x_bf16"].view(torch.int16), at["fc2x_bf16"].view(torch.int16))
+    own = torch.from_numpy(tiled_index(splits, N // 16).reshape(-1)).cuda()
+    for mode, x4 in ((0, True), (2, True), (2, False)):
+        y4, a4 = run_gpu(gm, d, 1, act, mask=0x3C5A, x4=x4, gemm_mode=mode)
+        assert np.array_equal(np_bits(y4), np_bits(yt)), (mode, x4)
+        for key in ("fc2x_codes", "fc2x_amax_pre", "fc2x_amax_post"):
+            assert torch.equal(a4[key], at[key]), (key, mode, x4)
+        assert torch.equal(a4["fc2x_scales"][own], at["fc2x_scales"][own]), (mode, x4)
+        assert torch.equal(a4["fc2x_bf16"].view(torch.int16), at["fc2x_bf16"].view(torch.int16)), (mode, x4)
 
 
 @pytest.mark.parametrize("use_rht", [True, False])

@@ -120,7 +120,7 @@ def test_colwise_equals_rowwise_of_the_transposed_groups(orc):
 def test_recompute_fc2x_equals_the_forward_fc2x(orc):
     """fc2_x rebuilt from the forward's saved activation input h is the
     forward's own fc2_x bit for bit (SwiGLU and SReLU, MXFP8 and NVFP4, random
-    operands): the rebuild reads h in logical column order and applies the prob
+    operands; tanh-SReLU too): the rebuild reads h in logical column order and applies the prob
     and the bf16 rounding exactly where the forward does.  For NVFP4 this is
     the pages' recompute on / off equality (PR #3837, Description): the rebuilt
     tensor, cast column-wise with the forward's saved amaxes, gives the same
@@ -129,11 +129,12 @@ def test_recompute_fc2x_equals_the_forward_fc2x(orc):
     d = make_inputs("tiny")
     sp = d["splits"].numpy()
     for fmt in (orc.MXFP8, orc.NVFP4):
-        for act in (orc.SWIGLU, orc.SRELU):
+        for act in (orc.SWIGLU, orc.SRELU, orc.TANH_SRELU):
             W1 = d["W1"] if act == orc.SWIGLU else d["W1"][:, :d["W2"].shape[2]].contiguous()
+            c = 8.0 if act == orc.TANH_SRELU else None
             fwd = orc.forward(bits(d["x"]), sp, bits(W1), bits(d["W2"]), d["probs"].numpy(), act, fmt,
-                              rht_mask=0x2D4B)
-            again = orc.recompute_fc2x(fwd["h"], d["probs"].numpy(), act)
+                              rht_mask=0x2D4B, tanh_clamp_scale=c)
+            again = orc.recompute_fc2x(fwd["h"], d["probs"].numpy(), act, c)
             assert np.array_equal(again, fwd["fc2x"]), (fmt, act)
             assert np.count_nonzero(fwd["fc2x"]) > fwd["fc2x"].size // 4
             if fmt == orc.NVFP4:
