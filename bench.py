@@ -475,10 +475,11 @@ def e2e_pipelined(gmlp, args, w, x, probs, splits, y, x_h, p_h, s_h, W1, W2, act
 def mma_ceiling(gmlp, fmt: int, iters: int = 32768, reps: int = 5) -> dict:
     """Tensor-core ceiling of the GEMM mainloop's MMA shape: gmlp_mma_peak on
     every SM (no global memory), with the per-stage scale copies of GEMM_TILED
-    weight scales, of GEMM_TILED_X4 ones (NVFP4), and with none."""
-    names = {1: "with_scale_copies", 2: "with_x4_scale_copies", 0: "scales_resident"}
+    weight scales, of GEMM_TILED_X4 ones (NVFP4), with the scales written into
+    tensor memory by the warps (tcgen05.st), and with none."""
+    names = {1: "with_scale_copies", 2: "with_x4_scale_copies", 3: "scales_written_by_warps", 0: "scales_resident"}
     out = {}
-    for copy in ((1, 2, 0) if fmt == gmlp.NVFP4 else (1, 0)):
+    for copy in ((1, 2, 3, 0) if fmt == gmlp.NVFP4 else (1, 3, 0)):
         for _ in range(3):
             gmlp.mma_peak(fmt, copy, iters)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

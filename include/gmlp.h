@@ -469,7 +469,9 @@ GMLP_API gmlp_status gmlp_selftest_bounded_wait(uint64_t limit_ns, gmlp_stream s
  * MMAs (K = 32 for GMLP_MXFP8, 64 for GMLP_NVFP4) and one commit, preceded by
  * the stage's scale-factor copies to TMEM as in the GEMM: scale_copy 0 none
  * (copied once up front), 1 those for GEMM_TILED weight scales (3 for MXFP8,
- * 12 for NVFP4), 2 (NVFP4 only) those for GEMM_TILED_X4 weight scales (4 + 4).
+ * 12 for NVFP4), 2 (NVFP4 only) those for GEMM_TILED_X4 weight scales (4 + 4),
+ * 3 none: the CTA's four warps write each stage's scale factors into their
+ * TMEM lane quarters with tcgen05.st while earlier stages' MMAs run.
  * Reads and writes no global memory.
  * One launch performs ctas * iters * 4 * 2 * 128 * 256 * K floating-point
  * operations; time it with events on `stream`.  A stage waits for the MMAs of

@@ -968,8 +968,8 @@ gmlp_status gmlp_replicate_weight_scales(const uint8_t* tiled, int32_t G, int64_
 gmlp_status gmlp_mma_peak(int32_t format, int32_t scale_copy, int64_t iters, int32_t ctas, gmlp_stream stream) {
   g_last_error[0] = 0;
   if (format != GMLP_MXFP8 && format != GMLP_NVFP4) return fail(GMLP_ERR_INVALID_ARG, "format %d", format);
-  if (scale_copy < 0 || scale_copy > 2 || (scale_copy == 2 && format != GMLP_NVFP4))
-    return fail(GMLP_ERR_INVALID_ARG, "scale_copy %d (0, 1, or 2 for NVFP4)", scale_copy);
+  if (scale_copy < 0 || scale_copy > 3 || (scale_copy == 2 && format != GMLP_NVFP4))
+    return fail(GMLP_ERR_INVALID_ARG, "scale_copy %d (0, 1, 3, or 2 for NVFP4)", scale_copy);
   if (iters < 1 || iters > (int64_t(1) << 24))
     return fail(GMLP_ERR_INVALID_ARG, "iters %lld outside [1, 2^24]", (long long)iters);
   GMLP_TRY(check_device());

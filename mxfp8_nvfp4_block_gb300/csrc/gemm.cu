@@ -929,6 +929,19 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_u16(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int box_cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int gemm_read_clear_status() { return read_clear_status(); }
 
 // Single-CTA tiles unless the caller asks for CTA pairs.  Biases and the

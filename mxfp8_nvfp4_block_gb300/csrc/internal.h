@@ -63,7 +63,7 @@ struct ColQuantArgs {
   int row_tiled;
   uint8_t* col_codes;
   uint8_t* col_scales;
-  uint32_t sgn[16];         // set by the launcher: 0x80008000 for the rows the sign mask negates
+  uint32_t sgn[16];         // set by the launcher: 0x80000000 (the FP32 sign bit) for the rows the mask negates
 };
 cudaError_t launch_col_quant(const ColQuantArgs& a, cudaStream_t s);
 
@@ -160,6 +160,10 @@ int num_sms();
 // box_bytes (gemm.cu); false if the driver entry point or the encode fails.
 bool make_tmap(CUtensorMap* m, const void* base, int64_t row_bytes, int64_t rows, int box_bytes, int box_rows,
                CUtensorMapSwizzle swz);
+
+// 2D 16-bit tensor map over [rows][cols] (row stride cols * 2 bytes) with a box
+// of box_cols x box_rows, no swizzle; out-of-range elements read as zero.
+bool make_tmap_u16(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int box_cols, int box_rows);
 
 cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_mma_peak(int format, int scale_copy, int64_t iters, int ctas, cudaStream_t s);

@@ -12,7 +12,11 @@
 // copied once before the loop, which isolates the copy cost; 1: the copies of
 // GEMM_TILED weight scales (3 per stage for MXFP8, 12 for NVFP4); 2 (NVFP4):
 // those of GEMM_TILED_X4 weight scales (4 SFA copies and 4 128x256b SFB copies
-// per stage, all from the stage's first 6 KB of scale bytes).
+// per stage, all from the stage's first 6 KB of scale bytes); 3: no copies --
+// the four warps write each stage's scale factors into their own lane
+// quarters of TMEM with tcgen05.st (the layout the 32x128b.warpx4 copies
+// produce) while the MMAs of earlier stages run, and signal the issuing
+// thread through an mbarrier.
 #include "device.cuh"
 
 namespace gmlp {
@@ -30,7 +34,7 @@ struct PeakCfg {
   static constexpr int kStageBytes = kATile + kBTile + 3 * kSfBytes;
   static constexpr uint32_t kSfCols = FMT == GMLP_MXFP8 ? 16 : 48;
   static constexpr uint32_t kSfbOff = FMT == GMLP_MXFP8 ? 4 : 16;
-  static constexpr size_t kSmem = (size_t)kStagesP * kStageBytes + 1024 + 256;
+  static constexpr size_t kSmem = (size_t)kStagesP * kStageBytes + 1024 + 256 + 64;
 };
 
 __device__ __forceinline__ uint32_t mix32(uint32_t x) {
@@ -62,6 +66,52 @@ __device__ __forceinline__ uint32_t scale_word(uint32_t i) {
   return FMT == GMLP_MXFP8 ? (0x78787878u + (h & 0x0f0f0f0fu)) : (0x30303030u + (h & 0x1f1f1f1fu));
 }
 
+// 16 / 32 consecutive 32-bit TMEM columns of this warp's 32 lanes from registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Scale factors of one stage from shared memory into this warp's lane quarter
+// of TMEM, in the layout the 32x128b.warpx4 copies produce: lane l, column c
+// of a 512-byte block's four columns holds the block's 4-byte word 4 l + c.
+template <int FMT>
+__device__ __forceinline__ void write_stage_scales(uint32_t lane_base, uint32_t sfa_t, uint32_t sfb_t,
+                                                   const uint8_t* sfa, const uint8_t* sfb, int lane) {
+  uint32_t r[16];
+  if (FMT == GMLP_MXFP8) {  // SFA one block (4 columns), SFB two blocks (8 columns): 12 of 16 columns
+    const uint4 a = *reinterpret_cast<const uint4*>(sfa + 16 * lane);
+    const uint4 b0 = *reinterpret_cast<const uint4*>(sfb + 16 * lane);
+    const uint4 b1 = *reinterpret_cast<const uint4*>(sfb + 512 + 16 * lane);
+    const uint32_t w[16] = {a.x, a.y, a.z, a.w, b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w, 0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = w[i];
+    tmem_st16(lane_base | sfa_t, r);
+  } else {  // SFA four blocks (16 columns); SFB per MMA k the two halves' blocks (8 columns), 32 columns
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 a = *reinterpret_cast<const uint4*>(sfa + 512 * k + 16 * lane);
+      r[4 * k] = a.x, r[4 * k + 1] = a.y, r[4 * k + 2] = a.z, r[4 * k + 3] = a.w;
+    }
+    tmem_st16(lane_base | sfa_t, r);
+#pragma unroll
+    for (int hk = 0; hk < 2; ++hk) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // columns 8k .. 8k + 7 for k = 2 hk + j / 2
+        const int k = 2 * hk + (j >> 1), h = j & 1;
+        const uint4 b = *reinterpret_cast<const uint4*>(sfb + 2048 * h + 512 * k + 16 * lane);
+        r[4 * j] = b.x, r[4 * j + 1] = b.y, r[4 * j + 2] = b.z, r[4 * j + 3] = b.w;
+      }
+      tmem_st16(lane_base | (sfb_t + 16 * hk), r);
+    }
+  }
+}
+
 template <int FMT, int SFCOPY>
 __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters) {
   using C = PeakCfg<FMT>;
@@ -72,7 +122,8 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters
   uint8_t* sSF = sB + kStagesP * kBTile;  // per stage: SFA block(s), then the two SFB halves
   uint64_t* done = reinterpret_cast<uint64_t*>(sSF + kStagesP * 3 * C::kSfBytes);
   uint64_t* retired = done + 1;  // one per stage
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(retired + kStagesP);
+  uint64_t* sfready = retired + kStagesP;  // SFCOPY 3: one per stage, 4 warp arrivals
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sfready + kStagesP);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -89,7 +140,10 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters
     tmem_alloc(tslot, 512);
   } else if (threadIdx.x == 0) {
     mbar_init(done, 1);
-    for (int s = 0; s < kStagesP; ++s) mbar_init(&retired[s], 1);
+    for (int s = 0; s < kStagesP; ++s) {
+      mbar_init(&retired[s], 1);
+      mbar_init(&sfready[s], 4);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -98,7 +152,63 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  if (threadIdx.x == 0) {
+  if (SFCOPY == 3) {
+    // all four warps write scale factors; thread 0 also issues the MMAs
+    const uint32_t sf_base = tbase + 256;
+    const int lane = threadIdx.x & 31;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    bool ok = true;
+    for (int64_t it = 0; it < iters && ok; ++it) {
+      const int stage = (int)(it & (kStagesP - 1));
+      const uint32_t sfa_t = sf_base + stage * C::kSfCols;
+      const uint32_t sfb_t = sfa_t + C::kSfbOff;
+      if (it >= kStagesP) {  // the MMAs that read this stage's scale columns have completed
+        ok = mbar_wait(&retired[stage], (uint32_t)((it / kStagesP - 1) & 1), abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const uint8_t* sfa = sSF + stage * 3 * C::kSfBytes;
+      write_stage_scales<FMT>(lane_base, sfa_t, sfb_t, sfa, sfa + C::kSfBytes, lane);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfready[stage]);
+      if (threadIdx.x == 0) {
+        ok = mbar_wait(&sfready[stage], (uint32_t)((it / kStagesP) & 1), abort_flag);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * kATile);
+          const uint32_t b_addr = smem_u32(sB + stage * kBTile);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = smem_desc(a_addr + 32 * k, 16, 1024, 2);
+            const uint64_t bd = smem_desc(b_addr + 32 * k, 16, 1024, 2);
+            const uint32_t acc = (it > 0 || k > 0) ? 1u : 0u;
+            if (FMT == GMLP_MXFP8) {
+              const uint32_t idesc = (256u >> 3 << 17) | (1u << 23) | (128u >> 4 << 24) | (uint32_t(k) << 4) |
+                                     (uint32_t(k) << 29);
+              tc_mma_mxf8(tbase, ad, bd, idesc, sfa_t, sfb_t, acc);
+            } else {
+              const uint32_t idesc = (1u << 7) | (1u << 10) | (256u >> 3 << 17) | (128u >> 4 << 24);
+              tc_mma_nvf4(tbase, ad, bd, idesc, sfa_t + 4 * k, sfb_t + 8 * k, acc);
+            }
+          }
+          tc_commit(&retired[stage]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0 && !*abort_flag;
+    }
+    if (threadIdx.x == 0) {
+      // every tcgen05 operation issued above completes before TMEM is freed
+      tc_commit(done);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(done, 0))
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          report_device_error(GMLP_ERR_DEVICE_TIMEOUT);
+          break;
+        }
+    }
+  } else if (threadIdx.x == 0) {
     const uint32_t sf_base = tbase + 256;
     auto copy_scales = [&](int stage) {
       const uint32_t sfa_t = sf_base + stage * C::kSfCols;
@@ -183,8 +293,11 @@ cudaError_t launch_peak_t(int64_t iters, int ctas, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_mma_peak(int format, int scale_copy, int64_t iters, int ctas, cudaStream_t s) {
-  if (format == GMLP_MXFP8)
+  if (format == GMLP_MXFP8) {
+    if (scale_copy == 3) return launch_peak_t<GMLP_MXFP8, 3>(iters, ctas, s);
     return scale_copy ? launch_peak_t<GMLP_MXFP8, 1>(iters, ctas, s) : launch_peak_t<GMLP_MXFP8, 0>(iters, ctas, s);
+  }
+  if (scale_copy == 3) return launch_peak_t<GMLP_NVFP4, 3>(iters, ctas, s);
   if (scale_copy == 2) return launch_peak_t<GMLP_NVFP4, 2>(iters, ctas, s);
   return scale_copy ? launch_peak_t<GMLP_NVFP4, 1>(iters, ctas, s) : launch_peak_t<GMLP_NVFP4, 0>(iters, ctas, s);
 }

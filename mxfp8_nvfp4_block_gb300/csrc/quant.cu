@@ -529,10 +529,11 @@ __global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const uint16_t*
 
 // ------------------------------------------------------------------ row + column NVFP4 cast
 
-// The 16-point FWHT stages of fwht16 on two columns at once.
-__device__ __forceinline__ void fwht16x2(f32x2* w) {
+// The 16-point FWHT stages of fwht16 on two columns at once (packed FP32
+// pairs): the first three stages (h = 1, 2, 4), then the last (h = 8).
+__device__ __forceinline__ void fwht16x2_first3(f32x2* w) {
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1)
+  for (int h = 1; h < 8; h <<= 1)
 #pragma unroll
     for (int i = 0; i < 16; ++i)
       if (!(i & h)) {
@@ -542,63 +543,178 @@ __device__ __forceinline__ void fwht16x2(f32x2* w) {
       }
 }
 
+__device__ __forceinline__ void fwht16x2_last(f32x2* w) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const f32x2 p = w[i], q = w[i + 8];
+    w[i] = add2(p, q);
+    w[i + 8] = sub2(p, q);
+  }
+}
+
+// a * b + c on 32-bit integers (modulo 2^32).
+__device__ __forceinline__ uint32_t umad(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+// Max |x| over the 16 bf16 values of two vectors, as amax8_bits does for 8.
+__device__ __forceinline__ uint32_t amax16_bits(const uint4& v, const uint4& u) {
+  uint32_t m = bmax_abs2(bmax_abs2(bmax_abs2(v.x, v.y), bmax_abs2(v.z, v.w)),
+                         bmax_abs2(bmax_abs2(u.x, u.y), bmax_abs2(u.z, u.w)));
+  m = bmax_abs2(m, __byte_perm(m, 0, 0x1032)) & 0x7fffu;
+  return m > 0x7f80u ? 0u : m;
+}
+
 // fp32(b / 6) for an FP32 block max b: the product with fp32(1/6) and one
 // residual correction equals the IEEE quotient for every b in [2^-125,
 // FLT_MAX] (checked exhaustively on the CPU); tiny, infinite or NaN b take the
 // IEEE division.
-__device__ __forceinline__ float div6(float b) {
+__device__ __forceinline__ bool div6_fast_ok(float b) {
+  return b >= __uint_as_float(0x01000000u) && b <= 3.402823466e38f;
+}
+__device__ __forceinline__ float div6_fast(float b) {
   const float r6 = __uint_as_float(0x3e2aaaabu);  // fp32(1/6)
-  if (b >= __uint_as_float(0x01000000u) && b <= 3.402823466e38f) {
-    const float q1 = __fmul_rn(b, r6);
-    return __fmaf_rn(__fmaf_rn(-6.0f, q1, b), r6, q1);
+  const float q1 = __fmul_rn(b, r6);
+  return __fmaf_rn(__fmaf_rn(-6.0f, q1, b), r6, q1);
+}
+__device__ __noinline__ float div6_ieee(float b) { return __fdiv_rn(b, 6.0f); }
+
+// Row + column NVFP4 cast on 64-row x 256-column tiles of one group, fed by
+// TMA.  Warp 8 is the producer: it streams the block's tiles (a contiguous
+// range, 64-row blocks fastest, so consecutive tiles continue each column's
+// columnwise run) into two shared-memory buffers, one mbarrier pair each.
+// Warps 0-7 compute, each on its own part of the tile, with no block-wide
+// barrier:
+//   rowwise (ROW): rows 8w .. 8w+7; lane l holds columns 8l .. 8l+7 of a row, a
+//     16-column block spans lanes 2m, 2m+1; the lanes' codes make one
+//     contiguous 128-byte run per row;
+//   columnwise: columns 32w .. 32w+31 in packed FP32 pairs; lane l takes pair
+//     l % 16 in the 16-row chunks l / 16 and l / 16 + 2: sign mask and 16-point
+//     FWHT (RHT), x 1/4, block scale, codes.  Rows past the group's end count
+//     as zero.  The warp stages its columns' codes and scales for the tile (4
+//     chunks, 32 + 4 bytes per column) and writes each column's run with four
+//     adjacent lanes, so global stores go out in 32-byte runs.
+constexpr int kRcRows = 64, kRcCols = 256, kRcWarps = 8, kRcBufs = 2;
+constexpr int kRcThreads = (kRcWarps + 1) * 32;
+constexpr int kRcTileBytes = kRcRows * kRcCols * 2;
+constexpr int kRcColStride = 40;  // staged codes per column: 4 chunks x 8 bytes + 8 bytes of bank padding
+
+struct RcShared {
+  uint16_t tile[kRcBufs][kRcRows * kRcCols];
+  uint8_t ccode[kRcWarps][32 * kRcColStride];
+  uint8_t cscale[kRcWarps][32 * 4];
+  float enc[kRcWarps][2][128];  // per warp: row and column encode factors of its current group
+  uint64_t full[kRcBufs];
+  uint64_t empty[kRcBufs];
+  int abort_flag;
+};
+
+// Walks a contiguous range of tiles in order (group, slab, 64-row block),
+// block fastest, without a division per tile.
+struct RcWalk {
+  int g, slab, blk, nblk, nvalid;
+
+  __device__ __forceinline__ void start(const SmemGroups& t, int G, int64_t u) {
+    g = find_unit_group(t, G, u);
+    const int m = t.off[g + 1] - t.off[g];
+    nblk = (m + kRcRows - 1) / kRcRows;
+    const int local = (int)(u - t.up[g]);
+    slab = local / nblk;
+    blk = local - slab * nblk;
+    nvalid = min(kRcRows, m - kRcRows * blk);
   }
-  return __fdiv_rn(b, 6.0f);
-}
 
-// Word k (0..3) of a 16-byte vector.
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
-  return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
-}
+  // the next tile (called only while one remains)
+  __device__ __forceinline__ void next(const SmemGroups& t, int slabs) {
+    if (++blk == nblk) {
+      blk = 0;
+      if (++slab == slabs) {
+        slab = 0;
+        do ++g; while (t.off[g + 1] == t.off[g]);  // skip empty groups
+        nblk = (t.off[g + 1] - t.off[g] + kRcRows - 1) / kRcRows;
+      }
+    }
+    nvalid = min(kRcRows, t.off[g + 1] - t.off[g] - kRcRows * blk);
+  }
+};
 
-// Row + column NVFP4 cast.  Work units are (group, 256-column slab, 16-row
-// chunk counted from the group's first row), chunk fastest; each warp takes a
-// contiguous range of units, so consecutive chunks of one slab (the adjacent
-// 8-byte pieces of each column's columnwise codes) go out back to back.  Lane
-// l holds 16 rows x 8 columns (col0 = slab * 256 + 8 l) in registers, rows
-// past the group's end as zeros:
-//   rowwise (ROW): a 16-column block spans lanes 2m, 2m+1; the lanes' row
-//     codes make a contiguous 128-byte run per row;
-//   columnwise: each of the lane's 8 columns is one 16-row block: sign mask
-//     and 16-point FWHT (RHT) in packed FP32 pairs of columns, x 1/4, block
-//     scale, codes; 8 code bytes and 1 scale byte per column and chunk.
-// No shared memory but the per-warp encode tables, no block-wide barrier.
 template <bool ROW, bool RHT, bool TILED>
-__global__ void __launch_bounds__(kThreads, 2) rowcol_quant_kernel(ColQuantArgs a) {
+__global__ void __launch_bounds__(kRcThreads, 2)
+    rowcol_quant_kernel(const __grid_constant__ CUtensorMap tmx, const ColQuantArgs a) {
   __shared__ SmemGroups t;
-  __shared__ float enc_tab[kWarps][2][128];  // per warp: row and column encode factors of its current group
+  extern __shared__ uint8_t rc_raw[];
+  RcShared& sm = *reinterpret_cast<RcShared*>((reinterpret_cast<uintptr_t>(rc_raw) + 127) & ~uintptr_t(127));
   const int64_t K = a.K;
-  const int slabs = (int)((K + 255) / 256);
-  build_group_tables(a.grp, slabs, t, 16);
+  const int slabs = (int)((K + kRcCols - 1) / kRcCols);
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < kRcBufs; ++b) {
+      mbar_init(&sm.full[b], 1);
+      mbar_init(&sm.empty[b], kRcWarps);
+    }
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  build_group_tables(a.grp, slabs, t, kRcRows);  // ends with a block barrier
   griddep_wait();
   griddep_launch_dependents();
   if (t.bad) return;
   const int G = a.grp.G;
-  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  const int64_t units = t.up[G];
-  const int64_t warps = (int64_t)gridDim.x * kWarps;
-  const int64_t w = (int64_t)blockIdx.x * kWarps + wib;
-  const int64_t u0 = units * w / warps, u1 = units * (w + 1) / warps;
-  if (u0 >= u1) return;
-  float* enc_row = enc_tab[wib][0];
-  float* enc_col = enc_tab[wib][1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t T = t.up[G];
+  const int64_t u0 = T * blockIdx.x / gridDim.x, u1 = T * (blockIdx.x + 1) / gridDim.x;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (warp == kRcWarps) {
+    // ---------------- producer
+    if (lane == 0 && u0 < u1) {
+      prefetch_tmap(&tmx);
+      uint32_t armed = 0;
+      RcWalk tl;
+      tl.start(t, G, u0);
+      int64_t it = 0;
+      const uint64_t pol = policy_evict_first();
+      for (int64_t u = u0; u < u1; ++u, ++it) {
+        const int b = (int)(it & 1);
+        const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+        if (it > 0) tl.next(t, slabs);
+        if (it >= kRcBufs && !mbar_wait(&sm.empty[b], ph ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(&sm.full[b], kRcTileBytes);
+        armed |= 1u << b;
+        tma_load_2d(sm.tile[b], &tmx, tl.slab * kRcCols, t.off[tl.g] + kRcRows * tl.blk, &sm.full[b], pol);
+      }
+      // the last loads of each buffer land before the block exits
+      for (int b = 0; b < kRcBufs; ++b) {
+        if (!(armed & (1u << b))) continue;
+        const int64_t last = it - 1 - ((it - 1 - b) & 1);  // last load index into buffer b
+        mbar_wait_drain(&sm.full[b], (uint32_t)(last >> 1) & 1u);
+      }
+    }
+    return;
+  }
+
+  // ---------------- compute warps
+  float* enc_row = sm.enc[warp][0];
+  float* enc_col = sm.enc[warp][1];
+  uint8_t* cstage = sm.ccode[warp];
+  uint8_t* sstage = sm.cscale[warp];
   const int nscale_row = (int)(K / 16);
-  int g = find_unit_group(t, G, u0), g_tab = -1;
+  int g_tab = -1;
   float S_row = 0.0f, S_col = 0.0f;
-  for (int64_t u = u0; u < u1; ++u) {
-    while (t.up[g + 1] <= u) ++g;
-    if (g != g_tab) {
-      S_row = ROW ? nvfp4_global_scale(a.amax_row[g]) : 0.0f;
-      S_col = nvfp4_global_scale(a.amax_col[g]);
+  uint32_t sg[16];  // the sign mask as FP32 sign bits per row, kept in registers
+#pragma unroll
+  for (int i = 0; i < 16; ++i) sg[i] = RHT ? a.sgn[i] : 0u;
+  RcWalk tl;
+  if (u0 < u1) tl.start(t, G, u0);
+  int64_t it = 0;
+  for (int64_t u = u0; u < u1; ++u, ++it) {
+    const int b = (int)(it & 1);
+    const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+    if (it > 0) tl.next(t, slabs);
+    if (tl.g != g_tab) {
+      S_row = ROW ? nvfp4_global_scale(a.amax_row[tl.g]) : 0.0f;
+      S_col = nvfp4_global_scale(a.amax_col[tl.g]);
       __syncwarp();
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -606,86 +722,161 @@ __global__ void __launch_bounds__(kThreads, 2) rowcol_quant_kernel(ColQuantArgs 
         enc_col[lane + 32 * i] = nvfp4_enc(S_col, (uint32_t)(lane + 32 * i));
       }
       __syncwarp();
-      g_tab = g;
+      g_tab = tl.g;
     }
-    const Unit un = decode_unit(t, g, u, K, lane);
-    uint4 v[16];
-    load_unit(a.x, K, un, v);
+    const int64_t row0 = (int64_t)t.off[tl.g] + kRcRows * tl.blk;
+    const int64_t col0 = (int64_t)tl.slab * kRcCols;
+    const int nch = (tl.nvalid + 15) >> 4;
+    if (!mbar_wait(&sm.full[b], ph, abort_flag)) break;
+    const uint16_t* tile = sm.tile[b];
 
     if (ROW) {
-      // rowwise NVFP4: lanes 2m, 2m+1 share block m of the slab (16 columns)
-      const int kblk = (int)(un.col0 >> 4);  // this lane pair's block column
-      uint8_t* crow = a.row_codes + un.row0 * (K / 2) + (un.col0 >> 1);
-      uint8_t* srow;
-      int64_t sstep;
-      if (TILED) {
-        const int lr0 = 16 * un.j, rr0 = lr0 & 127;
-        srow = a.row_scales + ((int64_t)(t.tb[g] + (lr0 >> 7)) * (nscale_row >> 2) + (kblk >> 2)) * 512 +
-               (rr0 & 31) * 16 + (rr0 >> 5) * 4;
-        sstep = 16;
-      } else {
-        srow = a.row_scales + un.row0 * nscale_row + kblk;
-        sstep = nscale_row;
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (i < un.nvalid) {
-          uint32_t m = amax8_bits(v[i]);
-          m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-          const uint32_t sf = nvfp4_block_sf_bf16(m, S_row);
-          float q[8];
-          scale8(v[i], enc_row[sf], q);
-          const uint32_t sw = gather4_bytes(sf, 2);
-          if (un.active) {
-            *reinterpret_cast<uint32_t*>(crow + i * (K / 2)) = e2m1_pack8(q);
-            if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(srow + i * sstep) = sw;
-          }
+      // lane l: block l % 16 (columns 16 (l % 16) ..) of rows 8w + 2k + l / 16
+      const int bl = lane & 15;
+      const int64_t gcol = col0 + 16 * bl;
+      const bool active = gcol < K;
+      const int kblk = (int)(gcol >> 4);
+      const int r0 = 8 * warp + (lane >> 4);  // this lane's first row; then r0 + 2, r0 + 4, r0 + 6
+      uint8_t* cptr = a.row_codes + (row0 + r0) * (K / 2) + (gcol >> 1);
+      // the scale word of row r: a 64-row tile is one half (64 (blk & 1) ..) of a
+      // 128-row scale tile, so the tile is fixed and row r sits at (r % 32) * 16 + (r / 32) * 4
+      uint8_t* sptr;
+      if (TILED)
+        sptr = a.row_scales + ((int64_t)(t.tb[tl.g] + (tl.blk >> 1)) * (nscale_row >> 2) + (kblk >> 2)) * 512 +
+               (tl.blk & 1) * 8;
+      else
+        sptr = a.row_scales + row0 * nscale_row + kblk;
+#pragma unroll 2
+      for (int k = 0; k < 4; ++k) {
+        const int r = r0 + 2 * k;
+        if (8 * warp + 2 * k >= tl.nvalid) break;
+        const uint4 v0 = *reinterpret_cast<const uint4*>(tile + r * kRcCols + 16 * bl);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(tile + r * kRcCols + 16 * bl + 8);
+        const uint32_t sf = nvfp4_block_sf_bf16(amax16_bits(v0, v1), S_row);
+        const float enc = enc_row[sf];
+        float q0[8], q1[8];
+        scale8(v0, enc, q0);
+        scale8(v1, enc, q1);
+        const uint32_t sw = gather4_bytes(sf, 1);
+        if (active && r < tl.nvalid) {
+          *reinterpret_cast<uint2*>(cptr + 2 * k * (K / 2)) = make_uint2(e2m1_pack8(q0), e2m1_pack8(q1));
+          if ((lane & 3) == 0)
+            *reinterpret_cast<uint32_t*>(sptr + (TILED ? (r & 31) * 16 + (r >> 5) * 4 : (int64_t)r * nscale_row)) = sw;
         }
       }
     }
 
-    // columnwise NVFP4: per column pair, the 16 rows as packed FP32 pairs
-    const int64_t mpad = (int64_t)(t.mp[g + 1] - t.mp[g]);
-    uint8_t* ccol = a.col_codes + K * (int64_t)t.mp[g] / 2 + un.col0 * (mpad / 2) + 8 * un.j;
-    uint8_t* scol = a.col_scales + K * (int64_t)t.mp[g] / 16 + un.col0 * (mpad / 16) + un.j;
-#pragma unroll
-    for (int cp = 0; cp < 4; ++cp) {
+    // columnwise: pair p of this warp's 16 column pairs, chunks c and c + 2
+    const uint32_t* tile32 = reinterpret_cast<const uint32_t*>(tile);
+    const int p = lane & 15, pr = 16 * warp + p;
+#pragma unroll 1
+    for (int q2 = 0; q2 < 2; ++q2) {
+      // every lane runs the item (the warp votes below); a lane whose chunk is
+      // past the tile's rows works on zeros and stores nothing
+      const int c = (lane >> 4) + 2 * q2;
+      if (2 * q2 >= nch) break;  // no lane of the warp has a chunk left
+      const bool live = c < nch;
       f32x2 y[16];
+      uint32_t wv[16];
+      const uint32_t* src = tile32 + 16 * c * (kRcCols / 2) + pr;
+      if (16 * c + 16 <= tl.nvalid) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) wv[i] = src[i * (kRcCols / 2)];
+      } else {  // the group's last chunk: rows past its end count as zero
+#pragma unroll
+        for (int i = 0; i < 16; ++i) wv[i] = 16 * c + i < tl.nvalid ? src[i * (kRcCols / 2)] : 0u;
+      }
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        uint32_t wd = word_of(v[i], cp);
-        if (RHT) wd ^= a.sgn[i];  // the sign mask on row i of both columns
-        y[i] = pk2(__uint_as_float(wd << 16), __uint_as_float(wd & 0xFFFF0000u));
+        // the two bf16 values widened to FP32 with row i's sign from the mask:
+        // lo = wd * 2^16 + s (adding 2^31 flips the top bit), hi = (wd & 0xFFFF0000) ^ s
+        y[i] = pk2(__uint_as_float(umad(wv[i], 65536u, sg[i])), __uint_as_float((wv[i] & 0xFFFF0000u) ^ sg[i]));
       }
+      float b0 = 0.0f, b1 = 0.0f, b0r = 0.0f, b1r = 0.0f;  // b*r: max |y| before the quarter
       if (RHT) {
-        fwht16x2(y);
-        const f32x2 quarter = pk2(0.25f, 0.25f);
+        fwht16x2_first3(y);
+        // max |y| over the last stage's outputs (p + q, p - q) is fp32(|p| + |q|)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] = mul2(y[i], quarter);
-      }
-      float b0 = 0.0f, b1 = 0.0f;
+        for (int i = 0; i < 8; ++i) {
+          b0 = fmaxf(b0, fabsf(lo2(y[i])) + fabsf(lo2(y[i + 8])));
+          b1 = fmaxf(b1, fabsf(hi2(y[i])) + fabsf(hi2(y[i + 8])));
+        }
+        fwht16x2_last(y);
+        b0r = b0;
+        b1r = b1;
+        b0 = __fmul_rn(b0, 0.25f);  // = max |fp32(y / 4)|: scaling by 1/4 rounds monotonically
+        b1 = __fmul_rn(b1, 0.25f);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        b0 = fmaxf(b0, fabsf(lo2(y[i])));
-        b1 = fmaxf(b1, fabsf(hi2(y[i])));
+        for (int i = 0; i < 16; ++i) {
+          b0 = fmaxf(b0, fabsf(lo2(y[i])));
+          b1 = fmaxf(b1, fabsf(hi2(y[i])));
+        }
       }
-      const uint32_t sf0 = e4m3x2(__fmul_rn(div6(b0), S_col), 0.0f) & 0xFF;
-      const uint32_t sf1 = e4m3x2(__fmul_rn(div6(b1), S_col), 0.0f) & 0xFF;
-      const f32x2 enc = pk2(enc_col[sf0], enc_col[sf1]);
+      float d0, d1;
+      if (__all_sync(0xffffffffu, !live || (div6_fast_ok(b0) && div6_fast_ok(b1)))) {  // the usual case
+        d0 = div6_fast(b0);
+        d1 = div6_fast(b1);
+      } else {
+        d0 = div6_fast_ok(b0) ? div6_fast(b0) : div6_ieee(b0);
+        d1 = div6_fast_ok(b1) ? div6_fast(b1) : div6_ieee(b1);
+      }
+      const uint32_t sf0 = e4m3x2(__fmul_rn(d0, S_col), 0.0f) & 0xFF;
+      const uint32_t sf1 = e4m3x2(__fmul_rn(d1, S_col), 0.0f) & 0xFF;
+      const float e0 = enc_col[sf0], e1 = enc_col[sf1];
+      f32x2 enc = pk2(e0, e1);
+      if (RHT) {
+        // fp32(fp32(y / 4) * enc) == fp32(y * (enc / 4)) whenever y / 4 and enc / 4
+        // are exact (no subnormal); elements below 2^-124 in a block whose max
+        // is at least 2^-100 quantise to a zero of their sign either way.  So
+        // the quarter folds into the encode factor unless a block is that
+        // small or enc is below 2^-124.
+        const float kTiny = __uint_as_float(0x0d800000u), kEnc = __uint_as_float(0x01800000u);  // 2^-100, 2^-124
+        if (__all_sync(0xffffffffu, !live || (b0r >= kTiny && b1r >= kTiny && e0 >= kEnc && e1 >= kEnc))) {
+          enc = pk2(__fmul_rn(e0, 0.25f), __fmul_rn(e1, 0.25f));
+        } else {  // some lane of the warp has a block below the fold's range: all take the plain path
+          const f32x2 quarter = pk2(0.25f, 0.25f);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) y[i] = mul2(y[i], quarter);
+        }
+      }
       float p0[16], p1[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const f32x2 q = mul2(y[i], enc);
-        p0[i] = lo2(q);
-        p1[i] = hi2(q);
+        const f32x2 qv = mul2(y[i], enc);
+        p0[i] = lo2(qv);
+        p1[i] = hi2(qv);
       }
-      if (un.active) {
-        *reinterpret_cast<uint2*>(ccol + (2 * cp) * (mpad / 2)) = make_uint2(e2m1_pack8(p0), e2m1_pack8(p0 + 8));
-        *reinterpret_cast<uint2*>(ccol + (2 * cp + 1) * (mpad / 2)) = make_uint2(e2m1_pack8(p1), e2m1_pack8(p1 + 8));
-        scol[(2 * cp) * (mpad / 16)] = (uint8_t)sf0;
-        scol[(2 * cp + 1) * (mpad / 16)] = (uint8_t)sf1;
+      if (live) {
+        *reinterpret_cast<uint2*>(cstage + (2 * p) * kRcColStride + 8 * c) =
+            make_uint2(e2m1_pack8(p0), e2m1_pack8(p0 + 8));
+        *reinterpret_cast<uint2*>(cstage + (2 * p + 1) * kRcColStride + 8 * c) =
+            make_uint2(e2m1_pack8(p1), e2m1_pack8(p1 + 8));
+        sstage[(2 * p) * 4 + c] = (uint8_t)sf0;
+        sstage[(2 * p + 1) * 4 + c] = (uint8_t)sf1;
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[b]);  // this warp is done reading the tile
+
+    // the warp's 32 columns: each column's chunks of this tile as one run, four lanes per column
+    const int64_t mpad = (int64_t)(t.mp[tl.g + 1] - t.mp[tl.g]);
+    const int c = lane & 3;
+    const int64_t gc0 = col0 + 32 * warp + (lane >> 2);  // this lane's column in step i: gc0 + 8 i
+    uint8_t* cp = a.col_codes + K * (int64_t)t.mp[tl.g] / 2 + gc0 * (mpad / 2) + 8 * (4 * tl.blk + c);
+    uint8_t* sp = a.col_scales + K * (int64_t)t.mp[tl.g] / 16 + gc0 * (mpad / 16) + 4 * tl.blk + c;
+    if (c < nch) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int cl = 8 * i + (lane >> 2);
+        if (gc0 + 8 * i < K) {
+          *reinterpret_cast<uint2*>(cp + 8 * i * (mpad / 2)) =
+              *reinterpret_cast<const uint2*>(cstage + cl * kRcColStride + 8 * c);
+          sp[8 * i * (mpad / 16)] = sstage[cl * 4 + c];
+        }
+      }
+    }
+    __syncwarp();  // the staging buffers are free for the next tile
   }
 }
 
@@ -885,15 +1076,34 @@ cudaError_t launch_fc2x_recompute(const uint16_t* h, const float* probs, int64_t
 template <bool ROW, bool RHT, bool TILED>
 cudaError_t launch_rowcol_t(const ColQuantArgs& a, cudaStream_t s) {
   auto kern = rowcol_quant_kernel<ROW, RHT, TILED>;
-  const int64_t units = ((a.M + 15) / 16 + a.grp.G) * ((a.K + 255) / 256);
-  kern<<<grid_for(kern, units), kThreads, 0, s>>>(a);
+  constexpr size_t smem = sizeof(RcShared) + 128;
+  static bool attr[64] = {};
+  static int per_sm[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kRcThreads, smem);
+    if (e != cudaSuccess) return e;
+    per_sm[dev & 63] = n < 1 ? 1 : n;
+    attr[dev & 63] = true;
+  }
+  CUtensorMap tmx;
+  if (!make_tmap_u16(&tmx, a.x, a.K, a.M, kRcCols, kRcRows)) return cudaErrorInvalidValue;
+  const int64_t tiles = ((a.M + kRcRows - 1) / kRcRows + a.grp.G) * ((a.K + kRcCols - 1) / kRcCols);
+  int64_t grid = (int64_t)num_sms() * per_sm[dev & 63];
+  if (grid > tiles) grid = tiles;
+  if (grid < 1) grid = 1;
+  kern<<<(unsigned)grid, kRcThreads, smem, s>>>(tmx, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_col_quant(const ColQuantArgs& a0, cudaStream_t s) {
-  if (a0.M == 0 && a0.grp.G == 0) return cudaSuccess;
+  if (a0.M == 0) return cudaSuccess;
   ColQuantArgs a = a0;
-  for (int i = 0; i < 16; ++i) a.sgn[i] = ((a.mask >> i) & 1u) ? 0x80008000u : 0u;
+  for (int i = 0; i < 16; ++i) a.sgn[i] = ((a.mask >> i) & 1u) ? 0x80000000u : 0u;
   const bool row = a.row_codes != nullptr;
   if (a.use_rht) {
     if (!row) return launch_rowcol_t<false, true, false>(a, s);

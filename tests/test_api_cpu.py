@@ -145,7 +145,7 @@ def test_mma_peak_argument_checks(lib):
     assert L.gmlp_mma_peak(g.NVFP4, 0, (1 << 24) + 1, 0, None) == g.ERR_INVALID_ARG
     assert b"iters" in L.gmlp_last_error()
     assert L.gmlp_mma_peak(g.MXFP8, 2, 100, 0, None) == g.ERR_INVALID_ARG       # X4 copies are NVFP4's
-    assert L.gmlp_mma_peak(g.NVFP4, 3, 100, 0, None) == g.ERR_INVALID_ARG
+    assert L.gmlp_mma_peak(g.NVFP4, 4, 100, 0, None) == g.ERR_INVALID_ARG
     assert b"scale_copy" in L.gmlp_last_error()
     assert g.mma_peak_flops(g.MXFP8, 10, 2) == 2 * 10 * 4 * 2 * 128 * 256 * 32
     assert g.mma_peak_flops(g.NVFP4, 10, 2) == 2 * 10 * 4 * 2 * 128 * 256 * 64

@@ -151,6 +151,31 @@ def test_nvfp4_row_col_with_amax_bitexact(orc, gm, case, rowwise, use_rht):
         assert np.array_equal(orc.tiled_to_compact(np_u8(out["row"][1]), splits, K // 16), ref["row_scales"])
 
 
+@pytest.mark.parametrize("scale_exp", [-110, -126, -133])
+def test_nvfp4_row_col_tiny_groups_bitexact(orc, gm, scale_exp):
+    """Groups whose values all lie far below 2^-100 (down to bf16 subnormals),
+    beside a group of ordinary magnitude: the columnwise RHT cast's quarter
+    scaling cannot fold into the encode factor there and takes the plain path;
+    codes and scales bit-exact, own amaxes."""
+    splits = np.array([48, 37, 16, 1], dtype=np.int64)
+    M, K = int(splits.sum()), 384
+    rng = np.random.default_rng(-scale_exp)
+    x = rng.standard_normal((M, K))
+    x[48:] *= 2.0 ** scale_exp
+    x = bf16_cpu(x)
+    pre, post = orc.group_hadamard_amax(bits(x), splits, 0x9E37)
+    rec = gm.recipe(gm.NVFP4, use_rht=True, mask=0x9E37, layout=1)
+    out = gpu_call(gm, gm.group_quantize_with_amax, x.cuda(), torch.from_numpy(splits).cuda(), rec,
+                   torch.from_numpy(pre).cuda(), torch.from_numpy(post).cuda(), rowwise=True, columnwise=True,
+                   splits_host=splits.tolist())
+    ref = orc.group_quantize_with_amax(bits(x), splits, orc.NVFP4, pre, post, rowwise=True, columnwise=True,
+                                       use_rht=True, mask=0x9E37)
+    assert np.array_equal(np_u8(out["col"][0], len(ref["col_codes"])), ref["col_codes"])
+    assert np.array_equal(np_u8(out["col"][1], len(ref["col_scales"])), ref["col_scales"])
+    assert np.array_equal(np_u8(out["row"][0], M * K // 2).reshape(M, K // 2), ref["row_codes"])
+    assert np.array_equal(orc.tiled_to_compact(np_u8(out["row"][1]), splits, K // 16), ref["row_scales"])
+
+
 @pytest.mark.parametrize("fmt", [0, 1], ids=["mxfp8", "nvfp4"])
 @pytest.mark.parametrize("swiglu", [False, True])
 def test_prepare_weights_bitexact(orc, gm, fmt, swiglu):
@@ -223,7 +248,7 @@ def test_mma_peak_loop_runs_at_a_plausible_rate(gm, fmt):
     4.5 PFLOP/s, FP4 13.5 PFLOP/s): far above would mean it skips work."""
     nominal = 4500.0 if fmt == gm.MXFP8 else 13500.0
     ctas = torch.cuda.get_device_properties(0).multi_processor_count
-    for copy in ((1, 2, 0) if fmt == gm.NVFP4 else (1, 0)):
+    for copy in ((1, 2, 3, 0) if fmt == gm.NVFP4 else (1, 3, 0)):
         gm.mma_peak(fmt, copy, 256)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
