@@ -22,7 +22,9 @@
 //             registers, frees the accumulator at once (so the next tile's
 //             mainloop overlaps the epilogue math), then computes and stores.
 // Tiles: (expert g, 128-row tile of g's tokens, 256-column output tile),
-// ordered expert-major and handed out round-robin to the persistent CTAs.
+// ordered expert-major and handed out round-robin to the persistent CTAs;
+// within an expert the order keeps the smaller operand resident in L2
+// (decode_tile).
 #include <cudaTypedefs.h>
 
 #include <cstring>
@@ -84,8 +86,13 @@ struct Tile {
   int g, mt, nt;
 };
 
+// Tile w of the expert-major work list.  Within an expert the tiles that run
+// at the same time (consecutive w, dealt round-robin to the CTAs) share one
+// operand and stream the other, which must then stay in L2 until the expert is
+// done: the expert's weight rows (n-tile fastest) when it has more tokens than
+// weight rows, else its tokens (m-tile fastest).
 template <int TILE_ROWS>
-__device__ __forceinline__ Tile decode_tile(const int* off, const int* ip, int G, int w) {
+__device__ __forceinline__ Tile decode_tile(const int* off, const int* ip, int G, int w, int64_t n_out, int n_tiles) {
   int lo = 0, hi = G - 1;  // largest g with ip[g] <= w
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -93,10 +100,16 @@ __device__ __forceinline__ Tile decode_tile(const int* off, const int* ip, int G
   }
   Tile t;
   t.g = lo;
-  const int mtiles = (off[lo + 1] - off[lo] + TILE_ROWS - 1) / TILE_ROWS;
+  const int m = off[lo + 1] - off[lo];
   const int local = w - ip[lo];
-  t.nt = local / mtiles;
-  t.mt = local % mtiles;
+  if (m > n_out) {
+    t.mt = local / n_tiles;
+    t.nt = local - t.mt * n_tiles;
+  } else {
+    const int mtiles = (m + TILE_ROWS - 1) / TILE_ROWS;
+    t.nt = local / mtiles;
+    t.mt = local - t.nt * mtiles;
+  }
   return t;
 }
 
@@ -638,7 +651,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     constexpr uint32_t kTx = (uint32_t)C::kStageBytes * PAIR;
     constexpr int kSfRows = C::kSfBytes / 256;  // SF tensor-map rows per 128-row block
     for (int w = unit; w < total && !*abort_flag; w += n_units) {
-      const Tile t = decode_tile<C::kTileRows>(off, ip, G, w);
+      const Tile t = decode_tile<C::kTileRows>(off, ip, G, w, a.n_out, n_tiles);
       const int row0 = t.mt * C::kTileRows + kBM * rank;  // first row of this CTA within the group
       const int rowA = off[t.g] + row0;
       const int64_t tileA = tb[t.g] + (row0 >> 7);
@@ -765,7 +778,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     const uint32_t tempty_addr = PAIR == 2 ? mapa_shared(smem_u32(tempty), leader) : 0;
     uint32_t acc_phase = 0;
     for (int w = unit; w < total && !*abort_flag; w += n_units) {
-      const Tile t = decode_tile<C::kTileRows>(off, ip, G, w);
+      const Tile t = decode_tile<C::kTileRows>(off, ip, G, w, a.n_out, n_tiles);
       const int row_base = t.mt * C::kTileRows + kBM * rank;
       float prob = 1.0f;
       if (EPI != EPI_FC2 && a.probs) {
