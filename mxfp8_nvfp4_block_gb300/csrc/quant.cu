@@ -581,30 +581,38 @@ __device__ __forceinline__ float div6_fast(float b) {
 }
 __device__ __noinline__ float div6_ieee(float b) { return __fdiv_rn(b, 6.0f); }
 
-// Row + column NVFP4 cast on 64-row x 256-column tiles of one group, fed by
+// Row + column NVFP4 cast on 64-row x 128-column tiles of one group, fed by
 // TMA.  Warp 8 is the producer: it streams the block's tiles (a contiguous
 // range, 64-row blocks fastest, so consecutive tiles continue each column's
 // columnwise run) into two shared-memory buffers, one mbarrier pair each.
 // Warps 0-7 compute, each on its own part of the tile, with no block-wide
 // barrier:
-//   rowwise (ROW): rows 8w .. 8w+7; lane l holds columns 8l .. 8l+7 of a row, a
-//     16-column block spans lanes 2m, 2m+1; the lanes' codes make one
-//     contiguous 128-byte run per row;
-//   columnwise: columns 32w .. 32w+31 in packed FP32 pairs; lane l takes pair
-//     l % 16 in the 16-row chunks l / 16 and l / 16 + 2: sign mask and 16-point
-//     FWHT (RHT), x 1/4, block scale, codes.  Rows past the group's end count
-//     as zero.  The warp stages its columns' codes and scales for the tile (4
-//     chunks, 32 + 4 bytes per column) and writes each column's run with four
-//     adjacent lanes, so global stores go out in 32-byte runs.
-constexpr int kRcRows = 64, kRcCols = 256, kRcWarps = 8, kRcBufs = 2;
+//   rowwise (ROW): rows 8w .. 8w+7, four at a time; lane l casts the 16-column
+//     block l % 8 of row 8w + l / 8 (+ 4): block max, scale, eight code bytes;
+//     four adjacent lanes make one 32-bit scale word;
+//   columnwise: columns 16w .. 16w+15 in packed FP32 pairs; lane l takes pair
+//     l % 8 in the 16-row chunk l / 8: sign mask and 16-point FWHT (RHT),
+//     x 1/4, block scale, codes.  Rows past the group's end count as zero.
+//     The warp stages its columns' codes and scales for the tile (4 chunks,
+//     32 + 4 bytes per column) and writes each column's run with four adjacent
+//     lanes, so global stores go out in 32-byte runs.
+// 128-column tiles at two blocks per SM measured faster than 256-column ones
+// (more tiles in flight per SM for the same shared memory).
+constexpr int kRcRows = 64, kRcCols = 128, kRcWarps = 8, kRcBufs = 2, kRcBlocksPerSM = 2;
 constexpr int kRcThreads = (kRcWarps + 1) * 32;
 constexpr int kRcTileBytes = kRcRows * kRcCols * 2;
 constexpr int kRcColStride = 40;  // staged codes per column: 4 chunks x 8 bytes + 8 bytes of bank padding
+constexpr int kRcRowLanes = kRcCols / 16;              // rowwise: lanes per row (one 16-column block each)
+constexpr int kRcRowsPerPass = 32 / kRcRowLanes;       // rows a warp casts per pass
+constexpr int kRcPairs = kRcCols / 2 / kRcWarps;       // columnwise: column pairs per warp
+constexpr int kRcChunkLanes = 32 / kRcPairs;           // lanes sharing a pair, one 16-row chunk each
+constexpr int kRcColsPerWarp = 2 * kRcPairs;
+static_assert(kRcRowsPerPass * (8 / kRcRowsPerPass) == 8 && kRcChunkLanes <= 4 && 4 % kRcChunkLanes == 0, "tile");
 
 struct RcShared {
   uint16_t tile[kRcBufs][kRcRows * kRcCols];
-  uint8_t ccode[kRcWarps][32 * kRcColStride];
-  uint8_t cscale[kRcWarps][32 * 4];
+  uint8_t ccode[kRcWarps][kRcColsPerWarp * kRcColStride];
+  uint8_t cscale[kRcWarps][kRcColsPerWarp * 4];
   float enc[kRcWarps][2][128];  // per warp: row and column encode factors of its current group
   uint64_t full[kRcBufs];
   uint64_t empty[kRcBufs];
@@ -641,7 +649,7 @@ struct RcWalk {
 };
 
 template <bool ROW, bool RHT, bool TILED>
-__global__ void __launch_bounds__(kRcThreads, 2)
+__global__ void __launch_bounds__(kRcThreads, kRcBlocksPerSM)
     rowcol_quant_kernel(const __grid_constant__ CUtensorMap tmx, const ColQuantArgs a) {
   __shared__ SmemGroups t;
   extern __shared__ uint8_t rc_raw[];
@@ -731,12 +739,12 @@ __global__ void __launch_bounds__(kRcThreads, 2)
     const uint16_t* tile = sm.tile[b];
 
     if (ROW) {
-      // lane l: block l % 16 (columns 16 (l % 16) ..) of rows 8w + 2k + l / 16
-      const int bl = lane & 15;
+      // lane l: block l % kRcRowLanes (16 columns) of rows 8w + kRcRowsPerPass k + l / kRcRowLanes
+      const int bl = lane % kRcRowLanes;
       const int64_t gcol = col0 + 16 * bl;
       const bool active = gcol < K;
       const int kblk = (int)(gcol >> 4);
-      const int r0 = 8 * warp + (lane >> 4);  // this lane's first row; then r0 + 2, r0 + 4, r0 + 6
+      const int r0 = 8 * warp + lane / kRcRowLanes;  // this lane's first row, then every kRcRowsPerPass
       uint8_t* cptr = a.row_codes + (row0 + r0) * (K / 2) + (gcol >> 1);
       // the scale word of row r: a 64-row tile is one half (64 (blk & 1) ..) of a
       // 128-row scale tile, so the tile is fixed and row r sits at (r % 32) * 16 + (r / 32) * 4
@@ -746,10 +754,10 @@ __global__ void __launch_bounds__(kRcThreads, 2)
                (tl.blk & 1) * 8;
       else
         sptr = a.row_scales + row0 * nscale_row + kblk;
-#pragma unroll 2
-      for (int k = 0; k < 4; ++k) {
-        const int r = r0 + 2 * k;
-        if (8 * warp + 2 * k >= tl.nvalid) break;
+#pragma unroll
+      for (int k = 0; k < 8 / kRcRowsPerPass; ++k) {
+        const int r = r0 + kRcRowsPerPass * k;
+        if (8 * warp + kRcRowsPerPass * k >= tl.nvalid) break;
         const uint4 v0 = *reinterpret_cast<const uint4*>(tile + r * kRcCols + 16 * bl);
         const uint4 v1 = *reinterpret_cast<const uint4*>(tile + r * kRcCols + 16 * bl + 8);
         const uint32_t sf = nvfp4_block_sf_bf16(amax16_bits(v0, v1), S_row);
@@ -759,22 +767,23 @@ __global__ void __launch_bounds__(kRcThreads, 2)
         scale8(v1, enc, q1);
         const uint32_t sw = gather4_bytes(sf, 1);
         if (active && r < tl.nvalid) {
-          *reinterpret_cast<uint2*>(cptr + 2 * k * (K / 2)) = make_uint2(e2m1_pack8(q0), e2m1_pack8(q1));
+          *reinterpret_cast<uint2*>(cptr + kRcRowsPerPass * k * (K / 2)) = make_uint2(e2m1_pack8(q0), e2m1_pack8(q1));
           if ((lane & 3) == 0)
             *reinterpret_cast<uint32_t*>(sptr + (TILED ? (r & 31) * 16 + (r >> 5) * 4 : (int64_t)r * nscale_row)) = sw;
         }
       }
     }
 
-    // columnwise: pair p of this warp's 16 column pairs, chunks c and c + 2
+    // columnwise: pair p of this warp's kRcPairs column pairs, 16-row chunks
+    // lane / kRcPairs + kRcChunkLanes q2
     const uint32_t* tile32 = reinterpret_cast<const uint32_t*>(tile);
-    const int p = lane & 15, pr = 16 * warp + p;
+    const int p = lane % kRcPairs, pr = kRcPairs * warp + p;
 #pragma unroll 1
-    for (int q2 = 0; q2 < 2; ++q2) {
+    for (int q2 = 0; q2 < 4 / kRcChunkLanes; ++q2) {
       // every lane runs the item (the warp votes below); a lane whose chunk is
       // past the tile's rows works on zeros and stores nothing
-      const int c = (lane >> 4) + 2 * q2;
-      if (2 * q2 >= nch) break;  // no lane of the warp has a chunk left
+      const int c = lane / kRcPairs + kRcChunkLanes * q2;
+      if (kRcChunkLanes * q2 >= nch) break;  // no lane of the warp has a chunk left
       const bool live = c < nch;
       f32x2 y[16];
       uint32_t wv[16];
@@ -859,15 +868,15 @@ __global__ void __launch_bounds__(kRcThreads, 2)
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[b]);  // this warp is done reading the tile
 
-    // the warp's 32 columns: each column's chunks of this tile as one run, four lanes per column
+    // the warp's columns: each column's chunks of this tile as one run, four lanes per column
     const int64_t mpad = (int64_t)(t.mp[tl.g + 1] - t.mp[tl.g]);
     const int c = lane & 3;
-    const int64_t gc0 = col0 + 32 * warp + (lane >> 2);  // this lane's column in step i: gc0 + 8 i
+    const int64_t gc0 = col0 + kRcColsPerWarp * warp + (lane >> 2);  // this lane's column in step i: gc0 + 8 i
     uint8_t* cp = a.col_codes + K * (int64_t)t.mp[tl.g] / 2 + gc0 * (mpad / 2) + 8 * (4 * tl.blk + c);
     uint8_t* sp = a.col_scales + K * (int64_t)t.mp[tl.g] / 16 + gc0 * (mpad / 16) + 4 * tl.blk + c;
     if (c < nch) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < kRcColsPerWarp / 8; ++i) {
         const int cl = 8 * i + (lane >> 2);
         if (gc0 + 8 * i < K) {
           *reinterpret_cast<uint2*>(cp + 8 * i * (mpad / 2)) =

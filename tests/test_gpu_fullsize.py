@@ -7,9 +7,11 @@ configuration the benchmark uses (persistent grids, many work units per CTA).
   Hadamard-amax pass and the quantize-with-amax cast; Description: the
   fc2-input group quantize, row + column): amax_pre / amax_post, rowwise codes
   and GEMM_TILED scales, columnwise RHT codes and scales.
-* The forward's x casts at the workloads' hidden sizes: NVFP4 at K = 4096
-  (32768 tokens with 0.1% outliers x50) and MXFP8 at K = 7168 (65536 tokens in
-  64 Zipf-routed experts, tail experts of 0-8 tokens).
+* The forward's x casts on each forward workload's whole x: MXFP8 at K = 256
+  (512 tokens in 4 ragged experts) and K = 2048 (16384 tokens, Dirichlet
+  routing with an empty expert), NVFP4 at K = 4096 (32768 tokens with 0.1%
+  outliers x50) and MXFP8 at K = 7168 (65536 tokens in 64 Zipf-routed experts,
+  tail experts of 0-8 tokens).
 
 Inputs come from the seeded generators; the oracle sees only their host
 copies and its own results.
@@ -80,7 +82,8 @@ def test_nv_quant_group_quantize_fullsize(orc, gm, nv_quant):
     _compare_row_col(orc, out, ref, s, M, K)
 
 
-@pytest.mark.parametrize("name,fmt", [("nv_srelu", 1), ("mx_skew", 0)], ids=["nvfp4_K4096", "mxfp8_K7168"])
+@pytest.mark.parametrize("name,fmt", [("tiny", 0), ("mx_swiglu", 0), ("nv_srelu", 1), ("mx_skew", 0)],
+                         ids=["mxfp8_K256", "mxfp8_K2048", "nvfp4_K4096", "mxfp8_K7168"])
 def test_forward_x_cast_fullsize(orc, gm, name, fmt):
     """The forward's x cast (rowwise, GEMM_TILED scales: fc1's A operand) on
     the workload's whole x."""
