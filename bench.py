@@ -196,8 +196,9 @@ def forward_leg(gmlp, name: str, args, dev, world: int, steps: int, warmup: int,
     x = d["x"].to(dev)
     splits = d["splits"].to(dev)
     probs = d["probs"].to(dev)
-    W1 = gmlp.prepare_weights(d["W1"].to(dev), fmt, swiglu_interleave=(act == gmlp.SWIGLU))
-    W2 = gmlp.prepare_weights(d["W2"].to(dev), fmt)
+    x4 = {"auto": None, "x4": True, "tiled": False}[args.weight_scales]
+    W1 = gmlp.prepare_weights(d["W1"].to(dev), fmt, swiglu_interleave=(act == gmlp.SWIGLU), x4=x4)
+    W2 = gmlp.prepare_weights(d["W2"].to(dev), fmt, x4=x4)
     if not keep_weights:
         del d["W1"], d["W2"]
     y = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=dev)
@@ -280,7 +281,9 @@ def forward_leg(gmlp, name: str, args, dev, world: int, steps: int, warmup: int,
                    "l2": L2_TEXT[args.l2_flush],
                    "timing": "value: per-step start/end events; stages_ms and roofline: a second timed pass with "
                              "an event after every kernel",
-                   "weights": "quantised once before timing", "flops_per_step": w.flops,
+                   "weights": "quantised once before timing; scales read in the " + (
+                       "replicated GEMM_TILED_X4 layout" if W1.scales_x4 is not None else "GEMM_TILED layout"),
+                   "flops_per_step": w.flops,
                    "gemm_mode": args.gemm_mode,
                    "fc2x_columnwise": bool(colwise)},
         "gpu_launches": steps * n_stage,
@@ -327,8 +330,15 @@ def forward_leg(gmlp, name: str, args, dev, world: int, steps: int, warmup: int,
     out["kernels"] = kern
     ceiling = mma_ceiling(gmlp, fmt)
     out["roofline"]["mma_loop_tflops"] = ceiling
-    # the loop with the copy mix the forward's GEMM issues (NVFP4 weights carry X4 scales)
-    loop = ceiling["with_x4_scale_copies" if fmt == gmlp.NVFP4 else "with_scale_copies"]
+    # the loop with the scale-factor path the forward's fc1 GEMM takes: NVFP4 with
+    # replicated weight scales copies them (X4); with GEMM_TILED ones, single-CTA
+    # tiles have them written by warps
+    if fmt == gmlp.MXFP8:
+        loop = ceiling["with_scale_copies"]
+    elif W1.scales_x4 is not None:
+        loop = ceiling["with_x4_scale_copies"]
+    else:
+        loop = ceiling["scales_written_by_warps" if args.gemm_mode == 0 else "with_scale_copies"]
     out["roofline"]["frac_of_mma_loop"] = round(achieved / loop, 4)
 
     if e2e:
@@ -822,6 +832,9 @@ def main():
     ap.add_argument("--no-extra", dest="extra", action="store_false",
                     help="skip the other workloads' forward legs (nv_srelu, mx_swiglu)")
     ap.add_argument("--extra-steps", type=int, default=50, help="timed steps of each extra leg (at most --steps)")
+    ap.add_argument("--weight-scales", default="auto", choices=["auto", "x4", "tiled"],
+                    help="weight scale layout the forward GEMMs read: the binding's default (auto), the replicated "
+                         "GEMM_TILED_X4 copy (NVFP4 only), or GEMM_TILED")
     ap.add_argument("--fc2x-colwise", action="store_true",
                     help="NVFP4: also write the columnwise (RHT) NVFP4 fc2_x each step (no-recompute training path)")
     ap.add_argument("--l2-flush", default="clean", choices=["write", "clean"],

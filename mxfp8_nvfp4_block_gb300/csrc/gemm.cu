@@ -35,7 +35,6 @@ namespace gmlp {
 
 namespace {
 
-constexpr int kThreadsGemm = 576;  // 2 control warps + 16 epilogue warps
 constexpr int kEpiWarps = 16;
 constexpr int kBM = 128, kBN = 256, kBKBytes = 128;
 constexpr int kATileBytes = kBM * kBKBytes;  // 16 KB
@@ -50,9 +49,10 @@ constexpr uint32_t kTmemCols = 512;
 // X4 (NVFP4): the B scales come replicated four times (weight layout
 // GEMM_TILED_X4), so one 128x256b copy places the scales of both 128-row
 // halves of the B tile for one MMA, replacing two 32x128b.warpx4 copies; each
-// copy instruction costs the same tensor-pipe time whatever its size, and
-// NVFP4 needs 12 of the small ones per stage.  A single-CTA stage is then
-// 66 KB (3 stages fit); a CTA-pair stage, with half the B tile, 50 KB (4).
+// copy instruction costs about the same tensor-pipe time whatever its size
+// (40-60 cycles), and NVFP4 needs 12 of the small ones per stage.  A
+// single-CTA stage is then 66 KB (3 stages fit); a CTA-pair stage, with half
+// the B tile, 50 KB (4).
 template <int FMT, int PAIR, bool X4 = false>
 struct Cfg {
   // bytes of scale factors per 128 rows per stage: MXFP8 4 scales/row (one
@@ -67,6 +67,14 @@ struct Cfg {
   static constexpr uint32_t kSfbOff = FMT == GMLP_MXFP8 ? 4 : 16;   // SFB after SFA within a stage
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes;
   static constexpr int kTileRows = kBM * PAIR;
+  // SST (NVFP4, GEMM_TILED weight scales, single CTA): no scale-factor copies;
+  // four scale-writer warps (after the 2 control and 16 epilogue warps) store
+  // each stage's scales into TMEM with tcgen05.st (12 small copies per stage
+  // otherwise)
+  static constexpr bool kSST = FMT == GMLP_NVFP4 && !X4 && PAIR == 1;
+  static constexpr int kEpiWarp0 = 2;  // first epilogue warp
+  static constexpr int kScaleWarp0 = kEpiWarp0 + kEpiWarps;
+  static constexpr int kThreads = 32 * (kScaleWarp0 + (kSST ? 4 : 0));
 };
 
 // Instruction descriptor (tcgen05 block-scaled kinds): A/B formats in bits
@@ -537,7 +545,7 @@ __device__ __forceinline__ void tc_mma_g(uint32_t d, uint64_t adesc, uint64_t bd
 // ------------------------------------------------------------------ kernel
 
 template <int FMT, int EPI, int PAIR, bool X4, bool XT>
-__global__ void __launch_bounds__(kThreadsGemm, 1)
+__global__ void __launch_bounds__(Cfg<FMT, PAIR, X4>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const GemmArgs a) {
@@ -554,7 +562,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sfready = drain + 1;  // SST: one per stage, the four scale writers arrive
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sfready + S);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   int* bad = reinterpret_cast<int*>(tslot + 2);
   int* off = reinterpret_cast<int*>(tslot + 4);
@@ -630,6 +639,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     mbar_init(tfull, 1);
     mbar_init(tempty, kEpiWarps * PAIR);
     mbar_init(drain, 1);
+    if (C::kSST)
+      for (int s = 0; s < S; ++s) mbar_init(&sfready[s], 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -715,7 +726,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       tc_fence_after();
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+        if (!mbar_wait(&full[stage], phase, abort_flag) ||
+            (C::kSST && !mbar_wait(&sfready[stage], phase, abort_flag))) {
           ok = false;
           break;
         }
@@ -730,6 +742,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           tc_cp_g<PAIR>(sfa_t, smem_desc(sfa_addr, 0, 128, 0));
           tc_cp_g<PAIR>(sfb_t, smem_desc(sfb_addr, 0, 128, 0));
           tc_cp_g<PAIR>(sfb_t + 4, smem_desc(sfb_addr + 512, 0, 128, 0));
+        } else if (C::kSST) {
+          // the scale writers have placed this stage's scales
         } else if (X4) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -770,11 +784,40 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     // all MMAs and copies this thread issued complete before TMEM is freed
     tc_commit_g<PAIR>(drain);
     mbar_wait_drain(drain, 0);
-  } else if (warp >= 2) {
+  } else if (C::kSST && warp >= C::kScaleWarp0) {
+    // ---------------- scale writers: warp w stores each stage's SFA / SFB into
+    // TMEM lanes 32 * (w % 4) .. + 31, in the layout the 32x128b.warpx4 copies
+    // would produce, and signals the issuer; the stage's shared memory is not
+    // refilled before the issuer's commit, which follows the signal
+    const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
+    const uint32_t sf_base = tbase + kAccCols;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int w = unit; ok && w < total && !*abort_flag; w += n_units) {
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sfa_t = sf_base + stage * C::kSfCols;
+        const uint8_t* sfa = sSFA + stage * C::kSfBytes;
+        write_stage_scales<FMT>(lane_base, sfa_t, sfa_t + C::kSfbOff, sfa, sSFB + stage * C::kSfBBytes, lane);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfready[stage]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp >= C::kEpiWarp0) {
     // ---------------- epilogue: 16 warps; warp w reads TMEM lanes 32 * (w % 4)
-    // and the 64-column slice (w - 2) / 4 of this CTA's 128 accumulator rows
+    // and the 64-column slice (w - kEpiWarp0) / 4 of this CTA's 128 accumulator rows
     const int q = warp & 3;
-    const int slice = (warp - 2) >> 2;
+    const int slice = (warp - C::kEpiWarp0) >> 2;
     const uint32_t tempty_addr = PAIR == 2 ? mapa_shared(smem_u32(tempty), leader) : 0;
     uint32_t acc_phase = 0;
     for (int w = unit; w < total && !*abort_flag; w += n_units) {
@@ -868,7 +911,7 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(kThreadsGemm);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -970,6 +1013,9 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
 #define GMLP_LAUNCH(F, E)                                        \
   if (pair) return launch_t<F, E, 2, false, false>(a, s);        \
   GMLP_ONE(F, E, false)
+#define GMLP_X4(F, E)                                    \
+  if (pair) return launch_t<F, E, 2, true, false>(a, s); \
+  GMLP_ONE(F, E, true)
   if (a.format == GMLP_MXFP8) {
     if (a.epi == EPI_FC1_SWIGLU) { GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_SWIGLU); }
     if (a.epi == EPI_FC1_SRELU) { GMLP_LAUNCH(GMLP_MXFP8, EPI_FC1_SRELU); }
@@ -979,19 +1025,16 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
     GMLP_LAUNCH(GMLP_MXFP8, EPI_FC2);
   }
   if (a.b_x4) {  // replicated B scales
-#define GMLP_X4(E)                                                 \
-  if (pair) return launch_t<GMLP_NVFP4, E, 2, true, false>(a, s); \
-  GMLP_ONE(GMLP_NVFP4, E, true)
-    if (a.epi == EPI_FC1_SWIGLU) { GMLP_X4(EPI_FC1_SWIGLU); }
-    if (a.epi == EPI_FC1_SRELU) { GMLP_X4(EPI_FC1_SRELU); }
-    if (a.epi == EPI_FC1_TANH_SRELU) { GMLP_X4(EPI_FC1_TANH_SRELU); }
-    GMLP_X4(EPI_FC2);
-#undef GMLP_X4
+    if (a.epi == EPI_FC1_SWIGLU) { GMLP_X4(GMLP_NVFP4, EPI_FC1_SWIGLU); }
+    if (a.epi == EPI_FC1_SRELU) { GMLP_X4(GMLP_NVFP4, EPI_FC1_SRELU); }
+    if (a.epi == EPI_FC1_TANH_SRELU) { GMLP_X4(GMLP_NVFP4, EPI_FC1_TANH_SRELU); }
+    GMLP_X4(GMLP_NVFP4, EPI_FC2);
   }
   if (a.epi == EPI_FC1_SWIGLU) { GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SWIGLU); }
   if (a.epi == EPI_FC1_SRELU) { GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_SRELU); }
   if (a.epi == EPI_FC1_TANH_SRELU) { GMLP_LAUNCH(GMLP_NVFP4, EPI_FC1_TANH_SRELU); }
   GMLP_LAUNCH(GMLP_NVFP4, EPI_FC2);
+#undef GMLP_X4
 #undef GMLP_LAUNCH
 #undef GMLP_ONE
 }

@@ -66,52 +66,6 @@ __device__ __forceinline__ uint32_t scale_word(uint32_t i) {
   return FMT == GMLP_MXFP8 ? (0x78787878u + (h & 0x0f0f0f0fu)) : (0x30303030u + (h & 0x1f1f1f1fu));
 }
 
-// 16 / 32 consecutive 32-bit TMEM columns of this warp's 32 lanes from registers.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Scale factors of one stage from shared memory into this warp's lane quarter
-// of TMEM, in the layout the 32x128b.warpx4 copies produce: lane l, column c
-// of a 512-byte block's four columns holds the block's 4-byte word 4 l + c.
-template <int FMT>
-__device__ __forceinline__ void write_stage_scales(uint32_t lane_base, uint32_t sfa_t, uint32_t sfb_t,
-                                                   const uint8_t* sfa, const uint8_t* sfb, int lane) {
-  uint32_t r[16];
-  if (FMT == GMLP_MXFP8) {  // SFA one block (4 columns), SFB two blocks (8 columns): 12 of 16 columns
-    const uint4 a = *reinterpret_cast<const uint4*>(sfa + 16 * lane);
-    const uint4 b0 = *reinterpret_cast<const uint4*>(sfb + 16 * lane);
-    const uint4 b1 = *reinterpret_cast<const uint4*>(sfb + 512 + 16 * lane);
-    const uint32_t w[16] = {a.x, a.y, a.z, a.w, b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w, 0, 0, 0, 0};
-#pragma unroll
-    for (int i = 0; i < 16; ++i) r[i] = w[i];
-    tmem_st16(lane_base | sfa_t, r);
-  } else {  // SFA four blocks (16 columns); SFB per MMA k the two halves' blocks (8 columns), 32 columns
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4 a = *reinterpret_cast<const uint4*>(sfa + 512 * k + 16 * lane);
-      r[4 * k] = a.x, r[4 * k + 1] = a.y, r[4 * k + 2] = a.z, r[4 * k + 3] = a.w;
-    }
-    tmem_st16(lane_base | sfa_t, r);
-#pragma unroll
-    for (int hk = 0; hk < 2; ++hk) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {  // columns 8k .. 8k + 7 for k = 2 hk + j / 2
-        const int k = 2 * hk + (j >> 1), h = j & 1;
-        const uint4 b = *reinterpret_cast<const uint4*>(sfb + 2048 * h + 512 * k + 16 * lane);
-        r[4 * j] = b.x, r[4 * j + 1] = b.y, r[4 * j + 2] = b.z, r[4 * j + 3] = b.w;
-      }
-      tmem_st16(lane_base | (sfb_t + 16 * hk), r);
-    }
-  }
-}
-
 template <int FMT, int SFCOPY>
 __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters) {
   using C = PeakCfg<FMT>;
