@@ -196,24 +196,29 @@ def forward_leg(gmlp, name: str, args, dev, world: int, steps: int, warmup: int,
     x = d["x"].to(dev)
     splits = d["splits"].to(dev)
     probs = d["probs"].to(dev)
-    x4 = {"auto": None, "x4": True, "tiled": False}[args.weight_scales]
+    x4 = {"auto": fmt == gmlp.NVFP4 and args.gemm_mode == 2, "x4": True, "tiled": False}[args.weight_scales]
     W1 = gmlp.prepare_weights(d["W1"].to(dev), fmt, swiglu_interleave=(act == gmlp.SWIGLU), x4=x4)
     W2 = gmlp.prepare_weights(d["W2"].to(dev), fmt, x4=x4)
     if not keep_weights:
         del d["W1"], d["W2"]
     y = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(gmlp.forward_workspace_size(w.M, w.K, w.N, w.G, act, rec), dtype=torch.uint8, device=dev)
-    colwise = None
+    fwd_aux = None
+    if fmt == gmlp.NVFP4:
+        # the step's own outputs for the backward: fc2_x's amaxes (pre- and
+        # post-RHT; the wgrad operand's global scale comes from the latter)
+        fwd_aux = {"fc2x_amax_pre": torch.empty(w.G, dtype=torch.float32, device=dev),
+                   "fc2x_amax_post": torch.empty(w.G, dtype=torch.float32, device=dev)}
     if args.fc2x_colwise and fmt == gmlp.NVFP4:
         # the no-recompute training variant: fc2_x also cast columnwise (RHT) in the same pass
         ncol = w.N * (w.M + 16 * w.G)
-        colwise = {"fc2x_col_codes": torch.empty(ncol // 2, dtype=torch.uint8, device=dev),
-                   "fc2x_col_scales": torch.empty(ncol // 16, dtype=torch.uint8, device=dev)}
+        fwd_aux.update({"fc2x_col_codes": torch.empty(ncol // 2, dtype=torch.uint8, device=dev),
+                        "fc2x_col_scales": torch.empty(ncol // 16, dtype=torch.uint8, device=dev)})
     flush_l2 = L2Flush(args.l2_flush, dev)
     n_stage = 3 if fmt == gmlp.MXFP8 else 5
 
     def fwd(**kw):
-        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=colwise,
+        gmlp.forward(x, splits, W1, W2, probs, act, rec, y=y, workspace=ws, gemm_mode=args.gemm_mode, aux=fwd_aux,
                      tanh_clamp_scale=w.tanh_clamp_scale, **kw)
 
     def ev():
@@ -285,7 +290,7 @@ def forward_leg(gmlp, name: str, args, dev, world: int, steps: int, warmup: int,
                        "replicated GEMM_TILED_X4 layout" if W1.scales_x4 is not None else "GEMM_TILED layout"),
                    "flops_per_step": w.flops,
                    "gemm_mode": args.gemm_mode,
-                   "fc2x_columnwise": bool(colwise)},
+                   "fc2x_columnwise": bool(fwd_aux and "fc2x_col_codes" in fwd_aux)},
         "gpu_launches": steps * n_stage,
         "stages_ms": [round(t, 5) for t in stage_ms],
         "gemm_path": {"ms": round(gemm_ms, 5), "TFLOP_s": round(w.flops / (gemm_ms * 1e-3) / 1e12, 1),
@@ -303,10 +308,12 @@ def forward_leg(gmlp, name: str, args, dev, world: int, steps: int, warmup: int,
                        "frac_hbm": round(q_bytes / (stage_ms[quant_idx] * 1e-3) / 1e9 / hbm, 4)},
         "clocks": clk.summary(),
     }
-    f_bytes = w.M * w.N * 2 + (w.M * w.N // 2 + w.M * w.N // 16) * (2 if colwise else 1)
+    has_col = bool(fwd_aux and "fc2x_col_codes" in fwd_aux)
+    f_bytes = w.M * w.N * 2 + (w.M * w.N // 2 + w.M * w.N // 16) * (2 if has_col else 1)
     if fmt == gmlp.NVFP4:
-        # fc2_x cast: bf16 in, rowwise NVFP4 out (+ the columnwise copy with --fc2x-colwise)
-        out["fc2x_cast"] = {"ms": round(stage_ms[3], 5), "bytes": f_bytes, "columnwise": bool(colwise),
+        # fc2_x cast: bf16 in, rowwise NVFP4 out and the post-RHT amax (+ the
+        # columnwise copy with --fc2x-colwise)
+        out["fc2x_cast"] = {"ms": round(stage_ms[3], 5), "bytes": f_bytes, "columnwise": has_col,
                             "GB_s": round(f_bytes / (stage_ms[3] * 1e-3) / 1e9, 1),
                             "frac_hbm": round(f_bytes / (stage_ms[3] * 1e-3) / 1e9 / hbm, 4)}
 
@@ -361,7 +368,7 @@ def forward_leg(gmlp, name: str, args, dev, world: int, steps: int, warmup: int,
         torch.cuda.synchronize()
         gmlp.check_device_status()
         e2e_seq_ms = e0.elapsed_time(e1) / steps
-        e2e_ms = e2e_pipelined(gmlp, args, w, x, probs, splits, y, x_h, p_h, s_h, W1, W2, act, rec, ws, colwise,
+        e2e_ms = e2e_pipelined(gmlp, args, w, x, probs, splits, y, x_h, p_h, s_h, W1, W2, act, rec, ws, fwd_aux,
                                steps, warmup)
         h2d = x_h.numel() * 2 + p_h.numel() * 4 + s_h.numel() * 8
         d2h = y_h.numel() * 2
@@ -422,7 +429,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
     return out
 
 
-def e2e_pipelined(gmlp, args, w, x, probs, splits, y, x_h, p_h, s_h, W1, W2, act, rec, ws, colwise,
+def e2e_pipelined(gmlp, args, w, x, probs, splits, y, x_h, p_h, s_h, W1, W2, act, rec, ws, fwd_aux,
                   K_steps: int, W_steps: int) -> float:
     """ms per step of the host-to-host forward with two slots of device and
     pinned host buffers: every step copies its x, probs and split sizes in
@@ -465,7 +472,7 @@ def e2e_pipelined(gmlp, args, w, x, probs, splits, y, x_h, p_h, s_h, W1, W2, act
             if started[b]:
                 s_cmp.wait_event(ev_out[b][k])    # the slot's previous y has been read out
         gmlp.forward(xs[b], ss[b], W1, W2, ps[b], act, rec, y=ys[b], workspace=ws, gemm_mode=args.gemm_mode,
-                     aux=colwise, tanh_clamp_scale=w.tanh_clamp_scale, stream=s_cmp)
+                     aux=fwd_aux, tanh_clamp_scale=w.tanh_clamp_scale, stream=s_cmp)
         ev_cmp[b].record(s_cmp)
         for k, st in enumerate(s_out):
             with torch.cuda.stream(st):
@@ -833,8 +840,8 @@ def main():
                     help="skip the other workloads' forward legs (nv_srelu, mx_swiglu)")
     ap.add_argument("--extra-steps", type=int, default=50, help="timed steps of each extra leg (at most --steps)")
     ap.add_argument("--weight-scales", default="auto", choices=["auto", "x4", "tiled"],
-                    help="weight scale layout the forward GEMMs read: the binding's default (auto), the replicated "
-                         "GEMM_TILED_X4 copy (NVFP4 only), or GEMM_TILED")
+                    help="weight scale layout the forward GEMMs read: auto = GEMM_TILED, except the replicated "
+                         "GEMM_TILED_X4 copy for NVFP4 in CTA-pair mode; x4 (NVFP4 only); tiled")
     ap.add_argument("--fc2x-colwise", action="store_true",
                     help="NVFP4: also write the columnwise (RHT) NVFP4 fc2_x each step (no-recompute training path)")
     ap.add_argument("--l2-flush", default="clean", choices=["write", "clean"],

@@ -605,14 +605,18 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   g1.pre_act_out = aux ? aux->fc1_pre_act : nullptr;
   g1.out_bf16 = f_bf16;
   g1.amax_pre = f_pre;
-  g1.amax_post = f_post;
+  // the post-RHT amax comes from the fc1 epilogue only when the columnwise
+  // cast below needs it up front; otherwise the rowwise cast of fc2_x takes it
+  // in its own pass over the tensor
+  const bool colwise = aux && aux->fc2x_col_codes;
+  g1.amax_post = colwise ? f_post : nullptr;
   g1.rht_mask = recipe->rht_sign_mask & 0xFFFFu;
   g1.n_cols_out = N;
     g1.pair = (aux && aux->gemm_mode == 2) ? 2 : 1;
     g1.pdl = 1;
   GMLP_CUDA(launch_gemm(g1, s), "fc1 launch");
   GMLP_TRY(mark());
-  if (aux && aux->fc2x_col_codes) {
+  if (colwise) {
     // rowwise (fc2's operand) and columnwise (RHT) NVFP4 of fc2_x in one pass,
     // both from the amaxes the fc1 epilogue produced
     ColQuantArgs c{};
@@ -630,6 +634,21 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     c.col_codes = aux->fc2x_col_codes;
     c.col_scales = aux->fc2x_col_scales;
     GMLP_CUDA(launch_col_quant(c, s), "fc2_x row + column quantise launch");
+  } else if (aux && aux->fc2x_amax_post) {
+    // rowwise NVFP4 of fc2_x (fc2's operand) and its post-RHT amax in one pass
+    ColQuantArgs c{};
+    c.x = f_bf16;
+    c.M = M;
+    c.K = N;
+    c.grp = gs;
+    c.use_rht = 1;
+    c.mask = recipe->rht_sign_mask & 0xFFFFu;
+    c.amax_row = f_pre;
+    c.row_codes = f_codes;
+    c.row_scales = f_scales;
+    c.row_tiled = 1;
+    c.amax_post_out = f_post;
+    GMLP_CUDA(launch_col_quant(c, s), "fc2_x quantise + post-RHT amax launch");
   } else {
     RowQuantArgs q{};
     q.x = f_bf16;

@@ -291,7 +291,52 @@ __device__ __forceinline__ float dglu_block(const GemmArgs& a, const uint32_t* d
   return dsum;
 }
 
-template <int FMT, int EPI, bool XT>
+// A thread's 64 bf16 outputs (its row's 128-byte run of the slice) as four
+// 32-byte units u[k].  quad_transpose swaps units inside each quad of lanes
+// (a 4 x 4 transpose in two xor-shuffle rounds) so that afterwards slot s of
+// lane 4g + r holds unit r of the quad's row 4g + s; store_quad_rows then
+// writes slot s of the four lanes as one whole 128-byte run, so each warp
+// store instruction covers 8 complete runs instead of one 32-byte piece of
+// 32 rows.  Used by the scale-writer (SST) kernels, whose bf16 outputs it
+// speeds up (NVFP4 fc2 164 -> 140 us); the other kernels measured slower
+// with it (MXFP8 fc2 on the 64-expert workload 0.76 -> 0.82 ms) and keep
+// row-per-lane stores.
+__device__ __forceinline__ void quad_transpose(uint32_t (&u)[4][8], int lane) {
+  const bool odd = lane & 1, upper = lane & 2;
+#pragma unroll
+  for (int p = 0; p < 2; ++p)
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      // after this round slot 2p + j holds unit 2p + (r & 1) of quad row (r & ~1) + j
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? u[2 * p][w] : u[2 * p + 1][w], 1);
+      if (odd)
+        u[2 * p][w] = recv;
+      else
+        u[2 * p + 1][w] = recv;
+    }
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, upper ? u[j][w] : u[2 + j][w], 2);
+      if (upper)
+        u[j][w] = recv;
+      else
+        u[2 + j][w] = recv;
+    }
+}
+
+// Stores the transposed units: rows row0 + 4 (lane / 4) + s (s = 0..3) of a
+// [rows x ld] bf16 matrix at column col0, rows at or past `limit` skipped.
+__device__ __forceinline__ void store_quad_rows(uint16_t* out, int64_t ld, int64_t row0, int limit_rel, int rel0,
+                                                int64_t col0, const uint32_t (&u)[4][8], int lane) {
+  const int rq = 4 * (lane >> 2);
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+    if (rel0 + rq + s < limit_rel) st_global_v8(out + (row0 + rq + s) * ld + col0 + 16 * (lane & 3), u[s]);
+}
+
+template <int FMT, int EPI, bool XT, bool QT>
 __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Tile& t, const int* off,
                                          const int* tb, int row_base, int q, int lane, int slice, float prob) {
   const int row = 32 * q + lane;
@@ -327,6 +372,18 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
     alpha = 1.0f;
   }
 
+  if (EPI == EPI_FC2 && QT) {
+    uint32_t u[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) u[j][k] = pack_bf16x2(acc[16 * j + 2 * k] * alpha, acc[16 * j + 2 * k + 1] * alpha);
+    quad_transpose(u, lane);
+    // warp rows 32 q .. 32 q + 31 of the tile; this lane's quad stores rows 4 (lane / 4) + s
+    store_quad_rows(a.out_bf16, a.n_cols_out, (int64_t)off[t.g] + row_base + 32 * q, m_g, row_base + 32 * q,
+                    (int64_t)t.nt * kBN + slice * kSliceCols, u, lane);
+    return;
+  }
   if (EPI == EPI_FC2) {
     if (!valid) return;
     uint16_t* yrow = a.out_bf16 + grow * a.n_cols_out + (int64_t)t.nt * kBN + slice * kSliceCols;
@@ -395,20 +452,32 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
     // 16-row column chunks (lanes 0-15 and 16-31 each hold one chunk; rows
     // past the group end count as zero).
     float pre = 0.0f, post = 0.0f;
+    const bool want_post = a.amax_post != nullptr;  // else the fc2_x cast takes it
     const bool neg = (a.rht_mask >> (lane & 15)) & 1u;
 #pragma unroll
     for (int c = 0; c < kOut; ++c) {
       float v = valid ? acc[c] : 0.0f;
       pre = fmaxf(pre, fabsf(v));
-      if (neg) v = -v;
+      if (want_post) {
+        if (neg) v = -v;
 #pragma unroll
-      for (int h = 1; h < 16; h <<= 1) {
-        const float p = __shfl_xor_sync(0xffffffffu, v, h);
-        v = (lane & h) ? (p - v) : (v + p);
+        for (int h = 1; h < 16; h <<= 1) {
+          const float p = __shfl_xor_sync(0xffffffffu, v, h);
+          v = (lane & h) ? (p - v) : (v + p);
+        }
+        post = fmaxf(post, fabsf(v));
       }
-      post = fmaxf(post, fabsf(v));
     }
-    if (valid) {
+    if (QT && kOut == 64) {
+      uint32_t u[4][8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) u[j][k] = pack_bf16x2(acc[16 * j + 2 * k], acc[16 * j + 2 * k + 1]);
+      quad_transpose(u, lane);
+      store_quad_rows(a.out_bf16, a.n_cols_out, (int64_t)off[t.g] + row_base + 32 * q, m_g, row_base + 32 * q, oc0, u,
+                      lane);
+    } else if (valid) {
       uint16_t* dst = a.out_bf16 + grow * a.n_cols_out + oc0;
 #pragma unroll
       for (int j = 0; j < kOut; j += 16) {
@@ -425,7 +494,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
     }
     if (lane == 0) {
       atomicMax(reinterpret_cast<int*>(a.amax_pre + t.g), __float_as_int(pre));
-      atomicMax(reinterpret_cast<int*>(a.amax_post + t.g), __float_as_int(post * 0.25f));
+      if (want_post) atomicMax(reinterpret_cast<int*>(a.amax_post + t.g), __float_as_int(post * 0.25f));
     }
   }
 }
@@ -881,7 +950,7 @@ __global__ void __launch_bounds__(Cfg<FMT, PAIR, X4>::kThreads, 1)
           mbar_arrive_cluster(tempty_addr);
       }
       acc_phase ^= 1;
-      epilogue<FMT, EPI, XT>(a, acc, t, off, tb, row_base, q, lane, slice, prob);
+      epilogue<FMT, EPI, XT, C::kSST>(a, acc, t, off, tb, row_base, q, lane, slice, prob);
     }
   }
   __syncthreads();

@@ -61,8 +61,9 @@ struct ColQuantArgs {
   uint8_t* row_codes;       // nullable: also write rowwise NVFP4 in the same pass
   uint8_t* row_scales;
   int row_tiled;
-  uint8_t* col_codes;
+  uint8_t* col_codes;       // nullable: then rowwise (GEMM_TILED) + amax_post_out only
   uint8_t* col_scales;
+  float* amax_post_out;     // with col_codes null: max-accumulates the post-RHT amax per group (zeroed before)
   uint32_t sgn[16];         // set by the launcher: 0x80000000 (the FP32 sign bit) for the rows the mask negates
 };
 cudaError_t launch_col_quant(const ColQuantArgs& a, cudaStream_t s);

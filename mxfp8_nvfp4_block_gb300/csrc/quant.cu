@@ -195,6 +195,12 @@ __device__ __forceinline__ uint32_t amax8_bits(const uint4& v) {
   return m > 0x7f80u ? 0u : m;
 }
 
+// The larger of the two bf16 magnitudes in a packed max (as amax8_bits).
+__device__ __forceinline__ uint32_t amax_pair_bits(uint32_t m) {
+  m = bmax_abs2(m, __byte_perm(m, 0, 0x1032)) & 0x7fffu;
+  return m > 0x7f80u ? 0u : m;
+}
+
 // Four FP32 values -> four E4M3 bytes (element 0 in the low byte).
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   uint32_t r;
@@ -416,29 +422,6 @@ __global__ void __launch_bounds__(kThreads) group_amax_kernel(const uint16_t* x,
 
 // ------------------------------------------------------------------ Hadamard helpers
 
-// 16-point FWHT in registers: stages h = 1, 2, 4, 8 mapping (w[i], w[i+h]),
-// (i & h) == 0, to (w[i] + w[i+h], w[i] - w[i+h]).
-__device__ __forceinline__ void fwht16(float* w) {
-#pragma unroll
-  for (int h = 1; h < 16; h <<= 1)
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (!(i & h)) {
-        const float p = w[i], q = w[i + h];
-        w[i] = p + q;
-        w[i + h] = p - q;
-      }
-}
-
-// Column cc (0..7) of a lane's 16 x 8 bf16 tile as 16 floats.
-__device__ __forceinline__ void column16(const uint4* v, int cc, float* w) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint32_t word = (cc >> 1) == 0 ? v[i].x : (cc >> 1) == 1 ? v[i].y : (cc >> 1) == 2 ? v[i].z : v[i].w;
-    w[i] = bf16_bits_to_float((cc & 1) ? (word >> 16) : (word & 0xFFFF));
-  }
-}
-
 // Work units: (group, 256-column slab, 16-row chunk), chunk fastest.  Each
 // warp loads its unit's 16 rows x 8 columns per lane (rows past the group end
 // are zero).
@@ -472,65 +455,9 @@ __device__ __forceinline__ void load_unit(const uint16_t* x, int64_t K, const Un
 
 // ------------------------------------------------------------------ group Hadamard-amax
 
-__global__ void __launch_bounds__(kThreads) hadamard_amax_kernel(const uint16_t* x, int64_t K, GroupSrc grp,
-                                                                 uint32_t mask, float* amax_pre,
-                                                                 float* amax_post) {
-  __shared__ SmemGroups t;
-  const int slabs = (int)((K + 255) / 256);
-  build_group_tables(grp, slabs, t);
-  griddep_wait();
-  griddep_launch_dependents();
-  if (t.bad) return;
-  const int G = grp.G;
-  const int lane = threadIdx.x & 31;
-  const int64_t units = t.up[G];
-  const int64_t warps = (int64_t)gridDim.x * kWarps;
-  const int64_t w = (int64_t)blockIdx.x * kWarps + threadIdx.x / 32;
-  const int64_t upw = (units + warps - 1) / warps;
-  const int64_t u0 = w * upw, u1 = min(units, u0 + upw);
-  if (u0 >= u1) return;
-  int g = find_unit_group(t, G, u0);
-  float pre = 0.0f, post = 0.0f;
-  for (int64_t u = u0; u < u1; ++u) {
-    if (t.up[g + 1] <= u) {
-      pre = warp_max(pre);
-      post = warp_max(post);
-      if (lane == 0) {
-        atomic_max_nonneg(amax_pre + g, pre);
-        atomic_max_nonneg(amax_post + g, post * 0.25f);
-      }
-      pre = post = 0.0f;
-      while (t.up[g + 1] <= u) ++g;
-    }
-    const Unit un = decode_unit(t, g, u, K, lane);
-    uint4 v[16];
-    load_unit(x, K, un, v);
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      float wv[16];
-      column16(v, cc, wv);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        pre = fmaxf(pre, fabsf(wv[i]));
-        if ((mask >> i) & 1u) wv[i] = -wv[i];
-      }
-      fwht16(wv);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) post = fmaxf(post, fabsf(wv[i]));
-    }
-  }
-  pre = warp_max(pre);
-  post = warp_max(post);
-  if (lane == 0) {
-    atomic_max_nonneg(amax_pre + g, pre);
-    atomic_max_nonneg(amax_post + g, post * 0.25f);
-  }
-}
-
-// ------------------------------------------------------------------ row + column NVFP4 cast
-
-// The 16-point FWHT stages of fwht16 on two columns at once (packed FP32
-// pairs): the first three stages (h = 1, 2, 4), then the last (h = 8).
+// The 16-point FWHT (stages h = 1, 2, 4, 8 mapping (w[i], w[i+h]), (i & h) ==
+// 0, to (w[i] + w[i+h], w[i] - w[i+h])) on two columns at once in packed FP32
+// pairs: the first three stages, then the last.
 __device__ __forceinline__ void fwht16x2_first3(f32x2* w) {
 #pragma unroll
   for (int h = 1; h < 8; h <<= 1)
@@ -558,6 +485,80 @@ __device__ __forceinline__ uint32_t umad(uint32_t a, uint32_t b, uint32_t c) {
   asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
   return r;
 }
+
+// The sign mask as FP32 sign bits per row (0x80000000 for a negated row).
+struct RowSigns {
+  uint32_t s[16];
+};
+
+// amax_pre: max |x| on the raw bf16 words (packed max of magnitudes); amax_post:
+// per lane, two columns at a time in packed FP32 pairs, the sign folded into
+// the widening, the first three FWHT stages, and max |y| over the last stage's
+// outputs (p + q, p - q) taken as fp32(|p| + |q|), which equals it; x 1/4 at
+// the end.
+__global__ void __launch_bounds__(kThreads, 2) hadamard_amax_kernel(const uint16_t* x, int64_t K, GroupSrc grp,
+                                                                 const RowSigns sg, float* amax_pre,
+                                                                 float* amax_post) {
+  __shared__ SmemGroups t;
+  const int slabs = (int)((K + 255) / 256);
+  build_group_tables(grp, slabs, t);
+  griddep_wait();
+  griddep_launch_dependents();
+  if (t.bad) return;
+  const int G = grp.G;
+  const int lane = threadIdx.x & 31;
+  const int64_t units = t.up[G];
+  const int64_t warps = (int64_t)gridDim.x * kWarps;
+  const int64_t w = (int64_t)blockIdx.x * kWarps + threadIdx.x / 32;
+  const int64_t upw = (units + warps - 1) / warps;
+  const int64_t u0 = w * upw, u1 = min(units, u0 + upw);
+  if (u0 >= u1) return;
+  int g = find_unit_group(t, G, u0);
+  uint32_t pre_bits = 0;  // packed bf16 magnitudes
+  float post = 0.0f;
+  for (int64_t u = u0; u < u1; ++u) {
+    if (t.up[g + 1] <= u) {
+      float pre = bf16_bits_to_float(amax_pair_bits(pre_bits));
+      pre = warp_max(pre);
+      post = warp_max(post);
+      if (lane == 0) {
+        atomic_max_nonneg(amax_pre + g, pre);
+        atomic_max_nonneg(amax_post + g, post * 0.25f);
+      }
+      pre_bits = 0;
+      post = 0.0f;
+      while (t.up[g + 1] <= u) ++g;
+    }
+    const Unit un = decode_unit(t, g, u, K, lane);
+    uint4 v[16];
+    load_unit(x, K, un, v);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {  // columns 2cc, 2cc + 1 of the lane's eight
+      f32x2 y[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t wd = cc == 0 ? v[i].x : cc == 1 ? v[i].y : cc == 2 ? v[i].z : v[i].w;
+        pre_bits = bmax_abs2(pre_bits, wd);
+        y[i] = pk2(__uint_as_float(umad(wd, 65536u, sg.s[i])), __uint_as_float((wd & 0xFFFF0000u) ^ sg.s[i]));
+      }
+      fwht16x2_first3(y);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        post = fmaxf(post, fabsf(lo2(y[i])) + fabsf(lo2(y[i + 8])));
+        post = fmaxf(post, fabsf(hi2(y[i])) + fabsf(hi2(y[i + 8])));
+      }
+    }
+  }
+  float pre = bf16_bits_to_float(amax_pair_bits(pre_bits));
+  pre = warp_max(pre);
+  post = warp_max(post);
+  if (lane == 0) {
+    atomic_max_nonneg(amax_pre + g, pre);
+    atomic_max_nonneg(amax_post + g, post * 0.25f);
+  }
+}
+
+// ------------------------------------------------------------------ row + column NVFP4 cast
 
 // Max |x| over the 16 bf16 values of two vectors, as amax8_bits does for 8.
 __device__ __forceinline__ uint32_t amax16_bits(const uint4& v, const uint4& u) {
@@ -648,7 +649,19 @@ struct RcWalk {
   }
 };
 
-template <bool ROW, bool RHT, bool TILED>
+// One warp's post-RHT amax of a group: the lanes' max |y| before the quarter,
+// then x 1/4 (exact), max-accumulated into the group's word.
+__device__ __forceinline__ void flush_post(float* dst, float& post, int lane) {
+  const float m = warp_max(post);
+  if (lane == 0) atomic_max_nonneg(dst, m * 0.25f);
+  post = 0.0f;
+}
+
+// COLQ = false (with ROW, RHT, TILED): no columnwise codes; the column phase
+// only takes the post-RHT amax of the 16-row chunks (per warp, then one
+// atomicMax per group and warp), the fused amax the columnwise cast of the
+// same tensor would use.
+template <bool ROW, bool RHT, bool TILED, bool COLQ>
 __global__ void __launch_bounds__(kRcThreads, kRcBlocksPerSM)
     rowcol_quant_kernel(const __grid_constant__ CUtensorMap tmx, const ColQuantArgs a) {
   __shared__ SmemGroups t;
@@ -710,6 +723,7 @@ __global__ void __launch_bounds__(kRcThreads, kRcBlocksPerSM)
   const int nscale_row = (int)(K / 16);
   int g_tab = -1;
   float S_row = 0.0f, S_col = 0.0f;
+  float post_acc = 0.0f;  // !COLQ: this lane's max |y| (before the quarter) in the current group
   uint32_t sg[16];  // the sign mask as FP32 sign bits per row, kept in registers
 #pragma unroll
   for (int i = 0; i < 16; ++i) sg[i] = RHT ? a.sgn[i] : 0u;
@@ -721,13 +735,14 @@ __global__ void __launch_bounds__(kRcThreads, kRcBlocksPerSM)
     const uint32_t ph = (uint32_t)(it >> 1) & 1u;
     if (it > 0) tl.next(t, slabs);
     if (tl.g != g_tab) {
+      if (!COLQ && g_tab >= 0) flush_post(a.amax_post_out + g_tab, post_acc, lane);
       S_row = ROW ? nvfp4_global_scale(a.amax_row[tl.g]) : 0.0f;
-      S_col = nvfp4_global_scale(a.amax_col[tl.g]);
+      S_col = COLQ ? nvfp4_global_scale(a.amax_col[tl.g]) : 0.0f;
       __syncwarp();
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (ROW) enc_row[lane + 32 * i] = nvfp4_enc(S_row, (uint32_t)(lane + 32 * i));
-        enc_col[lane + 32 * i] = nvfp4_enc(S_col, (uint32_t)(lane + 32 * i));
+        if (COLQ) enc_col[lane + 32 * i] = nvfp4_enc(S_col, (uint32_t)(lane + 32 * i));
       }
       __syncwarp();
       g_tab = tl.g;
@@ -810,6 +825,10 @@ __global__ void __launch_bounds__(kRcThreads, kRcBlocksPerSM)
           b0 = fmaxf(b0, fabsf(lo2(y[i])) + fabsf(lo2(y[i + 8])));
           b1 = fmaxf(b1, fabsf(hi2(y[i])) + fabsf(hi2(y[i + 8])));
         }
+        if (!COLQ) {  // the post-RHT amax only
+          post_acc = fmaxf(post_acc, fmaxf(b0, b1));
+          continue;
+        }
         fwht16x2_last(y);
         b0r = b0;
         b1r = b1;
@@ -867,6 +886,7 @@ __global__ void __launch_bounds__(kRcThreads, kRcBlocksPerSM)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[b]);  // this warp is done reading the tile
+    if (!COLQ) continue;
 
     // the warp's columns: each column's chunks of this tile as one run, four lanes per column
     const int64_t mpad = (int64_t)(t.mp[tl.g + 1] - t.mp[tl.g]);
@@ -887,6 +907,7 @@ __global__ void __launch_bounds__(kRcThreads, kRcBlocksPerSM)
     }
     __syncwarp();  // the staging buffers are free for the next tile
   }
+  if (!COLQ && g_tab >= 0) flush_post(a.amax_post_out + g_tab, post_acc, lane);
 }
 
 // Persistent grid: as many blocks as fit on the device at once (one wave),
@@ -1060,8 +1081,9 @@ cudaError_t launch_hadamard_amax(const uint16_t* x, int64_t M, int64_t K, GroupS
   if (e == cudaSuccess) e = cudaMemsetAsync(amax_post, 0, sizeof(float) * grp.G, s);
   if (e != cudaSuccess) return e;
   const int64_t units = ((M + 15) / 16 + grp.G) * ((K + 255) / 256);
-  hadamard_amax_kernel<<<grid_for(hadamard_amax_kernel, units), kThreads, 0, s>>>(x, K, grp, mask & 0xFFFFu, amax_pre,
-                                                                                  amax_post);
+  RowSigns sg;
+  for (int i = 0; i < 16; ++i) sg.s[i] = ((mask >> i) & 1u) ? 0x80000000u : 0u;
+  hadamard_amax_kernel<<<grid_for(hadamard_amax_kernel, units), kThreads, 0, s>>>(x, K, grp, sg, amax_pre, amax_post);
   return cudaGetLastError();
 }
 
@@ -1082,9 +1104,9 @@ cudaError_t launch_fc2x_recompute(const uint16_t* h, const float* probs, int64_t
   return cudaGetLastError();
 }
 
-template <bool ROW, bool RHT, bool TILED>
+template <bool ROW, bool RHT, bool TILED, bool COLQ = true>
 cudaError_t launch_rowcol_t(const ColQuantArgs& a, cudaStream_t s) {
-  auto kern = rowcol_quant_kernel<ROW, RHT, TILED>;
+  auto kern = rowcol_quant_kernel<ROW, RHT, TILED, COLQ>;
   constexpr size_t smem = sizeof(RcShared) + 128;
   static bool attr[64] = {};
   static int per_sm[64] = {};
@@ -1114,6 +1136,10 @@ cudaError_t launch_col_quant(const ColQuantArgs& a0, cudaStream_t s) {
   ColQuantArgs a = a0;
   for (int i = 0; i < 16; ++i) a.sgn[i] = ((a.mask >> i) & 1u) ? 0x80000000u : 0u;
   const bool row = a.row_codes != nullptr;
+  if (!a.col_codes) {  // rowwise (GEMM_TILED) + the post-RHT amax only
+    if (!row || !a.row_tiled || !a.amax_post_out) return cudaErrorInvalidValue;
+    return launch_rowcol_t<true, true, true, false>(a, s);
+  }
   if (a.use_rht) {
     if (!row) return launch_rowcol_t<false, true, false>(a, s);
     return a.row_tiled ? launch_rowcol_t<true, true, true>(a, s) : launch_rowcol_t<true, true, false>(a, s);

@@ -319,13 +319,15 @@ def replicate_weight_scales(q: "QWeight", stream=None) -> torch.Tensor:
     return out
 
 
-def prepare_weights(W, fmt: int, swiglu_interleave: bool = False, x4: bool | None = None, bias=None,
+def prepare_weights(W, fmt: int, swiglu_interleave: bool = False, x4: bool = False, bias=None,
                     stream=None) -> QWeight:
     """Quantise expert weights: W is a stacked bf16 [G, rows, cols] cuda tensor,
     or a list of G bf16 [rows, cols] tensors (discrete per-expert weights).
-    NVFP4 weights with rows and cols multiples of 256 also get the
-    GEMM_TILED_X4 scale copy the forward reads (x4=False keeps GEMM_TILED
-    only).  bias: optional bf16 [G, rows] added in fc1 / fc2."""
+    x4=True (NVFP4, rows and cols multiples of 256) also makes the
+    GEMM_TILED_X4 scale copy, which the forward then reads (the CTA-pair mode's
+    faster layout; single-CTA NVFP4 GEMMs measure faster on GEMM_TILED scales,
+    which their scale-writer warps place in tensor memory).  bias: optional
+    bf16 [G, rows] added in fc1 / fc2."""
     discrete = isinstance(W, (list, tuple))
     if discrete:
         Ws = [_bits(w) for w in W]
@@ -352,9 +354,9 @@ def prepare_weights(W, fmt: int, swiglu_interleave: bool = False, x4: bool | Non
     q = QWeight(codes, scales, gs, am, rows, cols, G, fmt, bool(swiglu_interleave))
     if bias is not None:
         q.bias = _bits(bias).reshape(G, rows).contiguous()
-    if x4 is None:
-        x4 = fmt == NVFP4 and rows % 256 == 0 and cols % 256 == 0
     if x4:
+        if fmt != NVFP4 or rows % 256 or cols % 256:
+            raise ValueError("x4 scales: NVFP4 weights with rows and cols multiples of 256")
         q.scales_x4 = replicate_weight_scales(q, stream)
     return q
 

@@ -25,10 +25,10 @@ SPILL_FREE = [
     "gemm_kernel<1, 1, 1, true, false>",    # NVFP4 fc1 + SReLU + amaxes
     "gemm_kernel<1, 2, 1, true, false>",    # NVFP4 fc2
     "row_quant_kernel<1, true>",            # NVFP4 casts (x, fc2_x)
-    "hadamard_amax_kernel",
-    "rowcol_quant_kernel<true, true, true>",    # NVFP4 row + column (RHT) cast, GEMM_TILED row scales
-    "rowcol_quant_kernel<true, true, false>",   # the same, compact row scales
-    "rowcol_quant_kernel<false, true, false>",  # column (RHT) only
+    "rowcol_quant_kernel<true, true, true, true>",    # NVFP4 row + column (RHT) cast, GEMM_TILED row scales
+    "rowcol_quant_kernel<true, true, false, true>",   # the same, compact row scales
+    "rowcol_quant_kernel<false, true, false, true>",  # column (RHT) only
+    "rowcol_quant_kernel<true, true, true, false>",   # forward fc2_x: rowwise + post-RHT amax
     "colq_kernel<0>", "colq_kernel<1>", "colq_kernel<2>",
 ]
 

@@ -28,7 +28,6 @@ def bf16_cpu(a):
 
 
 def run_gpu(gm, d, fmt, act, mask=0, probs=True, gemm_mode=0, x4=None, tanh_c=0.0):
-    # NVFP4 weights carry the replicated (GEMM_TILED_X4) scales by default
     w1 = gm.prepare_weights(d["W1"].cuda(), fmt, swiglu_interleave=(act == gm.SWIGLU), x4=x4)
     w2 = gm.prepare_weights(d["W2"].cuda(), fmt, x4=x4)
     M, N = d["x"].shape[0], d["W2"].shape[2]
@@ -241,8 +240,9 @@ def test_prepare_weights_discrete_matches_stacked(gm, fmt, swiglu):
     rng = np.random.default_rng(37)
     G, rows, cols = 3, 512, 512
     W = bf16_cpu(rng.standard_normal((G, rows, cols)) * np.array([1.0, 1e-3, 30.0])[:, None, None]).cuda()
-    a = gm.prepare_weights(W, fmt, swiglu_interleave=swiglu)
-    b = gm.prepare_weights([W[g].clone() for g in range(G)], fmt, swiglu_interleave=swiglu)
+    x4 = fmt == 1
+    a = gm.prepare_weights(W, fmt, swiglu_interleave=swiglu, x4=x4)
+    b = gm.prepare_weights([W[g].clone() for g in range(G)], fmt, swiglu_interleave=swiglu, x4=x4)
     gm.check_device_status()
     assert torch.equal(a.codes, b.codes)
     used = G * rows // 128 * (cols // (32 if fmt == 0 else 16) // 4) * 512
@@ -256,7 +256,7 @@ def test_replicate_weight_scales_bitexact(orc, gm):
     rng = np.random.default_rng(4)
     G, rows, cols = 3, 512, 768
     W = bf16_cpu(rng.standard_normal((G, rows, cols)))
-    q = gm.prepare_weights(W.cuda(), gm.NVFP4)
+    q = gm.prepare_weights(W.cuda(), gm.NVFP4, x4=True)
     gm.check_device_status()
     tiled = np_u8(q.scales)
     want = orc.tiled_to_x4(tiled, G * rows // 256, cols // 64)
