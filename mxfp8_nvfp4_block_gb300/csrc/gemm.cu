@@ -125,12 +125,8 @@ __device__ __forceinline__ float bf16_half(uint32_t w, int hi) {
   return bf16_bits_to_float(hi ? (w >> 16) : (w & 0xFFFFu));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return bf16_bits(lo) | (bf16_bits(hi) << 16);
-}
-
-// The same value as pack_bf16x2 in one paired conversion (fewer conversion
-// instructions; used where the epilogue is conversion-bound).
+// Two floats as a packed bf16 pair (round to nearest even; lo in the low half),
+// in one paired conversion.
 __device__ __forceinline__ uint32_t pack2_bf16_rn(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -338,14 +334,15 @@ __device__ __forceinline__ void store_quad_rows(uint16_t* out, int64_t ld, int64
 
 template <int FMT, int EPI, bool XT, bool QT>
 __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Tile& t, const int* off,
-                                         const int* tb, int row_base, int q, int lane, int slice, float prob) {
+                                         const int* tb, const float* atab, int row_base, int q, int lane, int slice,
+                                         float prob) {
   const int row = 32 * q + lane;
   const int m_g = off[t.g + 1] - off[t.g];
   const int lr = row_base + row;  // row within the group
   const bool valid = lr < m_g;
   const int64_t grow = (int64_t)off[t.g] + lr;
   float alpha = 1.0f;
-  if (FMT == GMLP_NVFP4) alpha = __fdiv_rn(1.0f, __fmul_rn(nvfp4_global_scale(a.a_amax[t.g]), a.b_S[t.g]));
+  if (FMT == GMLP_NVFP4) alpha = atab[t.g];  // 1 / (S_a S_b), per group, computed once per CTA
   if (XT && a.bias) {
     // per-expert bias, added to the FP32 accumulator before any rounding; the
     // slice's two 32-column runs map to logical rows b0 and b1 of the bias
@@ -374,10 +371,14 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
 
   if (EPI == EPI_FC2 && QT) {
     uint32_t u[4][8];
+    const f32x2 alpha2 = pk2(alpha, alpha);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
-      for (int k = 0; k < 8; ++k) u[j][k] = pack_bf16x2(acc[16 * j + 2 * k] * alpha, acc[16 * j + 2 * k + 1] * alpha);
+      for (int k = 0; k < 8; ++k) {
+        const f32x2 v = mul2(pk2(acc[16 * j + 2 * k], acc[16 * j + 2 * k + 1]), alpha2);
+        u[j][k] = pack2_bf16_rn(lo2(v), hi2(v));
+      }
     quad_transpose(u, lane);
     // warp rows 32 q .. 32 q + 31 of the tile; this lane's quad stores rows 4 (lane / 4) + s
     store_quad_rows(a.out_bf16, a.n_cols_out, (int64_t)off[t.g] + row_base + 32 * q, m_g, row_base + 32 * q,
@@ -391,7 +392,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
     for (int j = 0; j < kSliceCols; j += 16) {
       uint32_t o[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) o[k] = pack_bf16x2(acc[j + 2 * k] * alpha, acc[j + 2 * k + 1] * alpha);
+      for (int k = 0; k < 8; ++k) o[k] = pack2_bf16_rn(acc[j + 2 * k] * alpha, acc[j + 2 * k + 1] * alpha);
       st_global_v8(yrow + j, o);
     }
     return;
@@ -407,7 +408,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
     for (int j = 0; j < 64; j += 16) {
       uint32_t o[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) o[k] = pack_bf16x2(acc[j + 2 * k] * alpha, acc[j + 2 * k + 1] * alpha);
+      for (int k = 0; k < 8; ++k) o[k] = pack2_bf16_rn(acc[j + 2 * k] * alpha, acc[j + 2 * k + 1] * alpha);
       const int64_t col = EPI == EPI_FC1_SWIGLU ? (j < 32 ? oc0 + j : a.n_cols_out + oc0 + (j - 32)) : oc0 + j;
       st_global_v8(hrow + col, o);
     }
@@ -473,7 +474,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
 #pragma unroll
       for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) u[j][k] = pack_bf16x2(acc[16 * j + 2 * k], acc[16 * j + 2 * k + 1]);
+        for (int k = 0; k < 8; ++k) u[j][k] = pack2_bf16_rn(acc[16 * j + 2 * k], acc[16 * j + 2 * k + 1]);
       quad_transpose(u, lane);
       store_quad_rows(a.out_bf16, a.n_cols_out, (int64_t)off[t.g] + row_base + 32 * q, m_g, row_base + 32 * q, oc0, u,
                       lane);
@@ -483,7 +484,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, float* acc, const Ti
       for (int j = 0; j < kOut; j += 16) {
         uint32_t o[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) o[k] = pack_bf16x2(acc[j + 2 * k], acc[j + 2 * k + 1]);
+        for (int k = 0; k < 8; ++k) o[k] = pack2_bf16_rn(acc[j + 2 * k], acc[j + 2 * k + 1]);
         st_global_v8(dst + j, o);
       }
     }
@@ -638,6 +639,7 @@ __global__ void __launch_bounds__(Cfg<FMT, PAIR, X4>::kThreads, 1)
   int* off = reinterpret_cast<int*>(tslot + 4);
   int* tb = off + kMaxGroups + 1;
   int* ip = tb + kMaxGroups + 1;
+  float* atab = reinterpret_cast<float*>(ip + kMaxGroups + 1);  // NVFP4: per-group 1 / (S_a S_b)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int G = a.grp.G;
@@ -719,6 +721,12 @@ __global__ void __launch_bounds__(Cfg<FMT, PAIR, X4>::kThreads, 1)
   tc_fence_after();
   griddep_wait();                 // the previous kernel's outputs (A operand, amaxes) are complete
   griddep_launch_dependents();
+  if (FMT == GMLP_NVFP4) {
+    // the epilogue's alpha per group: the amaxes come from the previous kernels
+    for (int g = threadIdx.x; g < G; g += blockDim.x)
+      atab[g] = __fdiv_rn(1.0f, __fmul_rn(nvfp4_global_scale(a.a_amax[g]), a.b_S[g]));
+    __syncthreads();
+  }
   const uint32_t tbase = *tslot;
   const int total = *bad ? 0 : ip[G];
 
@@ -950,7 +958,7 @@ __global__ void __launch_bounds__(Cfg<FMT, PAIR, X4>::kThreads, 1)
           mbar_arrive_cluster(tempty_addr);
       }
       acc_phase ^= 1;
-      epilogue<FMT, EPI, XT, C::kSST>(a, acc, t, off, tb, row_base, q, lane, slice, prob);
+      epilogue<FMT, EPI, XT, C::kSST>(a, acc, t, off, tb, atab, row_base, q, lane, slice, prob);
     }
   }
   __syncthreads();
@@ -966,7 +974,8 @@ __global__ void __launch_bounds__(Cfg<FMT, PAIR, X4>::kThreads, 1)
 template <int FMT, int EPI, int PAIR, bool X4 = false, bool XT = false>
 cudaError_t launch_t(const GemmArgs& a, cudaStream_t s) {
   using C = Cfg<FMT, PAIR, X4>;
-  const size_t smem = C::kSmem + 1024 + 256 + 3 * (kMaxGroups + 1) * sizeof(int);
+  const size_t smem = C::kSmem + 1024 + 256 + 3 * (kMaxGroups + 1) * sizeof(int) +
+                      (FMT == GMLP_NVFP4 ? (kMaxGroups + 1) * sizeof(float) : 0);
   auto kern = gemm_kernel<FMT, EPI, PAIR, X4, XT>;
   static bool attr_set[64] = {};
   static int max_units[64] = {};
