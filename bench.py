@@ -53,7 +53,8 @@ WORKLOAD_TEXT = {
 NOMINAL_RATIO = {0: 2.0, 1: 6.0}   # dense FP8 / bf16 and FP4 / bf16 (4.5 and 13.5 vs 2.25 PFLOP/s)
 # DRAM bytes (read + write) per fc1 launch from one ncu capture of the gemm.cu
 # whose sha1 is in the key, valid only for that source.
-FC1_TRAFFIC = {("mx_swiglu", "b0e8fcf872c3051bf7b3c4106ed692b23271c65a"): 65024256 + 4080384}
+FC1_TRAFFIC = {("mx_skew", "02f738f26d2dedbef147cc985ad471866d897e57"): 2397696512 + 141248512,
+               ("nv_srelu", "02f738f26d2dedbef147cc985ad471866d897e57"): 113453312 + 91440896}
 
 
 def fc1_traffic(workload: str):

@@ -773,7 +773,6 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
     if (i < n_stage_events) GMLP_CUDA(cudaEventRecord((cudaEvent_t)stage_events[i], s), "stage event record");
     return GMLP_OK;
   };
-  if (dprob) GMLP_CUDA(cudaMemsetAsync(dprob, 0, sizeof(float) * M, s), "dprob memset");
   {
     RowQuantArgs q{};
     q.x = dy;
@@ -784,6 +783,8 @@ gmlp_status gmlp_backward_dgrad(const uint16_t* dy, int64_t M, int64_t K, int64_
     q.tiled = 1;
     q.codes = dy_codes;
     q.scales = dy_scales;
+    q.zero_ptr = dprob;  // the dGLU epilogue adds into it
+    q.zero_count = dprob ? M : 0;
     GMLP_CUDA(launch_row_quant(q, s), "dy quantise launch");
   }
   GMLP_TRY(stage_done(0));

@@ -35,7 +35,7 @@ struct RowQuantArgs {
   const float* amax;        // NVFP4: per-group amax giving S_g
   float* S_out;             // optional: write S_g for every group
   int swiglu_interleave;    // weights: gate/up 32-row interleave within each group
-  float* zero_ptr;          // optional: floats zeroed by the first CTA (for later atomics)
+  float* zero_ptr;          // optional: floats zeroed by the grid before any later kernel (for its atomics)
   int zero_count;
   float* zero_ptr2;         // optional second range
   int zero_count2;

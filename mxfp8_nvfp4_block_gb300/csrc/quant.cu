@@ -196,14 +196,15 @@ __device__ __forceinline__ uint32_t gather4_bytes(uint32_t byte, int s) {
   return pair | (__shfl_down_sync(0xffffffffu, pair, 2 * s) << 16);
 }
 
-// Work every launch of the row quantiser does first: the zeroing requests and
-// the per-group global scales (block 0 only).
+// Work every launch of the row quantiser does first: the zeroing requests
+// (spread over the grid) and the per-group global scales (block 0).
 __device__ __forceinline__ void row_quant_setup(const RowQuantArgs& a, int nthreads) {
-  if (blockIdx.x != 0) return;
+  const int64_t first = (int64_t)blockIdx.x * nthreads + threadIdx.x, step = (int64_t)gridDim.x * nthreads;
   if (a.zero_ptr)
-    for (int i = threadIdx.x; i < a.zero_count; i += nthreads) a.zero_ptr[i] = 0.0f;
+    for (int64_t i = first; i < a.zero_count; i += step) a.zero_ptr[i] = 0.0f;
   if (a.zero_ptr2)
-    for (int i = threadIdx.x; i < a.zero_count2; i += nthreads) a.zero_ptr2[i] = 0.0f;
+    for (int64_t i = first; i < a.zero_count2; i += step) a.zero_ptr2[i] = 0.0f;
+  if (blockIdx.x != 0) return;
   if (a.S_out)
     for (int g = threadIdx.x; g < a.grp.G; g += nthreads) a.S_out[g] = nvfp4_global_scale(a.amax[g]);
 }
@@ -273,7 +274,7 @@ __device__ __forceinline__ void row_pass(const uint4* xr, uint8_t* crow, uint8_t
 // the passes and sets up each row it touches once.  NVFP4 encode factors
 // S / E4M3(sf) come from a per-warp table of the current group.
 template <int FMT, bool TILED>
-__global__ void __launch_bounds__(kThreads, 5) row_quant_kernel(RowQuantArgs a) {
+__global__ void __launch_bounds__(kThreads, FMT == GMLP_MXFP8 ? 4 : 5) row_quant_kernel(RowQuantArgs a) {
   __shared__ SmemGroups t;
   __shared__ float enc_tab[FMT == GMLP_NVFP4 ? kWarps : 1][128];
   build_group_tables(a.grp, 1, t);

@@ -169,14 +169,25 @@ __global__ void __launch_bounds__(kColThreads) colq_kernel(const ColqArgs a) {
   float csum = 0.0f;
 #pragma unroll 1
   for (int j = 0; j < 4; ++j) {
-    float v[32];
-    float amax = 0.0f;
+    float v[32], m[16], sm[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      v[i] = bf16_bits_to_float(tile[32 * j + i][c]);
-      amax = fmaxf(amax, fabsf(v[i]));
-      csum += v[i];
+    for (int i = 0; i < 32; ++i) v[i] = bf16_bits_to_float(tile[32 * j + i][c]);
+    // block max and (for the bias gradient) block sum as balanced trees: short
+    // dependency chains instead of one 32-long chain each
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      m[i] = fmaxf(fabsf(v[i]), fabsf(v[i + 16]));
+      sm[i] = v[i] + v[i + 16];
     }
+#pragma unroll
+    for (int h = 8; h > 0; h >>= 1)
+#pragma unroll
+      for (int i = 0; i < h; ++i) {
+        m[i] = fmaxf(m[i], m[i + h]);
+        sm[i] = sm[i] + sm[i + h];
+      }
+    const float amax = m[0];
+    csum += sm[0];
     const int e = mxfp8_exponent(amax);
     const float mul = exp2_neg(e);
     uint32_t wd[8];

@@ -25,6 +25,7 @@ SPILL_FREE = [
     "gemm_kernel<1, 1, 1, true, false>",    # NVFP4 fc1 + SReLU + amaxes
     "gemm_kernel<1, 2, 1, true, false>",    # NVFP4 fc2
     "row_quant_kernel<1, true>",            # NVFP4 casts (x, fc2_x)
+    "row_quant_kernel<0, true>",            # MXFP8 casts (x, dy)
     "rowcol_quant_kernel<true, true, true, true>",    # NVFP4 row + column (RHT) cast, GEMM_TILED row scales
     "rowcol_quant_kernel<true, true, false, true>",   # the same, compact row scales
     "rowcol_quant_kernel<false, true, false, true>",  # column (RHT) only
