@@ -343,6 +343,9 @@ __global__ void __launch_bounds__(kThreads, FMT == GMLP_MXFP8 ? 4 : 5) row_quant
 
 // ------------------------------------------------------------------ group amax
 
+// Per-group max |x|.  Work units are 256 16-byte chunks of one row (eight per
+// lane, all loads issued before the max), so the warps' shares stay even when
+// there are only a few rows per warp; warp w takes a contiguous range of units.
 __global__ void __launch_bounds__(kThreads) group_amax_kernel(const uint16_t* x, int64_t K, GroupSrc grp,
                                                               float* amax) {
   __shared__ SmemGroups t;
@@ -352,17 +355,20 @@ __global__ void __launch_bounds__(kThreads) group_amax_kernel(const uint16_t* x,
   if (t.bad) return;
   const int G = grp.G;
   const int nch = (int)(K / 8);
+  constexpr int U = 8;
+  const int upr = (nch + 32 * U - 1) / (32 * U);  // units per row
   const int lane = threadIdx.x & 31;
   const int64_t rows = t.off[G];
   const int64_t warps = (int64_t)gridDim.x * kWarps;
   const int64_t w = (int64_t)blockIdx.x * kWarps + threadIdx.x / 32;
-  const int64_t rpw = (rows + warps - 1) / warps;
-  const int64_t r0 = w * rpw, r1 = min(rows, r0 + rpw);
-  if (r0 >= r1) return;
-  int g = find_group(t, G, r0);
+  const int64_t units = rows * upr;
+  const int64_t u0 = units * w / warps, u1 = units * (w + 1) / warps;
+  if (u0 >= u1) return;
+  int64_t r = u0 / upr;
+  int part = (int)(u0 - r * upr);
+  int g = find_group(t, G, r);
   uint32_t m = 0;  // running max |x| as bf16 bits (non-negative, so integer order is value order)
-  constexpr int U = 8;
-  for (int64_t r = r0; r < r1; ++r) {
+  for (int64_t u = u0; u < u1; ++u) {
     if (t.off[g + 1] <= r) {
       const float mf = warp_max(__uint_as_float(m << 16));
       if (lane == 0) atomic_max_nonneg(amax + g, mf);
@@ -370,15 +376,18 @@ __global__ void __launch_bounds__(kThreads) group_amax_kernel(const uint16_t* x,
       while (t.off[g + 1] <= r) ++g;
     }
     const uint4* xr = reinterpret_cast<const uint4*>(x + r * K);
-    for (int c0 = 0; c0 < nch; c0 += 32 * U) {
-      uint4 v[U];
+    const int c0 = part * 32 * U;
+    uint4 v[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int c = c0 + 32 * u + lane;
-        v[u] = c < nch ? ld_stream(xr + c) : make_uint4(0, 0, 0, 0);
-      }
+    for (int k = 0; k < U; ++k) {
+      const int c = c0 + 32 * k + lane;
+      v[k] = c < nch ? ld_stream(xr + c) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-      for (int u = 0; u < U; ++u) m = max(m, amax8_bits(v[u]));
+    for (int k = 0; k < U; ++k) m = max(m, amax8_bits(v[k]));
+    if (++part == upr) {
+      part = 0;
+      ++r;
     }
   }
   const float mf = warp_max(__uint_as_float(m << 16));
