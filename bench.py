@@ -170,6 +170,16 @@ L2_TEXT = {"write": "flushed between timed steps (256 MiB write, outside the ste
                     "step starts on a cold L2 without the write's dirty lines; outside the step events)"}
 
 
+def made_events(n: int) -> list:
+    """n timing events, each recorded once now (before the L2 flush) so that it
+    has its device handle: the binding would otherwise record a new event once
+    before the call's first kernel, inside the timed region."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record()
+    return evs
+
+
 class L2Flush:
     """Flush L2 between timed steps: write 256 MiB; in "clean" mode then read
     another 256 MiB, so the write's dirty lines are written back here and the
@@ -556,8 +566,8 @@ def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps
     # second pass: an event after every kernel (dy quantise, dGLU GEMM, dgrad GEMM)
     st = [0.0, 0.0, 0.0]
     for _ in range(K_steps):
+        se = made_events(4)
         flush()
-        se = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         se[0].record()
         gmlp.backward_dgrad(dy, splits, w2t, w1t, h, probs, w.act, rec, dx=dx, workspace=ws, events=se[1:])
         torch.cuda.synchronize()
@@ -592,8 +602,8 @@ def bench_backward(gmlp, d, w, W1b, W2b, x, splits, probs, K_steps: int, W_steps
     # fc1_dy cast, x cast, dW1 GEMM)
     wst = [0.0] * 6
     for _ in range(K_steps):
+        se = made_events(7)
         flush()
-        se = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
         se[0].record()
         gmlp.backward_wgrad(xin, dy, h, probs, f1, splits, w.act, workspace=wws, events=se[1:], **grads)
         torch.cuda.synchronize()

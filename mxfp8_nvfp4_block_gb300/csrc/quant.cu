@@ -534,6 +534,14 @@ __global__ void __launch_bounds__(kThreads, 2) hadamard_amax_kernel(const uint16
 
 // ------------------------------------------------------------------ row + column NVFP4 cast
 
+// One warp's post-RHT amax of a group: the lanes' max |y| before the quarter,
+// then x 1/4 (exact), max-accumulated into the group's word.
+__device__ __forceinline__ void flush_post(float* dst, float& post, int lane) {
+  const float m = warp_max(post);
+  if (lane == 0) atomic_max_nonneg(dst, m * 0.25f);
+  post = 0.0f;
+}
+
 // Max |x| over the 16 bf16 values of two vectors, as amax8_bits does for 8.
 __device__ __forceinline__ uint32_t amax16_bits(const uint4& v, const uint4& u) {
   uint32_t m = bmax_abs2(bmax_abs2(bmax_abs2(v.x, v.y), bmax_abs2(v.z, v.w)),
@@ -622,14 +630,6 @@ struct RcWalk {
     nvalid = min(kRcRows, t.off[g + 1] - t.off[g] - kRcRows * blk);
   }
 };
-
-// One warp's post-RHT amax of a group: the lanes' max |y| before the quarter,
-// then x 1/4 (exact), max-accumulated into the group's word.
-__device__ __forceinline__ void flush_post(float* dst, float& post, int lane) {
-  const float m = warp_max(post);
-  if (lane == 0) atomic_max_nonneg(dst, m * 0.25f);
-  post = 0.0f;
-}
 
 // COLQ = false (with ROW, RHT, TILED): no columnwise codes; the column phase
 // only takes the post-RHT amax of the 16-row chunks (per warp, then one
