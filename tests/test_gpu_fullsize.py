@@ -7,6 +7,8 @@ configuration the benchmark uses (persistent grids, many work units per CTA).
   Hadamard-amax pass and the quantize-with-amax cast; Description: the
   fc2-input group quantize, row + column): amax_pre / amax_post, rowwise codes
   and GEMM_TILED scales, columnwise RHT codes and scales.
+* The NVFP4 forward's fc2_x amaxes on the nv_srelu workload against the
+  standalone Hadamard-amax kernel and the oracle over the stored bf16 fc2_x.
 * The forward's x casts on each forward workload's whole x: MXFP8 at K = 256
   (512 tokens in 4 ragged experts) and K = 2048 (16384 tokens, Dirichlet
   routing with an empty expert), NVFP4 at K = 4096 (32768 tokens with 0.1%
@@ -97,3 +99,34 @@ def test_forward_x_cast_fullsize(orc, gm, name, fmt):
     assert np.array_equal(orc.tiled_to_compact(np_u8(out["row"][1]), s, K // blk), ref["row_scales"])
     if fmt == 1:
         assert np.array_equal(out["amax_pre"].cpu().numpy(), ref["amax_pre"])
+
+
+@pytest.mark.parametrize("colwise", [False, True], ids=["cast_pass", "epilogue"])
+def test_nv_srelu_forward_amaxes_fullsize(orc, gm, colwise):
+    """The NVFP4 forward's fc2_x amaxes on the nv_srelu workload (32768 tokens,
+    N = 2048): pre- and post-RHT amax equal, bit for bit, both the standalone
+    Hadamard-amax kernel and the oracle's group Hadamard-amax over the bf16
+    fc2_x the forward stored (PR #3837, Description: the fused amax equals the
+    quantizer's own).  cast_pass: the post-RHT amax comes from the rowwise
+    fc2_x cast; epilogue: from the fc1 epilogue (the columnwise variant)."""
+    d = make_inputs("nv_srelu")
+    w = d["workload"]
+    M, N, G = w.M, w.N, w.G
+    w1 = gm.prepare_weights(d["W1"].cuda(), gm.NVFP4)
+    w2 = gm.prepare_weights(d["W2"].cuda(), gm.NVFP4)
+    aux = {"fc2x_bf16": torch.zeros((M, N), dtype=torch.bfloat16, device="cuda"),
+           "fc2x_amax_pre": torch.zeros(G, dtype=torch.float32, device="cuda"),
+           "fc2x_amax_post": torch.zeros(G, dtype=torch.float32, device="cuda")}
+    if colwise:
+        ncol = N * (M + 16 * G)
+        aux["fc2x_col_codes"] = torch.zeros(ncol // 2, dtype=torch.uint8, device="cuda")
+        aux["fc2x_col_scales"] = torch.zeros(ncol // 16, dtype=torch.uint8, device="cuda")
+    rec = gm.recipe(gm.NVFP4, use_rht=True, mask=d["mask"])
+    gm.forward(d["x"].cuda(), d["splits"].cuda(), w1, w2, d["probs"].cuda(), w.act, rec, aux=aux)
+    _check(gm, None)
+    pre, post = gm.group_hadamard_amax(aux["fc2x_bf16"], d["splits"].cuda(), d["mask"])
+    _check(gm, None)
+    assert torch.equal(pre, aux["fc2x_amax_pre"]) and torch.equal(post, aux["fc2x_amax_post"])
+    opre, opost = orc.group_hadamard_amax(bits(aux["fc2x_bf16"].cpu()), d["splits"].numpy(), d["mask"])
+    assert np.array_equal(aux["fc2x_amax_pre"].cpu().numpy(), opre)
+    assert np.array_equal(aux["fc2x_amax_post"].cpu().numpy(), opost)
