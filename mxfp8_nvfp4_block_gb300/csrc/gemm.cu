@@ -633,7 +633,8 @@ __global__ void __launch_bounds__(Cfg<FMT, PAIR, X4>::kThreads, 1)
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
   uint64_t* sfready = drain + 1;  // SST: one per stage, the four scale writers arrive
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sfready + S);
+  uint64_t* sfull = sfready + S;  // SST: the stage's scale bytes have landed (A / B on full)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sfull + S);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   int* bad = reinterpret_cast<int*>(tslot + 2);
   int* off = reinterpret_cast<int*>(tslot + 4);
@@ -711,7 +712,10 @@ __global__ void __launch_bounds__(Cfg<FMT, PAIR, X4>::kThreads, 1)
     mbar_init(tempty, kEpiWarps * PAIR);
     mbar_init(drain, 1);
     if (C::kSST)
-      for (int s = 0; s < S; ++s) mbar_init(&sfready[s], 4);
+      for (int s = 0; s < S; ++s) {
+        mbar_init(&sfready[s], 4);
+        mbar_init(&sfull[s], 1);
+      }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -749,7 +753,21 @@ __global__ void __launch_bounds__(Cfg<FMT, PAIR, X4>::kThreads, 1)
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
         uint8_t* sfb = sSFB + stage * C::kSfBBytes;
-        if (PAIR == 1) {
+        if (C::kSST) {
+          // the scale bytes first, on their own barrier: the scale writers
+          // place them in TMEM while the A / B tiles are still arriving
+          mbar_arrive_expect_tx(&sfull[stage], (uint32_t)(C::kSfBytes + C::kSfBBytes));
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(kATileBytes + C::kBTileBytes));
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          bulk_load(sSFA + stage * C::kSfBytes, a.a_scales + (tileA * KB + kb) * C::kSfBytes, C::kSfBytes,
+                    &sfull[stage]);
+          bulk_load(sfb, a.b_scales + (tileB * KB + kb) * C::kSfBytes, C::kSfBytes, &sfull[stage]);
+          bulk_load(sfb + C::kSfBytes, a.b_scales + ((tileB + 1) * KB + kb) * C::kSfBytes, C::kSfBytes,
+                    &sfull[stage]);
+          tma_load_2d(sA + stage * kATileBytes, &tmA, kb * kBKBytes, rowA, &full[stage], pol_a);
+          tma_load_2d(sB + stage * C::kBTileBytes, &tmB, kb * kBKBytes, rowB, &full[stage], pol_b);
+        } else if (PAIR == 1) {
           mbar_arrive_expect_tx(&full[stage], kTx);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -792,7 +810,10 @@ __global__ void __launch_bounds__(Cfg<FMT, PAIR, X4>::kThreads, 1)
     }
     // every copy signalled on this CTA's barriers must land before it exits
     for (int s = 0; s < S; ++s)
-      if (armed & (1u << s)) mbar_wait_drain(&full[s], (armed_parity >> s) & 1u);
+      if (armed & (1u << s)) {
+        mbar_wait_drain(&full[s], (armed_parity >> s) & 1u);
+        if (C::kSST) mbar_wait_drain(&sfull[s], (armed_parity >> s) & 1u);
+      }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------- MMA issuer (the pair leader issues for both CTAs)
     int stage = 0;
@@ -864,8 +885,9 @@ __global__ void __launch_bounds__(Cfg<FMT, PAIR, X4>::kThreads, 1)
   } else if (C::kSST && warp >= C::kScaleWarp0) {
     // ---------------- scale writers: warp w stores each stage's SFA / SFB into
     // TMEM lanes 32 * (w % 4) .. + 31, in the layout the 32x128b.warpx4 copies
-    // would produce, and signals the issuer; the stage's shared memory is not
-    // refilled before the issuer's commit, which follows the signal
+    // would produce, as soon as the stage's scale bytes have landed (sfull,
+    // ahead of the A / B tiles), and signals the issuer; the stage's shared
+    // memory is not refilled before the issuer's commit, which follows the signal
     const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
     const uint32_t sf_base = tbase + kAccCols;
     int stage = 0;
@@ -873,7 +895,7 @@ __global__ void __launch_bounds__(Cfg<FMT, PAIR, X4>::kThreads, 1)
     bool ok = true;
     for (int w = unit; ok && w < total && !*abort_flag; w += n_units) {
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+        if (!mbar_wait(&sfull[stage], phase, abort_flag)) {
           ok = false;
           break;
         }
