@@ -53,8 +53,8 @@ WORKLOAD_TEXT = {
 NOMINAL_RATIO = {0: 2.0, 1: 6.0}   # dense FP8 / bf16 and FP4 / bf16 (4.5 and 13.5 vs 2.25 PFLOP/s)
 # DRAM bytes (read + write) per fc1 launch from one ncu capture of the gemm.cu
 # whose sha1 is in the key, valid only for that source.
-FC1_TRAFFIC = {("mx_skew", "02f738f26d2dedbef147cc985ad471866d897e57"): 2397696512 + 141248512,
-               ("nv_srelu", "02f738f26d2dedbef147cc985ad471866d897e57"): 113453312 + 91440896}
+FC1_TRAFFIC = {("mx_skew", "d5781b20ab7b176d6112da523493e7263b030ea0"): 2398632960 + 140919808,
+               ("nv_srelu", "d5781b20ab7b176d6112da523493e7263b030ea0"): 113472256 + 92643584}
 
 
 def fc1_traffic(workload: str):
