@@ -3,6 +3,7 @@
 // replacing the silent unfused fallback and its warning described in PR #3631
 // "Add NVTE_CUTEDSL_FUSED_GROUPED_MLP_WARN_FALLBACK", Changes), workspace
 // carving and the launch sequence of each call.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -564,7 +565,12 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   float* f_post = (aux && aux->fc2x_amax_post) ? aux->fc2x_amax_post : amax_ws + 2 * G;
   uint16_t* f_bf16 = (aux && aux->fc2x_bf16) ? aux->fc2x_bf16 : reinterpret_cast<uint16_t*>(ws + L.f_bf16);
   if (!aligned16(f_bf16)) return fail(GMLP_ERR_INVALID_ARG, "aux fc2x_bf16 misaligned");
-  GMLP_CUDA(launch_group_amax(x, M, K, gs, x_amax, s), "x amax launch");
+  // the amax pass and the x cast share one grid: the cast sweeps each warp's
+  // share backwards into the ~80 MB the amax pass left in L2 (evict-last)
+  const int xq_grid = row_quant_grid(GMLP_NVFP4, 1, M);
+  const double x_bytes = 2.0 * (double)M * (double)K;
+  const float keep = x_bytes > 0 ? (float)std::min(1.0, 80e6 / x_bytes) : 0.0f;
+  GMLP_CUDA(launch_group_amax(x, M, K, gs, x_amax, s, xq_grid, keep), "x amax launch");
   GMLP_TRY(mark());
   {
     RowQuantArgs q{};
@@ -582,6 +588,7 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
     q.zero_ptr2 = f_post;
     q.zero_count2 = G;
     q.pdl = 1;
+    q.reverse = 1;
     GMLP_CUDA(launch_row_quant(q, s), "x quantise launch");
   }
   GMLP_TRY(mark());

@@ -40,12 +40,20 @@ struct RowQuantArgs {
   float* zero_ptr2;         // optional second range
   int zero_count2;
   int pdl;                  // launch as a programmatic dependent of the previous kernel
+  int reverse;              // each warp sweeps its share last pass first (after launch_group_amax on
+                            // the same grid with keep > 0, whose evict-last reads are still in L2)
 };
 cudaError_t launch_row_quant(const RowQuantArgs& a, cudaStream_t s);
 
-// per-group max |x| into amax[G] (zeroed by the launcher)
-cudaError_t launch_group_amax(const uint16_t* x, int64_t M, int64_t K, GroupSrc grp, float* amax,
-                              cudaStream_t s);
+// the row quantiser's grid for M rows (one wave of its persistent blocks)
+int row_quant_grid(int format, int tiled, int64_t M);
+
+// per-group max |x| into amax[G] (zeroed by the launcher).  grid > 0 sets
+// the block count; the last `keep` fraction (0..1) of each warp's share is
+// read with an L2 evict-last policy (for a row cast on the same grid with
+// reverse = 1).
+cudaError_t launch_group_amax(const uint16_t* x, int64_t M, int64_t K, GroupSrc grp, float* amax, cudaStream_t s,
+                              int grid = 0, float keep = 0.0f);
 
 cudaError_t launch_hadamard_amax(const uint16_t* x, int64_t M, int64_t K, GroupSrc grp, uint32_t mask,
                                  float* amax_pre, float* amax_post, cudaStream_t s);

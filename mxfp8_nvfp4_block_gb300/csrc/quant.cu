@@ -91,6 +91,15 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return r;
 }
 
+// ld_stream with an L2 cache policy (createpolicy)
+__device__ __forceinline__ uint4 ld_stream_hint(const void* p, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
@@ -295,15 +304,20 @@ __global__ void __launch_bounds__(kThreads, FMT == GMLP_MXFP8 ? 4 : 5) row_quant
   const int64_t p0 = P * w / warps, p1 = P * (w + 1) / warps;
   if (p0 >= p1) return;
   float* enc = enc_tab[FMT == GMLP_NVFP4 ? wib : 0];
-  int r = (int)(p0 / ppr), j = (int)(p0 - (int64_t)r * ppr);  // first row and pass within it
-  int64_t left = p1 - p0;                                       // passes still to do
+  // the share's passes in order, or (a.reverse) last pass first: after an
+  // amax pass on the same grid that kept each share's last rows in L2
+  const int d = a.reverse ? -1 : 1;
+  const int64_t pf = a.reverse ? p1 - 1 : p0;
+  int r = (int)(pf / ppr), j = (int)(pf - (int64_t)r * ppr);  // first row and pass within it
+  int64_t left = p1 - p0;                                     // passes still to do
   int g = find_group(t, G, r);
   int g_tab = -1;
   float S = 0.0f;
-  for (; left > 0; ++r, j = 0) {
-    const int jend = (int)min((int64_t)ppr, j + left);
-    left -= jend - j;
+  for (; left > 0; r += d, j = a.reverse ? ppr - 1 : 0) {
+    int n = (int)min(left, (int64_t)(a.reverse ? j + 1 : ppr - j));
+    left -= n;
     while (t.off[g + 1] <= r) ++g;
+    while (t.off[g] > r) --g;
     int64_t src = r;
     if (a.swiglu_interleave) {
       const int pr = r - t.off[g];
@@ -331,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, FMT == GMLP_MXFP8 ? 4 : 5) row_quant
     }
     const uint4* xr = reinterpret_cast<const uint4*>(a.x + src * K);
     uint8_t* crow = a.codes + (int64_t)r * (FMT == GMLP_MXFP8 ? K : K / 2);
-    for (; j < jend; ++j) {
+    for (; n > 0; --n, j += d) {
       const int c0 = j * 128;
       if (c0 + 128 <= cpr)
         row_pass<FMT, TILED, true>(xr, crow, srow, c0, cpr, lane, S, enc);
@@ -346,8 +360,9 @@ __global__ void __launch_bounds__(kThreads, FMT == GMLP_MXFP8 ? 4 : 5) row_quant
 // Per-group max |x|.  Work units are 256 16-byte chunks of one row (eight per
 // lane, all loads issued before the max), so the warps' shares stay even when
 // there are only a few rows per warp; warp w takes a contiguous range of units.
-__global__ void __launch_bounds__(kThreads) group_amax_kernel(const uint16_t* x, int64_t K, GroupSrc grp,
-                                                              float* amax) {
+// (5 blocks per SM: it runs on the NVFP4 row cast's grid)
+__global__ void __launch_bounds__(kThreads, 5) group_amax_kernel(const uint16_t* x, int64_t K, GroupSrc grp,
+                                                                 float* amax, float keep) {
   __shared__ SmemGroups t;
   build_group_tables(grp, 1, t);
   griddep_wait();
@@ -367,6 +382,10 @@ __global__ void __launch_bounds__(kThreads) group_amax_kernel(const uint16_t* x,
   int64_t r = u0 / upr;
   int part = (int)(u0 - r * upr);
   int g = find_group(t, G, r);
+  // the share's last `keep` fraction is read with an L2 evict-last policy, so
+  // a row cast on the same grid sweeping its share backwards finds it in L2
+  const int64_t u_keep = u1 - (int64_t)(keep * (float)(u1 - u0));
+  const uint64_t pol_keep = policy_evict_last(), pol_rest = policy_evict_normal();
   uint32_t m = 0;  // running max |x| as bf16 bits (non-negative, so integer order is value order)
   for (int64_t u = u0; u < u1; ++u) {
     if (t.off[g + 1] <= r) {
@@ -377,11 +396,12 @@ __global__ void __launch_bounds__(kThreads) group_amax_kernel(const uint16_t* x,
     }
     const uint4* xr = reinterpret_cast<const uint4*>(x + r * K);
     const int c0 = part * 32 * U;
+    const uint64_t pol = u >= u_keep ? pol_keep : pol_rest;
     uint4 v[U];
 #pragma unroll
     for (int k = 0; k < U; ++k) {
       const int c = c0 + 32 * k + lane;
-      v[k] = c < nch ? ld_stream(xr + c) : make_uint4(0, 0, 0, 0);
+      v[k] = c < nch ? ld_stream_hint(xr + c, pol) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int k = 0; k < U; ++k) m = max(m, amax8_bits(v[k]));
@@ -1041,11 +1061,18 @@ cudaError_t launch_row_quant(const RowQuantArgs& a, cudaStream_t s) {
   return a.tiled ? launch_row_quant_t<GMLP_NVFP4, true>(a, s) : launch_row_quant_t<GMLP_NVFP4, false>(a, s);
 }
 
-cudaError_t launch_group_amax(const uint16_t* x, int64_t M, int64_t K, GroupSrc grp, float* amax,
-                              cudaStream_t s) {
+int row_quant_grid(int format, int tiled, int64_t M) {
+  if (format == GMLP_MXFP8)
+    return tiled ? grid_for(row_quant_kernel<GMLP_MXFP8, true>, M) : grid_for(row_quant_kernel<GMLP_MXFP8, false>, M);
+  return tiled ? grid_for(row_quant_kernel<GMLP_NVFP4, true>, M) : grid_for(row_quant_kernel<GMLP_NVFP4, false>, M);
+}
+
+cudaError_t launch_group_amax(const uint16_t* x, int64_t M, int64_t K, GroupSrc grp, float* amax, cudaStream_t s,
+                              int grid, float keep) {
   cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float) * grp.G, s);
   if (e != cudaSuccess) return e;
-  group_amax_kernel<<<grid_for(group_amax_kernel, M), kThreads, 0, s>>>(x, K, grp, amax);
+  if (grid <= 0) grid = grid_for(group_amax_kernel, M);
+  group_amax_kernel<<<grid, kThreads, 0, s>>>(x, K, grp, amax, keep);
   return cudaGetLastError();
 }
 
