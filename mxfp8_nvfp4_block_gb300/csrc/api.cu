@@ -278,6 +278,15 @@ gmlp_status gmlp_group_hadamard_amax(const uint16_t* x, int64_t M, int64_t K, co
   return GMLP_OK;
 }
 
+// An NVFP4 amax pass followed by a row cast of the same x: both on the cast's
+// grid, the amax pass reading the last ~80 MB of its warps' shares with an L2
+// evict-last policy, the cast (reverse = 1) sweeping its shares backwards
+// into them.
+static float nvfp4_amax_keep(int64_t M, int64_t K) {
+  const double x_bytes = 2.0 * (double)M * (double)K;
+  return x_bytes > 0 ? (float)std::min(1.0, 80e6 / x_bytes) : 0.0f;
+}
+
 static gmlp_status quantize_with_amax_impl(const uint16_t* x, int64_t M, int64_t K, const int64_t* split_sizes,
                                            int32_t G, const gmlp_recipe* r, const float* amax_pre,
                                            const float* amax_post, const gmlp_qtensor* row_out,
@@ -338,6 +347,7 @@ static gmlp_status quantize_with_amax_impl(const uint16_t* x, int64_t M, int64_t
   a.codes = row_out->codes;
   a.scales = row_out->scales;
   a.amax = amax_pre;
+  a.reverse = 1;  // pairs with gmlp_group_quantize's amax pass (any order is correct)
   GMLP_CUDA(launch_row_quant(a, s), "row_quant launch");
   return GMLP_OK;
 }
@@ -392,7 +402,8 @@ gmlp_status gmlp_group_quantize(const uint16_t* x, int64_t M, int64_t K, const i
   if (hadamard) {
     GMLP_CUDA(launch_hadamard_amax(x, M, K, gs, recipe->rht_sign_mask, amax_pre, amax_post, s), "hadamard_amax launch");
   } else if (recipe->format == GMLP_NVFP4) {
-    GMLP_CUDA(launch_group_amax(x, M, K, gs, amax_pre, s), "group_amax launch");
+    const int grid = row_quant_grid(GMLP_NVFP4, recipe->scale_layout == GMLP_SCALES_GEMM_TILED, M);
+    GMLP_CUDA(launch_group_amax(x, M, K, gs, amax_pre, s, grid, nvfp4_amax_keep(M, K)), "group_amax launch");
   }
   return quantize_with_amax_impl(x, M, K, split_sizes, G, recipe, amax_pre, amax_post, row_out, col_out, s);
 }
@@ -565,12 +576,9 @@ gmlp_status gmlp_forward(const uint16_t* x, int64_t M, int64_t K, int64_t N, con
   float* f_post = (aux && aux->fc2x_amax_post) ? aux->fc2x_amax_post : amax_ws + 2 * G;
   uint16_t* f_bf16 = (aux && aux->fc2x_bf16) ? aux->fc2x_bf16 : reinterpret_cast<uint16_t*>(ws + L.f_bf16);
   if (!aligned16(f_bf16)) return fail(GMLP_ERR_INVALID_ARG, "aux fc2x_bf16 misaligned");
-  // the amax pass and the x cast share one grid: the cast sweeps each warp's
-  // share backwards into the ~80 MB the amax pass left in L2 (evict-last)
-  const int xq_grid = row_quant_grid(GMLP_NVFP4, 1, M);
-  const double x_bytes = 2.0 * (double)M * (double)K;
-  const float keep = x_bytes > 0 ? (float)std::min(1.0, 80e6 / x_bytes) : 0.0f;
-  GMLP_CUDA(launch_group_amax(x, M, K, gs, x_amax, s, xq_grid, keep), "x amax launch");
+  // the amax pass on the x cast's grid (nvfp4_amax_keep)
+  GMLP_CUDA(launch_group_amax(x, M, K, gs, x_amax, s, row_quant_grid(GMLP_NVFP4, 1, M), nvfp4_amax_keep(M, K)),
+            "x amax launch");
   GMLP_TRY(mark());
   {
     RowQuantArgs q{};
