@@ -654,9 +654,10 @@ struct RcWalk {
 // COLQ = false (with ROW, RHT, TILED): no columnwise codes; the column phase
 // only takes the post-RHT amax of the 16-row chunks (per warp, then one
 // atomicMax per group and warp), the fused amax the columnwise cast of the
-// same tensor would use.
+// same tensor would use.  With nothing to stage it fits 72 registers and runs
+// three blocks per SM (measured 3% faster than two on nv_srelu's fc2_x).
 template <bool ROW, bool RHT, bool TILED, bool COLQ>
-__global__ void __launch_bounds__(kRcThreads, kRcBlocksPerSM)
+__global__ void __launch_bounds__(kRcThreads, COLQ ? kRcBlocksPerSM : 3)
     rowcol_quant_kernel(const __grid_constant__ CUtensorMap tmx, const ColQuantArgs a) {
   __shared__ SmemGroups t;
   extern __shared__ uint8_t rc_raw[];
